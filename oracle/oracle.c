@@ -1,0 +1,433 @@
+/*
+ * oracle.c -- float64 CPU oracle for split-KV decode attention.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The CUDA path shares no
+ * code, header, table or helper with it, and it never calls the CUDA path.
+ *
+ * What it computes (the definition, written out directly; no tiling, no online
+ * softmax, no reordering beyond the definition):
+ *
+ *   for every batch row b and query head hq, with kv head h = hq / G:
+ *     P(b,h)  = the valid KV positions of that row (dense: 0..N_b-1; block
+ *               sparse: the listed blocks, in list order, clipped to N_b)
+ *     s_n     = scale * sum_d q[d] * k_n[d]                  (n in P)
+ *     m       = max_n s_n
+ *     l       = sum_n exp(s_n - m)
+ *     out[d]  = sum_n exp(s_n - m) * v_n[d] / l
+ *     lse     = m + ln(l)                                    (natural log)
+ *   and out = 0, lse = -inf when P is empty.
+ *
+ * Sources: the per-split output and log-sum-exp of the split-K Triton decode
+ * kernel page (mslk splitk_kernels.py, `_fwd_kernel_splitK`, "write back O"
+ * and the LSE store), its reduce (`_splitK_reduce`), the GQA packing of the
+ * TorchInductor flex_decode.py.jinja template (query head hq reads kv head
+ * hq / G), its block-sparse traversal (KV_NUM_BLKS / KV_IDX, tables indexed
+ * by kv head), the paged translation of splitk_kernels.py (physical page =
+ * block_table[b][n / page_size]) and the MLA latent decode of FlashInfer
+ * include/flashinfer/attention/mla.cuh (scores over [ckv; kpe], values = ckv).
+ *
+ * Every input is converted exactly to float64 before any arithmetic:
+ *   - bf16 is the upper half of an IEEE-754 binary32 word;
+ *   - fp8 is OCP E4M3FN (the `float8e4nv` type of splitk_kernels.py): sign,
+ *     4-bit exponent with bias 7, 3-bit mantissa, subnormals at exponent 0,
+ *     no infinities, S.1111.111 is NaN, largest finite value 448; the
+ *     dequantised value is e4m3(byte) * scale[kv head].
+ *
+ * Parity pins: see tests/test_oracle_pins.py (closed forms, invariants, brute
+ * force with exact decimal arithmetic, all-code decoder checks).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* element decoders                                                   */
+/* ------------------------------------------------------------------ */
+
+double oracle_bf16_to_double(uint16_t bits) {
+  uint32_t word = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &word, sizeof f);
+  return (double)f;
+}
+
+double oracle_e4m3_to_double(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int expo = (byte >> 3) & 0xF;
+  int mant = byte & 0x7;
+  double mag;
+  if (expo == 0xF && mant == 0x7) return NAN;
+  if (expo == 0)
+    mag = ldexp((double)mant / 8.0, 1 - 7); /* subnormal: 0.mmm * 2^(1-bias) */
+  else
+    mag = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+  return sign ? -mag : mag;
+}
+
+/* ------------------------------------------------------------------ */
+/* the softmax-attention core over an explicit score list             */
+/* ------------------------------------------------------------------ */
+
+/*
+ * out[d] = sum_j exp(s_j - m) v_j[d] / sum_j exp(s_j - m);  lse = m + ln(sum).
+ * v is row-major [n][dv]. n == 0 gives out = 0 and lse = -inf (the empty-split
+ * convention of `_fwd_kernel_splitK`: l == 0 stores zeros, and `_splitK_reduce`
+ * keeps lse = -inf for such rows).
+ */
+void oracle_softmax_attend(int64_t n, const double *s, const double *v, int dv,
+                           double *out, double *lse) {
+  for (int d = 0; d < dv; ++d) out[d] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j)
+    if (s[j] > m) m = s[j];
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
+  for (int64_t j = 0; j < n; ++j) {
+    double w = exp(s[j] - m);
+    for (int d = 0; d < dv; ++d) out[d] += w * v[j * (int64_t)dv + d];
+  }
+  for (int d = 0; d < dv; ++d) out[d] /= l;
+  *lse = m + log(l);
+}
+
+/*
+ * LSE-weighted merge of per-split results, as `_splitK_reduce` of
+ * splitk_kernels.py defines it: M = max_s lse_s; w_s = exp(lse_s - M);
+ * out = sum_s w_s o_s / sum_s w_s; lse = M + ln(sum_s w_s). When M = -inf
+ * (every split empty) out = 0 and lse = -inf.
+ */
+void oracle_merge(int num_splits, int dv, const double *o, const double *lse_s,
+                  double *out, double *lse) {
+  double M = -INFINITY;
+  for (int s = 0; s < num_splits; ++s)
+    if (lse_s[s] > M) M = lse_s[s];
+  for (int d = 0; d < dv; ++d) out[d] = 0.0;
+  if (M == -INFINITY) {
+    *lse = -INFINITY;
+    return;
+  }
+  double wsum = 0.0;
+  for (int s = 0; s < num_splits; ++s) wsum += exp(lse_s[s] - M);
+  for (int s = 0; s < num_splits; ++s) {
+    double w = exp(lse_s[s] - M);
+    if (w == 0.0) continue; /* an empty split contributes nothing */
+    for (int d = 0; d < dv; ++d) out[d] += w * o[(int64_t)s * dv + d];
+  }
+  for (int d = 0; d < dv; ++d) out[d] /= wsum;
+  *lse = M + log(wsum);
+}
+
+/* ------------------------------------------------------------------ */
+/* problem description (the oracle's own; not shared with the kernels) */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;   /* MLA: 1 */
+  int32_t head_dim_qk;    /* GQA: D; MLA: ckv_dim + kpe_dim */
+  int32_t head_dim_v;     /* GQA: D; MLA: ckv_dim */
+  int32_t is_mla;
+  int32_t ckv_dim;
+  int32_t kpe_dim;
+  int32_t paged;          /* 0 contiguous, 1 paged through block_table */
+  int32_t page_size;
+  int32_t cache_len;      /* contiguous cache length L */
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  int32_t kv_fp8;         /* 0: bf16 bits, 1: e4m3 bytes with per-kv-head scale */
+  int32_t sparse_block_size; /* 0: dense */
+  int32_t max_sparse_blocks;
+} oracle_problem;
+
+typedef struct {
+  const uint16_t *q;      /* bf16 [B][HQ][Dq] (MLA: q_nope [B][HQ][ckv]) */
+  const uint16_t *q_pe;   /* MLA: bf16 [B][HQ][kpe] */
+  const void *k;          /* GQA contiguous [B][HKV][L][D]; paged [pages][HKV][P][D]
+                             MLA ckv: contiguous [B][L][ckv]; paged [pages][P][ckv] */
+  const void *v;          /* GQA: same layout as k; MLA kpe: [B][L][kpe] / [pages][P][kpe] */
+  const float *k_scale;   /* fp8: [HKV] */
+  const float *v_scale;   /* fp8: [HKV] */
+  const int32_t *block_table; /* paged: [B][max_pages_per_seq] */
+  const int32_t *seq_lens;    /* [B] */
+  const int32_t *kv_num_blks; /* sparse: [B][HKV] */
+  const int32_t *kv_idx;      /* sparse: [B][HKV][max_sparse_blocks] */
+  double scale;
+} oracle_inputs;
+
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
+
+/* ------------------------------------------------------------------ */
+/* positions and element fetches                                      */
+/* ------------------------------------------------------------------ */
+
+static int64_t max_positions(const oracle_problem *p) {
+  int64_t cap = p->paged ? (int64_t)p->max_pages_per_seq * p->page_size : p->cache_len;
+  if (p->sparse_block_size > 0) {
+    int64_t sp = (int64_t)p->max_sparse_blocks * p->sparse_block_size;
+    if (sp > cap) cap = sp;
+  }
+  return cap;
+}
+
+/*
+ * The valid positions of (b, h), in order. Dense: 0..N_b-1. Sparse (the
+ * block-sparse traversal of flex_decode.py.jinja): for each listed block j <
+ * KV_NUM_BLKS[b][h], positions KV_IDX[b][h][j] * SBS + t, t < SBS, kept when
+ * < N_b. Returns the count, or a negative error code.
+ */
+static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b, int h,
+                         int64_t *pos) {
+  int64_t nb = in->seq_lens[b];
+  int64_t capacity = p->paged ? (int64_t)p->max_pages_per_seq * p->page_size : p->cache_len;
+  if (nb < 0 || nb > capacity) return ORACLE_BAD_INDEX;
+  int64_t count = 0;
+  if (p->sparse_block_size == 0) {
+    for (int64_t n = 0; n < nb; ++n) pos[count++] = n;
+    return count;
+  }
+  int64_t sbs = p->sparse_block_size;
+  int32_t nblk = in->kv_num_blks[(int64_t)b * p->num_kv_heads + h];
+  if (nblk < 0 || nblk > p->max_sparse_blocks) return ORACLE_BAD_INDEX;
+  const int32_t *list = in->kv_idx + ((int64_t)b * p->num_kv_heads + h) * p->max_sparse_blocks;
+  for (int32_t j = 0; j < nblk; ++j) {
+    int64_t blk = list[j];
+    if (blk < 0 || blk * sbs >= capacity) return ORACLE_BAD_INDEX;
+    for (int64_t t = 0; t < sbs; ++t) {
+      int64_t n = blk * sbs + t;
+      if (n < nb) pos[count++] = n;
+    }
+  }
+  return count;
+}
+
+/* Row index of token n of (b, h) in the cache, or -1 when the page is invalid. */
+static int64_t cache_row(const oracle_problem *p, const oracle_inputs *in, int b, int h,
+                         int64_t n) {
+  int64_t heads = p->is_mla ? 1 : p->num_kv_heads;
+  if (!p->paged) {
+    return ((int64_t)b * heads + h) * p->cache_len + n;
+  }
+  int64_t page = in->block_table[(int64_t)b * p->max_pages_per_seq + n / p->page_size];
+  if (page < 0 || page >= p->num_pages) return -1;
+  return (page * heads + h) * p->page_size + n % p->page_size;
+}
+
+static double kv_elem(const oracle_problem *p, const void *base, int64_t idx, double scale) {
+  if (p->kv_fp8) return oracle_e4m3_to_double(((const uint8_t *)base)[idx]) * scale;
+  return oracle_bf16_to_double(((const uint16_t *)base)[idx]);
+}
+
+/* Fills key row kr[Dqk] and value row vr[Dv] for token n of (b, h). */
+static int fetch_kv(const oracle_problem *p, const oracle_inputs *in, int b, int h, int64_t n,
+                    double *kr, double *vr) {
+  int64_t row = cache_row(p, in, b, h, n);
+  if (row < 0) return ORACLE_BAD_INDEX;
+  if (p->is_mla) {
+    /* MLA latent cache: key = [ckv ; kpe], value = ckv */
+    for (int d = 0; d < p->ckv_dim; ++d) {
+      double c = kv_elem(p, in->k, row * p->ckv_dim + d, 1.0);
+      kr[d] = c;
+      vr[d] = c;
+    }
+    for (int d = 0; d < p->kpe_dim; ++d)
+      kr[p->ckv_dim + d] = kv_elem(p, in->v, row * p->kpe_dim + d, 1.0);
+    return ORACLE_OK;
+  }
+  double ks = p->kv_fp8 ? (double)in->k_scale[h] : 1.0;
+  double vs = p->kv_fp8 ? (double)in->v_scale[h] : 1.0;
+  for (int d = 0; d < p->head_dim_qk; ++d) kr[d] = kv_elem(p, in->k, row * p->head_dim_qk + d, ks);
+  for (int d = 0; d < p->head_dim_v; ++d) vr[d] = kv_elem(p, in->v, row * p->head_dim_v + d, vs);
+  return ORACLE_OK;
+}
+
+static void fetch_q(const oracle_problem *p, const oracle_inputs *in, int b, int hq, double *qr) {
+  if (p->is_mla) {
+    const uint16_t *qn = in->q + ((int64_t)b * p->num_q_heads + hq) * p->ckv_dim;
+    const uint16_t *qp = in->q_pe + ((int64_t)b * p->num_q_heads + hq) * p->kpe_dim;
+    for (int d = 0; d < p->ckv_dim; ++d) qr[d] = oracle_bf16_to_double(qn[d]);
+    for (int d = 0; d < p->kpe_dim; ++d) qr[p->ckv_dim + d] = oracle_bf16_to_double(qp[d]);
+    return;
+  }
+  const uint16_t *qq = in->q + ((int64_t)b * p->num_q_heads + hq) * p->head_dim_qk;
+  for (int d = 0; d < p->head_dim_qk; ++d) qr[d] = oracle_bf16_to_double(qq[d]);
+}
+
+static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
+  if (!p || !in || !in->q || !in->k || !in->v || !in->seq_lens) return ORACLE_BAD_ARG;
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return ORACLE_BAD_ARG;
+  if (p->num_q_heads % p->num_kv_heads) return ORACLE_BAD_ARG;
+  if (p->is_mla) {
+    if (p->num_kv_heads != 1 || !in->q_pe || p->kv_fp8) return ORACLE_BAD_ARG;
+    if (p->head_dim_qk != p->ckv_dim + p->kpe_dim || p->head_dim_v != p->ckv_dim)
+      return ORACLE_BAD_ARG;
+  }
+  if (p->paged && (!in->block_table || p->page_size <= 0 || p->max_pages_per_seq < 0))
+    return ORACLE_BAD_ARG;
+  if (p->kv_fp8 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
+  if (p->sparse_block_size > 0 && (!in->kv_num_blks || !in->kv_idx)) return ORACLE_BAD_ARG;
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* one (b, hq) row, optionally cut into chunks of the position list    */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+  const oracle_problem *p;
+  const oracle_inputs *in;
+  int num_chunks;              /* 0: unsplit */
+  const int64_t *chunk_bounds; /* [num_chunks + 1] list-index boundaries */
+  double *out;                 /* unsplit: [B][HQ][Dv]; split: [B][HQ][C][Dv] */
+  double *lse;                 /* unsplit: [B][HQ];     split: [B][HQ][C] */
+  int64_t next_row;
+  int64_t rows;
+  pthread_mutex_t lock;
+  int status;
+} job_t;
+
+static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vrows, double *qr,
+                   double *kr) {
+  const oracle_problem *p = job->p;
+  const oracle_inputs *in = job->in;
+  int b = (int)(row / p->num_q_heads);
+  int hq = (int)(row % p->num_q_heads);
+  int G = p->num_q_heads / p->num_kv_heads;
+  int h = hq / G;
+  int dq = p->head_dim_qk, dv = p->head_dim_v;
+
+  int64_t n = positions(p, in, b, h, pos);
+  if (n < 0) return (int)n;
+  fetch_q(p, in, b, hq, qr);
+  for (int64_t j = 0; j < n; ++j) {
+    int st = fetch_kv(p, in, b, h, pos[j], kr, vrows + j * (int64_t)dv);
+    if (st) return st;
+    double dot = 0.0;
+    for (int d = 0; d < dq; ++d) dot += qr[d] * kr[d];
+    s[j] = in->scale * dot;
+  }
+  if (job->num_chunks == 0) {
+    oracle_softmax_attend(n, s, vrows, dv, job->out + row * dv, job->lse + row);
+    return ORACLE_OK;
+  }
+  for (int c = 0; c < job->num_chunks; ++c) {
+    int64_t lo = job->chunk_bounds[c], hi = job->chunk_bounds[c + 1];
+    if (lo > n) lo = n;
+    if (hi > n) hi = n;
+    if (hi < lo) hi = lo;
+    oracle_softmax_attend(hi - lo, s + lo, vrows + lo * (int64_t)dv, dv,
+                          job->out + (row * job->num_chunks + c) * dv,
+                          job->lse + row * job->num_chunks + c);
+  }
+  return ORACLE_OK;
+}
+
+static void *worker(void *arg) {
+  job_t *job = (job_t *)arg;
+  const oracle_problem *p = job->p;
+  int64_t cap = max_positions(p);
+  int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
+  double *s = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+  double *vrows = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1) * p->head_dim_v);
+  double *qr = (double *)malloc(sizeof(double) * p->head_dim_qk);
+  double *kr = (double *)malloc(sizeof(double) * p->head_dim_qk);
+  int status = (pos && s && vrows && qr && kr) ? ORACLE_OK : ORACLE_NO_MEM;
+  while (status == ORACLE_OK) {
+    pthread_mutex_lock(&job->lock);
+    int64_t row = job->next_row++;
+    int failed = job->status;
+    pthread_mutex_unlock(&job->lock);
+    if (row >= job->rows || failed) break;
+    status = run_row(job, row, pos, s, vrows, qr, kr);
+  }
+  if (status) {
+    pthread_mutex_lock(&job->lock);
+    if (!job->status) job->status = status;
+    pthread_mutex_unlock(&job->lock);
+  }
+  free(pos);
+  free(s);
+  free(vrows);
+  free(qr);
+  free(kr);
+  return NULL;
+}
+
+static int run_job(job_t *job, int num_threads) {
+  if (num_threads < 1) num_threads = 1;
+  if (num_threads > 256) num_threads = 256;
+  pthread_t tid[256];
+  pthread_mutex_init(&job->lock, NULL);
+  job->next_row = 0;
+  job->status = ORACLE_OK;
+  int started = 0;
+  for (int t = 1; t < num_threads; ++t) {
+    if (pthread_create(&tid[started], NULL, worker, job) == 0) ++started;
+  }
+  worker(job);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&job->lock);
+  return job->status;
+}
+
+/*
+ * Full decode attention: out [B][HQ][Dv] and lse [B][HQ] (natural log).
+ * Returns 0, or a negative code (bad argument, or an index outside the cache:
+ * a page id outside [0, num_pages), a sparse block outside the cache, a
+ * sequence length over the cache capacity).
+ */
+int oracle_decode(const oracle_problem *p, const oracle_inputs *in, double *out, double *lse,
+                  int num_threads) {
+  int st = check_problem(p, in);
+  if (st) return st;
+  job_t job;
+  memset(&job, 0, sizeof job);
+  job.p = p;
+  job.in = in;
+  job.num_chunks = 0;
+  job.out = out;
+  job.lse = lse;
+  job.rows = (int64_t)p->batch * p->num_q_heads;
+  return run_job(&job, num_threads);
+}
+
+/*
+ * Split decode: the position list of every row is cut at the list indices
+ * chunk_bounds[0..num_chunks] (clipped to the row's length; chunks may be
+ * empty), and each chunk is attended on its own, giving per-chunk o
+ * [B][HQ][C][Dv] and lse [B][HQ][C] -- the per-split results the split-K
+ * kernel stores before its reduce.
+ */
+int oracle_split(const oracle_problem *p, const oracle_inputs *in, int num_chunks,
+                 const int64_t *chunk_bounds, double *o, double *lse, int num_threads) {
+  int st = check_problem(p, in);
+  if (st) return st;
+  if (num_chunks <= 0 || !chunk_bounds) return ORACLE_BAD_ARG;
+  for (int c = 0; c < num_chunks; ++c)
+    if (chunk_bounds[c] < 0 || chunk_bounds[c + 1] < chunk_bounds[c]) return ORACLE_BAD_ARG;
+  job_t job;
+  memset(&job, 0, sizeof job);
+  job.p = p;
+  job.in = in;
+  job.num_chunks = num_chunks;
+  job.chunk_bounds = chunk_bounds;
+  job.out = o;
+  job.lse = lse;
+  job.rows = (int64_t)p->batch * p->num_q_heads;
+  return run_job(&job, num_threads);
+}
+
+/* Merge for many rows at once: o [rows][S][dv], lse_s [rows][S]. */
+void oracle_merge_rows(int64_t rows, int num_splits, int dv, const double *o,
+                       const double *lse_s, double *out, double *lse) {
+  for (int64_t r = 0; r < rows; ++r)
+    oracle_merge(num_splits, dv, o + r * num_splits * (int64_t)dv, lse_s + r * num_splits,
+                 out + r * dv, lse + r);
+}

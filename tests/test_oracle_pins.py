@@ -1,0 +1,447 @@
+"""Pins for the float64 oracle: it is checked against things other than itself.
+
+* format definitions (bf16 and OCP E4M3, every code, against torch's casts and
+  the fixtures in tests/golden/);
+* closed forms (one key, equal values, q = 0, two keys) and the shift
+  invariance of softmax;
+* exact brute force (50-digit decimal) on tiny inputs in every cache layout;
+* invariants the definition fixes: split-then-merge equals unsplit, masked
+  or unlisted KV has no effect, paged equals contiguous on the de-paged cache,
+  sparse equals dense on the compacted cache, MLA equals GQA with
+  k = [ckv; kpe] and v = ckv.
+"""
+
+import math
+import os
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_flash_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# ------------------------------------------------------------------ decoders
+
+def test_bf16_decoder_every_code():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = codes.view(torch.bfloat16).double().numpy()
+    got = np.array([oracle.bf16_to_double(c & 0xFFFF) for c in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_decoder_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # 0x7f and 0xff
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.nanmax(np.abs(got)) == 448.0
+
+
+def test_e4m3_decoder_golden_codes():
+    with open(os.path.join(GOLDEN, "e4m3_codes.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 10
+    for code, value in rows:
+        got = oracle.e4m3_to_double(int(code, 16))
+        if value == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(value) and math.copysign(1, got) == math.copysign(1, float(value))
+
+
+# ------------------------------------------------------------------ core closed forms
+
+def test_core_single_key_returns_value_and_score():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal((1, 7))
+    out, lse = oracle.softmax_attend(np.array([0.37]), v)
+    assert np.array_equal(out, v[0])
+    assert lse == 0.37
+
+
+def test_core_empty_list():
+    out, lse = oracle.softmax_attend(np.zeros(0), np.zeros((0, 5)))
+    assert np.all(out == 0) and lse == -math.inf
+
+
+def test_core_equal_values_return_that_value():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal(50) * 4
+    v = np.tile(rng.standard_normal(9), (50, 1))
+    out, _ = oracle.softmax_attend(s, v)
+    assert rel_err(out, v[0]) < 1e-14
+
+
+def test_core_shift_invariance():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal(100) * 3
+    v = rng.standard_normal((100, 16))
+    out0, lse0 = oracle.softmax_attend(s, v)
+    for c in (-700.0, -3.5, 0.25, 50.0, 900.0):
+        out1, lse1 = oracle.softmax_attend(s + c, v)
+        assert rel_err(out1, out0) < 1e-12
+        assert abs(lse1 - (lse0 + c)) < 1e-12 * max(1.0, abs(c))
+
+
+def test_core_uniform_scores_give_mean_and_log_count():
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((37, 5))
+    out, lse = oracle.softmax_attend(np.zeros(37), v)
+    assert rel_err(out, v.mean(axis=0)) < 1e-13
+    assert abs(lse - math.log(37)) < 1e-14
+
+
+def test_core_two_keys_closed_form():
+    s0, s1 = 0.3, -1.7
+    v = np.array([[1.0, -2.0, 0.5], [3.0, 4.0, -1.0]])
+    out, lse = oracle.softmax_attend(np.array([s0, s1]), v)
+    sig = 1.0 / (1.0 + math.exp(-(s0 - s1)))
+    assert rel_err(out, sig * v[0] + (1 - sig) * v[1]) < 1e-15
+    assert abs(lse - math.log(math.exp(s0) + math.exp(s1))) < 1e-15
+
+
+def test_core_ordering_of_scores_does_not_matter():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal(64)
+    v = rng.standard_normal((64, 8))
+    perm = rng.permutation(64)
+    a, la = oracle.softmax_attend(s, v)
+    b, lb = oracle.softmax_attend(s[perm], v[perm])
+    assert rel_err(a, b) < 1e-14 and abs(la - lb) < 1e-14
+
+
+def test_core_a_dominant_score_selects_its_value():
+    # softmax with one score far above the rest is (numerically) a one-hot
+    v = np.array([[1.0, 2.0], [5.0, -7.0], [0.0, 3.0]])
+    out, lse = oracle.softmax_attend(np.array([0.0, 800.0, 1.0]), v)
+    assert np.array_equal(out, v[1]) and lse == 800.0
+
+
+# ------------------------------------------------------------------ merge closed forms
+
+def test_merge_single_split_is_identity():
+    rng = np.random.default_rng(6)
+    o = rng.standard_normal((1, 12))
+    out, lse = oracle.merge(o, np.array([1.25]))
+    assert np.array_equal(out, o[0]) and lse == 1.25
+
+
+def test_merge_ignores_empty_splits_and_handles_all_empty():
+    rng = np.random.default_rng(7)
+    o = rng.standard_normal((3, 4))
+    o[1] = np.nan  # an empty split's O is never read
+    out, lse = oracle.merge(o, np.array([0.5, -math.inf, 0.5]))
+    assert rel_err(out, (o[0] + o[2]) / 2) < 1e-15
+    assert abs(lse - (0.5 + math.log(2))) < 1e-15
+    out, lse = oracle.merge(o, np.full(3, -math.inf))
+    assert np.all(out == 0) and lse == -math.inf
+
+
+def test_merge_two_splits_closed_form():
+    o = np.array([[1.0, 0.0], [0.0, 1.0]])
+    a, b = 0.7, -0.4
+    out, lse = oracle.merge(o, np.array([a, b]))
+    wa = math.exp(a) / (math.exp(a) + math.exp(b))
+    assert rel_err(out, [wa, 1 - wa]) < 1e-15
+    assert abs(lse - math.log(math.exp(a) + math.exp(b))) < 1e-15
+
+
+# ------------------------------------------------------------------ golden: two keys
+
+def test_golden_two_keys_decode():
+    rows = {}
+    with open(os.path.join(GOLDEN, "two_keys.txt")) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                name, *vals = ln.split()
+                rows[name] = [float(x) for x in vals]
+    q = torch.tensor([[rows["q"]]], dtype=torch.bfloat16)  # [1][1][2]
+    k = torch.tensor([[[rows["k0"], rows["k1"]]]], dtype=torch.bfloat16)  # [1][1][2][2]
+    v = torch.tensor([[[rows["v0"], rows["v1"]]]], dtype=torch.bfloat16)
+    prob = dict(batch=1, num_q_heads=1, num_kv_heads=1, head_dim_qk=2, head_dim_v=2,
+                cache_len=2)
+    out, lse = oracle.decode(prob, dict(q=q, k=k, v=v, seq_lens=torch.tensor([2])), 1.0)
+    s0 = sum(a * b for a, b in zip(rows["q"], rows["k0"]))
+    s1 = sum(a * b for a, b in zip(rows["q"], rows["k1"]))
+    sig = 1.0 / (1.0 + math.exp(s1 - s0))
+    expect = [sig * a + (1 - sig) * b for a, b in zip(rows["v0"], rows["v1"])]
+    assert rel_err(out[0, 0], expect) < 1e-15
+    assert abs(lse[0, 0] - math.log(math.exp(s0) + math.exp(s1))) < 1e-15
+
+
+# ------------------------------------------------------------------ brute force (exact decimal)
+
+def _dec(x) -> Decimal:
+    return Decimal(float(x))
+
+
+def brute_force(w: W.Workload):
+    """Independent 50-digit evaluation straight from the cache layouts."""
+    getcontext().prec = 50
+    t = w.tensors
+    B, HQ, HKV = w.batch, w.num_q_heads, w.num_kv_heads
+    G = HQ // HKV
+    q = t["q"].double()
+    if w.kv_fp8:
+        k = t["k"].double() * t["k_scale"].double().view(1, -1, 1, 1)
+        v = t["v"].double() * t["v_scale"].double().view(1, -1, 1, 1)
+    else:
+        k, v = t["k"].double(), t["v"].double()
+    out = np.zeros((B, HQ, w.head_dim_v))
+    lse = np.zeros((B, HQ))
+    for b in range(B):
+        n_b = int(t["seq_lens"][b])
+        for hq in range(HQ):
+            h = hq // G
+            if w.sparse_block_size:
+                pos = []
+                for j in range(int(t["kv_num_blks"][b, h])):
+                    blk = int(t["kv_idx"][b, h, j])
+                    pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
+                            if blk * w.sparse_block_size + i < n_b]
+            else:
+                pos = list(range(n_b))
+            keys, vals = [], []
+            for n in pos:
+                if w.is_mla:
+                    page = int(t["block_table"][b, n // w.page_size])
+                    ckv = t["k"][page, n % w.page_size].double()
+                    kpe = t["v"][page, n % w.page_size].double()
+                    keys.append(torch.cat([ckv, kpe]))
+                    vals.append(ckv)
+                elif w.paged:
+                    page = int(t["block_table"][b, n // w.page_size])
+                    keys.append(k[page, h, n % w.page_size])
+                    vals.append(v[page, h, n % w.page_size])
+                else:
+                    keys.append(k[b, h, n])
+                    vals.append(v[b, h, n])
+            qv = torch.cat([q[b, hq], t["q_pe"][b, hq].double()]) if w.is_mla else q[b, hq]
+            if not pos:
+                lse[b, hq] = -math.inf
+                continue
+            s = [_dec(w.scale) * sum(_dec(a) * _dec(c) for a, c in zip(qv.tolist(), kk.tolist()))
+                 for kk in keys]
+            m = max(s)
+            e = [(x - m).exp() for x in s]
+            den = sum(e)
+            for d in range(w.head_dim_v):
+                out[b, hq, d] = float(sum(ei * _dec(vv[d]) for ei, vv in zip(e, vals)) / den)
+            lse[b, hq] = float(m + den.ln())
+    return out, lse
+
+
+def _tiny_cases():
+    cases = []
+    cases.append(W.make_gqa(name="contig", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                            seq_lens=[5, 1], cache_len=6, seed=11, scale=0.7))
+    cases.append(W.make_gqa(name="paged", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                            seq_lens=[6, 3], layout="paged", page_size=2, seed=12, scale=0.6))
+    cases.append(W.make_gqa(name="fp8", batch=1, num_q_heads=2, num_kv_heads=2, head_dim=4,
+                            seq_lens=[6], cache_len=6, kv_fp8=True, seed=13, scale=0.5))
+    num = torch.tensor([[2, 1]], dtype=torch.int32)
+    idx = torch.tensor([[[2, 0, 0], [1, 0, 0]]], dtype=torch.int32)
+    cases.append(W.make_gqa(name="sparse", batch=1, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                            seq_lens=[5], cache_len=6, sparse_block_size=2, kv_num_blks=num,
+                            kv_idx=idx, seed=14, scale=0.8))
+    cases.append(W.make_mla(name="mla", batch=2, num_q_heads=3, ckv_dim=4, kpe_dim=2,
+                            seq_lens=[4, 2], page_size=2, seed=15, scale=0.9))
+    cases.append(W.make_gqa(name="empty_row", batch=2, num_q_heads=2, num_kv_heads=1,
+                            head_dim=3, seq_lens=[0, 2], cache_len=2, seed=16, scale=1.0))
+    return cases
+
+
+@pytest.mark.parametrize("w", _tiny_cases(), ids=lambda w: w.name)
+def test_brute_force_tiny(w):
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=2)
+    bo, bl = brute_force(w)
+    assert np.all(np.isfinite(out))
+    fin = np.isfinite(bl)
+    assert np.array_equal(fin, np.isfinite(lse))
+    assert np.all(lse[~fin] == -math.inf)
+    assert np.max(np.abs(out - bo)) < 1e-12
+    assert np.max(np.abs(lse[fin] - bl[fin])) < 1e-12
+
+
+# ------------------------------------------------------------------ invariants at moderate size
+
+def _gqa_case(layout="contiguous", seed=21, **kw):
+    args = dict(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=32, seq_lens=[70, 1, 129],
+                layout=layout, page_size=16, seed=seed)
+    args.update(kw)
+    return W.make_gqa(**args)
+
+
+def test_split_then_merge_equals_unsplit():
+    w = _gqa_case(seq_lens=[70, 0, 129])
+    prob = oracle.problem_from(w)
+    out, lse = oracle.decode(prob, w.tensors, w.scale)
+    rng = np.random.default_rng(8)
+    for _ in range(6):
+        cuts = np.sort(rng.integers(0, 140, size=rng.integers(1, 7)))
+        bounds = np.concatenate([[0], cuts, [140]])  # repeated cuts give empty chunks
+        o_s, l_s = oracle.split(prob, w.tensors, w.scale, bounds)
+        mo, ml = oracle.merge(o_s, l_s)
+        assert np.max(np.abs(mo - out)) <= 1e-12 * max(1.0, np.max(np.abs(out)))
+        fin = np.isfinite(lse)
+        assert np.array_equal(np.isfinite(ml), fin)
+        assert np.max(np.abs(ml[fin] - lse[fin])) < 1e-12
+
+
+def test_values_past_sequence_end_have_no_effect():
+    w = _gqa_case(poison=False)
+    prob = oracle.problem_from(w)
+    out, lse = oracle.decode(prob, w.tensors, w.scale)
+    t = dict(w.tensors)
+    k, v = t["k"].clone(), t["v"].clone()
+    for b, n in enumerate(t["seq_lens"].tolist()):
+        k[b, :, n:] = 3.0e38
+        v[b, :, n:] = -1.0e38
+    t.update(k=k, v=v)
+    out2, lse2 = oracle.decode(prob, t, w.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_paged_equals_contiguous_on_depaged_cache():
+    w = _gqa_case(layout="paged", page_size=16, poison=False)
+    t = w.tensors
+    out_p, lse_p = oracle.decode(oracle.problem_from(w), t, w.scale)
+    L = w.max_pages_per_seq * w.page_size
+    # de-page with torch indexing: token n of row b is page table[b][n // P], slot n % P
+    pages = t["block_table"].long()  # [B][max_pages]
+    k = t["k"][pages].permute(0, 2, 1, 3, 4).reshape(w.batch, w.num_kv_heads, L, w.head_dim_qk)
+    v = t["v"][pages].permute(0, 2, 1, 3, 4).reshape(w.batch, w.num_kv_heads, L, w.head_dim_v)
+    c = W.Workload(name="depaged", batch=w.batch, num_q_heads=w.num_q_heads,
+                   num_kv_heads=w.num_kv_heads, head_dim_qk=w.head_dim_qk,
+                   head_dim_v=w.head_dim_v, scale=w.scale, cache_len=L)
+    out_c, lse_c = oracle.decode(oracle.problem_from(c), dict(q=t["q"], k=k.contiguous(),
+                                 v=v.contiguous(), seq_lens=t["seq_lens"]), w.scale)
+    assert np.array_equal(out_p, out_c) and np.array_equal(lse_p, lse_c)
+
+
+def _sparse_case(seed=31, poison=True):
+    g = torch.Generator().manual_seed(seed)
+    num, idx = W.sparse_lists(2, 2, 1024, 64, keep_random=3, keep_last=2, g=g, max_blocks=16)
+    return W.make_gqa(name="sparse", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                      seq_lens=[1000, 1024], cache_len=1024, sparse_block_size=64,
+                      kv_num_blks=num, kv_idx=idx, seed=seed, poison=poison)
+
+
+def test_sparse_equals_dense_on_compacted_cache():
+    w = _sparse_case(poison=True)
+    t = w.tensors
+    out_s, lse_s = oracle.decode(oracle.problem_from(w), t, w.scale)
+    assert np.all(np.isfinite(out_s))  # NaN-poisoned unlisted blocks never reached
+    # compact each (b, h) list into its own dense row, then attend densely
+    rows_k, rows_v, lens = [], [], []
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            blocks = t["kv_idx"][b, h, :int(t["kv_num_blks"][b, h])].long()
+            pos = (blocks[:, None] * 64 + torch.arange(64)).reshape(-1)
+            pos = pos[pos < int(t["seq_lens"][b])]
+            rows_k.append(t["k"][b, h, pos])
+            rows_v.append(t["v"][b, h, pos])
+            lens.append(pos.numel())
+    L = max(lens)
+    BH = w.batch * w.num_kv_heads
+    k = torch.zeros((BH, 1, L, 16), dtype=torch.bfloat16)
+    v = torch.zeros((BH, 1, L, 16), dtype=torch.bfloat16)
+    for i in range(BH):
+        k[i, 0, :lens[i]] = rows_k[i]
+        v[i, 0, :lens[i]] = rows_v[i]
+    # one dense "batch row" per (b, kv head), holding that head's G query heads
+    G = w.group
+    q = t["q"].reshape(BH, G, 16)
+    dense = dict(batch=BH, num_q_heads=G, num_kv_heads=1, head_dim_qk=16, head_dim_v=16,
+                 cache_len=L)
+    out_d, lse_d = oracle.decode(dense, dict(q=q, k=k, v=v, seq_lens=torch.tensor(lens)), w.scale)
+    assert np.array_equal(out_s.reshape(BH, G, 16), out_d)
+    assert np.array_equal(lse_s.reshape(BH, G), lse_d)
+
+
+def test_unlisted_sparse_blocks_have_no_effect():
+    w = _sparse_case(poison=False)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    t = dict(w.tensors)
+    k, v = t["k"].clone(), t["v"].clone()
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            keep = torch.zeros(16, dtype=torch.bool)
+            keep[t["kv_idx"][b, h, :int(t["kv_num_blks"][b, h])].long()] = True
+            mask = keep.repeat_interleave(64) & (torch.arange(1024) < int(t["seq_lens"][b]))
+            k[b, h, ~mask] = 1.0e30
+            v[b, h, ~mask] = -5.0e30
+    t.update(k=k, v=v)
+    out2, lse2 = oracle.decode(oracle.problem_from(w), t, w.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_mla_equals_gqa_with_concatenated_keys():
+    w = W.make_mla(batch=3, num_q_heads=16, ckv_dim=32, kpe_dim=8, seq_lens=[100, 7, 64],
+                   page_size=16, seed=41)
+    t = w.tensors
+    out_m, lse_m = oracle.decode(oracle.problem_from(w), t, w.scale)
+    # the same problem as GQA with one kv head: k = [ckv ; kpe], v = ckv, q = [q_nope ; q_pe]
+    q = torch.cat([t["q"], t["q_pe"]], dim=-1)
+    k = torch.cat([t["k"], t["v"]], dim=-1).unsqueeze(1)  # [pages][1][P][40]
+    v = t["k"].unsqueeze(1)
+    prob = dict(batch=3, num_q_heads=16, num_kv_heads=1, head_dim_qk=40, head_dim_v=32,
+                paged=1, page_size=16, max_pages_per_seq=w.max_pages_per_seq,
+                num_pages=w.num_pages)
+    out_g, lse_g = oracle.decode(prob, dict(q=q, k=k.contiguous(), v=v.contiguous(),
+                                            block_table=t["block_table"], seq_lens=t["seq_lens"]),
+                                 w.scale)
+    assert np.array_equal(out_m, out_g) and np.array_equal(lse_m, lse_g)
+
+
+def test_fp8_dequant_equals_bf16_path_on_dequantised_values():
+    w = _gqa_case(kv_fp8=True, poison=False, seq_lens=[33, 2, 64], head_dim=16)
+    t = w.tensors
+    out8, lse8 = oracle.decode(oracle.problem_from(w), t, w.scale)
+    # the dequantised cache, formed by torch, is not always exact in bf16, so compare
+    # against a float64 evaluation of the same values (numpy, per row)
+    kd = t["k"].double() * t["k_scale"].double().view(1, -1, 1, 1)
+    vd = t["v"].double() * t["v_scale"].double().view(1, -1, 1, 1)
+    q = t["q"].double()
+    for b in range(w.batch):
+        n = int(t["seq_lens"][b])
+        for hq in range(w.num_q_heads):
+            h = hq // w.group
+            s = w.scale * (kd[b, h, :n] @ q[b, hq]).numpy()
+            o, l = oracle.softmax_attend(s, vd[b, h, :n].numpy())
+            assert np.max(np.abs(o - out8[b, hq])) < 1e-12
+            assert abs(l - lse8[b, hq]) < 1e-12
+
+
+def test_bad_page_index_is_reported():
+    w = _gqa_case(layout="paged")
+    t = dict(w.tensors)
+    bt = t["block_table"].clone()
+    bt[0, 0] = w.num_pages  # out of the pool
+    t["block_table"] = bt
+    with pytest.raises(ValueError):
+        oracle.decode(oracle.problem_from(w), t, w.scale)
+
+
+def test_threads_do_not_change_results():
+    w = _gqa_case(layout="paged")
+    a = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=1)
+    b = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=7)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
