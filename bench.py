@@ -1,0 +1,361 @@
+"""Benchmark: split-KV decode attention on GB300 through the C ABI.
+
+One step = one decode call (split kernel + LSE merge) over the whole batch of
+the workload, K/V cache resident in HBM. Default workload: paged GQA decode
+(B=32, HQ=32, HKV=8, D=128, N_b ~ U[1024, 8192], page 16). The metric is the
+achieved KV-cache bandwidth (algorithmic KV bytes / time, GB/s), with us per
+call and the fraction of measured HBM peak alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+units are independent, no collective on the data path); rank 0 prints one
+JSON line with the whole-job aggregate (bytes of all ranks / max rank time).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from decode_attention_flash_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_CONFIG = 2
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """The method's own bytes per call: kept KV + Q + O (+ LSE)."""
+    t = w.tensors
+    if w.sparse_block_size:
+        nb = t["kv_num_blks"].long()
+        positions = 0
+        for b in range(w.batch):
+            n_b = int(t["seq_lens"][b])
+            for h in range(w.num_kv_heads):
+                blocks = t["kv_idx"][b, h, :int(nb[b, h])].long()
+                positions += int(torch.clamp(n_b - blocks * w.sparse_block_size, 0,
+                                             w.sparse_block_size).sum())
+        kv_tokens_heads = positions
+    else:
+        kv_tokens_heads = int(t["seq_lens"].long().sum()) * (1 if w.is_mla else w.num_kv_heads)
+    elt = 1 if w.kv_fp8 else 2
+    if w.is_mla:
+        kv = kv_tokens_heads * (w.ckv_dim + w.kpe_dim) * 2
+        q = w.batch * w.num_q_heads * (w.ckv_dim + w.kpe_dim) * 2
+        flops = kv_tokens_heads * w.num_q_heads * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
+    else:
+        kv = kv_tokens_heads * (w.head_dim_qk + w.head_dim_v) * elt
+        q = w.batch * w.num_q_heads * w.head_dim_qk * 2
+        flops = kv_tokens_heads * w.group * 2 * (w.head_dim_qk + w.head_dim_v)
+    o = w.batch * w.num_q_heads * (w.head_dim_v * 2 + 4)
+    return {"kv": kv, "q": q, "o": o, "total": kv + q + o, "flops": flops}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_oracle(w, rows, threads):
+    """The float64 oracle on a subset of batch rows; returns (seconds, fraction of KV)."""
+    import oracle
+    t0 = time.perf_counter()
+    sub = _subset(w, rows)
+    oracle.decode(oracle.problem_from(sub), sub.tensors, sub.scale, num_threads=threads)
+    dt = time.perf_counter() - t0
+    frac = algorithmic_bytes(sub)["kv"] / max(algorithmic_bytes(w)["kv"], 1)
+    return dt, frac
+
+
+def _subset(w, rows):
+    import copy
+    t = dict(w.tensors)
+    idx = torch.tensor(rows, dtype=torch.long)
+    for k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx"):
+        if k in t:
+            t[k] = t[k][idx].contiguous()
+    if not w.paged:
+        t["k"] = t["k"][idx].contiguous()
+        t["v"] = t["v"][idx].contiguous()
+    s = copy.copy(w)
+    s.batch = len(rows)
+    s.tensors = t
+    return s
+
+
+def pick_oracle_rows(w, target_s=1.0, threads=1):
+    """Batch rows of the workload sized for ~target_s seconds of oracle time."""
+    rows = [0]
+    timed_oracle(w, rows, threads)  # first call also loads the library
+    dt, _ = timed_oracle(w, rows, threads)
+    per_row = max(dt, 1e-4)
+    n = max(1, min(w.batch, int(target_s / per_row)))
+    return list(range(n))
+
+
+def run_reference(args, w, cfg):
+    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    threads = oracle.default_threads()
+    rows = pick_oracle_rows(w, target_s=2.0, threads=threads)
+    for _ in range(args.warmup):
+        timed_oracle(w, rows, threads)
+    times = []
+    frac = 1.0
+    for _ in range(args.steps):
+        dt, frac = timed_oracle(w, rows, threads)
+        times.append(dt)
+    ab = algorithmic_bytes(w)
+    mean = statistics.mean(times)
+    value = ab["kv"] * frac / mean / 1e9
+    line = {
+        "impl": "reference", "metric": "decode attention KV GB/s & % of GB300 HBM peak; \u00b5s per decode call", "value": value,
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.CONFIG_NAMES[cfg], "sample_rows": len(rows)},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"batch rows 0..{len(rows) - 1} of {w.batch}, all heads"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, cfg):
+    import decode_attention_flash_gb300 as da
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, tf_peak, tf_sus, peak_kind = measured_peaks()
+    nb = w.tensors.get("kv_num_blks") if w.sparse_block_size else None
+    eng = da.DecodeAttention(device=local, seq_lens_host=w.tensors["seq_lens"], kv_num_blks_host=nb,
+                             num_splits_override=args.splits if args.splits else w.num_splits,
+                             **da.problem_kwargs(w))
+    plan = eng.plan
+    t = w.to(dev)
+    out = torch.empty((w.batch, w.num_q_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    a = da.make_args(t, w.scale, out, lse)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        da.decode_attn_run(eng.ctx, a, eng.workspace, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if eng.errors() != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    # ---------------- device-timed region: split and merge timed apart, L2 flushed between steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            da.decode_attn_run_split(eng.ctx, a, eng.workspace, stream)
+            ev[i][1].record(stream)
+            da.decode_attn_run_merge(eng.ctx, a, eng.workspace, stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    split_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    call_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    mean_call = max_over_ranks(statistics.mean(call_ms), world)
+    mean_split = max_over_ranks(statistics.mean(split_ms), world)
+    launches_per_step = 1 + (0 if plan["writes_final"] else 1)
+
+    ab = algorithmic_bytes(w)
+    value = world * ab["kv"] / (mean_call * 1e-3) / 1e9
+    pct_hbm = ab["total"] / (mean_call * 1e-3) / 1e9 / hbm_peak
+    split_gbs = ab["total"] / (mean_split * 1e-3) / 1e9
+
+    # ---------------- end to end through the public API with host buffers
+    host_in = {k: v.pin_memory() for k, v in w.tensors.items()
+               if k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx")}
+    dev_in = {k: t[k] for k in host_in}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e_ms = []
+    for i in range(args.steps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k, hv in host_in.items():
+            dev_in[k].copy_(hv, non_blocking=True)
+        eng.run(t, w.scale, out=out, lse=lse, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            e2e_ms.append(e0.elapsed_time(e1))
+    mean_e2e = max_over_ranks(statistics.mean(e2e_ms), world)
+    e2e_value = world * ab["kv"] / (mean_e2e * 1e-3) / 1e9
+    if eng.errors() != 0:
+        raise RuntimeError("device error flags set during the timed region")
+
+    # ---------------- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        rows = pick_oracle_rows(w, target_s=10.0, threads=threads)
+        dt, frac = timed_oracle(w, rows, threads)
+        cpu = {"value": ab["kv"] * frac / dt / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"batch rows 0..{len(rows) - 1} of {w.batch} ({frac:.3f} of the KV bytes), "
+                         f"{dt:.1f} s wall"}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": "decode attention KV GB/s & % of GB300 HBM peak; \u00b5s per decode call",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_call, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f8e4m3" if w.kv_fp8 else "bf16",
+            "data": "synthetic",
+            "config": {"workload": W.CONFIG_NAMES[cfg], "us_per_call": mean_call * 1e3,
+                       "pct_hbm_peak_kv_q_o": pct_hbm, "hbm_peak_gbs": hbm_peak,
+                       "peak_source": peak_kind, "l2": "512 MiB buffer written between steps",
+                       "plan": {k: plan[k] for k in ("chunk_tokens", "num_splits", "grid_x",
+                                                     "grid_y", "grid_z", "ctas_per_sm")},
+                       "algorithmic_bytes": ab["total"], "kv_bytes": ab["kv"],
+                       "merge_us": (mean_call - mean_split) * 1e3},
+            "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": split_gbs / hbm_peak, "traffic": None,
+                         "kernel": "gqa_split_kernel" if not w.is_mla else "mla_split_kernel",
+                         "kernel_us": mean_split * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "us_per_call": mean_e2e * 1e3},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    eng.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--splits", type=int, default=0, help="num_splits_override (0 = planner)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = W.config(args.config)
+    if args.impl == "reference":
+        run_reference(args, w, args.config)
+    else:
+        run_ours(args, w, args.config)
+
+
+if __name__ == "__main__":
+    main()

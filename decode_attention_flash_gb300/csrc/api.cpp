@@ -1,0 +1,355 @@
+// api.cpp -- the C ABI (include/decode_attn.h): argument checks, the host
+// context, TMA descriptors and kernel launches. No device allocation happens
+// here; every device buffer is the caller's.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+struct da_ctx {
+  da_problem prob;
+  int device;
+  int num_sms;
+  int smem_per_sm;
+  bool planned;
+  da_plan_info plan;
+  // tensor maps are re-encoded only when the cache base pointers change
+  const void *map_k_base;
+  const void *map_v_base;
+  CUtensorMap kmap;
+  CUtensorMap vmap;
+};
+
+namespace {
+
+using da::kWorkspaceHeader;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A 2-D map over `rows` rows of `row_bytes` bytes, 128B-swizzled boxes of
+// `box_rows` rows; elements are bf16 (row_bytes = 128: a half head row) or bytes.
+da_status encode_rows(CUtensorMap *map, const void *base, bool bf16, uint64_t rows,
+                      uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {bf16 ? 64u : 128u, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {bf16 ? 64u : 128u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+da_status check_workspace(const da_ctx *ctx, const void *ws, size_t bytes) {
+  if (!ws || !aligned(ws, 256)) return DA_ERR_WORKSPACE;
+  if ((int64_t)bytes < ctx->plan.workspace_bytes) return DA_ERR_WORKSPACE;
+  return DA_OK;
+}
+
+// phase bit 1: split kernel, bit 2: merge kernel
+enum { kSplit = 1, kMerge = 2 };
+
+da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream, int phases) {
+  const da_problem &p = ctx->prob;
+  const bool fp8 = p.kv_dtype == DA_DTYPE_FP8_E4M3;
+  const bool paged = p.kv_layout == DA_KV_PAGED;
+  const bool sparse = p.sparse_block_size > 0;
+  if (!a->q || !a->k || !a->v || !a->seq_lens || !a->out) return DA_ERR_INVALID_ARG;
+  if (paged && !a->block_table) return DA_ERR_INVALID_ARG;
+  if (sparse && (!a->kv_num_blks || !a->kv_idx)) return DA_ERR_INVALID_ARG;
+  if (fp8 && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
+  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 16) || !aligned(a->out, 4))
+    return DA_ERR_INVALID_ARG;
+
+  const uint64_t rows = paged ? (uint64_t)p.num_pages * p.num_kv_heads * p.page_size
+                              : (uint64_t)p.batch * p.num_kv_heads * p.max_seq_len;
+  const uint32_t box_tokens = (uint32_t)da::gqa_box_tokens(p);
+  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v) {
+    da_status st;
+    if ((st = encode_rows(&ctx->kmap, a->k, !fp8, fp8 ? rows : rows * 2,
+                          fp8 ? box_tokens : box_tokens * 2)) != DA_OK)
+      return st;
+    if ((st = encode_rows(&ctx->vmap, a->v, !fp8, fp8 ? rows : rows * 2,
+                          fp8 ? box_tokens : box_tokens * 2)) != DA_OK) {
+      ctx->map_k_base = nullptr;
+      return st;
+    }
+    ctx->map_k_base = a->k;
+    ctx->map_v_base = a->v;
+  }
+
+  const da_plan_info &pl = ctx->plan;
+  da::GqaParams gp;
+  std::memset(&gp, 0, sizeof gp);
+  gp.q = reinterpret_cast<const __nv_bfloat16 *>(a->q);
+  gp.block_table = a->block_table;
+  gp.seq_lens = a->seq_lens;
+  gp.kv_num_blks = a->kv_num_blks;
+  gp.kv_idx = a->kv_idx;
+  gp.k_scale = a->k_scale;
+  gp.v_scale = a->v_scale;
+  gp.o_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_o_offset);
+  gp.lse_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_lse_offset);
+  gp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
+  gp.lse = a->lse;
+  gp.err = reinterpret_cast<uint32_t *>(ws);
+  gp.score_scale = a->scale * 1.4426950408889634f;
+  gp.batch = p.batch;
+  gp.num_q_heads = p.num_q_heads;
+  gp.num_kv_heads = p.num_kv_heads;
+  gp.group = p.num_q_heads / p.num_kv_heads;
+  gp.paged = paged ? 1 : 0;
+  gp.page_size = p.page_size;
+  gp.cache_len = paged ? 0 : p.max_seq_len;
+  gp.max_pages = p.max_pages_per_seq;
+  gp.num_pages = p.num_pages;
+  gp.capacity = paged ? p.max_pages_per_seq * p.page_size : p.max_seq_len;
+  gp.sparse_block_size = p.sparse_block_size;
+  gp.max_sparse_blocks = p.max_sparse_blocks;
+  gp.chunk = pl.chunk_tokens;
+  gp.num_splits = pl.num_splits;
+  gp.write_final = pl.writes_final;
+  const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
+  if ((phases & kSplit) &&
+      da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, gp, grid, stream) != cudaSuccess)
+    return DA_ERR_CUDA;
+  if ((phases & kMerge) && !pl.writes_final) {
+    da::MergeParams mp;
+    mp.o_part = gp.o_part;
+    mp.lse_part = gp.lse_part;
+    mp.out = gp.out;
+    mp.lse = a->lse;
+    mp.rows = p.batch * p.num_q_heads;
+    mp.num_splits = pl.num_splits;
+    mp.rows_per_unit = gp.group;
+    mp.dv = 128;
+    if (da::launch_merge(mp, stream) != cudaSuccess) return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream, int phases) {
+  const da_problem &p = ctx->prob;
+  if (!a->q || !a->q_pe || !a->k || !a->v || !a->seq_lens || !a->out || !a->block_table)
+    return DA_ERR_INVALID_ARG;
+  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 16) || !aligned(a->q_pe, 16) ||
+      !aligned(a->out, 16))
+    return DA_ERR_INVALID_ARG;
+  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v) {
+    da_status st;
+    // ckv rows are 1024 B = 8 TMA rows of 64 bf16; kpe rows are 128 B = 1 TMA row
+    const uint64_t tokens = (uint64_t)p.num_pages * p.page_size;
+    if ((st = encode_rows(&ctx->kmap, a->k, true, tokens * 8, 256)) != DA_OK) return st;
+    if ((st = encode_rows(&ctx->vmap, a->v, true, tokens, 64)) != DA_OK) {
+      ctx->map_k_base = nullptr;
+      return st;
+    }
+    ctx->map_k_base = a->k;
+    ctx->map_v_base = a->v;
+  }
+  const da_plan_info &pl = ctx->plan;
+  da::MlaParams mp;
+  std::memset(&mp, 0, sizeof mp);
+  mp.q_nope = reinterpret_cast<const __nv_bfloat16 *>(a->q);
+  mp.q_pe = reinterpret_cast<const __nv_bfloat16 *>(a->q_pe);
+  mp.block_table = a->block_table;
+  mp.seq_lens = a->seq_lens;
+  mp.o_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_o_offset);
+  mp.lse_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_lse_offset);
+  mp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
+  mp.lse = a->lse;
+  mp.err = reinterpret_cast<uint32_t *>(ws);
+  mp.score_scale = a->scale * 1.4426950408889634f;
+  mp.batch = p.batch;
+  mp.max_pages = p.max_pages_per_seq;
+  mp.num_pages = p.num_pages;
+  mp.capacity = p.max_pages_per_seq * p.page_size;
+  mp.chunk = pl.chunk_tokens;
+  mp.num_splits = pl.num_splits;
+  mp.write_final = pl.writes_final;
+  const dim3 grid(pl.grid_x, 1, pl.grid_z);
+  if (phases & kSplit) {
+    cudaError_t e = da::launch_mla(ctx->kmap, ctx->vmap, mp, grid, stream);
+    if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return DA_ERR_CUDA;
+  }
+  if ((phases & kMerge) && !pl.writes_final) {
+    da::MergeParams m;
+    m.o_part = mp.o_part;
+    m.lse_part = mp.lse_part;
+    m.out = mp.out;
+    m.lse = a->lse;
+    m.rows = p.batch * p.num_q_heads;
+    m.num_splits = pl.num_splits;
+    m.rows_per_unit = p.num_q_heads;
+    m.dv = 512;
+    if (da::launch_merge(m, stream) != cudaSuccess) return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+da_status decode_attn_create(const da_problem *problem, int device, da_ctx **out) {
+  if (!out) return DA_ERR_INVALID_ARG;
+  *out = nullptr;
+  da_status st = da::validate_problem(problem);
+  if (st != DA_OK) return st;
+  int sms = 0, smem = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return DA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) !=
+      cudaSuccess)
+    return DA_ERR_CUDA;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return DA_ERR_CUDA;
+  cudaError_t e = problem->is_mla ? da::mla_prepare(device) : da::gqa_prepare(device);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess && e != cudaErrorNotSupported) return DA_ERR_CUDA;
+  da_ctx *ctx = new (std::nothrow) da_ctx;
+  if (!ctx) return DA_ERR_INVALID_ARG;
+  std::memset(ctx, 0, sizeof *ctx);
+  ctx->prob = *problem;
+  ctx->device = device;
+  ctx->num_sms = sms;
+  ctx->smem_per_sm = smem;
+  *out = ctx;
+  return DA_OK;
+}
+
+da_status decode_attn_plan_ex(da_ctx *ctx, const int32_t *seq_lens_host,
+                              const int32_t *kv_num_blks_host, int32_t num_splits_override,
+                              size_t *workspace_bytes) {
+  if (!ctx) return DA_ERR_INVALID_ARG;
+  da_plan_info info;
+  da_status st = da::plan_compute(&ctx->prob, ctx->num_sms, ctx->smem_per_sm, seq_lens_host,
+                                  kv_num_blks_host, num_splits_override, &info);
+  if (st != DA_OK) return st;
+  ctx->plan = info;
+  ctx->planned = true;
+  if (workspace_bytes) *workspace_bytes = (size_t)info.workspace_bytes;
+  return DA_OK;
+}
+
+da_status decode_attn_plan(da_ctx *ctx, const int32_t *seq_lens_host, int32_t num_splits_override,
+                           size_t *workspace_bytes) {
+  return decode_attn_plan_ex(ctx, seq_lens_host, nullptr, num_splits_override, workspace_bytes);
+}
+
+da_status decode_attn_get_plan(const da_ctx *ctx, da_plan_info *info) {
+  if (!ctx || !info) return DA_ERR_INVALID_ARG;
+  if (!ctx->planned) return DA_ERR_NOT_PLANNED;
+  *info = ctx->plan;
+  return DA_OK;
+}
+
+da_status decode_attn_plan_info(const da_problem *problem, int32_t num_sms,
+                                const int32_t *seq_lens_host, int32_t num_splits_override,
+                                da_plan_info *info) {
+  // GB300: 228 KB of shared memory per SM
+  return da::plan_compute(problem, num_sms, 233472, seq_lens_host, nullptr, num_splits_override,
+                          info);
+}
+
+static da_status run_phases(da_ctx *ctx, const da_args *args, void *workspace,
+                            size_t workspace_bytes, da_stream_t stream, int phases) {
+  if (!ctx || !args) return DA_ERR_INVALID_ARG;
+  if (!ctx->planned) return DA_ERR_NOT_PLANNED;
+  da_status st = check_workspace(ctx, workspace, workspace_bytes);
+  if (st != DA_OK) return st;
+  if (!(args->scale == args->scale)) return DA_ERR_INVALID_ARG;  // NaN scale
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  if (dev != ctx->device) return DA_ERR_INVALID_ARG;  // the context's device must be current
+  auto *ws = reinterpret_cast<uint8_t *>(workspace);
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  return ctx->prob.is_mla ? run_mla(ctx, args, ws, s, phases) : run_gqa(ctx, args, ws, s, phases);
+}
+
+da_status decode_attn_run(da_ctx *ctx, const da_args *args, void *workspace, size_t workspace_bytes,
+                          da_stream_t stream) {
+  return run_phases(ctx, args, workspace, workspace_bytes, stream, kSplit | kMerge);
+}
+
+da_status decode_attn_run_split(da_ctx *ctx, const da_args *args, void *workspace,
+                                size_t workspace_bytes, da_stream_t stream) {
+  return run_phases(ctx, args, workspace, workspace_bytes, stream, kSplit);
+}
+
+da_status decode_attn_run_merge(da_ctx *ctx, const da_args *args, void *workspace,
+                                size_t workspace_bytes, da_stream_t stream) {
+  return run_phases(ctx, args, workspace, workspace_bytes, stream, kMerge);
+}
+
+da_status decode_attn_merge(da_ctx *ctx, const float *o_part, const float *lse_part,
+                            int32_t num_splits, int32_t rows, int32_t dv, void *out, float *lse,
+                            da_stream_t stream) {
+  (void)ctx;
+  if (!o_part || !lse_part || !out) return DA_ERR_INVALID_ARG;
+  if (num_splits <= 0 || rows < 0 || dv <= 0 || dv % 4 != 0 || dv > 1024) return DA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(out, 8)) return DA_ERR_INVALID_ARG;
+  da::MergeParams m;
+  m.o_part = o_part;
+  m.lse_part = lse_part;
+  m.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  m.lse = lse;
+  m.rows = rows;
+  m.num_splits = num_splits;
+  m.rows_per_unit = 1;
+  m.dv = dv;
+  return da::launch_merge(m, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DA_OK
+                                                                                      : DA_ERR_CUDA;
+}
+
+da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream, uint32_t *flags) {
+  (void)ctx;
+  if (!workspace || !flags) return DA_ERR_INVALID_ARG;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
+  *flags = word;
+  return word ? DA_ERR_DEVICE : DA_OK;
+}
+
+void decode_attn_destroy(da_ctx *ctx) { delete ctx; }
+
+const char *decode_attn_status_string(da_status status) {
+  switch (status) {
+    case DA_OK: return "ok";
+    case DA_ERR_INVALID_ARG: return "invalid argument";
+    case DA_ERR_UNSUPPORTED: return "unsupported problem";
+    case DA_ERR_CUDA: return "CUDA error";
+    case DA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DA_ERR_NOT_PLANNED: return "decode_attn_plan has not been called";
+    case DA_ERR_DEVICE: return "device reported an error (see the DA_DEVERR_* bits)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// internal.h -- host/device structures shared by the C ABI and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "decode_attn.h"
+
+namespace da {
+
+// Time limit of every pipeline wait inside a kernel (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
+
+// Workspace: [error word | pad to 256 B][partial O fp32][partial LSE fp32]
+constexpr int64_t kWorkspaceHeader = 256;
+
+struct GqaParams {
+  const __nv_bfloat16 *q;      // [B][HQ][128]
+  const int32_t *block_table;  // paged: [B][max_pages]
+  const int32_t *seq_lens;     // [B]
+  const int32_t *kv_num_blks;  // sparse: [B][HKV]
+  const int32_t *kv_idx;       // sparse: [B][HKV][max_sparse_blocks]
+  const float *k_scale;        // fp8: [HKV]
+  const float *v_scale;        // fp8: [HKV]
+  float *o_part;               // [units][S][G][128]
+  float *lse_part;             // [units][S][G]
+  __nv_bfloat16 *out;          // [B][HQ][128]
+  float *lse;                  // [B][HQ] or null
+  uint32_t *err;               // device error word
+  float score_scale;           // scale * log2(e)
+  int32_t batch, num_q_heads, num_kv_heads, group;
+  int32_t paged, page_size, cache_len, max_pages, num_pages;
+  int32_t capacity;            // max positions per row
+  int32_t sparse_block_size, max_sparse_blocks;
+  int32_t chunk;               // positions (dense) or list entries * block (sparse) per split
+  int32_t num_splits;
+  int32_t write_final;
+};
+
+struct MergeParams {
+  const float *o_part;   // element (u, s, g, d) at ((u*S + s)*R + g)*dv + d
+  const float *lse_part; // element (u, s, g) at (u*S + s)*R + g
+  __nv_bfloat16 *out;    // [rows][dv], row = u*R + g
+  float *lse;            // [rows] or null
+  int32_t rows, num_splits, rows_per_unit, dv;
+};
+
+struct MlaParams {
+  const __nv_bfloat16 *q_nope;  // [B][128][512]
+  const __nv_bfloat16 *q_pe;    // [B][128][64]
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  float *o_part;                // [B][S][128][512]
+  float *lse_part;              // [B][S][128]
+  __nv_bfloat16 *out;           // [B][128][512]
+  float *lse;
+  uint32_t *err;
+  float score_scale;
+  int32_t batch, max_pages, num_pages, capacity;
+  int32_t chunk, num_splits, write_final;
+};
+
+// Kernel launchers (return the launch error).
+cudaError_t gqa_prepare(int device);  // sets shared-memory attributes once per device
+int gqa_smem_bytes(bool fp8);
+int gqa_threads();
+cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                       const GqaParams &p, dim3 grid, cudaStream_t stream);
+int gqa_box_tokens(const da_problem &p);
+
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+
+cudaError_t mla_prepare(int device);
+int mla_smem_bytes();
+int mla_threads();
+cudaError_t launch_mla(const CUtensorMap &ckv_map, const CUtensorMap &kpe_map,
+                       const MlaParams &p, dim3 grid, cudaStream_t stream);
+
+// Planner (pure host code).
+da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm,
+                       const int32_t *seq_lens_host, const int32_t *kv_num_blks_host,
+                       int32_t num_splits_override, da_plan_info *info);
+da_status validate_problem(const da_problem *p);
+
+}  // namespace da

@@ -132,8 +132,10 @@ def quantize_e4m3(x: torch.Tensor, head_axis: int):
 def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_lens,
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
-             num_splits=0, poison=True) -> Workload:
-    """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths."""
+             num_splits=0, poison=True, shape_only=False) -> Workload:
+    """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths.
+    ``shape_only`` skips drawing the K/V caches (lengths, tables and lists are
+    drawn exactly as in the full workload)."""
     g = _gen(seed)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32)
     B, HQ, HKV, D = batch, num_q_heads, num_kv_heads, head_dim
@@ -146,16 +148,28 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
     t = {"q": q, "seq_lens": seq_lens}
     if layout == "paged":
         table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
+        w.paged, w.page_size, w.num_pages, w.max_pages_per_seq = True, page_size, num_pages, max_pages
+        t["block_table"] = table
+        if shape_only:
+            w.tensors = t
+            return w
         k = torch.randn((num_pages, HKV, page_size, D), generator=g, dtype=torch.float32)
         v = torch.randn((num_pages, HKV, page_size, D), generator=g, dtype=torch.float32)
         if poison:
             _poison_paged(k, table, seq_lens, page_size, used, True)
             _poison_paged(v, table, seq_lens, page_size, used, True)
-        w.paged, w.page_size, w.num_pages, w.max_pages_per_seq = True, page_size, num_pages, max_pages
-        t["block_table"] = table
         head_axis = 1
     else:
         L = int(cache_len if cache_len is not None else max(int(seq_lens.max()), 1))
+        w.cache_len = L
+        if shape_only:
+            if sparse_block_size:
+                w.sparse_block_size = sparse_block_size
+                t["kv_num_blks"] = torch.as_tensor(kv_num_blks, dtype=torch.int32).reshape(B, HKV)
+                t["kv_idx"] = torch.as_tensor(kv_idx, dtype=torch.int32).reshape(B, HKV, -1)
+                w.max_sparse_blocks = t["kv_idx"].shape[-1]
+            w.tensors = t
+            return w
         k = torch.randn((B, HKV, L, D), generator=g, dtype=torch.float32)
         v = torch.randn((B, HKV, L, D), generator=g, dtype=torch.float32)
         w.cache_len = L
@@ -215,7 +229,8 @@ def sparse_lists(batch, num_kv_heads, cache_len, block_size, keep_random, keep_l
 
 
 def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq_lens,
-             page_size=64, scale=None, seed=0, num_splits=0, poison=True) -> Workload:
+             page_size=64, scale=None, seed=0, num_splits=0, poison=True,
+             shape_only=False) -> Workload:
     g = _gen(seed)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32)
     B, HQ = batch, num_q_heads
@@ -223,16 +238,19 @@ def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq
     q_nope = _randn_bf16((B, HQ, ckv_dim), g)
     q_pe = _randn_bf16((B, HQ, kpe_dim), g)
     table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
-    ckv = torch.randn((num_pages, page_size, ckv_dim), generator=g, dtype=torch.float32)
-    kpe = torch.randn((num_pages, page_size, kpe_dim), generator=g, dtype=torch.float32)
-    if poison:
-        _poison_paged(ckv, table, seq_lens, page_size, used, False)
-        _poison_paged(kpe, table, seq_lens, page_size, used, False)
     w = Workload(name=name, batch=B, num_q_heads=HQ, num_kv_heads=1,
                  head_dim_qk=ckv_dim + kpe_dim, head_dim_v=ckv_dim,
                  scale=float(torch.tensor(scale, dtype=torch.float32)), is_mla=True,
                  ckv_dim=ckv_dim, kpe_dim=kpe_dim, paged=True, page_size=page_size,
                  max_pages_per_seq=max_pages, num_pages=num_pages, num_splits=num_splits)
+    if shape_only:
+        w.tensors = {"q": q_nope, "q_pe": q_pe, "block_table": table, "seq_lens": seq_lens}
+        return w
+    ckv = torch.randn((num_pages, page_size, ckv_dim), generator=g, dtype=torch.float32)
+    kpe = torch.randn((num_pages, page_size, kpe_dim), generator=g, dtype=torch.float32)
+    if poison:
+        _poison_paged(ckv, table, seq_lens, page_size, used, False)
+        _poison_paged(kpe, table, seq_lens, page_size, used, False)
     w.tensors = {"q": q_nope, "q_pe": q_pe, "k": ckv.to(torch.bfloat16).contiguous(),
                  "v": kpe.to(torch.bfloat16).contiguous(), "block_table": table,
                  "seq_lens": seq_lens}
@@ -250,28 +268,30 @@ CONFIG_NAMES = {
 }
 
 
-def config(i: int) -> Workload:
+def config(i: int, shape_only: bool = False) -> Workload:
+    """The five decode workloads; ``shape_only`` skips drawing the K/V caches."""
     seed = 1000 + i
+    so = dict(shape_only=shape_only)
     if i == 1:
         return make_gqa(name="tiny_gqa", batch=1, num_q_heads=8, num_kv_heads=1,
-                        seq_lens=[512], cache_len=512, seed=seed, num_splits=4)
+                        seq_lens=[512], cache_len=512, seed=seed, num_splits=4, **so)
     if i == 2:
         g = _gen(seed + 500)
         lens = _lengths(32, 1024, 8192, g)
         return make_gqa(name="paged_gqa", batch=32, num_q_heads=32, num_kv_heads=8,
-                        seq_lens=lens, layout="paged", page_size=16, seed=seed)
+                        seq_lens=lens, layout="paged", page_size=16, seed=seed, **so)
     if i == 3:
         return make_gqa(name="fp8_long", batch=1, num_q_heads=64, num_kv_heads=8,
-                        seq_lens=[131072], cache_len=131072, kv_fp8=True, seed=seed)
+                        seq_lens=[131072], cache_len=131072, kv_fp8=True, seed=seed, **so)
     if i == 4:
         g = _gen(seed + 500)
         num, idx = sparse_lists(8, 8, 32768, 128, keep_random=32, keep_last=4, g=g,
                                 max_blocks=256)
         return make_gqa(name="block_sparse", batch=8, num_q_heads=32, num_kv_heads=8,
                         seq_lens=[32768] * 8, cache_len=32768, sparse_block_size=128,
-                        kv_num_blks=num, kv_idx=idx, seed=seed)
+                        kv_num_blks=num, kv_idx=idx, seed=seed, **so)
     if i == 5:
         g = _gen(seed + 500)
         lens = _lengths(64, 2048, 8192, g)
-        return make_mla(name="mla", batch=64, seq_lens=lens, seed=seed)
+        return make_mla(name="mla", batch=64, seq_lens=lens, seed=seed, **so)
     raise ValueError(f"no workload {i}")

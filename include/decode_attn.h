@@ -1,0 +1,249 @@
+/*
+ * decode_attn.h -- C ABI of the GB300 split-KV decode-attention library.
+ *
+ * The operation (per batch row b and query head hq, with kv head h = hq / G,
+ * G = num_q_heads / num_kv_heads):
+ *
+ *     out[b][hq] = softmax(scale * q[b][hq] . K^T over P(b,h)) V
+ *     lse[b][hq] = ln sum_{n in P(b,h)} exp(scale * q[b][hq] . k_n)
+ *
+ * where P(b,h) is the row's valid KV positions: 0 .. seq_lens[b]-1, or, for
+ * block-sparse decode, the listed blocks kv_idx[b][h][0 .. kv_num_blks[b][h]-1]
+ * (each block of sparse_block_size positions, clipped to seq_lens[b]). An empty
+ * P gives out = 0 and lse = -inf.
+ *
+ * Sources of the operation:
+ *  - GQA packing and the block-sparse KV_NUM_BLKS / KV_IDX tables (indexed by
+ *    kv head): the TorchInductor flex_decode.py.jinja template (header comment
+ *    and the "normal blocks" traversal);
+ *  - paged translation page = block_table[b][n / page_size]: the split-K
+ *    decode kernel of mslk splitk_kernels.py (`_fwd_kernel_splitK`, paged
+ *    branch) and the KV page list of TensorRT-LLM xqa/mha.cu (`launchMHA`);
+ *  - per-split normalised O plus natural-log LSE and their LSE-weighted merge:
+ *    splitk_kernels.py (`_fwd_kernel_splitK` "write back O", `_splitK_reduce`);
+ *  - MLA latent decode (scores over [ckv ; kpe], values ckv): FlashInfer
+ *    include/flashinfer/attention/mla.cuh (`BatchMLAPagedAttentionKernel`);
+ *  - fp8 KV: e4m3 (`float8e4nv` in splitk_kernels.py) times a per-kv-head
+ *    fp32 scale (the single K/V cache scale of xqa/mha.cu, kept per head).
+ *
+ * Conventions for every entry point:
+ *  - All tensors are row-major, last index fastest, in device memory owned by
+ *    the caller; the library never allocates device memory and never frees a
+ *    caller pointer. The only library-owned object is the host-side context.
+ *  - Every function returns a da_status; no C++ exception or abort crosses
+ *    the ABI. A failed call leaves the outputs unspecified.
+ *  - decode_attn_run and decode_attn_merge only enqueue work on the given
+ *    stream (no allocation, no synchronisation).
+ */
+#ifndef DECODE_ATTN_H_
+#define DECODE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *da_stream_t;
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_INVALID_ARG = 1,  /* null pointer, bad dimension, bad override   */
+  DA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. D != 128)   */
+  DA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed           */
+  DA_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small  */
+  DA_ERR_NOT_PLANNED = 5,  /* decode_attn_run before decode_attn_plan     */
+  DA_ERR_DEVICE = 6        /* the device error word is non-zero           */
+} da_status;
+
+typedef enum { DA_KV_CONTIGUOUS = 0, DA_KV_PAGED = 1 } da_kv_layout;
+typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP8_E4M3 = 1 } da_dtype;
+
+/* Bits of the device error word (sticky until decode_attn_get_error clears it). */
+enum {
+  DA_DEVERR_PAGE_INDEX = 1u,   /* block_table entry outside [0, num_pages): page skipped   */
+  DA_DEVERR_SPARSE_INDEX = 2u, /* kv_idx outside the cache or kv_num_blks outside
+                                  [0, max_sparse_blocks]: block skipped / count clamped   */
+  DA_DEVERR_SEQ_LEN = 4u,      /* seq_lens[b] < 0 or over the cache capacity: clamped      */
+  DA_DEVERR_TIMEOUT = 8u       /* a pipeline wait gave up after its time limit             */
+};
+
+/*
+ * Problem description, fixed at create time.
+ *
+ *   GQA: head_dim_qk = head_dim_v = 128, num_q_heads % num_kv_heads == 0,
+ *        G = num_q_heads / num_kv_heads in 1..16.
+ *   MLA: is_mla = 1, num_kv_heads = 1, ckv_dim = 512, kpe_dim = 64,
+ *        head_dim_qk = 576, head_dim_v = 512, kv_layout = DA_KV_PAGED.
+ *   Paged: page_size a multiple of 16 that divides 64 or is a multiple of 64
+ *        (MLA: 64); max_pages_per_seq table columns; num_pages pool size.
+ *   Contiguous: max_seq_len is the cache length L of [B][HKV][L][D].
+ *   Sparse (GQA, contiguous only): sparse_block_size a multiple of 64,
+ *        max_sparse_blocks columns of kv_idx; 0 = dense.
+ */
+typedef struct {
+  int32_t batch, num_q_heads, num_kv_heads;
+  int32_t head_dim_qk, head_dim_v;
+  int32_t is_mla, ckv_dim, kpe_dim;
+  da_kv_layout kv_layout;
+  int32_t page_size;
+  int32_t max_seq_len;        /* contiguous: L; paged: at most max_pages_per_seq * page_size */
+  int32_t max_pages_per_seq;
+  int32_t num_pages;
+  da_dtype q_dtype;           /* DA_DTYPE_BF16 only */
+  da_dtype kv_dtype;          /* bf16, or e4m3 for GQA */
+  int32_t sparse_block_size;
+  int32_t max_sparse_blocks;
+} da_problem;
+
+/*
+ * Per-call arguments: device pointers, caller-owned.
+ *
+ *   q          bf16 [B][HQ][Dqk]   (MLA: q_nope [B][HQ][512])
+ *   q_pe       MLA only: bf16 [B][HQ][64]; else NULL
+ *   k, v       contiguous [B][HKV][L][D]; paged [num_pages][HKV][page_size][D];
+ *              MLA: k = ckv [num_pages][page_size][512], v = kpe [num_pages][page_size][64].
+ *              Element type bf16, or e4m3 bytes when kv_dtype is DA_DTYPE_FP8_E4M3.
+ *              Base addresses 16-byte aligned.
+ *   k_scale, v_scale  fp8 only: fp32 [HKV]; dequantised value = e4m3 * scale
+ *   block_table paged: int32 [B][max_pages_per_seq]; entries past a row's
+ *              last page are never read
+ *   seq_lens   int32 [B]
+ *   kv_num_blks, kv_idx  sparse only: int32 [B][HKV] and [B][HKV][max_sparse_blocks]
+ *   scale      the full softmax scale (e.g. 1/sqrt(128)); applied in fp32
+ *   out        bf16 [B][HQ][Dv]
+ *   lse        fp32 [B][HQ], natural log; may be NULL
+ */
+typedef struct {
+  const void *q;
+  const void *q_pe;
+  const void *k;
+  const void *v;
+  const float *k_scale;
+  const float *v_scale;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *kv_num_blks;
+  const int32_t *kv_idx;
+  float scale;
+  void *out;
+  float *lse;
+} da_args;
+
+/* What the planner decided (host-side, informational). */
+typedef struct {
+  int32_t kv_tile;          /* tokens per pipeline stage                               */
+  int32_t chunk_tokens;     /* positions per split (sparse: list entries x block size) */
+  int32_t num_splits;       /* S_max: splits per (b, kv head) unit                     */
+  int32_t num_units;        /* B x HKV (MLA: B)                                        */
+  int32_t rows_per_unit;    /* G (MLA: HQ)                                             */
+  int32_t grid_x, grid_y, grid_z;
+  int32_t ctas_per_sm;      /* resident CTAs of the split kernel per SM                */
+  int32_t writes_final;     /* 1: one split, the split kernel writes out/lse directly  */
+  int64_t partial_o_offset; /* byte offsets inside the workspace                       */
+  int64_t partial_lse_offset;
+  int64_t workspace_bytes;
+} da_plan_info;
+
+typedef struct da_ctx da_ctx;
+
+/*
+ * Validates the problem, reads the SM count and shared-memory limit of
+ * `device` and returns a new host context in *out. The caller owns the
+ * context and releases it with decode_attn_destroy.
+ * Errors: INVALID_ARG (null, bad dims), UNSUPPORTED, CUDA (device query).
+ */
+da_status decode_attn_create(const da_problem *problem, int device, da_ctx **out);
+
+/*
+ * Chooses the split size and grid (the XQA-style split count heuristic: enough
+ * (b, kv head, split) CTAs to fill every SM, splits a multiple of the KV tile,
+ * at least 256 positions each) and reports the workspace size in
+ * *workspace_bytes. seq_lens_host (int32 [B], host memory, may be NULL)
+ * lets the planner size splits from the real lengths; without it the plan
+ * assumes every row is max_seq_len long. num_splits_override > 0 forces that
+ * many splits per unit (positions are cut into equal tile-aligned chunks).
+ * Host-only; no GPU work. Errors: INVALID_ARG.
+ */
+da_status decode_attn_plan(da_ctx *ctx, const int32_t *seq_lens_host, int32_t num_splits_override,
+                           size_t *workspace_bytes);
+
+/*
+ * decode_attn_plan with the block-sparse list lengths too: kv_num_blks_host
+ * (int32 [B][HKV], host memory, may be NULL) lets the planner size splits of a
+ * block-sparse problem from the real list lengths instead of max_sparse_blocks.
+ */
+da_status decode_attn_plan_ex(da_ctx *ctx, const int32_t *seq_lens_host,
+                              const int32_t *kv_num_blks_host, int32_t num_splits_override,
+                              size_t *workspace_bytes);
+
+/* The plan the last decode_attn_plan produced. Errors: INVALID_ARG, NOT_PLANNED. */
+da_status decode_attn_get_plan(const da_ctx *ctx, da_plan_info *info);
+
+/*
+ * The planner as a pure host function of (problem, SM count): the same
+ * decision decode_attn_plan makes on a device with `num_sms` SMs. Needs no GPU.
+ */
+da_status decode_attn_plan_info(const da_problem *problem, int32_t num_sms,
+                                const int32_t *seq_lens_host, int32_t num_splits_override,
+                                da_plan_info *info);
+
+/*
+ * Enqueues the decode on `stream`: one split-kernel launch, then (when the
+ * plan has more than one split) one LSE-merge launch. `workspace` is device
+ * memory of at least the planned size, 256-byte aligned; its first 4 bytes
+ * hold the sticky device error word, which must be zero in a new workspace
+ * (allocate it zeroed or call decode_attn_get_error once). Out-of-range
+ * indices found on the device set error bits (DA_DEVERR_*) and are skipped,
+ * never read. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, NOT_PLANNED, CUDA.
+ */
+da_status decode_attn_run(da_ctx *ctx, const da_args *args, void *workspace, size_t workspace_bytes,
+                          da_stream_t stream);
+
+/*
+ * The two halves of decode_attn_run, for callers that schedule or time them
+ * apart: decode_attn_run_split enqueues only the split kernel (partials into
+ * the workspace, or the final output when the plan has one split);
+ * decode_attn_run_merge enqueues only the merge of those partials into
+ * args->out / args->lse (nothing when the plan has one split). Same
+ * arguments, ownership and errors as decode_attn_run.
+ */
+da_status decode_attn_run_split(da_ctx *ctx, const da_args *args, void *workspace,
+                                size_t workspace_bytes, da_stream_t stream);
+da_status decode_attn_run_merge(da_ctx *ctx, const da_args *args, void *workspace,
+                                size_t workspace_bytes, da_stream_t stream);
+
+/*
+ * Standalone LSE merge of `num_splits` partial results per row:
+ *   o_part   fp32 [rows][num_splits][dv]  (normalised per split)
+ *   lse_part fp32 [rows][num_splits]      (natural log; -inf marks an empty split,
+ *                                          whose o_part is never read)
+ *   out      bf16 [rows][dv];  lse fp32 [rows] (may be NULL)
+ * out = sum_s w_s o_s / sum_s w_s, w_s = exp(lse_s - max lse), lse = max + ln sum w;
+ * rows whose splits are all empty get out = 0, lse = -inf (`_splitK_reduce` of
+ * splitk_kernels.py). dv must be a multiple of 4, at most 1024; pointers 16-byte
+ * aligned. `ctx` may be NULL. Errors: INVALID_ARG, CUDA.
+ */
+da_status decode_attn_merge(da_ctx *ctx, const float *o_part, const float *lse_part,
+                            int32_t num_splits, int32_t rows, int32_t dv, void *out, float *lse,
+                            da_stream_t stream);
+
+/*
+ * Synchronises `stream`, copies the device error word of `workspace` to
+ * *flags and clears it. Returns DA_ERR_DEVICE when the word was non-zero.
+ */
+da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream, uint32_t *flags);
+
+/* Releases the context (NULL is allowed). */
+void decode_attn_destroy(da_ctx *ctx);
+
+/* A static, human-readable name for a status code. */
+const char *decode_attn_status_string(da_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H_ */

@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs, plus the bit-exact gather checks and device error flags.
+
+Tolerances (floating point): bf16 outputs max-abs 2e-2 and rel 1e-2
+(rel = max|gpu - oracle| / max(max|oracle|, 1e-6)), LSE within 1e-3 absolute,
+fp8 KV within 3e-2 against the oracle on the same dequantised values.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_flash_gb300 as da
+from decode_attention_flash_gb300 import workloads as W
+from helpers import assert_parity, reference, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ small cases, several tiles + ragged tails
+
+def test_tiny_config_four_splits():
+    w = W.config(1)
+    out, lse, flags, eng = run_gpu(w)
+    assert eng.plan["num_splits"] == 4 and flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="config 1")
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 5])
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+def test_paged_ragged(splits, page_size):
+    lens = [1, 17, 64, 65, 700, 1000, 0, 333]
+    w = W.make_gqa(name="paged", batch=8, num_q_heads=32, num_kv_heads=8, seq_lens=lens,
+                   layout="paged", page_size=page_size, seed=100 + page_size)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"paged P={page_size} S={splits}")
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+def test_contiguous_group_sizes(group):
+    hkv = 2
+    w = W.make_gqa(name="contig", batch=3, num_q_heads=group * hkv, num_kv_heads=hkv,
+                   seq_lens=[257, 1, 900], cache_len=1000, seed=200 + group)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=3)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"G={group}")
+
+
+def test_lse_pointer_may_be_null():
+    w = W.make_gqa(name="nolse", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[300, 40],
+                   cache_len=300, seed=5)
+    out, _, flags, _ = run_gpu(w, num_splits_override=2, with_lse=False)
+    ref_out, _ = reference(w)
+    assert_parity(out, None, ref_out, None, what="lse=NULL")
+
+
+def test_plan_without_host_lengths():
+    w = W.make_gqa(name="nohost", batch=4, num_q_heads=16, num_kv_heads=4, layout="paged",
+                   seq_lens=[100, 2000, 3, 1500], seed=6)
+    out, lse, flags, eng = run_gpu(w, seq_lens_host=False, num_splits_override=0)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="plan without host lengths")
+
+
+def test_fp8_small():
+    w = W.make_gqa(name="fp8", batch=2, num_q_heads=16, num_kv_heads=2, seq_lens=[3000, 77],
+                   cache_len=3000, kv_fp8=True, seed=8)
+    for S in (0, 1, 4):
+        out, lse, flags, _ = run_gpu(w, num_splits_override=S)
+        assert flags == 0
+        ref_out, ref_lse = reference(w)
+        assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8 S={S}")
+
+
+def test_fp8_paged():
+    w = W.make_gqa(name="fp8p", batch=3, num_q_heads=24, num_kv_heads=3, seq_lens=[500, 16, 95],
+                   layout="paged", page_size=16, kv_fp8=True, seed=9)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, fp8=True, what="fp8 paged")
+
+
+def _sparse(seed=10, lens=(4096, 4000), block=128):
+    g = torch.Generator().manual_seed(seed)
+    num, idx = W.sparse_lists(2, 4, 4096, block, keep_random=5, keep_last=2, g=g, max_blocks=12)
+    return W.make_gqa(name="sparse", batch=2, num_q_heads=16, num_kv_heads=4, seq_lens=list(lens),
+                      cache_len=4096, sparse_block_size=block, kv_num_blks=num, kv_idx=idx,
+                      seed=seed)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_sparse_small(splits):
+    w = _sparse()
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"sparse S={splits}")
+
+
+def test_sparse_block_64_and_empty_lists():
+    g = torch.Generator().manual_seed(11)
+    num, idx = W.sparse_lists(2, 2, 1024, 64, keep_random=3, keep_last=1, g=g, max_blocks=8)
+    num[1, 0] = 0  # an empty list: out 0, lse -inf
+    w = W.make_gqa(name="sparse64", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[1024, 1000],
+                   cache_len=1024, sparse_block_size=64, kv_num_blks=num, kv_idx=idx, seed=11)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="sparse 64")
+    assert torch.all(out[1, :4] == 0) and torch.all(lse[1, :4] == -float("inf"))
+
+
+def test_split_count_invariance():
+    w = W.make_gqa(name="inv", batch=2, num_q_heads=8, num_kv_heads=1, seq_lens=[4000, 2500],
+                   cache_len=4000, seed=12)
+    outs = [run_gpu(w, num_splits_override=s)[0].double() for s in (1, 2, 7, 16)]
+    for o in outs[1:]:
+        assert float((o - outs[0]).abs().max()) < 5e-3
+
+
+# ------------------------------------------------------------------ bit-exact gathers
+
+def test_paged_equals_contiguous_on_depaged_cache_bitwise():
+    w = W.make_gqa(name="pg", batch=4, num_q_heads=16, num_kv_heads=4,
+                   seq_lens=[1000, 64, 1, 513], layout="paged", page_size=16, seed=13)
+    t = w.tensors
+    L = w.max_pages_per_seq * w.page_size
+    pages = t["block_table"].long()
+    k = t["k"][pages].permute(0, 2, 1, 3, 4).reshape(w.batch, w.num_kv_heads, L, 128)
+    v = t["v"][pages].permute(0, 2, 1, 3, 4).reshape(w.batch, w.num_kv_heads, L, 128)
+    c = W.Workload(name="depaged", batch=w.batch, num_q_heads=16, num_kv_heads=4, head_dim_qk=128,
+                   head_dim_v=128, scale=w.scale, cache_len=L,
+                   tensors=dict(q=t["q"], k=k.contiguous(), v=v.contiguous(), seq_lens=t["seq_lens"]))
+    for S in (1, 3):
+        op, lp, _, _ = run_gpu(w, num_splits_override=S)
+        oc, lc, _, _ = run_gpu(c, num_splits_override=S)
+        assert torch.equal(op.view(torch.int16), oc.view(torch.int16))
+        assert torch.equal(lp, lc)
+
+
+def test_sparse_equals_contiguous_on_compacted_blocks_bitwise():
+    w = _sparse(seed=14, lens=(4096, 4096))
+    t = w.tensors
+    G, SBS = w.group, w.sparse_block_size
+    rows_k, rows_v, lens = [], [], []
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            blocks = t["kv_idx"][b, h, :int(t["kv_num_blks"][b, h])].long()
+            pos = (blocks[:, None] * SBS + torch.arange(SBS)).reshape(-1)
+            rows_k.append(t["k"][b, h, pos])
+            rows_v.append(t["v"][b, h, pos])
+            lens.append(pos.numel())
+    L = max(lens)
+    BH = w.batch * w.num_kv_heads
+    k = torch.zeros((BH, 1, L, 128), dtype=torch.bfloat16)
+    v = torch.zeros((BH, 1, L, 128), dtype=torch.bfloat16)
+    for i in range(BH):
+        k[i, 0, :lens[i]] = rows_k[i]
+        v[i, 0, :lens[i]] = rows_v[i]
+    c = W.Workload(name="compact", batch=BH, num_q_heads=G, num_kv_heads=1, head_dim_qk=128,
+                   head_dim_v=128, scale=w.scale, cache_len=L,
+                   tensors=dict(q=t["q"].reshape(BH, G, 128).contiguous(), k=k, v=v,
+                                seq_lens=torch.tensor(lens, dtype=torch.int32)))
+    S = 4  # 7 listed blocks: 256-position splits in both problems
+    os_, ls_, _, es = run_gpu(w, num_splits_override=S)
+    oc, lc, _, ec = run_gpu(c, num_splits_override=S)
+    assert es.plan["chunk_tokens"] == ec.plan["chunk_tokens"]
+    assert torch.equal(os_.reshape(BH, G, 128).view(torch.int16), oc.view(torch.int16))
+    assert torch.equal(ls_.reshape(BH, G), lc)
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_single_token_rows_return_the_value_row_bitwise(splits):
+    w = W.make_gqa(name="one", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[1, 1, 1],
+                   layout="paged", page_size=16, seed=15)
+    out, lse, _, _ = run_gpu(w, num_splits_override=splits)
+    t = w.tensors
+    for b in range(3):
+        page = int(t["block_table"][b, 0])
+        for hq in range(8):
+            assert torch.equal(out[b, hq].view(torch.int16), t["v"][page, hq // 4, 0].view(torch.int16))
+
+
+# ------------------------------------------------------------------ device error flags (host-made faults)
+
+def test_bad_page_index_sets_flag_and_is_skipped():
+    w = W.make_gqa(name="badpage", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[100, 50],
+                   layout="paged", page_size=16, seed=16)
+    bt = w.tensors["block_table"].clone()
+    bt[0, 1] = w.num_pages + 5
+    bt[1, 0] = -3
+    w.tensors["block_table"] = bt
+    out, lse, flags, _ = run_gpu(w, num_splits_override=1)
+    assert flags & da.DA_DEVERR_PAGE_INDEX
+    assert torch.all(torch.isfinite(out.float()))
+
+
+def test_seq_len_over_capacity_sets_flag():
+    w = W.make_gqa(name="badlen", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[100, 50],
+                   cache_len=128, seed=17, poison=False)
+    eng = da.DecodeAttention(device=0, num_splits_override=2, **da.problem_kwargs(w))
+    w.tensors["seq_lens"] = torch.tensor([5000, -4], dtype=torch.int32)
+    out, lse, flags, _ = run_gpu(w, engine=eng)
+    assert flags & da.DA_DEVERR_SEQ_LEN
+    assert torch.all(out[1] == 0) and torch.all(lse[1] == -float("inf"))
+
+
+def test_bad_sparse_index_sets_flag():
+    w = _sparse(seed=18)
+    idx = w.tensors["kv_idx"].clone()
+    idx[0, 0, 0] = 10_000
+    w.tensors["kv_idx"] = idx
+    out, lse, flags, _ = run_gpu(w, num_splits_override=1)
+    assert flags & da.DA_DEVERR_SPARSE_INDEX
+    assert torch.all(torch.isfinite(out.float()))
+
+
+def test_workspace_too_small_is_rejected():
+    w = W.make_gqa(name="ws", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[1000, 50],
+                   cache_len=1000, seed=19)
+    eng = da.DecodeAttention(device=0, num_splits_override=4, **da.problem_kwargs(w))
+    eng.workspace = eng.workspace[:64]
+    with pytest.raises(da.DecodeAttnError) as e:
+        eng.run(w.to("cuda"), w.scale)
+    assert e.value.status == da.DA_ERR_WORKSPACE
+
+
+# ------------------------------------------------------------------ standalone merge
+
+def test_standalone_merge_matches_oracle_merge():
+    import oracle
+    g = torch.Generator().manual_seed(20)
+    rows, S, dv = 300, 9, 512
+    o = torch.randn((rows, S, dv), generator=g)
+    lse = torch.randn((rows, S), generator=g) * 3
+    lse[::7, 2] = -float("inf")
+    lse[5] = -float("inf")  # a row with every split empty
+    o[::7, 2] = float("nan")  # never read
+    dev = torch.device("cuda", 0)
+    out = torch.empty((rows, dv), dtype=torch.bfloat16, device=dev)
+    lo = torch.empty((rows,), dtype=torch.float32, device=dev)
+    da.decode_attn_merge(None, o.to(dev), lse.to(dev), S, rows, dv, out, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.merge(o.double().numpy(), lse.double().numpy())
+    assert_parity(out.cpu(), lo.cpu(), ref_o, ref_l, what="merge")
