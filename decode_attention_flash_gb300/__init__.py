@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "DecodeAttnError", "Problem", "Args", "PlanInfo", "load", "decode_attn_create",
     "decode_attn_plan", "decode_attn_plan_ex", "decode_attn_get_plan", "decode_attn_plan_info",
-    "decode_attn_run", "decode_attn_run_split", "decode_attn_run_merge", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
+    "decode_attn_run", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
     "decode_attn_status_string", "DecodeAttention", "DA_KV_CONTIGUOUS", "DA_KV_PAGED",
     "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3",
 ]
@@ -63,7 +63,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "kv_tile", "chunk_tokens", "num_splits", "num_units", "rows_per_unit", "grid_x", "grid_y",
         "grid_z", "ctas_per_sm", "writes_final")] + [
-        ("partial_o_offset", ctypes.c_int64), ("partial_lse_offset", ctypes.c_int64),
+        ("counters_offset", ctypes.c_int64), ("partial_o_offset", ctypes.c_int64), ("partial_lse_offset", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
@@ -94,8 +94,6 @@ def load(build_if_missing: bool = False):
         "decode_attn_plan_info": (st, [ctypes.POINTER(Problem), i32, vp, i32,
                                        ctypes.POINTER(PlanInfo)]),
         "decode_attn_run": (st, [vp, ctypes.POINTER(Args), vp, ctypes.c_size_t, vp]),
-        "decode_attn_run_split": (st, [vp, ctypes.POINTER(Args), vp, ctypes.c_size_t, vp]),
-        "decode_attn_run_merge": (st, [vp, ctypes.POINTER(Args), vp, ctypes.c_size_t, vp]),
         "decode_attn_merge": (st, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
         "decode_attn_get_error": (st, [vp, vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "decode_attn_destroy": (None, [vp]),
@@ -202,18 +200,6 @@ def decode_attn_run(ctx, args: Args, workspace: torch.Tensor, stream=None):
     _check(load().decode_attn_run(ctx, ctypes.byref(args), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "decode_attn_run")
-
-
-def decode_attn_run_split(ctx, args: Args, workspace: torch.Tensor, stream=None):
-    _check(load().decode_attn_run_split(ctx, ctypes.byref(args), _ptr(workspace),
-                                        workspace.numel() * workspace.element_size(),
-                                        _stream(stream)), "decode_attn_run_split")
-
-
-def decode_attn_run_merge(ctx, args: Args, workspace: torch.Tensor, stream=None):
-    _check(load().decode_attn_run_merge(ctx, ctypes.byref(args), _ptr(workspace),
-                                        workspace.numel() * workspace.element_size(),
-                                        _stream(stream)), "decode_attn_run_merge")
 
 
 def decode_attn_merge(ctx, o_part, lse_part, num_splits: int, rows: int, dv: int, out, lse=None,

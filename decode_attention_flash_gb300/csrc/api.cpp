@@ -66,10 +66,7 @@ da_status check_workspace(const da_ctx *ctx, const void *ws, size_t bytes) {
   return DA_OK;
 }
 
-// phase bit 1: split kernel, bit 2: merge kernel
-enum { kSplit = 1, kMerge = 2 };
-
-da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream, int phases) {
+da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream) {
   const da_problem &p = ctx->prob;
   const bool fp8 = p.kv_dtype == DA_DTYPE_FP8_E4M3;
   const bool paged = p.kv_layout == DA_KV_PAGED;
@@ -113,6 +110,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
   gp.lse = a->lse;
   gp.err = reinterpret_cast<uint32_t *>(ws);
+  gp.counters = reinterpret_cast<uint32_t *>(ws + pl.counters_offset);
   gp.score_scale = a->scale * 1.4426950408889634f;
   gp.batch = p.batch;
   gp.num_q_heads = p.num_q_heads;
@@ -130,25 +128,12 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.num_splits = pl.num_splits;
   gp.write_final = pl.writes_final;
   const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
-  if ((phases & kSplit) &&
-      da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, gp, grid, stream) != cudaSuccess)
+  if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, gp, grid, stream) != cudaSuccess)
     return DA_ERR_CUDA;
-  if ((phases & kMerge) && !pl.writes_final) {
-    da::MergeParams mp;
-    mp.o_part = gp.o_part;
-    mp.lse_part = gp.lse_part;
-    mp.out = gp.out;
-    mp.lse = a->lse;
-    mp.rows = p.batch * p.num_q_heads;
-    mp.num_splits = pl.num_splits;
-    mp.rows_per_unit = gp.group;
-    mp.dv = 128;
-    if (da::launch_merge(mp, stream) != cudaSuccess) return DA_ERR_CUDA;
-  }
   return DA_OK;
 }
 
-da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream, int phases) {
+da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream) {
   const da_problem &p = ctx->prob;
   if (!a->q || !a->q_pe || !a->k || !a->v || !a->seq_lens || !a->out || !a->block_table)
     return DA_ERR_INVALID_ARG;
@@ -179,6 +164,7 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
   mp.lse = a->lse;
   mp.err = reinterpret_cast<uint32_t *>(ws);
+  mp.counters = reinterpret_cast<uint32_t *>(ws + pl.counters_offset);
   mp.score_scale = a->scale * 1.4426950408889634f;
   mp.batch = p.batch;
   mp.max_pages = p.max_pages_per_seq;
@@ -188,23 +174,9 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.num_splits = pl.num_splits;
   mp.write_final = pl.writes_final;
   const dim3 grid(pl.grid_x, 1, pl.grid_z);
-  if (phases & kSplit) {
-    cudaError_t e = da::launch_mla(ctx->kmap, ctx->vmap, mp, grid, stream);
-    if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return DA_ERR_CUDA;
-  }
-  if ((phases & kMerge) && !pl.writes_final) {
-    da::MergeParams m;
-    m.o_part = mp.o_part;
-    m.lse_part = mp.lse_part;
-    m.out = mp.out;
-    m.lse = a->lse;
-    m.rows = p.batch * p.num_q_heads;
-    m.num_splits = pl.num_splits;
-    m.rows_per_unit = p.num_q_heads;
-    m.dv = 512;
-    if (da::launch_merge(m, stream) != cudaSuccess) return DA_ERR_CUDA;
-  }
+  cudaError_t e = da::launch_mla(ctx->kmap, ctx->vmap, mp, grid, stream);
+  if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
 }
 
@@ -274,8 +246,8 @@ da_status decode_attn_plan_info(const da_problem *problem, int32_t num_sms,
                           info);
 }
 
-static da_status run_phases(da_ctx *ctx, const da_args *args, void *workspace,
-                            size_t workspace_bytes, da_stream_t stream, int phases) {
+da_status decode_attn_run(da_ctx *ctx, const da_args *args, void *workspace, size_t workspace_bytes,
+                          da_stream_t stream) {
   if (!ctx || !args) return DA_ERR_INVALID_ARG;
   if (!ctx->planned) return DA_ERR_NOT_PLANNED;
   da_status st = check_workspace(ctx, workspace, workspace_bytes);
@@ -286,22 +258,7 @@ static da_status run_phases(da_ctx *ctx, const da_args *args, void *workspace,
   if (dev != ctx->device) return DA_ERR_INVALID_ARG;  // the context's device must be current
   auto *ws = reinterpret_cast<uint8_t *>(workspace);
   auto s = reinterpret_cast<cudaStream_t>(stream);
-  return ctx->prob.is_mla ? run_mla(ctx, args, ws, s, phases) : run_gqa(ctx, args, ws, s, phases);
-}
-
-da_status decode_attn_run(da_ctx *ctx, const da_args *args, void *workspace, size_t workspace_bytes,
-                          da_stream_t stream) {
-  return run_phases(ctx, args, workspace, workspace_bytes, stream, kSplit | kMerge);
-}
-
-da_status decode_attn_run_split(da_ctx *ctx, const da_args *args, void *workspace,
-                                size_t workspace_bytes, da_stream_t stream) {
-  return run_phases(ctx, args, workspace, workspace_bytes, stream, kSplit);
-}
-
-da_status decode_attn_run_merge(da_ctx *ctx, const da_args *args, void *workspace,
-                                size_t workspace_bytes, da_stream_t stream) {
-  return run_phases(ctx, args, workspace, workspace_bytes, stream, kMerge);
+  return ctx->prob.is_mla ? run_mla(ctx, args, ws, s) : run_gqa(ctx, args, ws, s);
 }
 
 da_status decode_attn_merge(da_ctx *ctx, const float *o_part, const float *lse_part,
@@ -331,8 +288,17 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
   uint32_t word = 0;
   if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DA_ERR_CUDA;
-  if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return DA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
+  if (word) {
+    if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return DA_ERR_CUDA;
+    if ((word & DA_DEVERR_TIMEOUT) && ctx && ctx->planned) {
+      auto *ws = reinterpret_cast<uint8_t *>(workspace);
+      if (cudaMemsetAsync(ws + ctx->plan.counters_offset, 0, (size_t)ctx->plan.num_units * 4, s) !=
+          cudaSuccess)
+        return DA_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
+  }
   *flags = word;
   return word ? DA_ERR_DEVICE : DA_OK;
 }

@@ -57,42 +57,38 @@ struct Smem {
   static constexpr int kFull = Traits<FP8>::kRingBytes;
   static constexpr int kEmpty = kFull + 8 * Traits<FP8>::kStages;
   static constexpr int kMeta = kEmpty + 8 * Traits<FP8>::kStages;
-  static constexpr int kFlags = kMeta + 8 * Traits<FP8>::kStages;
+  static constexpr int kFlags = kMeta + 8 * Traits<FP8>::kStages;  // abort, last-CTA
   static constexpr int kStats = kFlags + 16;              // m, l per (warp, g): 2*4*16 floats
-  static constexpr int kTotal = kStats + 2 * kConsumerWarps * 16 * 4 + 1024;  // + align slack
+  static constexpr int kIds = kStats + 2 * kConsumerWarps * 16 * 4;  // page / block ids
+  static constexpr int kTotal = kIds + kGqaMaxIds * 4 + 1024;        // + align slack
 };
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
 // ------------------------------------------------------------------ producer
 
-// Fills tile `i` of this CTA into stage `st`: looks up the pages / sparse block,
-// checks every index, records which tokens are valid and issues the TMA boxes.
+// Fills tile `i` of this CTA into stage `st`: takes the pages / sparse block
+// from the ids staged in shared memory (already range-checked; -1 marks an
+// invalid one, which is skipped), records which tokens are valid and issues
+// the TMA boxes.
 template <bool FP8>
 __device__ __forceinline__ void produce_tile(const GqaParams &p, const CUtensorMap *kmap,
                                              const CUtensorMap *vmap, uint8_t *ring,
-                                             uint64_t *full, StageMeta *meta, int st, int i,
-                                             int b, int h, int n_valid, int range_lo,
-                                             int range_hi, uint64_t policy, uint32_t &err) {
+                                             uint64_t *full, StageMeta *meta, const int *ids,
+                                             int st, int i, int b, int h, int n_valid,
+                                             int range_lo, int range_hi, uint64_t policy) {
   using T = Traits<FP8>;
   uint8_t *kdst = ring + (size_t)st * 2 * T::kTileBytes;
   uint8_t *vdst = kdst + T::kTileBytes;
   const int row_mult = FP8 ? 1 : 2;  // bf16 rows are split into two 128-byte TMA rows
   uint64_t valid = 0;
-  uint32_t bytes = 0;
-  int tok_base;     // first token of the tile (position in the row)
   int64_t row0 = -1;  // first cache row of a single-box tile
 
   if (p.sparse_block_size > 0) {
     const int tiles_per_block = p.sparse_block_size / kTile;
-    const int j = range_lo + i / tiles_per_block;
-    const int sub = i % tiles_per_block;
-    const int blk = p.kv_idx[((int64_t)b * p.num_kv_heads + h) * p.max_sparse_blocks + j];
-    if (blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len) {
-      err |= DA_DEVERR_SPARSE_INDEX;
-      tok_base = 0;
-    } else {
-      tok_base = blk * p.sparse_block_size + sub * kTile;
+    const int blk = ids[i / tiles_per_block];
+    if (blk >= 0) {
+      const int tok_base = blk * p.sparse_block_size + (i % tiles_per_block) * kTile;
       int lim = min(n_valid - tok_base, kTile);
       lim = min(lim, p.cache_len - tok_base);
       if (lim > 0) {
@@ -101,7 +97,7 @@ __device__ __forceinline__ void produce_tile(const GqaParams &p, const CUtensorM
       }
     }
   } else {
-    tok_base = range_lo + i * kTile;
+    const int tok_base = range_lo + i * kTile;
     const int lim = min(range_hi - tok_base, kTile);
     if (!p.paged) {
       if (lim > 0) {
@@ -109,41 +105,35 @@ __device__ __forceinline__ void produce_tile(const GqaParams &p, const CUtensorM
         row0 = ((int64_t)b * p.num_kv_heads + h) * p.cache_len + tok_base;
       }
     } else if (p.page_size >= kTile) {
-      const int page = p.block_table[(int64_t)b * p.max_pages + tok_base / p.page_size];
-      if (page < 0 || page >= p.num_pages) {
-        err |= DA_DEVERR_PAGE_INDEX;
-      } else if (lim > 0) {
+      const int page = ids[tok_base / p.page_size - range_lo / p.page_size];
+      if (page >= 0 && lim > 0) {
         valid = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
         row0 = ((int64_t)page * p.num_kv_heads + h) * p.page_size + tok_base % p.page_size;
       }
     } else {
-      // several pages per tile: one box per page; look every page up first so
-      // the transaction count is set before any copy is issued
+      // several pages per tile: one box per page
       const int P = p.page_size;
-      int ys[kTile / 16];
+      const int first = tok_base / P - range_lo / P;
       int nbox = 0;
       for (int j = 0; j < kTile / P; ++j) {
         const int t0 = tok_base + j * P;
-        ys[j] = -1;
         if (t0 >= range_hi) break;
-        const int page = p.block_table[(int64_t)b * p.max_pages + t0 / P];
-        if (page < 0 || page >= p.num_pages) {
-          err |= DA_DEVERR_PAGE_INDEX;
-          continue;
-        }
+        if (ids[first + j] < 0) continue;
         const int cnt = min(range_hi - t0, P);
         valid |= ((cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull)) << (j * P));
-        ys[j] = (int)(((int64_t)page * p.num_kv_heads + h) * P * row_mult);
         ++nbox;
       }
       meta[st].valid = valid;
+      // the transaction count is set before any copy is issued
       mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)(nbox * P * T::kBytesPerTok));
       for (int j = 0; j < kTile / P; ++j) {
         if (tok_base + j * P >= range_hi) break;
-        if (ys[j] < 0) continue;
+        const int page = ids[first + j];
+        if (page < 0) continue;
+        const int y = (int)(((int64_t)page * p.num_kv_heads + h) * P * row_mult);
         const int off = j * P * T::kBytesPerTok;
-        tma_load_2d(kdst + off, kmap, &full[st], 0, ys[j], policy);
-        tma_load_2d(vdst + off, vmap, &full[st], 0, ys[j], policy);
+        tma_load_2d(kdst + off, kmap, &full[st], 0, y, policy);
+        tma_load_2d(vdst + off, vmap, &full[st], 0, y, policy);
       }
       return;
     }
@@ -151,13 +141,108 @@ __device__ __forceinline__ void produce_tile(const GqaParams &p, const CUtensorM
   meta[st].valid = valid;
   if (row0 >= 0) {
     const int y = (int)(row0 * row_mult);
-    bytes = 2u * (uint32_t)T::kTileBytes;
-    mbar_arrive_expect_tx(&full[st], bytes);
+    mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)T::kTileBytes);
     tma_load_2d(kdst, kmap, &full[st], 0, y, policy);
     tma_load_2d(vdst, vmap, &full[st], 0, y, policy);
   } else {
     mbar_arrive_expect_tx(&full[st], 0);
   }
+}
+
+// Stages the page ids (paged) or listed block ids (sparse) of this CTA's range
+// into shared memory with the producer warp's 32 lanes, checking every one:
+// an id outside the pool / cache becomes -1 and sets an error bit.
+__device__ __forceinline__ uint32_t stage_ids(const GqaParams &p, int *ids, int b, int h,
+                                              int range_lo, int range_hi, int lane) {
+  uint32_t err = 0;
+  if (p.sparse_block_size > 0) {
+    const int32_t *list = p.kv_idx + ((int64_t)b * p.num_kv_heads + h) * p.max_sparse_blocks;
+    for (int j = lane; j < range_hi - range_lo; j += 32) {
+      int blk = list[range_lo + j];
+      if (blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len) {
+        err |= DA_DEVERR_SPARSE_INDEX;
+        blk = -1;
+      }
+      ids[j] = blk;
+    }
+  } else if (p.paged) {
+    const int first = range_lo / p.page_size;
+    const int count = (range_hi - 1) / p.page_size - first + 1;
+    const int32_t *row = p.block_table + (int64_t)b * p.max_pages + first;
+    for (int j = lane; j < count; j += 32) {
+      int page = row[j];
+      if (page < 0 || page >= p.num_pages) {
+        err |= DA_DEVERR_PAGE_INDEX;
+        page = -1;
+      }
+      ids[j] = page;
+    }
+  }
+  return err;
+}
+
+// The last CTA of a (b, kv head) unit to finish merges the unit's per-split
+// results (LSE-weighted, as `_splitK_reduce` of splitk_kernels.py) into the
+// final bf16 output and LSE -- the multi-block merge of TensorRT-LLM
+// xqa/mha.cu, found with an atomic counter per unit and no spinning wait. The
+// counter is reset by the merging CTA, so it is zero again for the next call.
+__device__ __forceinline__ void merge_if_last(const GqaParams &p, int b, int h, int G,
+                                              float *scratch, volatile int *last_flag) {
+  const int64_t unit = (int64_t)b * p.num_kv_heads + h;
+  const int S = p.num_splits;
+  __threadfence();  // this CTA's partial results are visible before the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(p.counters + unit, 1u);
+    *last_flag = (prev == (unsigned)(S - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!*last_flag) return;
+  __threadfence();
+  float *w = scratch;           // [S][16] weights (lse first)
+  float *stat = w + S * 16;     // [16] 1/sum, [16] lse
+  const float *lse_part = p.lse_part + unit * S * G;
+  for (int i = threadIdx.x; i < S * G; i += blockDim.x)
+    w[(i / G) * 16 + (i % G)] = __ldcg(lse_part + i);
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
+    float M = neg_inf();
+    for (int s = 0; s < S; ++s) M = fmaxf(M, w[s * 16 + g]);
+    float sum = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float l = w[s * 16 + g];
+      const float e = (M == neg_inf() || l == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
+      w[s * 16 + g] = e;
+      sum += e;
+    }
+    stat[g] = sum > 0.f ? 1.f / sum : 0.f;
+    stat[16 + g] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+  }
+  __syncthreads();
+  const float4 *o_part = reinterpret_cast<const float4 *>(p.o_part + unit * S * G * kD);
+  for (int i = threadIdx.x; i < G * (kD / 4); i += blockDim.x) {
+    const int g = i / (kD / 4), c = i % (kD / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) {
+      const float e = w[s * 16 + g];
+      if (e != 0.f) {
+        const float4 v = __ldcg(o_part + ((int64_t)s * G + g) * (kD / 4) + c);
+        acc.x += e * v.x;
+        acc.y += e * v.y;
+        acc.z += e * v.z;
+        acc.w += e * v.w;
+      }
+    }
+    const float inv = stat[g];
+    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
+        p.out + ((int64_t)b * p.num_q_heads + h * G + g) * kD + 4 * c);
+    dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  }
+  if (threadIdx.x < G && p.lse) p.lse[(int64_t)b * p.num_q_heads + h * G + threadIdx.x] = stat[16 + threadIdx.x];
+  if (threadIdx.x == 0) p.counters[unit] = 0u;
 }
 
 // ------------------------------------------------------------------ consumer helpers
@@ -200,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + S::kEmpty);
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::kMeta);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlags);
+  volatile int *last_flag = abort_flag + 1;
+  int *ids = reinterpret_cast<int *>(smem + S::kIds);
   float *stat_m = reinterpret_cast<float *>(smem + S::kStats);
   float *stat_l = stat_m + kConsumerWarps * 16;
 
@@ -235,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t slot = unit * p.num_splits + split;
 
   if (num_tiles == 0) {
-    // empty split: O = 0, LSE = -inf
+    // empty split: O = 0, LSE = -inf (its O slot is never read by the merge)
+    if (threadIdx.x == 0 && dev_err) atomicOr(p.err, dev_err);
     if (threadIdx.x < G) {
       if (p.write_final) {
         const int64_t row = (int64_t)b * p.num_q_heads + h * G + threadIdx.x;
@@ -247,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.write_final) {
       for (int e = threadIdx.x; e < G * kD; e += blockDim.x)
         p.out[((int64_t)b * p.num_q_heads + h * G) * kD + e] = __float2bfloat16(0.f);
+      return;
     }
-    if (threadIdx.x == 0 && dev_err) atomicOr(p.err, dev_err);
+    merge_if_last(p, b, h, G, reinterpret_cast<float *>(ring), last_flag);
     return;
   }
 
@@ -279,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ================= producer =================
+    dev_err |= stage_ids(p, ids, b, h, range_lo, range_hi, lane);
+    __syncwarp();
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
@@ -293,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
-        produce_tile<FP8>(p, &kmap, &vmap, ring, full, meta, st, i, b, h, n_valid, range_lo,
-                          range_hi, policy, dev_err);
+        produce_tile<FP8>(p, &kmap, &vmap, ring, full, meta, ids, st, i, b, h, n_valid,
+                          range_lo, range_hi, policy);
       }
     }
   } else {
@@ -511,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&full[st], (i_last / T::kStages) & 1, kWaitLimitNs);
       }
     }
-    if (lane == 0) atomicOr(p.err, dev_err | DA_DEVERR_TIMEOUT);
+    if (lane == 0 || dev_err) atomicOr(p.err, dev_err | DA_DEVERR_TIMEOUT);
     return;
   }
 
@@ -575,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (threadIdx.x == 0 && dev_err) atomicOr(p.err, dev_err);
-  if (threadIdx.x == kConsumerWarps * 32 && dev_err) atomicOr(p.err, dev_err);
+  if (dev_err) atomicOr(p.err, dev_err);
+  if (!p.write_final) merge_if_last(p, b, h, G, red, last_flag);
 }
 
 template <bool FP8, int NT>

@@ -13,8 +13,12 @@ namespace da {
 // Time limit of every pipeline wait inside a kernel (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;
 
-// Workspace: [error word | pad to 256 B][partial O fp32][partial LSE fp32]
+// Workspace: [error word | pad to 256 B][unit counters u32][partial O fp32][partial LSE fp32]
 constexpr int64_t kWorkspaceHeader = 256;
+// Page / block ids one split CTA stages in shared memory (caps the split length).
+constexpr int kGqaMaxIds = 512;
+// Splits per unit the fused merge handles (its weights live in shared memory).
+constexpr int kMaxSplits = 256;
 
 struct GqaParams {
   const __nv_bfloat16 *q;      // [B][HQ][128]
@@ -29,6 +33,7 @@ struct GqaParams {
   __nv_bfloat16 *out;          // [B][HQ][128]
   float *lse;                  // [B][HQ] or null
   uint32_t *err;               // device error word
+  uint32_t *counters;          // [units] finished-split counters (self-resetting)
   float score_scale;           // scale * log2(e)
   int32_t batch, num_q_heads, num_kv_heads, group;
   int32_t paged, page_size, cache_len, max_pages, num_pages;
@@ -57,6 +62,7 @@ struct MlaParams {
   __nv_bfloat16 *out;           // [B][128][512]
   float *lse;
   uint32_t *err;
+  uint32_t *counters;
   float score_scale;
   int32_t batch, max_pages, num_pages, capacity;
   int32_t chunk, num_splits, write_final;

@@ -1,17 +1,21 @@
 // plan.cpp -- host planner: how many KV splits per (batch row, kv head) unit,
-// the grid, and the workspace layout. Pure host integer code.
+// the grid, and the workspace layout. Pure host code.
 //
-// The split count follows the idea of the XQA launcher (TensorRT-LLM
-// xqa/mha.cu, `launchMHA`: sub-sequences per sequence = SMs / (B x HKV),
-// capped by the sequence length in CTA tiles) and the tile-aligned split
-// length of the flex-decode template (flex_decode.py.jinja:
-// TILE_KV = cdiv(cdiv(KV_LEN, SPLIT_KV), BLOCK_N) * BLOCK_N): the planner
-// sizes one split length (a multiple of the KV tile; of the sparse block for
-// block-sparse decode) so that the CTAs of all units fill every SM a few
-// times over, with at least kMinChunk positions per split so the per-split
-// fixed cost (Q load, pipeline fill, partial write) stays small.
+// The split count generalises the XQA launcher (TensorRT-LLM xqa/mha.cu,
+// `launchMHA`: sub-sequences per sequence = SMs / (B x HKV), capped by the
+// sequence length in CTA tiles) and keeps the tile-aligned split length of
+// the flex-decode template (flex_decode.py.jinja: TILE_KV = cdiv(cdiv(KV_LEN,
+// SPLIT_KV), BLOCK_N) * BLOCK_N). Instead of a closed formula, the planner
+// tries every split count S that keeps the grid within a few dozen CTAs per
+// SM, simulates the hardware's in-order CTA dispatch onto the resident slots
+// (cost of a CTA = fixed start/epilogue cost + its KV bytes at the per-slot
+// share of HBM bandwidth, plus the fused merge of the unit's last CTA) and
+// keeps the S with the smallest estimated makespan.
 #include <algorithm>
 #include <cstring>
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "internal.h"
 
@@ -20,8 +24,12 @@ namespace da {
 namespace {
 constexpr int kGqaTile = 64;
 constexpr int kMlaTile = 64;
-constexpr int kMinChunk = 256;
-constexpr int kWaves = 2;  // CTA waves per SM the planner aims for
+// cost model (seconds); only ratios matter for the choice
+constexpr double kHbmBytesPerSec = 6.5e12;
+constexpr double kCtaFixedSec = 2.0e-6;
+constexpr double kMergeBytesPerSec = 100e9;  // one CTA reading the unit's partials
+constexpr double kMergeFixedSec = 1.0e-6;
+constexpr int kMaxCtasPerSlot = 24;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -47,7 +55,7 @@ da_status validate_problem(const da_problem *p) {
       return DA_ERR_UNSUPPORTED;
     if (p->kv_layout != DA_KV_PAGED || p->page_size != 64) return DA_ERR_UNSUPPORTED;
     if (p->kv_dtype != DA_DTYPE_BF16 || p->sparse_block_size != 0) return DA_ERR_UNSUPPORTED;
-    if ((int64_t)p->num_pages * p->page_size * 2 >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    if ((int64_t)p->num_pages * p->page_size * 8 >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     return DA_OK;
   }
   if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
@@ -74,9 +82,37 @@ da_status validate_problem(const da_problem *p) {
 
 // Resident CTAs of the split kernel per SM, from its shared-memory footprint.
 static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
-  const int per_cta = (p->is_mla ? mla_smem_bytes() : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3)) +
-                      1024;  // the runtime reserves 1 KB per CTA
-  return std::max(1, std::min(smem_per_sm / per_cta, 2048 / (p->is_mla ? mla_threads() : gqa_threads())));
+  const bool mla = p->is_mla != 0;
+  const int per_cta =
+      (mla ? mla_smem_bytes() : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3)) +
+      1024;  // the runtime reserves 1 KB per CTA
+  const int threads = mla ? mla_threads() : gqa_threads();
+  return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));
+}
+
+// Estimated time of the grid for split length `chunk` (see the file comment).
+static double makespan(const std::vector<int64_t> &unit_len, int heads, int64_t chunk,
+                       int64_t splits, int slots, double sec_per_pos, double merge_sec_per_split) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < slots; ++i) free_at.push(0.0);
+  const double per_slot = sec_per_pos * slots;  // a slot gets 1/slots of the bandwidth
+  double end = 0.0;
+  const int64_t units = (int64_t)unit_len.size();
+  (void)heads;
+  for (int64_t u = 0; u < units; ++u) {  // launch order: split fastest, then head, then row
+    double unit_done = 0.0;
+    for (int64_t s = 0; s < splits; ++s) {
+      const int64_t pos = std::max<int64_t>(0, std::min(chunk, unit_len[u] - s * chunk));
+      const double t0 = free_at.top();
+      free_at.pop();
+      const double t1 = t0 + (pos > 0 ? kCtaFixedSec + pos * per_slot : 0.2 * kCtaFixedSec);
+      free_at.push(t1);
+      unit_done = std::max(unit_done, t1);
+    }
+    if (splits > 1) unit_done += kMergeFixedSec + merge_sec_per_split * splits;
+    end = std::max(end, unit_done);
+  }
+  return end;
 }
 
 da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm,
@@ -89,51 +125,80 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
 
   const bool mla = p->is_mla != 0;
   const bool sparse = !mla && p->sparse_block_size > 0;
+  const bool paged = p->kv_layout == DA_KV_PAGED;
   const int tile = mla ? kMlaTile : kGqaTile;
   const int align = sparse ? p->sparse_block_size : tile;
   const int heads = mla ? 1 : p->num_kv_heads;
   const int64_t units = (int64_t)p->batch * heads;
-  const int64_t capacity = p->kv_layout == DA_KV_PAGED
-                               ? (int64_t)p->max_pages_per_seq * p->page_size
-                               : (int64_t)p->max_seq_len;
+  const int64_t capacity =
+      paged ? (int64_t)p->max_pages_per_seq * p->page_size : (int64_t)p->max_seq_len;
+  const int rows = mla ? p->num_q_heads : p->num_q_heads / p->num_kv_heads;
+  const int dv = p->head_dim_v;
 
   // positions per unit the split kernel walks (sparse: the compacted list)
-  int64_t max_len = 0, total = 0;
+  std::vector<int64_t> unit_len((size_t)units);
+  int64_t max_len = 0;
   for (int b = 0; b < p->batch; ++b) {
     for (int h = 0; h < heads; ++h) {
       int64_t len;
       if (sparse) {
         int64_t nblk = p->max_sparse_blocks;
-        if (kv_num_blks_host) {
+        if (kv_num_blks_host)
           nblk = std::min<int64_t>(std::max<int32_t>(kv_num_blks_host[(int64_t)b * heads + h], 0),
                                    p->max_sparse_blocks);
-        }
         len = nblk * p->sparse_block_size;
       } else {
         len = seq_lens_host ? std::min<int64_t>(std::max<int32_t>(seq_lens_host[b], 0), capacity)
                             : std::min<int64_t>(p->max_seq_len, capacity);
       }
+      unit_len[(size_t)((int64_t)b * heads + h)] = len;
       max_len = std::max(max_len, len);
-      total += len;
     }
   }
+  max_len = std::max<int64_t>(max_len, 1);
+
+  // largest split the kernel can take: its page / block ids fit in shared memory
+  int64_t max_chunk = round_up(max_len, align);
+  if (!mla && paged) max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size / align * align);
+  if (mla) max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size);
+  if (sparse) max_chunk = std::min<int64_t>(max_chunk, (int64_t)kGqaMaxIds * p->sparse_block_size);
+  max_chunk = std::max<int64_t>(max_chunk, align);
+  const int64_t min_splits = ceil_div(max_len, max_chunk);
+
   const int cps = ctas_per_sm(p, smem_per_sm);
+  const int slots = num_sms * cps;
   int64_t chunk;
   if (num_splits_override > 0) {
-    chunk = round_up(std::max<int64_t>(ceil_div(std::max<int64_t>(max_len, 1), num_splits_override), 1),
-                     align);
+    chunk = round_up(ceil_div(max_len, std::max<int64_t>(num_splits_override, min_splits)), align);
+    chunk = std::min(chunk, max_chunk);
   } else {
-    const int64_t target = (int64_t)num_sms * cps * kWaves;
-    chunk = round_up(std::max<int64_t>(ceil_div(total, target), 1), align);
-    chunk = std::max<int64_t>(chunk, round_up(kMinChunk, align));
+    const double bytes_per_pos =
+        mla ? (p->ckv_dim + p->kpe_dim) * 2.0 * 1.3  // MLA also pays its QK/PV flops
+            : (p->head_dim_qk + p->head_dim_v) * (p->kv_dtype == DA_DTYPE_FP8_E4M3 ? 1.0 : 2.0);
+    const double sec_per_pos = bytes_per_pos / kHbmBytesPerSec;
+    const double merge_sec_per_split = rows * (dv + 1) * 4.0 / kMergeBytesPerSec;
+    const int64_t max_ctas = (int64_t)slots * kMaxCtasPerSlot;
+    double best = 0.0;
+    chunk = max_chunk;
+    int64_t last_chunk = -1;
+    for (int64_t S = min_splits; S <= kMaxSplits; ++S) {
+      const int64_t c = std::min(round_up(ceil_div(max_len, S), align), max_chunk);
+      if (c == last_chunk) continue;
+      last_chunk = c;
+      const int64_t splits = ceil_div(max_len, c);
+      if (splits > kMaxSplits) break;
+      if (splits > 1 && units * splits > max_ctas) break;
+      const double t = makespan(unit_len, heads, c, splits, slots, sec_per_pos, merge_sec_per_split);
+      if (last_chunk == c && (best == 0.0 || t < best * 0.999)) {
+        best = t;
+        chunk = c;
+      }
+      if (c == align) break;
+    }
   }
-  chunk = std::min<int64_t>(chunk, round_up(std::max<int64_t>(max_len, 1), align));
-  if (chunk > (1ll << 30)) return DA_ERR_UNSUPPORTED;
   const int64_t splits = std::max<int64_t>(1, ceil_div(max_len, chunk));
-  if (splits > 65535) return DA_ERR_UNSUPPORTED;
+  if (splits > kMaxSplits) return DA_ERR_UNSUPPORTED;
 
-  const int rows = mla ? p->num_q_heads : p->num_q_heads / p->num_kv_heads;
-  const int dv = p->head_dim_v;
   info->kv_tile = tile;
   info->chunk_tokens = (int32_t)chunk;
   info->num_splits = (int32_t)splits;
@@ -145,6 +210,8 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   info->ctas_per_sm = cps;
   info->writes_final = splits == 1 ? 1 : 0;
   int64_t off = kWorkspaceHeader;
+  info->counters_offset = off;
+  off = align256(off + units * 4);
   if (!info->writes_final) {
     info->partial_o_offset = off;
     off = align256(off + units * splits * rows * (int64_t)dv * 4);

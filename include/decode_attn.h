@@ -142,7 +142,8 @@ typedef struct {
   int32_t grid_x, grid_y, grid_z;
   int32_t ctas_per_sm;      /* resident CTAs of the split kernel per SM                */
   int32_t writes_final;     /* 1: one split, the split kernel writes out/lse directly  */
-  int64_t partial_o_offset; /* byte offsets inside the workspace                       */
+  int64_t counters_offset;  /* byte offsets inside the workspace: per-unit counters,   */
+  int64_t partial_o_offset; /* per-split O and per-split LSE                           */
   int64_t partial_lse_offset;
   int64_t workspace_bytes;
 } da_plan_info;
@@ -191,29 +192,21 @@ da_status decode_attn_plan_info(const da_problem *problem, int32_t num_sms,
                                 da_plan_info *info);
 
 /*
- * Enqueues the decode on `stream`: one split-kernel launch, then (when the
- * plan has more than one split) one LSE-merge launch. `workspace` is device
- * memory of at least the planned size, 256-byte aligned; its first 4 bytes
- * hold the sticky device error word, which must be zero in a new workspace
- * (allocate it zeroed or call decode_attn_get_error once). Out-of-range
+ * Enqueues the decode on `stream` as ONE kernel launch: every (b, kv head,
+ * split) CTA writes its split's normalised O and LSE into the workspace, and
+ * the last CTA of each (b, kv head) to finish -- found with a per-unit atomic
+ * counter, without any spinning wait -- merges that unit's splits into `out`
+ * and `lse` (a plan with one split writes them directly). `workspace` is
+ * device memory of at least the planned size, 256-byte aligned, and must be
+ * zero when first used (allocate it zeroed): it holds the sticky device error
+ * word and the per-unit counters, which each call leaves at zero again.
+ * Calls that share a workspace must not overlap on the GPU. Out-of-range
  * indices found on the device set error bits (DA_DEVERR_*) and are skipped,
- * never read. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, NOT_PLANNED, CUDA.
+ * never read. The context's device must be current.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, NOT_PLANNED, CUDA.
  */
 da_status decode_attn_run(da_ctx *ctx, const da_args *args, void *workspace, size_t workspace_bytes,
                           da_stream_t stream);
-
-/*
- * The two halves of decode_attn_run, for callers that schedule or time them
- * apart: decode_attn_run_split enqueues only the split kernel (partials into
- * the workspace, or the final output when the plan has one split);
- * decode_attn_run_merge enqueues only the merge of those partials into
- * args->out / args->lse (nothing when the plan has one split). Same
- * arguments, ownership and errors as decode_attn_run.
- */
-da_status decode_attn_run_split(da_ctx *ctx, const da_args *args, void *workspace,
-                                size_t workspace_bytes, da_stream_t stream);
-da_status decode_attn_run_merge(da_ctx *ctx, const da_args *args, void *workspace,
-                                size_t workspace_bytes, da_stream_t stream);
 
 /*
  * Standalone LSE merge of `num_splits` partial results per row:
@@ -232,7 +225,10 @@ da_status decode_attn_merge(da_ctx *ctx, const float *o_part, const float *lse_p
 
 /*
  * Synchronises `stream`, copies the device error word of `workspace` to
- * *flags and clears it. Returns DA_ERR_DEVICE when the word was non-zero.
+ * *flags and clears it; after a DA_DEVERR_TIMEOUT it also re-zeroes the
+ * per-unit counters (an aborted call may leave them non-zero). Returns
+ * DA_ERR_DEVICE when the word was non-zero. `ctx` may be NULL (then the
+ * counters are left as they are).
  */
 da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream, uint32_t *flags);
 

@@ -123,10 +123,10 @@ def test_planner_covers_every_position_once(lib, cfg):
     if cfg == 1:
         assert plan["num_splits"] == 4 and plan["chunk_tokens"] == 128
     else:
-        # enough CTAs with work to fill every SM
+        # enough CTAs with work to fill every SM, and splits within the fused merge's limit
         busy = sum(math.ceil(n / plan["chunk_tokens"]) for n in lens) * plan["grid_y"]
         assert busy >= 152
-        assert plan["chunk_tokens"] >= 256
+        assert 1 <= plan["num_splits"] <= 256
 
 
 def test_planner_sparse_splits_whole_blocks(lib):
@@ -146,9 +146,10 @@ def test_planner_override_and_workspace_layout(lib):
         plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], S)
         assert plan["num_splits"] <= S
         _check_cover(plan, [1000, 5], 64)
+        assert plan["counters_offset"] == 256
         if plan["num_splits"] == 1:
             assert plan["writes_final"] == 1
-            assert plan["workspace_bytes"] == 256
+            assert plan["workspace_bytes"] == 512
         else:
             units, rows = 4, 4
             need_o = units * plan["num_splits"] * rows * 128 * 4
