@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "DecodeAttnError", "Problem", "Args", "PlanInfo", "load", "decode_attn_create",
     "decode_attn_plan", "decode_attn_plan_ex", "decode_attn_get_plan", "decode_attn_plan_info",
-    "decode_attn_run", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
+    "decode_attn_run", "decode_attn_run_noalloc", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
     "decode_attn_status_string", "DecodeAttention", "DA_KV_CONTIGUOUS", "DA_KV_PAGED",
     "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3",
 ]
@@ -95,6 +95,7 @@ def load(build_if_missing: bool = False):
                                        ctypes.POINTER(PlanInfo)]),
         "decode_attn_run": (st, [vp, ctypes.POINTER(Args), vp, ctypes.c_size_t, vp]),
         "decode_attn_merge": (st, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
+        "decode_attn_run_noalloc": (st, [vp, ctypes.POINTER(Args), vp]),
         "decode_attn_get_error": (st, [vp, vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "decode_attn_destroy": (None, [vp]),
         "decode_attn_status_string": (ctypes.c_char_p, [st]),
@@ -200,6 +201,13 @@ def decode_attn_run(ctx, args: Args, workspace: torch.Tensor, stream=None):
     _check(load().decode_attn_run(ctx, ctypes.byref(args), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
            "decode_attn_run")
+
+
+def decode_attn_run_noalloc(ctx, args: Args, stream=None):
+    """decode_attn_run without a workspace: the library's static device scratch
+    (32 MiB per device) is used instead, for callers that cannot allocate."""
+    _check(load().decode_attn_run_noalloc(ctx, ctypes.byref(args), _stream(stream)),
+           "decode_attn_run_noalloc")
 
 
 def decode_attn_merge(ctx, o_part, lse_part, num_splits: int, rows: int, dv: int, out, lse=None,

@@ -232,6 +232,30 @@ da_status decode_attn_merge(da_ctx *ctx, const float *o_part, const float *lse_p
  */
 da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream, uint32_t *flags);
 
+/*
+ * decode_attn_run for callers that cannot allocate device memory (an
+ * allocator's own hooks, server plugins that own every device allocation,
+ * code that must not risk an out-of-memory error or the synchronisation of
+ * cudaFree mid-step). The paper has no counterpart: it is a packaging variant
+ * of decode_attn_run. Instead of a caller workspace it uses one file-scope
+ * device array of 32 MiB (DA_NOALLOC_SCRATCH_BYTES) in this library, which
+ * every GPU that loads the library keeps until the process exits; it calls no
+ * cudaMalloc, cudaFree or allocating library routine. The caller still passes
+ * the inputs and outputs in `args`, as for decode_attn_run.
+ *
+ * The first call on a device looks up the array's device address and clears
+ * it synchronously, so make it before any stream capture starts. Each call
+ * then clears the error word and counters with a memset on `stream` and
+ * enqueues the same kernel as decode_attn_run. All calls on a device share
+ * the array: calls whose work overlaps on the GPU (other streams, other
+ * threads) race on it. Device-side error bits are not reported to the caller
+ * (bad indices are still skipped on the device). A plan whose workspace
+ * exceeds the array is refused with DA_ERR_WORKSPACE.
+ * Errors: INVALID_ARG, NOT_PLANNED, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+#define DA_NOALLOC_SCRATCH_BYTES (32u << 20)
+da_status decode_attn_run_noalloc(da_ctx *ctx, const da_args *args, da_stream_t stream);
+
 /* Releases the context (NULL is allowed). */
 void decode_attn_destroy(da_ctx *ctx);
 
