@@ -21,6 +21,11 @@ struct da_ctx {
   const void *map_v_base;
   CUtensorMap kmap;
   CUtensorMap vmap;
+  // MLA also maps the two query tensors
+  const void *map_q_base;
+  const void *map_qpe_base;
+  CUtensorMap qmap;
+  CUtensorMap qpemap;
 };
 
 namespace {
@@ -56,6 +61,22 @@ da_status encode_rows(CUtensorMap *map, const void *base, bool bf16, uint64_t ro
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                   const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+// A 2-D bf16 map over `rows` rows of `row_elems` elements (row pitch = row_elems * 2
+// bytes), 128B-swizzled boxes of 64 elements x `box_rows` rows.
+da_status encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t row_elems, uint64_t rows,
+                           uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * 2};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
@@ -137,20 +158,23 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   const da_problem &p = ctx->prob;
   if (!a->q || !a->q_pe || !a->k || !a->v || !a->seq_lens || !a->out || !a->block_table)
     return DA_ERR_INVALID_ARG;
-  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 16) || !aligned(a->q_pe, 16) ||
+  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 128) || !aligned(a->q_pe, 128) ||
       !aligned(a->out, 16))
     return DA_ERR_INVALID_ARG;
-  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v) {
-    da_status st;
-    // ckv rows are 1024 B = 8 TMA rows of 64 bf16; kpe rows are 128 B = 1 TMA row
+  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v || ctx->map_q_base != a->q ||
+      ctx->map_qpe_base != a->q_pe) {
     const uint64_t tokens = (uint64_t)p.num_pages * p.page_size;
-    if ((st = encode_rows(&ctx->kmap, a->k, true, tokens * 8, 256)) != DA_OK) return st;
-    if ((st = encode_rows(&ctx->vmap, a->v, true, tokens, 64)) != DA_OK) {
-      ctx->map_k_base = nullptr;
-      return st;
-    }
+    const uint64_t qrows = (uint64_t)p.batch * p.num_q_heads;
+    ctx->map_k_base = ctx->map_v_base = ctx->map_q_base = ctx->map_qpe_base = nullptr;
+    da_status st;
+    if ((st = encode_bf16_rows(&ctx->kmap, a->k, 512, tokens, 64)) != DA_OK) return st;
+    if ((st = encode_bf16_rows(&ctx->vmap, a->v, 64, tokens, 64)) != DA_OK) return st;
+    if ((st = encode_bf16_rows(&ctx->qmap, a->q, 512, qrows, 128)) != DA_OK) return st;
+    if ((st = encode_bf16_rows(&ctx->qpemap, a->q_pe, 64, qrows, 128)) != DA_OK) return st;
     ctx->map_k_base = a->k;
     ctx->map_v_base = a->v;
+    ctx->map_q_base = a->q;
+    ctx->map_qpe_base = a->q_pe;
   }
   const da_plan_info &pl = ctx->plan;
   da::MlaParams mp;
@@ -174,7 +198,7 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.num_splits = pl.num_splits;
   mp.write_final = pl.writes_final;
   const dim3 grid(pl.grid_x, 1, pl.grid_z);
-  cudaError_t e = da::launch_mla(ctx->kmap, ctx->vmap, mp, grid, stream);
+  cudaError_t e = da::launch_mla(ctx->qmap, ctx->qpemap, ctx->kmap, ctx->vmap, mp, grid, stream);
   if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
@@ -293,7 +317,8 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
     if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return DA_ERR_CUDA;
     if ((word & DA_DEVERR_TIMEOUT) && ctx && ctx->planned) {
       auto *ws = reinterpret_cast<uint8_t *>(workspace);
-      if (cudaMemsetAsync(ws + ctx->plan.counters_offset, 0, (size_t)ctx->plan.num_units * 4, s) !=
+      const size_t ncount = (size_t)ctx->plan.num_units * (ctx->prob.is_mla ? 2 : 1);
+      if (cudaMemsetAsync(ws + ctx->plan.counters_offset, 0, ncount * 4, s) !=
           cudaSuccess)
         return DA_ERR_CUDA;
     }

@@ -57,8 +57,8 @@ struct MlaParams {
   const __nv_bfloat16 *q_pe;    // [B][128][64]
   const int32_t *block_table;
   const int32_t *seq_lens;
-  float *o_part;                // [B][S][128][512]
-  float *lse_part;              // [B][S][128]
+  float *o_part;                // [B][S][128][512] (rank r writes columns 256r..256r+255)
+  float *lse_part;              // [B][S][2][128]   (one copy per rank)
   __nv_bfloat16 *out;           // [B][128][512]
   float *lse;
   uint32_t *err;
@@ -81,7 +81,9 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t mla_prepare(int device);
 int mla_smem_bytes();
 int mla_threads();
-cudaError_t launch_mla(const CUtensorMap &ckv_map, const CUtensorMap &kpe_map,
+int mla_max_splits();
+cudaError_t launch_mla(const CUtensorMap &qn_map, const CUtensorMap &qp_map,
+                       const CUtensorMap &ckv_map, const CUtensorMap &kpe_map,
                        const MlaParams &p, dim3 grid, cudaStream_t stream);
 
 // Planner (pure host code).

@@ -166,7 +166,9 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   const int64_t min_splits = ceil_div(max_len, max_chunk);
 
   const int cps = ctas_per_sm(p, smem_per_sm);
-  const int slots = num_sms * cps;
+  // an MLA split runs on a cluster of two CTAs: count cluster slots
+  const int slots = mla ? std::max(1, num_sms * cps / 2) : num_sms * cps;
+  const int max_splits = mla ? mla_max_splits() : kMaxSplits;
   int64_t chunk;
   if (num_splits_override > 0) {
     chunk = round_up(ceil_div(max_len, std::max<int64_t>(num_splits_override, min_splits)), align);
@@ -181,12 +183,12 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
     double best = 0.0;
     chunk = max_chunk;
     int64_t last_chunk = -1;
-    for (int64_t S = min_splits; S <= kMaxSplits; ++S) {
+    for (int64_t S = min_splits; S <= max_splits; ++S) {
       const int64_t c = std::min(round_up(ceil_div(max_len, S), align), max_chunk);
       if (c == last_chunk) continue;
       last_chunk = c;
       const int64_t splits = ceil_div(max_len, c);
-      if (splits > kMaxSplits) break;
+      if (splits > max_splits) break;
       if (splits > 1 && units * splits > max_ctas) break;
       const double t = makespan(unit_len, heads, c, splits, slots, sec_per_pos, merge_sec_per_split);
       if (last_chunk == c && (best == 0.0 || t < best * 0.999)) {
@@ -197,26 +199,26 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
     }
   }
   const int64_t splits = std::max<int64_t>(1, ceil_div(max_len, chunk));
-  if (splits > kMaxSplits) return DA_ERR_UNSUPPORTED;
+  if (splits > max_splits) return DA_ERR_UNSUPPORTED;
 
   info->kv_tile = tile;
   info->chunk_tokens = (int32_t)chunk;
   info->num_splits = (int32_t)splits;
   info->num_units = (int32_t)units;
   info->rows_per_unit = rows;
-  info->grid_x = (int32_t)splits;
+  info->grid_x = (int32_t)(mla ? 2 * splits : splits);  // MLA: a CTA pair per split
   info->grid_y = heads;
   info->grid_z = p->batch;
   info->ctas_per_sm = cps;
   info->writes_final = splits == 1 ? 1 : 0;
   int64_t off = kWorkspaceHeader;
   info->counters_offset = off;
-  off = align256(off + units * 4);
+  off = align256(off + units * (mla ? 2 : 1) * 4);
   if (!info->writes_final) {
     info->partial_o_offset = off;
     off = align256(off + units * splits * rows * (int64_t)dv * 4);
     info->partial_lse_offset = off;
-    off = align256(off + units * splits * rows * 4);
+    off = align256(off + units * splits * rows * (mla ? 2 : 1) * 4);
   }
   info->workspace_bytes = off;
   return DA_OK;

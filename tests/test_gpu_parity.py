@@ -246,3 +246,43 @@ def test_standalone_merge_matches_oracle_merge():
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.merge(o.double().numpy(), lse.double().numpy())
     assert_parity(out.cpu(), lo.cpu(), ref_o, ref_l, what="merge")
+
+
+# ------------------------------------------------------------------ MLA latent decode (cluster-pair tcgen05 kernel)
+
+@pytest.mark.parametrize("splits", [1, 2, 3])
+def test_mla_small(splits):
+    w = W.make_mla(name="mla", batch=4, seq_lens=[100, 64, 1000, 1], seed=40 + splits)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"MLA S={splits}")
+
+
+def test_mla_empty_row_and_auto_plan():
+    w = W.make_mla(name="mla0", batch=3, seq_lens=[0, 2500, 700], seed=45)
+    out, lse, flags, eng = run_gpu(w)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="MLA auto plan")
+    assert torch.all(out[0] == 0) and torch.all(lse[0] == -float("inf"))
+
+
+def test_mla_single_token_returns_the_latent_row_bitwise():
+    w = W.make_mla(name="mla1", batch=2, seq_lens=[1, 1], seed=46)
+    out, lse, _, _ = run_gpu(w, num_splits_override=1)
+    t = w.tensors
+    for b in range(2):
+        page = int(t["block_table"][b, 0])
+        row = t["k"][page, 0]
+        for h in range(128):
+            assert torch.equal(out[b, h].view(torch.int16), row.view(torch.int16))
+
+
+def test_mla_bad_page_sets_flag():
+    w = W.make_mla(name="mla2", batch=2, seq_lens=[300, 200], seed=47)
+    bt = w.tensors["block_table"].clone()
+    bt[0, 1] = -1
+    w.tensors["block_table"] = bt
+    out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+    assert flags & da.DA_DEVERR_PAGE_INDEX
+    assert torch.all(torch.isfinite(out.float()))
