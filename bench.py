@@ -47,6 +47,35 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "gqa_split_kernel": ["gqa_split.cu", "ptx.cuh", "internal.h"],
+    "mla_split_kernel": ["mla_split.cu", "ptx.cuh", "internal.h"],
+}
+
+
+def kernel_hash(kernel: str) -> str:
+    """Hash of the sources of a kernel: traffic figures are only valid for it."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "decode_attention_flash_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, cfg: int):
+    """DRAM read+write bytes per launch from the committed ncu summary, or None
+    when the kernel's sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"config{cfg}")
+    if not rec or rec.get("kernel") != kernel or rec.get("source_hash") != kernel_hash(kernel):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def algorithmic_bytes(w) -> dict:
     """The method's own bytes per call: kept KV + Q + O (+ LSE)."""
     t = w.tensors
@@ -308,6 +337,10 @@ def run_ours(args, w, cfg):
                "sample": f"batch rows 0..{len(rows) - 1} of {w.batch} ({frac:.3f} of the KV bytes), "
                          f"{dt:.1f} s wall"}
 
+    kname = "mla_split_kernel" if w.is_mla else "gqa_split_kernel"
+    if w.is_mla:
+        # MLA sits near the ridge: report the tensor side of its roofline too
+        tflops = ab["flops"] / (mean_split * 1e-3) / 1e12
     if rank == 0:
         clocks = clk.summary()
         line = {
@@ -324,15 +357,20 @@ def run_ours(args, w, cfg):
                        "algorithmic_bytes": ab["total"], "kv_bytes": ab["kv"],
                        "us_min": min(call_ms) * 1e3, "us_max": max(call_ms) * 1e3},
             "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": split_gbs / hbm_peak, "traffic": None,
-                         "kernel": "gqa_split_kernel" if not w.is_mla else "mla_split_kernel",
-                         "kernel_us": mean_split * 1e3},
+                         "frac": split_gbs / hbm_peak,
+                         "traffic": recorded_traffic(kname, cfg),
+                         "kernel": kname, "kernel_us": mean_split * 1e3,
+                         "peak_source": f"of {peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'fallback'})"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "us_per_call": mean_e2e * 1e3},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if w.is_mla:
+            line["roofline_tensor"] = {"bound": "tensor", "achieved": tflops, "peak": tf_peak,
+                                       "unit": "TFLOP/s", "frac": tflops / tf_peak,
+                                       "flops_per_launch": ab["flops"]}
         print(json.dumps(line), flush=True)
     eng.close()
 
