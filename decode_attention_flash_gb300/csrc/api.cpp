@@ -81,6 +81,36 @@ da_status encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t row_elem
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
+// A bf16 cache of rows of 128 elements as a 3-D tensor (64 elements, row, half)
+// with the half stride (128 B) below the row stride (256 B): one box copies
+// `box_rows` rows and lands as [half][row][64], 128B-swizzled.
+da_status encode_bf16_halves(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, rows, 2};
+  const cuuint64_t strides[2] = {256, 128};
+  const cuuint32_t box[3] = {64u, box_rows, 2u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+// Query map: [rows][128] bf16, unswizzled boxes of 128 elements x `box_rows` rows.
+da_status encode_q_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
 da_status check_workspace(const da_ctx *ctx, const void *ws, size_t bytes) {
   if (!ws || !aligned(ws, 256)) return DA_ERR_WORKSPACE;
   if ((int64_t)bytes < ctx->plan.workspace_bytes) return DA_ERR_WORKSPACE;
@@ -96,24 +126,32 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   if (paged && !a->block_table) return DA_ERR_INVALID_ARG;
   if (sparse && (!a->kv_num_blks || !a->kv_idx)) return DA_ERR_INVALID_ARG;
   if (fp8 && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
-  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 16) || !aligned(a->out, 4))
+  if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 128) || !aligned(a->out, 8))
     return DA_ERR_INVALID_ARG;
 
   const uint64_t rows = paged ? (uint64_t)p.num_pages * p.num_kv_heads * p.page_size
                               : (uint64_t)p.batch * p.num_kv_heads * p.max_seq_len;
   const uint32_t box_tokens = (uint32_t)da::gqa_box_tokens(p);
-  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+  if (ctx->map_k_base != a->k || ctx->map_v_base != a->v || ctx->map_q_base != a->q) {
+    ctx->map_k_base = ctx->map_v_base = ctx->map_q_base = nullptr;
     da_status st;
-    if ((st = encode_rows(&ctx->kmap, a->k, !fp8, fp8 ? rows : rows * 2,
-                          fp8 ? box_tokens : box_tokens * 2)) != DA_OK)
-      return st;
-    if ((st = encode_rows(&ctx->vmap, a->v, !fp8, fp8 ? rows : rows * 2,
-                          fp8 ? box_tokens : box_tokens * 2)) != DA_OK) {
-      ctx->map_k_base = nullptr;
-      return st;
+    if (fp8) {
+      // one 128-byte row per token
+      if ((st = encode_rows(&ctx->kmap, a->k, false, rows, box_tokens)) != DA_OK) return st;
+      if ((st = encode_rows(&ctx->vmap, a->v, false, rows, box_tokens)) != DA_OK) return st;
+    } else {
+      // rows of 128 bf16, viewed as (64 elements, row, half): a box of `box_tokens`
+      // rows lands half-major in shared memory
+      if ((st = encode_bf16_halves(&ctx->kmap, a->k, rows, box_tokens)) != DA_OK) return st;
+      if ((st = encode_bf16_halves(&ctx->vmap, a->v, rows, box_tokens)) != DA_OK) return st;
     }
+    if ((st = encode_q_rows(&ctx->qmap, a->q, (uint64_t)p.batch * p.num_q_heads, (uint32_t)G)) !=
+        DA_OK)
+      return st;
     ctx->map_k_base = a->k;
     ctx->map_v_base = a->v;
+    ctx->map_q_base = a->q;
   }
 
   const da_plan_info &pl = ctx->plan;
@@ -126,8 +164,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.kv_idx = a->kv_idx;
   gp.k_scale = a->k_scale;
   gp.v_scale = a->v_scale;
-  gp.o_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_o_offset);
-  gp.lse_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_lse_offset);
+  gp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);
+  gp.lse_part = reinterpret_cast<float *>(ws + pl.partial_lse_offset);
   gp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
   gp.lse = a->lse;
   gp.err = reinterpret_cast<uint32_t *>(ws);
@@ -145,11 +183,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.capacity = paged ? p.max_pages_per_seq * p.page_size : p.max_seq_len;
   gp.sparse_block_size = p.sparse_block_size;
   gp.max_sparse_blocks = p.max_sparse_blocks;
-  gp.chunk = pl.chunk_tokens;
-  gp.num_splits = pl.num_splits;
-  gp.write_final = pl.writes_final;
-  const dim3 grid(pl.grid_x, pl.grid_y, pl.grid_z);
-  if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, gp, grid, stream) != cudaSuccess)
+  if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap, gp, pl.grid_x, stream) !=
+      cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;
 }

@@ -1,31 +1,41 @@
-// gqa_split.cu -- split-KV GQA decode kernel for sm_103a.
+// gqa_split.cu -- persistent split-KV GQA decode kernel for sm_103a.
 //
-// One CTA per (split s, kv head h, batch row b). It owns the contiguous slice
-// of the row's valid positions [s*chunk, (s+1)*chunk) (block-sparse: that
-// slice of the row's compacted block list), loads the whole GQA group of G
-// query heads once (the row packing of the TorchInductor flex_decode.py.jinja
-// template, hq = h*G + g), streams K/V tiles of 64 tokens by TMA into a
-// multi-stage shared-memory ring guarded by mbarriers, and runs
+// What it computes: for every batch row b and query head hq = h*G + g (the
+// GQA row packing of the TorchInductor flex_decode.py.jinja template), the
+// softmax attention of q[b][hq] over the valid KV positions of kv head h --
+// contiguous, paged through a block table, or the listed blocks of a
+// block-sparse row (KV_NUM_BLKS / KV_IDX, indexed by kv head) -- with K/V in
+// bf16 or in e4m3 with a per-kv-head scale.
+//
+// How. Every (b, kv head) pair is a "unit" of ceil(len / 64) KV tiles. The
+// tiles of all units, laid end to end, are cut into gridDim.x equal ranges,
+// one per CTA (a persistent grid sized to the resident CTA slots): every CTA
+// streams the same number of 64-token tiles, wherever the unit boundaries
+// fall, so all SMs stay busy to the end. A CTA's range covers pieces
+// ("segments") of one or more units; a unit cut into several segments is the
+// split-KV decomposition of the flex-decode / split-K pages. The range is
+// computed on the device from seq_lens (and kv_num_blks), so the schedule
+// follows the lengths the kernel actually reads.
+//
+// Per CTA: warp 4 produces -- it walks the tiles, looks up page / block ids one
+// tile ahead, checks them, and streams K/V (and the segment's query group) by
+// TMA into a multi-stage shared-memory ring guarded by mbarriers -- and warps
+// 0-3 consume: each owns 16 tokens of every tile and runs
 //   S^T = K Q^T  and  O^T += V^T P^T
-// on the tensor cores (bf16 or, for e4m3 KV, f16 operands, fp32 accumulate).
-// The GQA group is the MMA's N dimension (8 per n-tile) and the tokens / the
-// head dimension are its M dimension, so no MMA rows are spent on padding the
-// 4-8 query heads up to 16.
+// on the tensor cores (mma.sync m16n8k16, bf16 or -- for e4m3 KV, decoded
+// exactly in registers -- f16 operands, fp32 accumulate). The GQA group is the
+// MMA's N dimension (8 per n-tile), so no MMA rows are spent padding 4-8 query
+// heads up to 16. The online softmax follows the exp2 form of the split-K
+// Triton kernel page (mslk splitk_kernels.py, `_fwd_kernel_splitK`), with
+// scale*log2(e) folded into the scores (flex's PRESCALE_QK idea) and guards
+// for fully masked rows.
 //
-// Online softmax follows the exp2 form of the split-K Triton kernel page
-// (mslk splitk_kernels.py, `_fwd_kernel_splitK`: m_new = max(m, rowmax),
-// alpha = 2^(m - m_new), p = 2^(s - m_new), l = alpha*l + sum p), with the
-// scale*log2(e) factor folded into the scores (the PRESCALE_QK idea of
-// flex_decode.py.jinja) and the guards for a fully masked row. Each of the
-// four consumer warps keeps its own running (m, l, acc) over its 16 tokens of
-// every tile; the warps are merged once at the end through shared memory.
-//
-// Split epilogue (`_fwd_kernel_splitK` "write back O"): O_part = acc / l (0
-// when l = 0) and lse = ln(l) + m*ln 2 (-inf when l = 0); a plan with a single
-// split writes the final bf16 output and LSE directly.
-//
-// Warp roles: warps 0-3 consume (16 tokens of each tile each), warp 4 lane 0
-// produces (page-table / sparse-list lookups, bounds checks, TMA issue).
+// Segment epilogue (`_fwd_kernel_splitK` "write back O"): the four warps'
+// (m, l, O) are merged in shared memory; a unit held by one segment writes
+// the final bf16 output and natural-log LSE, otherwise the segment writes its
+// normalised O and LSE to a partial slot and the last segment of the unit to
+// finish (an atomic counter, the multi-block merge of TensorRT-LLM
+// xqa/mha.cu) merges the unit's segments LSE-weighted (`_splitK_reduce`).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -36,227 +46,129 @@ constexpr int kTile = 64;             // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kD = 128;               // head dimension
-constexpr int kRedStride = kD + 4;    // padded row of the end-of-split reduction buffer
+constexpr int kRedStride = kD + 4;    // padded row of the epilogue reduction buffer
+constexpr uint32_t kConsumerBar = 1;  // named barrier of the 128 consumer threads
 
-template <bool FP8>
-struct Traits {
+template <bool FP8, int NT>
+struct Cfg {
   static constexpr int kBytesPerTok = FP8 ? kD : 2 * kD;
   static constexpr int kTileBytes = kTile * kBytesPerTok;  // one of K or V
-  static constexpr int kStages = FP8 ? 6 : 3;
-  static constexpr int kRingBytes = kStages * 2 * kTileBytes;
+  static constexpr int kStages = FP8 ? (NT == 1 ? 5 : 4) : (NT == 1 ? 3 : 2);
+  static constexpr int kQSlot = NT * 8 * kD * 2;             // the query group (bf16 rows)
+  // shared-memory layout (byte offsets from a 1024-aligned base)
+  static constexpr int oRing = 0;                            // [stage][K|V][tile]
+  static constexpr int oQ = oRing + kStages * 2 * kTileBytes;
+  static constexpr int oRed = oQ + kStages * kQSlot;          // [8*NT][kRedStride] fp32
+  static constexpr int oFull = oRed + 8 * NT * kRedStride * 4;
+  static constexpr int oEmpty = oFull + 8 * kStages;
+  static constexpr int oMeta = oEmpty + 8 * kStages;
+  static constexpr int oStats = oMeta + 24 * kStages;        // m, l per (warp, g)
+  static constexpr int oScan = oStats + 2 * kConsumerWarps * 16 * 4;
+  static constexpr int oFlags = oScan + 16 * 4;              // 16 ints (see the kernel)
+  static constexpr int oMergeBar = oFlags + 16 * 4;          // 2 mbarriers of the merge staging
+  static constexpr int kTotal = oMergeBar + 16 + 1024;       // + alignment slack
 };
 
+// What the producer tells the consumers about the tile in a stage.
 struct __align__(8) StageMeta {
-  uint64_t valid;  // bit j: token j of the tile is a valid position
+  uint64_t valid;   // bit t: token t of the tile is a valid position
+  int32_t unit;     // b * HKV + h
+  int32_t flags;    // kFirst: first tile of a segment (query group in the stage); kLast
+  int32_t c_first;  // first CTA holding a segment of this unit
+  int32_t n_seg;    // segments of this unit
 };
-
-template <bool FP8>
-struct Smem {
-  // ring: stage s holds K at [s][0] and V at [s][1], each kTileBytes, 1024-aligned
-  static constexpr int kRing = 0;
-  static constexpr int kFull = Traits<FP8>::kRingBytes;
-  static constexpr int kEmpty = kFull + 8 * Traits<FP8>::kStages;
-  static constexpr int kMeta = kEmpty + 8 * Traits<FP8>::kStages;
-  static constexpr int kFlags = kMeta + 8 * Traits<FP8>::kStages;  // abort, last-CTA
-  static constexpr int kStats = kFlags + 16;              // m, l per (warp, g): 2*4*16 floats
-  static constexpr int kIds = kStats + 2 * kConsumerWarps * 16 * 4;  // page / block ids
-  static constexpr int kTotal = kIds + kGqaMaxIds * 4 + 1024;        // + align slack
-};
+constexpr int32_t kFirst = 1, kLast = 2;
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
-// ------------------------------------------------------------------ producer
+__device__ __forceinline__ uint64_t low_bits(int n) {
+  return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+}
 
-// Fills tile `i` of this CTA into stage `st`: takes the pages / sparse block
-// from the ids staged in shared memory (already range-checked; -1 marks an
-// invalid one, which is skipped), records which tokens are valid and issues
-// the TMA boxes.
-template <bool FP8>
-__device__ __forceinline__ void produce_tile(const GqaParams &p, const CUtensorMap *kmap,
-                                             const CUtensorMap *vmap, uint8_t *ring,
-                                             uint64_t *full, StageMeta *meta, const int *ids,
-                                             int st, int i, int b, int h, int n_valid,
-                                             int range_lo, int range_hi, uint64_t policy) {
-  using T = Traits<FP8>;
-  uint8_t *kdst = ring + (size_t)st * 2 * T::kTileBytes;
-  uint8_t *vdst = kdst + T::kTileBytes;
-  const int row_mult = FP8 ? 1 : 2;  // bf16 rows are split into two 128-byte TMA rows
-  uint64_t valid = 0;
-  int64_t row0 = -1;  // first cache row of a single-box tile
+// ------------------------------------------------------------------ units and the schedule
 
+struct UnitInfo {
+  int b, h, n_valid, tiles;
+};
+
+// Length (checked against the cache) and tile count of unit u.
+__device__ __forceinline__ UnitInfo unit_info(const GqaParams &p, int u, uint32_t &err) {
+  UnitInfo x;
+  x.b = u / p.num_kv_heads;
+  x.h = u - x.b * p.num_kv_heads;
+  int n = p.seq_lens[x.b];
+  if (n < 0 || n > p.capacity) {
+    err |= DA_DEVERR_SEQ_LEN;
+    n = n < 0 ? 0 : p.capacity;
+  }
+  x.n_valid = n;
   if (p.sparse_block_size > 0) {
-    const int tiles_per_block = p.sparse_block_size / kTile;
-    const int blk = ids[i / tiles_per_block];
-    if (blk >= 0) {
-      const int tok_base = blk * p.sparse_block_size + (i % tiles_per_block) * kTile;
-      int lim = min(n_valid - tok_base, kTile);
-      lim = min(lim, p.cache_len - tok_base);
-      if (lim > 0) {
-        valid = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
-        row0 = ((int64_t)b * p.num_kv_heads + h) * p.cache_len + tok_base;
-      }
+    int nb = p.kv_num_blks[u];
+    if (nb < 0 || nb > p.max_sparse_blocks) {
+      err |= DA_DEVERR_SPARSE_INDEX;
+      nb = nb < 0 ? 0 : p.max_sparse_blocks;
     }
+    x.tiles = nb * (p.sparse_block_size / kTile);
   } else {
-    const int tok_base = range_lo + i * kTile;
-    const int lim = min(range_hi - tok_base, kTile);
-    if (!p.paged) {
-      if (lim > 0) {
-        valid = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
-        row0 = ((int64_t)b * p.num_kv_heads + h) * p.cache_len + tok_base;
-      }
-    } else if (p.page_size >= kTile) {
-      const int page = ids[tok_base / p.page_size - range_lo / p.page_size];
-      if (page >= 0 && lim > 0) {
-        valid = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
-        row0 = ((int64_t)page * p.num_kv_heads + h) * p.page_size + tok_base % p.page_size;
-      }
-    } else {
-      // several pages per tile: one box per page
-      const int P = p.page_size;
-      const int first = tok_base / P - range_lo / P;
-      int nbox = 0;
-      for (int j = 0; j < kTile / P; ++j) {
-        const int t0 = tok_base + j * P;
-        if (t0 >= range_hi) break;
-        if (ids[first + j] < 0) continue;
-        const int cnt = min(range_hi - t0, P);
-        valid |= ((cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull)) << (j * P));
-        ++nbox;
-      }
-      meta[st].valid = valid;
-      // the transaction count is set before any copy is issued
-      mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)(nbox * P * T::kBytesPerTok));
-      for (int j = 0; j < kTile / P; ++j) {
-        if (tok_base + j * P >= range_hi) break;
-        const int page = ids[first + j];
-        if (page < 0) continue;
-        const int y = (int)(((int64_t)page * p.num_kv_heads + h) * P * row_mult);
-        const int off = j * P * T::kBytesPerTok;
-        tma_load_2d(kdst + off, kmap, &full[st], 0, y, policy);
-        tma_load_2d(vdst + off, vmap, &full[st], 0, y, policy);
-      }
-      return;
-    }
+    x.tiles = (n + kTile - 1) / kTile;
   }
-  meta[st].valid = valid;
-  if (row0 >= 0) {
-    const int y = (int)(row0 * row_mult);
-    mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)T::kTileBytes);
-    tma_load_2d(kdst, kmap, &full[st], 0, y, policy);
-    tma_load_2d(vdst, vmap, &full[st], 0, y, policy);
-  } else {
-    mbar_arrive_expect_tx(&full[st], 0);
-  }
+  return x;
 }
 
-// Stages the page ids (paged) or listed block ids (sparse) of this CTA's range
-// into shared memory with the producer warp's 32 lanes, checking every one:
-// an id outside the pool / cache becomes -1 and sets an error bit.
-__device__ __forceinline__ uint32_t stage_ids(const GqaParams &p, int *ids, int b, int h,
-                                              int range_lo, int range_hi, int lane) {
-  uint32_t err = 0;
-  if (p.sparse_block_size > 0) {
-    const int32_t *list = p.kv_idx + ((int64_t)b * p.num_kv_heads + h) * p.max_sparse_blocks;
-    for (int j = lane; j < range_hi - range_lo; j += 32) {
-      int blk = list[range_lo + j];
-      if (blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len) {
-        err |= DA_DEVERR_SPARSE_INDEX;
-        blk = -1;
-      }
-      ids[j] = blk;
-    }
-  } else if (p.paged) {
-    const int first = range_lo / p.page_size;
-    const int count = (range_hi - 1) / p.page_size - first + 1;
-    const int32_t *row = p.block_table + (int64_t)b * p.max_pages + first;
-    for (int j = lane; j < count; j += 32) {
-      int page = row[j];
-      if (page < 0 || page >= p.num_pages) {
-        err |= DA_DEVERR_PAGE_INDEX;
-        page = -1;
-      }
-      ids[j] = page;
-    }
-  }
-  return err;
+// CTA whose tile range [floor(c*T/C), floor((c+1)*T/C)) contains global tile t.
+__device__ __forceinline__ int cta_of(int64_t t, int64_t T, int C) {
+  return (int)(((t + 1) * C - 1) / T);
 }
 
-// The last CTA of a (b, kv head) unit to finish merges the unit's per-split
-// results (LSE-weighted, as `_splitK_reduce` of splitk_kernels.py) into the
-// final bf16 output and LSE -- the multi-block merge of TensorRT-LLM
-// xqa/mha.cu, found with an atomic counter per unit and no spinning wait. The
-// counter is reset by the merging CTA, so it is zero again for the next call.
-__device__ __forceinline__ void merge_if_last(const GqaParams &p, int b, int h, int G,
-                                              float *scratch, volatile int *last_flag) {
-  const int64_t unit = (int64_t)b * p.num_kv_heads + h;
-  const int S = p.num_splits;
-  __threadfence();  // this CTA's partial results are visible before the count
+// Inclusive scan over the block's threads; returns the block total in *total.
+__device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(p.counters + unit, 1u);
-    *last_flag = (prev == (unsigned)(S - 1)) ? 1 : 0;
+  int before = 0, sum = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int t = scratch[w];
+    if (w < warp) before += t;
+    sum += t;
   }
   __syncthreads();
-  if (!*last_flag) return;
-  __threadfence();
-  float *w = scratch;           // [S][16] weights (lse first)
-  float *stat = w + S * 16;     // [16] 1/sum, [16] lse
-  const float *lse_part = p.lse_part + unit * S * G;
-  for (int i = threadIdx.x; i < S * G; i += blockDim.x)
-    w[(i / G) * 16 + (i % G)] = __ldcg(lse_part + i);
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    float M = neg_inf();
-    for (int s = 0; s < S; ++s) M = fmaxf(M, w[s * 16 + g]);
-    float sum = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float l = w[s * 16 + g];
-      const float e = (M == neg_inf() || l == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
-      w[s * 16 + g] = e;
-      sum += e;
-    }
-    stat[g] = sum > 0.f ? 1.f / sum : 0.f;
-    stat[16 + g] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
-  }
-  __syncthreads();
-  const float4 *o_part = reinterpret_cast<const float4 *>(p.o_part + unit * S * G * kD);
-  for (int i = threadIdx.x; i < G * (kD / 4); i += blockDim.x) {
-    const int g = i / (kD / 4), c = i % (kD / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < S; ++s) {
-      const float e = w[s * 16 + g];
-      if (e != 0.f) {
-        const float4 v = __ldcg(o_part + ((int64_t)s * G + g) * (kD / 4) + c);
-        acc.x += e * v.x;
-        acc.y += e * v.y;
-        acc.z += e * v.z;
-        acc.w += e * v.w;
-      }
-    }
-    const float inv = stat[g];
-    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
-        p.out + ((int64_t)b * p.num_q_heads + h * G + g) * kD + 4 * c);
-    dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  }
-  if (threadIdx.x < G && p.lse) p.lse[(int64_t)b * p.num_q_heads + h * G + threadIdx.x] = stat[16 + threadIdx.x];
-  if (threadIdx.x == 0) p.counters[unit] = 0u;
+  *total = sum;
+  return v + before;
 }
+
+struct TileDesc {
+  int unit, b, h, n_valid, j, tiles;  // unit, its row / head, length, tile index, tile count
+  int64_t P;                          // global index of the unit's first tile
+  int c_first, n_seg;                 // CTAs holding the unit's segments
+};
 
 // ------------------------------------------------------------------ consumer helpers
 
-// Address of the 16-byte chunk `c` (0..15 for bf16 rows of 256 bytes, 0..7 for
-// fp8 rows of 128 bytes) of token `t` in a 128B-swizzled tile.
+// Byte offset of token t inside a K or V tile of shared memory. A tile is
+// filled by boxes of `br` tokens (one page, or the whole 64-token tile). fp8:
+// one 128-byte row per token. bf16: each box holds its rows' two 64-element
+// halves in two regions of `br` 128-byte rows ([box][half][row]), so eight
+// consecutive tokens of one 16-byte chunk fall on eight different swizzle
+// phases (no bank conflicts); the half stride is br * 128 bytes.
 template <bool FP8>
-__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int t, int c) {
-  if (FP8) {
-    return base + t * 128 + (((c ^ t) & 7) << 4);
-  } else {
-    const int r = 2 * t + (c >> 3);
-    return base + r * 128 + ((((c & 7) ^ r) & 7) << 4);
-  }
+__device__ __forceinline__ uint32_t token_offset(int t, int br_shift) {
+  if (FP8) return (uint32_t)t * 128;
+  const int br = 1 << br_shift;
+  return (uint32_t)((t >> br_shift) * (2 * br * 128) + (t & (br - 1)) * 128);
+}
+
+// Address of 16-byte chunk c (bf16: 0..15, fp8: 0..7) of the token at
+// `tok_off` (token t) in the 128B-swizzled tile at `base`.
+template <bool FP8>
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, uint32_t tok_off, int t, int c,
+                                               int br_shift) {
+  if (FP8) return base + tok_off + (((c ^ t) & 7) << 4);
+  return base + tok_off + (uint32_t)(c >> 3) * (128u << br_shift) + ((((c & 7) ^ t) & 7) << 4);
 }
 
 __device__ __forceinline__ uint32_t lo16_mask(bool a, bool b) {
@@ -269,204 +181,534 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
   return pack_f16(f.x, f.y);
 }
 
+// Merge of one unit's segments (slots unit + c_first .. unit + c_first + n_seg
+// - 1) into the final output, run by the CTA that finished the unit's last
+// segment once its own range is done (so its K/V ring is free). The partial O
+// blocks are staged into the two halves of the ring by bulk copies, each half
+// refilled while the other is summed, and the first copies start before the
+// LSEs are read; the weighted sum goes into shared-memory accumulators. The
+// loops are kept compact on purpose: this code runs once per unit, so its
+// instructions are usually not cached when it starts. Returns false if a
+// staging wait gave up.
+__device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_first, int n_seg,
+                                        int G, uint8_t *stage, int stage_bytes, float *buf,
+                                        int cap, float *acc, uint64_t *bars, uint32_t *phase) {
+  const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
+  const int tid = threadIdx.x;  // 0..127 (consumer threads)
+  const int nthr = kConsumerWarps * 32;
+  const int blk = G * kD * 4;                // bytes of one segment's partial O
+  float *stat = buf;                         // [16] max, [16] sum of weights
+  float *w = buf + 32;                       // LSE, then weights, [s][g]
+  const int wcap = cap - 32;
+  const int half = stage_bytes / 2;
+  const int seg_chunk = max(1, half / blk);  // segments per staging half
+  const int nchunks = (n_seg + seg_chunk - 1) / seg_chunk;
+  const bool all_lse = n_seg * G <= wcap;    // every LSE fits at once (the usual case)
+  const float *lse_base = p.lse_part + ((int64_t)unit + c_first) * G;
+  const float *o_base = p.o_part + ((int64_t)unit + c_first) * G * kD;
+
+  auto issue = [&](int k) {  // chunk k -> half k & 1, completion on bars[k & 1]
+    // the unit's slots are consecutive: one copy per chunk
+    const int s0 = k * seg_chunk, ns = min(seg_chunk, n_seg - s0);
+    mbar_arrive_expect_tx(&bars[k & 1], (uint32_t)(ns * blk));
+    bulk_copy_g2s(stage + (k & 1) * half, o_base + (int64_t)s0 * G * kD, (uint32_t)(ns * blk),
+                  &bars[k & 1]);
+  };
+  if (tid == 0) {
+    fence_proxy_async_shared();  // earlier reads of the ring before the copies
+    fence_proxy_async_global();  // the partials other CTAs wrote, for the copies
+    issue(0);
+  }
+  for (int e = tid; e < G * kD; e += nthr) acc[e] = 0.f;
+  // ---- LSEs: maximum, weights and their sum per head
+  if (tid < 16) {
+    stat[tid] = neg_inf();
+    stat[16 + tid] = 0.f;
+  }
+  named_barrier_sync(kConsumerBar, nthr);
+  const int lchunk = all_lse ? n_seg : max(1, wcap / G);
+#pragma unroll 1
+  for (int pass = 0; pass < (all_lse ? 1 : 2); ++pass) {
+#pragma unroll 1
+    for (int s0 = 0; s0 < n_seg; s0 += lchunk) {
+      const int ns = min(lchunk, n_seg - s0);
+#pragma unroll 1
+      for (int i = tid; i < ns * G; i += nthr) w[i] = __ldcg(lse_base + (int64_t)s0 * G + i);
+      named_barrier_sync(kConsumerBar, nthr);
+      if (tid < 32) {  // warp 0: lane = (segment group, head); groups of 32/Gp lanes per head
+        const int Gp = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 16)));
+        const int g = tid & (Gp - 1), lanes = 32 / Gp;
+        float M = neg_inf();
+        if (g < G)
+#pragma unroll 1
+          for (int s = tid / Gp; s < ns; s += lanes) M = fmaxf(M, w[s * G + g]);
+        for (int o = Gp; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if (tid < G) stat[tid] = fmaxf(stat[tid], M);
+      }
+      named_barrier_sync(kConsumerBar, nthr);
+    }
+  }
+  if (all_lse) {  // turn the LSEs (still in w) into weights
+#pragma unroll 1
+    for (int i = tid; i < n_seg * G; i += nthr) {
+      const float l = w[i], Mg = stat[i % G];
+      w[i] = (l == neg_inf() || Mg == neg_inf()) ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
+    }
+    named_barrier_sync(kConsumerBar, nthr);
+    if (tid < 32) {
+      const int Gp = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : (G <= 8 ? 8 : 16)));
+      const int g = tid & (Gp - 1), lanes = 32 / Gp;
+      float sum = 0.f;
+      if (g < G)
+#pragma unroll 1
+        for (int s = tid / Gp; s < n_seg; s += lanes) sum += w[s * G + g];
+      for (int o = Gp; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (tid < G) stat[16 + tid] = sum;
+    }
+  }
+  // ---- weighted sum of the staged partial O blocks, two halves in flight
+  bool ok = true;
+#pragma unroll 1
+  for (int k = 0; k < nchunks; ++k) {
+    const int s0 = k * seg_chunk, ns = min(seg_chunk, n_seg - s0);
+    if (tid == 0 && k + 1 < nchunks) issue(k + 1);  // its half was freed by chunk k - 1
+    float *wk = w + (all_lse ? s0 * G : 0);
+    if (!all_lse) {  // weights of this chunk only (the rare long case)
+#pragma unroll 1
+      for (int i = tid; i < ns * G; i += nthr) {
+        const float l = __ldcg(lse_base + (int64_t)s0 * G + i), Mg = stat[i % G];
+        w[i] = (l == neg_inf() || Mg == neg_inf()) ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
+      }
+      named_barrier_sync(kConsumerBar, nthr);
+      if (tid < G) {
+        float sum = stat[16 + tid];
+#pragma unroll 1
+        for (int s = 0; s < ns; ++s) sum += w[s * G + tid];
+        stat[16 + tid] = sum;
+      }
+    }
+    if (!mbar_wait_bounded(&bars[k & 1], phase[k & 1], kWaitLimitNs)) ok = false;
+    phase[k & 1] ^= 1u;
+    const float *sf = reinterpret_cast<const float *>(stage + (k & 1) * half);
+    // four independent accumulation chains per thread (G * kD is a multiple of 4 * nthr)
+#pragma unroll 1
+    for (int e0 = tid; e0 < G * kD; e0 += 4 * nthr) {
+      float a[4];
+      int gi[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q * nthr;
+        gi[q] = e < G * kD ? e / kD : 0;
+        a[q] = e < G * kD ? acc[e] : 0.f;
+      }
+#pragma unroll 2
+      for (int s = 0; s < ns; ++s) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = e0 + q * nthr;
+          if (e < G * kD) a[q] += wk[s * G + gi[q]] * sf[(size_t)s * G * kD + e];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = e0 + q * nthr;
+        if (e < G * kD) acc[e] = a[q];
+      }
+    }
+    named_barrier_sync(kConsumerBar, nthr);
+  }
+  // ---- output rows b, h*G .. h*G+G-1 are contiguous
+  __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
+#pragma unroll 1
+  for (int e = tid; e < G * kD; e += nthr) {
+    const float sum = stat[16 + e / kD];
+    out[e] = __float2bfloat16(sum > 0.f ? acc[e] / sum : 0.f);
+  }
+  if (tid < G && p.lse) {
+    const float sum = stat[16 + tid];
+    p.lse[(int64_t)b * p.num_q_heads + h * G + tid] =
+        sum > 0.f ? stat[tid] + __log2f(sum) * 0.69314718055994531f : neg_inf();
+  }
+  if (tid == 0) p.counters[unit] = 0u;  // ready for the next call
+  named_barrier_sync(kConsumerBar, nthr);
+  return ok;
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <bool FP8, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, const GqaParams p) {
-  using T = Traits<FP8>;
-  using S = Smem<FP8>;
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap, const GqaParams p) {
+  using C = Cfg<FP8, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem + S::kRing;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kFull);
-  uint64_t *empty = reinterpret_cast<uint64_t *>(smem + S::kEmpty);
-  StageMeta *meta = reinterpret_cast<StageMeta *>(smem + S::kMeta);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlags);
-  volatile int *last_flag = abort_flag + 1;
-  int *ids = reinterpret_cast<int *>(smem + S::kIds);
-  float *stat_m = reinterpret_cast<float *>(smem + S::kStats);
+  uint8_t *ring = smem + C::oRing;
+  uint8_t *qslots = smem + C::oQ;
+  float *red = reinterpret_cast<float *>(smem + C::oRed);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oFull);
+  uint64_t *empty = reinterpret_cast<uint64_t *>(smem + C::oEmpty);
+  StageMeta *meta = reinterpret_cast<StageMeta *>(smem + C::oMeta);
+  float *stat_m = reinterpret_cast<float *>(smem + C::oStats);
   float *stat_l = stat_m + kConsumerWarps * 16;
+  int *scan = reinterpret_cast<int *>(smem + C::oScan);
+  volatile int *flags = reinterpret_cast<volatile int *>(smem + C::oFlags);
+  // flags: [0] abort, [2] start unit, [3] start tile, [4..5] start P (int64),
+  //        [6..11] up to two merges owed (unit, c_first, n_seg), [12] their count
+  uint64_t *merge_bar = reinterpret_cast<uint64_t *>(smem + C::oMergeBar);
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-
-  // ---- this CTA's slice of the row
-  int n_valid = p.seq_lens[b];
+  const int U = p.batch * p.num_kv_heads;
+  const int cta = blockIdx.x;
   uint32_t dev_err = 0;
-  if (n_valid < 0 || n_valid > p.capacity) {
-    dev_err |= DA_DEVERR_SEQ_LEN;
-    n_valid = n_valid < 0 ? 0 : p.capacity;
-  }
-  int range_lo, range_hi, num_tiles;
-  if (p.sparse_block_size > 0) {
-    int nblk = p.kv_num_blks[(int64_t)b * p.num_kv_heads + h];
-    if (nblk < 0 || nblk > p.max_sparse_blocks) {
-      dev_err |= DA_DEVERR_SPARSE_INDEX;
-      nblk = nblk < 0 ? 0 : p.max_sparse_blocks;
-    }
-    const int per_split = p.chunk / p.sparse_block_size;  // list entries per split
-    range_lo = split * per_split;
-    range_hi = min(range_lo + per_split, nblk);
-    num_tiles = range_hi > range_lo ? (range_hi - range_lo) * (p.sparse_block_size / kTile) : 0;
-  } else {
-    range_lo = split * p.chunk;
-    range_hi = min(range_lo + p.chunk, n_valid);
-    num_tiles = range_hi > range_lo ? (range_hi - range_lo + kTile - 1) / kTile : 0;
-  }
 
-  const int64_t unit = (int64_t)b * p.num_kv_heads + h;
-  const int64_t slot = unit * p.num_splits + split;
-
-  if (num_tiles == 0) {
-    // empty split: O = 0, LSE = -inf (its O slot is never read by the merge)
-    if (threadIdx.x == 0 && dev_err) atomicOr(p.err, dev_err);
-    if (threadIdx.x < G) {
-      if (p.write_final) {
-        const int64_t row = (int64_t)b * p.num_q_heads + h * G + threadIdx.x;
-        if (p.lse) p.lse[row] = neg_inf();
-      } else {
-        p.lse_part[slot * G + threadIdx.x] = neg_inf();
+  // ---- the schedule: this CTA's range of the global tile sequence
+  int local = 0;
+  for (int u = threadIdx.x; u < U; u += kThreads) local += unit_info(p, u, dev_err).tiles;
+  int T32 = 0;
+  block_inclusive_scan(local, scan, &T32);
+  const int64_t T = T32;
+  // Never more ranges than tiles, so every working CTA holds at least one tile
+  // and a unit's segments come from consecutive CTAs c_first..c_last.
+  const int CTAS = (int)(T < (int64_t)gridDim.x ? T : (int64_t)gridDim.x);
+  const int64_t lo = cta < CTAS ? (int64_t)cta * T / CTAS : 0;
+  const int64_t hi = cta < CTAS ? (int64_t)(cta + 1) * T / CTAS : 0;
+  const int owner_of_tail = CTAS > 0 ? CTAS - 1 : 0;  // writes empty units past the last tile
+  if (threadIdx.x == 0) {
+    flags[0] = 0;
+    flags[2] = -1;
+    flags[12] = 0;
+  }
+  {
+    int64_t base = 0;
+    for (int u0 = 0; u0 < U; u0 += kThreads) {
+      const int u = u0 + threadIdx.x;
+      UnitInfo x{};
+      if (u < U) x = unit_info(p, u, dev_err);
+      const int t_u = u < U ? x.tiles : 0;
+      int total = 0;
+      const int incl = block_inclusive_scan(t_u, scan, &total);
+      const int64_t Pu = base + incl - t_u;
+      if (u < U) {
+        if (t_u > 0 && Pu <= lo && lo < Pu + t_u) {
+          flags[2] = u;
+          flags[3] = (int)(lo - Pu);
+          *reinterpret_cast<volatile int64_t *>(flags + 4) = Pu;
+        }
+        // a unit without tiles is written here by the CTA whose range holds its start
+        if (t_u == 0 && ((Pu >= lo && Pu < hi) || (Pu >= T && cta == owner_of_tail))) {
+          const int64_t row0 = (int64_t)x.b * p.num_q_heads + x.h * G;
+          for (int e = 0; e < G * kD; ++e) p.out[row0 * kD + e] = __float2bfloat16(0.f);
+          if (p.lse)
+            for (int g = 0; g < G; ++g) p.lse[row0 + g] = neg_inf();
+        }
       }
+      base += total;
     }
-    if (p.write_final) {
-      for (int e = threadIdx.x; e < G * kD; e += blockDim.x)
-        p.out[((int64_t)b * p.num_q_heads + h * G) * kD + e] = __float2bfloat16(0.f);
-      return;
-    }
-    merge_if_last(p, b, h, G, reinterpret_cast<float *>(ring), last_flag);
+  }
+  const int ntiles = (int)(hi - lo);
+  if (ntiles <= 0) {
+    if (dev_err) atomicOr(p.err, dev_err);
     return;
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < T::kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    *abort_flag = 0;
+    mbar_init(&merge_bar[0], 1);
+    mbar_init(&merge_bar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
-
-  // consumer state (per thread): O^T accumulators and the running softmax state
-  float oacc[NT][8][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) oacc[nt][mt][e] = 0.f;
-  float m_run[NT][2], l_part[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = neg_inf();
-    l_part[nt][0] = l_part[nt][1] = 0.f;
-  }
+  const int start_u = flags[2], start_j = flags[3];
+  const int64_t start_P = *reinterpret_cast<volatile int64_t *>(flags + 4);
 
   if (warp == kConsumerWarps) {
-    // ================= producer =================
-    dev_err |= stage_ids(p, ids, b, h, range_lo, range_hi, lane);
-    __syncwarp();
+    // ======================================================= producer
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      const uint64_t policy = l2_policy_evict_first();
-      for (int i = 0; i < num_tiles; ++i) {
-        const int st = i % T::kStages;
-        if (i >= T::kStages) {
-          const uint32_t par = ((i / T::kStages) & 1) ^ 1;
-          if (!mbar_wait_bounded(&empty[st], par, kWaitLimitNs)) {
-            dev_err |= DA_DEVERR_TIMEOUT;
-            *abort_flag = 1;
-            break;
-          }
+      tma_prefetch_desc(&qmap);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    const uint64_t q_policy = l2_policy_evict_last();
+    const int P = p.page_size;
+    const int pages_per_tile = p.paged ? (P >= kTile ? 1 : kTile / P) : 1;
+
+    // walker over (unit, tile) starting at this CTA's first tile
+    TileDesc cur;
+    {
+      UnitInfo x = unit_info(p, start_u, dev_err);
+      cur.unit = start_u;
+      cur.b = x.b;
+      cur.h = x.h;
+      cur.n_valid = x.n_valid;
+      cur.tiles = x.tiles;
+      cur.j = start_j;
+      cur.P = start_P;
+      cur.c_first = cta_of(cur.P, T, CTAS);
+      cur.n_seg = cta_of(cur.P + cur.tiles - 1, T, CTAS) - cur.c_first + 1;
+    }
+    // Page (paged) or block (sparse) id number k of a tile; -1 when absent or
+    // invalid (an invalid one also sets its error bit and is skipped).
+    auto load_id = [&](const TileDesc &d, int k) -> int {
+      if (p.sparse_block_size > 0) {
+        const int e = d.j / (p.sparse_block_size / kTile);
+        const int blk = p.kv_idx[(int64_t)d.unit * p.max_sparse_blocks + e];
+        if (blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len) {
+          dev_err |= DA_DEVERR_SPARSE_INDEX;
+          return -1;
         }
-        produce_tile<FP8>(p, &kmap, &vmap, ring, full, meta, ids, st, i, b, h, n_valid,
-                          range_lo, range_hi, policy);
+        return blk;
+      }
+      const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
+      if (tok0 >= d.n_valid) return -1;
+      const int page = p.block_table[(int64_t)d.b * p.max_pages + tok0 / P];
+      if (page < 0 || page >= p.num_pages) {
+        dev_err |= DA_DEVERR_PAGE_INDEX;
+        return -1;
+      }
+      return page;
+    };
+    auto advance = [&](TileDesc &d) {
+      if (++d.j < d.tiles) return;
+      d.P += d.tiles;
+      int u = d.unit;
+      UnitInfo x;
+      do {  // units without tiles were written in the prologue
+        ++u;
+        x = unit_info(p, u < U ? u : U - 1, dev_err);
+      } while (u < U && x.tiles == 0);
+      d.unit = u;
+      d.b = x.b;
+      d.h = x.h;
+      d.n_valid = x.n_valid;
+      d.tiles = x.tiles;
+      d.j = 0;
+      d.c_first = cta_of(d.P, T, CTAS);
+      d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;
+    };
+
+    // Ids are looked up kAhead tiles before they are used, in a queue that
+    // lives in the warp's lanes: lanes k*L .. k*L+L-1 hold the L ids of the
+    // k-th next tile (L ids per tile: pages of a tile, or one block / page).
+    const bool needs_ids = p.paged || p.sparse_block_size > 0;
+    const int L = pages_per_tile;
+    const int ahead_n = min(8, 32 / L);  // tiles in flight in the queue
+    int idq = -1;
+    TileDesc ahead = cur;
+    if (needs_ids) {
+      for (int k = 0; k < ahead_n && k < ntiles; ++k) {
+        if (lane >= k * L && lane < (k + 1) * L) idq = load_id(ahead, lane - k * L);
+        if (k + 1 < ntiles) advance(ahead);
       }
     }
-  } else {
-    // ================= consumers =================
-    const int q4 = lane & 3;      // quad index: owns g = nt*8 + 2*q4 + {0,1}
-    const int r8 = lane >> 2;     // row inside an 8-row group
-    // Q^T as the B operand (k = head dim, n = query head of the group)
-    uint32_t qf[NT][8][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + r8;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          p.q + ((int64_t)b * p.num_q_heads + h * G + (g < G ? g : 0)) * kD);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (!FP8) {
-          // b0: d = 16ks + 2q4 (+1), b1: d = 16ks + 8 + 2q4 (+1)
-          qf[nt][ks][0] = g < G ? qrow[(16 * ks + 2 * q4) / 2] : 0u;
-          qf[nt][ks][1] = g < G ? qrow[(16 * ks + 8 + 2 * q4) / 2] : 0u;
-        } else {
-          // k-step ks = 2pp + e covers bytes 32pp + 16e + 4q4 .. +3 of each key row:
-          // logical k (2q4, 2q4+1) -> d +0,+1 ; (2q4+8, 2q4+9) -> d +2,+3
-          const int pp = ks >> 1, e = ks & 1;
-          const int d0 = 32 * pp + 16 * e + 4 * q4;
-          qf[nt][ks][0] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2]) : 0u;
-          qf[nt][ks][1] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2 + 1]) : 0u;
-        }
-      }
-    }
-    float sscale = p.score_scale;
-    if (FP8) sscale *= p.k_scale[h];
-
-
-    const int tok_lane = 16 * warp + (lane & 7);  // ldmatrix row supplied by this lane
-    const int mi = lane >> 3;                      // which 8x8 matrix this lane addresses
-
-    for (int i = 0; i < num_tiles; ++i) {
-      const int st = i % T::kStages;
-      const uint32_t par = (i / T::kStages) & 1;
-      if (!mbar_wait_bounded(&full[st], par, kWaitLimitNs)) {
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % C::kStages;
+      bool ok = true;
+      if (lane == 0 && i >= C::kStages)
+        ok = mbar_wait_bounded(&empty[st], ((i / C::kStages) & 1) ^ 1, kWaitLimitNs);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
         dev_err |= DA_DEVERR_TIMEOUT;
-        *abort_flag = 1;
+        if (lane == 0) flags[0] = 1;
         break;
       }
-      const uint32_t vbits = (uint32_t)(meta[st].valid >> (16 * warp)) & 0xFFFFu;
+      const int id_cur = idq;  // lanes 0 .. L-1: this tile's ids
+      // ---- this tile's boxes (y = first cache row of the box)
+      uint64_t valid = 0;
+      int nbox = 0;
+      int ys[kTile / 16];
+      const int tok_base = cur.j * kTile;
+      if (p.sparse_block_size > 0) {
+        const int blk = __shfl_sync(0xffffffffu, id_cur, 0);
+        if (blk >= 0) {
+          const int tb = blk * p.sparse_block_size + (cur.j % (p.sparse_block_size / kTile)) * kTile;
+          const int lim = min(min(cur.n_valid - tb, kTile), p.cache_len - tb);
+          valid = low_bits(lim);
+          if (lim > 0) {
+            ys[0] = (int)(((int64_t)cur.unit * p.cache_len + tb) );
+            nbox = 1;
+          }
+        }
+      } else if (!p.paged) {
+        const int lim = min(cur.n_valid - tok_base, kTile);
+        valid = low_bits(lim);
+        ys[0] = (int)(((int64_t)cur.unit * p.cache_len + tok_base) );
+        nbox = 1;
+      } else if (P >= kTile) {
+        const int page = __shfl_sync(0xffffffffu, id_cur, 0);
+        if (page >= 0) {
+          valid = low_bits(min(cur.n_valid - tok_base, kTile));
+          ys[0] = (int)((((int64_t)page * p.num_kv_heads + cur.h) * P + tok_base % P) );
+          nbox = 1;
+        }
+      } else {
+        for (int k = 0; k < kTile / P; ++k) {
+          const int page = __shfl_sync(0xffffffffu, id_cur, k);
+          ys[k] = -1;
+          if (page >= 0) {
+            valid |= low_bits(min(cur.n_valid - (tok_base + k * P), P)) << (k * P);
+            ys[k] = (int)(((int64_t)page * p.num_kv_heads + cur.h) * P );
+            ++nbox;
+          }
+        }
+      }
+      if (lane == 0) {
+        const bool first = (i == 0) || (cur.j == 0);
+        const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
+        StageMeta m;
+        m.valid = valid;
+        m.unit = cur.unit;
+        m.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+        m.c_first = cur.c_first;
+        m.n_seg = cur.n_seg;
+        meta[st] = m;
+        const uint32_t box_tokens = (p.paged && P < kTile) ? (uint32_t)P : (uint32_t)kTile;
+        uint32_t bytes = 2u * (uint32_t)nbox * box_tokens * C::kBytesPerTok;
+        if (first) bytes += (uint32_t)G * kD * 2;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        uint8_t *kdst = ring + (size_t)st * 2 * C::kTileBytes;
+        uint8_t *vdst = kdst + C::kTileBytes;
+        if (first)
+          tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
+                      (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
+        const int nb = (p.paged && P < kTile) ? kTile / P : (nbox ? 1 : 0);
+        const int box_rows = (p.paged && P < kTile) ? P : kTile;
+        for (int k = 0; k < nb; ++k) {
+          if (ys[k] < 0) continue;
+          const int off = k * box_rows * C::kBytesPerTok;  // box k of a multi-page tile
+          if (FP8) {
+            tma_load_2d(kdst + off, &kmap, &full[st], 0, ys[k], policy);
+            tma_load_2d(vdst + off, &vmap, &full[st], 0, ys[k], policy);
+          } else {
+            // one 3-D box: both 64-element halves of box_rows rows, half-major
+            tma_load_3d(kdst + off, &kmap, &full[st], 0, ys[k], 0, policy);
+            tma_load_3d(vdst + off, &vmap, &full[st], 0, ys[k], 0, policy);
+          }
+        }
+      }
+      // shift the id queue by one tile and look up tile i + ahead_n
+      if (needs_ids) {
+        idq = __shfl_down_sync(0xffffffffu, idq, L);
+        if (i + ahead_n < ntiles) {
+          if (lane >= (ahead_n - 1) * L && lane < ahead_n * L)
+            idq = load_id(ahead, lane - (ahead_n - 1) * L);
+          if (i + ahead_n + 1 < ntiles) advance(ahead);
+        }
+      }
+      if (i + 1 < ntiles) advance(cur);
+    }
+  } else {
+    // ======================================================= consumers
+    const int q4 = lane & 3;   // owns heads g = nt*8 + 2*q4 + {0,1}
+    const int r8 = lane >> 2;  // row inside an 8-row group
+    const int tok_lane = 16 * warp + (lane & 7);
+    const int mi = lane >> 3;  // which 8x8 matrix this lane addresses
+    const int br_shift = (p.paged && p.page_size < kTile) ? __ffs(p.page_size) - 1 : 6;
+    // this lane's ldmatrix row tokens: (mi & 1) selects +8 for QK / fp8 V, (mi >> 1) for bf16 V
+    const uint32_t toff_a = token_offset<FP8>(tok_lane + (mi & 1) * 8, br_shift);
+    const uint32_t toff_b = token_offset<FP8>(tok_lane + (mi >> 1) * 8, br_shift);
+    uint32_t qf[NT][8][2];
+    float oacc[NT][8][4];
+    float m_run[NT][2], l_part[NT][2];
+    float sscale = p.score_scale, vmul = 1.f;
+    auto reset = [&]() {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oacc[nt][mt][e] = 0.f;
+        m_run[nt][0] = m_run[nt][1] = neg_inf();
+        l_part[nt][0] = l_part[nt][1] = 0.f;
+      }
+    };
+    reset();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
+    bool ok = true;
+
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % C::kStages;
+      if (!mbar_wait_bounded(&full[st], (i / C::kStages) & 1, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      const StageMeta m = meta[st];
+      const int unit = m.unit;
+      if (m.flags & kFirst) {
+        // the segment's query group: Q^T fragments (B operand), read once per segment
+        const int h = unit % p.num_kv_heads;
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(qslots + st * C::kQSlot);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int g = nt * 8 + r8;
+          const uint32_t *qrow = qs + (g < G ? g : 0) * (kD / 2);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            if (!FP8) {
+              qf[nt][ks][0] = g < G ? qrow[(16 * ks + 2 * q4) / 2] : 0u;
+              qf[nt][ks][1] = g < G ? qrow[(16 * ks + 8 + 2 * q4) / 2] : 0u;
+            } else {
+              // k-step 2pp+e covers bytes 32pp + 16e + 4q4 .. +3 of each fp8 key row
+              const int pp = ks >> 1, e = ks & 1;
+              const int d0 = 32 * pp + 16 * e + 4 * q4;
+              qf[nt][ks][0] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2]) : 0u;
+              qf[nt][ks][1] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2 + 1]) : 0u;
+            }
+          }
+        }
+        if (FP8) {
+          sscale = p.score_scale * p.k_scale[h];
+          vmul = p.v_scale[h];
+        }
+      }
+      const uint32_t vbits = (uint32_t)(m.valid >> (16 * warp)) & 0xFFFFu;
       if (vbits != 0) {
-        const uint32_t kbase = smem_u32(ring + (size_t)st * 2 * T::kTileBytes);
-        const uint32_t vbase = kbase + T::kTileBytes;
+        const uint32_t kbase = smem_u32(ring + (size_t)st * 2 * C::kTileBytes);
+        const uint32_t vbase = kbase + C::kTileBytes;
         // ---------------- S^T = K Q^T (16 tokens x 8*NT heads)
         float sacc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-        if (!FP8) {
+        {
           const int t = tok_lane + (mi & 1) * 8;
+          if (!FP8) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(chunk_addr<false>(kbase, t, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+            for (int ks = 0; ks < 8; ++ks) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(chunk_addr<false>(kbase, toff_a, t, 2 * ks + (mi >> 1), br_shift), a0, a1, a2, a3);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_bf16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
-          }
-        } else {
-          const int t = tok_lane + (mi & 1) * 8;
+              for (int nt = 0; nt < NT; ++nt)
+                mma_bf16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+            }
+          } else {
 #pragma unroll
-          for (int pp = 0; pp < 4; ++pp) {
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(chunk_addr<true>(kbase, t, 2 * pp + (mi >> 1)), r0, r1, r2, r3);
-            const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(r0 & 0xFFFF));
-            const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(r0 >> 16));
-            const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(r1 & 0xFFFF));
-            const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(r1 >> 16));
-            const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(r2 & 0xFFFF));
-            const uint32_t c2 = e4m3x2_to_f16x2((uint16_t)(r2 >> 16));
-            const uint32_t c1 = e4m3x2_to_f16x2((uint16_t)(r3 & 0xFFFF));
-            const uint32_t c3 = e4m3x2_to_f16x2((uint16_t)(r3 >> 16));
+            for (int pp = 0; pp < 4; ++pp) {
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4(chunk_addr<true>(kbase, toff_a, t, 2 * pp + (mi >> 1), br_shift), r0, r1, r2, r3);
+              const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(r0 & 0xFFFF));
+              const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(r0 >> 16));
+              const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(r1 & 0xFFFF));
+              const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(r1 >> 16));
+              const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(r2 & 0xFFFF));
+              const uint32_t c2 = e4m3x2_to_f16x2((uint16_t)(r2 >> 16));
+              const uint32_t c1 = e4m3x2_to_f16x2((uint16_t)(r3 & 0xFFFF));
+              const uint32_t c3 = e4m3x2_to_f16x2((uint16_t)(r3 >> 16));
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma_f16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][2 * pp][0], qf[nt][2 * pp][1]);
-              mma_f16_16816(sacc[nt], c0, c1, c2, c3, qf[nt][2 * pp + 1][0],
-                            qf[nt][2 * pp + 1][1]);
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_f16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][2 * pp][0], qf[nt][2 * pp][1]);
+                mma_f16_16816(sacc[nt], c0, c1, c2, c3, qf[nt][2 * pp + 1][0],
+                              qf[nt][2 * pp + 1][1]);
+              }
             }
           }
         }
@@ -504,7 +746,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             oacc[nt][mt][2] *= alpha[0];
             oacc[nt][mt][3] *= alpha[1];
           }
-          // P^T as the B operand: transpose the (token x head) 8x8 blocks
           const uint32_t x0 = FP8 ? pack_f16(sacc[nt][0], sacc[nt][1])
                                   : pack_bf16(sacc[nt][0], sacc[nt][1]);
           const uint32_t x1 = FP8 ? pack_f16(sacc[nt][2], sacc[nt][3])
@@ -512,8 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb[nt][0] = movmatrix_trans(x0);
           pb[nt][1] = movmatrix_trans(x1);
         }
-        // ---------------- O^T += V^T P^T
-        // tokens of this lane in the A fragment: 2q4, 2q4+1 (a0, a1) and +8 (a2, a3)
+        // ---------------- O^T += V^T P^T (masked tokens' V zeroed in registers)
         const bool full16 = vbits == 0xFFFFu;
         const uint32_t m01 = lo16_mask((vbits >> (2 * q4)) & 1u, (vbits >> (2 * q4 + 1)) & 1u);
         const uint32_t m89 =
@@ -523,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(chunk_addr<false>(vbase, t, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+            ldsm_x4_trans(chunk_addr<false>(vbase, toff_b, t, 2 * mt + (mi & 1), br_shift), a0, a1, a2, a3);
             if (!full16) {
               a0 &= m01;
               a1 &= m01;
@@ -539,13 +779,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(chunk_addr<true>(vbase, t, 2 * pp + (mi >> 1)), r0, r1, r2, r3);
+            ldsm_x4_trans(chunk_addr<true>(vbase, toff_a, t, 2 * pp + (mi >> 1), br_shift), r0, r1, r2, r3);
             // r = [V[2q][2c], V[2q][2c+1], V[2q+1][2c], V[2q+1][2c+1]] -> token pairs per d
             const uint32_t s0 = prmt(r0, 0, 0x3120), s1 = prmt(r1, 0, 0x3120);
             const uint32_t s2 = prmt(r2, 0, 0x3120), s3 = prmt(r3, 0, 0x3120);
-            uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(s0 & 0xFFFF));  // d 2c,   tokens 2q..
-            uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(s0 >> 16));     // d 2c+1, tokens 2q..
-            uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(s1 & 0xFFFF));  // d 2c,   tokens 2q+8..
+            uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(s0 & 0xFFFF));
+            uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(s0 >> 16));
+            uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(s1 & 0xFFFF));
             uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(s1 >> 16));
             uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(s2 & 0xFFFF));
             uint32_t c1 = e4m3x2_to_f16x2((uint16_t)(s2 >> 16));
@@ -571,114 +811,144 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-    }
 
-    // ---------------- merge the four warps' partial softmax states
+      if (!(m.flags & kLast)) continue;
+      // ======================= segment epilogue (consumer threads only)
+      const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float l = l_part[nt][e];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        l_part[nt][e] = l;
-        if (r8 == 0) {
-          const int g = nt * 8 + 2 * q4 + e;
-          stat_m[warp * 16 + g] = m_run[nt][e];
-          stat_l[warp * 16 + g] = l;
+        for (int e = 0; e < 2; ++e) {
+          float l = l_part[nt][e];
+          l += __shfl_xor_sync(0xffffffffu, l, 4);
+          l += __shfl_xor_sync(0xffffffffu, l, 8);
+          l += __shfl_xor_sync(0xffffffffu, l, 16);
+          l_part[nt][e] = l;
+          if (r8 == 0) {
+            const int g = nt * 8 + 2 * q4 + e;
+            stat_m[warp * 16 + g] = m_run[nt][e];
+            stat_l[warp * 16 + g] = l;
+          }
         }
-      }
-  }
-
-  __syncthreads();  // all loops done: every issued TMA box has been consumed
-
-  if (*abort_flag) {
-    // a wait gave up: drain copies still in flight (bounded), report, leave
-    if (threadIdx.x == kConsumerWarps * 32) {
-      const int last = num_tiles - 1;
-      for (int st = 0; st < T::kStages && st <= last; ++st) {
-        const int i_last = last - ((last - st) % T::kStages);
-        mbar_wait_bounded(&full[st], (i_last / T::kStages) & 1, kWaitLimitNs);
-      }
-    }
-    if (lane == 0 || dev_err) atomicOr(p.err, dev_err | DA_DEVERR_TIMEOUT);
-    return;
-  }
-
-  // Reduction buffer (reuses the ring): red[warp][g][kRedStride] fp32
-  float *red = reinterpret_cast<float *>(ring);
-  if (warp < kConsumerWarps) {
-    const int q4 = lane & 3, r8 = lane >> 2;
+      named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+      // the warps add their rescaled O^T into one buffer, one warp at a time
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        if (warp == w) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int g = nt * 8 + 2 * q4 + e;
+            for (int e = 0; e < 2; ++e) {
+              const int g = nt * 8 + 2 * q4 + e;
+              float M = neg_inf();
+#pragma unroll
+              for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, stat_m[ww * 16 + g]);
+              const float wscale = (M == neg_inf()) ? 0.f : ex2(m_run[nt][e] - M);
+              float *dst = red + (size_t)g * kRedStride;
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt) {
+                const int d0 = FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8;
+                const int d1 = FP8 ? d0 + 1 : d0 + 8;
+                const float v0 = oacc[nt][mt][e] * wscale, v1 = oacc[nt][mt][2 + e] * wscale;
+                if (w == 0) {
+                  dst[d0] = v0;
+                  dst[d1] = v1;
+                } else {
+                  dst[d0] += v0;
+                  dst[d1] += v1;
+                }
+              }
+            }
+        }
+        named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+      }
+      // thread tid (< 128) owns head-dim element d = tid for every g of the group
+      const int d = threadIdx.x;
+      const bool whole = m.n_seg == 1;
+      const int64_t slot = (int64_t)unit + cta;
+      for (int g = 0; g < G; ++g) {
         float M = neg_inf();
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stat_m[w * 16 + g]);
-        const float wscale = (M == neg_inf()) ? 0.f : ex2(m_run[nt][e] - M);
-        float *dst = red + ((size_t)warp * 16 + g) * kRedStride;
+        float L = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          int d0, d1;
-          if (!FP8) {
-            d0 = 16 * mt + r8;
-            d1 = d0 + 8;
-          } else {
-            d0 = 16 * mt + 2 * r8;
-            d1 = d0 + 1;
-          }
-          dst[d0] = oacc[nt][mt][e] * wscale;
-          dst[d1] = oacc[nt][mt][2 + e] * wscale;
+        for (int w = 0; w < kConsumerWarps; ++w)
+          L += (M == neg_inf()) ? 0.f : stat_l[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
+        const float o = (L > 0.f) ? red[(size_t)g * kRedStride + d] * vmul / L : 0.f;
+        const float lse = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf();
+        if (whole) {
+          const int64_t row = (int64_t)b * p.num_q_heads + h * G + g;
+          p.out[row * kD + d] = __float2bfloat16(o);
+          if (d == 0 && p.lse) p.lse[row] = lse;
+        } else {
+          p.o_part[(slot * G + g) * kD + d] = o;
+          if (d == 0) p.lse_part[slot * G + g] = lse;
         }
       }
-  }
-  __syncthreads();
-
-  // thread tid < 128 owns head-dim element d = tid for every g of the group
-  if (threadIdx.x < kD) {
-    const int d = threadIdx.x;
-    const float vmul = FP8 ? p.v_scale[h] : 1.f;
-    for (int g = 0; g < G; ++g) {
-      float M = neg_inf();
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, stat_m[w * 16 + g]);
-      float L = 0.f, acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = stat_m[w * 16 + g];
-        const float sw = (M == neg_inf()) ? 0.f : ex2(mw - M);
-        L += stat_l[w * 16 + g] * sw;
-        acc += red[((size_t)w * 16 + g) * kRedStride + d];
+      named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+      if (!whole && threadIdx.x == 0) {
+        // one release/acquire count per segment; the barrier above ordered all
+        // consumer threads' partial writes before it
+        const unsigned prev = atomic_add_acq_rel_gpu(p.counters + unit, 1u);
+        if (prev == (unsigned)(m.n_seg - 1) && flags[12] < 2) {
+          // this CTA finished the unit's last segment: merge once its range is done
+          const int k = flags[12];
+          flags[6 + 3 * k] = unit;
+          flags[7 + 3 * k] = m.c_first;
+          flags[8 + 3 * k] = m.n_seg;
+          flags[12] = k + 1;
+        }
       }
-      const float o = (L > 0.f) ? acc * vmul / L : 0.f;
-      // natural-log LSE: (m + log2 l) * ln 2
-      const float lse = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf();
-      if (p.write_final) {
-        const int64_t row = (int64_t)b * p.num_q_heads + h * G + g;
-        p.out[row * kD + d] = __float2bfloat16(o);
-        if (d == 0 && p.lse) p.lse[row] = lse;
-      } else {
-        p.o_part[(slot * G + g) * kD + d] = o;
-        if (d == 0) p.lse_part[slot * G + g] = lse;
-      }
+      reset();
+    }
+    // ---- merges this CTA owes (its ring is free now: every tile was consumed)
+    if (!ok) flags[0] = 1;
+    named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+    uint32_t merge_phase[2] = {0u, 0u};
+    const int npending = flags[0] ? 0 : flags[12];  // the same for all consumer threads
+    for (int k = 0; k < npending; ++k) {
+      if (!merge_unit(p, flags[6 + 3 * k], flags[7 + 3 * k], flags[8 + 3 * k], G, ring,
+                      C::kStages * 2 * C::kTileBytes, red, 8 * NT * kRedStride,
+                      reinterpret_cast<float *>(qslots), merge_bar, merge_phase))
+        ok = false;
+    }
+    if (!ok) {
+      dev_err |= DA_DEVERR_TIMEOUT;
+      flags[0] = 1;
     }
   }
+
+  __syncthreads();  // every issued TMA box has been consumed (or a wait gave up)
+  if (flags[0]) {
+    // a wait gave up: drain copies still in flight (bounded) before leaving
+    if (threadIdx.x == kConsumerWarps * 32) {
+      for (int st = 0; st < C::kStages && st < ntiles; ++st) {
+        const int i_last = (ntiles - 1) - ((ntiles - 1 - st) % C::kStages);
+        mbar_wait_bounded(&full[st], (i_last / C::kStages) & 1, kWaitLimitNs);
+      }
+    }
+    dev_err |= DA_DEVERR_TIMEOUT;
+  }
   if (dev_err) atomicOr(p.err, dev_err);
-  if (!p.write_final) merge_if_last(p, b, h, G, red, last_flag);
 }
 
 template <bool FP8, int NT>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<FP8>::kTotal);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FP8, NT>::kTotal);
+}
+
+template <bool FP8, int NT>
+void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
+            const GqaParams &p, int ctas, cudaStream_t stream) {
+  gqa_split_kernel<FP8, NT><<<ctas, kThreads, Cfg<FP8, NT>::kTotal, stream>>>(kmap, vmap, qmap, p);
 }
 
 }  // namespace
 
-int gqa_smem_bytes(bool fp8) { return fp8 ? Smem<true>::kTotal : Smem<false>::kTotal; }
+int gqa_smem_bytes(bool fp8, int group) {
+  if (fp8) return group <= 8 ? Cfg<true, 1>::kTotal : Cfg<true, 2>::kTotal;
+  return group <= 8 ? Cfg<false, 1>::kTotal : Cfg<false, 2>::kTotal;
+}
 int gqa_threads() { return kThreads; }
 
 int gqa_box_tokens(const da_problem &p) {
@@ -696,18 +966,18 @@ cudaError_t gqa_prepare(int /*device*/) {
 }
 
 cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                       const GqaParams &p, dim3 grid, cudaStream_t stream) {
-  const dim3 block(kThreads);
+                       const CUtensorMap &qmap, const GqaParams &p, int ctas,
+                       cudaStream_t stream) {
   if (!fp8) {
     if (group <= 8)
-      gqa_split_kernel<false, 1><<<grid, block, Smem<false>::kTotal, stream>>>(kmap, vmap, p);
+      launch<false, 1>(kmap, vmap, qmap, p, ctas, stream);
     else
-      gqa_split_kernel<false, 2><<<grid, block, Smem<false>::kTotal, stream>>>(kmap, vmap, p);
+      launch<false, 2>(kmap, vmap, qmap, p, ctas, stream);
   } else {
     if (group <= 8)
-      gqa_split_kernel<true, 1><<<grid, block, Smem<true>::kTotal, stream>>>(kmap, vmap, p);
+      launch<true, 1>(kmap, vmap, qmap, p, ctas, stream);
     else
-      gqa_split_kernel<true, 2><<<grid, block, Smem<true>::kTotal, stream>>>(kmap, vmap, p);
+      launch<true, 2>(kmap, vmap, qmap, p, ctas, stream);
   }
   return cudaGetLastError();
 }

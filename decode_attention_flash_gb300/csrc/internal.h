@@ -28,8 +28,8 @@ struct GqaParams {
   const int32_t *kv_idx;       // sparse: [B][HKV][max_sparse_blocks]
   const float *k_scale;        // fp8: [HKV]
   const float *v_scale;        // fp8: [HKV]
-  float *o_part;               // [units][S][G][128]
-  float *lse_part;             // [units][S][G]
+  float *o_part;               // [units + ctas][G][128] partial slots (slot = unit + cta)
+  float *lse_part;             // [units + ctas][G]
   __nv_bfloat16 *out;          // [B][HQ][128]
   float *lse;                  // [B][HQ] or null
   uint32_t *err;               // device error word
@@ -39,9 +39,6 @@ struct GqaParams {
   int32_t paged, page_size, cache_len, max_pages, num_pages;
   int32_t capacity;            // max positions per row
   int32_t sparse_block_size, max_sparse_blocks;
-  int32_t chunk;               // positions (dense) or list entries * block (sparse) per split
-  int32_t num_splits;
-  int32_t write_final;
 };
 
 struct MergeParams {
@@ -70,10 +67,11 @@ struct MlaParams {
 
 // Kernel launchers (return the launch error).
 cudaError_t gqa_prepare(int device);  // sets shared-memory attributes once per device
-int gqa_smem_bytes(bool fp8);
+int gqa_smem_bytes(bool fp8, int group);
 int gqa_threads();
 cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                       const GqaParams &p, dim3 grid, cudaStream_t stream);
+                       const CUtensorMap &qmap, const GqaParams &p, int ctas,
+                       cudaStream_t stream);
 int gqa_box_tokens(const da_problem &p);
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);

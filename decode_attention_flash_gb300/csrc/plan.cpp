@@ -83,9 +83,10 @@ da_status validate_problem(const da_problem *p) {
 // Resident CTAs of the split kernel per SM, from its shared-memory footprint.
 static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
   const bool mla = p->is_mla != 0;
-  const int per_cta =
-      (mla ? mla_smem_bytes() : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3)) +
-      1024;  // the runtime reserves 1 KB per CTA
+  const int per_cta = (mla ? mla_smem_bytes()
+                           : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3,
+                                            p->num_q_heads / p->num_kv_heads)) +
+                      1024;  // the runtime reserves 1 KB per CTA
   const int threads = mla ? mla_threads() : gqa_threads();
   return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));
 }
@@ -157,26 +158,54 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   }
   max_len = std::max<int64_t>(max_len, 1);
 
+  const int cps = ctas_per_sm(p, smem_per_sm);
+  if (!mla) {
+    // Persistent GQA grid: the tiles of all units are cut into equal ranges, one
+    // per CTA, on the device; the host only sizes the grid (one wave of the
+    // resident CTA slots, never more CTAs than tiles).
+    int64_t tiles = 0;
+    for (int64_t len : unit_len) tiles += ceil_div(len, tile);
+    tiles = std::max<int64_t>(tiles, 1);
+    int64_t ctas = (int64_t)num_sms * cps;
+    if (num_splits_override > 0) ctas = (int64_t)num_splits_override * units;
+    ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, tiles));
+    ctas = std::min<int64_t>(ctas, 65535);
+    info->kv_tile = tile;
+    info->chunk_tokens = (int32_t)(ceil_div(tiles, ctas) * tile);
+    info->num_splits = (int32_t)ceil_div(ctas, units);
+    info->num_units = (int32_t)units;
+    info->rows_per_unit = rows;
+    info->grid_x = (int32_t)ctas;
+    info->grid_y = 1;
+    info->grid_z = 1;
+    info->ctas_per_sm = cps;
+    info->writes_final = 0;  // decided per unit on the device
+    int64_t off = kWorkspaceHeader;
+    info->counters_offset = off;
+    off = align256(off + units * 4);
+    info->partial_o_offset = off;  // slots unit + cta
+    off = align256(off + (units + ctas) * rows * (int64_t)dv * 4);
+    info->partial_lse_offset = off;
+    off = align256(off + (units + ctas) * rows * 4);
+    info->workspace_bytes = off;
+    return DA_OK;
+  }
+
   // largest split the kernel can take: its page / block ids fit in shared memory
   int64_t max_chunk = round_up(max_len, align);
-  if (!mla && paged) max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size / align * align);
-  if (mla) max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size);
-  if (sparse) max_chunk = std::min<int64_t>(max_chunk, (int64_t)kGqaMaxIds * p->sparse_block_size);
+  max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size);
   max_chunk = std::max<int64_t>(max_chunk, align);
   const int64_t min_splits = ceil_div(max_len, max_chunk);
 
-  const int cps = ctas_per_sm(p, smem_per_sm);
   // an MLA split runs on a cluster of two CTAs: count cluster slots
-  const int slots = mla ? std::max(1, num_sms * cps / 2) : num_sms * cps;
-  const int max_splits = mla ? mla_max_splits() : kMaxSplits;
+  const int slots = std::max(1, num_sms * cps / 2);
+  const int max_splits = mla_max_splits();
   int64_t chunk;
   if (num_splits_override > 0) {
     chunk = round_up(ceil_div(max_len, std::max<int64_t>(num_splits_override, min_splits)), align);
     chunk = std::min(chunk, max_chunk);
   } else {
-    const double bytes_per_pos =
-        mla ? (p->ckv_dim + p->kpe_dim) * 2.0 * 1.3  // MLA also pays its QK/PV flops
-            : (p->head_dim_qk + p->head_dim_v) * (p->kv_dtype == DA_DTYPE_FP8_E4M3 ? 1.0 : 2.0);
+    const double bytes_per_pos = (p->ckv_dim + p->kpe_dim) * 2.0 * 1.3;  // MLA also pays flops
     const double sec_per_pos = bytes_per_pos / kHbmBytesPerSec;
     const double merge_sec_per_split = rows * (dv + 1) * 4.0 / kMergeBytesPerSec;
     const int64_t max_ctas = (int64_t)slots * kMaxCtasPerSlot;
@@ -191,7 +220,7 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
       if (splits > max_splits) break;
       if (splits > 1 && units * splits > max_ctas) break;
       const double t = makespan(unit_len, heads, c, splits, slots, sec_per_pos, merge_sec_per_split);
-      if (last_chunk == c && (best == 0.0 || t < best * 0.999)) {
+      if (best == 0.0 || t < best * 0.999) {
         best = t;
         chunk = c;
       }
@@ -206,19 +235,19 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   info->num_splits = (int32_t)splits;
   info->num_units = (int32_t)units;
   info->rows_per_unit = rows;
-  info->grid_x = (int32_t)(mla ? 2 * splits : splits);  // MLA: a CTA pair per split
+  info->grid_x = (int32_t)(2 * splits);  // MLA: a CTA pair per split
   info->grid_y = heads;
   info->grid_z = p->batch;
   info->ctas_per_sm = cps;
   info->writes_final = splits == 1 ? 1 : 0;
   int64_t off = kWorkspaceHeader;
   info->counters_offset = off;
-  off = align256(off + units * (mla ? 2 : 1) * 4);
+  off = align256(off + units * 2 * 4);
   if (!info->writes_final) {
     info->partial_o_offset = off;
     off = align256(off + units * splits * rows * (int64_t)dv * 4);
     info->partial_lse_offset = off;
-    off = align256(off + units * splits * rows * (mla ? 2 : 1) * 4);
+    off = align256(off + units * splits * rows * 2 * 4);
   }
   info->workspace_bytes = off;
   return DA_OK;

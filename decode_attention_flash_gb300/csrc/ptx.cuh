@@ -287,3 +287,50 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 }  // namespace da
+
+namespace da {
+
+// 3-D tiled TMA load (x innermost).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *desc, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z,
+                                            uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+      "l"(cache_policy)
+      : "memory");
+}
+
+// Contiguous global -> shared bulk copy (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                              uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy global accesses (and those it has
+// observed) before its later async-proxy (TMA / bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// atomicAdd with release (for this thread's and observed writes) and acquire
+// (for the writes of whoever released the earlier counts) at GPU scope.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t *ptr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
+}
+
+}  // namespace da

@@ -96,7 +96,7 @@ def _problem(w):
 
 
 def _check_cover(plan, lengths, align):
-    """Every position of every unit is in exactly one split, splits are tile-aligned."""
+    """MLA plans: every position of every unit is in exactly one tile-aligned split."""
     chunk, S = plan["chunk_tokens"], plan["num_splits"]
     assert chunk % align == 0 and chunk > 0
     for n in lengths:
@@ -112,56 +112,97 @@ def _check_cover(plan, lengths, align):
         assert covered == n
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def _gqa_schedule(ctas, unit_tiles):
+    """The persistent GQA kernel's schedule, as its comments define it: the units'
+    tiles laid end to end are cut into `ctas` equal ranges [floor(c*T/C),
+    floor((c+1)*T/C)); returns per-unit lists of (cta, first tile, last tile)."""
+    T = sum(unit_tiles)
+    bounds = [c * T // ctas for c in range(ctas + 1)]
+    segs = []
+    start = 0
+    for t in unit_tiles:
+        seg = []
+        for c in range(ctas):
+            lo, hi = max(bounds[c], start), min(bounds[c + 1], start + t)
+            if hi > lo:
+                seg.append((c, lo - start, hi - start))
+        segs.append(seg)
+        start += t
+    return segs, bounds
+
+
+def _check_gqa_plan(plan, unit_tiles, num_sms=152):
+    C = plan["grid_x"]
+    assert plan["grid_y"] == plan["grid_z"] == 1
+    assert 1 <= C <= max(sum(unit_tiles), 1)
+    assert C <= num_sms * plan["ctas_per_sm"] or plan["num_splits"] > 0
+    segs, bounds = _gqa_schedule(C, unit_tiles)
+    # every tile of every unit is in exactly one segment, segments are contiguous
+    for t, seg in zip(unit_tiles, segs):
+        pos = 0
+        for _, lo, hi in seg:
+            assert lo == pos
+            pos = hi
+        assert pos == t
+        # the device finds a unit's segments from its first and last tile: c_first..c_last
+        if seg:
+            assert [c for c, _, _ in seg] == list(range(seg[0][0], seg[-1][0] + 1))
+    # balance: every CTA streams floor or ceil of T/C tiles
+    sizes = [bounds[c + 1] - bounds[c] for c in range(C)]
+    assert max(sizes) - min(sizes) <= 1
+    # the workspace holds a partial slot for every (unit + cta)
+    U, G = plan["num_units"], plan["rows_per_unit"]
+    assert plan["counters_offset"] == 256
+    assert plan["partial_lse_offset"] - plan["partial_o_offset"] >= (U + C) * G * 128 * 4
+    assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * G * 4
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 def test_planner_covers_every_position_once(lib, cfg):
     w = W.config(cfg, shape_only=True)
+    nb = w.tensors.get("kv_num_blks")
     plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], w.num_splits)
     lens = [int(x) for x in w.tensors["seq_lens"]]
-    _check_cover(plan, lens, plan["kv_tile"])
-    # MLA runs each split on a cluster of two CTAs
-    assert plan["grid_x"] == plan["num_splits"] * (2 if w.is_mla else 1)
-    assert plan["grid_z"] == w.batch
-    if cfg == 1:
-        assert plan["num_splits"] == 4 and plan["chunk_tokens"] == 128
-    else:
-        # enough CTAs with work to fill every SM, and splits within the fused merge's limit
-        busy = sum(math.ceil(n / plan["chunk_tokens"]) for n in lens) * plan["grid_y"]
-        busy *= 2 if w.is_mla else 1  # CTAs per split
+    if w.is_mla:
+        _check_cover(plan, lens, plan["kv_tile"])
+        assert plan["grid_x"] == 2 * plan["num_splits"]  # a cluster of two CTAs per split
+        busy = sum(math.ceil(n / plan["chunk_tokens"]) for n in lens) * 2
         assert busy >= 152
-        assert 1 <= plan["num_splits"] <= 256
+        return
+    if w.sparse_block_size:
+        tiles = [int(x) * (w.sparse_block_size // 64) for x in w.tensors["kv_num_blks"].flatten()]
+        tiles = [256 * 2] * len(tiles)  # plan_info assumes full lists without host counts
+    else:
+        tiles = [math.ceil(n / 64) for n in lens for _ in range(w.num_kv_heads)]
+    _check_gqa_plan(plan, tiles)
+    if cfg == 1:
+        assert plan["grid_x"] == 4  # the forced 4 splits of the one unit
+    else:
+        assert plan["grid_x"] == min(152 * plan["ctas_per_sm"], sum(tiles))
 
 
-def test_planner_sparse_splits_whole_blocks(lib):
+def test_planner_sparse_with_list_lengths(lib):
+    """With the host list lengths the grid covers exactly the listed blocks."""
     w = W.config(4, shape_only=True)
+    tiles = [int(x) * 2 for x in w.tensors["kv_num_blks"].flatten()]
     plan = da.decode_attn_plan_info(_problem(w), 152, None, 0)
-    assert plan["chunk_tokens"] % w.sparse_block_size == 0
-    # with the real list lengths the splits cover the 36 listed blocks
-    nb = w.tensors["kv_num_blks"].contiguous()
-    lengths = [int(x) * w.sparse_block_size for x in nb.flatten()]
-    _check_cover(plan, lengths, w.sparse_block_size)
+    _check_gqa_plan(plan, [512] * len(tiles))
+    # the schedule of the real lists: balanced and gap-free
+    segs, bounds = _gqa_schedule(min(304, sum(tiles)), tiles)
+    assert sum(hi - lo for seg in segs for _, lo, hi in seg) == sum(tiles)
 
 
 def test_planner_override_and_workspace_layout(lib):
     w = W.make_gqa(batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[1000, 5], cache_len=1024,
                    seed=1)
+    tiles = [16, 16, 1, 1]
     for S in (1, 2, 3, 7, 16):
         plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], S)
-        assert plan["num_splits"] <= S
-        _check_cover(plan, [1000, 5], 64)
-        assert plan["counters_offset"] == 256
-        if plan["num_splits"] == 1:
-            assert plan["writes_final"] == 1
-            assert plan["workspace_bytes"] == 512
-        else:
-            units, rows = 4, 4
-            need_o = units * plan["num_splits"] * rows * 128 * 4
-            assert plan["partial_lse_offset"] - plan["partial_o_offset"] >= need_o
-            assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= units * plan[
-                "num_splits"] * rows * 4
-            assert plan["partial_o_offset"] % 256 == 0 and plan["partial_lse_offset"] % 256 == 0
+        _check_gqa_plan(plan, tiles)
+        assert plan["grid_x"] == min(S * 4, sum(tiles))
 
 
 def test_planner_without_host_lengths_assumes_full_rows(lib):
     w = W.config(2, shape_only=True)
     p1 = da.decode_attn_plan_info(_problem(w), 152, None, 0)
-    _check_cover(p1, [w.max_seq_len] * w.batch, 64)
+    _check_gqa_plan(p1, [w.max_seq_len // 64] * (w.batch * w.num_kv_heads))
