@@ -204,7 +204,6 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
     da_status st;
     if ((st = encode_bf16_rows(&ctx->kmap, a->k, 512, tokens, 64)) != DA_OK) return st;
     if ((st = encode_bf16_rows(&ctx->vmap, a->v, 64, tokens, 64)) != DA_OK) return st;
-    if ((st = encode_bf16_rows(&ctx->qmap, a->q, 512, qrows, 128)) != DA_OK) return st;
     if ((st = encode_bf16_rows(&ctx->qpemap, a->q_pe, 64, qrows, 128)) != DA_OK) return st;
     ctx->map_k_base = a->k;
     ctx->map_v_base = a->v;
@@ -233,7 +232,7 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.num_splits = pl.num_splits;
   mp.write_final = pl.writes_final;
   const dim3 grid(pl.grid_x, 1, pl.grid_z);
-  cudaError_t e = da::launch_mla(ctx->qmap, ctx->qpemap, ctx->kmap, ctx->vmap, mp, grid, stream);
+  cudaError_t e = da::launch_mla(ctx->qpemap, ctx->kmap, ctx->vmap, mp, grid, stream);
   if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;

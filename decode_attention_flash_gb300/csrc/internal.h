@@ -80,9 +80,9 @@ cudaError_t mla_prepare(int device);
 int mla_smem_bytes();
 int mla_threads();
 int mla_max_splits();
-cudaError_t launch_mla(const CUtensorMap &qn_map, const CUtensorMap &qp_map,
-                       const CUtensorMap &ckv_map, const CUtensorMap &kpe_map,
-                       const MlaParams &p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_mla(const CUtensorMap &qp_map, const CUtensorMap &ckv_map,
+                       const CUtensorMap &kpe_map, const MlaParams &p, dim3 grid,
+                       cudaStream_t stream);
 
 // Planner (pure host code).
 da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm,

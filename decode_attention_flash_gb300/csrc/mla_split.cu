@@ -21,12 +21,25 @@
 // shared memory (MN-major operand). Every KV byte is read from HBM once, no
 // tensor-core work is repeated, and nothing is multicast.
 //
-// Warp roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer
-// (and TMEM owner), warps 2-5 = softmax (one thread per head row: the TMEM
-// lane layout gives each thread a whole score row, so no shuffles). The
-// online softmax rescales O lazily: only when a row's maximum grows by more
+// Tensor memory per CTA: O half in columns 0-255, the CTA's 256 q_nope values
+// per head in 256-383 (the A operand of the score MMAs, read from TMEM so that
+// only the 2 KB K slice of each MMA comes from shared memory), two score
+// buffers in 384-447 and 448-511. The kpe block of rank 1 is an ordinary
+// shared-memory MMA (q_pe is a TMA tile).
+//
+// Warp roles per CTA (352 threads): warp 0 = TMA producer (three KV stages),
+// warp 1 = MMA issuer (and TMEM owner), warp 2 = exchange helper, warps 3-10 =
+// softmax. Two softmax warps share each TMEM lane quadrant: thread (h, t) owns
+// head row h and tokens 32t..32t+31 of every tile; the pair agrees on the row
+// maximum through shared memory. The score exchange is double-buffered and
+// uses st.async, whose bytes complete on the receiver's mbarrier, so the
+// sender never waits for the remote stores; the helper warp returns each
+// buffer to the peer (a cluster-scope release) off the softmax warps' path.
+// The online softmax rescales O lazily: only when a row's maximum grows by more
 // than 2^8 is the TMEM accumulator rescaled (exact: O and l always share the
 // same reference maximum).
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -35,28 +48,48 @@ namespace {
 
 constexpr int kTok = 64;          // tokens per tile (= page)
 constexpr int kHeads = 128;
-constexpr int kThreads = 192;
-constexpr int kQBlock = kHeads * 128;  // 16 KB: 128 rows x 64 bf16, 128B-swizzled
-constexpr int kKvBlock = kTok * 128;   // 8 KB: 64 tokens x 64 bf16
-constexpr int kXStride = 68;           // floats per row of the score exchange buffer
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kThreads = 32 * (kFirstSoftmaxWarp + kSoftmaxWarps);
+constexpr int kStages = 3;                // KV ring depth
+constexpr int kQBlock = kHeads * 128;     // 16 KB: 128 rows x 64 bf16, 128B-swizzled
+constexpr int kKvBlock = kTok * 128;      // 8 KB: 64 tokens x 64 bf16
+constexpr int kKvStage = 5 * kKvBlock;    // 4 ckv blocks (+ kpe on rank 1)
+constexpr int kXBytes = kHeads * kTok * 4;  // one exchange buffer: 128 x 64 fp32
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;         // O half: columns 0..255
-constexpr uint32_t kTmemS = 256;       // two score buffers: 256..319, 320..383
+constexpr uint32_t kTmemO = 0;     // O half: columns 0..255
+constexpr uint32_t kTmemQ = 256;   // q_nope half, two bf16 per column: 256..383
+constexpr uint32_t kTmemS = 384;   // two score buffers: 384..447, 448..511
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kMaxMlaSplits = 32;
 
 struct Lay {
-  static constexpr int Q = 0;                                // 5 x 16 KB
-  static constexpr int KV = Q + 5 * kQBlock;                 // 2 stages x 5 x 8 KB
-  static constexpr int P = KV + 2 * 5 * kKvBlock;            // 16 KB
-  static constexpr int X = P + kQBlock;                      // 128 x 68 fp32
-  static constexpr int BAR = X + kHeads * kXStride * 4;
-  static constexpr int NBAR = 13;
+  static constexpr int QPE = 0;                              // 16 KB (rank 1)
+  static constexpr int KV = QPE + kQBlock;                   // kStages x 40 KB
+  static constexpr int P = KV + kStages * kKvStage;          // 16 KB
+  static constexpr int X = P + kQBlock;                      // 2 x [16][128] float4
+  static constexpr int RED = X + 2 * kXBytes;                // [2][2][128] fp32
+  static constexpr int BAR = RED + 2 * 2 * kHeads * 4;
+  static constexpr int NBAR = 22;
   static constexpr int FLAGS = BAR + NBAR * 8;               // tmem base, abort, last
   static constexpr int IDS = FLAGS + 16;
   static constexpr int TOTAL = IDS + kGqaMaxIds * 4 + 1024;  // + alignment slack
 };
-enum { B_Q = 0, B_KVF = 1, B_KVE = 3, B_SF = 5, B_SE = 7, B_PF = 9, B_PE = 10, B_XF = 11, B_XE = 12 };
+enum {
+  B_QPE = 0,   // q_pe tile landed (rank 1)
+  B_QT = 1,    // q_nope half stored in TMEM (one arrival per softmax thread)
+  B_KVF = 2,   // [kStages] KV stage full
+  B_KVE = 5,   // [kStages] KV stage consumed by the PV MMA
+  B_SF = 8,    // [2] score buffer written
+  B_SE = 10,   // [2] score buffer read
+  B_PF = 12,   // P tile written
+  B_PE = 13,   // PV MMA done
+  B_XF = 14,   // [2] peer scores landed (local expect_tx + the peer's bytes)
+  B_XE = 16,   // [2] the peer has read what this CTA sent into its buffer
+  B_XR = 18,   // [2] this CTA's softmax threads have read the buffer
+  B_RED = 20,  // [2] row-maximum / row-sum exchange between the two token halves
+};
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -72,10 +105,15 @@ __device__ __forceinline__ uint32_t mapa_peer(uint32_t smem_addr, uint32_t rank)
   return d;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
+// Asynchronous store into the peer CTA's shared memory; its 16 bytes are
+// counted on the peer's mbarrier (complete_tx), so the sender never waits.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
@@ -102,6 +140,15 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// Warp-uniform outcomes of bounded waits (the lanes then stay converged for
+// the .sync.aligned tensor-memory instructions that follow).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, kWaitLimitNs));
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster_bounded(bar, parity));
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -176,8 +223,7 @@ __device__ void mla_merge_if_last(const MlaParams &p, int b, int r, float *scrat
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_split_kernel(const __grid_constant__ CUtensorMap qn_map,
-                     const __grid_constant__ CUtensorMap qp_map,
+    mla_split_kernel(const __grid_constant__ CUtensorMap qp_map,
                      const __grid_constant__ CUtensorMap ckv_map,
                      const __grid_constant__ CUtensorMap kpe_map, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -193,7 +239,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = r ^ 1u;
   const int split = blockIdx.x >> 1, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = r == 0 ? 4 : 5;  // 64-wide contraction blocks this CTA holds
+  const int nkb = r == 0 ? 4 : 5;  // 64-wide KV blocks this CTA streams
 
   uint32_t dev_err = 0;
   int n_valid = p.seq_lens[b];
@@ -223,17 +269,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
-    mbar_init(&bar[B_Q], 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(&bar[B_QPE], 1);
+    mbar_init(&bar[B_QT], kSoftmaxThreads);
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar[B_KVF + s], 1);
       mbar_init(&bar[B_KVE + s], 1);
-      mbar_init(&bar[B_SF + s], 1);
-      mbar_init(&bar[B_SE + s], 128);
     }
-    mbar_init(&bar[B_PF], 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[B_SF + s], 1);
+      mbar_init(&bar[B_SE + s], kSoftmaxThreads);
+      mbar_init(&bar[B_XF + s], 1);  // the local expect_tx; the bytes come from the peer
+      mbar_init(&bar[B_XE + s], 1);  // the peer helper's arrival
+      mbar_init(&bar[B_XR + s], kSoftmaxThreads);
+      mbar_init(&bar[B_RED + s], kSoftmaxThreads);
+    }
+    mbar_init(&bar[B_PF], kSoftmaxThreads);
     mbar_init(&bar[B_PE], 1);
-    mbar_init(&bar[B_XF], 128);
-    mbar_init(&bar[B_XE], 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -260,37 +311,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers exist before any remote arrive
   const uint32_t tmem = *tmem_base_slot;
 
-  uint8_t *sQ = smem + Lay::Q;
+  uint8_t *sQpe = smem + Lay::QPE;
   uint8_t *sKV = smem + Lay::KV;
   uint8_t *sP = smem + Lay::P;
   float *sX = reinterpret_cast<float *>(smem + Lay::X);
+  float *sRed = reinterpret_cast<float *>(smem + Lay::RED);
 
   int issued_kv = 0, issued_qk = 0, issued_pv = 0;  // for draining after an abort
 
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&qn_map);
       tma_prefetch_desc(&ckv_map);
       const uint64_t kv_policy = l2_policy_evict_first();
-      const uint64_t q_policy = l2_policy_evict_last();
-      mbar_arrive_expect_tx(&bar[B_Q], (uint32_t)nkb * kQBlock);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sQ + c * kQBlock, &qn_map, &bar[B_Q], 64 * (4 * (int)r + c), b * kHeads,
-                    q_policy);
-      if (r == 1) tma_load_2d(sQ + 4 * kQBlock, &qp_map, &bar[B_Q], 0, b * kHeads, q_policy);
-      for (int j = 0; j < num_tiles; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait_bounded(&bar[B_KVE + st], ((j >> 1) - 1) & 1, kWaitLimitNs)) {
+      if (r == 1) {
+        mbar_arrive_expect_tx(&bar[B_QPE], kQBlock);
+        tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 0, b * kHeads, l2_policy_evict_last());
+      }
+      for (int j = 0, st = 0, ph = 0; j < num_tiles; ++j) {
+        if (j >= kStages && !mbar_wait_bounded(&bar[B_KVE + st], ph ^ 1, kWaitLimitNs)) {
           dev_err |= DA_DEVERR_TIMEOUT;
           *abort_flag = 1;
           break;
         }
-        uint8_t *dst = sKV + st * 5 * kKvBlock;
+        uint8_t *dst = sKV + st * kKvStage;
         const int page = ids[j];
         if (page < 0) {
           // a skipped page: zeros instead of stale data (its scores are masked)
-          for (int i = 0; i < 5 * kKvBlock / 16; ++i)
+          for (int i = 0; i < nkb * kKvBlock / 16; ++i)
             reinterpret_cast<uint4 *>(dst)[i] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&bar[B_KVF + st], 0);
@@ -303,6 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d(dst + 4 * kKvBlock, &kpe_map, &bar[B_KVF + st], 0, page * kTok, kv_policy);
         }
         ++issued_kv;
+        if (++st == kStages) st = 0, ph ^= 1;
       }
     }
   } else if (warp == 1) {
@@ -310,23 +359,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, kTok, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
-      bool ok = mbar_wait_bounded(&bar[B_Q], 0, kWaitLimitNs);
+      bool ok = mbar_wait_bounded(&bar[B_QT], 0, kWaitLimitNs);
+      if (ok && r == 1) ok = mbar_wait_bounded(&bar[B_QPE], 0, kWaitLimitNs);
       auto issue_qk = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait_bounded(&bar[B_KVF + st], (j >> 1) & 1, kWaitLimitNs)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&bar[B_SE + st], ((j >> 1) - 1) & 1, kWaitLimitNs))
+        const int st = j % kStages, sb = j & 1;
+        if (!mbar_wait_bounded(&bar[B_KVF + st], (j / kStages) & 1, kWaitLimitNs)) return false;
+        if (j >= 2 && !mbar_wait_bounded(&bar[B_SE + sb], ((j >> 1) - 1) & 1, kWaitLimitNs))
           return false;
         tc_fence_after();
-        const uint32_t kv = smem_u32(sKV + st * 5 * kKvBlock);
-        const uint32_t q = smem_u32(sQ);
-        for (int c = 0; c < nkb; ++c)
+        const uint32_t kv = smem_u32(sKV + st * kKvStage);
+        const uint32_t d = tmem + kTmemS + 64 * sb;
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ss(tmem + kTmemS + 64 * st,
-                         umma_desc_sw128(q + c * kQBlock + kk * 32, 16, 1024),
+            umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
                          umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
                          (c | kk) != 0);
-        umma_commit(&bar[B_SF + st]);
+        if (r == 1) {
+          const uint32_t q = smem_u32(sQpe);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
+                         umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
+        }
+        umma_commit(&bar[B_SF + sb]);
         ++issued_qk;
         return true;
       };
@@ -336,14 +392,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (j + 1 < num_tiles && !(ok = issue_qk(j + 1))) break;
         if (!(ok = mbar_wait_bounded(&bar[B_PF], j & 1, kWaitLimitNs))) break;
         tc_fence_after();
-        const int st = j & 1;
-        const uint32_t v = smem_u32(sKV + st * 5 * kKvBlock);
+        const int st = j % kStages;
+        const uint32_t v = smem_u32(sKV + st * kKvStage);
         const uint32_t pa = smem_u32(sP);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
-                       umma_desc_sw128(v + kk * 2048, kKvBlock, 1024),
-                       idesc_pv, (j | kk) != 0);
+                       umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv, (j | kk) != 0);
         umma_commit(&bar[B_PE]);
         umma_commit(&bar[B_KVE + st]);
         ++issued_pv;
@@ -353,96 +408,185 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
     }
+  } else if (warp == 2) {
+    // ============================================================ exchange helper
+    // hands each exchange buffer back to the peer once this CTA has read it
+    // (only the buffers the peer still writes into are returned)
+    if (lane == 0) {
+      const uint32_t peer_xe0 = mapa_peer(smem_u32(&bar[B_XE]), peer);
+      for (int j = 0; j + 2 < num_tiles; ++j) {
+        if (!mbar_wait_bounded(&bar[B_XR + (j & 1)], (j >> 1) & 1, kWaitLimitNs)) {
+          dev_err |= DA_DEVERR_TIMEOUT;
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_remote(peer_xe0 + 8 * (j & 1));
+        if (*abort_flag) break;
+      }
+    }
   } else {
-    // ============================================================ softmax (one head row per thread)
-    const int quad = warp & 3;                  // TMEM lane quadrant of this warp
-    const int h = quad * 32 + lane;             // head row
+    // ============================================================ softmax
+    const int tid = threadIdx.x - 32 * kFirstSoftmaxWarp;  // 0..255
+    const int th = tid >> 7;                                // token half: 32 th .. 32 th + 31
+    const int quad = warp & 3;                              // TMEM lane quadrant of this warp
+    const int h = quad * 32 + lane;                         // head row
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t peer_x = mapa_peer(smem_u32(sX + h * kXStride), peer);
-    const uint32_t peer_xf = mapa_peer(smem_u32(&bar[B_XF]), peer);
-    const uint32_t peer_xe = mapa_peer(smem_u32(&bar[B_XE]), peer);
-    const float sscale = p.score_scale;
-    float m_ref = neg_inf(), l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < num_tiles; ++j) {
-      const int st = j & 1;
-      if (!(ok = mbar_wait_bounded(&bar[B_SF + st], (j >> 1) & 1, kWaitLimitNs))) break;
-      tc_fence_after();
-      float s[64];
+    // this CTA's q_nope half of row h into TMEM (columns kTmemQ + 64 th ...)
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 +
+                                                         256 * r + 128 * th);
+      uint4 qv[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int i = 0; i < 16; ++i) qv[i] = __ldg(src + i);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         float v[16];
-        tmem_ld16(tmem + lane_off + kTmemS + 64 * st + 16 * q, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[16 * q + i] = v[i];
+        for (int i = 0; i < 4; ++i) {
+          v[4 * i] = __uint_as_float(qv[4 * c + i].x);
+          v[4 * i + 1] = __uint_as_float(qv[4 * c + i].y);
+          v[4 * i + 2] = __uint_as_float(qv[4 * c + i].z);
+          v[4 * i + 3] = __uint_as_float(qv[4 * c + i].w);
+        }
+        tmem_st16(tmem + lane_off + kTmemQ + 64 * th + 16 * c, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar[B_QT]);
+    }
+    // exchange buffers: the float4 holding scores 4q..4q+3 of head h sits at
+    // [q][h], so one warp-wide store moves 512 contiguous bytes; this thread
+    // sends and receives q = 8 th .. 8 th + 7
+    const uint32_t peer_x = mapa_peer(smem_u32(sX + 4 * (8 * th * kHeads + h)), peer);
+    const uint32_t peer_xf0 = mapa_peer(smem_u32(&bar[B_XF]), peer);
+    const float4 *my_x = reinterpret_cast<const float4 *>(sX) + 8 * th * kHeads + h;
+    const float sscale = p.score_scale;
+    float m_ref = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
+    bool ok = true;
+    int x_next = 0;         // first tile whose peer scores have not been waited for
+    bool x_posted = false;  // whether its expect_tx has been posted
+    for (int j = 0; j < num_tiles; ++j) {
+      const int sb = j & 1;
+      if (!(ok = warp_wait(&bar[B_SF + sb], (j >> 1) & 1))) break;
+      tc_fence_after();
+      float s[32];
+      {
+        float v[16];
+        tmem_ld16(tmem + lane_off + kTmemS + 64 * sb + 32 * th, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = v[i];
+        tmem_ld16(tmem + lane_off + kTmemS + 64 * sb + 32 * th + 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[16 + i] = v[i];
       }
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar[B_SE + st]);
+      mbar_arrive(&bar[B_SE + sb]);
       // ---- exchange the partial scores with the peer CTA
-      if (j >= 1 && !(ok = mbar_wait_cluster_bounded(&bar[B_XE], (j - 1) & 1))) break;
+      if (j >= 2 && !(ok = warp_wait_cluster(&bar[B_XE + sb], ((j >> 1) - 1) & 1))) break;
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_cluster_v4(peer_x + 16 * q, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
-      mbar_arrive_remote(peer_xf);
-      if (!(ok = mbar_wait_cluster_bounded(&bar[B_XF], j & 1))) break;
-      const float4 *xr = reinterpret_cast<const float4 *>(sX + h * kXStride);
+      for (int i = 0; i < 8; ++i)
+        st_async_v4(peer_x + sb * kXBytes + i * kHeads * 16, s[4 * i], s[4 * i + 1], s[4 * i + 2],
+                    s[4 * i + 3], peer_xf0 + 8 * sb);
+      // this tile's phase of x_full completes once the peer's 32 KB have landed
+      if (tid == 0) mbar_arrive_expect_tx(&bar[B_XF + sb], kXBytes);
+      x_posted = true;
+      if (!(ok = warp_wait_cluster(&bar[B_XF + sb], (j >> 1) & 1))) break;
+      x_next = j + 1;
+      x_posted = false;
+      {
+        const float4 *xr = my_x + sb * (kXBytes / 16);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 o = xr[q];
-        s[4 * q] += o.x;
-        s[4 * q + 1] += o.y;
-        s[4 * q + 2] += o.z;
-        s[4 * q + 3] += o.w;
+        for (int i = 0; i < 8; ++i) {
+          const float4 o = xr[i * kHeads];
+          s[4 * i] += o.x;
+          s[4 * i + 1] += o.y;
+          s[4 * i + 2] += o.z;
+          s[4 * i + 3] += o.w;
+        }
       }
-      mbar_arrive_remote(peer_xe);
-      // ---- mask, lazy-rescaled online softmax (exp2 domain)
+      mbar_arrive(&bar[B_XR + sb]);
+      // ---- mask, row maximum over both token halves, lazy-rescaled online softmax
       const int tok0 = range_lo + j * kTok;
       const int nval = ids[j] < 0 ? 0 : min(kTok, range_hi - tok0);
-      float mt = neg_inf();
+      const int nmine = min(max(nval - 32 * th, 0), 32);  // valid tokens of this half
+      // raw scores past the valid tokens become a value that never wins the
+      // extreme below (uniform branch: ragged tiles only)
+      const float pad = sscale >= 0.f ? neg_inf() : -neg_inf();
+      if (nmine < 32) {
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        s[k] = k < nval ? s[k] * sscale : neg_inf();
-        mt = fmaxf(mt, s[k]);
+        for (int k = 0; k < 32; ++k)
+          if (k >= nmine) s[k] = pad;
       }
+      // the scaled maximum is the raw maximum (minimum for a negative scale)
+      // times the scale; four independent chains
+      float e4[4] = {s[0], s[1], s[2], s[3]};
+      if (sscale >= 0.f) {
+#pragma unroll
+        for (int k = 4; k < 32; ++k) e4[k & 3] = fmaxf(e4[k & 3], s[k]);
+      } else {
+#pragma unroll
+        for (int k = 4; k < 32; ++k) e4[k & 3] = fminf(e4[k & 3], s[k]);
+      }
+      float ext = sscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
+                                : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
+      {
+        float *red = sRed + sb * 2 * kHeads;
+        red[th * kHeads + h] = ext;
+        mbar_arrive(&bar[B_RED + sb]);
+        if (!(ok = warp_wait(&bar[B_RED + sb], (j >> 1) & 1))) break;
+        const float other = red[(th ^ 1) * kHeads + h];
+        ext = sscale >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
+      }
+      const float mt = nval > 0 ? ext * sscale : neg_inf();
       const bool need = mt > m_ref + kRescaleThreshold || (m_ref == neg_inf() && mt != neg_inf());
       const float alpha = need ? ex2(m_ref - mt) : 1.f;
       if (need) m_ref = mt;
-      float psum = 0.f;
-      uint32_t pk[32];
+      // p = 2^(scale * s - m_ref), 0 past the valid tokens and while no score is valid
+      const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[16];
+      auto exp_pack = [&](auto ragged) {
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        const float p0 = m_ref == neg_inf() ? 0.f : ex2(s[k] - m_ref);
-        const float p1 = m_ref == neg_inf() ? 0.f : ex2(s[k + 1] - m_ref);
-        psum += p0 + p1;
-        pk[k / 2] = pack_bf16(p0, p1);
-      }
-      l = l * alpha + psum;
+        for (int k = 0; k < 32; k += 2) {
+          float t0 = fmaf(s[k], sscale, neg_m), t1 = fmaf(s[k + 1], sscale, neg_m);
+          if (decltype(ragged)::value) {
+            t0 = k < nmine ? t0 : neg_inf();
+            t1 = k + 1 < nmine ? t1 : neg_inf();
+          }
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          ps4[(k >> 1) & 3] += p0 + p1;
+          pk[k / 2] = pack_bf16(p0, p1);
+        }
+      };
+      if (nmine < 32) exp_pack(std::true_type{});
+      else exp_pack(std::false_type{});
+      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       // ---- PV of the previous tile must be done before O or P change
-      if (j >= 1 && !(ok = mbar_wait_bounded(&bar[B_PE], (j - 1) & 1, kWaitLimitNs))) break;
+      if (j >= 1 && !(ok = warp_wait(&bar[B_PE], (j - 1) & 1))) break;
       tc_fence_after();
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
-        for (int c = 0; c < 256; c += 16) {
+        // this thread's row, value columns 128 th .. 128 th + 127
+        for (int c = 0; c < 128; c += 16) {
           float v[16];
-          tmem_ld16(tmem + lane_off + kTmemO + c, v);
+          tmem_ld16(tmem + lane_off + kTmemO + 128 * th + c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          tmem_st16(tmem + lane_off + kTmemO + c, v);
+          tmem_st16(tmem + lane_off + kTmemO + 128 * th + c, v);
         }
         tmem_wait_st();
       }
-      // P row h (bf16, 64 tokens = 128 bytes), 128B-swizzled K-major A operand
+      // P row h, tokens 32 th .. 32 th + 31 (64 bytes), 128B-swizzled K-major A operand
       uint8_t *prow = sP + h * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4 *>(prow + (((4 * th + c) ^ (h & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (nval < kTok) {
-        // rows past the valid tokens may hold anything: zero their value part
-        uint8_t *kv = sKV + st * 5 * kKvBlock;
-        const int t_id = threadIdx.x - 64;  // 0..127
-        for (int i = t_id; i < (kTok - nval) * 4 * 8; i += 128) {
+        // value rows past the valid tokens may hold anything: zero them
+        uint8_t *kv = sKV + (j % kStages) * kKvStage;
+        for (int i = tid; i < (kTok - nval) * 4 * 8; i += kSoftmaxThreads) {
           const int t = nval + i / 32, blk = (i / 8) % 4, c = i % 8;
           *reinterpret_cast<uint4 *>(kv + blk * kKvBlock + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -454,32 +598,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
       *abort_flag = 1;
-    }
-    // ---- epilogue: O_r / l for this CTA's value half
-    if (ok && mbar_wait_bounded(&bar[B_PE], (num_tiles - 1) & 1, kWaitLimitNs)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : neg_inf();
-      for (int c = 0; c < 256; c += 16) {
-        float v[16];
-        tmem_ld16(tmem + lane_off + kTmemO + c, v);
-        tmem_wait_ld();
-        if (p.write_final) {
-          __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
-              p.out + ((int64_t)b * kHeads + h) * 512 + r * 256 + c);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) dst[i] = __floats2bfloat162_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
-        } else {
-          float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + r * 256 + c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+      // the peer may still be storing the scores of tiles x_next and x_next + 1
+      // into this CTA's buffers (it cannot start a later one): let them land
+      if (tid == 0) {
+        for (int t = x_next; t < min(x_next + 2, num_tiles); ++t) {
+          if (!(t == x_next && x_posted)) mbar_arrive_expect_tx(&bar[B_XF + (t & 1)], kXBytes);
+          mbar_wait_cluster_bounded(&bar[B_XF + (t & 1)], (t >> 1) & 1);
         }
       }
-      if (p.write_final) {
-        if (r == 0 && p.lse) p.lse[(int64_t)b * kHeads + h] = lse;
+    }
+    // ---- epilogue: O_r / l for this CTA's value half
+    if (ok && warp_wait(&bar[B_PE], (num_tiles - 1) & 1)) {
+      tc_fence_after();
+      // the row sum over both token halves, added in the same order by both
+      const int rb = num_tiles & 1;
+      float *red = sRed + rb * 2 * kHeads;
+      red[th * kHeads + h] = l;
+      mbar_arrive(&bar[B_RED + rb]);
+      if (warp_wait(&bar[B_RED + rb], (num_tiles >> 1) & 1)) {
+        const float lt = red[h] + red[kHeads + h];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float lse = lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : neg_inf();
+        for (int c = 0; c < 128; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_off + kTmemO + 128 * th + c, v);
+          tmem_wait_ld();
+          const int col = r * 256 + 128 * th + c;
+          if (p.write_final) {
+            __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
+                p.out + ((int64_t)b * kHeads + h) * 512 + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = __floats2bfloat162_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+          }
+        }
+        if (th == 0) {
+          if (p.write_final) {
+            if (r == 0 && p.lse) p.lse[(int64_t)b * kHeads + h] = lse;
+          } else {
+            p.lse_part[(slot * 2 + r) * kHeads + h] = lse;
+          }
+        }
       } else {
-        p.lse_part[(slot * 2 + r) * kHeads + h] = lse;
+        dev_err |= DA_DEVERR_TIMEOUT;
+        *abort_flag = 1;
       }
     } else if (ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
@@ -491,8 +657,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (*abort_flag) {
     // drain what is still in flight (bounded), so nothing lands after exit
     if (warp == 0 && lane == 0) {
-      for (int j = max(0, issued_kv - 2); j < issued_kv; ++j)
-        mbar_wait_bounded(&bar[B_KVF + (j & 1)], (j >> 1) & 1, kWaitLimitNs);
+      for (int j = max(0, issued_kv - kStages); j < issued_kv; ++j)
+        mbar_wait_bounded(&bar[B_KVF + j % kStages], (j / kStages) & 1, kWaitLimitNs);
     }
     if (warp == 1 && lane == 0) {
       if (issued_qk > 0)
@@ -522,10 +688,10 @@ cudaError_t mla_prepare(int /*device*/) {
                               Lay::TOTAL);
 }
 
-cudaError_t launch_mla(const CUtensorMap &qn_map, const CUtensorMap &qp_map,
-                       const CUtensorMap &ckv_map, const CUtensorMap &kpe_map,
-                       const MlaParams &p, dim3 grid, cudaStream_t stream) {
-  mla_split_kernel<<<grid, kThreads, Lay::TOTAL, stream>>>(qn_map, qp_map, ckv_map, kpe_map, p);
+cudaError_t launch_mla(const CUtensorMap &qp_map, const CUtensorMap &ckv_map,
+                       const CUtensorMap &kpe_map, const MlaParams &p, dim3 grid,
+                       cudaStream_t stream) {
+  mla_split_kernel<<<grid, kThreads, Lay::TOTAL, stream>>>(qp_map, ckv_map, kpe_map, p);
   return cudaGetLastError();
 }
 

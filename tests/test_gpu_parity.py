@@ -259,6 +259,27 @@ def test_mla_small(splits):
     assert_parity(out, lse, ref_out, ref_lse, what=f"MLA S={splits}")
 
 
+@pytest.mark.parametrize("scale", [-0.07, 0.0])
+def test_mla_negative_and_zero_scale(scale):
+    # a negative scale turns the running maximum into a minimum of the raw
+    # scores; a zero scale gives uniform weights over exactly the valid tokens
+    w = W.make_mla(name="mla_scale", batch=3, seq_lens=[130, 1, 777], scale=scale, seed=48)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=2)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"MLA scale={scale}")
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0])
+def test_gqa_negative_and_zero_scale(scale):
+    w = W.make_gqa(name="gqa_scale", batch=3, num_q_heads=16, num_kv_heads=4, seq_lens=[130, 1, 777],
+                   layout="paged", page_size=16, scale=scale, seed=49)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"GQA scale={scale}")
+
+
 def test_mla_empty_row_and_auto_plan():
     w = W.make_mla(name="mla0", batch=3, seq_lens=[0, 2500, 700], seed=45)
     out, lse, flags, eng = run_gpu(w)
