@@ -29,15 +29,18 @@
 //
 // Warp roles per CTA (352 threads): warp 0 = TMA producer (three KV stages),
 // warp 1 = MMA issuer (and TMEM owner), warp 2 = exchange helper, warps 3-10 =
-// softmax. Two softmax warps share each TMEM lane quadrant: thread (h, t) owns
-// head row h and tokens 32t..32t+31 of every tile; the pair agrees on the row
-// maximum through shared memory. The score exchange is double-buffered and
-// uses st.async, whose bytes complete on the receiver's mbarrier, so the
-// sender never waits for the remote stores; the helper warp returns each
-// buffer to the peer (a cluster-scope release) off the softmax warps' path.
-// The online softmax rescales O lazily: only when a row's maximum grows by more
-// than 2^8 is the TMEM accumulator rescaled (exact: O and l always share the
-// same reference maximum).
+// softmax in two groups of four warps (one warp per TMEM lane quadrant, one
+// thread per head row). Group g takes the tiles j = g (mod 2) with their own
+// score buffer and exchange buffer, so one group's exchange and exponentials
+// overlap the other's; the only hand-over between consecutive tiles is the
+// running maximum of each row (shared memory + mbarrier), and each group keeps
+// its part of the row sum relative to the maximum of its own latest tile.
+// The score exchange uses st.async, whose bytes complete on the receiver's
+// mbarrier, so the sender never waits for the remote stores; the helper warp
+// returns each buffer to the peer (a cluster-scope release) off the softmax
+// warps' path. The online softmax rescales O lazily: only when a row's maximum
+// grows by more than 2^8 is the TMEM accumulator rescaled (exact: O is always
+// relative to the running maximum, and so is every P tile).
 #include <type_traits>
 
 #include "internal.h"
@@ -48,8 +51,9 @@ namespace {
 
 constexpr int kTok = 64;          // tokens per tile (= page)
 constexpr int kHeads = 128;
-constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxWarps = 8;                       // two groups of four
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kGroupThreads = kSoftmaxThreads / 2;      // one thread per head row
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kThreads = 32 * (kFirstSoftmaxWarp + kSoftmaxWarps);
 constexpr int kStages = 3;                // KV ring depth
@@ -69,9 +73,10 @@ struct Lay {
   static constexpr int KV = QPE + kQBlock;                   // kStages x 40 KB
   static constexpr int P = KV + kStages * kKvStage;          // 16 KB
   static constexpr int X = P + kQBlock;                      // 2 x [16][128] float4
-  static constexpr int RED = X + 2 * kXBytes;                // [2][2][128] fp32
-  static constexpr int BAR = RED + 2 * 2 * kHeads * 4;
-  static constexpr int NBAR = 22;
+  static constexpr int MR = X + 2 * kXBytes;                 // [2 groups][128] running max
+  static constexpr int FIN = MR + 2 * kHeads * 4;            // [2 groups][l, m][128]
+  static constexpr int BAR = FIN + 2 * 2 * kHeads * 4;
+  static constexpr int NBAR = 24;
   static constexpr int FLAGS = BAR + NBAR * 8;               // tmem base, abort, last
   static constexpr int IDS = FLAGS + 16;
   static constexpr int TOTAL = IDS + kGqaMaxIds * 4 + 1024;  // + alignment slack
@@ -87,8 +92,9 @@ enum {
   B_PE = 13,   // PV MMA done
   B_XF = 14,   // [2] peer scores landed (local expect_tx + the peer's bytes)
   B_XE = 16,   // [2] the peer has read what this CTA sent into its buffer
-  B_XR = 18,   // [2] this CTA's softmax threads have read the buffer
-  B_RED = 20,  // [2] row-maximum / row-sum exchange between the two token halves
+  B_XR = 18,   // [2] this CTA's softmax group has read the buffer
+  B_MRF = 20,  // [2] group g has published the running maximum of its latest tile
+  B_FIN = 22,  // both groups have published their row sums
 };
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -140,6 +146,19 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// Non-blocking check of a phase (the MMA issuer polls several barriers).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Warp-uniform outcomes of bounded waits (the lanes then stay converged for
@@ -271,19 +290,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar[B_QPE], 1);
     mbar_init(&bar[B_QT], kSoftmaxThreads);
+    mbar_init(&bar[B_FIN], kSoftmaxThreads);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar[B_KVF + s], 1);
       mbar_init(&bar[B_KVE + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar[B_SF + s], 1);
-      mbar_init(&bar[B_SE + s], kSoftmaxThreads);
+      mbar_init(&bar[B_SE + s], kGroupThreads);
       mbar_init(&bar[B_XF + s], 1);  // the local expect_tx; the bytes come from the peer
       mbar_init(&bar[B_XE + s], 1);  // the peer helper's arrival
-      mbar_init(&bar[B_XR + s], kSoftmaxThreads);
-      mbar_init(&bar[B_RED + s], kSoftmaxThreads);
+      mbar_init(&bar[B_XR + s], kGroupThreads);
+      mbar_init(&bar[B_MRF + s], kGroupThreads);
     }
-    mbar_init(&bar[B_PF], kSoftmaxThreads);
+    mbar_init(&bar[B_PF], kGroupThreads);
     mbar_init(&bar[B_PE], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -315,7 +335,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t *sKV = smem + Lay::KV;
   uint8_t *sP = smem + Lay::P;
   float *sX = reinterpret_cast<float *>(smem + Lay::X);
-  float *sRed = reinterpret_cast<float *>(smem + Lay::RED);
+  float *sMr = reinterpret_cast<float *>(smem + Lay::MR);
+  float *sFin = reinterpret_cast<float *>(smem + Lay::FIN);
 
   int issued_kv = 0, issued_qk = 0, issued_pv = 0;  // for draining after an abort
 
@@ -361,47 +382,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
       bool ok = mbar_wait_bounded(&bar[B_QT], 0, kWaitLimitNs);
       if (ok && r == 1) ok = mbar_wait_bounded(&bar[B_QPE], 0, kWaitLimitNs);
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % kStages, sb = j & 1;
-        if (!mbar_wait_bounded(&bar[B_KVF + st], (j / kStages) & 1, kWaitLimitNs)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&bar[B_SE + sb], ((j >> 1) - 1) & 1, kWaitLimitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t kv = smem_u32(sKV + st * kKvStage);
-        const uint32_t d = tmem + kTmemS + 64 * sb;
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
-                         umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
-                         (c | kk) != 0);
-        if (r == 1) {
-          const uint32_t q = smem_u32(sQpe);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
-                         umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
-        }
-        umma_commit(&bar[B_SF + sb]);
-        ++issued_qk;
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int j = 0; ok && j < num_tiles; ++j) {
+      // Scores of tile k need its KV stage and the score buffer read back from
+      // tile k - 2; PV of tile k needs its P. Neither waits for the other: the
+      // issuer polls both and issues what is ready, so the next scores are in
+      // flight while a softmax group still works on the previous tile. (No
+      // barrier polled here can run a phase ahead of the tile being tested.)
+      uint64_t idle_since = 0;
+      while (ok && issued_pv < num_tiles) {
         if (*abort_flag) break;
-        if (j + 1 < num_tiles && !(ok = issue_qk(j + 1))) break;
-        if (!(ok = mbar_wait_bounded(&bar[B_PF], j & 1, kWaitLimitNs))) break;
-        tc_fence_after();
-        const int st = j % kStages;
-        const uint32_t v = smem_u32(sKV + st * kKvStage);
-        const uint32_t pa = smem_u32(sP);
+        bool progress = false;
+        const int k = issued_qk;
+        if (k < num_tiles && mbar_test(&bar[B_KVF + k % kStages], (k / kStages) & 1) &&
+            (k < 2 || mbar_test(&bar[B_SE + (k & 1)], ((k >> 1) - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
+          const uint32_t d = tmem + kTmemS + 64 * (k & 1);
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
-                       umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv, (j | kk) != 0);
-        umma_commit(&bar[B_PE]);
-        umma_commit(&bar[B_KVE + st]);
-        ++issued_pv;
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
+                           umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
+                           (c | kk) != 0);
+          if (r == 1) {
+            const uint32_t q = smem_u32(sQpe);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
+                           umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
+          }
+          umma_commit(&bar[B_SF + (k & 1)]);
+          ++issued_qk;
+          progress = true;
+        }
+        const int j = issued_pv;
+        if (j < issued_qk && mbar_test(&bar[B_PF], j & 1)) {
+          tc_fence_after();
+          const int st = j % kStages;
+          const uint32_t v = smem_u32(sKV + st * kKvStage);
+          const uint32_t pa = smem_u32(sP);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
+                         umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv, (j | kk) != 0);
+          umma_commit(&bar[B_PE]);
+          umma_commit(&bar[B_KVE + st]);
+          ++issued_pv;
+          progress = true;
+        }
+        if (progress) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (idle_since == 0) idle_since = now;
+          else if (now - idle_since > kWaitLimitNs) ok = false;
+        }
       }
       if (!ok) {
         dev_err |= DA_DEVERR_TIMEOUT;
@@ -427,14 +461,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ============================================================ softmax
     const int tid = threadIdx.x - 32 * kFirstSoftmaxWarp;  // 0..255
-    const int th = tid >> 7;                                // token half: 32 th .. 32 th + 31
+    const int g = tid >> 7;                                 // group: tiles j = g (mod 2)
     const int quad = warp & 3;                              // TMEM lane quadrant of this warp
     const int h = quad * 32 + lane;                         // head row
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // this CTA's q_nope half of row h into TMEM (columns kTmemQ + 64 th ...)
+    // this CTA's q_nope half of row h into TMEM: group g stores columns
+    // kTmemQ + 64 g .. + 63 (values 128 g .. 128 g + 127 of the half)
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 +
-                                                         256 * r + 128 * th);
+                                                         256 * r + 128 * g);
       uint4 qv[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) qv[i] = __ldg(src + i);
@@ -448,146 +483,143 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           v[4 * i + 2] = __uint_as_float(qv[4 * c + i].z);
           v[4 * i + 3] = __uint_as_float(qv[4 * c + i].w);
         }
-        tmem_st16(tmem + lane_off + kTmemQ + 64 * th + 16 * c, v);
+        tmem_st16(tmem + lane_off + kTmemQ + 64 * g + 16 * c, v);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar[B_QT]);
     }
-    // exchange buffers: the float4 holding scores 4q..4q+3 of head h sits at
-    // [q][h], so one warp-wide store moves 512 contiguous bytes; this thread
-    // sends and receives q = 8 th .. 8 th + 7
-    const uint32_t peer_x = mapa_peer(smem_u32(sX + 4 * (8 * th * kHeads + h)), peer);
-    const uint32_t peer_xf0 = mapa_peer(smem_u32(&bar[B_XF]), peer);
-    const float4 *my_x = reinterpret_cast<const float4 *>(sX) + 8 * th * kHeads + h;
+    // exchange buffer g: the float4 holding scores 4q..4q+3 of head h sits at
+    // [q][h], so one warp-wide store moves 512 contiguous bytes
+    const uint32_t peer_x = mapa_peer(smem_u32(sX + g * (kXBytes / 4) + 4 * h), peer);
+    const uint32_t peer_xf = mapa_peer(smem_u32(&bar[B_XF + g]), peer);
+    const float4 *my_x = reinterpret_cast<const float4 *>(sX + g * (kXBytes / 4)) + h;
     const float sscale = p.score_scale;
-    float m_ref = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
+    // m_last: running maximum after this group's latest tile (scaled, log2
+    // units); l: this group's part of the row sum, relative to m_last
+    float m_last = neg_inf(), l = 0.f;
     bool ok = true;
-    int x_next = 0;         // first tile whose peer scores have not been waited for
+    int x_next = g;         // first tile of this group whose peer scores have not been waited for
     bool x_posted = false;  // whether its expect_tx has been posted
-    for (int j = 0; j < num_tiles; ++j) {
-      const int sb = j & 1;
-      if (!(ok = warp_wait(&bar[B_SF + sb], (j >> 1) & 1))) break;
+    for (int j = g; j < num_tiles; j += 2) {
+      const int i = j >> 1;  // this group's tile counter (phase of its barriers)
+      if (!(ok = warp_wait(&bar[B_SF + g], i & 1))) break;
       tc_fence_after();
-      float s[32];
-      {
+      float s[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
         float v[16];
-        tmem_ld16(tmem + lane_off + kTmemS + 64 * sb + 32 * th, v);
+        tmem_ld16(tmem + lane_off + kTmemS + 64 * g + 16 * q, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) s[i] = v[i];
-        tmem_ld16(tmem + lane_off + kTmemS + 64 * sb + 32 * th + 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s[16 + i] = v[i];
+        for (int e = 0; e < 16; ++e) s[16 * q + e] = v[e];
       }
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar[B_SE + sb]);
+      mbar_arrive(&bar[B_SE + g]);
       // ---- exchange the partial scores with the peer CTA
-      if (j >= 2 && !(ok = warp_wait_cluster(&bar[B_XE + sb], ((j >> 1) - 1) & 1))) break;
+      if (i >= 1 && !(ok = warp_wait_cluster(&bar[B_XE + g], (i - 1) & 1))) break;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        st_async_v4(peer_x + sb * kXBytes + i * kHeads * 16, s[4 * i], s[4 * i + 1], s[4 * i + 2],
-                    s[4 * i + 3], peer_xf0 + 8 * sb);
+      for (int q = 0; q < 16; ++q)
+        st_async_v4(peer_x + q * kHeads * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3],
+                    peer_xf);
       // this tile's phase of x_full completes once the peer's 32 KB have landed
-      if (tid == 0) mbar_arrive_expect_tx(&bar[B_XF + sb], kXBytes);
+      if (tid == kGroupThreads * g) mbar_arrive_expect_tx(&bar[B_XF + g], kXBytes);
       x_posted = true;
-      if (!(ok = warp_wait_cluster(&bar[B_XF + sb], (j >> 1) & 1))) break;
-      x_next = j + 1;
+      if (!(ok = warp_wait_cluster(&bar[B_XF + g], i & 1))) break;
+      x_next = j + 2;
       x_posted = false;
-      {
-        const float4 *xr = my_x + sb * (kXBytes / 16);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 o = xr[i * kHeads];
-          s[4 * i] += o.x;
-          s[4 * i + 1] += o.y;
-          s[4 * i + 2] += o.z;
-          s[4 * i + 3] += o.w;
-        }
+      for (int q = 0; q < 16; ++q) {
+        const float4 o = my_x[q * kHeads];
+        s[4 * q] += o.x;
+        s[4 * q + 1] += o.y;
+        s[4 * q + 2] += o.z;
+        s[4 * q + 3] += o.w;
       }
-      mbar_arrive(&bar[B_XR + sb]);
-      // ---- mask, row maximum over both token halves, lazy-rescaled online softmax
+      mbar_arrive(&bar[B_XR + g]);
+      // ---- mask and tile maximum
       const int tok0 = range_lo + j * kTok;
       const int nval = ids[j] < 0 ? 0 : min(kTok, range_hi - tok0);
-      const int nmine = min(max(nval - 32 * th, 0), 32);  // valid tokens of this half
       // raw scores past the valid tokens become a value that never wins the
       // extreme below (uniform branch: ragged tiles only)
       const float pad = sscale >= 0.f ? neg_inf() : -neg_inf();
-      if (nmine < 32) {
+      if (nval < kTok) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (k >= nmine) s[k] = pad;
+        for (int k = 0; k < 64; ++k)
+          if (k >= nval) s[k] = pad;
       }
       // the scaled maximum is the raw maximum (minimum for a negative scale)
       // times the scale; four independent chains
       float e4[4] = {s[0], s[1], s[2], s[3]};
       if (sscale >= 0.f) {
 #pragma unroll
-        for (int k = 4; k < 32; ++k) e4[k & 3] = fmaxf(e4[k & 3], s[k]);
+        for (int k = 4; k < 64; ++k) e4[k & 3] = fmaxf(e4[k & 3], s[k]);
       } else {
 #pragma unroll
-        for (int k = 4; k < 32; ++k) e4[k & 3] = fminf(e4[k & 3], s[k]);
+        for (int k = 4; k < 64; ++k) e4[k & 3] = fminf(e4[k & 3], s[k]);
       }
-      float ext = sscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
-                                : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
-      {
-        float *red = sRed + sb * 2 * kHeads;
-        red[th * kHeads + h] = ext;
-        mbar_arrive(&bar[B_RED + sb]);
-        if (!(ok = warp_wait(&bar[B_RED + sb], (j >> 1) & 1))) break;
-        const float other = red[(th ^ 1) * kHeads + h];
-        ext = sscale >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
-      }
+      const float ext = sscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
+                                      : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
       const float mt = nval > 0 ? ext * sscale : neg_inf();
-      const bool need = mt > m_ref + kRescaleThreshold || (m_ref == neg_inf() && mt != neg_inf());
-      const float alpha = need ? ex2(m_ref - mt) : 1.f;
-      if (need) m_ref = mt;
-      // p = 2^(scale * s - m_ref), 0 past the valid tokens and while no score is valid
-      const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
+      // ---- running maximum: that of tile j - 1 (the other group) grows lazily
+      float m_prev = neg_inf();
+      if (j >= 1) {
+        const int jp = j - 1;
+        if (!(ok = warp_wait(&bar[B_MRF + (jp & 1)], (jp >> 1) & 1))) break;
+        m_prev = sMr[(jp & 1) * kHeads + h];
+      }
+      const bool need = mt > m_prev + kRescaleThreshold || (m_prev == neg_inf() && mt != neg_inf());
+      const float m_new = need ? mt : m_prev;
+      sMr[g * kHeads + h] = m_new;
+      mbar_arrive(&bar[B_MRF + g]);
+      // p = 2^(scale * s - m_new), 0 past the valid tokens and while no score is valid
+      const float neg_m = m_new == neg_inf() ? 0.f : -m_new;
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[16];
+      uint32_t pk[32];
       auto exp_pack = [&](auto ragged) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
+        for (int k = 0; k < 64; k += 2) {
           float t0 = fmaf(s[k], sscale, neg_m), t1 = fmaf(s[k + 1], sscale, neg_m);
           if (decltype(ragged)::value) {
-            t0 = k < nmine ? t0 : neg_inf();
-            t1 = k + 1 < nmine ? t1 : neg_inf();
+            t0 = k < nval ? t0 : neg_inf();
+            t1 = k + 1 < nval ? t1 : neg_inf();
           }
           const float p0 = ex2(t0), p1 = ex2(t1);
           ps4[(k >> 1) & 3] += p0 + p1;
           pk[k / 2] = pack_bf16(p0, p1);
         }
       };
-      if (nmine < 32) exp_pack(std::true_type{});
+      if (nval < kTok) exp_pack(std::true_type{});
       else exp_pack(std::false_type{});
-      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+      if (l != 0.f && m_new != m_last) l *= ex2(m_last - m_new);
+      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      m_last = m_new;
       // ---- PV of the previous tile must be done before O or P change
       if (j >= 1 && !(ok = warp_wait(&bar[B_PE], (j - 1) & 1))) break;
       tc_fence_after();
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
-        // this thread's row, value columns 128 th .. 128 th + 127
-        for (int c = 0; c < 128; c += 16) {
+        const float alpha = need ? ex2(m_prev - m_new) : 1.f;  // 0 when m_prev is -inf
+        for (int c = 0; c < 256; c += 16) {
           float v[16];
-          tmem_ld16(tmem + lane_off + kTmemO + 128 * th + c, v);
+          tmem_ld16(tmem + lane_off + kTmemO + c, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          tmem_st16(tmem + lane_off + kTmemO + 128 * th + c, v);
+          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          tmem_st16(tmem + lane_off + kTmemO + c, v);
         }
         tmem_wait_st();
       }
-      // P row h, tokens 32 th .. 32 th + 31 (64 bytes), 128B-swizzled K-major A operand
+      // P row h (bf16, 64 tokens = 128 bytes), 128B-swizzled K-major A operand
       uint8_t *prow = sP + h * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4 *>(prow + (((4 * th + c) ^ (h & 7)) << 4)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (nval < kTok) {
         // value rows past the valid tokens may hold anything: zero them
         uint8_t *kv = sKV + (j % kStages) * kKvStage;
-        for (int i = tid; i < (kTok - nval) * 4 * 8; i += kSoftmaxThreads) {
-          const int t = nval + i / 32, blk = (i / 8) % 4, c = i % 8;
+        for (int e = tid - kGroupThreads * g; e < (kTok - nval) * 4 * 8; e += kGroupThreads) {
+          const int t = nval + e / 32, blk = (e / 8) % 4, c = e % 8;
           *reinterpret_cast<uint4 *>(kv + blk * kKvBlock + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
@@ -598,45 +630,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
       *abort_flag = 1;
-      // the peer may still be storing the scores of tiles x_next and x_next + 1
-      // into this CTA's buffers (it cannot start a later one): let them land
-      if (tid == 0) {
-        for (int t = x_next; t < min(x_next + 2, num_tiles); ++t) {
-          if (!(t == x_next && x_posted)) mbar_arrive_expect_tx(&bar[B_XF + (t & 1)], kXBytes);
-          mbar_wait_cluster_bounded(&bar[B_XF + (t & 1)], (t >> 1) & 1);
-        }
+      // the peer may still be storing the scores of tile x_next into this
+      // group's buffer (it cannot start the group's next one): let them land
+      if (tid == kGroupThreads * g && x_next < num_tiles) {
+        if (!x_posted) mbar_arrive_expect_tx(&bar[B_XF + g], kXBytes);
+        mbar_wait_cluster_bounded(&bar[B_XF + g], (x_next >> 1) & 1);
       }
     }
-    // ---- epilogue: O_r / l for this CTA's value half
+    // ---- epilogue: O_r / l for this CTA's value half (group g: columns 128 g ..)
     if (ok && warp_wait(&bar[B_PE], (num_tiles - 1) & 1)) {
       tc_fence_after();
-      // the row sum over both token halves, added in the same order by both
-      const int rb = num_tiles & 1;
-      float *red = sRed + rb * 2 * kHeads;
-      red[th * kHeads + h] = l;
-      mbar_arrive(&bar[B_RED + rb]);
-      if (warp_wait(&bar[B_RED + rb], (num_tiles >> 1) & 1)) {
-        const float lt = red[h] + red[kHeads + h];
+      sFin[g * 2 * kHeads + h] = l;
+      sFin[g * 2 * kHeads + kHeads + h] = m_last;
+      mbar_arrive(&bar[B_FIN]);
+      if (warp_wait(&bar[B_FIN], 0)) {
+        // both groups' sums relative to the final maximum, added in one order
+        const float l0 = sFin[h], m0 = sFin[kHeads + h];
+        const float l1 = sFin[2 * kHeads + h], m1 = sFin[3 * kHeads + h];
+        const float mf = fmaxf(m0, m1);
+        const float lt = (l0 != 0.f ? l0 * ex2(m0 - mf) : 0.f) + (l1 != 0.f ? l1 * ex2(m1 - mf) : 0.f);
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float lse = lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : neg_inf();
+        const float lse = lt > 0.f ? (mf + __log2f(lt)) * 0.69314718055994531f : neg_inf();
         for (int c = 0; c < 128; c += 16) {
           float v[16];
-          tmem_ld16(tmem + lane_off + kTmemO + 128 * th + c, v);
+          tmem_ld16(tmem + lane_off + kTmemO + 128 * g + c, v);
           tmem_wait_ld();
-          const int col = r * 256 + 128 * th + c;
+          const int col = r * 256 + 128 * g + c;
           if (p.write_final) {
             __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
                 p.out + ((int64_t)b * kHeads + h) * 512 + col);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = __floats2bfloat162_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
+            for (int e = 0; e < 8; ++e) dst[e] = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
           } else {
             float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + col);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
           }
         }
-        if (th == 0) {
+        if (g == 0) {
           if (p.write_final) {
             if (r == 0 && p.lse) p.lse[(int64_t)b * kHeads + h] = lse;
           } else {
