@@ -217,8 +217,8 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.q_pe = reinterpret_cast<const __nv_bfloat16 *>(a->q_pe);
   mp.block_table = a->block_table;
   mp.seq_lens = a->seq_lens;
-  mp.o_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_o_offset);
-  mp.lse_part = pl.writes_final ? nullptr : reinterpret_cast<float *>(ws + pl.partial_lse_offset);
+  mp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);
+  mp.lse_part = reinterpret_cast<float *>(ws + pl.partial_lse_offset);
   mp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
   mp.lse = a->lse;
   mp.err = reinterpret_cast<uint32_t *>(ws);
@@ -228,10 +228,7 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.max_pages = p.max_pages_per_seq;
   mp.num_pages = p.num_pages;
   mp.capacity = p.max_pages_per_seq * p.page_size;
-  mp.chunk = pl.chunk_tokens;
-  mp.num_splits = pl.num_splits;
-  mp.write_final = pl.writes_final;
-  const dim3 grid(pl.grid_x, 1, pl.grid_z);
+  const dim3 grid(pl.grid_x, 1, 1);
   cudaError_t e = da::launch_mla(ctx->qpemap, ctx->kmap, ctx->vmap, mp, grid, stream);
   if (e == cudaErrorNotSupported) return DA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DA_ERR_CUDA;

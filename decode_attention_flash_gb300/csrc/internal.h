@@ -54,15 +54,15 @@ struct MlaParams {
   const __nv_bfloat16 *q_pe;    // [B][128][64]
   const int32_t *block_table;
   const int32_t *seq_lens;
-  float *o_part;                // [B][S][128][512] (rank r writes columns 256r..256r+255)
-  float *lse_part;              // [B][S][2][128]   (one copy per rank)
+  float *o_part;                // [B + clusters][128][512]: slot b + cluster of a row segment
+                                // (rank r writes columns 256r..256r+255)
+  float *lse_part;              // [B + clusters][2][128] (one copy per rank)
   __nv_bfloat16 *out;           // [B][128][512]
   float *lse;
   uint32_t *err;
-  uint32_t *counters;
+  uint32_t *counters;           // [B][2]: finished segments per (row, rank)
   float score_scale;
   int32_t batch, max_pages, num_pages, capacity;
-  int32_t chunk, num_splits, write_final;
 };
 
 // Kernel launchers (return the launch error).
@@ -79,7 +79,6 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t mla_prepare(int device);
 int mla_smem_bytes();
 int mla_threads();
-int mla_max_splits();
 cudaError_t launch_mla(const CUtensorMap &qp_map, const CUtensorMap &ckv_map,
                        const CUtensorMap &kpe_map, const MlaParams &p, dim3 grid,
                        cudaStream_t stream);

@@ -9,8 +9,8 @@
 // normalised O plus LSE and an LSE-weighted merge (as the GQA kernels do).
 //
 // GB300 design. A 128-head x 512-wide fp32 output accumulator fills all 512
-// columns of one SM's tensor memory, so one (b, split) is handled by a CLUSTER
-// OF TWO CTAs, each owning half of the value dimension (256 TMEM columns of O):
+// columns of one SM's tensor memory, so the work is done by CLUSTERS OF TWO
+// CTAs, each owning half of the value dimension (256 TMEM columns of O):
 //   * rank 0 holds q_nope[:, 0:256] and streams ckv[:, 0:256] of every page;
 //   * rank 1 holds q_nope[:, 256:512] and q_pe, and streams ckv[:, 256:512] and kpe.
 // Each CTA computes a partial score tile S_r = Q_r K_r^T (128 heads x 64 tokens,
@@ -21,21 +21,30 @@
 // shared memory (MN-major operand). Every KV byte is read from HBM once, no
 // tensor-core work is repeated, and nothing is multicast.
 //
+// Persistent schedule: the tiles (pages) of all rows, concatenated, are cut
+// into one equal range per cluster (computed on the device from seq_lens), so
+// the split of a row is decided by where the cluster boundaries fall. A
+// cluster streams its range without draining between rows: at a row boundary
+// the new q_nope is written into TMEM once the previous scores are complete,
+// and the first PV of the new row overwrites O once the previous row's
+// epilogue has read it. A row wholly inside one range is written directly;
+// the pieces of a row cut by range boundaries are written as normalised
+// partials (O, LSE) to slot row + cluster, and the last piece to finish (a
+// per-row counter) merges them after its cluster's stream.
+//
 // Tensor memory per CTA: O half in columns 0-255, the CTA's 256 q_nope values
-// per head in 256-383 (the A operand of the score MMAs, read from TMEM so that
-// only the 2 KB K slice of each MMA comes from shared memory), two score
-// buffers in 384-447 and 448-511. The kpe block of rank 1 is an ordinary
-// shared-memory MMA (q_pe is a TMA tile).
+// per head in 256-383 (the A operand of the score MMAs), two score buffers in
+// 384-447 and 448-511. The kpe block of rank 1 is a shared-memory MMA (q_pe is
+// a TMA tile).
 //
 // Warp roles per CTA (352 threads): warp 0 = TMA producer (three KV stages),
 // warp 1 = MMA issuer (and TMEM owner), warp 2 = exchange helper, warps 3-10 =
 // softmax in two groups of four warps (one warp per TMEM lane quadrant, one
-// thread per head row). Group g takes the tiles j = g (mod 2) with their own
-// score buffer and exchange buffer, so one group's exchange and exponentials
-// overlap the other's; the only hand-over between consecutive tiles is the
-// running maximum of each row (shared memory + mbarrier), and each group keeps
-// its part of the row sum relative to the maximum of its own latest tile.
-// The score exchange uses st.async, whose bytes complete on the receiver's
+// thread per head row). Group g takes the tiles j = g (mod 2) of the range
+// with their own score and exchange buffers, so one group's exchange and
+// exponentials overlap the other's; between consecutive tiles each row's
+// running maximum and running sum are handed over through shared memory. The
+// score exchange uses st.async, whose bytes complete on the receiver's
 // mbarrier, so the sender never waits for the remote stores; the helper warp
 // returns each buffer to the peer (a cluster-scope release) off the softmax
 // warps' path. The online softmax rescales O lazily: only when a row's maximum
@@ -66,35 +75,54 @@ constexpr uint32_t kTmemO = 0;     // O half: columns 0..255
 constexpr uint32_t kTmemQ = 256;   // q_nope half, two bf16 per column: 256..383
 constexpr uint32_t kTmemS = 384;   // two score buffers: 384..447, 448..511
 constexpr float kRescaleThreshold = 8.f;
-constexpr int kMaxMlaSplits = 32;
+
+// What the producer tells the other roles about the tile in a KV stage.
+struct TileMeta {
+  int32_t b, k, nval, flags;  // row, tile of the row, valid tokens, kFirst | kLast | kFullRow
+  int32_t c_first, n_seg, pad0, pad1;  // clusters holding the row's pieces
+};
+enum { kFirst = 1, kLast = 2, kFullRow = 4 };
+
+struct Ctrl {
+  uint32_t tmem_base;
+  int abort;
+  int start_b, start_k;
+  long long start_P;
+  int npend, nempty;
+  int pend[4][3];  // rows this CTA merges: b, c_first, n_seg
+};
 
 struct Lay {
   static constexpr int QPE = 0;                              // 16 KB (rank 1)
   static constexpr int KV = QPE + kQBlock;                   // kStages x 40 KB
   static constexpr int P = KV + kStages * kKvStage;          // 16 KB
   static constexpr int X = P + kQBlock;                      // 2 x [16][128] float4
-  static constexpr int MR = X + 2 * kXBytes;                 // [2 groups][128] running max
-  static constexpr int FIN = MR + 2 * kHeads * 4;            // [2 groups][l, m][128]
-  static constexpr int BAR = FIN + 2 * 2 * kHeads * 4;
-  static constexpr int NBAR = 24;
-  static constexpr int FLAGS = BAR + NBAR * 8;               // tmem base, abort, last
-  static constexpr int IDS = FLAGS + 16;
-  static constexpr int TOTAL = IDS + kGqaMaxIds * 4 + 1024;  // + alignment slack
+  static constexpr int MR = X + 2 * kXBytes;                 // [2][128] running maximum
+  static constexpr int LR = MR + 2 * kHeads * 4;             // [2][128] running sum
+  static constexpr int META = LR + 2 * kHeads * 4;           // [kStages] TileMeta
+  static constexpr int SCAN = META + kStages * 32;           // [kThreads / 32] + empty rows
+  static constexpr int EMPTY = SCAN + 64;                    // [kThreads] rows without tokens
+  static constexpr int CTRL = EMPTY + kThreads * 4;
+  static constexpr int BAR = CTRL + 128;
+  static constexpr int NBAR = 28;
+  static constexpr int TOTAL = BAR + NBAR * 8 + 1024;        // + alignment slack
 };
 enum {
-  B_QPE = 0,   // q_pe tile landed (rank 1)
-  B_QT = 1,    // q_nope half stored in TMEM (one arrival per softmax thread)
-  B_KVF = 2,   // [kStages] KV stage full
-  B_KVE = 5,   // [kStages] KV stage consumed by the PV MMA
-  B_SF = 8,    // [2] score buffer written
-  B_SE = 10,   // [2] score buffer read
-  B_PF = 12,   // P tile written
-  B_PE = 13,   // PV MMA done
-  B_XF = 14,   // [2] peer scores landed (local expect_tx + the peer's bytes)
-  B_XE = 16,   // [2] the peer has read what this CTA sent into its buffer
-  B_XR = 18,   // [2] this CTA's softmax group has read the buffer
-  B_MRF = 20,  // [2] group g has published the running maximum of its latest tile
-  B_FIN = 22,  // both groups have published their row sums
+  B_QPE = 0,    // q_pe tile of the current row landed (rank 1)
+  B_QT = 1,     // q_nope half of the current row stored in TMEM
+  B_KVF = 2,    // [kStages] KV stage full
+  B_KVE = 5,    // [kStages] KV stage consumed by the PV MMA
+  B_SF = 8,     // [2] score buffer written
+  B_SE = 10,    // [2] score buffer read
+  B_PF = 12,    // P tile written
+  B_PE = 13,    // PV MMA done
+  B_XF = 14,    // [2] peer scores landed (local expect_tx + the peer's bytes)
+  B_XE = 16,    // [2] the peer has read what this CTA sent into its buffer
+  B_XR = 18,    // [2] this CTA's softmax group has read the buffer
+  B_MRF = 20,   // [2] group g has published the running maximum of its latest tile
+  B_LRF = 22,   // [2] group g has published the running sum of its latest tile
+  B_OFREE = 24, // a row's epilogue has read O (the next row may overwrite it)
+  B_EPI = 25,   // [2] group g has written a partial (before the row counter counts it)
 };
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -179,33 +207,60 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Last CTA of rank r for batch row b merges that row's splits for its value half.
-__device__ void mla_merge_if_last(const MlaParams &p, int b, int r, float *scratch,
-                                  volatile int *last_flag) {
-  const int S = p.num_splits;
-  __threadfence();
+__device__ __forceinline__ int cluster_of(int64_t t, int64_t T, int C) {
+  return (int)(((t + 1) * C - 1) / T);
+}
+
+// Tiles of row b; an out-of-range length is clamped and flagged.
+__device__ __forceinline__ int row_tiles(const MlaParams &p, int b, int &len, uint32_t &err) {
+  int n = p.seq_lens[b];
+  if (n < 0 || n > p.capacity) {
+    err |= DA_DEVERR_SEQ_LEN;
+    n = n < 0 ? 0 : p.capacity;
+  }
+  len = n;
+  return (n + kTok - 1) / kTok;
+}
+
+__device__ int block_scan(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(p.counters + b * 2 + r, 1u);
-    *last_flag = (prev == (unsigned)(S - 1)) ? 1 : 0;
+  int before = 0, sum = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int t = scratch[w];
+    if (w < warp) before += t;
+    sum += t;
   }
   __syncthreads();
-  if (!*last_flag) return;
-  __threadfence();
-  float *w = scratch;             // [S][128] weights (lse first)
-  float *inv = w + S * kHeads;    // [128]
-  float *lse_out = inv + kHeads;  // [128]
-  for (int i = threadIdx.x; i < S * kHeads; i += blockDim.x) {
+  *total = sum;
+  return v + before;
+}
+
+// Merges the n_seg partials of row b (slots b + c_first ..) for value half r:
+// LSE-weighted sum of the normalised pieces.
+__device__ void mla_merge_row(const MlaParams &p, int b, int r, int c_first, int n_seg,
+                              float *scratch) {
+  float *w = scratch;                 // [n_seg][128] weights (lse first)
+  float *inv = w + n_seg * kHeads;    // [128]
+  float *lse_out = inv + kHeads;      // [128]
+  const int64_t slot0 = (int64_t)b + c_first;
+  for (int i = threadIdx.x; i < n_seg * kHeads; i += blockDim.x) {
     const int s = i / kHeads, h = i % kHeads;
-    w[i] = __ldcg(p.lse_part + (((int64_t)b * S + s) * 2 + r) * kHeads + h);
+    w[i] = __ldcg(p.lse_part + ((slot0 + s) * 2 + r) * kHeads + h);
   }
   __syncthreads();
   if (threadIdx.x < kHeads) {
     const int h = threadIdx.x;
     float M = neg_inf();
-    for (int s = 0; s < S; ++s) M = fmaxf(M, w[s * kHeads + h]);
+    for (int s = 0; s < n_seg; ++s) M = fmaxf(M, w[s * kHeads + h]);
     float sum = 0.f;
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < n_seg; ++s) {
       const float l = w[s * kHeads + h];
       const float e = (M == neg_inf() || l == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
       w[s * kHeads + h] = e;
@@ -219,11 +274,11 @@ __device__ void mla_merge_if_last(const MlaParams &p, int b, int r, float *scrat
   for (int i = threadIdx.x; i < kHeads * 64; i += blockDim.x) {
     const int h = i / 64, c = i % 64;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < n_seg; ++s) {
       const float e = w[s * kHeads + h];
       if (e != 0.f) {
         const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                    p.o_part + (((int64_t)b * S + s) * kHeads + h) * 512 + r * 256) +
+                                    p.o_part + ((slot0 + s) * kHeads + h) * 512 + r * 256) +
                                 c);
         acc.x += e * v.x;
         acc.y += e * v.y;
@@ -238,7 +293,8 @@ __device__ void mla_merge_if_last(const MlaParams &p, int b, int r, float *scrat
     dst[1] = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
   }
   if (r == 0 && threadIdx.x < kHeads && p.lse) p.lse[(int64_t)b * kHeads + threadIdx.x] = lse_out[threadIdx.x];
-  if (threadIdx.x == 0) p.counters[b * 2 + r] = 0u;
+  if (threadIdx.x == 0) p.counters[b * 2 + r] = 0u;  // ready for the next call
+  __syncthreads();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -249,48 +305,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Lay::BAR);
-  volatile uint32_t *tmem_base_slot = reinterpret_cast<volatile uint32_t *>(smem + Lay::FLAGS);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lay::FLAGS + 4);
-  volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Lay::FLAGS + 8);
-  int *ids = reinterpret_cast<int *>(smem + Lay::IDS);
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + Lay::CTRL);
+  TileMeta *meta = reinterpret_cast<TileMeta *>(smem + Lay::META);
+  int *scan = reinterpret_cast<int *>(smem + Lay::SCAN);
+  int *empty_rows = reinterpret_cast<int *>(smem + Lay::EMPTY);
 
   const uint32_t r = cluster_rank();  // 0: value dims 0..255; 1: 256..511 (+ rope part)
   const uint32_t peer = r ^ 1u;
-  const int split = blockIdx.x >> 1, b = blockIdx.z;
+  const int cl = blockIdx.x >> 1, NC = gridDim.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = r == 0 ? 4 : 5;  // 64-wide KV blocks this CTA streams
 
+  // ---------------------------------------------------------------- the cluster's tile range
   uint32_t dev_err = 0;
-  int n_valid = p.seq_lens[b];
-  if (n_valid < 0 || n_valid > p.capacity) {
-    dev_err |= DA_DEVERR_SEQ_LEN;
-    n_valid = n_valid < 0 ? 0 : p.capacity;
+  int local = 0;
+  for (int b = threadIdx.x; b < p.batch; b += kThreads) {
+    int len;
+    local += row_tiles(p, b, len, dev_err);
   }
-  const int range_lo = split * p.chunk;
-  const int range_hi = min(range_lo + p.chunk, n_valid);
-  const int num_tiles = range_hi > range_lo ? (range_hi - range_lo + kTok - 1) / kTok : 0;
-  const int64_t slot = (int64_t)b * p.num_splits + split;
-
-  if (num_tiles == 0) {
-    if (threadIdx.x == 0 && dev_err) atomicOr(p.err, dev_err);
-    if (p.write_final) {
-      for (int e = threadIdx.x; e < kHeads * 256; e += blockDim.x) {
-        const int h = e / 256, d = e % 256;
-        p.out[((int64_t)b * kHeads + h) * 512 + r * 256 + d] = __float2bfloat16(0.f);
+  int T32 = 0;
+  block_scan(local, scan, &T32);
+  const int64_t T = T32;
+  // never more ranges than tiles: every working cluster holds at least one tile
+  // and the pieces of a row come from consecutive clusters c_first..c_last
+  const int C = (int)(T < (int64_t)NC ? T : (int64_t)NC);
+  const int64_t lo = cl < C ? (int64_t)cl * T / C : 0;
+  const int64_t hi = cl < C ? (int64_t)(cl + 1) * T / C : 0;
+  const int tail_owner = C > 0 ? C - 1 : 0;  // writes rows without tokens past the last tile
+  if (threadIdx.x == 0) {
+    ctrl->abort = 0;
+    ctrl->start_b = -1;
+    ctrl->npend = 0;
+    ctrl->nempty = 0;
+  }
+  __syncthreads();
+  {
+    int64_t base = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += kThreads) {
+      const int b = b0 + threadIdx.x;
+      int len = 0;
+      uint32_t ignored = 0;
+      const int t_b = b < p.batch ? row_tiles(p, b, len, ignored) : 0;
+      int total = 0;
+      const int incl = block_scan(t_b, scan, &total);
+      const int64_t Pb = base + incl - t_b;
+      if (b < p.batch) {
+        if (t_b > 0 && Pb <= lo && lo < Pb + t_b) {
+          ctrl->start_b = b;
+          ctrl->start_k = (int)(lo - Pb);
+          ctrl->start_P = Pb;
+        }
+        // a row without tokens is written by the cluster whose range holds its start
+        if (t_b == 0 && ((Pb >= lo && Pb < hi) || (Pb >= T && cl == tail_owner)))
+          empty_rows[atomicAdd(&ctrl->nempty, 1)] = b;
       }
-      if (r == 0 && p.lse && threadIdx.x < kHeads) p.lse[(int64_t)b * kHeads + threadIdx.x] = neg_inf();
-      return;
+      __syncthreads();
+      const int ne = ctrl->nempty;
+      for (int e = threadIdx.x; e < ne * kHeads * 32; e += kThreads) {
+        // this CTA's value half of the row: zeros; lse = -inf
+        const int rb = empty_rows[e / (kHeads * 32)], h = (e / 32) % kHeads, c = e % 32;
+        *reinterpret_cast<uint4 *>(p.out + ((int64_t)rb * kHeads + h) * 512 + r * 256 + 8 * c) =
+            make_uint4(0, 0, 0, 0);
+        if (r == 0 && c == 0 && p.lse) p.lse[(int64_t)rb * kHeads + h] = neg_inf();
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) ctrl->nempty = 0;
+      base += total;
     }
-    if (threadIdx.x < kHeads) p.lse_part[(slot * 2 + r) * kHeads + threadIdx.x] = neg_inf();
-    mla_merge_if_last(p, b, r, reinterpret_cast<float *>(smem + Lay::KV), last_flag);
+  }
+  __syncthreads();
+  if (cl >= C) {  // no tiles for this cluster (both CTAs take this exit)
+    if (dev_err) atomicOr(p.err, dev_err);
     return;
   }
+  const int n = (int)(hi - lo);  // >= 1
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     mbar_init(&bar[B_QPE], 1);
-    mbar_init(&bar[B_QT], kSoftmaxThreads);
-    mbar_init(&bar[B_FIN], kSoftmaxThreads);
+    mbar_init(&bar[B_QT], kGroupThreads);
+    mbar_init(&bar[B_OFREE], kGroupThreads);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar[B_KVF + s], 1);
       mbar_init(&bar[B_KVE + s], 1);
@@ -302,65 +396,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_XE + s], 1);  // the peer helper's arrival
       mbar_init(&bar[B_XR + s], kGroupThreads);
       mbar_init(&bar[B_MRF + s], kGroupThreads);
+      mbar_init(&bar[B_LRF + s], kGroupThreads);
+      mbar_init(&bar[B_EPI + s], kGroupThreads);
     }
     mbar_init(&bar[B_PF], kGroupThreads);
     mbar_init(&bar[B_PE], 1);
-    *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
-    // page ids of this split, checked against the pool
-    const int first = range_lo / kTok;
-    const int32_t *row = p.block_table + (int64_t)b * p.max_pages + first;
-    for (int j = lane; j < num_tiles; j += 32) {
-      int page = row[j];
-      if (page < 0 || page >= p.num_pages) {
-        dev_err |= DA_DEVERR_PAGE_INDEX;
-        page = -1;
-      }
-      ids[j] = page;
-    }
-  }
   if (warp == 1) {
-    tmem_alloc(const_cast<uint32_t *>(tmem_base_slot), kTmemCols);
+    tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote arrive
-  const uint32_t tmem = *tmem_base_slot;
+  const uint32_t tmem = ctrl->tmem_base;
+  volatile int *abort_flag = &ctrl->abort;
 
   uint8_t *sQpe = smem + Lay::QPE;
   uint8_t *sKV = smem + Lay::KV;
   uint8_t *sP = smem + Lay::P;
   float *sX = reinterpret_cast<float *>(smem + Lay::X);
   float *sMr = reinterpret_cast<float *>(smem + Lay::MR);
-  float *sFin = reinterpret_cast<float *>(smem + Lay::FIN);
+  float *sLr = reinterpret_cast<float *>(smem + Lay::LR);
 
-  int issued_kv = 0, issued_qk = 0, issued_pv = 0;  // for draining after an abort
+  int issued_kv = 0, issued_qk = 0, issued_pv = 0, qpe_seg = -1;  // for draining after an abort
 
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&ckv_map);
       const uint64_t kv_policy = l2_policy_evict_first();
-      if (r == 1) {
-        mbar_arrive_expect_tx(&bar[B_QPE], kQBlock);
-        tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 0, b * kHeads, l2_policy_evict_last());
-      }
-      for (int j = 0, st = 0, ph = 0; j < num_tiles; ++j) {
-        if (j >= kStages && !mbar_wait_bounded(&bar[B_KVE + st], ph ^ 1, kWaitLimitNs)) {
+      uint32_t ignored = 0;
+      int b = ctrl->start_b, k = ctrl->start_k, len = 0;
+      int64_t Pb = ctrl->start_P;
+      int t_b = row_tiles(p, b, len, ignored);
+      auto row_pieces = [&](int &c_first, int &n_seg, bool &full) {
+        c_first = cluster_of(Pb, T, C);
+        n_seg = cluster_of(Pb + t_b - 1, T, C) - c_first + 1;
+        full = Pb >= lo && Pb + t_b <= hi;
+      };
+      int c_first, n_seg;
+      bool full;
+      row_pieces(c_first, n_seg, full);
+      int page_next = p.block_table[(int64_t)b * p.max_pages + k];
+      for (int i = 0, st = 0, ph = 0; i < n; ++i) {
+        if (i >= kStages && !mbar_wait_bounded(&bar[B_KVE + st], ph ^ 1, kWaitLimitNs)) {
           dev_err |= DA_DEVERR_TIMEOUT;
           *abort_flag = 1;
           break;
         }
+        int page = page_next;
+        const bool bad = page < 0 || page >= p.num_pages;
+        if (bad) dev_err |= DA_DEVERR_PAGE_INDEX;
+        TileMeta &m = meta[st];
+        m.b = b;
+        m.k = k;
+        m.nval = bad ? 0 : min(kTok, len - k * kTok);
+        m.flags = ((i == 0 || k == 0) ? kFirst : 0) | ((i == n - 1 || k == t_b - 1) ? kLast : 0) |
+                  (full ? kFullRow : 0);
+        m.c_first = c_first;
+        m.n_seg = n_seg;
         uint8_t *dst = sKV + st * kKvStage;
-        const int page = ids[j];
-        if (page < 0) {
+        if (bad) {
           // a skipped page: zeros instead of stale data (its scores are masked)
-          for (int i = 0; i < nkb * kKvBlock / 16; ++i)
-            reinterpret_cast<uint4 *>(dst)[i] = make_uint4(0, 0, 0, 0);
+          for (int e = 0; e < nkb * kKvBlock / 16; ++e)
+            reinterpret_cast<uint4 *>(dst)[e] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&bar[B_KVF + st], 0);
         } else {
@@ -373,6 +475,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++issued_kv;
         if (++st == kStages) st = 0, ph ^= 1;
+        // the next tile (possibly of the next row with tokens); its page id is
+        // fetched now, while this warp waits for a free stage
+        if (i + 1 < n) {
+          if (++k == t_b) {
+            Pb += t_b;
+            do {
+              ++b;
+              t_b = b < p.batch ? row_tiles(p, b, len, ignored) : 1;
+            } while (t_b == 0);
+            k = 0;
+            row_pieces(c_first, n_seg, full);
+          }
+          page_next = b < p.batch ? p.block_table[(int64_t)b * p.max_pages + k] : -1;
+        }
       }
     }
   } else if (warp == 1) {
@@ -380,54 +496,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, kTok, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
-      bool ok = mbar_wait_bounded(&bar[B_QT], 0, kWaitLimitNs);
-      if (ok && r == 1) ok = mbar_wait_bounded(&bar[B_QPE], 0, kWaitLimitNs);
-      // Scores of tile k need its KV stage and the score buffer read back from
-      // tile k - 2; PV of tile k needs its P. Neither waits for the other: the
-      // issuer polls both and issues what is ready, so the next scores are in
-      // flight while a softmax group still works on the previous tile. (No
-      // barrier polled here can run a phase ahead of the tile being tested.)
+      const uint64_t q_policy = l2_policy_evict_last();
+      // Scores of tile k need its KV stage, the score buffer read back from
+      // tile k - 2 and, on a row's first tile, that row's q (TMEM, and q_pe on
+      // rank 1, loaded here once the previous row's scores are complete). PV of
+      // tile k needs its P and, on a row's first tile, the previous row's O
+      // read out. The issuer polls both and issues what is ready. (No barrier
+      // polled here can run a phase ahead of the tile being tested.)
+      int qk_seg = -1, pv_seg = -1;  // row segment of the latest QK / PV
+      bool ok = true;
       uint64_t idle_since = 0;
-      while (ok && issued_pv < num_tiles) {
+      while (ok && issued_pv < n) {
         if (*abort_flag) break;
         bool progress = false;
         const int k = issued_qk;
-        if (k < num_tiles && mbar_test(&bar[B_KVF + k % kStages], (k / kStages) & 1) &&
-            (k < 2 || mbar_test(&bar[B_SE + (k & 1)], ((k >> 1) - 1) & 1))) {
-          tc_fence_after();
-          const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
-          const uint32_t d = tmem + kTmemS + 64 * (k & 1);
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
-                           umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
-                           (c | kk) != 0);
-          if (r == 1) {
-            const uint32_t q = smem_u32(sQpe);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
-                           umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
+        if (k < n && mbar_test(&bar[B_KVF + k % kStages], (k / kStages) & 1)) {
+          const TileMeta m = meta[k % kStages];
+          const bool first = (m.flags & kFirst) != 0;
+          const int seg = first ? qk_seg + 1 : qk_seg;
+          bool ready = k < 2 || mbar_test(&bar[B_SE + (k & 1)], ((k >> 1) - 1) & 1);
+          if (first) {
+            if (r == 1 && qpe_seg < seg) {
+              if (k == 0 || mbar_test(&bar[B_SF + ((k - 1) & 1)], ((k - 1) >> 1) & 1)) {
+                mbar_arrive_expect_tx(&bar[B_QPE], kQBlock);
+                tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 0, m.b * kHeads, q_policy);
+                qpe_seg = seg;
+              }
+              ready = false;
+            }
+            ready = ready && mbar_test(&bar[B_QT], seg & 1) &&
+                    (r == 0 || mbar_test(&bar[B_QPE], seg & 1));
           }
-          umma_commit(&bar[B_SF + (k & 1)]);
-          ++issued_qk;
-          progress = true;
+          if (ready) {
+            tc_fence_after();
+            const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
+            const uint32_t d = tmem + kTmemS + 64 * (k & 1);
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
+                             umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
+                             (c | kk) != 0);
+            if (r == 1) {
+              const uint32_t q = smem_u32(sQpe);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
+                             umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
+            }
+            umma_commit(&bar[B_SF + (k & 1)]);
+            qk_seg = seg;
+            ++issued_qk;
+            progress = true;
+          }
         }
         const int j = issued_pv;
         if (j < issued_qk && mbar_test(&bar[B_PF], j & 1)) {
-          tc_fence_after();
-          const int st = j % kStages;
-          const uint32_t v = smem_u32(sKV + st * kKvStage);
-          const uint32_t pa = smem_u32(sP);
+          const TileMeta m = meta[j % kStages];
+          const bool first = (m.flags & kFirst) != 0;
+          const int seg = first ? pv_seg + 1 : pv_seg;
+          if (!first || seg == 0 || mbar_test(&bar[B_OFREE], (seg - 1) & 1)) {
+            tc_fence_after();
+            const int st = j % kStages;
+            const uint32_t v = smem_u32(sKV + st * kKvStage);
+            const uint32_t pa = smem_u32(sP);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
-                         umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv, (j | kk) != 0);
-          umma_commit(&bar[B_PE]);
-          umma_commit(&bar[B_KVE + st]);
-          ++issued_pv;
-          progress = true;
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
+                           umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv,
+                           kk != 0 || !first);
+            umma_commit(&bar[B_PE]);
+            umma_commit(&bar[B_KVE + st]);
+            pv_seg = seg;
+            ++issued_pv;
+            progress = true;
+          }
         }
         if (progress) {
           idle_since = 0;
@@ -448,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // (only the buffers the peer still writes into are returned)
     if (lane == 0) {
       const uint32_t peer_xe0 = mapa_peer(smem_u32(&bar[B_XE]), peer);
-      for (int j = 0; j + 2 < num_tiles; ++j) {
+      for (int j = 0; j + 2 < n; ++j) {
         if (!mbar_wait_bounded(&bar[B_XR + (j & 1)], (j >> 1) & 1, kWaitLimitNs)) {
           dev_err |= DA_DEVERR_TIMEOUT;
           *abort_flag = 1;
@@ -461,49 +604,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ============================================================ softmax
     const int tid = threadIdx.x - 32 * kFirstSoftmaxWarp;  // 0..255
-    const int g = tid >> 7;                                 // group: tiles j = g (mod 2)
+    const int g = tid >> 7;                                 // group: tiles i = g (mod 2)
     const int quad = warp & 3;                              // TMEM lane quadrant of this warp
     const int h = quad * 32 + lane;                         // head row
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // this CTA's q_nope half of row h into TMEM: group g stores columns
-    // kTmemQ + 64 g .. + 63 (values 128 g .. 128 g + 127 of the half)
-    {
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 +
-                                                         256 * r + 128 * g);
-      uint4 qv[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) qv[i] = __ldg(src + i);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[4 * i] = __uint_as_float(qv[4 * c + i].x);
-          v[4 * i + 1] = __uint_as_float(qv[4 * c + i].y);
-          v[4 * i + 2] = __uint_as_float(qv[4 * c + i].z);
-          v[4 * i + 3] = __uint_as_float(qv[4 * c + i].w);
-        }
-        tmem_st16(tmem + lane_off + kTmemQ + 64 * g + 16 * c, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar[B_QT]);
-    }
     // exchange buffer g: the float4 holding scores 4q..4q+3 of head h sits at
     // [q][h], so one warp-wide store moves 512 contiguous bytes
     const uint32_t peer_x = mapa_peer(smem_u32(sX + g * (kXBytes / 4) + 4 * h), peer);
     const uint32_t peer_xf = mapa_peer(smem_u32(&bar[B_XF + g]), peer);
     const float4 *my_x = reinterpret_cast<const float4 *>(sX + g * (kXBytes / 4)) + h;
     const float sscale = p.score_scale;
-    // m_last: running maximum after this group's latest tile (scaled, log2
-    // units); l: this group's part of the row sum, relative to m_last
-    float m_last = neg_inf(), l = 0.f;
     bool ok = true;
     int x_next = g;         // first tile of this group whose peer scores have not been waited for
     bool x_posted = false;  // whether its expect_tx has been posted
-    for (int j = g; j < num_tiles; j += 2) {
-      const int i = j >> 1;  // this group's tile counter (phase of its barriers)
-      if (!(ok = warp_wait(&bar[B_SF + g], i & 1))) break;
+    int epi = 0;            // partials written by this group (phase of B_EPI + g)
+    for (int i = g; i < n; i += 2) {
+      const int ii = i >> 1;  // this group's tile counter (phase of its barriers)
+      // the tile's description (its stage cannot be refilled before this tile's PV)
+      if (!(ok = warp_wait(&bar[B_KVF + i % kStages], (i / kStages) & 1))) break;
+      const TileMeta m = meta[i % kStages];
+      const bool first = (m.flags & kFirst) != 0;
+      if (first) {
+        // q_nope of the row into TMEM once the previous tile's scores are complete
+        if (i >= 1 && !(ok = warp_wait(&bar[B_SF + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
+        tc_fence_after();
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)m.b * kHeads + h) * 512 + 256 * r);
+#pragma unroll
+        for (int c0 = 0; c0 < 8; c0 += 2) {
+          uint4 qv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qv[e] = __ldg(src + 4 * c0 + e);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[4 * e] = __uint_as_float(qv[4 * c + e].x);
+              v[4 * e + 1] = __uint_as_float(qv[4 * c + e].y);
+              v[4 * e + 2] = __uint_as_float(qv[4 * c + e].z);
+              v[4 * e + 3] = __uint_as_float(qv[4 * c + e].w);
+            }
+            tmem_st16(tmem + lane_off + kTmemQ + 16 * (c0 + c), v);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar[B_QT]);
+      }
+      if (!(ok = warp_wait(&bar[B_SF + g], ii & 1))) break;
       tc_fence_after();
       float s[64];
 #pragma unroll
@@ -517,7 +666,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar[B_SE + g]);
       // ---- exchange the partial scores with the peer CTA
-      if (i >= 1 && !(ok = warp_wait_cluster(&bar[B_XE + g], (i - 1) & 1))) break;
+      if (ii >= 1 && !(ok = warp_wait_cluster(&bar[B_XE + g], (ii - 1) & 1))) break;
 #pragma unroll
       for (int q = 0; q < 16; ++q)
         st_async_v4(peer_x + q * kHeads * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3],
@@ -525,8 +674,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // this tile's phase of x_full completes once the peer's 32 KB have landed
       if (tid == kGroupThreads * g) mbar_arrive_expect_tx(&bar[B_XF + g], kXBytes);
       x_posted = true;
-      if (!(ok = warp_wait_cluster(&bar[B_XF + g], i & 1))) break;
-      x_next = j + 2;
+      if (!(ok = warp_wait_cluster(&bar[B_XF + g], ii & 1))) break;
+      x_next = i + 2;
       x_posted = false;
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -538,8 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&bar[B_XR + g]);
       // ---- mask and tile maximum
-      const int tok0 = range_lo + j * kTok;
-      const int nval = ids[j] < 0 ? 0 : min(kTok, range_hi - tok0);
+      const int nval = m.nval;
       // raw scores past the valid tokens become a value that never wins the
       // extreme below (uniform branch: ragged tiles only)
       const float pad = sscale >= 0.f ? neg_inf() : -neg_inf();
@@ -561,12 +709,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float ext = sscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
                                       : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
       const float mt = nval > 0 ? ext * sscale : neg_inf();
-      // ---- running maximum: that of tile j - 1 (the other group) grows lazily
+      // ---- running maximum of the row through tile i - 1 (the other group);
+      // the hand-off is waited for on a row's first tile too, which keeps the
+      // other group's read of this group's previous value ahead of the overwrite
       float m_prev = neg_inf();
-      if (j >= 1) {
-        const int jp = j - 1;
-        if (!(ok = warp_wait(&bar[B_MRF + (jp & 1)], (jp >> 1) & 1))) break;
-        m_prev = sMr[(jp & 1) * kHeads + h];
+      if (i >= 1) {
+        if (!(ok = warp_wait(&bar[B_MRF + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
+        if (!first) m_prev = sMr[((i - 1) & 1) * kHeads + h];
       }
       const bool need = mt > m_prev + kRescaleThreshold || (m_prev == neg_inf() && mt != neg_inf());
       const float m_new = need ? mt : m_prev;
@@ -591,13 +740,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       if (nval < kTok) exp_pack(std::true_type{});
       else exp_pack(std::false_type{});
-      if (l != 0.f && m_new != m_last) l *= ex2(m_last - m_new);
-      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-      m_last = m_new;
+      // ---- running sum of the row through tile i, relative to m_new
+      float l_prev = 0.f;
+      if (i >= 1) {
+        if (!(ok = warp_wait(&bar[B_LRF + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
+        if (!first) l_prev = sLr[((i - 1) & 1) * kHeads + h];
+      }
+      const float l_new = (l_prev != 0.f && m_new != m_prev ? l_prev * ex2(m_prev - m_new) : l_prev) +
+                          ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+      sLr[g * kHeads + h] = l_new;
+      mbar_arrive(&bar[B_LRF + g]);
       // ---- PV of the previous tile must be done before O or P change
-      if (j >= 1 && !(ok = warp_wait(&bar[B_PE], (j - 1) & 1))) break;
+      if (i >= 1 && !(ok = warp_wait(&bar[B_PE], (i - 1) & 1))) break;
       tc_fence_after();
-      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+      if (!first && __any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2(m_prev - m_new) : 1.f;  // 0 when m_prev is -inf
         for (int c = 0; c < 256; c += 16) {
           float v[16];
@@ -617,7 +773,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (nval < kTok) {
         // value rows past the valid tokens may hold anything: zero them
-        uint8_t *kv = sKV + (j % kStages) * kKvStage;
+        uint8_t *kv = sKV + (i % kStages) * kKvStage;
         for (int e = tid - kGroupThreads * g; e < (kTok - nval) * 4 * 8; e += kGroupThreads) {
           const int t = nval + e / 32, blk = (e / 8) % 4, c = e % 8;
           *reinterpret_cast<uint4 *>(kv + blk * kKvBlock + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
@@ -626,62 +782,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar[B_PF]);
+      if (m.flags & kLast) {
+        // ---- end of the row's piece: O / l of this value half
+        if (!(ok = warp_wait(&bar[B_PE], i & 1))) break;
+        tc_fence_after();
+        const bool full = (m.flags & kFullRow) != 0;
+        const float inv = l_new > 0.f ? 1.f / l_new : 0.f;
+        const float lse = l_new > 0.f ? (m_new + __log2f(l_new)) * 0.69314718055994531f : neg_inf();
+        const int64_t slot = (int64_t)m.b + cl;
+        for (int c = 0; c < 256; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_off + kTmemO + c, v);
+          tmem_wait_ld();
+          if (full) {
+            __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
+                p.out + ((int64_t)m.b * kHeads + h) * 512 + r * 256 + c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + r * 256 + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[B_OFREE]);
+        if (full) {
+          if (r == 0 && p.lse) p.lse[(int64_t)m.b * kHeads + h] = lse;
+        } else {
+          p.lse_part[(slot * 2 + r) * kHeads + h] = lse;
+          // the whole piece is in global memory before the row's counter counts it
+          mbar_arrive(&bar[B_EPI + g]);
+          if (!(ok = warp_wait(&bar[B_EPI + g], epi & 1))) break;
+          ++epi;
+          if (tid == kGroupThreads * g) {
+            const uint32_t prev = atomic_add_acq_rel_gpu(p.counters + m.b * 2 + r, 1u);
+            if (prev == (uint32_t)(m.n_seg - 1)) {
+              const int q = atomicAdd(&ctrl->npend, 1);
+              ctrl->pend[q][0] = m.b;
+              ctrl->pend[q][1] = m.c_first;
+              ctrl->pend[q][2] = m.n_seg;
+            }
+          }
+        }
+      }
     }
     if (!ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
       *abort_flag = 1;
       // the peer may still be storing the scores of tile x_next into this
       // group's buffer (it cannot start the group's next one): let them land
-      if (tid == kGroupThreads * g && x_next < num_tiles) {
+      if (tid == kGroupThreads * g && x_next < n) {
         if (!x_posted) mbar_arrive_expect_tx(&bar[B_XF + g], kXBytes);
         mbar_wait_cluster_bounded(&bar[B_XF + g], (x_next >> 1) & 1);
       }
-    }
-    // ---- epilogue: O_r / l for this CTA's value half (group g: columns 128 g ..)
-    if (ok && warp_wait(&bar[B_PE], (num_tiles - 1) & 1)) {
-      tc_fence_after();
-      sFin[g * 2 * kHeads + h] = l;
-      sFin[g * 2 * kHeads + kHeads + h] = m_last;
-      mbar_arrive(&bar[B_FIN]);
-      if (warp_wait(&bar[B_FIN], 0)) {
-        // both groups' sums relative to the final maximum, added in one order
-        const float l0 = sFin[h], m0 = sFin[kHeads + h];
-        const float l1 = sFin[2 * kHeads + h], m1 = sFin[3 * kHeads + h];
-        const float mf = fmaxf(m0, m1);
-        const float lt = (l0 != 0.f ? l0 * ex2(m0 - mf) : 0.f) + (l1 != 0.f ? l1 * ex2(m1 - mf) : 0.f);
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float lse = lt > 0.f ? (mf + __log2f(lt)) * 0.69314718055994531f : neg_inf();
-        for (int c = 0; c < 128; c += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_off + kTmemO + 128 * g + c, v);
-          tmem_wait_ld();
-          const int col = r * 256 + 128 * g + c;
-          if (p.write_final) {
-            __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
-                p.out + ((int64_t)b * kHeads + h) * 512 + col);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
-          } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + col);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
-          }
-        }
-        if (g == 0) {
-          if (p.write_final) {
-            if (r == 0 && p.lse) p.lse[(int64_t)b * kHeads + h] = lse;
-          } else {
-            p.lse_part[(slot * 2 + r) * kHeads + h] = lse;
-          }
-        }
-      } else {
-        dev_err |= DA_DEVERR_TIMEOUT;
-        *abort_flag = 1;
-      }
-    } else if (ok) {
-      dev_err |= DA_DEVERR_TIMEOUT;
-      *abort_flag = 1;
     }
   }
 
@@ -696,6 +851,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (issued_qk > 0)
         mbar_wait_bounded(&bar[B_SF + ((issued_qk - 1) & 1)], ((issued_qk - 1) >> 1) & 1, kWaitLimitNs);
       if (issued_pv > 0) mbar_wait_bounded(&bar[B_PE], (issued_pv - 1) & 1, kWaitLimitNs);
+      if (qpe_seg >= 0) mbar_wait_bounded(&bar[B_QPE], qpe_seg & 1, kWaitLimitNs);
     }
     __syncthreads();
   }
@@ -706,14 +862,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   cluster_sync();  // the peer no longer writes into this CTA's shared memory
   if (*abort_flag) return;
-  if (!p.write_final) mla_merge_if_last(p, b, (int)r, reinterpret_cast<float *>(smem + Lay::KV), last_flag);
+  // ---- rows whose last piece finished here: merge them (this value half)
+  const int npend = ctrl->npend;
+  for (int q = 0; q < npend; ++q)
+    mla_merge_row(p, ctrl->pend[q][0], (int)r, ctrl->pend[q][1], ctrl->pend[q][2],
+                  reinterpret_cast<float *>(smem + Lay::KV));
 }
 
 }  // namespace
 
 int mla_smem_bytes() { return Lay::TOTAL; }
 int mla_threads() { return kThreads; }
-int mla_max_splits() { return kMaxMlaSplits; }
 
 cudaError_t mla_prepare(int /*device*/) {
   return cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,20 +1,16 @@
-// plan.cpp -- host planner: how many KV splits per (batch row, kv head) unit,
-// the grid, and the workspace layout. Pure host code.
+// plan.cpp -- host planner: the grid and the workspace layout of the split
+// kernels. Pure host code.
 //
-// The split count generalises the XQA launcher (TensorRT-LLM xqa/mha.cu,
-// `launchMHA`: sub-sequences per sequence = SMs / (B x HKV), capped by the
-// sequence length in CTA tiles) and keeps the tile-aligned split length of
-// the flex-decode template (flex_decode.py.jinja: TILE_KV = cdiv(cdiv(KV_LEN,
-// SPLIT_KV), BLOCK_N) * BLOCK_N). Instead of a closed formula, the planner
-// tries every split count S that keeps the grid within a few dozen CTAs per
-// SM, simulates the hardware's in-order CTA dispatch onto the resident slots
-// (cost of a CTA = fixed start/epilogue cost + its KV bytes at the per-slot
-// share of HBM bandwidth, plus the fused merge of the unit's last CTA) and
-// keeps the S with the smallest estimated makespan.
+// Both kernels are persistent: the host sizes one wave of resident CTAs (GQA)
+// or CTA pairs (MLA clusters), never more than there are KV tiles, and the
+// device cuts the concatenated tiles of all (row, kv head) units into one equal
+// range per CTA or cluster. How a unit is split therefore follows from where
+// the range boundaries fall: the split-KV decomposition of the flash-decoding
+// method with the split lengths chosen for an even load rather than a fixed
+// count (the XQA launcher, TensorRT-LLM xqa/mha.cu `launchMHA`, and the
+// flex-decode template, flex_decode.py.jinja, both fix a split count per unit).
 #include <algorithm>
 #include <cstring>
-#include <functional>
-#include <queue>
 #include <vector>
 
 #include "internal.h"
@@ -24,12 +20,6 @@ namespace da {
 namespace {
 constexpr int kGqaTile = 64;
 constexpr int kMlaTile = 64;
-// cost model (seconds); only ratios matter for the choice
-constexpr double kHbmBytesPerSec = 6.5e12;
-constexpr double kCtaFixedSec = 2.0e-6;
-constexpr double kMergeBytesPerSec = 100e9;  // one CTA reading the unit's partials
-constexpr double kMergeFixedSec = 1.0e-6;
-constexpr int kMaxCtasPerSlot = 24;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -91,31 +81,6 @@ static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
   return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));
 }
 
-// Estimated time of the grid for split length `chunk` (see the file comment).
-static double makespan(const std::vector<int64_t> &unit_len, int heads, int64_t chunk,
-                       int64_t splits, int slots, double sec_per_pos, double merge_sec_per_split) {
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int i = 0; i < slots; ++i) free_at.push(0.0);
-  const double per_slot = sec_per_pos * slots;  // a slot gets 1/slots of the bandwidth
-  double end = 0.0;
-  const int64_t units = (int64_t)unit_len.size();
-  (void)heads;
-  for (int64_t u = 0; u < units; ++u) {  // launch order: split fastest, then head, then row
-    double unit_done = 0.0;
-    for (int64_t s = 0; s < splits; ++s) {
-      const int64_t pos = std::max<int64_t>(0, std::min(chunk, unit_len[u] - s * chunk));
-      const double t0 = free_at.top();
-      free_at.pop();
-      const double t1 = t0 + (pos > 0 ? kCtaFixedSec + pos * per_slot : 0.2 * kCtaFixedSec);
-      free_at.push(t1);
-      unit_done = std::max(unit_done, t1);
-    }
-    if (splits > 1) unit_done += kMergeFixedSec + merge_sec_per_split * splits;
-    end = std::max(end, unit_done);
-  }
-  return end;
-}
-
 da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm,
                        const int32_t *seq_lens_host, const int32_t *kv_num_blks_host,
                        int32_t num_splits_override, da_plan_info *info) {
@@ -138,7 +103,6 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
 
   // positions per unit the split kernel walks (sparse: the compacted list)
   std::vector<int64_t> unit_len((size_t)units);
-  int64_t max_len = 0;
   for (int b = 0; b < p->batch; ++b) {
     for (int h = 0; h < heads; ++h) {
       int64_t len;
@@ -153,10 +117,8 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
                             : std::min<int64_t>(p->max_seq_len, capacity);
       }
       unit_len[(size_t)((int64_t)b * heads + h)] = len;
-      max_len = std::max(max_len, len);
     }
   }
-  max_len = std::max<int64_t>(max_len, 1);
 
   const int cps = ctas_per_sm(p, smem_per_sm);
   if (!mla) {
@@ -191,64 +153,32 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
     return DA_OK;
   }
 
-  // largest split the kernel can take: its page / block ids fit in shared memory
-  int64_t max_chunk = round_up(max_len, align);
-  max_chunk = std::min<int64_t>(max_chunk, (int64_t)(kGqaMaxIds - 1) * p->page_size);
-  max_chunk = std::max<int64_t>(max_chunk, align);
-  const int64_t min_splits = ceil_div(max_len, max_chunk);
-
-  // an MLA split runs on a cluster of two CTAs: count cluster slots
-  const int slots = std::max(1, num_sms * cps / 2);
-  const int max_splits = mla_max_splits();
-  int64_t chunk;
-  if (num_splits_override > 0) {
-    chunk = round_up(ceil_div(max_len, std::max<int64_t>(num_splits_override, min_splits)), align);
-    chunk = std::min(chunk, max_chunk);
-  } else {
-    const double bytes_per_pos = (p->ckv_dim + p->kpe_dim) * 2.0 * 1.3;  // MLA also pays flops
-    const double sec_per_pos = bytes_per_pos / kHbmBytesPerSec;
-    const double merge_sec_per_split = rows * (dv + 1) * 4.0 / kMergeBytesPerSec;
-    const int64_t max_ctas = (int64_t)slots * kMaxCtasPerSlot;
-    double best = 0.0;
-    chunk = max_chunk;
-    int64_t last_chunk = -1;
-    for (int64_t S = min_splits; S <= max_splits; ++S) {
-      const int64_t c = std::min(round_up(ceil_div(max_len, S), align), max_chunk);
-      if (c == last_chunk) continue;
-      last_chunk = c;
-      const int64_t splits = ceil_div(max_len, c);
-      if (splits > max_splits) break;
-      if (splits > 1 && units * splits > max_ctas) break;
-      const double t = makespan(unit_len, heads, c, splits, slots, sec_per_pos, merge_sec_per_split);
-      if (best == 0.0 || t < best * 0.999) {
-        best = t;
-        chunk = c;
-      }
-      if (c == align) break;
-    }
-  }
-  const int64_t splits = std::max<int64_t>(1, ceil_div(max_len, chunk));
-  if (splits > max_splits) return DA_ERR_UNSUPPORTED;
-
+  // Persistent MLA grid: one cluster of two CTAs (one per value half) per pair
+  // of SMs, never more clusters than tiles.
+  int64_t tiles = 0;
+  for (int64_t len : unit_len) tiles += ceil_div(len, tile);
+  tiles = std::max<int64_t>(tiles, 1);
+  int64_t clusters = std::max<int64_t>(1, (int64_t)num_sms * cps / 2);
+  if (num_splits_override > 0) clusters = (int64_t)num_splits_override * units;
+  clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, tiles));
+  clusters = std::min<int64_t>(clusters, 32767);
   info->kv_tile = tile;
-  info->chunk_tokens = (int32_t)chunk;
-  info->num_splits = (int32_t)splits;
+  info->chunk_tokens = (int32_t)(ceil_div(tiles, clusters) * tile);
+  info->num_splits = (int32_t)ceil_div(clusters, units);
   info->num_units = (int32_t)units;
   info->rows_per_unit = rows;
-  info->grid_x = (int32_t)(2 * splits);  // MLA: a CTA pair per split
-  info->grid_y = heads;
-  info->grid_z = p->batch;
+  info->grid_x = (int32_t)(2 * clusters);
+  info->grid_y = 1;
+  info->grid_z = 1;
   info->ctas_per_sm = cps;
-  info->writes_final = splits == 1 ? 1 : 0;
+  info->writes_final = 0;  // decided per row on the device
   int64_t off = kWorkspaceHeader;
   info->counters_offset = off;
   off = align256(off + units * 2 * 4);
-  if (!info->writes_final) {
-    info->partial_o_offset = off;
-    off = align256(off + units * splits * rows * (int64_t)dv * 4);
-    info->partial_lse_offset = off;
-    off = align256(off + units * splits * rows * 2 * 4);
-  }
+  info->partial_o_offset = off;  // slots row + cluster
+  off = align256(off + (units + clusters) * rows * (int64_t)dv * 4);
+  info->partial_lse_offset = off;
+  off = align256(off + (units + clusters) * rows * 2 * 4);
   info->workspace_bytes = off;
   return DA_OK;
 }

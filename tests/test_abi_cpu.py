@@ -95,23 +95,6 @@ def _problem(w):
     return da.make_problem(**da.problem_kwargs(w))
 
 
-def _check_cover(plan, lengths, align):
-    """MLA plans: every position of every unit is in exactly one tile-aligned split."""
-    chunk, S = plan["chunk_tokens"], plan["num_splits"]
-    assert chunk % align == 0 and chunk > 0
-    for n in lengths:
-        covered = 0
-        prev_hi = 0
-        for s in range(S):
-            lo, hi = s * chunk, min((s + 1) * chunk, n)
-            if hi <= lo:
-                continue
-            assert lo == prev_hi  # contiguous, no overlap, no gap
-            covered += hi - lo
-            prev_hi = hi
-        assert covered == n
-
-
 def _gqa_schedule(ctas, unit_tiles):
     """The persistent GQA kernel's schedule, as its comments define it: the units'
     tiles laid end to end are cut into `ctas` equal ranges [floor(c*T/C),
@@ -157,6 +140,31 @@ def _check_gqa_plan(plan, unit_tiles, num_sms=152):
     assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * G * 4
 
 
+def _check_mla_plan(plan, row_tiles, num_sms=152):
+    """Persistent MLA grid: one cluster of two CTAs per pair of SMs (never more
+    clusters than tiles); the rows' tiles are cut into one range per cluster,
+    exactly as for the GQA CTAs, with a partial slot per (row + cluster)."""
+    assert plan["grid_x"] % 2 == 0 and plan["grid_y"] == plan["grid_z"] == 1
+    C = plan["grid_x"] // 2
+    assert C == min(num_sms * plan["ctas_per_sm"] // 2, max(sum(row_tiles), 1))
+    segs, bounds = _gqa_schedule(C, row_tiles)
+    for t, seg in zip(row_tiles, segs):
+        pos = 0
+        for _, lo, hi in seg:
+            assert lo == pos
+            pos = hi
+        assert pos == t
+        if seg:
+            assert [c for c, _, _ in seg] == list(range(seg[0][0], seg[-1][0] + 1))
+    sizes = [bounds[c + 1] - bounds[c] for c in range(C)]
+    assert max(sizes) - min(sizes) <= 1
+    U = plan["num_units"]
+    assert plan["counters_offset"] == 256
+    assert plan["partial_o_offset"] - plan["counters_offset"] >= U * 2 * 4
+    assert plan["partial_lse_offset"] - plan["partial_o_offset"] >= (U + C) * 128 * 512 * 4
+    assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * 2 * 128 * 4
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 def test_planner_covers_every_position_once(lib, cfg):
     w = W.config(cfg, shape_only=True)
@@ -164,10 +172,7 @@ def test_planner_covers_every_position_once(lib, cfg):
     plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], w.num_splits)
     lens = [int(x) for x in w.tensors["seq_lens"]]
     if w.is_mla:
-        _check_cover(plan, lens, plan["kv_tile"])
-        assert plan["grid_x"] == 2 * plan["num_splits"]  # a cluster of two CTAs per split
-        busy = sum(math.ceil(n / plan["chunk_tokens"]) for n in lens) * 2
-        assert busy >= 152
+        _check_mla_plan(plan, [math.ceil(n / 64) for n in lens])
         return
     if w.sparse_block_size:
         tiles = [int(x) * (w.sparse_block_size // 64) for x in w.tensors["kv_num_blks"].flatten()]
