@@ -81,6 +81,22 @@ da_status encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t row_elem
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
+// Rows of `row_elems` bf16 read 32 columns at a time (64 bytes, 64B-swizzled):
+// the per-rank halves of the MLA rope part.
+da_status encode_bf16_rows_sw64(CUtensorMap *map, const void *base, uint64_t row_elems, uint64_t rows,
+                                uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * 2};
+  const cuuint32_t box[2] = {32u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
 // A bf16 cache of rows of 128 elements as a 3-D tensor (64 elements, row, half)
 // with the half stride (128 B) below the row stride (256 B): one box copies
 // `box_rows` rows and lands as [half][row][64], 128B-swizzled.
@@ -203,8 +219,8 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
     ctx->map_k_base = ctx->map_v_base = ctx->map_q_base = ctx->map_qpe_base = nullptr;
     da_status st;
     if ((st = encode_bf16_rows(&ctx->kmap, a->k, 512, tokens, 64)) != DA_OK) return st;
-    if ((st = encode_bf16_rows(&ctx->vmap, a->v, 64, tokens, 64)) != DA_OK) return st;
-    if ((st = encode_bf16_rows(&ctx->qpemap, a->q_pe, 64, qrows, 128)) != DA_OK) return st;
+    if ((st = encode_bf16_rows_sw64(&ctx->vmap, a->v, 64, tokens, 64)) != DA_OK) return st;
+    if ((st = encode_bf16_rows_sw64(&ctx->qpemap, a->q_pe, 64, qrows, 128)) != DA_OK) return st;
     ctx->map_k_base = a->k;
     ctx->map_v_base = a->v;
     ctx->map_q_base = a->q;

@@ -11,8 +11,9 @@
 // GB300 design. A 128-head x 512-wide fp32 output accumulator fills all 512
 // columns of one SM's tensor memory, so the work is done by CLUSTERS OF TWO
 // CTAs, each owning half of the value dimension (256 TMEM columns of O):
-//   * rank 0 holds q_nope[:, 0:256] and streams ckv[:, 0:256] of every page;
-//   * rank 1 holds q_nope[:, 256:512] and q_pe, and streams ckv[:, 256:512] and kpe.
+//   * rank r holds q_nope[:, 256r:256r+256] and q_pe[:, 32r:32r+32], and streams
+//     ckv[:, 256r:256r+256] and kpe[:, 32r:32r+32] of every page (288 of the 576
+//     contraction elements each, so the two score MMAs take equal time).
 // Each CTA computes a partial score tile S_r = Q_r K_r^T (128 heads x 64 tokens,
 // tcgen05.mma, fp32 in TMEM) over its part of the 576-long contraction, the two
 // partials are exchanged through distributed shared memory and added (both
@@ -33,11 +34,13 @@
 // per-row counter) merges them after its cluster's stream.
 //
 // Tensor memory per CTA: O half in columns 0-255, the CTA's 256 q_nope values
-// per head in 256-383 (the A operand of the score MMAs), two score buffers in
-// 384-447 and 448-511. The kpe block of rank 1 is a shared-memory MMA (q_pe is
-// a TMA tile).
+// per head in 256-383 (the A operand of the score MMAs), the score tile in
+// 384-447 (the next tile's scores are issued as soon as a softmax group has
+// read it), and two P tiles (bf16, the A operand of the PV MMAs) in 448-479
+// and 480-511, one per softmax group. The kpe part is a shared-memory MMA on
+// 64-byte-swizzled tiles (q_pe is a TMA tile).
 //
-// Warp roles per CTA (352 threads): warp 0 = TMA producer (three KV stages),
+// Warp roles per CTA (352 threads): warp 0 = TMA producer (four KV stages),
 // warp 1 = MMA issuer (and TMEM owner), warp 2 = exchange helper, warps 3-10 =
 // softmax in two groups of four warps (one warp per TMEM lane quadrant, one
 // thread per head row). Group g takes the tiles j = g (mod 2) of the range
@@ -65,15 +68,17 @@ constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kGroupThreads = kSoftmaxThreads / 2;      // one thread per head row
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kThreads = 32 * (kFirstSoftmaxWarp + kSoftmaxWarps);
-constexpr int kStages = 3;                // KV ring depth
-constexpr int kQBlock = kHeads * 128;     // 16 KB: 128 rows x 64 bf16, 128B-swizzled
+constexpr int kStages = 4;                // KV ring depth
 constexpr int kKvBlock = kTok * 128;      // 8 KB: 64 tokens x 64 bf16
-constexpr int kKvStage = 5 * kKvBlock;    // 4 ckv blocks (+ kpe on rank 1)
+constexpr int kKpeBlock = kTok * 64;     // 4 KB: 64 tokens x 32 bf16, 64B-swizzled
+constexpr int kKvStage = 4 * kKvBlock + kKpeBlock;  // 4 ckv blocks + the kpe half
+constexpr int kQpeBlock = kHeads * 64;   // 8 KB: 128 rows x 32 bf16, 64B-swizzled
 constexpr int kXBytes = kHeads * kTok * 4;  // one exchange buffer: 128 x 64 fp32
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O half: columns 0..255
 constexpr uint32_t kTmemQ = 256;   // q_nope half, two bf16 per column: 256..383
-constexpr uint32_t kTmemS = 384;   // two score buffers: 384..447, 448..511
+constexpr uint32_t kTmemS = 384;   // score tile: 384..447
+constexpr uint32_t kTmemP = 448;   // P tiles of the two groups: 448..479, 480..511
 constexpr float kRescaleThreshold = 8.f;
 
 // What the producer tells the other roles about the tile in a KV stage.
@@ -93,10 +98,9 @@ struct Ctrl {
 };
 
 struct Lay {
-  static constexpr int QPE = 0;                              // 16 KB (rank 1)
-  static constexpr int KV = QPE + kQBlock;                   // kStages x 40 KB
-  static constexpr int P = KV + kStages * kKvStage;          // 16 KB
-  static constexpr int X = P + kQBlock;                      // 2 x [16][128] float4
+  static constexpr int QPE = 0;                              // 8 KB
+  static constexpr int KV = QPE + kQpeBlock;                 // kStages x 36 KB
+  static constexpr int X = KV + kStages * kKvStage;          // 2 x [16][128] float4
   static constexpr int MR = X + 2 * kXBytes;                 // [2][128] running maximum
   static constexpr int LR = MR + 2 * kHeads * 4;             // [2][128] running sum
   static constexpr int META = LR + 2 * kHeads * 4;           // [kStages] TileMeta
@@ -104,25 +108,26 @@ struct Lay {
   static constexpr int EMPTY = SCAN + 64;                    // [kThreads] rows without tokens
   static constexpr int CTRL = EMPTY + kThreads * 4;
   static constexpr int BAR = CTRL + 128;
-  static constexpr int NBAR = 28;
+  static constexpr int NBAR = 30;
   static constexpr int TOTAL = BAR + NBAR * 8 + 1024;        // + alignment slack
 };
 enum {
-  B_QPE = 0,    // q_pe tile of the current row landed (rank 1)
+  B_QPE = 0,    // q_pe tile of the current row landed
   B_QT = 1,     // q_nope half of the current row stored in TMEM
   B_KVF = 2,    // [kStages] KV stage full
-  B_KVE = 5,    // [kStages] KV stage consumed by the PV MMA
-  B_SF = 8,     // [2] score buffer written
-  B_SE = 10,    // [2] score buffer read
-  B_PF = 12,    // P tile written
-  B_PE = 13,    // PV MMA done
-  B_XF = 14,    // [2] peer scores landed (local expect_tx + the peer's bytes)
-  B_XE = 16,    // [2] the peer has read what this CTA sent into its buffer
-  B_XR = 18,    // [2] this CTA's softmax group has read the buffer
-  B_MRF = 20,   // [2] group g has published the running maximum of its latest tile
-  B_LRF = 22,   // [2] group g has published the running sum of its latest tile
-  B_OFREE = 24, // a row's epilogue has read O (the next row may overwrite it)
-  B_EPI = 25,   // [2] group g has written a partial (before the row counter counts it)
+  B_KVE = 6,    // [kStages] KV stage consumed by the PV MMA
+  B_SF = 10,    // [2] score tile of a tile of that parity written (per parity, so
+                //     that each group waits on its own tiles' phases only)
+  B_SE = 12,    // score tile read (the next one may be written)
+  B_PF = 13,    // [2] P of a tile of that parity written (TMEM)
+  B_PE = 15,    // [2] PV MMA of a tile of that parity done (its P buffer is free)
+  B_XF = 17,    // [2] peer scores landed (local expect_tx + the peer's bytes)
+  B_XE = 19,    // [2] the peer has read what this CTA sent into its buffer
+  B_XR = 21,    // [2] this CTA's softmax group has read the buffer
+  B_MRF = 23,   // [2] group g has published the running maximum of its latest tile
+  B_LRF = 25,   // [2] group g has published the running sum of its latest tile
+  B_OFREE = 27, // a row's epilogue has read O (the next row may overwrite it)
+  B_EPI = 28,   // [2] group g has written a partial (before the row counter counts it)
 };
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -270,27 +275,54 @@ __device__ void mla_merge_row(const MlaParams &p, int b, int r, int c_first, int
     lse_out[h] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
   }
   __syncthreads();
-  // out[b][h][256 r + 4c .. +3] for c < 64
-  for (int i = threadIdx.x; i < kHeads * 64; i += blockDim.x) {
-    const int h = i / 64, c = i % 64;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < n_seg; ++s) {
-      const float e = w[s * kHeads + h];
-      if (e != 0.f) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                                    p.o_part + ((slot0 + s) * kHeads + h) * 512 + r * 256) +
-                                c);
-        acc.x += e * v.x;
-        acc.y += e * v.y;
-        acc.z += e * v.z;
-        acc.w += e * v.w;
+  // out[b][h][256 r + 4c .. +3] for c < 64: each thread sums 8 float4 outputs
+  // at a time, two slots' loads in flight together (the pieces live in L2)
+  constexpr int kU = 8;
+  const int nthr = blockDim.x;
+  for (int base = threadIdx.x; base < kHeads * 64; base += kU * nthr) {
+    float4 acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n_seg; s += 2) {
+      float4 v0[kU], v1[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = min(base + u * nthr, kHeads * 64 - 1), h = i / 64, c = i % 64;
+        const float4 *src = reinterpret_cast<const float4 *>(p.o_part + ((slot0 + s) * kHeads + h) * 512 + r * 256) + c;
+        v0[u] = __ldcg(src);
+        v1[u] = s + 1 < n_seg ? __ldcg(src + kHeads * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int h = min(base + u * nthr, kHeads * 64 - 1) / 64;
+        const float e0 = w[s * kHeads + h], e1 = s + 1 < n_seg ? w[(s + 1) * kHeads + h] : 0.f;
+        // a piece with weight 0 (no valid token) may hold anything: skip it
+        if (e0 != 0.f) {
+          acc[u].x += e0 * v0[u].x;
+          acc[u].y += e0 * v0[u].y;
+          acc[u].z += e0 * v0[u].z;
+          acc[u].w += e0 * v0[u].w;
+        }
+        if (e1 != 0.f) {
+          acc[u].x += e1 * v1[u].x;
+          acc[u].y += e1 * v1[u].y;
+          acc[u].z += e1 * v1[u].z;
+          acc[u].w += e1 * v1[u].w;
+        }
       }
     }
-    const float iv = inv[h];
-    __nv_bfloat162 *dst =
-        reinterpret_cast<__nv_bfloat162 *>(p.out + ((int64_t)b * kHeads + h) * 512 + r * 256 + 4 * c);
-    dst[0] = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
-    dst[1] = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * nthr;
+      if (i < kHeads * 64) {
+        const int h = i / 64, c = i % 64;
+        const float iv = inv[h];
+        __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(p.out + ((int64_t)b * kHeads + h) * 512 +
+                                                                 r * 256 + 4 * c);
+        dst[0] = __floats2bfloat162_rn(acc[u].x * iv, acc[u].y * iv);
+        dst[1] = __floats2bfloat162_rn(acc[u].z * iv, acc[u].w * iv);
+      }
+    }
   }
   if (r == 0 && threadIdx.x < kHeads && p.lse) p.lse[(int64_t)b * kHeads + threadIdx.x] = lse_out[threadIdx.x];
   if (threadIdx.x == 0) p.counters[b * 2 + r] = 0u;  // ready for the next call
@@ -314,7 +346,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = r ^ 1u;
   const int cl = blockIdx.x >> 1, NC = gridDim.x >> 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = r == 0 ? 4 : 5;  // 64-wide KV blocks this CTA streams
 
   // ---------------------------------------------------------------- the cluster's tile range
   uint32_t dev_err = 0;
@@ -385,13 +416,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_QPE], 1);
     mbar_init(&bar[B_QT], kGroupThreads);
     mbar_init(&bar[B_OFREE], kGroupThreads);
+    mbar_init(&bar[B_SE], kGroupThreads);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar[B_KVF + s], 1);
       mbar_init(&bar[B_KVE + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar[B_PE + s], 1);
       mbar_init(&bar[B_SF + s], 1);
-      mbar_init(&bar[B_SE + s], kGroupThreads);
+      mbar_init(&bar[B_PF + s], kGroupThreads);
       mbar_init(&bar[B_XF + s], 1);  // the local expect_tx; the bytes come from the peer
       mbar_init(&bar[B_XE + s], 1);  // the peer helper's arrival
       mbar_init(&bar[B_XR + s], kGroupThreads);
@@ -399,8 +432,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_LRF + s], kGroupThreads);
       mbar_init(&bar[B_EPI + s], kGroupThreads);
     }
-    mbar_init(&bar[B_PF], kGroupThreads);
-    mbar_init(&bar[B_PE], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -416,7 +447,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   uint8_t *sQpe = smem + Lay::QPE;
   uint8_t *sKV = smem + Lay::KV;
-  uint8_t *sP = smem + Lay::P;
   float *sX = reinterpret_cast<float *>(smem + Lay::X);
   float *sMr = reinterpret_cast<float *>(smem + Lay::MR);
   float *sLr = reinterpret_cast<float *>(smem + Lay::LR);
@@ -461,17 +491,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t *dst = sKV + st * kKvStage;
         if (bad) {
           // a skipped page: zeros instead of stale data (its scores are masked)
-          for (int e = 0; e < nkb * kKvBlock / 16; ++e)
+          for (int e = 0; e < kKvStage / 16; ++e)
             reinterpret_cast<uint4 *>(dst)[e] = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(&bar[B_KVF + st], 0);
         } else {
-          mbar_arrive_expect_tx(&bar[B_KVF + st], (uint32_t)nkb * kKvBlock);
+          mbar_arrive_expect_tx(&bar[B_KVF + st], (uint32_t)kKvStage);
           for (int c = 0; c < 4; ++c)
             tma_load_2d(dst + c * kKvBlock, &ckv_map, &bar[B_KVF + st], 64 * (4 * (int)r + c),
                         page * kTok, kv_policy);
-          if (r == 1)
-            tma_load_2d(dst + 4 * kKvBlock, &kpe_map, &bar[B_KVF + st], 0, page * kTok, kv_policy);
+          tma_load_2d(dst + 4 * kKvBlock, &kpe_map, &bar[B_KVF + st], 32 * (int)r, page * kTok,
+                      kv_policy);
         }
         ++issued_kv;
         if (++st == kStages) st = 0, ph ^= 1;
@@ -497,11 +527,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idesc_qk = umma_idesc_bf16(128, kTok, false, false);
       const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
       const uint64_t q_policy = l2_policy_evict_last();
-      // Scores of tile k need its KV stage, the score buffer read back from
-      // tile k - 2 and, on a row's first tile, that row's q (TMEM, and q_pe on
-      // rank 1, loaded here once the previous row's scores are complete). PV of
-      // tile k needs its P and, on a row's first tile, the previous row's O
-      // read out. The issuer polls both and issues what is ready. (No barrier
+      // Scores of tile k need its KV stage, the scores of tile k - 1 read out
+      // and, on a row's first tile, that row's q (q_nope in TMEM, and q_pe,
+      // loaded here once the previous row's scores are complete). PV of tile k
+      // needs its P and, on a row's first tile, the previous row's O read out. The issuer polls both and issues what is ready. (No barrier
       // polled here can run a phase ahead of the tile being tested.)
       int qk_seg = -1, pv_seg = -1;  // row segment of the latest QK / PV
       bool ok = true;
@@ -514,35 +543,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const TileMeta m = meta[k % kStages];
           const bool first = (m.flags & kFirst) != 0;
           const int seg = first ? qk_seg + 1 : qk_seg;
-          bool ready = k < 2 || mbar_test(&bar[B_SE + (k & 1)], ((k >> 1) - 1) & 1);
+          bool ready = k < 1 || mbar_test(&bar[B_SE], (k - 1) & 1);
           if (first) {
-            if (r == 1 && qpe_seg < seg) {
+            if (qpe_seg < seg) {
               if (k == 0 || mbar_test(&bar[B_SF + ((k - 1) & 1)], ((k - 1) >> 1) & 1)) {
-                mbar_arrive_expect_tx(&bar[B_QPE], kQBlock);
-                tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 0, m.b * kHeads, q_policy);
+                mbar_arrive_expect_tx(&bar[B_QPE], kQpeBlock);
+                tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b * kHeads, q_policy);
                 qpe_seg = seg;
               }
               ready = false;
             }
-            ready = ready && mbar_test(&bar[B_QT], seg & 1) &&
-                    (r == 0 || mbar_test(&bar[B_QPE], seg & 1));
+            ready = ready && mbar_test(&bar[B_QT], seg & 1) && mbar_test(&bar[B_QPE], seg & 1);
           }
           if (ready) {
             tc_fence_after();
             const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
-            const uint32_t d = tmem + kTmemS + 64 * (k & 1);
+            const uint32_t d = tmem + kTmemS;
             for (int c = 0; c < 4; ++c)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
                              umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
                              (c | kk) != 0);
-            if (r == 1) {
+            {
               const uint32_t q = smem_u32(sQpe);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16_ss(d, umma_desc_sw128(q + kk * 32, 16, 1024),
-                             umma_desc_sw128(kv + 4 * kKvBlock + kk * 32, 16, 1024), idesc_qk, true);
+              for (int kk = 0; kk < 2; ++kk)
+                umma_bf16_ss(d, umma_desc_sw64(q + kk * 32), umma_desc_sw64(kv + 4 * kKvBlock + kk * 32),
+                             idesc_qk, true);
             }
             umma_commit(&bar[B_SF + (k & 1)]);
             qk_seg = seg;
@@ -551,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         const int j = issued_pv;
-        if (j < issued_qk && mbar_test(&bar[B_PF], j & 1)) {
+        if (j < issued_qk && mbar_test(&bar[B_PF + (j & 1)], (j >> 1) & 1)) {
           const TileMeta m = meta[j % kStages];
           const bool first = (m.flags & kFirst) != 0;
           const int seg = first ? pv_seg + 1 : pv_seg;
@@ -559,13 +587,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int st = j % kStages;
             const uint32_t v = smem_u32(sKV + st * kKvStage);
-            const uint32_t pa = smem_u32(sP);
+            const uint32_t pa = tmem + kTmemP + 32 * (j & 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ss(tmem + kTmemO, umma_desc_sw128(pa + kk * 32, 16, 1024),
-                           umma_desc_sw128(v + kk * 2048, kKvBlock, 1024), idesc_pv,
-                           kk != 0 || !first);
-            umma_commit(&bar[B_PE]);
+              umma_bf16_ts(tmem + kTmemO, pa + 8 * kk, umma_desc_sw128(v + kk * 2048, kKvBlock, 1024),
+                           idesc_pv, kk != 0 || !first);
+            umma_commit(&bar[B_PE + (j & 1)]);
             umma_commit(&bar[B_KVE + st]);
             pv_seg = seg;
             ++issued_pv;
@@ -658,13 +685,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float v[16];
-        tmem_ld16(tmem + lane_off + kTmemS + 64 * g + 16 * q, v);
+        tmem_ld16(tmem + lane_off + kTmemS + 16 * q, v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) s[16 * q + e] = v[e];
       }
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&bar[B_SE + g]);
+      mbar_arrive(&bar[B_SE]);
       // ---- exchange the partial scores with the peer CTA
       if (ii >= 1 && !(ok = warp_wait_cluster(&bar[B_XE + g], (ii - 1) & 1))) break;
 #pragma unroll
@@ -750,10 +777,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                           ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       sLr[g * kHeads + h] = l_new;
       mbar_arrive(&bar[B_LRF + g]);
-      // ---- PV of the previous tile must be done before O or P change
-      if (i >= 1 && !(ok = warp_wait(&bar[B_PE], (i - 1) & 1))) break;
+      // ---- P into this group's TMEM buffer (the A operand of the tile's PV),
+      // free once the PV of the group's previous tile is done
+      if (i >= 2 && !(ok = warp_wait(&bar[B_PE + g], ((i >> 1) - 1) & 1))) break;
       tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(pk[16 * c + e]);
+        tmem_st16(tmem + lane_off + kTmemP + 32 * g + 16 * c, v);
+      }
+      // ---- a grown maximum rescales O, after the PV of the previous tile
       if (!first && __any_sync(0xffffffffu, need)) {
+        if (!(ok = warp_wait(&bar[B_PE + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
+        tc_fence_after();
         const float alpha = need ? ex2(m_prev - m_new) : 1.f;  // 0 when m_prev is -inf
         for (int c = 0; c < 256; c += 16) {
           float v[16];
@@ -763,14 +801,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e) v[e] *= alpha;
           tmem_st16(tmem + lane_off + kTmemO + c, v);
         }
-        tmem_wait_st();
       }
-      // P row h (bf16, 64 tokens = 128 bytes), 128B-swizzled K-major A operand
-      uint8_t *prow = sP + h * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(prow + ((c ^ (h & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      tmem_wait_st();
       if (nval < kTok) {
         // value rows past the valid tokens may hold anything: zero them
         uint8_t *kv = sKV + (i % kStages) * kKvStage;
@@ -778,31 +810,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int t = nval + e / 32, blk = (e / 8) % 4, c = e % 8;
           *reinterpret_cast<uint4 *>(kv + blk * kKvBlock + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar[B_PF]);
+      mbar_arrive(&bar[B_PF + g]);
       if (m.flags & kLast) {
         // ---- end of the row's piece: O / l of this value half
-        if (!(ok = warp_wait(&bar[B_PE], i & 1))) break;
+        if (!(ok = warp_wait(&bar[B_PE + (i & 1)], (i >> 1) & 1))) break;
         tc_fence_after();
         const bool full = (m.flags & kFullRow) != 0;
         const float inv = l_new > 0.f ? 1.f / l_new : 0.f;
         const float lse = l_new > 0.f ? (m_new + __log2f(l_new)) * 0.69314718055994531f : neg_inf();
         const int64_t slot = (int64_t)m.b + cl;
-        for (int c = 0; c < 256; c += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_off + kTmemO + c, v);
+        for (int c0 = 0; c0 < 256; c0 += 64) {
+          float v[64];  // four loads per wait
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float t[16];
+            tmem_ld16(tmem + lane_off + kTmemO + c0 + 16 * q, t);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[16 * q + e] = t[e];
+          }
           tmem_wait_ld();
           if (full) {
-            __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
-                p.out + ((int64_t)m.b * kHeads + h) * 512 + r * 256 + c);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)m.b * kHeads + h) * 512 + r * 256 + c0);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = __floats2bfloat162_rn(v[2 * e] * inv, v[2 * e + 1] * inv);
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_uint4(pack_bf16(v[8 * e] * inv, v[8 * e + 1] * inv),
+                                  pack_bf16(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
+                                  pack_bf16(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
+                                  pack_bf16(v[8 * e + 6] * inv, v[8 * e + 7] * inv));
           } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + r * 256 + c);
+            float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + r * 256 + c0);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
+            for (int e = 0; e < 16; ++e)
               dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
           }
         }
@@ -850,7 +891,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0) {
       if (issued_qk > 0)
         mbar_wait_bounded(&bar[B_SF + ((issued_qk - 1) & 1)], ((issued_qk - 1) >> 1) & 1, kWaitLimitNs);
-      if (issued_pv > 0) mbar_wait_bounded(&bar[B_PE], (issued_pv - 1) & 1, kWaitLimitNs);
+      if (issued_pv > 0)
+        mbar_wait_bounded(&bar[B_PE + ((issued_pv - 1) & 1)], ((issued_pv - 1) >> 1) & 1, kWaitLimitNs);
       if (qpe_seg >= 0) mbar_wait_bounded(&bar[B_QPE], qpe_seg & 1, kWaitLimitNs);
     }
     __syncthreads();

@@ -237,6 +237,18 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, u
 }
 
 // Arrives on `bar` once all previously issued tcgen05.mma of this thread complete.
+// Descriptor of a K-major operand in 64-byte-swizzled rows (TMA SWIZZLE_64B):
+// rows of 32 bf16, 8-row groups 512 bytes apart; a K=16 step is +32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;           // leading byte offset: unused for this layout
+  d |= (uint64_t)(512 >> 4) << 32;  // stride byte offset: 8 rows x 64 B
+  d |= (uint64_t)1 << 46;           // descriptor version
+  d |= (uint64_t)4 << 61;           // 64-byte swizzle
+  return d;
+}
+
 // The same with A read from tensor memory: row m of A in lane m, each 32-bit
 // column holding two consecutive k elements (the lower k in the low half), so
 // one K=16 step spans 8 columns starting at a_tmem.
