@@ -44,7 +44,14 @@ namespace {
 
 constexpr int kTile = 64;             // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// With one n-tile (up to 8 query heads per kv head) a sixth warp takes the
+// row-counter atomics of partial segments off the consumers; with two n-tiles
+// the consumers' registers leave no room for it and thread 0 does them.
+template <int NT>
+constexpr bool has_helper() { return NT == 1; }
+template <int NT>
+constexpr int threads_for() { return (kConsumerWarps + 1 + (has_helper<NT>() ? 1 : 0)) * 32; }
+constexpr int kMaxThreads = (kConsumerWarps + 2) * 32;
 constexpr int kD = 128;               // head dimension
 constexpr int kRedStride = kD + 4;    // padded row of the epilogue reduction buffer
 constexpr uint32_t kConsumerBar = 1;  // named barrier of the 128 consumer threads
@@ -64,9 +71,12 @@ struct Cfg {
   static constexpr int oMeta = oEmpty + 8 * kStages;
   static constexpr int oStats = oMeta + 24 * kStages;        // m, l per (warp, g)
   static constexpr int oScan = oStats + 2 * kConsumerWarps * 16 * 4;
-  static constexpr int oFlags = oScan + 16 * 4;              // 16 ints (see the kernel)
-  static constexpr int oMergeBar = oFlags + 16 * 4;          // 2 mbarriers of the merge staging
-  static constexpr int kTotal = oMergeBar + 16 + 1024;       // + alignment slack
+  static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
+  static constexpr int oMergeBar = oFlags + 32 * 4;          // 2 mbarriers of the merge staging,
+                                                             // 2 partial-segment, 1 helper-done
+  static constexpr int kTotal = oMergeBar + 5 * 8 + 1024;    // + alignment slack
+  // the segment epilogue's per-warp partials fit in the segment's last stage
+  static constexpr bool kStageScratch = kConsumerWarps * 8 * NT * kRedStride * 4 <= 2 * kTileBytes;
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -122,6 +132,7 @@ __device__ __forceinline__ int cta_of(int64_t t, int64_t T, int C) {
 
 // Inclusive scan over the block's threads; returns the block total in *total.
 __device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int *total) {
+  const int nwarps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -131,7 +142,7 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int *to
   if (lane == 31) scratch[warp] = v;
   __syncthreads();
   int before = 0, sum = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
+  for (int w = 0; w < nwarps; ++w) {
     const int t = scratch[w];
     if (w < warp) before += t;
     sum += t;
@@ -145,6 +156,7 @@ struct TileDesc {
   int unit, b, h, n_valid, j, tiles;  // unit, its row / head, length, tile index, tile count
   int64_t P;                          // global index of the unit's first tile
   int c_first, n_seg;                 // CTAs holding the unit's segments
+  int wi;                             // position in this CTA's processing order
 };
 
 // ------------------------------------------------------------------ consumer helpers
@@ -336,12 +348,81 @@ __device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_firs
 
 // ------------------------------------------------------------------ kernel
 
+// One warp merges a unit held by at most kWarpMergeSegs pieces (G <= 8): lane l
+// owns head dims 4l..4l+3; per head the pieces' LSE give weights
+// exp(lse_s - max) and the output is the weighted mean of their normalised O.
+constexpr int kWarpMergeSegs = 4;
+__device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c_first, int n_seg,
+                                             int G) {
+  const int lane = threadIdx.x & 31;
+  const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
+  const int64_t slot0 = (int64_t)unit + c_first;
+  const float my_lse = lane < n_seg * G ? __ldcg(p.lse_part + slot0 * G + lane) : neg_inf();
+  const float4 *o_base = reinterpret_cast<const float4 *>(p.o_part + slot0 * G * kD);
+  __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    float4 v[kWarpMergeSegs];
+#pragma unroll
+    for (int s = 0; s < kWarpMergeSegs; ++s)
+      v[s] = s < n_seg ? __ldcg(o_base + ((int64_t)s * G + g) * (kD / 4) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    float l[kWarpMergeSegs], M = neg_inf();
+#pragma unroll
+    for (int s = 0; s < kWarpMergeSegs; ++s) {
+      l[s] = __shfl_sync(0xffffffffu, my_lse, min(s * G + g, 31));
+      if (s < n_seg) M = fmaxf(M, l[s]);
+    }
+    float sum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kWarpMergeSegs; ++s) {
+      const float w = (s < n_seg && l[s] != neg_inf() && M != neg_inf())
+                          ? ex2((l[s] - M) * 1.4426950408889634f)
+                          : 0.f;
+      if (w != 0.f) {  // a piece of weight 0 may hold anything
+        sum += w;
+        acc.x += w * v[s].x;
+        acc.y += w * v[s].y;
+        acc.z += w * v[s].z;
+        acc.w += w * v[s].w;
+      }
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    *reinterpret_cast<uint2 *>(out + (int64_t)g * kD + 4 * lane) =
+        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+    if (lane == 0 && p.lse)
+      p.lse[(int64_t)b * p.num_q_heads + h * G + g] =
+          sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+  }
+  if (lane == 0) p.counters[unit] = 0u;  // ready for the next call
+}
+
+// Counts one finished partial segment of `unit` (release: its writes are
+// visible before the count); the segment that completes the count records the
+// unit's merge for this CTA (at most two: a range holds at most two partial
+// segments, its first and its last).
+__device__ __forceinline__ bool count_segment(const GqaParams &p, int unit, int n_seg) {
+  return atomic_add_acq_rel_gpu(p.counters + unit, 1u) == (unsigned)(n_seg - 1);
+}
+__device__ __forceinline__ void record_merge(volatile int *flags, int unit, int c_first, int n_seg) {
+  if (flags[12] < 2) {
+    const int k = flags[12];
+    flags[6 + 3 * k] = unit;
+    flags[7 + 3 * k] = c_first;
+    flags[8 + 3 * k] = n_seg;
+    flags[12] = k + 1;
+  }
+}
+
 template <bool FP8, int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for<NT>(), 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap, const GqaParams p) {
   using C = Cfg<FP8, NT>;
+  constexpr int kThreads = threads_for<NT>();
+  constexpr bool kHelper = has_helper<NT>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -356,8 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *scan = reinterpret_cast<int *>(smem + C::oScan);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + C::oFlags);
   // flags: [0] abort, [2] start unit, [3] start tile, [4..5] start P (int64),
-  //        [6..11] up to two merges owed (unit, c_first, n_seg), [12] their count
+  //        [6..11] up to two merges owed (unit, c_first, n_seg), [12] their count,
+  //        [14..19] the range's partial segments (unit, c_first, n_seg) handed to
+  //        the helper warp, [20] unit holding the range's last tile, [21] whether
+  //        its segment here is partial, [22..23] its first tile (int64)
   uint64_t *merge_bar = reinterpret_cast<uint64_t *>(smem + C::oMergeBar);
+  uint64_t *part_bar = merge_bar + 2;  // [2] a partial segment is in global memory
+  uint64_t *helper_done = merge_bar + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
@@ -365,11 +451,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = blockIdx.x;
   uint32_t dev_err = 0;
 
-  // ---- the schedule: this CTA's range of the global tile sequence
+  // ---- the schedule: this CTA's range of the global tile sequence. Thread t
+  // takes the consecutive units [t*per, t*per + per): one scan gives each
+  // thread the first tile of its block, and a second walk over its own units
+  // (their lengths now in L1) finds the range's first and last unit.
+  if (threadIdx.x == 0) {
+    flags[0] = 0;
+    flags[2] = -1;
+    flags[12] = 0;
+  }
+  const int per = (U + kThreads - 1) / kThreads;
+  const int u_beg = min(U, (int)threadIdx.x * per), u_end = min(U, u_beg + per);
   int local = 0;
-  for (int u = threadIdx.x; u < U; u += kThreads) local += unit_info(p, u, dev_err).tiles;
+  for (int u = u_beg; u < u_end; ++u) local += unit_info(p, u, dev_err).tiles;
   int T32 = 0;
-  block_inclusive_scan(local, scan, &T32);
+  const int incl = block_inclusive_scan(local, scan, &T32);
   const int64_t T = T32;
   // Never more ranges than tiles, so every working CTA holds at least one tile
   // and a unit's segments come from consecutive CTAs c_first..c_last.
@@ -377,36 +473,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t lo = cta < CTAS ? (int64_t)cta * T / CTAS : 0;
   const int64_t hi = cta < CTAS ? (int64_t)(cta + 1) * T / CTAS : 0;
   const int owner_of_tail = CTAS > 0 ? CTAS - 1 : 0;  // writes empty units past the last tile
-  if (threadIdx.x == 0) {
-    flags[0] = 0;
-    flags[2] = -1;
-    flags[12] = 0;
-  }
   {
-    int64_t base = 0;
-    for (int u0 = 0; u0 < U; u0 += kThreads) {
-      const int u = u0 + threadIdx.x;
-      UnitInfo x{};
-      if (u < U) x = unit_info(p, u, dev_err);
-      const int t_u = u < U ? x.tiles : 0;
-      int total = 0;
-      const int incl = block_inclusive_scan(t_u, scan, &total);
-      const int64_t Pu = base + incl - t_u;
-      if (u < U) {
-        if (t_u > 0 && Pu <= lo && lo < Pu + t_u) {
-          flags[2] = u;
-          flags[3] = (int)(lo - Pu);
-          *reinterpret_cast<volatile int64_t *>(flags + 4) = Pu;
-        }
-        // a unit without tiles is written here by the CTA whose range holds its start
-        if (t_u == 0 && ((Pu >= lo && Pu < hi) || (Pu >= T && cta == owner_of_tail))) {
-          const int64_t row0 = (int64_t)x.b * p.num_q_heads + x.h * G;
-          for (int e = 0; e < G * kD; ++e) p.out[row0 * kD + e] = __float2bfloat16(0.f);
-          if (p.lse)
-            for (int g = 0; g < G; ++g) p.lse[row0 + g] = neg_inf();
-        }
+    int64_t Pu = incl - local;
+    uint32_t ignored = 0;
+    for (int u = u_beg; u < u_end; ++u) {
+      const UnitInfo x = unit_info(p, u, ignored);
+      const int t_u = x.tiles;
+      if (t_u > 0 && Pu <= lo && lo < Pu + t_u) {
+        flags[2] = u;
+        flags[3] = (int)(lo - Pu);
+        *reinterpret_cast<volatile int64_t *>(flags + 4) = Pu;
       }
-      base += total;
+      if (t_u > 0 && Pu < hi && hi <= Pu + t_u) {
+        // the unit holding the last tile: its segment here is partial when
+        // the unit goes on past this range or started before it
+        flags[20] = u;
+        flags[21] = (Pu + t_u > hi || Pu < lo) ? 1 : 0;
+        *reinterpret_cast<volatile int64_t *>(flags + 22) = Pu;
+      }
+      // a unit without tiles is written here by the CTA whose range holds its start
+      if (t_u == 0 && ((Pu >= lo && Pu < hi) || (Pu >= T && cta == owner_of_tail))) {
+        const int64_t row0 = (int64_t)x.b * p.num_q_heads + x.h * G;
+        for (int e = 0; e < G * kD; ++e) p.out[row0 * kD + e] = __float2bfloat16(0.f);
+        if (p.lse)
+          for (int g = 0; g < G; ++g) p.lse[row0 + g] = neg_inf();
+      }
+      Pu += t_u;
     }
   }
   const int ntiles = (int)(hi - lo);
@@ -422,6 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&merge_bar[0], 1);
     mbar_init(&merge_bar[1], 1);
+    mbar_init(&part_bar[0], kConsumerWarps * 32);
+    mbar_init(&part_bar[1], kConsumerWarps * 32);
+    mbar_init(helper_done, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -440,42 +535,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int P = p.page_size;
     const int pages_per_tile = p.paged ? (P >= kTile ? 1 : kTile / P) : 1;
 
-    // walker over (unit, tile) starting at this CTA's first tile
+    // Walker over (unit, tile) in processing order. When the range ends in the
+    // head of a unit that goes on into the next CTA, that segment is streamed
+    // first and the walk then jumps back to lo: both pieces of such a unit are
+    // then finished early in their CTAs, so its merge (by the helper warp)
+    // overlaps streaming instead of trailing the range.
+    auto set_at = [&](TileDesc &d, int u, int j, int64_t P0) {
+      UnitInfo x = unit_info(p, u, dev_err);
+      d.unit = u;
+      d.b = x.b;
+      d.h = x.h;
+      d.n_valid = x.n_valid;
+      d.tiles = x.tiles;
+      d.j = j;
+      d.P = P0;
+      d.c_first = cta_of(d.P, T, CTAS);
+      d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;
+    };
+    const int last_u = flags[20];
+    const int64_t last_P = *reinterpret_cast<volatile int64_t *>(flags + 22);
+    const bool reorder = kHelper && last_u != start_u && flags[21];
+    const int i_jump = reorder ? (int)(hi - last_P) : ntiles;  // position of the jump back to lo
     TileDesc cur;
-    {
-      UnitInfo x = unit_info(p, start_u, dev_err);
-      cur.unit = start_u;
-      cur.b = x.b;
-      cur.h = x.h;
-      cur.n_valid = x.n_valid;
-      cur.tiles = x.tiles;
-      cur.j = start_j;
-      cur.P = start_P;
-      cur.c_first = cta_of(cur.P, T, CTAS);
-      cur.n_seg = cta_of(cur.P + cur.tiles - 1, T, CTAS) - cur.c_first + 1;
-    }
+    if (reorder) set_at(cur, last_u, 0, last_P);
+    else set_at(cur, start_u, start_j, start_P);
+    cur.wi = 0;
     // Page (paged) or block (sparse) id number k of a tile; -1 when absent or
-    // invalid (an invalid one also sets its error bit and is skipped).
+    // invalid (an invalid one also sets its error bit and is skipped). The
+    // check is a select, not a branch, so the lookahead's loads stay in flight
+    // together instead of each waiting for the one before.
     auto load_id = [&](const TileDesc &d, int k) -> int {
       if (p.sparse_block_size > 0) {
         const int e = d.j / (p.sparse_block_size / kTile);
         const int blk = p.kv_idx[(int64_t)d.unit * p.max_sparse_blocks + e];
-        if (blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len) {
-          dev_err |= DA_DEVERR_SPARSE_INDEX;
-          return -1;
-        }
-        return blk;
+        const bool bad = blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len;
+        dev_err |= bad ? DA_DEVERR_SPARSE_INDEX : 0u;
+        return bad ? -1 : blk;
       }
       const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
       if (tok0 >= d.n_valid) return -1;
       const int page = p.block_table[(int64_t)d.b * p.max_pages + tok0 / P];
-      if (page < 0 || page >= p.num_pages) {
-        dev_err |= DA_DEVERR_PAGE_INDEX;
-        return -1;
-      }
-      return page;
+      const bool bad = page < 0 || page >= p.num_pages;
+      dev_err |= bad ? DA_DEVERR_PAGE_INDEX : 0u;
+      return bad ? -1 : page;
     };
     auto advance = [&](TileDesc &d) {
+      if (++d.wi == i_jump) {
+        set_at(d, start_u, start_j, start_P);
+        return;
+      }
       if (++d.j < d.tiles) return;
       d.P += d.tiles;
       int u = d.unit;
@@ -503,10 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int idq = -1;
     TileDesc ahead = cur;
     if (needs_ids) {
+      // walk the first ahead_n tiles, each lane group keeping its tile, then
+      // load every lane's id at once (one load in flight per lane)
+      TileDesc mine = ahead;
+      const int my_k = lane / L;
       for (int k = 0; k < ahead_n && k < ntiles; ++k) {
-        if (lane >= k * L && lane < (k + 1) * L) idq = load_id(ahead, lane - k * L);
+        if (k == my_k) mine = ahead;
         if (k + 1 < ntiles) advance(ahead);
       }
+      if (my_k < ahead_n && my_k < ntiles) idq = load_id(mine, lane - my_k * L);
     }
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
@@ -560,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lane == 0) {
-        const bool first = (i == 0) || (cur.j == 0);
-        const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
+        const bool first = (i == 0) || (i == i_jump) || (cur.j == 0);
+        const bool last = (i + 1 == ntiles) || (i + 1 == i_jump) || (cur.j + 1 == cur.tiles);
         StageMeta m;
         m.valid = valid;
         m.unit = cur.unit;
@@ -604,6 +717,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (i + 1 < ntiles) advance(cur);
     }
+  } else if (warp > kConsumerWarps) {
+    // ======================================================= helper (kHelper only)
+    // Counts this range's partial segments as the consumers finish them and,
+    // when one completes a unit of at most kWarpMergeSegs pieces, merges the
+    // unit right away (larger merges are left to the consumers' end).
+    // Partial segments: the first (its unit started before lo, or goes on past
+    // hi when the range holds a single unit) and the last.
+    const int n_partial = flags[20] == start_u ? flags[21] : (start_j > 0 ? 1 : 0) + flags[21];
+    bool ok = true;
+    for (int k = 0; k < n_partial; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&part_bar[k & 1], (k >> 1) & 1, kWaitLimitNs))))
+        break;
+      const int unit = flags[14 + 3 * k], c_first = flags[15 + 3 * k], n_seg = flags[16 + 3 * k];
+      const bool last = __shfl_sync(0xffffffffu, lane == 0 ? count_segment(p, unit, n_seg) : false, 0);
+      __syncwarp();  // lane 0's acquire covers the whole warp's reads of the pieces
+      if (last) {
+        if (n_seg <= kWarpMergeSegs) merge_unit_warp(p, unit, c_first, n_seg, G);
+        else if (lane == 0) record_merge(flags, unit, c_first, n_seg);
+      }
+    }
+    if (!ok) {
+      dev_err |= DA_DEVERR_TIMEOUT;
+      if (lane == 0) flags[0] = 1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(helper_done);
   } else {
     // ======================================================= consumers
     const int q4 = lane & 3;   // owns heads g = nt*8 + 2*q4 + {0,1}
@@ -635,6 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
     bool ok = true;
+    int npart = 0;  // partial segments written so far
 
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
@@ -810,10 +950,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-
-      if (!(m.flags & kLast)) continue;
+      if (!(m.flags & kLast)) {
+        if (lane == 0) mbar_arrive(&empty[st]);
+        continue;
+      }
       // ======================= segment epilogue (consumer threads only)
+      // (the segment's last stage is released at its end: it may serve as scratch)
       const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -831,35 +973,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
-      // the warps add their rescaled O^T into one buffer, one warp at a time
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        if (warp == w) {
+      // each warp's O^T rescaled to the group maximum: into its own region of the
+      // consumed stage when it fits (one barrier), else added into one buffer
+      // one warp at a time
+      float *scr = reinterpret_cast<float *>(ring + (size_t)st * 2 * C::kTileBytes);
+      constexpr int kWarpScr = 8 * NT * kRedStride;
+      auto put = [&](float *dst_base, bool add) {
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int g = nt * 8 + 2 * q4 + e;
-              float M = neg_inf();
+          for (int e = 0; e < 2; ++e) {
+            const int g = nt * 8 + 2 * q4 + e;
+            float M = neg_inf();
 #pragma unroll
-              for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, stat_m[ww * 16 + g]);
-              const float wscale = (M == neg_inf()) ? 0.f : ex2(m_run[nt][e] - M);
-              float *dst = red + (size_t)g * kRedStride;
+            for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, stat_m[ww * 16 + g]);
+            const float wscale = (M == neg_inf()) ? 0.f : ex2(m_run[nt][e] - M);
+            float *dst = dst_base + (size_t)g * kRedStride;
 #pragma unroll
-              for (int mt = 0; mt < 8; ++mt) {
-                const int d0 = FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8;
-                const int d1 = FP8 ? d0 + 1 : d0 + 8;
-                const float v0 = oacc[nt][mt][e] * wscale, v1 = oacc[nt][mt][2 + e] * wscale;
-                if (w == 0) {
-                  dst[d0] = v0;
-                  dst[d1] = v1;
-                } else {
-                  dst[d0] += v0;
-                  dst[d1] += v1;
-                }
+            for (int mt = 0; mt < 8; ++mt) {
+              const int d0 = FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8;
+              const int d1 = FP8 ? d0 + 1 : d0 + 8;
+              const float v0 = oacc[nt][mt][e] * wscale, v1 = oacc[nt][mt][2 + e] * wscale;
+              if (!add) {
+                dst[d0] = v0;
+                dst[d1] = v1;
+              } else {
+                dst[d0] += v0;
+                dst[d1] += v1;
               }
             }
-        }
+          }
+      };
+      if (C::kStageScratch) {
+        put(scr + warp * kWarpScr, false);
         named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+      } else {
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          if (warp == w) put(red, w > 0);
+          named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+        }
       }
       // thread tid (< 128) owns head-dim element d = tid for every g of the group
       const int d = threadIdx.x;
@@ -873,7 +1025,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w)
           L += (M == neg_inf()) ? 0.f : stat_l[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
-        const float o = (L > 0.f) ? red[(size_t)g * kRedStride + d] * vmul / L : 0.f;
+        float acc;
+        if (C::kStageScratch) {
+          acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) acc += scr[w * kWarpScr + (size_t)g * kRedStride + d];
+        } else {
+          acc = red[(size_t)g * kRedStride + d];
+        }
+        const float o = (L > 0.f) ? acc * vmul / L : 0.f;
         const float lse = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf();
         if (whole) {
           const int64_t row = (int64_t)b * p.num_q_heads + h * G + g;
@@ -884,24 +1044,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (d == 0) p.lse_part[slot * G + g] = lse;
         }
       }
-      named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
-      if (!whole && threadIdx.x == 0) {
-        // one release/acquire count per segment; the barrier above ordered all
-        // consumer threads' partial writes before it
-        const unsigned prev = atomic_add_acq_rel_gpu(p.counters + unit, 1u);
-        if (prev == (unsigned)(m.n_seg - 1) && flags[12] < 2) {
-          // this CTA finished the unit's last segment: merge once its range is done
-          const int k = flags[12];
-          flags[6 + 3 * k] = unit;
-          flags[7 + 3 * k] = m.c_first;
-          flags[8 + 3 * k] = m.n_seg;
-          flags[12] = k + 1;
+      // the stage was read through the generic proxy: order that before the
+      // next TMA write into it, then release it
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      if (!whole) {
+        if (kHelper) {
+          // the helper counts the segment (its writes are released by the arrivals)
+          if (threadIdx.x == 0) {
+            flags[14 + 3 * npart] = unit;
+            flags[15 + 3 * npart] = m.c_first;
+            flags[16 + 3 * npart] = m.n_seg;
+          }
+          mbar_arrive(&part_bar[npart & 1]);
+        } else {
+          named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+          if (threadIdx.x == 0 && count_segment(p, unit, m.n_seg)) record_merge(flags, unit, m.c_first, m.n_seg);
         }
+        ++npart;
       }
       reset();
     }
-    // ---- merges this CTA owes (its ring is free now: every tile was consumed)
+    // ---- merges this CTA owes (its ring is free now: every tile was consumed),
+    // known once the helper has counted the partial segments
     if (!ok) flags[0] = 1;
+    if (kHelper && ok && !mbar_wait_bounded(helper_done, 0, kWaitLimitNs)) {
+      ok = false;
+      flags[0] = 1;
+    }
     named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
     uint32_t merge_phase[2] = {0u, 0u};
     const int npending = flags[0] ? 0 : flags[12];  // the same for all consumer threads
@@ -940,7 +1111,7 @@ cudaError_t set_attr() {
 template <bool FP8, int NT>
 void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
             const GqaParams &p, int ctas, cudaStream_t stream) {
-  gqa_split_kernel<FP8, NT><<<ctas, kThreads, Cfg<FP8, NT>::kTotal, stream>>>(kmap, vmap, qmap, p);
+  gqa_split_kernel<FP8, NT><<<ctas, threads_for<NT>(), Cfg<FP8, NT>::kTotal, stream>>>(kmap, vmap, qmap, p);
 }
 
 }  // namespace
@@ -949,7 +1120,7 @@ int gqa_smem_bytes(bool fp8, int group) {
   if (fp8) return group <= 8 ? Cfg<true, 1>::kTotal : Cfg<true, 2>::kTotal;
   return group <= 8 ? Cfg<false, 1>::kTotal : Cfg<false, 2>::kTotal;
 }
-int gqa_threads() { return kThreads; }
+int gqa_threads() { return kMaxThreads; }
 
 int gqa_box_tokens(const da_problem &p) {
   if (p.kv_layout == DA_KV_PAGED && p.page_size < kTile) return p.page_size;
