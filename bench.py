@@ -200,8 +200,12 @@ def _subset(w, rows):
         if k in t:
             t[k] = t[k][idx].contiguous()
     if not w.paged:
-        t["k"] = t["k"][idx].contiguous()
-        t["v"] = t["v"][idx].contiguous()
+        # row selection through a byte view: CPU indexing of float8 tensors is
+        # missing in some PyTorch releases
+        for k in ("k", "v"):
+            x = t[k]
+            t[k] = (x.view(torch.uint8)[idx].contiguous().view(x.dtype)
+                    if x.dtype == torch.float8_e4m3fn else x[idx].contiguous())
     s = copy.copy(w)
     s.batch = len(rows)
     s.tensors = t
