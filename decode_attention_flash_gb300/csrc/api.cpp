@@ -364,9 +364,9 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
     if (cudaMemsetAsync(workspace, 0, sizeof word, s) != cudaSuccess) return DA_ERR_CUDA;
     if ((word & DA_DEVERR_TIMEOUT) && ctx && ctx->planned) {
       auto *ws = reinterpret_cast<uint8_t *>(workspace);
-      const size_t ncount = (size_t)ctx->plan.num_units * (ctx->prob.is_mla ? 2 : 1);
-      if (cudaMemsetAsync(ws + ctx->plan.counters_offset, 0, ncount * 4, s) !=
-          cudaSuccess)
+      // every counter (the region between the counters and the partials)
+      const size_t nbytes = (size_t)(ctx->plan.partial_o_offset - ctx->plan.counters_offset);
+      if (cudaMemsetAsync(ws + ctx->plan.counters_offset, 0, nbytes, s) != cudaSuccess)
         return DA_ERR_CUDA;
     }
     if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;

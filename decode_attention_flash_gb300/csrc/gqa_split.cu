@@ -73,8 +73,8 @@ struct Cfg {
   static constexpr int oScan = oStats + 2 * kConsumerWarps * 16 * 4;
   static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
   static constexpr int oMergeBar = oFlags + 32 * 4;          // 2 mbarriers of the merge staging,
-                                                             // 2 partial-segment, 1 helper-done
-  static constexpr int kTotal = oMergeBar + 5 * 8 + 1024;    // + alignment slack
+                                                             // 2 partial-segment
+  static constexpr int kTotal = oMergeBar + 4 * 8 + 1024;    // + alignment slack
   // the segment epilogue's per-warp partials fit in the segment's last stage
   static constexpr bool kStageScratch = kConsumerWarps * 8 * NT * kRedStride * 4 <= 2 * kTileBytes;
 };
@@ -348,10 +348,192 @@ __device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_firs
 
 // ------------------------------------------------------------------ kernel
 
+// Units held by more than kOneLevelSegs pieces are merged in two levels, so
+// that no merge reads more than about sqrt(n_seg) pieces: consecutive groups of
+// K = ceil(sqrt(n_seg)) pieces, each merged (in place, into the slot of its
+// first piece) by the piece that completes the group's counter, then the
+// group results merged by the group that completes the unit's counter. No
+// CTA ever waits for another.
+constexpr int kOneLevelSegs = 8;
+constexpr int kWarpMergeSegs = 4;  // a unit of at most this many pieces: merged by one warp
+__host__ __device__ inline int merge_group_size(int n_seg) { return ceil_sqrt(n_seg); }
+
+// All threads of the CTA merge n pieces of `unit`, slots slot0 + s * stride
+// (after the stream, shared memory free): the LSEs in one load round, per head
+// the maximum, weights exp(lse_s - max) and their sum in one warp, then the
+// weighted sum of the pieces' normalised O in work items of (output float4, 16
+// pieces), each with its 16 loads in flight, added into shared memory. The
+// result goes to the final output or, as a normalised piece, to slot `dst`.
+// Needs merge_cta_floats(n, G) floats of scratch.
+__host__ __device__ constexpr int merge_cta_floats(int n, int G) {
+  return ((n * G + 2 * G + 3) & ~3) + G * kD;
+}
+__device__ __noinline__ void merge_slots_cta(const GqaParams &p, int unit, int G, int64_t slot0,
+                                             int stride, int n_seg, bool final_out, int64_t dst,
+                                             float *scratch) {
+  const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = nthr >> 5;
+  const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
+  const int nout = G * (kD / 4);                    // float4 outputs of the unit
+  float *w = scratch;                               // [n_seg][G]: LSE, then weights
+  float *mx = w + n_seg * G, *sum = mx + G;         // [G] each
+  float4 *acc = reinterpret_cast<float4 *>(scratch + ((n_seg * G + 2 * G + 3) & ~3));  // [nout]
+  for (int i = tid; i < n_seg * G; i += nthr)
+    w[i] = __ldcg(p.lse_part + (slot0 + (int64_t)(i / G) * stride) * G + i % G);
+  for (int i = tid; i < nout; i += nthr) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  for (int g = warp; g < G; g += nwarps) {
+    float M = neg_inf();
+    for (int s = lane; s < n_seg; s += 32) M = fmaxf(M, w[s * G + g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float ssum = 0.f;
+    for (int s = lane; s < n_seg; s += 32) {
+      const float l = w[s * G + g];
+      const float e = (l == neg_inf() || M == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
+      w[s * G + g] = e;
+      ssum += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (lane == 0) {
+      mx[g] = M;
+      sum[g] = ssum;
+    }
+  }
+  __syncthreads();
+  constexpr int kChunk = 16;
+  const int nch = (n_seg + kChunk - 1) / kChunk;
+  const float4 *src = reinterpret_cast<const float4 *>(p.o_part + slot0 * G * kD);
+  for (int item = tid; item < nout * nch; item += nthr) {
+    const int o = item % nout, s0 = (item / nout) * kChunk, g = o / (kD / 4);
+    float4 v[kChunk];
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k)
+      v[k] = s0 + k < n_seg ? __ldcg(src + (int64_t)(s0 + k) * stride * nout + o)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const float e = s0 + k < n_seg ? w[(s0 + k) * G + g] : 0.f;
+      if (e != 0.f) {  // a piece of weight 0 may hold anything
+        a.x += e * v[k].x;
+        a.y += e * v[k].y;
+        a.z += e * v[k].z;
+        a.w += e * v[k].w;
+      }
+    }
+    if (nch == 1) {
+      acc[o] = a;
+    } else {
+      atomicAdd(&acc[o].x, a.x);
+      atomicAdd(&acc[o].y, a.y);
+      atomicAdd(&acc[o].z, a.z);
+      atomicAdd(&acc[o].w, a.w);
+    }
+  }
+  __syncthreads();  // every piece has been read: `dst` may be one of them
+  if (final_out) {
+    __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
+    for (int o = tid; o < nout; o += nthr) {
+      const int g = o / (kD / 4);
+      const float inv = sum[g] > 0.f ? 1.f / sum[g] : 0.f;
+      const float4 a = acc[o];
+      *reinterpret_cast<uint2 *>(out + 4 * o) =
+          make_uint2(pack_bf16(a.x * inv, a.y * inv), pack_bf16(a.z * inv, a.w * inv));
+    }
+  } else {
+    float4 *out = reinterpret_cast<float4 *>(p.o_part + dst * G * kD);
+    for (int o = tid; o < nout; o += nthr) {
+      const int g = o / (kD / 4);
+      const float inv = sum[g] > 0.f ? 1.f / sum[g] : 0.f;
+      const float4 a = acc[o];
+      out[o] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    }
+  }
+  if (tid < G) {
+    const float lse = sum[tid] > 0.f ? mx[tid] + __log2f(sum[tid]) * 0.69314718055994531f : neg_inf();
+    if (!final_out) p.lse_part[dst * G + tid] = lse;
+    else if (p.lse) p.lse[(int64_t)b * p.num_q_heads + h * G + tid] = lse;
+  }
+  __syncthreads();
+}
+
+// The same for n <= kSmallMerge pieces in one round of loads: each thread
+// issues, for its (at most two) output float4s, the loads of every piece's O
+// and of the pieces' LSEs of its head together, then weights, sums and
+// writes. One barrier keeps an in-place result's LSE write behind every
+// thread's reads. Needs G floats of scratch.
+constexpr int kSmallMerge = 8;
+__device__ __noinline__ void merge_slots_small(const GqaParams &p, int unit, int G, int64_t slot0,
+                                               int stride, int n, bool final_out, int64_t dst,
+                                               float *scratch) {
+  const int nthr = blockDim.x, tid = threadIdx.x;
+  const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
+  const int nout = G * (kD / 4);
+  const float4 *src = reinterpret_cast<const float4 *>(p.o_part + slot0 * G * kD);
+  float4 v[2][kSmallMerge];
+  float l[2][kSmallMerge];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int o = tid + u * nthr, g = o / (kD / 4);
+#pragma unroll
+    for (int k = 0; k < kSmallMerge; ++k) {
+      const bool on = o < nout && k < n;
+      v[u][k] = on ? __ldcg(src + (int64_t)k * stride * nout + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+      l[u][k] = on ? __ldcg(p.lse_part + (slot0 + (int64_t)k * stride) * G + g) : neg_inf();
+    }
+  }
+  float lse_out[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int o = tid + u * nthr;
+    float M = neg_inf();
+#pragma unroll
+    for (int k = 0; k < kSmallMerge; ++k) M = fmaxf(M, l[u][k]);
+    float sum = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kSmallMerge; ++k) {
+      const float e = (l[u][k] == neg_inf() || M == neg_inf()) ? 0.f : ex2((l[u][k] - M) * 1.4426950408889634f);
+      if (e != 0.f) {  // a piece of weight 0 may hold anything
+        sum += e;
+        a.x += e * v[u][k].x;
+        a.y += e * v[u][k].y;
+        a.z += e * v[u][k].z;
+        a.w += e * v[u][k].w;
+      }
+    }
+    lse_out[u] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+    if (o < nout) {
+      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      if (final_out) {
+        __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
+        *reinterpret_cast<uint2 *>(out + 4 * o) =
+            make_uint2(pack_bf16(a.x * inv, a.y * inv), pack_bf16(a.z * inv, a.w * inv));
+      } else {
+        reinterpret_cast<float4 *>(p.o_part + dst * G * kD)[o] =
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      }
+    }
+  }
+  // the head's LSE (every thread of a head computed the same value)
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int o = tid + u * nthr;
+    if (o < nout && o % (kD / 4) == 0) scratch[o / (kD / 4)] = lse_out[u];
+  }
+  __syncthreads();  // every thread has read the pieces' LSEs
+  if (tid < G) {
+    if (!final_out) p.lse_part[dst * G + tid] = scratch[tid];
+    else if (p.lse) p.lse[(int64_t)b * p.num_q_heads + h * G + tid] = scratch[tid];
+  }
+  __syncthreads();
+}
+
 // One warp merges a unit held by at most kWarpMergeSegs pieces (G <= 8): lane l
 // owns head dims 4l..4l+3; per head the pieces' LSE give weights
 // exp(lse_s - max) and the output is the weighted mean of their normalised O.
-constexpr int kWarpMergeSegs = 4;
 __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c_first, int n_seg,
                                              int G) {
   const int lane = threadIdx.x & 31;
@@ -405,18 +587,40 @@ __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c
 __device__ __forceinline__ bool count_segment(const GqaParams &p, int unit, int n_seg) {
   return atomic_add_acq_rel_gpu(p.counters + unit, 1u) == (unsigned)(n_seg - 1);
 }
-__device__ __forceinline__ void record_merge(volatile int *flags, int unit, int c_first, int n_seg) {
+// Merges this CTA owes after its stream (at most two: a range holds at most two
+// partial segments): (unit, c_first, n_seg, group), group -1 for a one-level merge.
+__device__ __forceinline__ void record_merge(volatile int *flags, int unit, int c_first, int n_seg,
+                                             int group) {
   if (flags[12] < 2) {
     const int k = flags[12];
-    flags[6 + 3 * k] = unit;
-    flags[7 + 3 * k] = c_first;
-    flags[8 + 3 * k] = n_seg;
+    flags[24 + 4 * k] = unit;
+    flags[25 + 4 * k] = c_first;
+    flags[26 + 4 * k] = n_seg;
+    flags[27 + 4 * k] = group;
     flags[12] = k + 1;
   }
 }
+// Counts this CTA's finished piece of a unit of n_seg > 1 pieces. Returns true
+// when it completes a unit of at most kWarpMergeSegs pieces that the caller
+// merges right away (warp_merge); otherwise records the merge this CTA owes.
+__device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *flags, int unit,
+                                            int c_first, int n_seg, bool warp_merge) {
+  if (n_seg <= kOneLevelSegs) {
+    if (!count_segment(p, unit, n_seg)) return false;
+    if (warp_merge && n_seg <= kWarpMergeSegs) return true;
+    record_merge(flags, unit, c_first, n_seg, -1);
+    return false;
+  }
+  const int K = merge_group_size(n_seg), q = ((int)blockIdx.x - c_first) / K;
+  const int gs = min(K, n_seg - q * K);
+  uint32_t *gc = p.counters + p.batch * p.num_kv_heads +
+                 (int64_t)unit * max_merge_groups(gridDim.x) + q;
+  if (atomic_add_acq_rel_gpu(gc, 1u) == (unsigned)(gs - 1)) record_merge(flags, unit, c_first, n_seg, q);
+  return false;
+}
 
 template <bool FP8, int NT>
-__global__ void __launch_bounds__(threads_for<NT>(), 1)
+__global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap, const GqaParams p) {
@@ -437,13 +641,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
   int *scan = reinterpret_cast<int *>(smem + C::oScan);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + C::oFlags);
   // flags: [0] abort, [2] start unit, [3] start tile, [4..5] start P (int64),
-  //        [6..11] up to two merges owed (unit, c_first, n_seg), [12] their count,
+  //        [12] merges owed after the stream, [13] scratch, [24..31] those merges
+  //        (unit, c_first, n_seg, group),
   //        [14..19] the range's partial segments (unit, c_first, n_seg) handed to
   //        the helper warp, [20] unit holding the range's last tile, [21] whether
   //        its segment here is partial, [22..23] its first tile (int64)
   uint64_t *merge_bar = reinterpret_cast<uint64_t *>(smem + C::oMergeBar);
   uint64_t *part_bar = merge_bar + 2;  // [2] a partial segment is in global memory
-  uint64_t *helper_done = merge_bar + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
@@ -516,7 +720,6 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
     mbar_init(&merge_bar[1], 1);
     mbar_init(&part_bar[0], kConsumerWarps * 32);
     mbar_init(&part_bar[1], kConsumerWarps * 32);
-    mbar_init(helper_done, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -730,19 +933,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(&part_bar[k & 1], (k >> 1) & 1, kWaitLimitNs))))
         break;
       const int unit = flags[14 + 3 * k], c_first = flags[15 + 3 * k], n_seg = flags[16 + 3 * k];
-      const bool last = __shfl_sync(0xffffffffu, lane == 0 ? count_segment(p, unit, n_seg) : false, 0);
+      const bool merge_now = __shfl_sync(
+          0xffffffffu, lane == 0 ? count_piece(p, flags, unit, c_first, n_seg, true) : false, 0);
       __syncwarp();  // lane 0's acquire covers the whole warp's reads of the pieces
-      if (last) {
-        if (n_seg <= kWarpMergeSegs) merge_unit_warp(p, unit, c_first, n_seg, G);
-        else if (lane == 0) record_merge(flags, unit, c_first, n_seg);
-      }
+      if (merge_now) merge_unit_warp(p, unit, c_first, n_seg, G);
     }
     if (!ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
       if (lane == 0) flags[0] = 1;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(helper_done);
   } else {
     // ======================================================= consumers
     const int q4 = lane & 3;   // owns heads g = nt*8 + 2*q4 + {0,1}
@@ -1060,27 +1259,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
           mbar_arrive(&part_bar[npart & 1]);
         } else {
           named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
-          if (threadIdx.x == 0 && count_segment(p, unit, m.n_seg)) record_merge(flags, unit, m.c_first, m.n_seg);
+          if (threadIdx.x == 0) count_piece(p, flags, unit, m.c_first, m.n_seg, false);
         }
         ++npart;
       }
       reset();
-    }
-    // ---- merges this CTA owes (its ring is free now: every tile was consumed),
-    // known once the helper has counted the partial segments
-    if (!ok) flags[0] = 1;
-    if (kHelper && ok && !mbar_wait_bounded(helper_done, 0, kWaitLimitNs)) {
-      ok = false;
-      flags[0] = 1;
-    }
-    named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
-    uint32_t merge_phase[2] = {0u, 0u};
-    const int npending = flags[0] ? 0 : flags[12];  // the same for all consumer threads
-    for (int k = 0; k < npending; ++k) {
-      if (!merge_unit(p, flags[6 + 3 * k], flags[7 + 3 * k], flags[8 + 3 * k], G, ring,
-                      C::kStages * 2 * C::kTileBytes, red, 8 * NT * kRedStride,
-                      reinterpret_cast<float *>(qslots), merge_bar, merge_phase))
-        ok = false;
     }
     if (!ok) {
       dev_err |= DA_DEVERR_TIMEOUT;
@@ -1088,7 +1271,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
     }
   }
 
-  __syncthreads();  // every issued TMA box has been consumed (or a wait gave up)
+  // every issued TMA box has been consumed (or a wait gave up), and the helper
+  // has recorded every merge this CTA owes
+  __syncthreads();
   if (flags[0]) {
     // a wait gave up: drain copies still in flight (bounded) before leaving
     if (threadIdx.x == kConsumerWarps * 32) {
@@ -1098,6 +1283,55 @@ __global__ void __launch_bounds__(threads_for<NT>(), 1)
       }
     }
     dev_err |= DA_DEVERR_TIMEOUT;
+  } else {
+    // ---- the merges this CTA owes, by all its threads (the ring is free now)
+    const int npending = flags[12];
+    float *scr = reinterpret_cast<float *>(ring);
+    const int scr_floats = C::kStages * 2 * C::kTileBytes / 4;
+    volatile int *last_group = flags + 13;
+    for (int k = 0; k < npending; ++k) {
+      const int unit = flags[24 + 4 * k], c_first = flags[25 + 4 * k], n_seg = flags[26 + 4 * k];
+      const int q = flags[27 + 4 * k];
+      const int64_t slot0 = (int64_t)unit + c_first;
+      if (q < 0) {
+        if (n_seg <= kSmallMerge && 2 * kThreads >= G * (kD / 4)) {
+          merge_slots_small(p, unit, G, slot0, 1, n_seg, true, 0, scr);
+        } else if (merge_cta_floats(n_seg, G) <= scr_floats) {
+          merge_slots_cta(p, unit, G, slot0, 1, n_seg, true, 0, scr);
+        } else if (warp < kConsumerWarps) {
+          // more pieces than the ring holds at once: the staged merge of the consumers
+          uint32_t merge_phase[2] = {0u, 0u};
+          if (!merge_unit(p, unit, c_first, n_seg, G, ring, C::kStages * 2 * C::kTileBytes, red,
+                          8 * NT * kRedStride, reinterpret_cast<float *>(qslots), merge_bar,
+                          merge_phase))
+            dev_err |= DA_DEVERR_TIMEOUT;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) p.counters[unit] = 0u;  // ready for the next call
+        continue;
+      }
+      // two levels: this CTA completed group q; merge it in place into its first slot
+      const int K = merge_group_size(n_seg), ng = (n_seg + K - 1) / K;
+      const int gs = min(K, n_seg - q * K);
+      const bool small = 2 * kThreads >= G * (kD / 4);
+      if (small && gs <= kSmallMerge)
+        merge_slots_small(p, unit, G, slot0 + (int64_t)q * K, 1, gs, false, slot0 + (int64_t)q * K, scr);
+      else
+        merge_slots_cta(p, unit, G, slot0 + (int64_t)q * K, 1, gs, false, slot0 + (int64_t)q * K, scr);
+      if (threadIdx.x == 0)  // the group result is written (barrier above): count the group
+        *last_group = atomic_add_acq_rel_gpu(p.counters + unit, 1u) == (unsigned)(ng - 1) ? 1 : 0;
+      __syncthreads();
+      if (*last_group) {
+        if (small && ng <= kSmallMerge) merge_slots_small(p, unit, G, slot0, K, ng, true, 0, scr);
+        else merge_slots_cta(p, unit, G, slot0, K, ng, true, 0, scr);
+        // ready for the next call: the unit's counter and its group counters
+        uint32_t *gc = p.counters + p.batch * p.num_kv_heads +
+                       (int64_t)unit * max_merge_groups(gridDim.x);
+        for (int i = threadIdx.x; i < ng; i += kThreads) gc[i] = 0u;
+        if (threadIdx.x == 0) p.counters[unit] = 0u;
+      }
+      __syncthreads();
+    }
   }
   if (dev_err) atomicOr(p.err, dev_err);
 }

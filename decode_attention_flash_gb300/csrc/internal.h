@@ -41,6 +41,16 @@ struct GqaParams {
   int32_t sparse_block_size, max_sparse_blocks;
 };
 
+// Group counters per GQA unit for the two-level merge of a unit cut into many
+// pieces (groups of ceil(sqrt(pieces)) pieces; pieces <= CTAs): shared by the
+// planner, which sizes the workspace, and the kernel.
+__host__ __device__ inline int ceil_sqrt(int n) {
+  int k = 1;
+  while (k * k < n) ++k;
+  return k;
+}
+__host__ __device__ inline int max_merge_groups(int ctas) { return ceil_sqrt(ctas) + 1; }
+
 struct MergeParams {
   const float *o_part;   // element (u, s, g, d) at ((u*S + s)*R + g)*dv + d
   const float *lse_part; // element (u, s, g) at (u*S + s)*R + g

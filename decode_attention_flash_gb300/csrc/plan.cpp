@@ -143,8 +143,8 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
     info->ctas_per_sm = cps;
     info->writes_final = 0;  // decided per unit on the device
     int64_t off = kWorkspaceHeader;
-    info->counters_offset = off;
-    off = align256(off + units * 4);
+    info->counters_offset = off;  // per unit: its counter, then its merge-group counters
+    off = align256(off + units * (1 + max_merge_groups((int)ctas)) * 4);
     info->partial_o_offset = off;  // slots unit + cta
     off = align256(off + (units + ctas) * rows * (int64_t)dv * 4);
     info->partial_lse_offset = off;

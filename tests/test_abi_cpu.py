@@ -133,9 +133,12 @@ def _check_gqa_plan(plan, unit_tiles, num_sms=152):
     # balance: every CTA streams floor or ceil of T/C tiles
     sizes = [bounds[c + 1] - bounds[c] for c in range(C)]
     assert max(sizes) - min(sizes) <= 1
-    # the workspace holds a partial slot for every (unit + cta)
+    # the workspace holds a partial slot for every (unit + cta), and per unit its
+    # counter plus the counters of a two-level merge (groups of ceil(sqrt(pieces))
+    # pieces, pieces <= CTAs: at most ceil(sqrt(C)) + 1 groups)
     U, G = plan["num_units"], plan["rows_per_unit"]
     assert plan["counters_offset"] == 256
+    assert plan["partial_o_offset"] - plan["counters_offset"] >= U * (1 + math.isqrt(C - 1) + 2) * 4
     assert plan["partial_lse_offset"] - plan["partial_o_offset"] >= (U + C) * G * 128 * 4
     assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * G * 4
 

@@ -39,6 +39,21 @@ def test_paged_ragged(splits, page_size):
     assert_parity(out, lse, ref_out, ref_lse, what=f"paged P={page_size} S={splits}")
 
 
+@pytest.mark.parametrize("pieces", [9, 10, 16, 31])
+def test_unit_cut_into_many_pieces_merges_in_two_levels(pieces):
+    # one unit over `pieces` CTAs: groups of ceil(sqrt(pieces)) pieces are merged
+    # first (the last group may be short), then the groups; repeated calls give
+    # the same bits (every counter is back at zero after a call)
+    w = W.make_gqa(name="many", batch=1, num_q_heads=8, num_kv_heads=1, seq_lens=[64 * pieces - 17],
+                   layout="paged", page_size=16, seed=300 + pieces)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=pieces)
+    assert flags == 0 and eng.plan["grid_x"] == pieces
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"{pieces} pieces")
+    out2, lse2, flags2, _ = run_gpu(w, engine=eng)  # same workspace: counters reused
+    assert flags2 == 0 and torch.equal(out2, out) and torch.equal(lse2, lse)
+
+
 @pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
 def test_contiguous_group_sizes(group):
     hkv = 2
