@@ -737,6 +737,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
     const uint64_t q_policy = l2_policy_evict_last();
     const int P = p.page_size;
     const int pages_per_tile = p.paged ? (P >= kTile ? 1 : kTile / P) : 1;
+    const bool multi_box = !FP8 && pages_per_tile > 1;  // several page boxes per tile
 
     // Walker over (unit, tile) in processing order. When the range ends in the
     // head of a unit that goes on into the next CTA, that segment is streamed
@@ -889,25 +890,49 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
         uint32_t bytes = 2u * (uint32_t)nbox * box_tokens * C::kBytesPerTok;
         if (first) bytes += (uint32_t)G * kD * 2;
         mbar_arrive_expect_tx(&full[st], bytes);
-        uint8_t *kdst = ring + (size_t)st * 2 * C::kTileBytes;
-        uint8_t *vdst = kdst + C::kTileBytes;
-        if (first)
-          tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
-                      (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
-        const int nb = (p.paged && P < kTile) ? kTile / P : (nbox ? 1 : 0);
-        const int box_rows = (p.paged && P < kTile) ? P : kTile;
-        for (int k = 0; k < nb; ++k) {
-          if (ys[k] < 0) continue;
-          const int off = k * box_rows * C::kBytesPerTok;  // box k of a multi-page tile
-          if (FP8) {
-            tma_load_2d(kdst + off, &kmap, &full[st], 0, ys[k], policy);
-            tma_load_2d(vdst + off, &vmap, &full[st], 0, ys[k], policy);
-          } else {
-            // one 3-D box: both 64-element halves of box_rows rows, half-major
-            tma_load_3d(kdst + off, &kmap, &full[st], 0, ys[k], 0, policy);
-            tma_load_3d(vdst + off, &vmap, &full[st], 0, ys[k], 0, policy);
+        if (!multi_box) {
+          uint8_t *kdst = ring + (size_t)st * 2 * C::kTileBytes;
+          uint8_t *vdst = kdst + C::kTileBytes;
+          if (first)
+            tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
+                        (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
+          const int nb = (p.paged && P < kTile) ? kTile / P : (nbox ? 1 : 0);
+          const int box_rows = (p.paged && P < kTile) ? P : kTile;
+          for (int k = 0; k < nb; ++k) {
+            if (ys[k] < 0) continue;
+            const int off = k * box_rows * C::kBytesPerTok;  // box k of a multi-page tile
+            if (FP8) {
+              tma_load_2d(kdst + off, &kmap, &full[st], 0, ys[k], policy);
+              tma_load_2d(vdst + off, &vmap, &full[st], 0, ys[k], policy);
+            } else {
+              // one 3-D box: both 64-element halves of box_rows rows, half-major
+              tma_load_3d(kdst + off, &kmap, &full[st], 0, ys[k], 0, policy);
+              tma_load_3d(vdst + off, &vmap, &full[st], 0, ys[k], 0, policy);
+            }
           }
         }
+      }
+      if (multi_box) {
+        // the page boxes of the tile are issued by several lanes at once (lane
+        // k: K box k, lane 8 + k: V box k, lane 16: the query group) once lane
+        // 0 has set the stage's byte count: one lane issuing them in turn
+        // limits the rate at which a CTA streams small pages
+        __syncwarp();
+        const bool first = (i == 0) || (i == i_jump) || (cur.j == 0);
+        const int k = lane & 7;
+        int y = -1;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          if (kk == k) y = ys[kk];
+        if (lane < 16 && k < kTile / P && y >= 0) {
+          const bool isv = lane >= 8;
+          uint8_t *dst = ring + (size_t)st * 2 * C::kTileBytes + (isv ? C::kTileBytes : 0) +
+                         k * P * C::kBytesPerTok;
+          tma_load_3d(dst, isv ? &vmap : &kmap, &full[st], 0, y, 0, policy);
+        }
+        if (first && lane == 16)
+          tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
+                      (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
       }
       // shift the id queue by one tile and look up tile i + ahead_n
       if (needs_ids) {
