@@ -67,7 +67,8 @@ constexpr int kSoftmaxWarps = 8;                       // two groups of four
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kGroupThreads = kSoftmaxThreads / 2;      // one thread per head row
 constexpr int kFirstSoftmaxWarp = 3;
-constexpr int kThreads = 32 * (kFirstSoftmaxWarp + kSoftmaxWarps);
+constexpr int kPvWarp = kFirstSoftmaxWarp + kSoftmaxWarps;  // issues the PV MMAs
+constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr int kStages = 4;                // KV ring depth
 constexpr int kKvBlock = kTok * 128;      // 8 KB: 64 tokens x 64 bf16
 constexpr int kKpeBlock = kTok * 64;     // 4 KB: 64 tokens x 32 bf16, 64B-swizzled
@@ -488,6 +489,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   (full ? kFullRow : 0);
         m.c_first = c_first;
         m.n_seg = n_seg;
+        if (m.flags & kFirst) {
+          // the row's queries into L2 ahead of their use at the row's first
+          // tile (this CTA's half of q_nope's rows, and its q_pe columns' rows)
+          prefetch_l2(p.q_nope + ((int64_t)b * kHeads + 64 * (int)r) * 512, 64 * 512 * 2);
+          prefetch_l2(p.q_pe + ((int64_t)b * kHeads + 64 * (int)r) * 64, 64 * 64 * 2);
+        }
         uint8_t *dst = sKV + st * kKvStage;
         if (bad) {
           // a skipped page: zeros instead of stale data (its scores are masked)
@@ -522,90 +529,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ============================================================ MMA issuer
+    // ============================================================ QK issuer
     if (lane == 0) {
       const uint32_t idesc_qk = umma_idesc_bf16(128, kTok, false, false);
-      const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
       const uint64_t q_policy = l2_policy_evict_last();
       // Scores of tile k need its KV stage, the scores of tile k - 1 read out
       // and, on a row's first tile, that row's q (q_nope in TMEM, and q_pe,
-      // loaded here once the previous row's scores are complete). PV of tile k
-      // needs its P and, on a row's first tile, the previous row's O read out. The issuer polls both and issues what is ready. (No barrier
-      // polled here can run a phase ahead of the tile being tested.)
-      int qk_seg = -1, pv_seg = -1;  // row segment of the latest QK / PV
+      // loaded here once the previous tile's scores -- which read the previous
+      // row's q_pe -- are complete). The PV MMAs are issued by their own warp,
+      // so a tile's PV never waits behind the next tile's score MMAs.
+      int qk_seg = -1;
       bool ok = true;
-      uint64_t idle_since = 0;
-      while (ok && issued_pv < n) {
+      for (int k = 0; k < n && ok; ++k) {
         if (*abort_flag) break;
-        bool progress = false;
-        const int k = issued_qk;
-        if (k < n && mbar_test(&bar[B_KVF + k % kStages], (k / kStages) & 1)) {
-          const TileMeta m = meta[k % kStages];
-          const bool first = (m.flags & kFirst) != 0;
-          const int seg = first ? qk_seg + 1 : qk_seg;
-          bool ready = k < 1 || mbar_test(&bar[B_SE], (k - 1) & 1);
-          if (first) {
-            if (qpe_seg < seg) {
-              if (k == 0 || mbar_test(&bar[B_SF + ((k - 1) & 1)], ((k - 1) >> 1) & 1)) {
-                mbar_arrive_expect_tx(&bar[B_QPE], kQpeBlock);
-                tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b * kHeads, q_policy);
-                qpe_seg = seg;
-              }
-              ready = false;
-            }
-            ready = ready && mbar_test(&bar[B_QT], seg & 1) && mbar_test(&bar[B_QPE], seg & 1);
-          }
-          if (ready) {
-            tc_fence_after();
-            const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
-            const uint32_t d = tmem + kTmemS;
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
-                             umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
-                             (c | kk) != 0);
-            {
-              const uint32_t q = smem_u32(sQpe);
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk)
-                umma_bf16_ss(d, umma_desc_sw64(q + kk * 32), umma_desc_sw64(kv + 4 * kKvBlock + kk * 32),
-                             idesc_qk, true);
-            }
-            umma_commit(&bar[B_SF + (k & 1)]);
-            qk_seg = seg;
-            ++issued_qk;
-            progress = true;
-          }
+        if (!(ok = mbar_wait_bounded(&bar[B_KVF + k % kStages], (k / kStages) & 1, kWaitLimitNs))) break;
+        const TileMeta m = meta[k % kStages];
+        const bool first = (m.flags & kFirst) != 0;
+        const int seg = first ? qk_seg + 1 : qk_seg;
+        if (k >= 1 && !(ok = mbar_wait_bounded(&bar[B_SE], (k - 1) & 1, kWaitLimitNs))) break;
+        if (first) {
+          if (k >= 1 && !(ok = mbar_wait_bounded(&bar[B_SF + ((k - 1) & 1)], ((k - 1) >> 1) & 1, kWaitLimitNs)))
+            break;
+          mbar_arrive_expect_tx(&bar[B_QPE], kQpeBlock);
+          tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b * kHeads, q_policy);
+          qpe_seg = seg;
+          if (!(ok = mbar_wait_bounded(&bar[B_QT], seg & 1, kWaitLimitNs))) break;
+          if (!(ok = mbar_wait_bounded(&bar[B_QPE], seg & 1, kWaitLimitNs))) break;
         }
-        const int j = issued_pv;
-        if (j < issued_qk && mbar_test(&bar[B_PF + (j & 1)], (j >> 1) & 1)) {
-          const TileMeta m = meta[j % kStages];
-          const bool first = (m.flags & kFirst) != 0;
-          const int seg = first ? pv_seg + 1 : pv_seg;
-          if (!first || seg == 0 || mbar_test(&bar[B_OFREE], (seg - 1) & 1)) {
-            tc_fence_after();
-            const int st = j % kStages;
-            const uint32_t v = smem_u32(sKV + st * kKvStage);
-            const uint32_t pa = tmem + kTmemP + 32 * (j & 1);
+        tc_fence_after();
+        const uint32_t kv = smem_u32(sKV + (k % kStages) * kKvStage);
+        const uint32_t d = tmem + kTmemS;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16_ts(tmem + kTmemO, pa + 8 * kk, umma_desc_sw128(v + kk * 2048, kKvBlock, 1024),
-                           idesc_pv, kk != 0 || !first);
-            umma_commit(&bar[B_PE + (j & 1)]);
-            umma_commit(&bar[B_KVE + st]);
-            pv_seg = seg;
-            ++issued_pv;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = global_timer_ns();
-          if (idle_since == 0) idle_since = now;
-          else if (now - idle_since > kWaitLimitNs) ok = false;
-        }
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk,
+                         umma_desc_sw128(kv + c * kKvBlock + kk * 32, 16, 1024), idesc_qk,
+                         (c | kk) != 0);
+        const uint32_t q = smem_u32(sQpe);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          umma_bf16_ss(d, umma_desc_sw64(q + kk * 32), umma_desc_sw64(kv + 4 * kKvBlock + kk * 32),
+                       idesc_qk, true);
+        umma_commit(&bar[B_SF + (k & 1)]);
+        qk_seg = seg;
+        ++issued_qk;
+      }
+      if (!ok) {
+        dev_err |= DA_DEVERR_TIMEOUT;
+        *abort_flag = 1;
+      }
+    }
+  } else if (warp == kPvWarp) {
+    // ============================================================ PV issuer
+    // PV of tile j needs its P and, on a row's first tile, the previous row's O
+    // read out by that row's epilogue.
+    if (lane == 0) {
+      const uint32_t idesc_pv = umma_idesc_bf16(128, 256, false, true);
+      int pv_seg = -1;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (*abort_flag) break;
+        if (!(ok = mbar_wait_bounded(&bar[B_PF + (j & 1)], (j >> 1) & 1, kWaitLimitNs))) break;
+        const TileMeta m = meta[j % kStages];
+        const bool first = (m.flags & kFirst) != 0;
+        const int seg = first ? pv_seg + 1 : pv_seg;
+        if (first && seg > 0 && !(ok = mbar_wait_bounded(&bar[B_OFREE], (seg - 1) & 1, kWaitLimitNs)))
+          break;
+        tc_fence_after();
+        const int st = j % kStages;
+        const uint32_t v = smem_u32(sKV + st * kKvStage);
+        const uint32_t pa = tmem + kTmemP + 32 * (j & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts(tmem + kTmemO, pa + 8 * kk, umma_desc_sw128(v + kk * 2048, kKvBlock, 1024),
+                       idesc_pv, kk != 0 || !first);
+        umma_commit(&bar[B_PE + (j & 1)]);
+        umma_commit(&bar[B_KVE + st]);
+        pv_seg = seg;
+        ++issued_pv;
       }
       if (!ok) {
         dev_err |= DA_DEVERR_TIMEOUT;
@@ -645,39 +647,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int x_next = g;         // first tile of this group whose peer scores have not been waited for
     bool x_posted = false;  // whether its expect_tx has been posted
     int epi = 0;            // partials written by this group (phase of B_EPI + g)
+    // q_nope of a row (this CTA's half) into TMEM, the A operand of its score MMAs
+    auto store_q = [&](int b) {
+      const uint4 *src =
+          reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 + 256 * r);
+#pragma unroll
+      for (int c0 = 0; c0 < 8; c0 += 2) {
+        uint4 qv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[e] = __ldg(src + 4 * c0 + e);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[4 * e] = __uint_as_float(qv[4 * c + e].x);
+            v[4 * e + 1] = __uint_as_float(qv[4 * c + e].y);
+            v[4 * e + 2] = __uint_as_float(qv[4 * c + e].z);
+            v[4 * e + 3] = __uint_as_float(qv[4 * c + e].w);
+          }
+          tmem_st16(tmem + lane_off + kTmemQ + 16 * (c0 + c), v);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar[B_QT]);
+    };
+    // the range's first row is known from the schedule: its q goes in at once,
+    // while the first KV stage is still in flight
+    if (g == 0) store_q(ctrl->start_b);
     for (int i = g; i < n; i += 2) {
       const int ii = i >> 1;  // this group's tile counter (phase of its barriers)
       // the tile's description (its stage cannot be refilled before this tile's PV)
       if (!(ok = warp_wait(&bar[B_KVF + i % kStages], (i / kStages) & 1))) break;
       const TileMeta m = meta[i % kStages];
       const bool first = (m.flags & kFirst) != 0;
-      if (first) {
+      if (first && i > 0) {
         // q_nope of the row into TMEM once the previous tile's scores are complete
-        if (i >= 1 && !(ok = warp_wait(&bar[B_SF + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
+        if (!(ok = warp_wait(&bar[B_SF + ((i - 1) & 1)], ((i - 1) >> 1) & 1))) break;
         tc_fence_after();
-        const uint4 *src =
-            reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)m.b * kHeads + h) * 512 + 256 * r);
-#pragma unroll
-        for (int c0 = 0; c0 < 8; c0 += 2) {
-          uint4 qv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qv[e] = __ldg(src + 4 * c0 + e);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            float v[16];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[4 * e] = __uint_as_float(qv[4 * c + e].x);
-              v[4 * e + 1] = __uint_as_float(qv[4 * c + e].y);
-              v[4 * e + 2] = __uint_as_float(qv[4 * c + e].z);
-              v[4 * e + 3] = __uint_as_float(qv[4 * c + e].w);
-            }
-            tmem_st16(tmem + lane_off + kTmemQ + 16 * (c0 + c), v);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar[B_QT]);
+        store_q(m.b);
       }
       if (!(ok = warp_wait(&bar[B_SF + g], ii & 1))) break;
       tc_fence_after();
@@ -891,10 +900,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1 && lane == 0) {
       if (issued_qk > 0)
         mbar_wait_bounded(&bar[B_SF + ((issued_qk - 1) & 1)], ((issued_qk - 1) >> 1) & 1, kWaitLimitNs);
-      if (issued_pv > 0)
-        mbar_wait_bounded(&bar[B_PE + ((issued_pv - 1) & 1)], ((issued_pv - 1) >> 1) & 1, kWaitLimitNs);
       if (qpe_seg >= 0) mbar_wait_bounded(&bar[B_QPE], qpe_seg & 1, kWaitLimitNs);
     }
+    if (warp == kPvWarp && lane == 0 && issued_pv > 0)
+      mbar_wait_bounded(&bar[B_PE + ((issued_pv - 1) & 1)], ((issued_pv - 1) >> 1) & 1, kWaitLimitNs);
     __syncthreads();
   }
   if (dev_err) atomicOr(p.err, dev_err | (*abort_flag ? DA_DEVERR_TIMEOUT : 0u));

@@ -84,6 +84,14 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *desc, ui
       : "memory");
 }
 
+// Asynchronous prefetch of a contiguous global range into L2 (the address and
+// the size multiples of 16 bytes); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // An L2 policy that marks streamed KV as first to evict.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
