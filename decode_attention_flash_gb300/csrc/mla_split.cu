@@ -182,19 +182,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_
   }
 }
 
-// Non-blocking check of a phase (the MMA issuer polls several barriers).
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Warp-uniform outcomes of bounded waits (the lanes then stay converged for
 // the .sync.aligned tensor-memory instructions that follow).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
