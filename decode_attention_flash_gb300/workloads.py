@@ -7,6 +7,7 @@ the float64 oracle see bit-identical inputs.
 
 Layouts (row-major, last index fastest):
   q            bf16 [B][HQ][D]          query head hq reads kv head hq // G
+               (q_len > 1: [B][HQ][q_len][D], the row's last q_len tokens)
   k, v         contiguous bf16|e4m3 [B][HKV][L][D]
                paged      bf16      [num_pages][HKV][page_size][D]
   MLA          q_nope [B][HQ][512], q_pe [B][HQ][64],
@@ -59,6 +60,7 @@ class Workload:
     sparse_block_size: int = 0
     max_sparse_blocks: int = 0
     num_splits: int = 0  # 0: planner decides
+    q_len: int = 1       # query tokens per row
     tensors: dict = field(default_factory=dict)
 
     @property
@@ -132,8 +134,9 @@ def quantize_e4m3(x: torch.Tensor, head_axis: int):
 def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_lens,
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
-             num_splits=0, poison=True, shape_only=False) -> Workload:
-    """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths.
+             num_splits=0, poison=True, shape_only=False, q_len=1) -> Workload:
+    """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths;
+    ``q_len`` > 1 gives each row that many query tokens (its last positions).
     ``shape_only`` skips drawing the K/V caches (lengths, tables and lists are
     drawn exactly as in the full workload)."""
     g = _gen(seed)
@@ -141,10 +144,10 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
     B, HQ, HKV, D = batch, num_q_heads, num_kv_heads, head_dim
     assert seq_lens.numel() == B and HQ % HKV == 0
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    q = _randn_bf16((B, HQ, D), g)
+    q = _randn_bf16((B, HQ, D) if q_len <= 1 else (B, HQ, q_len, D), g)
     w = Workload(name=name, batch=B, num_q_heads=HQ, num_kv_heads=HKV, head_dim_qk=D,
                  head_dim_v=D, scale=float(torch.tensor(scale, dtype=torch.float32)),
-                 kv_fp8=kv_fp8, num_splits=num_splits)
+                 kv_fp8=kv_fp8, num_splits=num_splits, q_len=max(1, q_len))
     t = {"q": q, "seq_lens": seq_lens}
     if layout == "paged":
         table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
@@ -257,7 +260,9 @@ def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq
     return w
 
 
-# ------------------------------------------------------------------ the five workloads
+# ------------------------------------------------------------------ the workloads
+# 1-5 are the five decode configurations; 6 is the multi-token query extension
+# (speculative decoding) on the paged GQA shapes.
 
 CONFIG_NAMES = {
     1: "tiny GQA decode (B1 HQ8 HKV1 D128, contiguous L512, 4 splits)",
@@ -265,11 +270,12 @@ CONFIG_NAMES = {
     3: "long-context fp8 KV (B1 HQ64 HKV8 D128, contiguous L131072, e4m3)",
     4: "block-sparse decode (B8 HQ32 HKV8 D128, L32768, 36 of 256 blocks of 128)",
     5: "MLA latent decode (B64 HQ128, ckv512+kpe64, N_b~U[2048,8192], page 64)",
+    6: "speculative paged GQA decode (B32 HQ32 HKV8 D128, 4 query tokens, N_b~U[1024,8192], page 16)",
 }
 
 
 def config(i: int, shape_only: bool = False) -> Workload:
-    """The five decode workloads; ``shape_only`` skips drawing the K/V caches."""
+    """The decode workloads (CONFIG_NAMES); ``shape_only`` skips drawing the K/V caches."""
     seed = 1000 + i
     so = dict(shape_only=shape_only)
     if i == 1:
@@ -294,4 +300,9 @@ def config(i: int, shape_only: bool = False) -> Workload:
         g = _gen(seed + 500)
         lens = _lengths(64, 2048, 8192, g)
         return make_mla(name="mla", batch=64, seq_lens=lens, seed=seed, **so)
+    if i == 6:
+        g = _gen(seed + 500)
+        lens = _lengths(32, 1024, 8192, g)
+        return make_gqa(name="spec_paged_gqa", batch=32, num_q_heads=32, num_kv_heads=8,
+                        seq_lens=lens, layout="paged", page_size=16, seed=seed, q_len=4, **so)
     raise ValueError(f"no workload {i}")

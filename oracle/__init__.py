@@ -44,7 +44,7 @@ class OracleProblem(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "is_mla",
         "ckv_dim", "kpe_dim", "paged", "page_size", "cache_len", "max_pages_per_seq",
-        "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks")]
+        "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks", "q_len")]
 
 
 class OracleInputs(ctypes.Structure):
@@ -183,15 +183,17 @@ def problem_from(work) -> dict:
         ckv_dim=w.ckv_dim, kpe_dim=w.kpe_dim, paged=int(w.paged), page_size=w.page_size,
         cache_len=w.cache_len, max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
         kv_fp8=int(w.kv_fp8), sparse_block_size=w.sparse_block_size,
-        max_sparse_blocks=w.max_sparse_blocks)
+        max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1))
 
 
 def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = None):
-    """Full decode attention -> (out [B][HQ][Dv] float64, lse [B][HQ] float64)."""
+    """Full decode attention -> (out [B][HQ][Dv], lse [B][HQ]) in float64; with
+    several query tokens (q_len = Q > 1) out [B][HQ][Q][Dv] and lse [B][HQ][Q]."""
     prep = _Prepared(prob, tensors, scale)
     p = prep.problem
-    out = np.zeros((p.batch, p.num_q_heads, p.head_dim_v), dtype=np.float64)
-    lse = np.zeros((p.batch, p.num_q_heads), dtype=np.float64)
+    lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
+    out = np.zeros(lead + (p.head_dim_v,), dtype=np.float64)
+    lse = np.zeros(lead, dtype=np.float64)
     st = lib().oracle_decode(ctypes.byref(p), ctypes.byref(prep.inputs), out.ctypes.data,
                              lse.ctypes.data, num_threads or default_threads())
     if st != 0:
@@ -200,13 +202,15 @@ def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = No
 
 
 def split(prob: dict, tensors: dict, scale: float, chunk_bounds, num_threads: int | None = None):
-    """Per-chunk results over list-index boundaries -> (o [B][HQ][C][Dv], lse [B][HQ][C])."""
+    """Per-chunk results over list-index boundaries -> (o [B][HQ][C][Dv], lse [B][HQ][C]);
+    with several query tokens (q_len = Q > 1) o [B][HQ][Q][C][Dv], lse [B][HQ][Q][C]."""
     prep = _Prepared(prob, tensors, scale)
     p = prep.problem
     bounds = np.ascontiguousarray(np.asarray(chunk_bounds, dtype=np.int64))
     C = bounds.shape[0] - 1
-    o = np.zeros((p.batch, p.num_q_heads, C, p.head_dim_v), dtype=np.float64)
-    lse = np.zeros((p.batch, p.num_q_heads, C), dtype=np.float64)
+    lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
+    o = np.zeros(lead + (C, p.head_dim_v), dtype=np.float64)
+    lse = np.zeros(lead + (C,), dtype=np.float64)
     st = lib().oracle_split(ctypes.byref(p), ctypes.byref(prep.inputs), C, bounds.ctypes.data,
                             o.ctypes.data, lse.ctypes.data, num_threads or default_threads())
     if st != 0:

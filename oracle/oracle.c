@@ -18,6 +18,13 @@
  *     lse     = m + ln(l)                                    (natural log)
  *   and out = 0, lse = -inf when P is empty.
  *
+ *   Several query tokens per row (q_len = Q > 1, speculative decoding): the
+ *   row's new tokens are its last Q positions, so query token t < Q keeps the
+ *   positions of P(b,h) with n <= N_b - Q + t (the causal mask of the split-K
+ *   decode kernel, `_fwd_kernel_splitK` with IS_CAUSAL: q_pos = kv_len -
+ *   num_queries + t, position kept when q_pos - kv_pos >= 0). Rows are then
+ *   (b, hq, t) with t fastest.
+ *
  * Sources: the per-split output and log-sum-exp of the split-K Triton decode
  * kernel page (mslk splitk_kernels.py, `_fwd_kernel_splitK`, "write back O"
  * and the LSE store), its reduce (`_splitK_reduce`), the GQA packing of the
@@ -145,11 +152,12 @@ typedef struct {
   int32_t kv_fp8;         /* 0: bf16 bits, 1: e4m3 bytes with per-kv-head scale */
   int32_t sparse_block_size; /* 0: dense */
   int32_t max_sparse_blocks;
+  int32_t q_len;          /* query tokens per row (0 or 1: one) */
 } oracle_problem;
 
 typedef struct {
-  const uint16_t *q;      /* bf16 [B][HQ][Dq] (MLA: q_nope [B][HQ][ckv]) */
-  const uint16_t *q_pe;   /* MLA: bf16 [B][HQ][kpe] */
+  const uint16_t *q;      /* bf16 [B][HQ][Q][Dq] (MLA: q_nope [B][HQ][Q][ckv]), Q = q_len */
+  const uint16_t *q_pe;   /* MLA: bf16 [B][HQ][Q][kpe] */
   const void *k;          /* GQA contiguous [B][HKV][L][D]; paged [pages][HKV][P][D]
                              MLA ckv: contiguous [B][L][ckv]; paged [pages][P][ckv] */
   const void *v;          /* GQA: same layout as k; MLA kpe: [B][L][kpe] / [pages][P][kpe] */
@@ -248,21 +256,27 @@ static int fetch_kv(const oracle_problem *p, const oracle_inputs *in, int b, int
   return ORACLE_OK;
 }
 
-static void fetch_q(const oracle_problem *p, const oracle_inputs *in, int b, int hq, double *qr) {
+static int q_tokens(const oracle_problem *p) { return p->q_len > 1 ? p->q_len : 1; }
+
+/* Query token t of (b, hq). */
+static void fetch_q(const oracle_problem *p, const oracle_inputs *in, int b, int hq, int t,
+                    double *qr) {
+  const int64_t r = ((int64_t)b * p->num_q_heads + hq) * q_tokens(p) + t;
   if (p->is_mla) {
-    const uint16_t *qn = in->q + ((int64_t)b * p->num_q_heads + hq) * p->ckv_dim;
-    const uint16_t *qp = in->q_pe + ((int64_t)b * p->num_q_heads + hq) * p->kpe_dim;
+    const uint16_t *qn = in->q + r * p->ckv_dim;
+    const uint16_t *qp = in->q_pe + r * p->kpe_dim;
     for (int d = 0; d < p->ckv_dim; ++d) qr[d] = oracle_bf16_to_double(qn[d]);
     for (int d = 0; d < p->kpe_dim; ++d) qr[p->ckv_dim + d] = oracle_bf16_to_double(qp[d]);
     return;
   }
-  const uint16_t *qq = in->q + ((int64_t)b * p->num_q_heads + hq) * p->head_dim_qk;
+  const uint16_t *qq = in->q + r * p->head_dim_qk;
   for (int d = 0; d < p->head_dim_qk; ++d) qr[d] = oracle_bf16_to_double(qq[d]);
 }
 
 static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   if (!p || !in || !in->q || !in->k || !in->v || !in->seq_lens) return ORACLE_BAD_ARG;
-  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return ORACLE_BAD_ARG;
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->q_len < 0)
+    return ORACLE_BAD_ARG;
   if (p->num_q_heads % p->num_kv_heads) return ORACLE_BAD_ARG;
   if (p->is_mla) {
     if (p->num_kv_heads != 1 || !in->q_pe || p->kv_fp8) return ORACLE_BAD_ARG;
@@ -297,15 +311,28 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
                    double *kr) {
   const oracle_problem *p = job->p;
   const oracle_inputs *in = job->in;
-  int b = (int)(row / p->num_q_heads);
-  int hq = (int)(row % p->num_q_heads);
+  const int Q = q_tokens(p);
+  int b = (int)(row / ((int64_t)p->num_q_heads * Q));
+  int hq = (int)((row / Q) % p->num_q_heads);
+  int t = (int)(row % Q);
   int G = p->num_q_heads / p->num_kv_heads;
   int h = hq / G;
   int dq = p->head_dim_qk, dv = p->head_dim_v;
 
   int64_t n = positions(p, in, b, h, pos);
   if (n < 0) return (int)n;
-  fetch_q(p, in, b, hq, qr);
+  if (Q > 1) {
+    /* Several new query tokens (speculative decoding): they are the row's last
+     * Q positions, and token t sees the positions up to its own,
+     * n <= N_b - Q + t (the causal mask of the split-K decode kernel,
+     * splitk_kernels.py `_fwd_kernel_splitK`, IS_CAUSAL). */
+    const int64_t limit = (int64_t)in->seq_lens[b] - Q + 1 + t;
+    int64_t kept = 0;
+    for (int64_t j = 0; j < n; ++j)
+      if (pos[j] < limit) pos[kept++] = pos[j];
+    n = kept;
+  }
+  fetch_q(p, in, b, hq, t, qr);
   for (int64_t j = 0; j < n; ++j) {
     int st = fetch_kv(p, in, b, h, pos[j], kr, vrows + j * (int64_t)dv);
     if (st) return st;
@@ -378,7 +405,8 @@ static int run_job(job_t *job, int num_threads) {
 }
 
 /*
- * Full decode attention: out [B][HQ][Dv] and lse [B][HQ] (natural log).
+ * Full decode attention: out [B][HQ][Q][Dv] and lse [B][HQ][Q] (natural log;
+ * Q = q_len, the [Q] axis absent for one query token).
  * Returns 0, or a negative code (bad argument, or an index outside the cache:
  * a page id outside [0, num_pages), a sparse block outside the cache, a
  * sequence length over the cache capacity).
@@ -394,7 +422,7 @@ int oracle_decode(const oracle_problem *p, const oracle_inputs *in, double *out,
   job.num_chunks = 0;
   job.out = out;
   job.lse = lse;
-  job.rows = (int64_t)p->batch * p->num_q_heads;
+  job.rows = (int64_t)p->batch * p->num_q_heads * q_tokens(p);
   return run_job(&job, num_threads);
 }
 
@@ -420,7 +448,7 @@ int oracle_split(const oracle_problem *p, const oracle_inputs *in, int num_chunk
   job.chunk_bounds = chunk_bounds;
   job.out = o;
   job.lse = lse;
-  job.rows = (int64_t)p->batch * p->num_q_heads;
+  job.rows = (int64_t)p->batch * p->num_q_heads * q_tokens(p);
   return run_job(&job, num_threads);
 }
 

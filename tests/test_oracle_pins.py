@@ -11,6 +11,7 @@
   k = [ckv; kpe] and v = ckv.
 """
 
+import itertools
 import math
 import os
 from decimal import Decimal, getcontext
@@ -204,47 +205,53 @@ def brute_force(w: W.Workload):
         v = t["v"].double() * t["v_scale"].double().view(1, -1, 1, 1)
     else:
         k, v = t["k"].double(), t["v"].double()
-    out = np.zeros((B, HQ, w.head_dim_v))
-    lse = np.zeros((B, HQ))
-    for b in range(B):
+    Q = w.q_len
+    out = np.zeros((B, HQ, Q, w.head_dim_v))
+    lse = np.zeros((B, HQ, Q))
+    for b, hq, tq in itertools.product(range(B), range(HQ), range(Q)):
         n_b = int(t["seq_lens"][b])
-        for hq in range(HQ):
-            h = hq // G
-            if w.sparse_block_size:
-                pos = []
-                for j in range(int(t["kv_num_blks"][b, h])):
-                    blk = int(t["kv_idx"][b, h, j])
-                    pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
-                            if blk * w.sparse_block_size + i < n_b]
+        h = hq // G
+        if w.sparse_block_size:
+            pos = []
+            for j in range(int(t["kv_num_blks"][b, h])):
+                blk = int(t["kv_idx"][b, h, j])
+                pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
+                        if blk * w.sparse_block_size + i < n_b]
+        else:
+            pos = list(range(n_b))
+        # query token tq of Q is the row's position n_b - Q + tq: it sees n <= that
+        pos = [n for n in pos if n <= n_b - Q + tq]
+        keys, vals = [], []
+        for n in pos:
+            if w.is_mla:
+                page = int(t["block_table"][b, n // w.page_size])
+                ckv = t["k"][page, n % w.page_size].double()
+                kpe = t["v"][page, n % w.page_size].double()
+                keys.append(torch.cat([ckv, kpe]))
+                vals.append(ckv)
+            elif w.paged:
+                page = int(t["block_table"][b, n // w.page_size])
+                keys.append(k[page, h, n % w.page_size])
+                vals.append(v[page, h, n % w.page_size])
             else:
-                pos = list(range(n_b))
-            keys, vals = [], []
-            for n in pos:
-                if w.is_mla:
-                    page = int(t["block_table"][b, n // w.page_size])
-                    ckv = t["k"][page, n % w.page_size].double()
-                    kpe = t["v"][page, n % w.page_size].double()
-                    keys.append(torch.cat([ckv, kpe]))
-                    vals.append(ckv)
-                elif w.paged:
-                    page = int(t["block_table"][b, n // w.page_size])
-                    keys.append(k[page, h, n % w.page_size])
-                    vals.append(v[page, h, n % w.page_size])
-                else:
-                    keys.append(k[b, h, n])
-                    vals.append(v[b, h, n])
-            qv = torch.cat([q[b, hq], t["q_pe"][b, hq].double()]) if w.is_mla else q[b, hq]
-            if not pos:
-                lse[b, hq] = -math.inf
-                continue
-            s = [_dec(w.scale) * sum(_dec(a) * _dec(c) for a, c in zip(qv.tolist(), kk.tolist()))
-                 for kk in keys]
-            m = max(s)
-            e = [(x - m).exp() for x in s]
-            den = sum(e)
-            for d in range(w.head_dim_v):
-                out[b, hq, d] = float(sum(ei * _dec(vv[d]) for ei, vv in zip(e, vals)) / den)
-            lse[b, hq] = float(m + den.ln())
+                keys.append(k[b, h, n])
+                vals.append(v[b, h, n])
+        qv = torch.cat([q[b, hq], t["q_pe"][b, hq].double()]) if w.is_mla else q[b, hq]
+        if Q > 1:
+            qv = q[b, hq, tq]
+        if not pos:
+            lse[b, hq, tq] = -math.inf
+            continue
+        s = [_dec(w.scale) * sum(_dec(a) * _dec(c) for a, c in zip(qv.tolist(), kk.tolist()))
+             for kk in keys]
+        m = max(s)
+        e = [(x - m).exp() for x in s]
+        den = sum(e)
+        for d in range(w.head_dim_v):
+            out[b, hq, tq, d] = float(sum(ei * _dec(vv[d]) for ei, vv in zip(e, vals)) / den)
+        lse[b, hq, tq] = float(m + den.ln())
+    if Q == 1:
+        return out[:, :, 0], lse[:, :, 0]
     return out, lse
 
 
@@ -265,6 +272,14 @@ def _tiny_cases():
                             seq_lens=[4, 2], page_size=2, seed=15, scale=0.9))
     cases.append(W.make_gqa(name="empty_row", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=3, seq_lens=[0, 2], cache_len=2, seed=16, scale=1.0))
+    # several query tokens per row, causal over the new tokens; the second row is
+    # shorter than q_len, so its first query token sees no position at all
+    cases.append(W.make_gqa(name="causal_q3", batch=2, num_q_heads=4, num_kv_heads=2,
+                            head_dim=4, seq_lens=[5, 2], cache_len=6, seed=17, scale=0.7,
+                            q_len=3))
+    cases.append(W.make_gqa(name="causal_q2_paged", batch=2, num_q_heads=2, num_kv_heads=1,
+                            head_dim=4, seq_lens=[5, 3], layout="paged", page_size=2, seed=18,
+                            scale=0.6, q_len=2))
     return cases
 
 
@@ -281,6 +296,27 @@ def test_brute_force_tiny(w):
 
 
 # ------------------------------------------------------------------ invariants at moderate size
+
+def test_query_token_t_equals_a_single_token_decode_over_its_prefix():
+    # token t of q_len new tokens is position N_b - q_len + t: the same as one
+    # query over the first N_b - q_len + 1 + t positions (a shorter row)
+    Q = 4
+    lens = [70, 3, 129, 1]
+    w = W.make_gqa(name="spec", batch=4, num_q_heads=8, num_kv_heads=2, head_dim=32,
+                   seq_lens=lens, layout="paged", page_size=16, seed=41, q_len=Q)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=2)
+    assert out.shape == (4, 8, Q, 32) and lse.shape == (4, 8, Q)
+    for t in range(Q):
+        one = dict(w.tensors)
+        one["q"] = w.tensors["q"][:, :, t].contiguous()
+        one["seq_lens"] = torch.clamp(torch.tensor(lens) - Q + 1 + t, min=0).to(torch.int32)
+        prob = dict(oracle.problem_from(w), q_len=1)
+        o1, l1 = oracle.decode(prob, one, w.scale, num_threads=2)
+        assert np.array_equal(o1, out[:, :, t]) and np.array_equal(l1, lse[:, :, t])
+    # rows shorter than q_len: their first tokens see nothing
+    assert np.all(lse[3, :, :Q - 1] == -math.inf) and np.all(out[3, :, :Q - 1] == 0)
+    assert np.all(lse[1, :, 0] == -math.inf) and np.all(np.isfinite(lse[1, :, 1:]))
+
 
 def _gqa_case(layout="contiguous", seed=21, **kw):
     args = dict(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=32, seq_lens=[70, 1, 129],
