@@ -6,7 +6,10 @@ the workload, K/V cache resident in HBM. Default workload: paged GQA decode
 achieved KV-cache bandwidth (algorithmic KV bytes / time, GB/s), with us per
 call and the fraction of measured HBM peak alongside.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6] [--impl reference]
+
+Configs 1-5 are the five decode workloads; 6 is the speculative-decoding one
+(the paged GQA shapes with 4 query tokens per row, causal over the new tokens).
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 units are independent, no collective on the data path); rank 0 prints one
@@ -92,15 +95,16 @@ def algorithmic_bytes(w) -> dict:
     else:
         kv_tokens_heads = int(t["seq_lens"].long().sum()) * (1 if w.is_mla else w.num_kv_heads)
     elt = 1 if w.kv_fp8 else 2
+    Q = getattr(w, "q_len", 1)  # query tokens per row (their causal triangle is not subtracted)
     if w.is_mla:
         kv = kv_tokens_heads * (w.ckv_dim + w.kpe_dim) * 2
         q = w.batch * w.num_q_heads * (w.ckv_dim + w.kpe_dim) * 2
         flops = kv_tokens_heads * w.num_q_heads * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
     else:
         kv = kv_tokens_heads * (w.head_dim_qk + w.head_dim_v) * elt
-        q = w.batch * w.num_q_heads * w.head_dim_qk * 2
-        flops = kv_tokens_heads * w.group * 2 * (w.head_dim_qk + w.head_dim_v)
-    o = w.batch * w.num_q_heads * (w.head_dim_v * 2 + 4)
+        q = w.batch * w.num_q_heads * Q * w.head_dim_qk * 2
+        flops = kv_tokens_heads * w.group * Q * 2 * (w.head_dim_qk + w.head_dim_v)
+    o = w.batch * w.num_q_heads * Q * (w.head_dim_v * 2 + 4)
     return {"kv": kv, "q": q, "o": o, "total": kv + q + o, "flops": flops}
 
 
@@ -265,8 +269,9 @@ def run_ours(args, w, cfg):
                              **da.problem_kwargs(w))
     plan = eng.plan
     t = w.to(dev)
-    out = torch.empty((w.batch, w.num_q_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device=dev)
+    lead = (w.batch, w.num_q_heads) + ((w.q_len,) if w.q_len > 1 else ())
+    out = torch.empty(lead + (w.head_dim_v,), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(lead, dtype=torch.float32, device=dev)
     a = da.make_args(t, w.scale, out, lse)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -46,6 +46,7 @@ class Problem(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
         ("sparse_block_size", ctypes.c_int32), ("max_sparse_blocks", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
     ]
 
 
@@ -255,8 +256,8 @@ class DecodeAttention:
     def run(self, tensors: dict, scale: float, out=None, lse=None, stream=None):
         p = self.problem
         if out is None:
-            out = torch.empty((p.batch, p.num_q_heads, p.head_dim_v), dtype=torch.bfloat16,
-                              device=self.device)
+            lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
+            out = torch.empty(lead + (p.head_dim_v,), dtype=torch.bfloat16, device=self.device)
         decode_attn_run(self.ctx, make_args(tensors, scale, out, lse), self.workspace, stream)
         return out
 
@@ -286,4 +287,5 @@ def problem_kwargs(work) -> dict:
                 max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
                 q_dtype=DA_DTYPE_BF16,
                 kv_dtype=DA_DTYPE_FP8_E4M3 if w.kv_fp8 else DA_DTYPE_BF16,
-                sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks)
+                sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks,
+                q_len=getattr(w, "q_len", 1))

@@ -148,7 +148,10 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   const uint64_t rows = paged ? (uint64_t)p.num_pages * p.num_kv_heads * p.page_size
                               : (uint64_t)p.batch * p.num_kv_heads * p.max_seq_len;
   const uint32_t box_tokens = (uint32_t)da::gqa_box_tokens(p);
-  const int G = p.num_q_heads / p.num_kv_heads;
+  // the G query heads of a kv head, each with Q query tokens, are the unit's
+  // R = G x Q consecutive rows of q viewed as [B * HQ * Q][D]
+  const int Q = p.q_len > 1 ? p.q_len : 1;
+  const int R = p.num_q_heads / p.num_kv_heads * Q;
   if (ctx->map_k_base != a->k || ctx->map_v_base != a->v || ctx->map_q_base != a->q) {
     ctx->map_k_base = ctx->map_v_base = ctx->map_q_base = nullptr;
     da_status st;
@@ -162,7 +165,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
       if ((st = encode_bf16_halves(&ctx->kmap, a->k, rows, box_tokens)) != DA_OK) return st;
       if ((st = encode_bf16_halves(&ctx->vmap, a->v, rows, box_tokens)) != DA_OK) return st;
     }
-    if ((st = encode_q_rows(&ctx->qmap, a->q, (uint64_t)p.batch * p.num_q_heads, (uint32_t)G)) !=
+    if ((st = encode_q_rows(&ctx->qmap, a->q, (uint64_t)p.batch * p.num_q_heads * Q, (uint32_t)R)) !=
         DA_OK)
       return st;
     ctx->map_k_base = a->k;
@@ -188,9 +191,10 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.counters = reinterpret_cast<uint32_t *>(ws + pl.counters_offset);
   gp.score_scale = a->scale * 1.4426950408889634f;
   gp.batch = p.batch;
-  gp.num_q_heads = p.num_q_heads;
+  gp.num_q_heads = p.num_q_heads * Q;  // rows of q / out / lse per batch row
   gp.num_kv_heads = p.num_kv_heads;
-  gp.group = p.num_q_heads / p.num_kv_heads;
+  gp.group = R;
+  gp.q_len = Q;
   gp.paged = paged ? 1 : 0;
   gp.page_size = p.page_size;
   gp.cache_len = paged ? 0 : p.max_seq_len;

@@ -60,23 +60,32 @@ template <bool FP8, int NT>
 struct Cfg {
   static constexpr int kBytesPerTok = FP8 ? kD : 2 * kD;
   static constexpr int kTileBytes = kTile * kBytesPerTok;  // one of K or V
-  static constexpr int kStages = FP8 ? (NT == 1 ? 5 : 4) : (NT == 1 ? 3 : 2);
+  static constexpr int kStages = FP8 ? 5 : 3;
   static constexpr int kQSlot = NT * 8 * kD * 2;             // the query group (bf16 rows)
   // shared-memory layout (byte offsets from a 1024-aligned base)
   static constexpr int oRing = 0;                            // [stage][K|V][tile]
   static constexpr int oQ = oRing + kStages * 2 * kTileBytes;
-  static constexpr int oRed = oQ + kStages * kQSlot;          // [8*NT][kRedStride] fp32
-  static constexpr int oFull = oRed + 8 * NT * kRedStride * 4;
+  // The segment epilogue reduces the four warps' partial O^T through the
+  // segment's consumed stage: rows padded to kRedStride floats when that fits,
+  // else plain 128-float rows with an XOR swizzle of the column (both free of
+  // bank conflicts); a separate buffer only when neither fits (e4m3 stages).
+  static constexpr bool kScrPadded = kConsumerWarps * 8 * NT * kRedStride * 4 <= 2 * kTileBytes;
+  static constexpr bool kScrSwizzled = !kScrPadded && kConsumerWarps * 8 * NT * kD * 4 <= 2 * kTileBytes;
+  static constexpr bool kStageScratch = kScrPadded || kScrSwizzled;
+  static constexpr int kScrStride = kScrPadded ? kRedStride : kD;
+  // (the separate buffer also serves the rare staged merge; two n-tiles of
+  // bf16 drop it for a third KV stage and use the query slots there instead)
+  static constexpr int kRedBytes = (kStageScratch && NT == 2) ? 0 : 8 * NT * kRedStride * 4;
+  static constexpr int oRed = oQ + kStages * kQSlot;          // [8*NT][kRedStride] fp32, or nothing
+  static constexpr int oFull = oRed + kRedBytes;
   static constexpr int oEmpty = oFull + 8 * kStages;
   static constexpr int oMeta = oEmpty + 8 * kStages;
-  static constexpr int oStats = oMeta + 24 * kStages;        // m, l per (warp, g)
+  static constexpr int oStats = oMeta + 32 * kStages;        // m, l per (warp, g)
   static constexpr int oScan = oStats + 2 * kConsumerWarps * 16 * 4;
   static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
   static constexpr int oMergeBar = oFlags + 32 * 4;          // 2 mbarriers of the merge staging,
                                                              // 2 partial-segment
   static constexpr int kTotal = oMergeBar + 4 * 8 + 1024;    // + alignment slack
-  // the segment epilogue's per-warp partials fit in the segment's last stage
-  static constexpr bool kStageScratch = kConsumerWarps * 8 * NT * kRedStride * 4 <= 2 * kTileBytes;
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -86,7 +95,9 @@ struct __align__(8) StageMeta {
   int32_t flags;    // kFirst: first tile of a segment (query group in the stage); kLast
   int32_t c_first;  // first CTA holding a segment of this unit
   int32_t n_seg;    // segments of this unit
+  int32_t nval;     // the row's length minus the tile's first position (sparse: kTile)
 };
+static_assert(sizeof(StageMeta) == 32, "the shared-memory layout keeps 32 bytes per stage");
 constexpr int32_t kFirst = 1, kLast = 2;
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -620,7 +631,7 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
 }
 
 template <bool FP8, int NT>
-__global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
+__global__ void __launch_bounds__(threads_for<NT>(), 2)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap, const GqaParams p) {
@@ -885,6 +896,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
         m.flags = (first ? kFirst : 0) | (last ? kLast : 0);
         m.c_first = cur.c_first;
         m.n_seg = cur.n_seg;
+        m.nval = p.sparse_block_size > 0 ? kTile : cur.n_valid - tok_base;
         meta[st] = m;
         const uint32_t box_tokens = (p.paged && P < kTile) ? (uint32_t)P : (uint32_t)kTile;
         uint32_t bytes = 2u * (uint32_t)nbox * box_tokens * C::kBytesPerTok;
@@ -981,6 +993,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
     float oacc[NT][8][4];
     float m_run[NT][2], l_part[NT][2];
     float sscale = p.score_scale, vmul = 1.f;
+    // Query row g * q_len + t (several query tokens per row) sees the positions
+    // n < seq_len - (q_len - 1 - t): its own position among the row's last
+    // q_len tokens and the ones before it. qshift = q_len - 1 - t per held row.
+    int qshift[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) qshift[nt][e] = p.q_len - 1 - (nt * 8 + 2 * q4 + e) % p.q_len;
     auto reset = [&]() {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -1084,8 +1104,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
           float alpha[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float x0 = ok_r ? sacc[nt][e] * sscale : neg_inf();
-            const float x1 = ok_r8 ? sacc[nt][2 + e] * sscale : neg_inf();
+            // causal limit of the query row (the tile's valid bits already stop
+            // at the row's length, so one query token per row changes nothing)
+            const int lim = m.nval - qshift[nt][e];
+            const bool ok0 = ok_r && 16 * warp + r8 < lim, ok1 = ok_r8 && 16 * warp + r8 + 8 < lim;
+            const float x0 = ok0 ? sacc[nt][e] * sscale : neg_inf();
+            const float x1 = ok1 ? sacc[nt][2 + e] * sscale : neg_inf();
             float tmax = fmaxf(x0, x1);
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
@@ -1201,8 +1225,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
       // consumed stage when it fits (one barrier), else added into one buffer
       // one warp at a time
       float *scr = reinterpret_cast<float *>(ring + (size_t)st * 2 * C::kTileBytes);
-      constexpr int kWarpScr = 8 * NT * kRedStride;
+      constexpr int kWarpScr = 8 * NT * C::kScrStride;
+      // column of element (g, d) in a warp's region (swizzled 128-float rows)
+      auto col = [](int g, int d) { return C::kScrSwizzled ? d ^ ((g & 7) << 2) : d; };
+      // this warp's O^T rescaled to the group maximum, to dst (row stride
+      // `stride`, column d at d ^ x); `add` accumulates into the shared buffer
       auto put = [&](float *dst_base, bool add) {
+        constexpr int stride = C::kStageScratch ? C::kScrStride : kRedStride;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1212,15 +1241,16 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
 #pragma unroll
             for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, stat_m[ww * 16 + g]);
             const float wscale = (M == neg_inf()) ? 0.f : ex2(m_run[nt][e] - M);
-            float *dst = dst_base + (size_t)g * kRedStride;
+            float *dst = dst_base + (size_t)g * stride;
+            const int x = C::kScrSwizzled ? (g & 7) << 2 : 0;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
               const int d0 = FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8;
               const int d1 = FP8 ? d0 + 1 : d0 + 8;
               const float v0 = oacc[nt][mt][e] * wscale, v1 = oacc[nt][mt][2 + e] * wscale;
               if (!add) {
-                dst[d0] = v0;
-                dst[d1] = v1;
+                dst[d0 ^ x] = v0;
+                dst[d1 ^ x] = v1;
               } else {
                 dst[d0] += v0;
                 dst[d1] += v1;
@@ -1253,7 +1283,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
         if (C::kStageScratch) {
           acc = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) acc += scr[w * kWarpScr + (size_t)g * kRedStride + d];
+          for (int w = 0; w < kConsumerWarps; ++w)
+            acc += scr[w * kWarpScr + (size_t)g * C::kScrStride + col(g, d)];
         } else {
           acc = red[(size_t)g * kRedStride + d];
         }
@@ -1326,9 +1357,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), NT == 1 ? 2 : 1)
         } else if (warp < kConsumerWarps) {
           // more pieces than the ring holds at once: the staged merge of the consumers
           uint32_t merge_phase[2] = {0u, 0u};
-          if (!merge_unit(p, unit, c_first, n_seg, G, ring, C::kStages * 2 * C::kTileBytes, red,
-                          8 * NT * kRedStride, reinterpret_cast<float *>(qslots), merge_bar,
-                          merge_phase))
+          // scratch: the epilogue buffer, else the query slots past the accumulators
+          float *buf = red;
+          int cap = 8 * NT * kRedStride;
+          if constexpr (C::kRedBytes == 0) {
+            buf = reinterpret_cast<float *>(qslots) + G * kD;
+            cap = C::kStages * C::kQSlot / 4 - G * kD;
+          }
+          if (!merge_unit(p, unit, c_first, n_seg, G, ring, C::kStages * 2 * C::kTileBytes, buf,
+                          cap, reinterpret_cast<float *>(qslots), merge_bar, merge_phase))
             dev_err |= DA_DEVERR_TIMEOUT;
         }
         __syncthreads();

@@ -35,7 +35,9 @@ struct GqaParams {
   uint32_t *err;               // device error word
   uint32_t *counters;          // [units] finished-split counters (self-resetting)
   float score_scale;           // scale * log2(e)
-  int32_t batch, num_q_heads, num_kv_heads, group;
+  int32_t batch, num_q_heads, num_kv_heads, group;  // num_q_heads, group: rows (heads x q_len)
+  int32_t q_len;               // query tokens per row: token t of a unit row g * q_len + t
+                               // sees the positions n <= seq_len - q_len + t
   int32_t paged, page_size, cache_len, max_pages, num_pages;
   int32_t capacity;            // max positions per row
   int32_t sparse_block_size, max_sparse_blocks;

@@ -32,7 +32,8 @@ da_status validate_problem(const da_problem *p) {
   if (p->q_dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout != DA_KV_CONTIGUOUS && p->kv_layout != DA_KV_PAGED) return DA_ERR_INVALID_ARG;
   if (p->kv_dtype != DA_DTYPE_BF16 && p->kv_dtype != DA_DTYPE_FP8_E4M3) return DA_ERR_INVALID_ARG;
-  if (p->max_seq_len < 0) return DA_ERR_INVALID_ARG;
+  if (p->max_seq_len < 0 || p->q_len < 0) return DA_ERR_INVALID_ARG;
+  const int Q = p->q_len > 1 ? p->q_len : 1;  // query tokens per row
   if (p->kv_layout == DA_KV_PAGED) {
     if (p->page_size <= 0 || p->max_pages_per_seq <= 0 || p->num_pages <= 0)
       return DA_ERR_INVALID_ARG;
@@ -40,6 +41,7 @@ da_status validate_problem(const da_problem *p) {
       return DA_ERR_INVALID_ARG;
   }
   if (p->is_mla) {
+    if (Q > 1) return DA_ERR_UNSUPPORTED;
     if (p->num_kv_heads != 1 || p->ckv_dim != 512 || p->kpe_dim != 64 || p->head_dim_qk != 576 ||
         p->head_dim_v != 512 || p->num_q_heads != 128)
       return DA_ERR_UNSUPPORTED;
@@ -50,7 +52,8 @@ da_status validate_problem(const da_problem *p) {
   }
   if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
-  if (G > 16) return DA_ERR_UNSUPPORTED;
+  if (G * Q > 16) return DA_ERR_UNSUPPORTED;  // the G x Q rows of a kv head: two n-tiles at most
+  if (Q > 1 && p->sparse_block_size > 0) return DA_ERR_UNSUPPORTED;
   if (p->head_dim_qk != 128 || p->head_dim_v != 128) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout == DA_KV_PAGED) {
     const int P = p->page_size;
@@ -75,7 +78,8 @@ static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
   const bool mla = p->is_mla != 0;
   const int per_cta = (mla ? mla_smem_bytes()
                            : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3,
-                                            p->num_q_heads / p->num_kv_heads)) +
+                                            p->num_q_heads / p->num_kv_heads *
+                                                (p->q_len > 1 ? p->q_len : 1))) +
                       1024;  // the runtime reserves 1 KB per CTA
   const int threads = mla ? mla_threads() : gqa_threads();
   return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));
@@ -98,7 +102,9 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   const int64_t units = (int64_t)p->batch * heads;
   const int64_t capacity =
       paged ? (int64_t)p->max_pages_per_seq * p->page_size : (int64_t)p->max_seq_len;
-  const int rows = mla ? p->num_q_heads : p->num_q_heads / p->num_kv_heads;
+  // rows per unit: the G query heads (times the query tokens) of a kv head; MLA: all heads
+  const int rows = mla ? p->num_q_heads
+                       : p->num_q_heads / p->num_kv_heads * (p->q_len > 1 ? p->q_len : 1);
   const int dv = p->head_dim_v;
 
   // positions per unit the split kernel walks (sparse: the compacted list)

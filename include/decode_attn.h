@@ -12,6 +12,14 @@
  * (each block of sparse_block_size positions, clipped to seq_lens[b]). An empty
  * P gives out = 0 and lse = -inf.
  *
+ * Several query tokens per row (q_len = Q > 1, speculative decoding; GQA with a
+ * dense cache): the row's new tokens are its last Q positions, already in the
+ * cache, and query token t < Q attends to the positions n <= seq_lens[b] - Q + t
+ * of P(b,h) -- the causal mask of the split-K decode kernel (mslk
+ * splitk_kernels.py, `_fwd_kernel_splitK` with IS_CAUSAL). q, out and lse then
+ * carry a [Q] axis after the head axis (the flex_decode.py.jinja query layout
+ * [.., head, M, D]).
+ *
  * Sources of the operation:
  *  - GQA packing and the block-sparse KV_NUM_BLKS / KV_IDX tables (indexed by
  *    kv head): the TorchInductor flex_decode.py.jinja template (header comment
@@ -82,6 +90,8 @@ enum {
  *   Contiguous: max_seq_len is the cache length L of [B][HKV][L][D].
  *   Sparse (GQA, contiguous only): sparse_block_size a multiple of 64,
  *        max_sparse_blocks columns of kv_idx; 0 = dense.
+ *   q_len: query tokens per row, 0 or 1 = one. Q > 1 needs GQA, a dense
+ *        cache and G * Q <= 16 (the G*Q rows of a kv head share one pass).
  */
 typedef struct {
   int32_t batch, num_q_heads, num_kv_heads;
@@ -96,12 +106,13 @@ typedef struct {
   da_dtype kv_dtype;          /* bf16, or e4m3 for GQA */
   int32_t sparse_block_size;
   int32_t max_sparse_blocks;
+  int32_t q_len;              /* query tokens per row; 0 or 1 = one */
 } da_problem;
 
 /*
  * Per-call arguments: device pointers, caller-owned.
  *
- *   q          bf16 [B][HQ][Dqk]   (MLA: q_nope [B][HQ][512])
+ *   q          bf16 [B][HQ][Dqk]   (MLA: q_nope [B][HQ][512]; q_len Q > 1: [B][HQ][Q][Dqk])
  *   q_pe       MLA only: bf16 [B][HQ][64]; else NULL
  *   k, v       contiguous [B][HKV][L][D]; paged [num_pages][HKV][page_size][D];
  *              MLA: k = ckv [num_pages][page_size][512], v = kpe [num_pages][page_size][64].
@@ -113,8 +124,8 @@ typedef struct {
  *   seq_lens   int32 [B]
  *   kv_num_blks, kv_idx  sparse only: int32 [B][HKV] and [B][HKV][max_sparse_blocks]
  *   scale      the full softmax scale (e.g. 1/sqrt(128)); applied in fp32
- *   out        bf16 [B][HQ][Dv]
- *   lse        fp32 [B][HQ], natural log; may be NULL
+ *   out        bf16 [B][HQ][Dv]    (q_len Q > 1: [B][HQ][Q][Dv])
+ *   lse        fp32 [B][HQ], natural log; may be NULL (q_len Q > 1: [B][HQ][Q])
  */
 typedef struct {
   const void *q;
@@ -138,7 +149,7 @@ typedef struct {
   int32_t chunk_tokens;     /* positions per split (sparse: list entries x block size) */
   int32_t num_splits;       /* S_max: splits per (b, kv head) unit                     */
   int32_t num_units;        /* B x HKV (MLA: B)                                        */
-  int32_t rows_per_unit;    /* G (MLA: HQ)                                             */
+  int32_t rows_per_unit;    /* G x q_len (MLA: HQ)                                     */
   int32_t grid_x, grid_y, grid_z;
   int32_t ctas_per_sm;      /* resident CTAs of the split kernel per SM                */
   int32_t writes_final;     /* 1: one split, the split kernel writes out/lse directly  */

@@ -20,10 +20,9 @@ def run_gpu(w, num_splits_override=None, with_lse=True, seq_lens_host=True, engi
             num_splits_override=w.num_splits if num_splits_override is None else num_splits_override,
             **da.problem_kwargs(w))
     t = w.to(dev)
-    lse = torch.full((w.batch, w.num_q_heads), 12345.0, dtype=torch.float32, device=dev) \
-        if with_lse else None
-    out = torch.full((w.batch, w.num_q_heads, w.head_dim_v), 777.0, dtype=torch.bfloat16,
-                     device=dev)
+    lead = (w.batch, w.num_q_heads) + ((w.q_len,) if w.q_len > 1 else ())
+    lse = torch.full(lead, 12345.0, dtype=torch.float32, device=dev) if with_lse else None
+    out = torch.full(lead + (w.head_dim_v,), 777.0, dtype=torch.bfloat16, device=dev)
     engine.run(t, w.scale, out=out, lse=lse)
     torch.cuda.synchronize()
     flags = engine.errors()

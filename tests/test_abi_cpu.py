@@ -168,7 +168,7 @@ def _check_mla_plan(plan, row_tiles, num_sms=152):
     assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * 2 * 128 * 4
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6])
 def test_planner_covers_every_position_once(lib, cfg):
     w = W.config(cfg, shape_only=True)
     nb = w.tensors.get("kv_num_blks")
@@ -214,3 +214,32 @@ def test_planner_without_host_lengths_assumes_full_rows(lib):
     w = W.config(2, shape_only=True)
     p1 = da.decode_attn_plan_info(_problem(w), 152, None, 0)
     _check_gqa_plan(p1, [w.max_seq_len // 64] * (w.batch * w.num_kv_heads))
+
+
+def test_several_query_tokens_per_row(lib):
+    """q_len > 1: the G x q_len rows of a kv head are one unit (rows_per_unit), at
+    most 16 of them; MLA and block-sparse problems take one query token."""
+    w = W.config(6, shape_only=True)
+    assert w.q_len == 4 and w.tensors["q"].shape == (32, 32, 4, 128)
+    plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], 0)
+    assert plan["rows_per_unit"] == 16 and plan["num_units"] == 256
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim_qk=128, head_dim_v=128,
+                max_seq_len=64)
+    for q_len, status in ((0, da.DA_OK), (1, da.DA_OK), (4, da.DA_OK), (5, da.DA_ERR_UNSUPPORTED),
+                          (-1, da.DA_ERR_INVALID_ARG)):
+        prob = da.make_problem(**base, q_len=q_len)
+        if status == da.DA_OK:
+            info = da.decode_attn_plan_info(prob, 152)
+            assert info["rows_per_unit"] == 4 * max(q_len, 1)
+        else:
+            with pytest.raises(da.DecodeAttnError) as e:
+                da.decode_attn_plan_info(prob, 152)
+            assert e.value.status == status
+    sparse = dict(base, sparse_block_size=64, max_sparse_blocks=1, q_len=2)
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_plan_info(da.make_problem(**sparse), 152)
+    assert e.value.status == da.DA_ERR_UNSUPPORTED
+    m = W.config(5, shape_only=True)
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=2)), 152)
+    assert e.value.status == da.DA_ERR_UNSUPPORTED

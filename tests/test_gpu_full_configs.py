@@ -1,4 +1,5 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the
+"""Parity at the workloads' full sizes (the five decode configurations and the
+speculative-decoding one), in the launch configuration the
 benchmark times (the planner's own split choice from the host lengths), against
 the float64 oracle on every output row (MLA: on a sample of batch rows, which
 the oracle computes independently of the others)."""
@@ -13,7 +14,7 @@ from helpers import assert_parity, reference, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 6])
 def test_full_size_gqa_configs(cfg):
     w = W.config(cfg)
     out, lse, flags, eng = run_gpu(w)

@@ -322,3 +322,33 @@ def test_mla_bad_page_sets_flag():
     out, lse, flags, _ = run_gpu(w, num_splits_override=2)
     assert flags & da.DA_DEVERR_PAGE_INDEX
     assert torch.all(torch.isfinite(out.float()))
+
+
+# ------------------------------------------------------------------ several query tokens per row (causal)
+
+@pytest.mark.parametrize("q_len,group,layout", [(2, 4, "paged"), (3, 2, "contiguous"),
+                                                (4, 4, "paged"), (2, 8, "contiguous"),
+                                                (16, 1, "paged"), (5, 3, "paged")])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_several_query_tokens_causal(q_len, group, layout, splits):
+    # rows shorter than q_len leave their first query tokens without a position
+    # (out 0, LSE -inf); the causal cut falls inside a tile, on a tile boundary
+    # (64, 65) and inside a page
+    lens = [1, 2, 17, 64, 65, 700, 0, 333]
+    w = W.make_gqa(name="spec", batch=8, num_q_heads=2 * group, num_kv_heads=2, seq_lens=lens,
+                   layout=layout, page_size=16, q_len=q_len, seed=400 + 10 * q_len + group)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=splits)
+    assert flags == 0 and eng.plan["rows_per_unit"] == group * q_len
+    assert out.shape == (8, 2 * group, q_len, 128)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"q_len={q_len} G={group} {layout} S={splits}")
+
+
+def test_several_query_tokens_fp8():
+    w = W.make_gqa(name="spec8", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[900, 3, 130],
+                   cache_len=900, kv_fp8=True, q_len=4, seed=431)
+    for S in (0, 2):
+        out, lse, flags, _ = run_gpu(w, num_splits_override=S)
+        assert flags == 0
+        ref_out, ref_lse = reference(w)
+        assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8 q_len=4 S={S}")
