@@ -44,11 +44,10 @@ namespace {
 
 constexpr int kTile = 64;             // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
-// With one n-tile (up to 8 query heads per kv head) a sixth warp takes the
-// row-counter atomics of partial segments off the consumers; with two n-tiles
-// the consumers' registers leave no room for it and thread 0 does them.
+// A sixth warp takes the row-counter atomics of partial segments off the
+// consumers and merges small units while they stream.
 template <int NT>
-constexpr bool has_helper() { return NT == 1; }
+constexpr bool has_helper() { return true; }
 template <int NT>
 constexpr int threads_for() { return (kConsumerWarps + 1 + (has_helper<NT>() ? 1 : 0)) * 32; }
 constexpr int kMaxThreads = (kConsumerWarps + 2) * 32;
@@ -542,8 +541,9 @@ __device__ __noinline__ void merge_slots_small(const GqaParams &p, int unit, int
   __syncthreads();
 }
 
-// One warp merges a unit held by at most kWarpMergeSegs pieces (G <= 8): lane l
-// owns head dims 4l..4l+3; per head the pieces' LSE give weights
+// One warp merges a unit held by at most kWarpMergeSegs pieces whose LSEs fit
+// in its lanes (pieces x rows <= 32): lane l owns head dims 4l..4l+3 of each
+// row in turn; per row the pieces' LSE give weights
 // exp(lse_s - max) and the output is the weighted mean of their normalised O.
 __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c_first, int n_seg,
                                              int G) {
@@ -618,7 +618,7 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
                                             int c_first, int n_seg, bool warp_merge) {
   if (n_seg <= kOneLevelSegs) {
     if (!count_segment(p, unit, n_seg)) return false;
-    if (warp_merge && n_seg <= kWarpMergeSegs) return true;
+    if (warp_merge && n_seg <= kWarpMergeSegs && n_seg * p.group <= 32) return true;
     record_merge(flags, unit, c_first, n_seg, -1);
     return false;
   }
