@@ -15,7 +15,10 @@ Layouts (row-major, last index fastest):
   block_table  int32 [B][max_pages_per_seq]
   seq_lens     int32 [B]
   kv_num_blks  int32 [B][HKV],  kv_idx int32 [B][HKV][max_sparse_blocks]
-  k_scale, v_scale  fp32 [HKV] (fp8 KV only)
+  k_scale, v_scale  fp32 [HKV] (fp8 KV with per-kv-head scales)
+  k_scale_shift, v_scale_shift  int32, one word per cache row (fp8 KV with
+               per-token scales): fp16 scale in the low half, fp16 shift in
+               the high half; contiguous [B][HKV][L], paged [pages][HKV][P]
 
 Conventions of the synthetic data:
   * paged pools hold sum_b ceil(N_b / page_size) pages plus 64 spare pages;
@@ -25,7 +28,10 @@ Conventions of the synthetic data:
     sparse blocks are filled with NaN, so any read of them shows up in the
     output;
   * fp8 KV is quantised per kv head with scale = amax / 448 and a
-    round-to-nearest-even saturating cast to float8_e4m3fn.
+    round-to-nearest-even saturating cast to float8_e4m3fn; with per-token
+    scales each cache row gets shift = (max + min) / 2 and scale =
+    (max - min) / 2 / 448, both rounded to fp16, then the same cast of
+    (x - shift) / scale.
 """
 
 from __future__ import annotations
@@ -61,6 +67,7 @@ class Workload:
     max_sparse_blocks: int = 0
     num_splits: int = 0  # 0: planner decides
     q_len: int = 1       # query tokens per row
+    kv_token_scale: bool = False  # fp8 KV with a per-token fp16 scale and shift
     tensors: dict = field(default_factory=dict)
 
     @property
@@ -120,6 +127,24 @@ def _poison_paged(cache: torch.Tensor, table, seq_lens, page_size, used, head_ax
                 cache[last, n % page_size:] = nan
 
 
+def quantize_e4m3_per_token(x: torch.Tensor):
+    """Per cache row (last axis = D) asymmetric e4m3: fp16 shift = (max + min) / 2,
+    fp16 scale = (max - min) / 2 / 448 (1 for a constant row), RNE saturating
+    cast of (x - shift) / scale. NaN rows stay NaN. Returns (codes, scale_shift
+    int32 words: scale bits low, shift bits high)."""
+    finite = torch.nan_to_num(x, nan=0.0)
+    mx, mn = finite.amax(dim=-1), finite.amin(dim=-1)
+    shift = ((mx + mn) / 2).to(torch.float16)
+    scale = ((mx - mn) / 2 / E4M3_MAX).to(torch.float16)
+    scale = torch.where(scale > 0, scale, torch.ones_like(scale))
+    y = ((finite - shift.float().unsqueeze(-1)) / scale.float().unsqueeze(-1))
+    y = y.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    y = y.view(torch.uint8).masked_fill(torch.isnan(x), 0x7F).view(torch.float8_e4m3fn)
+    words = (scale.view(torch.int16).to(torch.int32) & 0xFFFF) | (
+        shift.view(torch.int16).to(torch.int32) << 16)
+    return y.contiguous(), words.contiguous()
+
+
 def quantize_e4m3(x: torch.Tensor, head_axis: int):
     """Per-kv-head e4m3 quantisation: scale_h = amax_h / 448, RNE saturating cast."""
     dims = [d for d in range(x.dim()) if d != head_axis]
@@ -134,7 +159,8 @@ def quantize_e4m3(x: torch.Tensor, head_axis: int):
 def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_lens,
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
-             num_splits=0, poison=True, shape_only=False, q_len=1) -> Workload:
+             num_splits=0, poison=True, shape_only=False, q_len=1,
+             kv_token_scale=False) -> Workload:
     """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths;
     ``q_len`` > 1 gives each row that many query tokens (its last positions).
     ``shape_only`` skips drawing the K/V caches (lengths, tables and lists are
@@ -147,7 +173,8 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
     q = _randn_bf16((B, HQ, D) if q_len <= 1 else (B, HQ, q_len, D), g)
     w = Workload(name=name, batch=B, num_q_heads=HQ, num_kv_heads=HKV, head_dim_qk=D,
                  head_dim_v=D, scale=float(torch.tensor(scale, dtype=torch.float32)),
-                 kv_fp8=kv_fp8, num_splits=num_splits, q_len=max(1, q_len))
+                 kv_fp8=kv_fp8, num_splits=num_splits, q_len=max(1, q_len),
+                 kv_token_scale=bool(kv_fp8 and kv_token_scale))
     t = {"q": q, "seq_lens": seq_lens}
     if layout == "paged":
         table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
@@ -197,7 +224,11 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
                     mask &= torch.arange(w.cache_len) < int(seq_lens[b])
                     k[b, h, ~mask] = float("nan")
                     v[b, h, ~mask] = float("nan")
-    if kv_fp8:
+    if kv_fp8 and kv_token_scale:
+        kq, kss = quantize_e4m3_per_token(k)
+        vq, vss = quantize_e4m3_per_token(v)
+        t.update(k=kq, v=vq, k_scale_shift=kss, v_scale_shift=vss)
+    elif kv_fp8:
         # quantise the finite values; NaN poison stays NaN (e4m3fn has NaN)
         kf = torch.nan_to_num(k, nan=0.0)
         vf = torch.nan_to_num(v, nan=0.0)

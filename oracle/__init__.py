@@ -53,6 +53,7 @@ class OracleInputs(ctypes.Structure):
         ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("kv_num_blks", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("scale", ctypes.c_double),
+        ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
     ]
 
 
@@ -63,6 +64,8 @@ def lib():
         L = ctypes.CDLL(_LIB)
         L.oracle_bf16_to_double.restype = ctypes.c_double
         L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_double.restype = ctypes.c_double
+        L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         L.oracle_e4m3_to_double.restype = ctypes.c_double
         L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         L.oracle_softmax_attend.restype = None
@@ -120,6 +123,10 @@ def bf16_to_double(bits: int) -> float:
     return lib().oracle_bf16_to_double(bits)
 
 
+def f16_to_double(bits: int) -> float:
+    return lib().oracle_f16_to_double(bits)
+
+
 def e4m3_to_double(byte: int) -> float:
     return lib().oracle_e4m3_to_double(byte)
 
@@ -160,7 +167,7 @@ class _Prepared:
             setattr(p, name, int(prob.get(name, 0)))
         self.problem = p
         self.keep = {k: _bits(v) for k, v in tensors.items()}
-        for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx"):
+        for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift"):
             if self.keep.get(k) is not None:
                 self.keep[k] = self.keep[k].to(torch.int32).contiguous()
         for k in ("k_scale", "v_scale"):
@@ -168,7 +175,7 @@ class _Prepared:
                 self.keep[k] = self.keep[k].to(torch.float32).contiguous()
         i = OracleInputs()
         for k in ("q", "q_pe", "k", "v", "k_scale", "v_scale", "block_table", "seq_lens",
-                  "kv_num_blks", "kv_idx"):
+                  "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift"):
             setattr(i, k, _ptr(self.keep.get(k)))
         i.scale = float(scale)
         self.inputs = i
@@ -182,7 +189,8 @@ def problem_from(work) -> dict:
         head_dim_qk=w.head_dim_qk, head_dim_v=w.head_dim_v, is_mla=int(w.is_mla),
         ckv_dim=w.ckv_dim, kpe_dim=w.kpe_dim, paged=int(w.paged), page_size=w.page_size,
         cache_len=w.cache_len, max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
-        kv_fp8=int(w.kv_fp8), sparse_block_size=w.sparse_block_size,
+        kv_fp8=(2 if getattr(w, "kv_token_scale", False) else 1) if w.kv_fp8 else 0,
+        sparse_block_size=w.sparse_block_size,
         max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1))
 
 

@@ -39,7 +39,10 @@
  *   - fp8 is OCP E4M3FN (the `float8e4nv` type of splitk_kernels.py): sign,
  *     4-bit exponent with bias 7, 3-bit mantissa, subnormals at exponent 0,
  *     no infinities, S.1111.111 is NaN, largest finite value 448; the
- *     dequantised value is e4m3(byte) * scale[kv head].
+ *     dequantised value is e4m3(byte) * scale[kv head], or, with a per-token
+ *     scale and shift (the split-K page's fp8 scale_shift words),
+ *     e4m3(byte) * scale[row] + shift[row];
+ *   - fp16 (the scale and shift) is IEEE-754 binary16.
  *
  * Parity pins: see tests/test_oracle_pins.py (closed forms, invariants, brute
  * force with exact decimal arithmetic, all-code decoder checks).
@@ -59,6 +62,20 @@ double oracle_bf16_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &word, sizeof f);
   return (double)f;
+}
+
+/* IEEE-754 binary16: sign, 5-bit exponent with bias 15, 10-bit mantissa. */
+double oracle_f16_to_double(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int expo = (bits >> 10) & 0x1F;
+  int mant = bits & 0x3FF;
+  double mag;
+  if (expo == 0x1F) return mant ? NAN : (sign ? -INFINITY : INFINITY);
+  if (expo == 0)
+    mag = ldexp((double)mant / 1024.0, 1 - 15); /* subnormal */
+  else
+    mag = ldexp(1.0 + (double)mant / 1024.0, expo - 15);
+  return sign ? -mag : mag;
 }
 
 double oracle_e4m3_to_double(uint8_t byte) {
@@ -149,7 +166,8 @@ typedef struct {
   int32_t cache_len;      /* contiguous cache length L */
   int32_t max_pages_per_seq;
   int32_t num_pages;
-  int32_t kv_fp8;         /* 0: bf16 bits, 1: e4m3 bytes with per-kv-head scale */
+  int32_t kv_fp8;         /* 0: bf16 bits, 1: e4m3 bytes with per-kv-head scale,
+                             2: e4m3 bytes with a per-token fp16 scale and shift */
   int32_t sparse_block_size; /* 0: dense */
   int32_t max_sparse_blocks;
   int32_t q_len;          /* query tokens per row (0 or 1: one) */
@@ -168,6 +186,9 @@ typedef struct {
   const int32_t *kv_num_blks; /* sparse: [B][HKV] */
   const int32_t *kv_idx;      /* sparse: [B][HKV][max_sparse_blocks] */
   double scale;
+  const int32_t *k_scale_shift; /* kv_fp8 == 2: one word per cache row of k: fp16 scale in
+                                   the low half, fp16 shift in the high half */
+  const int32_t *v_scale_shift; /* the same for v */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -249,6 +270,23 @@ static int fetch_kv(const oracle_problem *p, const oracle_inputs *in, int b, int
       kr[p->ckv_dim + d] = kv_elem(p, in->v, row * p->kpe_dim + d, 1.0);
     return ORACLE_OK;
   }
+  if (p->kv_fp8 == 2) {
+    /* per-token asymmetric e4m3 (the split-K decode page's fp8 K/V with a
+     * per-token scale_shift word: `cast_uint32_to_half2` splits it into an
+     * fp16 scale (low half) and shift (high half), and `dequantize` gives
+     * value = e4m3 * scale + shift) */
+    uint32_t kw = (uint32_t)in->k_scale_shift[row], vw = (uint32_t)in->v_scale_shift[row];
+    double ksc = oracle_f16_to_double((uint16_t)(kw & 0xFFFF));
+    double ksh = oracle_f16_to_double((uint16_t)(kw >> 16));
+    double vsc = oracle_f16_to_double((uint16_t)(vw & 0xFFFF));
+    double vsh = oracle_f16_to_double((uint16_t)(vw >> 16));
+    const uint8_t *kb = (const uint8_t *)in->k, *vb = (const uint8_t *)in->v;
+    for (int d = 0; d < p->head_dim_qk; ++d)
+      kr[d] = oracle_e4m3_to_double(kb[row * p->head_dim_qk + d]) * ksc + ksh;
+    for (int d = 0; d < p->head_dim_v; ++d)
+      vr[d] = oracle_e4m3_to_double(vb[row * p->head_dim_v + d]) * vsc + vsh;
+    return ORACLE_OK;
+  }
   double ks = p->kv_fp8 ? (double)in->k_scale[h] : 1.0;
   double vs = p->kv_fp8 ? (double)in->v_scale[h] : 1.0;
   for (int d = 0; d < p->head_dim_qk; ++d) kr[d] = kv_elem(p, in->k, row * p->head_dim_qk + d, ks);
@@ -285,7 +323,9 @@ static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   }
   if (p->paged && (!in->block_table || p->page_size <= 0 || p->max_pages_per_seq < 0))
     return ORACLE_BAD_ARG;
-  if (p->kv_fp8 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
+  if (p->kv_fp8 == 1 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
+  if (p->kv_fp8 == 2 && (!in->k_scale_shift || !in->v_scale_shift || p->is_mla)) return ORACLE_BAD_ARG;
+  if (p->kv_fp8 < 0 || p->kv_fp8 > 2) return ORACLE_BAD_ARG;
   if (p->sparse_block_size > 0 && (!in->kv_num_blks || !in->kv_idx)) return ORACLE_BAD_ARG;
   return ORACLE_OK;
 }

@@ -55,6 +55,16 @@ def test_e4m3_decoder_every_code():
     assert np.nanmax(np.abs(got)) == 448.0
 
 
+def test_f16_decoder_every_code():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = codes.view(torch.float16).double().numpy()
+    got = np.array([oracle.f16_to_double(c & 0xFFFF) for c in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
 def test_e4m3_decoder_golden_codes():
     with open(os.path.join(GOLDEN, "e4m3_codes.txt")) as f:
         rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
@@ -193,6 +203,14 @@ def _dec(x) -> Decimal:
     return Decimal(float(x))
 
 
+def _token_dequant(codes, words):
+    """e4m3 * scale + shift with the per-row words split by torch (fp16 views)."""
+    w = words.to(torch.int32)
+    scale = (w & 0xFFFF).to(torch.int16).view(torch.float16).double()
+    shift = ((w >> 16) & 0xFFFF).to(torch.int16).view(torch.float16).double()
+    return codes.double() * scale.unsqueeze(-1) + shift.unsqueeze(-1)
+
+
 def brute_force(w: W.Workload):
     """Independent 50-digit evaluation straight from the cache layouts."""
     getcontext().prec = 50
@@ -200,7 +218,10 @@ def brute_force(w: W.Workload):
     B, HQ, HKV = w.batch, w.num_q_heads, w.num_kv_heads
     G = HQ // HKV
     q = t["q"].double()
-    if w.kv_fp8:
+    if w.kv_fp8 and w.kv_token_scale:
+        k = _token_dequant(t["k"], t["k_scale_shift"])
+        v = _token_dequant(t["v"], t["v_scale_shift"])
+    elif w.kv_fp8:
         k = t["k"].double() * t["k_scale"].double().view(1, -1, 1, 1)
         v = t["v"].double() * t["v_scale"].double().view(1, -1, 1, 1)
     else:
@@ -263,6 +284,9 @@ def _tiny_cases():
                             seq_lens=[6, 3], layout="paged", page_size=2, seed=12, scale=0.6))
     cases.append(W.make_gqa(name="fp8", batch=1, num_q_heads=2, num_kv_heads=2, head_dim=4,
                             seq_lens=[6], cache_len=6, kv_fp8=True, seed=13, scale=0.5))
+    cases.append(W.make_gqa(name="fp8_token", batch=2, num_q_heads=2, num_kv_heads=1, head_dim=4,
+                            seq_lens=[6, 3], layout="paged", page_size=2, kv_fp8=True,
+                            kv_token_scale=True, seed=19, scale=0.5))
     num = torch.tensor([[2, 1]], dtype=torch.int32)
     idx = torch.tensor([[[2, 0, 0], [1, 0, 0]]], dtype=torch.int32)
     cases.append(W.make_gqa(name="sparse", batch=1, num_q_heads=4, num_kv_heads=2, head_dim=4,
@@ -464,6 +488,52 @@ def test_fp8_dequant_equals_bf16_path_on_dequantised_values():
             o, l = oracle.softmax_attend(s, vd[b, h, :n].numpy())
             assert np.max(np.abs(o - out8[b, hq])) < 1e-12
             assert abs(l - lse8[b, hq]) < 1e-12
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_fp8_per_token_scale_shift_equals_float64_on_dequantised_values(layout):
+    # value = e4m3 * scale[row] + shift[row]: against a numpy evaluation of the
+    # same dequantised rows, gathered through the table independently
+    w = _gqa_case(layout=layout, kv_fp8=True, kv_token_scale=True, poison=False,
+                  seq_lens=[33, 2, 64], head_dim=16, seed=27)
+    t = w.tensors
+    assert oracle.problem_from(w)["kv_fp8"] == 2
+    out8, lse8 = oracle.decode(oracle.problem_from(w), t, w.scale)
+    kd = _token_dequant(t["k"], t["k_scale_shift"])
+    vd = _token_dequant(t["v"], t["v_scale_shift"])
+    q = t["q"].double()
+    for b in range(w.batch):
+        n = int(t["seq_lens"][b])
+        for hq in range(w.num_q_heads):
+            h = hq // w.group
+            if layout == "paged":
+                rows = [(int(t["block_table"][b, i // w.page_size]), i % w.page_size) for i in range(n)]
+                kk = torch.stack([kd[pg, h, r] for pg, r in rows]) if rows else kd[0, h, :0]
+                vv = torch.stack([vd[pg, h, r] for pg, r in rows]) if rows else vd[0, h, :0]
+            else:
+                kk, vv = kd[b, h, :n], vd[b, h, :n]
+            s_ = w.scale * (kk @ q[b, hq]).numpy()
+            o, l = oracle.softmax_attend(s_, vv.numpy())
+            assert np.max(np.abs(o - out8[b, hq])) < 1e-12
+            assert abs(l - lse8[b, hq]) < 1e-12
+
+
+def test_fp8_per_token_shift_alone_moves_scores_by_q_sum():
+    # the same codes and scales with every key shift 0, then every key shift c:
+    # each score of a row grows by c * sum_d q[d], so the softmax is unchanged
+    # and the LSE grows by scale * c * sum(q)
+    w = _gqa_case(kv_fp8=True, kv_token_scale=True, poison=False, seq_lens=[40, 9, 1],
+                  head_dim=16, seed=28)
+    words = w.tensors["k_scale_shift"] & 0xFFFF  # the scales, shift 0
+    c = torch.tensor(0.375, dtype=torch.float16)  # exact in fp16 and float64
+    t0, t1 = dict(w.tensors), dict(w.tensors)
+    t0["k_scale_shift"] = words
+    t1["k_scale_shift"] = words | (int(c.view(torch.int16)) << 16)
+    out0, lse0 = oracle.decode(oracle.problem_from(w), t0, w.scale)
+    out1, lse1 = oracle.decode(oracle.problem_from(w), t1, w.scale)
+    qsum = w.tensors["q"].double().sum(-1).numpy()  # [B][HQ]
+    assert np.max(np.abs(out1 - out0)) < 1e-12
+    assert np.max(np.abs(lse1 - lse0 - w.scale * 0.375 * qsum)) < 1e-9
 
 
 def test_bad_page_index_is_reported():
