@@ -6,10 +6,11 @@ the workload, K/V cache resident in HBM. Default workload: paged GQA decode
 achieved KV-cache bandwidth (algorithmic KV bytes / time, GB/s), with us per
 call and the fraction of measured HBM peak alongside.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..7] [--impl reference]
 
 Configs 1-5 are the five decode workloads; 6 is the speculative-decoding one
-(the paged GQA shapes with 4 query tokens per row, causal over the new tokens).
+(the paged GQA shapes with 4 query tokens per row, causal over the new tokens);
+7 is config 3 with e4m3 K/V scaled per token (fp16 scale and shift per row).
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 units are independent, no collective on the data path); rank 0 prints one
@@ -102,6 +103,8 @@ def algorithmic_bytes(w) -> dict:
         flops = kv_tokens_heads * w.num_q_heads * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
     else:
         kv = kv_tokens_heads * (w.head_dim_qk + w.head_dim_v) * elt
+        if getattr(w, "kv_token_scale", False):
+            kv += kv_tokens_heads * 2 * 4  # the K and V scale words of every row
         q = w.batch * w.num_q_heads * Q * w.head_dim_qk * 2
         flops = kv_tokens_heads * w.group * Q * 2 * (w.head_dim_qk + w.head_dim_v)
     o = w.batch * w.num_q_heads * Q * (w.head_dim_v * 2 + 4)

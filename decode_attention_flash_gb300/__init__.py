@@ -21,13 +21,13 @@ __all__ = [
     "decode_attn_plan", "decode_attn_plan_ex", "decode_attn_get_plan", "decode_attn_plan_info",
     "decode_attn_run", "decode_attn_run_noalloc", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
     "decode_attn_status_string", "DecodeAttention", "DA_KV_CONTIGUOUS", "DA_KV_PAGED",
-    "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3",
+    "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3", "DA_DTYPE_FP8_E4M3_TOKEN_SCALE",
 ]
 
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_CUDA = 0, 1, 2, 3
 DA_ERR_WORKSPACE, DA_ERR_NOT_PLANNED, DA_ERR_DEVICE = 4, 5, 6
 DA_KV_CONTIGUOUS, DA_KV_PAGED = 0, 1
-DA_DTYPE_BF16, DA_DTYPE_FP8_E4M3 = 0, 1
+DA_DTYPE_BF16, DA_DTYPE_FP8_E4M3, DA_DTYPE_FP8_E4M3_TOKEN_SCALE = 0, 1, 2
 DA_DEVERR_PAGE_INDEX, DA_DEVERR_SPARSE_INDEX, DA_DEVERR_SEQ_LEN, DA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 
@@ -57,6 +57,7 @@ class Args(ctypes.Structure):
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("kv_num_blks", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
     ]
 
 
@@ -195,6 +196,8 @@ def make_args(tensors: dict, scale: float, out, lse=None) -> Args:
     a.scale = float(scale)
     a.out = _ptr(out)
     a.lse = _ptr(lse)
+    a.k_scale_shift = _ptr(tensors.get("k_scale_shift"))
+    a.v_scale_shift = _ptr(tensors.get("v_scale_shift"))
     return a
 
 
@@ -286,6 +289,7 @@ def problem_kwargs(work) -> dict:
                 page_size=w.page_size, max_seq_len=w.max_seq_len,
                 max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
                 q_dtype=DA_DTYPE_BF16,
-                kv_dtype=DA_DTYPE_FP8_E4M3 if w.kv_fp8 else DA_DTYPE_BF16,
+                kv_dtype=(DA_DTYPE_FP8_E4M3_TOKEN_SCALE if getattr(w, "kv_token_scale", False)
+                          else DA_DTYPE_FP8_E4M3) if w.kv_fp8 else DA_DTYPE_BF16,
                 sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks,
                 q_len=getattr(w, "q_len", 1))

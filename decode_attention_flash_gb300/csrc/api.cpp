@@ -26,6 +26,11 @@ struct da_ctx {
   const void *map_qpe_base;
   CUtensorMap qmap;
   CUtensorMap qpemap;
+  // per-token scale words of e4m3 K/V (DA_DTYPE_FP8_E4M3_TOKEN_SCALE)
+  const void *map_kss_base;
+  const void *map_vss_base;
+  CUtensorMap kssmap;
+  CUtensorMap vssmap;
 };
 
 namespace {
@@ -113,6 +118,21 @@ da_status encode_bf16_halves(CUtensorMap *map, const void *base, uint64_t rows, 
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
+// Per-token scale words: one int32 per cache row, viewed as [rows / 4][4] so a
+// box of `box_rows` rows is 4 words wide (16 bytes); rows past the end read 0.
+da_status encode_scale_words(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {4, rows / 4};
+  const cuuint64_t strides[1] = {16};
+  const cuuint32_t box[2] = {4u, box_rows / 4};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
 // Query map: [rows][128] bf16, unswizzled boxes of 128 elements x `box_rows` rows.
 da_status encode_q_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -135,13 +155,17 @@ da_status check_workspace(const da_ctx *ctx, const void *ws, size_t bytes) {
 
 da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t stream) {
   const da_problem &p = ctx->prob;
-  const bool fp8 = p.kv_dtype == DA_DTYPE_FP8_E4M3;
+  const bool fp8 = p.kv_dtype != DA_DTYPE_BF16;
+  const bool token_scale = p.kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE;
   const bool paged = p.kv_layout == DA_KV_PAGED;
   const bool sparse = p.sparse_block_size > 0;
   if (!a->q || !a->k || !a->v || !a->seq_lens || !a->out) return DA_ERR_INVALID_ARG;
   if (paged && !a->block_table) return DA_ERR_INVALID_ARG;
   if (sparse && (!a->kv_num_blks || !a->kv_idx)) return DA_ERR_INVALID_ARG;
-  if (fp8 && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
+  if (fp8 && !token_scale && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
+  if (token_scale && (!a->k_scale_shift || !a->v_scale_shift || !aligned(a->k_scale_shift, 16) ||
+                      !aligned(a->v_scale_shift, 16)))
+    return DA_ERR_INVALID_ARG;
   if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 128) || !aligned(a->out, 8))
     return DA_ERR_INVALID_ARG;
 
@@ -172,6 +196,14 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
     ctx->map_v_base = a->v;
     ctx->map_q_base = a->q;
   }
+  if (token_scale && (ctx->map_kss_base != a->k_scale_shift || ctx->map_vss_base != a->v_scale_shift)) {
+    ctx->map_kss_base = ctx->map_vss_base = nullptr;
+    da_status st;
+    if ((st = encode_scale_words(&ctx->kssmap, a->k_scale_shift, rows, box_tokens)) != DA_OK) return st;
+    if ((st = encode_scale_words(&ctx->vssmap, a->v_scale_shift, rows, box_tokens)) != DA_OK) return st;
+    ctx->map_kss_base = a->k_scale_shift;
+    ctx->map_vss_base = a->v_scale_shift;
+  }
 
   const da_plan_info &pl = ctx->plan;
   da::GqaParams gp;
@@ -195,6 +227,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.num_kv_heads = p.num_kv_heads;
   gp.group = R;
   gp.q_len = Q;
+  gp.token_scale = token_scale ? 1 : 0;
   gp.paged = paged ? 1 : 0;
   gp.page_size = p.page_size;
   gp.cache_len = paged ? 0 : p.max_seq_len;
@@ -203,7 +236,9 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.capacity = paged ? p.max_pages_per_seq * p.page_size : p.max_seq_len;
   gp.sparse_block_size = p.sparse_block_size;
   gp.max_sparse_blocks = p.max_sparse_blocks;
-  if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap, gp, pl.grid_x, stream) !=
+  if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,
+                     token_scale ? ctx->kssmap : ctx->kmap, token_scale ? ctx->vssmap : ctx->vmap,
+                     gp, pl.grid_x, stream) !=
       cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;

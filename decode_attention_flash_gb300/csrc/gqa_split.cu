@@ -55,11 +55,11 @@ constexpr int kD = 128;               // head dimension
 constexpr int kRedStride = kD + 4;    // padded row of the epilogue reduction buffer
 constexpr uint32_t kConsumerBar = 1;  // named barrier of the 128 consumer threads
 
-template <bool FP8, int NT>
+template <bool FP8, int NT, bool TOK = false>
 struct Cfg {
   static constexpr int kBytesPerTok = FP8 ? kD : 2 * kD;
   static constexpr int kTileBytes = kTile * kBytesPerTok;  // one of K or V
-  static constexpr int kStages = FP8 ? 5 : 3;
+  static constexpr int kStages = FP8 ? (NT == 1 ? 5 : 4) : 3;
   static constexpr int kQSlot = NT * 8 * kD * 2;             // the query group (bf16 rows)
   // shared-memory layout (byte offsets from a 1024-aligned base)
   static constexpr int oRing = 0;                            // [stage][K|V][tile]
@@ -84,7 +84,17 @@ struct Cfg {
   static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
   static constexpr int oMergeBar = oFlags + 32 * 4;          // 2 mbarriers of the merge staging,
                                                              // 2 partial-segment
-  static constexpr int kTotal = oMergeBar + 4 * 8 + 1024;    // + alignment slack
+  // e4m3 with per-token scales: [stage][K|V][kSSWords] scale words (TMA
+  // destinations: 128-byte aligned, each box at a multiple of 128 bytes, so a
+  // 16-token page box takes 32 words), and the per-warp sums of p * shift of
+  // the value rows ([warp][16])
+  static constexpr int kSSWords = 2 * kTile;
+  static constexpr int oSS = (oMergeBar + 4 * 8 + 127) & ~127;
+  static constexpr int kSSBytes = TOK ? kStages * 2 * kSSWords * 4 : 0;
+  static constexpr int oStatZ = oSS + kSSBytes;
+  static constexpr int kTotal = oStatZ + (TOK ? kConsumerWarps * 16 * 4 : 0) + 1024;  // + slack
+  static_assert(oSS % 128 == 0 && (2 * kSSWords * 4) % 128 == 0, "TMA destinations need 128 B");
+  static_assert(oQ % 128 == 0 && kQSlot % 128 == 0 && kTileBytes % 128 == 0, "TMA destinations");
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -97,6 +107,12 @@ struct __align__(8) StageMeta {
   int32_t nval;     // the row's length minus the tile's first position (sparse: kTile)
 };
 static_assert(sizeof(StageMeta) == 32, "the shared-memory layout keeps 32 bytes per stage");
+
+// Word of token t of a tile in a stage's scale words: boxes of `box_rows` tokens
+// start every max(box_rows, 32) words (128-byte aligned TMA destinations).
+__device__ __forceinline__ int ss_word(int t, int box_rows) {
+  return box_rows >= 32 ? t : t + (t / box_rows) * (32 - box_rows);
+}
 constexpr int32_t kFirst = 1, kLast = 2;
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
@@ -630,12 +646,16 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
   return false;
 }
 
-template <bool FP8, int NT>
+// TOK: e4m3 K/V with per-token scale and shift words (FP8 only).
+template <bool FP8, int NT, bool TOK>
 __global__ void __launch_bounds__(threads_for<NT>(), 2)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
-                     const __grid_constant__ CUtensorMap qmap, const GqaParams p) {
-  using C = Cfg<FP8, NT>;
+                     const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap kssmap,
+                     const __grid_constant__ CUtensorMap vssmap, const GqaParams p) {
+  using C = Cfg<FP8, NT, TOK>;
+  static_assert(!TOK || FP8, "per-token scales are an e4m3 format");
   constexpr int kThreads = threads_for<NT>();
   constexpr bool kHelper = has_helper<NT>();
   extern __shared__ uint8_t smem_raw[];
@@ -900,6 +920,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         meta[st] = m;
         const uint32_t box_tokens = (p.paged && P < kTile) ? (uint32_t)P : (uint32_t)kTile;
         uint32_t bytes = 2u * (uint32_t)nbox * box_tokens * C::kBytesPerTok;
+        if (TOK) bytes += 2u * (uint32_t)nbox * box_tokens * 4;  // scale words
         if (first) bytes += (uint32_t)G * kD * 2;
         mbar_arrive_expect_tx(&full[st], bytes);
         if (!multi_box) {
@@ -916,6 +937,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             if (FP8) {
               tma_load_2d(kdst + off, &kmap, &full[st], 0, ys[k], policy);
               tma_load_2d(vdst + off, &vmap, &full[st], 0, ys[k], policy);
+              if (TOK) {
+                // the boxes' per-token scale words ([K|V][kTile] per stage; the
+                // rows of a box start at a multiple of 4)
+                int32_t *ss = reinterpret_cast<int32_t *>(smem + C::oSS) + st * 2 * C::kSSWords +
+                              ss_word(k * box_rows, box_rows);
+                tma_load_2d(ss, &kssmap, &full[st], 0, ys[k] / 4, policy);
+                tma_load_2d(ss + C::kSSWords, &vssmap, &full[st], 0, ys[k] / 4, policy);
+              }
             } else {
               // one 3-D box: both 64-element halves of box_rows rows, half-major
               tma_load_3d(kdst + off, &kmap, &full[st], 0, ys[k], 0, policy);
@@ -993,6 +1022,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     float oacc[NT][8][4];
     float m_run[NT][2], l_part[NT][2];
     float sscale = p.score_scale, vmul = 1.f;
+    // e4m3 with per-token scale and shift (value = e4m3 * sc + sh): the score
+    // of a key is sc * (q . e4m3) + sh * sum(q), so the MMA runs on the codes
+    // and qsum holds sum(q) of the thread's two query rows; a value's scale
+    // multiplies its row in the PV operand, and its shift adds p * sh to every
+    // output element of the query row (zacc, rescaled like l).
+    constexpr bool tok_scale = TOK;
+    const int32_t *ssw = reinterpret_cast<const int32_t *>(smem + C::oSS);
+    const int ss_rows = (p.paged && p.page_size < kTile) ? p.page_size : kTile;  // rows per box
+    float qsum[NT][2], zacc[NT][2];
     // Query row g * q_len + t (several query tokens per row) sees the positions
     // n < seq_len - (q_len - 1 - t): its own position among the row's last
     // q_len tokens and the ones before it. qshift = q_len - 1 - t per held row.
@@ -1010,6 +1048,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           for (int e = 0; e < 4; ++e) oacc[nt][mt][e] = 0.f;
         m_run[nt][0] = m_run[nt][1] = neg_inf();
         l_part[nt][0] = l_part[nt][1] = 0.f;
+        zacc[nt][0] = zacc[nt][1] = 0.f;
+        qsum[nt][0] = qsum[nt][1] = 0.f;
       }
     };
     reset();
@@ -1050,7 +1090,27 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             }
           }
         }
-        if (FP8) {
+        if (tok_scale) {
+          sscale = p.score_scale;
+          vmul = 1.f;
+          // sum of each query row's values as the MMA sees them (f16): this
+          // thread holds 32 of row r8's elements; the quad's four threads hold all
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float part = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qf[nt][ks][j]));
+                part += f.x + f.y;
+              }
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            qsum[nt][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * q4));
+            qsum[nt][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * q4 + 1));
+          }
+        } else if (FP8) {
           sscale = p.score_scale * p.k_scale[h];
           vmul = p.v_scale[h];
         }
@@ -1098,6 +1158,26 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         }
         // ---------------- mask, online softmax (exp2), P^T fragments
         const bool ok_r = (vbits >> r8) & 1u, ok_r8 = (vbits >> (r8 + 8)) & 1u;
+        float vsh0 = 0.f, vsh1 = 0.f;  // value shifts of the thread's two tokens
+        if (tok_scale) {
+          const int32_t *ssk = ssw + st * 2 * C::kSSWords;
+          const int w0 = ss_word(16 * warp + r8, ss_rows), w1 = ss_word(16 * warp + r8 + 8, ss_rows);
+          const uint32_t k0 = (uint32_t)ssk[w0], k1 = (uint32_t)ssk[w1];
+          const uint32_t v0 = (uint32_t)ssk[C::kSSWords + w0], v1 = (uint32_t)ssk[C::kSSWords + w1];
+          const float2 kf0 = __half22float2(*reinterpret_cast<const __half2 *>(&k0));
+          const float2 kf1 = __half22float2(*reinterpret_cast<const __half2 *>(&k1));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              sacc[nt][e] = fmaf(sacc[nt][e], kf0.x, kf0.y * qsum[nt][e]);
+              sacc[nt][2 + e] = fmaf(sacc[nt][2 + e], kf1.x, kf1.y * qsum[nt][e]);
+            }
+          // a token past the row's end may hold any word: its shift must not
+          // meet its zero weight (0 * inf)
+          vsh0 = ok_r ? __half2float(__ushort_as_half((unsigned short)(v0 >> 16))) : 0.f;
+          vsh1 = ok_r8 ? __half2float(__ushort_as_half((unsigned short)(v1 >> 16))) : 0.f;
+        }
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -1122,6 +1202,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
               p1 = ex2(x1 - m_new);
             }
             l_part[nt][e] = l_part[nt][e] * a + (p0 + p1);
+            if (tok_scale) zacc[nt][e] = zacc[nt][e] * a + (p0 * vsh0 + p1 * vsh1);
             m_run[nt][e] = m_new;
             sacc[nt][e] = p0;
             sacc[nt][2 + e] = p1;
@@ -1164,6 +1245,22 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           }
         } else {
           const int t = tok_lane + (mi & 1) * 8;
+          // per-token value scales of the fragment's token pairs (2q4, 2q4+1) and
+          // (2q4+8, 2q4+9), f16x2, zero past the row's end
+          uint32_t s01 = 0u, s89 = 0u;
+          if (tok_scale) {
+            const int32_t *ssv = ssw + st * 2 * C::kSSWords + C::kSSWords;
+            const int t0 = 16 * warp + 2 * q4;
+            s01 = (((uint32_t)ssv[ss_word(t0, ss_rows)] & 0xFFFFu) |
+                   ((uint32_t)ssv[ss_word(t0 + 1, ss_rows)] << 16)) & m01;
+            s89 = (((uint32_t)ssv[ss_word(t0 + 8, ss_rows)] & 0xFFFFu) |
+                   ((uint32_t)ssv[ss_word(t0 + 9, ss_rows)] << 16)) & m89;
+          }
+          auto hmul2 = [](uint32_t x, uint32_t y) {
+            const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&x),
+                                      *reinterpret_cast<const __half2 *>(&y));
+            return *reinterpret_cast<const uint32_t *>(&r);
+          };
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
             uint32_t r0, r1, r2, r3;
@@ -1188,6 +1285,16 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
               c1 &= m01;
               c2 &= m89;
               c3 &= m89;
+            }
+            if (tok_scale) {
+              a0 = hmul2(a0, s01);
+              a1 = hmul2(a1, s01);
+              a2 = hmul2(a2, s89);
+              a3 = hmul2(a3, s89);
+              c0 = hmul2(c0, s01);
+              c1 = hmul2(c1, s01);
+              c2 = hmul2(c2, s89);
+              c3 = hmul2(c3, s89);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -1214,10 +1321,18 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           l += __shfl_xor_sync(0xffffffffu, l, 8);
           l += __shfl_xor_sync(0xffffffffu, l, 16);
           l_part[nt][e] = l;
+          float z = 0.f;
+          if (tok_scale) {
+            z = zacc[nt][e];
+            z += __shfl_xor_sync(0xffffffffu, z, 4);
+            z += __shfl_xor_sync(0xffffffffu, z, 8);
+            z += __shfl_xor_sync(0xffffffffu, z, 16);
+          }
           if (r8 == 0) {
             const int g = nt * 8 + 2 * q4 + e;
             stat_m[warp * 16 + g] = m_run[nt][e];
             stat_l[warp * 16 + g] = l;
+            if (tok_scale) reinterpret_cast<float *>(smem + C::oStatZ)[warp * 16 + g] = z;
           }
         }
       named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
@@ -1287,6 +1402,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             acc += scr[w * kWarpScr + (size_t)g * C::kScrStride + col(g, d)];
         } else {
           acc = red[(size_t)g * kRedStride + d];
+        }
+        if (tok_scale) {  // the value shifts: the same term for every element of the row
+          const float *stat_z = reinterpret_cast<const float *>(smem + C::oStatZ);
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w)
+            acc += (M == neg_inf()) ? 0.f : stat_z[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
         }
         const float o = (L > 0.f) ? acc * vmul / L : 0.f;
         const float lse = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf();
@@ -1398,21 +1519,25 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   if (dev_err) atomicOr(p.err, dev_err);
 }
 
-template <bool FP8, int NT>
+template <bool FP8, int NT, bool TOK>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FP8, NT>::kTotal);
+  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<FP8, NT, TOK>::kTotal);
 }
 
-template <bool FP8, int NT>
+template <bool FP8, int NT, bool TOK>
 void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
-            const GqaParams &p, int ctas, cudaStream_t stream) {
-  gqa_split_kernel<FP8, NT><<<ctas, threads_for<NT>(), Cfg<FP8, NT>::kTotal, stream>>>(kmap, vmap, qmap, p);
+            const CUtensorMap &kssmap, const CUtensorMap &vssmap, const GqaParams &p, int ctas,
+            cudaStream_t stream) {
+  gqa_split_kernel<FP8, NT, TOK><<<ctas, threads_for<NT>(), Cfg<FP8, NT, TOK>::kTotal, stream>>>(
+      kmap, vmap, qmap, kssmap, vssmap, p);
 }
 
 }  // namespace
 
-int gqa_smem_bytes(bool fp8, int group) {
+int gqa_smem_bytes(bool fp8, int group, bool token_scale) {
+  if (fp8 && token_scale) return group <= 8 ? Cfg<true, 1, true>::kTotal : Cfg<true, 2, true>::kTotal;
   if (fp8) return group <= 8 ? Cfg<true, 1>::kTotal : Cfg<true, 2>::kTotal;
   return group <= 8 ? Cfg<false, 1>::kTotal : Cfg<false, 2>::kTotal;
 }
@@ -1425,26 +1550,29 @@ int gqa_box_tokens(const da_problem &p) {
 
 cudaError_t gqa_prepare(int /*device*/) {
   cudaError_t e;
-  if ((e = set_attr<false, 1>()) != cudaSuccess) return e;
-  if ((e = set_attr<false, 2>()) != cudaSuccess) return e;
-  if ((e = set_attr<true, 1>()) != cudaSuccess) return e;
-  if ((e = set_attr<true, 2>()) != cudaSuccess) return e;
+  if ((e = set_attr<false, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<false, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 1, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 2, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 1, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 2, true>()) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
 cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                       const CUtensorMap &qmap, const GqaParams &p, int ctas,
+                       const CUtensorMap &qmap, const CUtensorMap &kssmap,
+                       const CUtensorMap &vssmap, const GqaParams &p, int ctas,
                        cudaStream_t stream) {
+  const bool two = group > 8;
   if (!fp8) {
-    if (group <= 8)
-      launch<false, 1>(kmap, vmap, qmap, p, ctas, stream);
-    else
-      launch<false, 2>(kmap, vmap, qmap, p, ctas, stream);
+    if (!two) launch<false, 1, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+    else launch<false, 2, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+  } else if (!p.token_scale) {
+    if (!two) launch<true, 1, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+    else launch<true, 2, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   } else {
-    if (group <= 8)
-      launch<true, 1>(kmap, vmap, qmap, p, ctas, stream);
-    else
-      launch<true, 2>(kmap, vmap, qmap, p, ctas, stream);
+    if (!two) launch<true, 1, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+    else launch<true, 2, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   }
   return cudaGetLastError();
 }

@@ -36,6 +36,7 @@ struct GqaParams {
   uint32_t *counters;          // [units] finished-split counters (self-resetting)
   float score_scale;           // scale * log2(e)
   int32_t batch, num_q_heads, num_kv_heads, group;  // num_q_heads, group: rows (heads x q_len)
+  int32_t token_scale;         // e4m3 K/V with per-token scale words (maps kss / vss)
   int32_t q_len;               // query tokens per row: token t of a unit row g * q_len + t
                                // sees the positions n <= seq_len - q_len + t
   int32_t paged, page_size, cache_len, max_pages, num_pages;
@@ -79,10 +80,11 @@ struct MlaParams {
 
 // Kernel launchers (return the launch error).
 cudaError_t gqa_prepare(int device);  // sets shared-memory attributes once per device
-int gqa_smem_bytes(bool fp8, int group);
+int gqa_smem_bytes(bool fp8, int group, bool token_scale);
 int gqa_threads();
 cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                       const CUtensorMap &qmap, const GqaParams &p, int ctas,
+                       const CUtensorMap &qmap, const CUtensorMap &kssmap,
+                       const CUtensorMap &vssmap, const GqaParams &p, int ctas,
                        cudaStream_t stream);
 int gqa_box_tokens(const da_problem &p);
 

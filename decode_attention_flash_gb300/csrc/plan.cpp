@@ -31,7 +31,9 @@ da_status validate_problem(const da_problem *p) {
   if (p->batch <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return DA_ERR_INVALID_ARG;
   if (p->q_dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout != DA_KV_CONTIGUOUS && p->kv_layout != DA_KV_PAGED) return DA_ERR_INVALID_ARG;
-  if (p->kv_dtype != DA_DTYPE_BF16 && p->kv_dtype != DA_DTYPE_FP8_E4M3) return DA_ERR_INVALID_ARG;
+  if (p->kv_dtype != DA_DTYPE_BF16 && p->kv_dtype != DA_DTYPE_FP8_E4M3 &&
+      p->kv_dtype != DA_DTYPE_FP8_E4M3_TOKEN_SCALE)
+    return DA_ERR_INVALID_ARG;
   if (p->max_seq_len < 0 || p->q_len < 0) return DA_ERR_INVALID_ARG;
   const int Q = p->q_len > 1 ? p->q_len : 1;  // query tokens per row
   if (p->kv_layout == DA_KV_PAGED) {
@@ -60,6 +62,11 @@ da_status validate_problem(const da_problem *p) {
     if (P % 16 != 0 || !(kGqaTile % P == 0 || P % kGqaTile == 0)) return DA_ERR_UNSUPPORTED;
   }
   if (p->sparse_block_size < 0 || p->max_sparse_blocks < 0) return DA_ERR_INVALID_ARG;
+  // per-token scale words are fetched by TMA in rows of four: cache rows per
+  // (b, kv head) a multiple of 4
+  if (p->kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE && p->kv_layout == DA_KV_CONTIGUOUS &&
+      p->max_seq_len % 4 != 0)
+    return DA_ERR_UNSUPPORTED;
   if (p->sparse_block_size > 0) {
     if (p->sparse_block_size % kGqaTile != 0) return DA_ERR_UNSUPPORTED;
     if (p->kv_layout != DA_KV_CONTIGUOUS) return DA_ERR_UNSUPPORTED;
@@ -77,9 +84,10 @@ da_status validate_problem(const da_problem *p) {
 static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
   const bool mla = p->is_mla != 0;
   const int per_cta = (mla ? mla_smem_bytes()
-                           : gqa_smem_bytes(p->kv_dtype == DA_DTYPE_FP8_E4M3,
+                           : gqa_smem_bytes(p->kv_dtype != DA_DTYPE_BF16,
                                             p->num_q_heads / p->num_kv_heads *
-                                                (p->q_len > 1 ? p->q_len : 1))) +
+                                                (p->q_len > 1 ? p->q_len : 1),
+                                            p->kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE)) +
                       1024;  // the runtime reserves 1 KB per CTA
   const int threads = mla ? mla_threads() : gqa_threads();
   return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));

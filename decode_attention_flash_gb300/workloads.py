@@ -293,7 +293,8 @@ def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq
 
 # ------------------------------------------------------------------ the workloads
 # 1-5 are the five decode configurations; 6 is the multi-token query extension
-# (speculative decoding) on the paged GQA shapes.
+# (speculative decoding) on the paged GQA shapes; 7 is config 3 with e4m3 K/V
+# scaled per token (fp16 scale and shift per cache row).
 
 CONFIG_NAMES = {
     1: "tiny GQA decode (B1 HQ8 HKV1 D128, contiguous L512, 4 splits)",
@@ -302,6 +303,7 @@ CONFIG_NAMES = {
     4: "block-sparse decode (B8 HQ32 HKV8 D128, L32768, 36 of 256 blocks of 128)",
     5: "MLA latent decode (B64 HQ128, ckv512+kpe64, N_b~U[2048,8192], page 64)",
     6: "speculative paged GQA decode (B32 HQ32 HKV8 D128, 4 query tokens, N_b~U[1024,8192], page 16)",
+    7: "long-context fp8 KV, per-token scale+shift (B1 HQ64 HKV8 D128, contiguous L131072, e4m3)",
 }
 
 
@@ -336,4 +338,8 @@ def config(i: int, shape_only: bool = False) -> Workload:
         lens = _lengths(32, 1024, 8192, g)
         return make_gqa(name="spec_paged_gqa", batch=32, num_q_heads=32, num_kv_heads=8,
                         seq_lens=lens, layout="paged", page_size=16, seed=seed, q_len=4, **so)
+    if i == 7:
+        return make_gqa(name="fp8_token_long", batch=1, num_q_heads=64, num_kv_heads=8,
+                        seq_lens=[131072], cache_len=131072, kv_fp8=True, kv_token_scale=True,
+                        seed=seed, **so)
     raise ValueError(f"no workload {i}")

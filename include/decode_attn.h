@@ -67,7 +67,15 @@ typedef enum {
 } da_status;
 
 typedef enum { DA_KV_CONTIGUOUS = 0, DA_KV_PAGED = 1 } da_kv_layout;
-typedef enum { DA_DTYPE_BF16 = 0, DA_DTYPE_FP8_E4M3 = 1 } da_dtype;
+/* KV element types: bf16; e4m3 with one fp32 scale per kv head (k_scale /
+ * v_scale); or e4m3 with a per-token fp16 scale and shift (k_scale_shift /
+ * v_scale_shift: value = e4m3 * scale + shift, the fp8 scale_shift words of
+ * the split-K decode page, mslk splitk_kernels.py `dequantize`). */
+typedef enum {
+  DA_DTYPE_BF16 = 0,
+  DA_DTYPE_FP8_E4M3 = 1,
+  DA_DTYPE_FP8_E4M3_TOKEN_SCALE = 2
+} da_dtype;
 
 /* Bits of the device error word (sticky until decode_attn_get_error clears it). */
 enum {
@@ -103,7 +111,7 @@ typedef struct {
   int32_t max_pages_per_seq;
   int32_t num_pages;
   da_dtype q_dtype;           /* DA_DTYPE_BF16 only */
-  da_dtype kv_dtype;          /* bf16, or e4m3 for GQA */
+  da_dtype kv_dtype;          /* bf16, or (GQA) e4m3 with per-head or per-token scales */
   int32_t sparse_block_size;
   int32_t max_sparse_blocks;
   int32_t q_len;              /* query tokens per row; 0 or 1 = one */
@@ -116,9 +124,14 @@ typedef struct {
  *   q_pe       MLA only: bf16 [B][HQ][64]; else NULL
  *   k, v       contiguous [B][HKV][L][D]; paged [num_pages][HKV][page_size][D];
  *              MLA: k = ckv [num_pages][page_size][512], v = kpe [num_pages][page_size][64].
- *              Element type bf16, or e4m3 bytes when kv_dtype is DA_DTYPE_FP8_E4M3.
+ *              Element type bf16, or e4m3 bytes when kv_dtype is an e4m3 type.
  *              Base addresses 16-byte aligned.
- *   k_scale, v_scale  fp8 only: fp32 [HKV]; dequantised value = e4m3 * scale
+ *   k_scale, v_scale  DA_DTYPE_FP8_E4M3 only: fp32 [HKV]; dequantised value = e4m3 * scale
+ *   k_scale_shift, v_scale_shift  DA_DTYPE_FP8_E4M3_TOKEN_SCALE only: int32, one word per
+ *              cache row of k / v (contiguous [B][HKV][L], paged [num_pages][HKV][page_size]):
+ *              fp16 scale in the low half, fp16 shift in the high half; dequantised
+ *              value = e4m3 * scale + shift. Base addresses 16-byte aligned; L a
+ *              multiple of 4 (contiguous)
  *   block_table paged: int32 [B][max_pages_per_seq]; entries past a row's
  *              last page are never read
  *   seq_lens   int32 [B]
@@ -141,6 +154,8 @@ typedef struct {
   float scale;
   void *out;
   float *lse;
+  const int32_t *k_scale_shift;
+  const int32_t *v_scale_shift;
 } da_args;
 
 /* What the planner decided (host-side, informational). */

@@ -168,7 +168,7 @@ def _check_mla_plan(plan, row_tiles, num_sms=152):
     assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * 2 * 128 * 4
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
 def test_planner_covers_every_position_once(lib, cfg):
     w = W.config(cfg, shape_only=True)
     nb = w.tensors.get("kv_num_blks")

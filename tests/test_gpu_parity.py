@@ -352,3 +352,31 @@ def test_several_query_tokens_fp8():
         assert flags == 0
         ref_out, ref_lse = reference(w)
         assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8 q_len=4 S={S}")
+
+
+# ------------------------------------------------------------------ e4m3 with a per-token scale and shift
+
+@pytest.mark.parametrize("layout,splits", [("contiguous", 0), ("contiguous", 3), ("paged", 0),
+                                           ("paged", 2)])
+def test_fp8_per_token_scale_shift(layout, splits):
+    lens = [3000, 77, 1, 640] if layout == "contiguous" else [1000, 16, 95, 0]
+    w = W.make_gqa(name="fp8tok", batch=4, num_q_heads=16, num_kv_heads=2, seq_lens=lens,
+                   layout=layout, page_size=16, cache_len=3000 if layout == "contiguous" else None,
+                   kv_fp8=True, kv_token_scale=True, seed=440 + splits)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8/token {layout} S={splits}")
+
+
+def test_fp8_per_token_scale_shift_two_n_tiles_and_several_queries():
+    # 12 query heads per kv head and 2 query tokens: 24 rows -> capped at 16, so use
+    # 16 heads x 1 token (two n-tiles) and 4 heads x 3 tokens (12 rows)
+    for hq, hkv, q_len in ((32, 2, 1), (8, 2, 3)):
+        w = W.make_gqa(name="fp8tok2", batch=2, num_q_heads=hq, num_kv_heads=hkv,
+                       seq_lens=[700, 5], cache_len=700, kv_fp8=True, kv_token_scale=True,
+                       q_len=q_len, seed=450 + hq)
+        out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+        assert flags == 0
+        ref_out, ref_lse = reference(w)
+        assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8/token hq={hq} q_len={q_len}")
