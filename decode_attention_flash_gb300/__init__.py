@@ -10,6 +10,7 @@ fails loudly when the compiled library is missing.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -258,9 +259,15 @@ class DecodeAttention:
 
     def run(self, tensors: dict, scale: float, out=None, lse=None, stream=None):
         p = self.problem
+        lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
         if out is None:
-            lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
             out = torch.empty(lead + (p.head_dim_v,), dtype=torch.bfloat16, device=self.device)
+        # the library writes through raw pointers: refuse buffers of the wrong size
+        # or type here rather than let it write past them
+        if out.dtype != torch.bfloat16 or out.numel() != math.prod(lead) * p.head_dim_v:
+            raise ValueError(f"out must be bf16 with {lead + (p.head_dim_v,)} elements")
+        if lse is not None and (lse.dtype != torch.float32 or lse.numel() != math.prod(lead)):
+            raise ValueError(f"lse must be float32 with {lead} elements")
         decode_attn_run(self.ctx, make_args(tensors, scale, out, lse), self.workspace, stream)
         return out
 

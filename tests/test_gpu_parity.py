@@ -380,3 +380,20 @@ def test_fp8_per_token_scale_shift_two_n_tiles_and_several_queries():
         assert flags == 0
         ref_out, ref_lse = reference(w)
         assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8/token hq={hq} q_len={q_len}")
+
+
+def test_binding_refuses_output_buffers_of_the_wrong_size():
+    # the library writes through raw pointers: the binding checks out / lse first
+    w = W.make_gqa(name="shape", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[70, 5],
+                   cache_len=72, q_len=2, seed=460)
+    dev = torch.device("cuda", 0)
+    eng = da.DecodeAttention(device=0, seq_lens_host=w.tensors["seq_lens"], **da.problem_kwargs(w))
+    t = w.to(dev)
+    with pytest.raises(ValueError):
+        eng.run(t, w.scale, out=torch.empty((2, 8, 128), dtype=torch.bfloat16, device=dev))
+    with pytest.raises(ValueError):
+        eng.run(t, w.scale, lse=torch.empty((2, 8), dtype=torch.float32, device=dev))
+    out = eng.run(t, w.scale)
+    torch.cuda.synchronize()
+    assert out.shape == (2, 8, 2, 128) and eng.errors() == 0
+    eng.close()
