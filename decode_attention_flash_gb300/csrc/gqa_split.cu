@@ -569,40 +569,50 @@ __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c
   const float my_lse = lane < n_seg * G ? __ldcg(p.lse_part + slot0 * G + lane) : neg_inf();
   const float4 *o_base = reinterpret_cast<const float4 *>(p.o_part + slot0 * G * kD);
   __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
+  // rows in rounds of four, every load of a round issued before any use
+  constexpr int kRows = 4;
 #pragma unroll 1
-  for (int g = 0; g < G; ++g) {
-    float4 v[kWarpMergeSegs];
+  for (int g0 = 0; g0 < G; g0 += kRows) {
+    float4 v[kRows][kWarpMergeSegs];
 #pragma unroll
-    for (int s = 0; s < kWarpMergeSegs; ++s)
-      v[s] = s < n_seg ? __ldcg(o_base + ((int64_t)s * G + g) * (kD / 4) + lane)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    float l[kWarpMergeSegs], M = neg_inf();
+    for (int r = 0; r < kRows; ++r)
 #pragma unroll
-    for (int s = 0; s < kWarpMergeSegs; ++s) {
-      l[s] = __shfl_sync(0xffffffffu, my_lse, min(s * G + g, 31));
-      if (s < n_seg) M = fmaxf(M, l[s]);
-    }
-    float sum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < kWarpMergeSegs; ++s)
+        v[r][s] = (g0 + r < G && s < n_seg)
+                      ? __ldcg(o_base + ((int64_t)s * G + g0 + r) * (kD / 4) + lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int s = 0; s < kWarpMergeSegs; ++s) {
-      const float w = (s < n_seg && l[s] != neg_inf() && M != neg_inf())
-                          ? ex2((l[s] - M) * 1.4426950408889634f)
-                          : 0.f;
-      if (w != 0.f) {  // a piece of weight 0 may hold anything
-        sum += w;
-        acc.x += w * v[s].x;
-        acc.y += w * v[s].y;
-        acc.z += w * v[s].z;
-        acc.w += w * v[s].w;
+    for (int r = 0; r < kRows; ++r) {
+      const int g = g0 + r;
+      float l[kWarpMergeSegs], M = neg_inf();
+#pragma unroll
+      for (int s = 0; s < kWarpMergeSegs; ++s) {
+        l[s] = __shfl_sync(0xffffffffu, my_lse, min(s * G + g, 31));
+        if (s < n_seg) M = fmaxf(M, l[s]);
       }
+      if (g >= G) continue;
+      float sum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kWarpMergeSegs; ++s) {
+        const float w = (s < n_seg && l[s] != neg_inf() && M != neg_inf())
+                            ? ex2((l[s] - M) * 1.4426950408889634f)
+                            : 0.f;
+        if (w != 0.f) {  // a piece of weight 0 may hold anything
+          sum += w;
+          acc.x += w * v[r][s].x;
+          acc.y += w * v[r][s].y;
+          acc.z += w * v[r][s].z;
+          acc.w += w * v[r][s].w;
+        }
+      }
+      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      *reinterpret_cast<uint2 *>(out + (int64_t)g * kD + 4 * lane) =
+          make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+      if (lane == 0 && p.lse)
+        p.lse[(int64_t)b * p.num_q_heads + h * G + g] =
+            sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
     }
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    *reinterpret_cast<uint2 *>(out + (int64_t)g * kD + 4 * lane) =
-        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
-    if (lane == 0 && p.lse)
-      p.lse[(int64_t)b * p.num_q_heads + h * G + g] =
-          sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
   }
   if (lane == 0) p.counters[unit] = 0u;  // ready for the next call
 }
