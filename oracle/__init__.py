@@ -54,6 +54,7 @@ class OracleInputs(ctypes.Structure):
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("kv_num_blks", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("scale", ctypes.c_double),
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
+        ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
     ]
 
 
@@ -167,7 +168,8 @@ class _Prepared:
             setattr(p, name, int(prob.get(name, 0)))
         self.problem = p
         self.keep = {k: _bits(v) for k, v in tensors.items()}
-        for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift"):
+        for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift",
+                  "kv_full_num_blks", "kv_full_idx"):
             if self.keep.get(k) is not None:
                 self.keep[k] = self.keep[k].to(torch.int32).contiguous()
         for k in ("k_scale", "v_scale"):
@@ -175,7 +177,8 @@ class _Prepared:
                 self.keep[k] = self.keep[k].to(torch.float32).contiguous()
         i = OracleInputs()
         for k in ("q", "q_pe", "k", "v", "k_scale", "v_scale", "block_table", "seq_lens",
-                  "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift"):
+                  "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift", "kv_full_num_blks",
+                  "kv_full_idx"):
             setattr(i, k, _ptr(self.keep.get(k)))
         i.scale = float(scale)
         self.inputs = i

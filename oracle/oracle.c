@@ -10,7 +10,8 @@
  *
  *   for every batch row b and query head hq, with kv head h = hq / G:
  *     P(b,h)  = the valid KV positions of that row (dense: 0..N_b-1; block
- *               sparse: the listed blocks, in list order, clipped to N_b)
+ *               sparse: the listed blocks, in list order, clipped to N_b --
+ *               the blocks of KV_IDX, then those of FULL_KV_IDX when given)
  *     s_n     = scale * sum_d q[d] * k_n[d]                  (n in P)
  *     m       = max_n s_n
  *     l       = sum_n exp(s_n - m)
@@ -189,6 +190,8 @@ typedef struct {
   const int32_t *k_scale_shift; /* kv_fp8 == 2: one word per cache row of k: fp16 scale in
                                    the low half, fp16 shift in the high half */
   const int32_t *v_scale_shift; /* the same for v */
+  const int32_t *kv_full_num_blks; /* sparse, optional: [B][HKV] blocks of the full list */
+  const int32_t *kv_full_idx;      /* sparse, optional: [B][HKV][max_sparse_blocks] */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -200,7 +203,8 @@ enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM 
 static int64_t max_positions(const oracle_problem *p) {
   int64_t cap = p->paged ? (int64_t)p->max_pages_per_seq * p->page_size : p->cache_len;
   if (p->sparse_block_size > 0) {
-    int64_t sp = (int64_t)p->max_sparse_blocks * p->sparse_block_size;
+    /* both tables of the block mask */
+    int64_t sp = 2 * (int64_t)p->max_sparse_blocks * p->sparse_block_size;
     if (sp > cap) cap = sp;
   }
   return cap;
@@ -232,6 +236,22 @@ static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b
     for (int64_t t = 0; t < sbs; ++t) {
       int64_t n = blk * sbs + t;
       if (n < nb) pos[count++] = n;
+    }
+  }
+  /* the second table of the flex block mask (FULL_KV_NUM_BLKS / FULL_KV_IDX):
+   * blocks that need no mask_mod; with no mask_mod in this definition they
+   * are attended exactly like the first table's blocks, after them */
+  if (in->kv_full_num_blks) {
+    int32_t nfull = in->kv_full_num_blks[(int64_t)b * p->num_kv_heads + h];
+    if (nfull < 0 || nfull > p->max_sparse_blocks) return ORACLE_BAD_INDEX;
+    const int32_t *full = in->kv_full_idx + ((int64_t)b * p->num_kv_heads + h) * p->max_sparse_blocks;
+    for (int32_t j = 0; j < nfull; ++j) {
+      int64_t blk = full[j];
+      if (blk < 0 || blk * sbs >= capacity) return ORACLE_BAD_INDEX;
+      for (int64_t t = 0; t < sbs; ++t) {
+        int64_t n = blk * sbs + t;
+        if (n < nb) pos[count++] = n;
+      }
     }
   }
   return count;
@@ -327,6 +347,8 @@ static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   if (p->kv_fp8 == 2 && (!in->k_scale_shift || !in->v_scale_shift || p->is_mla)) return ORACLE_BAD_ARG;
   if (p->kv_fp8 < 0 || p->kv_fp8 > 2) return ORACLE_BAD_ARG;
   if (p->sparse_block_size > 0 && (!in->kv_num_blks || !in->kv_idx)) return ORACLE_BAD_ARG;
+  if ((in->kv_full_num_blks != NULL) != (in->kv_full_idx != NULL)) return ORACLE_BAD_ARG;
+  if (in->kv_full_num_blks && p->sparse_block_size <= 0) return ORACLE_BAD_ARG;
   return ORACLE_OK;
 }
 

@@ -234,10 +234,14 @@ def brute_force(w: W.Workload):
         h = hq // G
         if w.sparse_block_size:
             pos = []
-            for j in range(int(t["kv_num_blks"][b, h])):
-                blk = int(t["kv_idx"][b, h, j])
-                pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
-                        if blk * w.sparse_block_size + i < n_b]
+            lists = [(t["kv_num_blks"], t["kv_idx"])]
+            if "kv_full_num_blks" in t:
+                lists.append((t["kv_full_num_blks"], t["kv_full_idx"]))
+            for nums, idx in lists:
+                for j in range(int(nums[b, h])):
+                    blk = int(idx[b, h, j])
+                    pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
+                            if blk * w.sparse_block_size + i < n_b]
         else:
             pos = list(range(n_b))
         # query token tq of Q is the row's position n_b - Q + tq: it sees n <= that
@@ -292,6 +296,13 @@ def _tiny_cases():
     cases.append(W.make_gqa(name="sparse", batch=1, num_q_heads=4, num_kv_heads=2, head_dim=4,
                             seq_lens=[5], cache_len=6, sparse_block_size=2, kv_num_blks=num,
                             kv_idx=idx, seed=14, scale=0.8))
+    full = W.make_gqa(name="sparse_full", batch=1, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                      seq_lens=[7], cache_len=8, sparse_block_size=2,
+                      kv_num_blks=torch.tensor([[1, 0]]), kv_idx=torch.tensor([[[3, 0, 0], [0, 0, 0]]]),
+                      seed=20, scale=0.8, poison=False)
+    full.tensors["kv_full_num_blks"] = torch.tensor([[1, 2]], dtype=torch.int32)
+    full.tensors["kv_full_idx"] = torch.tensor([[[0, 0, 0], [2, 1, 0]]], dtype=torch.int32)
+    cases.append(full)
     cases.append(W.make_mla(name="mla", batch=2, num_q_heads=3, ckv_dim=4, kpe_dim=2,
                             seq_lens=[4, 2], page_size=2, seed=15, scale=0.9))
     cases.append(W.make_gqa(name="empty_row", batch=2, num_q_heads=2, num_kv_heads=1,
@@ -534,6 +545,33 @@ def test_fp8_per_token_shift_alone_moves_scores_by_q_sum():
     qsum = w.tensors["q"].double().sum(-1).numpy()  # [B][HQ]
     assert np.max(np.abs(out1 - out0)) < 1e-12
     assert np.max(np.abs(lse1 - lse0 - w.scale * 0.375 * qsum)) < 1e-9
+
+
+def test_full_block_table_equals_appending_its_blocks_to_the_first():
+    # without a mask_mod, the flex block mask's FULL_KV tables are attended like
+    # the KV tables: the same result as one list holding both, in that order
+    w = _sparse_case(poison=False)
+    t = dict(w.tensors)
+    nb, idx = t["kv_num_blks"], t["kv_idx"]
+    keep = (nb // 2).to(torch.int32)  # first half of each list stays, the rest moves
+    full_n = (nb - keep).to(torch.int32)
+    full_idx = torch.zeros_like(idx)
+    part_idx = torch.zeros_like(idx)
+    for b in range(idx.shape[0]):
+        for h in range(idx.shape[1]):
+            k, n = int(keep[b, h]), int(nb[b, h])
+            part_idx[b, h, :k] = idx[b, h, :k]
+            full_idx[b, h, :n - k] = idx[b, h, k:n]
+    split = dict(t, kv_num_blks=keep, kv_idx=part_idx, kv_full_num_blks=full_n, kv_full_idx=full_idx)
+    o1, l1 = oracle.decode(oracle.problem_from(w), t, w.scale, num_threads=2)
+    o2, l2 = oracle.decode(oracle.problem_from(w), split, w.scale, num_threads=2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # a bad full-list entry is an index error, like a bad first-list entry
+    assert int(full_n[0, 0]) > 0
+    bad = dict(split, kv_full_idx=full_idx.clone())
+    bad["kv_full_idx"][0, 0, 0] = 10 ** 6
+    with pytest.raises(ValueError):
+        oracle.decode(oracle.problem_from(w), bad, w.scale)
 
 
 def test_bad_page_index_is_reported():
