@@ -59,6 +59,7 @@ class Args(ctypes.Structure):
         ("kv_num_blks", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
+        ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
     ]
 
 
@@ -199,6 +200,8 @@ def make_args(tensors: dict, scale: float, out, lse=None) -> Args:
     a.lse = _ptr(lse)
     a.k_scale_shift = _ptr(tensors.get("k_scale_shift"))
     a.v_scale_shift = _ptr(tensors.get("v_scale_shift"))
+    a.kv_full_num_blks = _ptr(tensors.get("kv_full_num_blks"))
+    a.kv_full_idx = _ptr(tensors.get("kv_full_idx"))
     return a
 
 

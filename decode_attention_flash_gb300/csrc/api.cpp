@@ -162,6 +162,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   if (!a->q || !a->k || !a->v || !a->seq_lens || !a->out) return DA_ERR_INVALID_ARG;
   if (paged && !a->block_table) return DA_ERR_INVALID_ARG;
   if (sparse && (!a->kv_num_blks || !a->kv_idx)) return DA_ERR_INVALID_ARG;
+  if ((a->kv_full_num_blks != nullptr) != (a->kv_full_idx != nullptr)) return DA_ERR_INVALID_ARG;
+  if (a->kv_full_num_blks && !sparse) return DA_ERR_INVALID_ARG;
   if (fp8 && !token_scale && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
   if (token_scale && (!a->k_scale_shift || !a->v_scale_shift || !aligned(a->k_scale_shift, 16) ||
                       !aligned(a->v_scale_shift, 16)))
@@ -213,6 +215,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.seq_lens = a->seq_lens;
   gp.kv_num_blks = a->kv_num_blks;
   gp.kv_idx = a->kv_idx;
+  gp.kv_full_num_blks = a->kv_full_num_blks;
+  gp.kv_full_idx = a->kv_full_idx;
   gp.k_scale = a->k_scale;
   gp.v_scale = a->v_scale;
   gp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);

@@ -125,6 +125,7 @@ __device__ __forceinline__ uint64_t low_bits(int n) {
 
 struct UnitInfo {
   int b, h, n_valid, tiles;
+  int nbp;  // sparse: blocks of the first table (the full table's follow them)
 };
 
 // Length (checked against the cache) and tile count of unit u.
@@ -144,8 +145,15 @@ __device__ __forceinline__ UnitInfo unit_info(const GqaParams &p, int u, uint32_
       err |= DA_DEVERR_SPARSE_INDEX;
       nb = nb < 0 ? 0 : p.max_sparse_blocks;
     }
-    x.tiles = nb * (p.sparse_block_size / kTile);
+    int nf = p.kv_full_num_blks ? p.kv_full_num_blks[u] : 0;  // the flex FULL_KV table
+    if (nf < 0 || nf > p.max_sparse_blocks) {
+      err |= DA_DEVERR_SPARSE_INDEX;
+      nf = nf < 0 ? 0 : p.max_sparse_blocks;
+    }
+    x.nbp = nb;
+    x.tiles = (nb + nf) * (p.sparse_block_size / kTile);
   } else {
+    x.nbp = 0;
     x.tiles = (n + kTile - 1) / kTile;
   }
   return x;
@@ -179,7 +187,7 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int *to
 }
 
 struct TileDesc {
-  int unit, b, h, n_valid, j, tiles;  // unit, its row / head, length, tile index, tile count
+  int unit, b, h, n_valid, j, tiles, nbp;  // unit, its row / head, length, tile index, tile count
   int64_t P;                          // global index of the unit's first tile
   int c_first, n_seg;                 // CTAs holding the unit's segments
   int wi;                             // position in this CTA's processing order
@@ -792,6 +800,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.h = x.h;
       d.n_valid = x.n_valid;
       d.tiles = x.tiles;
+      d.nbp = x.nbp;
       d.j = j;
       d.P = P0;
       d.c_first = cta_of(d.P, T, CTAS);
@@ -812,7 +821,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     auto load_id = [&](const TileDesc &d, int k) -> int {
       if (p.sparse_block_size > 0) {
         const int e = d.j / (p.sparse_block_size / kTile);
-        const int blk = p.kv_idx[(int64_t)d.unit * p.max_sparse_blocks + e];
+        // list entry e: the first table's, then the full table's
+        const int blk = e < d.nbp ? p.kv_idx[(int64_t)d.unit * p.max_sparse_blocks + e]
+                                  : p.kv_full_idx[(int64_t)d.unit * p.max_sparse_blocks + e - d.nbp];
         const bool bad = blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len;
         dev_err |= bad ? DA_DEVERR_SPARSE_INDEX : 0u;
         return bad ? -1 : blk;
@@ -842,6 +853,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.h = x.h;
       d.n_valid = x.n_valid;
       d.tiles = x.tiles;
+      d.nbp = x.nbp;
       d.j = 0;
       d.c_first = cta_of(d.P, T, CTAS);
       d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;

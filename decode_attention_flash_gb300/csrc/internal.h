@@ -26,6 +26,8 @@ struct GqaParams {
   const int32_t *seq_lens;     // [B]
   const int32_t *kv_num_blks;  // sparse: [B][HKV]
   const int32_t *kv_idx;       // sparse: [B][HKV][max_sparse_blocks]
+  const int32_t *kv_full_num_blks;  // sparse, optional: the full-block table, [B][HKV]
+  const int32_t *kv_full_idx;       // and [B][HKV][max_sparse_blocks] (attended after kv_idx)
   const float *k_scale;        // fp8: [HKV]
   const float *v_scale;        // fp8: [HKV]
   float *o_part;               // [units + ctas][G][128] partial slots (slot = unit + cta)

@@ -136,6 +136,11 @@ typedef struct {
  *              last page are never read
  *   seq_lens   int32 [B]
  *   kv_num_blks, kv_idx  sparse only: int32 [B][HKV] and [B][HKV][max_sparse_blocks]
+ *   kv_full_num_blks, kv_full_idx  sparse only, optional (both NULL or both set): the
+ *              second table pair of the flex block mask (FULL_KV_NUM_BLKS / FULL_KV_IDX,
+ *              blocks that need no mask_mod), same shapes; their blocks are attended
+ *              after the kv_idx blocks. Pass the two tables' summed counts as the
+ *              planner's kv_num_blks_host, or none.
  *   scale      the full softmax scale (e.g. 1/sqrt(128)); applied in fp32
  *   out        bf16 [B][HQ][Dv]    (q_len Q > 1: [B][HQ][Q][Dv])
  *   lse        fp32 [B][HQ], natural log; may be NULL (q_len Q > 1: [B][HQ][Q])
@@ -156,6 +161,8 @@ typedef struct {
   float *lse;
   const int32_t *k_scale_shift;
   const int32_t *v_scale_shift;
+  const int32_t *kv_full_num_blks;
+  const int32_t *kv_full_idx;
 } da_args;
 
 /* What the planner decided (host-side, informational). */

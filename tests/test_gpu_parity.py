@@ -397,3 +397,51 @@ def test_binding_refuses_output_buffers_of_the_wrong_size():
     torch.cuda.synchronize()
     assert out.shape == (2, 8, 2, 128) and eng.errors() == 0
     eng.close()
+
+
+# ------------------------------------------------------------------ the flex block mask's full-block table
+
+def _split_lists(w):
+    """The same kept blocks as two tables: the first half of each list stays in
+    KV_NUM_BLKS / KV_IDX, the rest moves to FULL_KV_NUM_BLKS / FULL_KV_IDX."""
+    nb, idx = w.tensors["kv_num_blks"], w.tensors["kv_idx"]
+    keep = (nb // 2).to(torch.int32)
+    part, full = torch.zeros_like(idx), torch.zeros_like(idx)
+    for b in range(idx.shape[0]):
+        for h in range(idx.shape[1]):
+            k, n = int(keep[b, h]), int(nb[b, h])
+            part[b, h, :k] = idx[b, h, :k]
+            full[b, h, :n - k] = idx[b, h, k:n]
+    return dict(w.tensors, kv_num_blks=keep, kv_idx=part, kv_full_num_blks=(nb - keep).to(torch.int32),
+                kv_full_idx=full)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_full_block_table(splits):
+    w = _sparse()
+    whole = dict(w.tensors)
+    w.tensors = _split_lists(w)
+    nb_total = whole["kv_num_blks"]  # the planner's host counts: both tables summed
+    eng = da.DecodeAttention(device=0, seq_lens_host=w.tensors["seq_lens"], kv_num_blks_host=nb_total,
+                             num_splits_override=splits, **da.problem_kwargs(w))
+    out, lse, flags, _ = run_gpu(w, engine=eng)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"full table S={splits}")
+    # the same tiles in the same order as one list: bit-identical on the GPU
+    w.tensors = whole
+    out1, lse1, flags1, _ = run_gpu(w, engine=eng)
+    assert flags1 == 0 and torch.equal(out1, out) and torch.equal(lse1, lse)
+    eng.close()
+
+
+def test_bad_full_table_index_sets_flag():
+    w = _sparse()
+    t = _split_lists(w)
+    t["kv_full_idx"] = t["kv_full_idx"].clone()
+    t["kv_full_idx"][0, 0, 0] = 10 ** 6
+    assert int(t["kv_full_num_blks"][0, 0]) > 0
+    w.tensors = t
+    out, lse, flags, _ = run_gpu(w)
+    assert flags & da.DA_DEVERR_SPARSE_INDEX
+    assert torch.all(torch.isfinite(out.float()))
