@@ -55,6 +55,7 @@ class OracleInputs(ctypes.Structure):
         ("kv_num_blks", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p), ("scale", ctypes.c_double),
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
+        ("softcap", ctypes.c_double),
     ]
 
 
@@ -162,7 +163,7 @@ def merge(o, lse):
 class _Prepared:
     """Keeps the marshalled host tensors alive while the C call runs."""
 
-    def __init__(self, prob: dict, tensors: dict, scale: float):
+    def __init__(self, prob: dict, tensors: dict, scale: float, softcap: float = 0.0):
         p = OracleProblem()
         for name, _ in OracleProblem._fields_:
             setattr(p, name, int(prob.get(name, 0)))
@@ -181,6 +182,7 @@ class _Prepared:
                   "kv_full_idx"):
             setattr(i, k, _ptr(self.keep.get(k)))
         i.scale = float(scale)
+        i.softcap = float(softcap)
         self.inputs = i
 
 
@@ -197,10 +199,11 @@ def problem_from(work) -> dict:
         max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1))
 
 
-def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = None):
+def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = None,
+           softcap: float = 0.0):
     """Full decode attention -> (out [B][HQ][Dv], lse [B][HQ]) in float64; with
     several query tokens (q_len = Q > 1) out [B][HQ][Q][Dv] and lse [B][HQ][Q]."""
-    prep = _Prepared(prob, tensors, scale)
+    prep = _Prepared(prob, tensors, scale, softcap)
     p = prep.problem
     lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
     out = np.zeros(lead + (p.head_dim_v,), dtype=np.float64)

@@ -13,6 +13,7 @@
  *               sparse: the listed blocks, in list order, clipped to N_b --
  *               the blocks of KV_IDX, then those of FULL_KV_IDX when given)
  *     s_n     = scale * sum_d q[d] * k_n[d]                  (n in P)
+ *               (with a soft cap c > 0: s_n = c * tanh(s_n / c))
  *     m       = max_n s_n
  *     l       = sum_n exp(s_n - m)
  *     out[d]  = sum_n exp(s_n - m) * v_n[d] / l
@@ -192,6 +193,7 @@ typedef struct {
   const int32_t *v_scale_shift; /* the same for v */
   const int32_t *kv_full_num_blks; /* sparse, optional: [B][HKV] blocks of the full list */
   const int32_t *kv_full_idx;      /* sparse, optional: [B][HKV][max_sparse_blocks] */
+  double softcap;                  /* > 0: scores become softcap * tanh(score / softcap) */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -401,6 +403,9 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
     double dot = 0.0;
     for (int d = 0; d < dq; ++d) dot += qr[d] * kr[d];
     s[j] = in->scale * dot;
+    /* tanh soft-capping of the scaled score (the FlashAttention-3 page:
+     * tanh(scores * softmax_scale / softcap_val) * softcap_val) */
+    if (in->softcap > 0.0) s[j] = in->softcap * tanh(s[j] / in->softcap);
   }
   if (job->num_chunks == 0) {
     oracle_softmax_attend(n, s, vrows, dv, job->out + row * dv, job->lse + row);

@@ -211,7 +211,12 @@ def _token_dequant(codes, words):
     return codes.double() * scale.unsqueeze(-1) + shift.unsqueeze(-1)
 
 
-def brute_force(w: W.Workload):
+def _dec_tanh(x: Decimal) -> Decimal:
+    e = (2 * x).exp()
+    return (e - 1) / (e + 1)
+
+
+def brute_force(w: W.Workload, softcap: float = 0.0):
     """Independent 50-digit evaluation straight from the cache layouts."""
     getcontext().prec = 50
     t = w.tensors
@@ -269,6 +274,9 @@ def brute_force(w: W.Workload):
             continue
         s = [_dec(w.scale) * sum(_dec(a) * _dec(c) for a, c in zip(qv.tolist(), kk.tolist()))
              for kk in keys]
+        if softcap > 0:
+            cap = _dec(softcap)
+            s = [cap * _dec_tanh(x / cap) for x in s]
         m = max(s)
         e = [(x - m).exp() for x in s]
         den = sum(e)
@@ -572,6 +580,37 @@ def test_full_block_table_equals_appending_its_blocks_to_the_first():
     bad["kv_full_idx"][0, 0, 0] = 10 ** 6
     with pytest.raises(ValueError):
         oracle.decode(oracle.problem_from(w), bad, w.scale)
+
+
+@pytest.mark.parametrize("softcap", [0.5, 3.0])
+def test_softcap_brute_force(softcap):
+    # tanh soft-capping of the scaled score, against 50-digit exp-based tanh
+    w = W.make_gqa(name="cap", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                   seq_lens=[5, 2], cache_len=6, seed=21, scale=1.7)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=2,
+                             softcap=softcap)
+    bo, bl = brute_force(w, softcap=softcap)
+    assert np.max(np.abs(out - bo)) < 1e-12 and np.max(np.abs(lse - bl)) < 1e-12
+
+
+def test_softcap_limits():
+    w = _gqa_case(seed=22)
+    o0, l0 = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    # a cap far above every score changes them by O(s^3 / cap^2): nothing at 1e-9
+    o1, l1 = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, softcap=1e6)
+    assert np.max(np.abs(o1 - o0)) < 1e-9 and np.max(np.abs(l1 - l0)) < 1e-9
+    # a tiny cap flattens every score to about +-cap: weights within e^(2 cap) of
+    # each other, so the output is the plain mean of the values within that ratio
+    cap = 1e-6
+    o2, l2 = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, softcap=cap)
+    t = w.tensors
+    for b in range(w.batch):
+        n = int(t["seq_lens"][b])
+        for hq in range(w.num_q_heads):
+            h = hq // w.group
+            mean = t["v"][b, h, :n].double().mean(0).numpy()
+            assert np.max(np.abs(o2[b, hq] - mean)) < 1e-5
+            assert abs(l2[b, hq] - math.log(n)) < 1e-5
 
 
 def test_bad_page_index_is_reported():
