@@ -188,12 +188,17 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def timed_oracle(w, rows, threads):
+def workload_name(cfg, softcap):
+    return W.CONFIG_NAMES[cfg] + (f", tanh soft cap {softcap:g}" if softcap else "")
+
+
+def timed_oracle(w, rows, threads, softcap=0.0):
     """The float64 oracle on a subset of batch rows; returns (seconds, fraction of KV)."""
     import oracle
     t0 = time.perf_counter()
     sub = _subset(w, rows)
-    oracle.decode(oracle.problem_from(sub), sub.tensors, sub.scale, num_threads=threads)
+    oracle.decode(oracle.problem_from(sub), sub.tensors, sub.scale, num_threads=threads,
+                  softcap=softcap)
     dt = time.perf_counter() - t0
     frac = algorithmic_bytes(sub)["kv"] / max(algorithmic_bytes(w)["kv"], 1)
     return dt, frac
@@ -238,11 +243,11 @@ def run_reference(args, w, cfg):
     threads = oracle.default_threads()
     rows = pick_oracle_rows(w, target_s=2.0, threads=threads)
     for _ in range(args.warmup):
-        timed_oracle(w, rows, threads)
+        timed_oracle(w, rows, threads, args.softcap)
     times = []
     frac = 1.0
     for _ in range(args.steps):
-        dt, frac = timed_oracle(w, rows, threads)
+        dt, frac = timed_oracle(w, rows, threads, args.softcap)
         times.append(dt)
     ab = algorithmic_bytes(w)
     mean = statistics.mean(times)
@@ -252,7 +257,7 @@ def run_reference(args, w, cfg):
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": W.CONFIG_NAMES[cfg], "sample_rows": len(rows)},
+        "config": {"workload": workload_name(cfg, args.softcap), "sample_rows": len(rows)},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"batch rows 0..{len(rows) - 1} of {w.batch}, all heads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -275,7 +280,7 @@ def run_ours(args, w, cfg):
     lead = (w.batch, w.num_q_heads) + ((w.q_len,) if w.q_len > 1 else ())
     out = torch.empty(lead + (w.head_dim_v,), dtype=torch.bfloat16, device=dev)
     lse = torch.empty(lead, dtype=torch.float32, device=dev)
-    a = da.make_args(t, w.scale, out, lse)
+    a = da.make_args(t, w.scale, out, lse, softcap=args.softcap)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -325,7 +330,7 @@ def run_ours(args, w, cfg):
         e0.record(stream)
         for k, hv in host_in.items():
             dev_in[k].copy_(hv, non_blocking=True)
-        eng.run(t, w.scale, out=out, lse=lse, stream=stream)
+        eng.run(t, w.scale, out=out, lse=lse, stream=stream, softcap=args.softcap)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         e1.record(stream)
@@ -361,7 +366,7 @@ def run_ours(args, w, cfg):
             "warmup": args.warmup, "ms_per_step": mean_call, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f8e4m3" if w.kv_fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": W.CONFIG_NAMES[cfg], "us_per_call": mean_call * 1e3,
+            "config": {"workload": workload_name(cfg, args.softcap), "us_per_call": mean_call * 1e3,
                        "pct_hbm_peak_kv_q_o": pct_hbm, "hbm_peak_gbs": hbm_peak,
                        "peak_source": peak_kind, "l2": "512 MiB buffer written between steps",
                        "plan": {k: plan[k] for k in ("chunk_tokens", "num_splits", "grid_x",
@@ -395,6 +400,8 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--splits", type=int, default=0, help="num_splits_override (0 = planner)")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="tanh soft cap c of the scaled scores, s -> c tanh(s / c) (0 = off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = W.config(args.config)

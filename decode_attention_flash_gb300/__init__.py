@@ -60,6 +60,7 @@ class Args(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
+        ("softcap", ctypes.c_float),
     ]
 
 
@@ -190,7 +191,7 @@ def decode_attn_plan_info(problem: Problem, num_sms: int, seq_lens_host=None,
     return info.as_dict()
 
 
-def make_args(tensors: dict, scale: float, out, lse=None) -> Args:
+def make_args(tensors: dict, scale: float, out, lse=None, softcap: float = 0.0) -> Args:
     a = Args()
     for k in ("q", "q_pe", "k", "v", "k_scale", "v_scale", "block_table", "seq_lens",
               "kv_num_blks", "kv_idx"):
@@ -202,6 +203,7 @@ def make_args(tensors: dict, scale: float, out, lse=None) -> Args:
     a.v_scale_shift = _ptr(tensors.get("v_scale_shift"))
     a.kv_full_num_blks = _ptr(tensors.get("kv_full_num_blks"))
     a.kv_full_idx = _ptr(tensors.get("kv_full_idx"))
+    a.softcap = float(softcap)
     return a
 
 
@@ -260,7 +262,7 @@ class DecodeAttention:
         self.plan = decode_attn_get_plan(self.ctx)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=self.device)
 
-    def run(self, tensors: dict, scale: float, out=None, lse=None, stream=None):
+    def run(self, tensors: dict, scale: float, out=None, lse=None, stream=None, softcap=0.0):
         p = self.problem
         lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
         if out is None:
@@ -271,7 +273,7 @@ class DecodeAttention:
             raise ValueError(f"out must be bf16 with {lead + (p.head_dim_v,)} elements")
         if lse is not None and (lse.dtype != torch.float32 or lse.numel() != math.prod(lead)):
             raise ValueError(f"lse must be float32 with {lead} elements")
-        decode_attn_run(self.ctx, make_args(tensors, scale, out, lse), self.workspace, stream)
+        decode_attn_run(self.ctx, make_args(tensors, scale, out, lse, softcap), self.workspace, stream)
         return out
 
     def errors(self, stream=None) -> int:

@@ -226,6 +226,9 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.err = reinterpret_cast<uint32_t *>(ws);
   gp.counters = reinterpret_cast<uint32_t *>(ws + pl.counters_offset);
   gp.score_scale = a->scale * 1.4426950408889634f;
+  if (!(a->softcap >= 0.f)) return DA_ERR_INVALID_ARG;  // negative or NaN
+  gp.softcap_l2 = a->softcap * 1.4426950408889634f;
+  gp.softcap_k = a->softcap > 0.f ? 2.f / a->softcap : 0.f;
   gp.batch = p.batch;
   gp.num_q_heads = p.num_q_heads * Q;  // rows of q / out / lse per batch row
   gp.num_kv_heads = p.num_kv_heads;
@@ -252,6 +255,7 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   const da_problem &p = ctx->prob;
   if (!a->q || !a->q_pe || !a->k || !a->v || !a->seq_lens || !a->out || !a->block_table)
     return DA_ERR_INVALID_ARG;
+  if (a->softcap != 0.f) return DA_ERR_UNSUPPORTED;  // no score modification in the MLA kernel
   if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 128) || !aligned(a->q_pe, 128) ||
       !aligned(a->out, 16))
     return DA_ERR_INVALID_ARG;

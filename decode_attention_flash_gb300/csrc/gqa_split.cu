@@ -117,6 +117,14 @@ constexpr int32_t kFirst = 1, kLast = 2;
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
+// Soft cap of a score x in log2 units: c2 * tanh(x / c2), from the identity
+// tanh(u) = 1 - 2 / (exp(2u) + 1) with exp(2u) = exp2(x * k), k = 2 log2(e) / c2.
+// Both ends saturate: exp2 -> inf gives c2, exp2 -> 0 gives -c2. The error is
+// absolute, a few ulp of c2, which is what the softmax weight exp2(x - m) sees.
+__device__ __forceinline__ float cap_tanh(float x, float c2, float k) {
+  return c2 - __fdividef(2.f * c2, ex2(x * k) + 1.f);
+}
+
 __device__ __forceinline__ uint64_t low_bits(int n) {
   return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
 }
@@ -1044,6 +1052,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     float oacc[NT][8][4];
     float m_run[NT][2], l_part[NT][2];
     float sscale = p.score_scale, vmul = 1.f;
+    const bool softcap = p.softcap_l2 > 0.f;
     // e4m3 with per-token scale and shift (value = e4m3 * sc + sh): the score
     // of a key is sc * (q . e4m3) + sh * sum(q), so the MMA runs on the codes
     // and qsum holds sum(q) of the thread's two query rows; a value's scale
@@ -1210,8 +1219,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             // at the row's length, so one query token per row changes nothing)
             const int lim = m.nval - qshift[nt][e];
             const bool ok0 = ok_r && 16 * warp + r8 < lim, ok1 = ok_r8 && 16 * warp + r8 + 8 < lim;
-            const float x0 = ok0 ? sacc[nt][e] * sscale : neg_inf();
-            const float x1 = ok1 ? sacc[nt][2 + e] * sscale : neg_inf();
+            float x0 = sacc[nt][e] * sscale, x1 = sacc[nt][2 + e] * sscale;
+            if (softcap) {  // c * tanh(s / c), in log2 units: c2 * tanh(x / c2)
+              x0 = cap_tanh(x0, p.softcap_l2, p.softcap_k);
+              x1 = cap_tanh(x1, p.softcap_l2, p.softcap_k);
+            }
+            x0 = ok0 ? x0 : neg_inf();
+            x1 = ok1 ? x1 : neg_inf();
             float tmax = fmaxf(x0, x1);
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));

@@ -37,6 +37,8 @@ struct GqaParams {
   uint32_t *err;               // device error word
   uint32_t *counters;          // [units] finished-split counters (self-resetting)
   float score_scale;           // scale * log2(e)
+  float softcap_l2;            // 0, or the soft cap c times log2(e): x -> c2 * tanh(x / c2)
+  float softcap_k;             // 2 / c: exp(2 x / c2) = exp2(x * softcap_k)
   int32_t batch, num_q_heads, num_kv_heads, group;  // num_q_heads, group: rows (heads x q_len)
   int32_t token_scale;         // e4m3 K/V with per-token scale words (maps kss / vss)
   int32_t q_len;               // query tokens per row: token t of a unit row g * q_len + t

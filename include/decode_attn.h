@@ -142,6 +142,8 @@ typedef struct {
  *              after the kv_idx blocks. Pass the two tables' summed counts as the
  *              planner's kv_num_blks_host, or none.
  *   scale      the full softmax scale (e.g. 1/sqrt(128)); applied in fp32
+ *   softcap    GQA: 0, or a tanh soft cap c > 0 on the scaled scores, s -> c * tanh(s / c)
+ *              (the logit soft-capping of the FlashAttention-3 page); MLA: 0 only
  *   out        bf16 [B][HQ][Dv]    (q_len Q > 1: [B][HQ][Q][Dv])
  *   lse        fp32 [B][HQ], natural log; may be NULL (q_len Q > 1: [B][HQ][Q])
  */
@@ -163,6 +165,7 @@ typedef struct {
   const int32_t *v_scale_shift;
   const int32_t *kv_full_num_blks;
   const int32_t *kv_full_idx;
+  float softcap;
 } da_args;
 
 /* What the planner decided (host-side, informational). */

@@ -10,7 +10,8 @@ import oracle
 BF16_ATOL, BF16_RTOL, LSE_ATOL, FP8_TOL = 2e-2, 1e-2, 1e-3, 3e-2
 
 
-def run_gpu(w, num_splits_override=None, with_lse=True, seq_lens_host=True, engine=None):
+def run_gpu(w, num_splits_override=None, with_lse=True, seq_lens_host=True, engine=None,
+            softcap=0.0):
     dev = torch.device("cuda", 0)
     if engine is None:
         nb = w.tensors.get("kv_num_blks") if w.sparse_block_size else None
@@ -23,16 +24,16 @@ def run_gpu(w, num_splits_override=None, with_lse=True, seq_lens_host=True, engi
     lead = (w.batch, w.num_q_heads) + ((w.q_len,) if w.q_len > 1 else ())
     lse = torch.full(lead, 12345.0, dtype=torch.float32, device=dev) if with_lse else None
     out = torch.full(lead + (w.head_dim_v,), 777.0, dtype=torch.bfloat16, device=dev)
-    engine.run(t, w.scale, out=out, lse=lse)
+    engine.run(t, w.scale, out=out, lse=lse, softcap=softcap)
     torch.cuda.synchronize()
     flags = engine.errors()
     return out.cpu(), (lse.cpu() if lse is not None else None), flags, engine
 
 
-def reference(w, rows=None):
+def reference(w, rows=None, softcap=0.0):
     """Oracle output; `rows` (list of batch rows) restricts it to a subset."""
     if rows is None:
-        return oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+        return oracle.decode(oracle.problem_from(w), w.tensors, w.scale, softcap=softcap)
     t = dict(w.tensors)
     idx = torch.tensor(rows, dtype=torch.long)
     t["q"] = t["q"][idx].contiguous()

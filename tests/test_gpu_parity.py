@@ -445,3 +445,54 @@ def test_bad_full_table_index_sets_flag():
     out, lse, flags, _ = run_gpu(w)
     assert flags & da.DA_DEVERR_SPARSE_INDEX
     assert torch.all(torch.isfinite(out.float()))
+
+
+# ------------------------------------------------------------------ tanh soft-capping of the scores
+
+@pytest.mark.parametrize("softcap", [0.7, 5.0])
+@pytest.mark.parametrize("kind", ["paged", "fp8", "fp8token", "spec", "sparse"])
+def test_softcap(kind, softcap):
+    if kind == "paged":
+        w = W.make_gqa(name="cap", batch=4, num_q_heads=16, num_kv_heads=2,
+                       seq_lens=[1000, 17, 1, 300], page_size=16, seed=470)
+    elif kind == "fp8":
+        w = W.make_gqa(name="cap8", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[900, 40],
+                       cache_len=900, kv_fp8=True, seed=471)
+    elif kind == "fp8token":
+        w = W.make_gqa(name="cap8t", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[640, 90],
+                       cache_len=640, kv_fp8=True, kv_token_scale=True, seed=472)
+    elif kind == "spec":
+        w = W.make_gqa(name="capq", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[500, 2, 65],
+                       layout="paged", page_size=16, q_len=3, seed=473)
+    else:
+        w = _sparse(seed=474)
+    fp8 = bool(w.kv_fp8)
+    ref_out, ref_lse = reference(w, softcap=softcap)
+    plain_out, _ = reference(w)
+    # the cap changes the answer: a test that ignored it would fail
+    assert float(np.abs(ref_out - plain_out).max()) > 0.05
+    for S in (0, 3):
+        out, lse, flags, _ = run_gpu(w, num_splits_override=S, softcap=softcap)
+        assert flags == 0
+        assert_parity(out, lse, ref_out, ref_lse, fp8=fp8, what=f"softcap {softcap} {kind} S={S}")
+
+
+def test_softcap_zero_is_bitwise_the_uncapped_path():
+    w = W.make_gqa(name="cap0", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[333, 70],
+                   page_size=16, seed=475)
+    out0, lse0, _, eng = run_gpu(w)
+    out1, lse1, _, _ = run_gpu(w, engine=eng, softcap=0.0)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    eng.close()
+
+
+def test_softcap_rejected_when_negative_and_for_mla():
+    w = W.make_gqa(name="capbad", batch=1, num_q_heads=8, num_kv_heads=2, seq_lens=[64],
+                   cache_len=64, seed=476)
+    with pytest.raises(da.DecodeAttnError):
+        run_gpu(w, softcap=-1.0)
+    with pytest.raises(da.DecodeAttnError):
+        run_gpu(w, softcap=float("nan"))
+    m = W.make_mla(name="mlacap", batch=1, seq_lens=[100], seed=477)
+    with pytest.raises(da.DecodeAttnError):
+        run_gpu(m, softcap=1.0)
