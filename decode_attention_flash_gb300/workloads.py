@@ -39,6 +39,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 SPARE_PAGES = 64
@@ -160,9 +161,11 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
              num_splits=0, poison=True, shape_only=False, q_len=1,
-             kv_token_scale=False) -> Workload:
+             kv_token_scale=False, tree_mask=False) -> Workload:
     """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths;
-    ``q_len`` > 1 gives each row that many query tokens (its last positions).
+    ``q_len`` > 1 gives each row that many query tokens (its last positions);
+    ``tree_mask`` adds a random draft-token tree over them (``spec_mask``).
+
     ``shape_only`` skips drawing the K/V caches (lengths, tables and lists are
     drawn exactly as in the full workload)."""
     g = _gen(seed)
@@ -176,6 +179,8 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
                  kv_fp8=kv_fp8, num_splits=num_splits, q_len=max(1, q_len),
                  kv_token_scale=bool(kv_fp8 and kv_token_scale))
     t = {"q": q, "seq_lens": seq_lens}
+    if tree_mask and q_len > 1:
+        t["spec_mask"] = draft_tree_mask(B, q_len, _gen(seed + 7919))
     if layout == "paged":
         table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
         w.paged, w.page_size, w.num_pages, w.max_pages_per_seq = True, page_size, num_pages, max_pages
@@ -242,6 +247,23 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
         t.update(k=k.to(torch.bfloat16).contiguous(), v=v.to(torch.bfloat16).contiguous())
     w.tensors = t
     return w
+
+
+def draft_tree_mask(batch, q_len, g):
+    """Packed masks of a random tree of ``q_len`` draft tokens per row, as int32
+    words ``[batch][q_len][ceil(q_len / 32)]``: token j hangs under a parent
+    drawn from the earlier tokens (or under the verified prefix), and its row
+    has bit i set for itself and each of its ancestors i."""
+    words = (q_len + 31) // 32
+    bits = np.zeros((batch, q_len, words), dtype=np.uint32)
+    for b in range(batch):
+        parent = [-1] + [int(torch.randint(-1, j, (1,), generator=g)) for j in range(1, q_len)]
+        for j in range(q_len):
+            i = j
+            while i >= 0:
+                bits[b, j, i // 32] |= np.uint32(1) << np.uint32(i % 32)
+                i = parent[i]
+    return torch.from_numpy(bits.view(np.int32)).contiguous()
 
 
 def sparse_lists(batch, num_kv_heads, cache_len, block_size, keep_random, keep_last, g,

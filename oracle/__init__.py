@@ -56,6 +56,7 @@ class OracleInputs(ctypes.Structure):
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
         ("softcap", ctypes.c_double),
+        ("spec_mask", ctypes.c_void_p),
     ]
 
 
@@ -170,7 +171,7 @@ class _Prepared:
         self.problem = p
         self.keep = {k: _bits(v) for k, v in tensors.items()}
         for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift",
-                  "kv_full_num_blks", "kv_full_idx"):
+                  "kv_full_num_blks", "kv_full_idx", "spec_mask"):
             if self.keep.get(k) is not None:
                 self.keep[k] = self.keep[k].to(torch.int32).contiguous()
         for k in ("k_scale", "v_scale"):
@@ -179,7 +180,7 @@ class _Prepared:
         i = OracleInputs()
         for k in ("q", "q_pe", "k", "v", "k_scale", "v_scale", "block_table", "seq_lens",
                   "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift", "kv_full_num_blks",
-                  "kv_full_idx"):
+                  "kv_full_idx", "spec_mask"):
             setattr(i, k, _ptr(self.keep.get(k)))
         i.scale = float(scale)
         i.softcap = float(softcap)

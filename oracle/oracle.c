@@ -25,7 +25,11 @@
  *   positions of P(b,h) with n <= N_b - Q + t (the causal mask of the split-K
  *   decode kernel, `_fwd_kernel_splitK` with IS_CAUSAL: q_pos = kv_len -
  *   num_queries + t, position kept when q_pos - kv_pos >= 0). Rows are then
- *   (b, hq, t) with t fastest.
+ *   (b, hq, t) with t fastest. With a packed tree mask instead (the
+ *   speculative-decoding mask of the TensorRT-LLM XQA kernel page, mha.cu,
+ *   `applyMaskFromInput` under SPEC_DEC): every position before the Q new
+ *   ones is kept, and new position N_b - Q + j is kept for token t when bit
+ *   j % 32 of word j / 32 of mask row (b, t) is set.
  *
  * Sources: the per-split output and log-sum-exp of the split-K Triton decode
  * kernel page (mslk splitk_kernels.py, `_fwd_kernel_splitK`, "write back O"
@@ -194,6 +198,8 @@ typedef struct {
   const int32_t *kv_full_num_blks; /* sparse, optional: [B][HKV] blocks of the full list */
   const int32_t *kv_full_idx;      /* sparse, optional: [B][HKV][max_sparse_blocks] */
   double softcap;                  /* > 0: scores become softcap * tanh(score / softcap) */
+  const uint32_t *spec_mask;       /* Q > 1, optional (else causal): [B][Q][ceil(Q / 32)] words;
+                                      bit j of row (b, t) keeps position N_b - Q + j for token t */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -387,13 +393,25 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
   if (n < 0) return (int)n;
   if (Q > 1) {
     /* Several new query tokens (speculative decoding): they are the row's last
-     * Q positions, and token t sees the positions up to its own,
-     * n <= N_b - Q + t (the causal mask of the split-K decode kernel,
-     * splitk_kernels.py `_fwd_kernel_splitK`, IS_CAUSAL). */
-    const int64_t limit = (int64_t)in->seq_lens[b] - Q + 1 + t;
+     * Q positions. Token t sees every older position and, among the new ones,
+     * those up to its own, n <= N_b - Q + t (the causal mask of the split-K
+     * decode kernel, splitk_kernels.py `_fwd_kernel_splitK`, IS_CAUSAL), or
+     * those its tree-mask row selects (XQA mha.cu, SPEC_DEC). */
+    const int64_t first_new = (int64_t)in->seq_lens[b] - Q;
+    const int64_t words = (Q + 31) / 32;
+    const uint32_t *mrow = in->spec_mask ? in->spec_mask + ((int64_t)b * Q + t) * words : NULL;
     int64_t kept = 0;
-    for (int64_t j = 0; j < n; ++j)
-      if (pos[j] < limit) pos[kept++] = pos[j];
+    for (int64_t j = 0; j < n; ++j) {
+      const int64_t d = pos[j] - first_new; /* index among the new positions, < 0: an old one */
+      int keep;
+      if (d < 0)
+        keep = 1;
+      else if (mrow) /* the tree mask (XQA SPEC_DEC): bit d of the token's mask row */
+        keep = (int)((mrow[d / 32] >> (d % 32)) & 1u);
+      else
+        keep = d <= t; /* causal */
+      if (keep) pos[kept++] = pos[j];
+    }
     n = kept;
   }
   fetch_q(p, in, b, hq, t, qr);

@@ -249,8 +249,14 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
                             if blk * w.sparse_block_size + i < n_b]
         else:
             pos = list(range(n_b))
-        # query token tq of Q is the row's position n_b - Q + tq: it sees n <= that
-        pos = [n for n in pos if n <= n_b - Q + tq]
+        # query token tq of Q is the row's position n_b - Q + tq: it sees n <= that,
+        # or, with a draft-tree mask, the older positions and the new ones its row marks
+        if "spec_mask" in t:
+            words = t["spec_mask"][b, tq].tolist()
+            pos = [n for n in pos if n < n_b - Q or
+                   (words[(n - n_b + Q) // 32] >> ((n - n_b + Q) % 32)) & 1]
+        else:
+            pos = [n for n in pos if n <= n_b - Q + tq]
         keys, vals = [], []
         for n in pos:
             if w.is_mla:
@@ -323,6 +329,13 @@ def _tiny_cases():
     cases.append(W.make_gqa(name="causal_q2_paged", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=4, seq_lens=[5, 3], layout="paged", page_size=2, seed=18,
                             scale=0.6, q_len=2))
+    # a draft-token tree over the new tokens; the second row is shorter than q_len
+    cases.append(W.make_gqa(name="tree_q5", batch=2, num_q_heads=4, num_kv_heads=2,
+                            head_dim=4, seq_lens=[8, 3], cache_len=8, seed=19, scale=0.8,
+                            q_len=5, tree_mask=True))
+    cases.append(W.make_gqa(name="tree_q4_paged", batch=2, num_q_heads=2, num_kv_heads=1,
+                            head_dim=4, seq_lens=[6, 4], layout="paged", page_size=2, seed=20,
+                            scale=0.7, q_len=4, tree_mask=True))
     return cases
 
 
@@ -359,6 +372,55 @@ def test_query_token_t_equals_a_single_token_decode_over_its_prefix():
     # rows shorter than q_len: their first tokens see nothing
     assert np.all(lse[3, :, :Q - 1] == -math.inf) and np.all(out[3, :, :Q - 1] == 0)
     assert np.all(lse[1, :, 0] == -math.inf) and np.all(np.isfinite(lse[1, :, 1:]))
+
+
+def _with_mask(w, rows):
+    """The workload with every row's draft mask set to ``rows`` (one int per token)."""
+    m = torch.tensor(rows, dtype=torch.int64).view(1, -1, 1).expand(w.batch, -1, -1)
+    return dict(w.tensors, spec_mask=m.to(torch.int32).contiguous())
+
+
+def test_tree_mask_lower_triangle_is_the_causal_mask():
+    Q = 5
+    w = W.make_gqa(name="tri", batch=3, num_q_heads=6, num_kv_heads=2, head_dim=16,
+                   seq_lens=[40, 3, 17], layout="paged", page_size=4, seed=42, q_len=Q)
+    causal = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=2)
+    tri = oracle.decode(oracle.problem_from(w), _with_mask(w, [(2 << t) - 1 for t in range(Q)]),
+                        w.scale, num_threads=2)
+    assert np.array_equal(causal[0], tri[0]) and np.array_equal(causal[1], tri[1])
+    # the reversed bit order (the upper triangle) is a different mask
+    up = oracle.decode(oracle.problem_from(w),
+                       _with_mask(w, [((1 << Q) - 1) ^ ((1 << t) - 1) for t in range(Q)]),
+                       w.scale, num_threads=2)
+    assert not np.array_equal(causal[0], up[0])
+
+
+def test_tree_mask_of_all_ones_sees_the_whole_row():
+    Q = 3
+    lens = [33, 2, 9]
+    w = W.make_gqa(name="ones", batch=3, num_q_heads=4, num_kv_heads=1, head_dim=16,
+                   seq_lens=lens, cache_len=33, seed=43, q_len=Q)
+    out, lse = oracle.decode(oracle.problem_from(w), _with_mask(w, [(1 << Q) - 1] * Q),
+                             w.scale, num_threads=2)
+    for t in range(Q):
+        one = dict(w.tensors, q=w.tensors["q"][:, :, t].contiguous())
+        o1, l1 = oracle.decode(dict(oracle.problem_from(w), q_len=1), one, w.scale, num_threads=2)
+        assert np.array_equal(o1, out[:, :, t]) and np.array_equal(l1, lse[:, :, t])
+
+
+def test_tree_mask_each_token_alone_returns_its_value_row():
+    # a row made only of the new tokens, each seeing itself alone: one key each,
+    # so out is that position's value row and lse its score
+    Q = 6
+    w = W.make_gqa(name="self", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=8,
+                   seq_lens=[Q, Q], cache_len=Q, seed=44, scale=0.9, q_len=Q)
+    out, lse = oracle.decode(oracle.problem_from(w), _with_mask(w, [1 << t for t in range(Q)]),
+                             w.scale, num_threads=2)
+    k, v, q = (w.tensors[x].double() for x in ("k", "v", "q"))
+    for b, hq, t in itertools.product(range(2), range(4), range(Q)):
+        h = hq // 2
+        assert np.array_equal(out[b, hq, t], v[b, h, t].numpy())
+        assert abs(lse[b, hq, t] - w.scale * float(q[b, hq, t] @ k[b, h, t])) < 1e-12
 
 
 def _gqa_case(layout="contiguous", seed=21, **kw):
