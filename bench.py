@@ -188,8 +188,13 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def workload_name(cfg, softcap):
-    return W.CONFIG_NAMES[cfg] + (f", tanh soft cap {softcap:g}" if softcap else "")
+def workload_name(cfg, args):
+    name = W.CONFIG_NAMES[cfg]
+    if args.tree_mask:
+        name += ", draft-tree mask"
+    if args.softcap:
+        name += f", tanh soft cap {args.softcap:g}"
+    return name
 
 
 def timed_oracle(w, rows, threads, softcap=0.0):
@@ -208,10 +213,13 @@ def _subset(w, rows):
     import copy
     t = dict(w.tensors)
     idx = torch.tensor(rows, dtype=torch.long)
-    for k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx"):
+    for k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx", "spec_mask"):
         if k in t:
             t[k] = t[k][idx].contiguous()
     if not w.paged:
+        for k in ("k_scale_shift", "v_scale_shift"):
+            if k in t:
+                t[k] = t[k][idx].contiguous()
         # row selection through a byte view: CPU indexing of float8 tensors is
         # missing in some PyTorch releases
         for k in ("k", "v"):
@@ -257,7 +265,7 @@ def run_reference(args, w, cfg):
         "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(cfg, args.softcap), "sample_rows": len(rows)},
+        "config": {"workload": workload_name(cfg, args), "sample_rows": len(rows)},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"batch rows 0..{len(rows) - 1} of {w.batch}, all heads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -317,7 +325,8 @@ def run_ours(args, w, cfg):
 
     # ---------------- end to end through the public API with host buffers
     host_in = {k: v.pin_memory() for k, v in w.tensors.items()
-               if k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx")}
+               if k in ("q", "q_pe", "seq_lens", "block_table", "kv_num_blks", "kv_idx",
+                        "spec_mask")}
     dev_in = {k: t[k] for k in host_in}
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -366,7 +375,7 @@ def run_ours(args, w, cfg):
             "warmup": args.warmup, "ms_per_step": mean_call, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f8e4m3" if w.kv_fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": workload_name(cfg, args.softcap), "us_per_call": mean_call * 1e3,
+            "config": {"workload": workload_name(cfg, args), "us_per_call": mean_call * 1e3,
                        "pct_hbm_peak_kv_q_o": pct_hbm, "hbm_peak_gbs": hbm_peak,
                        "peak_source": peak_kind, "l2": "512 MiB buffer written between steps",
                        "plan": {k: plan[k] for k in ("chunk_tokens", "num_splits", "grid_x",
@@ -400,11 +409,18 @@ def main():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--splits", type=int, default=0, help="num_splits_override (0 = planner)")
+    ap.add_argument("--tree-mask", action="store_true",
+                    help="several-token configs: a random draft-token tree instead of the causal mask")
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="tanh soft cap c of the scaled scores, s -> c tanh(s / c) (0 = off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = W.config(args.config)
+    if args.tree_mask:
+        if w.q_len < 2:
+            raise SystemExit("--tree-mask needs a configuration with several query tokens")
+        w.tensors["spec_mask"] = W.draft_tree_mask(w.batch, w.q_len,
+                                                   torch.Generator().manual_seed(1234))
     if args.impl == "reference":
         run_reference(args, w, args.config)
     else:

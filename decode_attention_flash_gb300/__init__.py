@@ -60,7 +60,7 @@ class Args(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
-        ("softcap", ctypes.c_float),
+        ("softcap", ctypes.c_float), ("spec_mask", ctypes.c_void_p),
     ]
 
 
@@ -204,6 +204,7 @@ def make_args(tensors: dict, scale: float, out, lse=None, softcap: float = 0.0) 
     a.kv_full_num_blks = _ptr(tensors.get("kv_full_num_blks"))
     a.kv_full_idx = _ptr(tensors.get("kv_full_idx"))
     a.softcap = float(softcap)
+    a.spec_mask = _ptr(tensors.get("spec_mask"))
     return a
 
 

@@ -217,6 +217,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.kv_idx = a->kv_idx;
   gp.kv_full_num_blks = a->kv_full_num_blks;
   gp.kv_full_idx = a->kv_full_idx;
+  gp.spec_mask = Q > 1 ? a->spec_mask : nullptr;
   gp.k_scale = a->k_scale;
   gp.v_scale = a->v_scale;
   gp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);

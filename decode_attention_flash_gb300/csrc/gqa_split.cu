@@ -1062,14 +1062,19 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     const int32_t *ssw = reinterpret_cast<const int32_t *>(smem + C::oSS);
     const int ss_rows = (p.paged && p.page_size < kTile) ? p.page_size : kTile;  // rows per box
     float qsum[NT][2], zacc[NT][2];
-    // Query row g * q_len + t (several query tokens per row) sees the positions
-    // n < seq_len - (q_len - 1 - t): its own position among the row's last
-    // q_len tokens and the ones before it. qshift = q_len - 1 - t per held row.
-    int qshift[NT][2];
+    // Query row g * q_len + t (several query tokens per row): the row's last
+    // q_len positions are its new tokens, new token j at seq_len - q_len + j.
+    // Token t sees every older position and the new tokens set in its mask
+    // word: bits 0..t (causal) unless a draft-tree mask gives the word.
+    int trow[NT][2];
+    uint32_t mword[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) qshift[nt][e] = p.q_len - 1 - (nt * 8 + 2 * q4 + e) % p.q_len;
+      for (int e = 0; e < 2; ++e) {
+        trow[nt][e] = (nt * 8 + 2 * q4 + e) % p.q_len;
+        mword[nt][e] = (2u << trow[nt][e]) - 1u;
+      }
     auto reset = [&]() {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -1145,6 +1150,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           sscale = p.score_scale * p.k_scale[h];
           vmul = p.v_scale[h];
         }
+        if (p.spec_mask != nullptr) {
+          const uint32_t *mrow = p.spec_mask + (size_t)(unit / p.num_kv_heads) * p.q_len;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) mword[nt][e] = mrow[trow[nt][e]];
+        }
       }
       const uint32_t vbits = (uint32_t)(m.valid >> (16 * warp)) & 0xFFFFu;
       if (vbits != 0) {
@@ -1209,16 +1221,18 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           vsh0 = ok_r ? __half2float(__ushort_as_half((unsigned short)(v0 >> 16))) : 0.f;
           vsh1 = ok_r8 ? __half2float(__ushort_as_half((unsigned short)(v1 >> 16))) : 0.f;
         }
+        // new-token index of this thread's first token (negative: an older position)
+        const int jnew = 16 * warp + r8 - (m.nval - p.q_len);
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float alpha[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            // causal limit of the query row (the tile's valid bits already stop
-            // at the row's length, so one query token per row changes nothing)
-            const int lim = m.nval - qshift[nt][e];
-            const bool ok0 = ok_r && 16 * warp + r8 < lim, ok1 = ok_r8 && 16 * warp + r8 + 8 < lim;
+            // the query token's mask over the new tokens (the tile's valid bits
+            // already stop at the row's length; one query token keeps all)
+            const bool ok0 = ok_r && (jnew < 0 || ((mword[nt][e] >> min(jnew, 31)) & 1u));
+            const bool ok1 = ok_r8 && (jnew + 8 < 0 || ((mword[nt][e] >> min(jnew + 8, 31)) & 1u));
             float x0 = sacc[nt][e] * sscale, x1 = sacc[nt][2 + e] * sscale;
             if (softcap) {  // c * tanh(s / c), in log2 units: c2 * tanh(x / c2)
               x0 = cap_tanh(x0, p.softcap_l2, p.softcap_k);

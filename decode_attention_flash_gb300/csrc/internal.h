@@ -28,6 +28,7 @@ struct GqaParams {
   const int32_t *kv_idx;       // sparse: [B][HKV][max_sparse_blocks]
   const int32_t *kv_full_num_blks;  // sparse, optional: the full-block table, [B][HKV]
   const int32_t *kv_full_idx;       // and [B][HKV][max_sparse_blocks] (attended after kv_idx)
+  const uint32_t *spec_mask;   // q_len > 1, optional: [B][q_len] draft-tree mask words
   const float *k_scale;        // fp8: [HKV]
   const float *v_scale;        // fp8: [HKV]
   float *o_part;               // [units + ctas][G][128] partial slots (slot = unit + cta)

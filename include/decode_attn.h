@@ -144,6 +144,11 @@ typedef struct {
  *   scale      the full softmax scale (e.g. 1/sqrt(128)); applied in fp32
  *   softcap    GQA: 0, or a tanh soft cap c > 0 on the scaled scores, s -> c * tanh(s / c)
  *              (the logit soft-capping of the FlashAttention-3 page); MLA: 0 only
+ *   spec_mask  q_len Q > 1, optional: uint32 [B][Q], the draft-token tree mask of
+ *              speculative decoding (the packed mask rows of the TensorRT-LLM XQA
+ *              kernel, SPEC_DEC, for Q <= 32): every position before the row's Q new
+ *              ones is attended, and new position N_b - Q + j by query token t when
+ *              bit j of word [b][t] is set. NULL: causal (bits 0..t). Ignored for Q = 1
  *   out        bf16 [B][HQ][Dv]    (q_len Q > 1: [B][HQ][Q][Dv])
  *   lse        fp32 [B][HQ], natural log; may be NULL (q_len Q > 1: [B][HQ][Q])
  */
@@ -166,6 +171,7 @@ typedef struct {
   const int32_t *kv_full_num_blks;
   const int32_t *kv_full_idx;
   float softcap;
+  const uint32_t *spec_mask;
 } da_args;
 
 /* What the planner decided (host-side, informational). */

@@ -496,3 +496,47 @@ def test_softcap_rejected_when_negative_and_for_mla():
     m = W.make_mla(name="mlacap", batch=1, seq_lens=[100], seed=477)
     with pytest.raises(da.DecodeAttnError):
         run_gpu(m, softcap=1.0)
+
+
+# ------------------------------------------------------------------ draft-tree masks (speculative decoding)
+
+@pytest.mark.parametrize("q_len,group,layout", [(4, 4, "paged"), (5, 3, "contiguous"),
+                                                (16, 1, "paged"), (8, 2, "contiguous")])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_tree_mask(q_len, group, layout, splits):
+    lens = [1, 3, 17, 64, 65, 700, 0, 333]
+    w = W.make_gqa(name="tree", batch=8, num_q_heads=2 * group, num_kv_heads=2, seq_lens=lens,
+                   layout=layout, page_size=16, q_len=q_len, tree_mask=True,
+                   seed=480 + 10 * q_len + group)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"tree q_len={q_len} G={group} {layout} S={splits}")
+
+
+def test_tree_mask_fp8_and_per_token_fp8():
+    for tok in (False, True):
+        w = W.make_gqa(name="tree8", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[900, 3, 130],
+                       cache_len=900, kv_fp8=True, kv_token_scale=tok, q_len=4, tree_mask=True,
+                       seed=490 + tok)
+        for S in (0, 2):
+            out, lse, flags, _ = run_gpu(w, num_splits_override=S)
+            assert flags == 0
+            ref_out, ref_lse = reference(w)
+            assert_parity(out, lse, ref_out, ref_lse, fp8=True, what=f"tree fp8 tok={tok} S={S}")
+
+
+def test_tree_mask_lower_triangle_is_bitwise_causal():
+    Q = 6
+    w = W.make_gqa(name="tri", batch=4, num_q_heads=12, num_kv_heads=6, seq_lens=[5, 600, 64, 97],
+                   page_size=16, q_len=Q, seed=495)
+    out0, lse0, _, eng = run_gpu(w)
+    tri = torch.tensor([(2 << t) - 1 for t in range(Q)], dtype=torch.int32).repeat(4, 1)
+    w.tensors = dict(w.tensors, spec_mask=tri.contiguous())
+    out1, lse1, flags, _ = run_gpu(w, engine=eng)
+    assert flags == 0 and torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    # and a different tree changes the answer
+    w.tensors["spec_mask"] = W.draft_tree_mask(4, Q, W._gen(5))
+    out2, _, _, _ = run_gpu(w, engine=eng)
+    assert not torch.equal(out0, out2)
+    eng.close()
