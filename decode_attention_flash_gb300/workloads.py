@@ -68,6 +68,8 @@ class Workload:
     max_sparse_blocks: int = 0
     num_splits: int = 0  # 0: planner decides
     q_len: int = 1       # query tokens per row
+    sparse_batch: int = 0  # block mask extents (batch, kv heads), broadcast by
+    sparse_heads: int = 0  # modulo; 0 = the problem's
     kv_token_scale: bool = False  # fp8 KV with a per-token fp16 scale and shift
     tensors: dict = field(default_factory=dict)
 
@@ -161,10 +163,12 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
              num_splits=0, poison=True, shape_only=False, q_len=1,
-             kv_token_scale=False, tree_mask=False) -> Workload:
+             kv_token_scale=False, tree_mask=False, sparse_shape=None) -> Workload:
     """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths;
     ``q_len`` > 1 gives each row that many query tokens (its last positions);
     ``tree_mask`` adds a random draft-token tree over them (``spec_mask``).
+    ``sparse_shape`` = (SZ, SH): the block tables' batch and head extents when
+    the mask is broadcast (row b, kv head h read table (b % SZ, h % SH)).
 
     ``shape_only`` skips drawing the K/V caches (lengths, tables and lists are
     drawn exactly as in the full workload)."""
@@ -200,8 +204,11 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
         if shape_only:
             if sparse_block_size:
                 w.sparse_block_size = sparse_block_size
-                t["kv_num_blks"] = torch.as_tensor(kv_num_blks, dtype=torch.int32).reshape(B, HKV)
-                t["kv_idx"] = torch.as_tensor(kv_idx, dtype=torch.int32).reshape(B, HKV, -1)
+                SZ, SH = sparse_shape if sparse_shape else (B, HKV)
+                if sparse_shape:
+                    w.sparse_batch, w.sparse_heads = SZ, SH
+                t["kv_num_blks"] = torch.as_tensor(kv_num_blks, dtype=torch.int32).reshape(SZ, SH)
+                t["kv_idx"] = torch.as_tensor(kv_idx, dtype=torch.int32).reshape(SZ, SH, -1)
                 w.max_sparse_blocks = t["kv_idx"].shape[-1]
             w.tensors = t
             return w
@@ -215,8 +222,11 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
                 v[b, :, n:] = float("nan")
     if sparse_block_size:
         assert layout != "paged", "block-sparse decode reads a contiguous cache"
-        kv_num_blks = torch.as_tensor(kv_num_blks, dtype=torch.int32).reshape(B, HKV)
-        kv_idx = torch.as_tensor(kv_idx, dtype=torch.int32).reshape(B, HKV, -1)
+        SZ, SH = sparse_shape if sparse_shape else (B, HKV)
+        if sparse_shape:
+            w.sparse_batch, w.sparse_heads = SZ, SH
+        kv_num_blks = torch.as_tensor(kv_num_blks, dtype=torch.int32).reshape(SZ, SH)
+        kv_idx = torch.as_tensor(kv_idx, dtype=torch.int32).reshape(SZ, SH, -1)
         w.sparse_block_size, w.max_sparse_blocks = sparse_block_size, kv_idx.shape[-1]
         t["kv_num_blks"], t["kv_idx"] = kv_num_blks.contiguous(), kv_idx.contiguous()
         if poison:
@@ -224,7 +234,8 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
             for b in range(B):
                 for h in range(HKV):
                     keep = torch.zeros(nblocks, dtype=torch.bool)
-                    keep[kv_idx[b, h, :int(kv_num_blks[b, h])].long()] = True
+                    zb, zh = b % SZ, h % SH
+                    keep[kv_idx[zb, zh, :int(kv_num_blks[zb, zh])].long()] = True
                     mask = keep.repeat_interleave(sparse_block_size)[:w.cache_len]
                     mask &= torch.arange(w.cache_len) < int(seq_lens[b])
                     k[b, h, ~mask] = float("nan")

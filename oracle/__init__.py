@@ -44,7 +44,8 @@ class OracleProblem(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "is_mla",
         "ckv_dim", "kpe_dim", "paged", "page_size", "cache_len", "max_pages_per_seq",
-        "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks", "q_len")]
+        "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks", "q_len",
+        "sparse_batch", "sparse_heads")]
 
 
 class OracleInputs(ctypes.Structure):
@@ -197,7 +198,8 @@ def problem_from(work) -> dict:
         cache_len=w.cache_len, max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
         kv_fp8=(2 if getattr(w, "kv_token_scale", False) else 1) if w.kv_fp8 else 0,
         sparse_block_size=w.sparse_block_size,
-        max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1))
+        max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1),
+        sparse_batch=getattr(w, "sparse_batch", 0), sparse_heads=getattr(w, "sparse_heads", 0))
 
 
 def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = None,

@@ -177,6 +177,8 @@ typedef struct {
   int32_t sparse_block_size; /* 0: dense */
   int32_t max_sparse_blocks;
   int32_t q_len;          /* query tokens per row (0 or 1: one) */
+  int32_t sparse_batch;   /* sparse: extents of the tables' batch and head axes, */
+  int32_t sparse_heads;   /* 0 = B and HKV; row (b, h) reads table (b % SZ, h % SH) */
 } oracle_problem;
 
 typedef struct {
@@ -189,14 +191,14 @@ typedef struct {
   const float *v_scale;   /* fp8: [HKV] */
   const int32_t *block_table; /* paged: [B][max_pages_per_seq] */
   const int32_t *seq_lens;    /* [B] */
-  const int32_t *kv_num_blks; /* sparse: [B][HKV] */
-  const int32_t *kv_idx;      /* sparse: [B][HKV][max_sparse_blocks] */
+  const int32_t *kv_num_blks; /* sparse: [SZ][SH] (SZ, SH = sparse_batch, sparse_heads) */
+  const int32_t *kv_idx;      /* sparse: [SZ][SH][max_sparse_blocks] */
   double scale;
   const int32_t *k_scale_shift; /* kv_fp8 == 2: one word per cache row of k: fp16 scale in
                                    the low half, fp16 shift in the high half */
   const int32_t *v_scale_shift; /* the same for v */
-  const int32_t *kv_full_num_blks; /* sparse, optional: [B][HKV] blocks of the full list */
-  const int32_t *kv_full_idx;      /* sparse, optional: [B][HKV][max_sparse_blocks] */
+  const int32_t *kv_full_num_blks; /* sparse, optional: [SZ][SH] blocks of the full list */
+  const int32_t *kv_full_idx;      /* sparse, optional: [SZ][SH][max_sparse_blocks] */
   double softcap;                  /* > 0: scores become softcap * tanh(score / softcap) */
   const uint32_t *spec_mask;       /* Q > 1, optional (else causal): [B][Q][ceil(Q / 32)] words;
                                       bit j of row (b, t) keeps position N_b - Q + j for token t */
@@ -235,9 +237,15 @@ static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b
     return count;
   }
   int64_t sbs = p->sparse_block_size;
-  int32_t nblk = in->kv_num_blks[(int64_t)b * p->num_kv_heads + h];
+  /* the block mask may have fewer batch rows or heads than the problem and is
+   * then broadcast: flex_decode.py.jinja reads the tables at (off_z % SPARSE_Z,
+   * off_hkv % SPARSE_HQ), the extents of KV_NUM_BLKS' first two axes */
+  const int64_t sz = p->sparse_batch > 0 ? p->sparse_batch : p->batch;
+  const int64_t sh = p->sparse_heads > 0 ? p->sparse_heads : p->num_kv_heads;
+  const int64_t trow = (b % sz) * sh + h % sh;
+  int32_t nblk = in->kv_num_blks[trow];
   if (nblk < 0 || nblk > p->max_sparse_blocks) return ORACLE_BAD_INDEX;
-  const int32_t *list = in->kv_idx + ((int64_t)b * p->num_kv_heads + h) * p->max_sparse_blocks;
+  const int32_t *list = in->kv_idx + trow * p->max_sparse_blocks;
   for (int32_t j = 0; j < nblk; ++j) {
     int64_t blk = list[j];
     if (blk < 0 || blk * sbs >= capacity) return ORACLE_BAD_INDEX;
@@ -250,9 +258,9 @@ static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b
    * blocks that need no mask_mod; with no mask_mod in this definition they
    * are attended exactly like the first table's blocks, after them */
   if (in->kv_full_num_blks) {
-    int32_t nfull = in->kv_full_num_blks[(int64_t)b * p->num_kv_heads + h];
+    int32_t nfull = in->kv_full_num_blks[trow];
     if (nfull < 0 || nfull > p->max_sparse_blocks) return ORACLE_BAD_INDEX;
-    const int32_t *full = in->kv_full_idx + ((int64_t)b * p->num_kv_heads + h) * p->max_sparse_blocks;
+    const int32_t *full = in->kv_full_idx + trow * p->max_sparse_blocks;
     for (int32_t j = 0; j < nfull; ++j) {
       int64_t blk = full[j];
       if (blk < 0 || blk * sbs >= capacity) return ORACLE_BAD_INDEX;
@@ -341,7 +349,8 @@ static void fetch_q(const oracle_problem *p, const oracle_inputs *in, int b, int
 
 static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   if (!p || !in || !in->q || !in->k || !in->v || !in->seq_lens) return ORACLE_BAD_ARG;
-  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->q_len < 0)
+  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->q_len < 0 ||
+      p->sparse_batch < 0 || p->sparse_heads < 0)
     return ORACLE_BAD_ARG;
   if (p->num_q_heads % p->num_kv_heads) return ORACLE_BAD_ARG;
   if (p->is_mla) {

@@ -242,9 +242,10 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
             lists = [(t["kv_num_blks"], t["kv_idx"])]
             if "kv_full_num_blks" in t:
                 lists.append((t["kv_full_num_blks"], t["kv_full_idx"]))
+            zb, zh = b % (w.sparse_batch or B), h % (w.sparse_heads or HKV)
             for nums, idx in lists:
-                for j in range(int(nums[b, h])):
-                    blk = int(idx[b, h, j])
+                for j in range(int(nums[zb, zh])):
+                    blk = int(idx[zb, zh, j])
                     pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
                             if blk * w.sparse_block_size + i < n_b]
         else:
@@ -329,6 +330,16 @@ def _tiny_cases():
     cases.append(W.make_gqa(name="causal_q2_paged", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=4, seq_lens=[5, 3], layout="paged", page_size=2, seed=18,
                             scale=0.6, q_len=2))
+    # one block table broadcast over every row and kv head, and one per kv head
+    # broadcast over the rows (flex's SPARSE_Z / SPARSE_HQ extents)
+    cases.append(W.make_gqa(name="sparse_bcast_1x1", batch=3, num_q_heads=4, num_kv_heads=2,
+                            head_dim=4, seq_lens=[7, 3, 8], cache_len=8, sparse_block_size=2,
+                            kv_num_blks=[2], kv_idx=[[3, 1, 0]], sparse_shape=(1, 1), seed=21,
+                            scale=0.8))
+    cases.append(W.make_gqa(name="sparse_bcast_1xH", batch=2, num_q_heads=4, num_kv_heads=2,
+                            head_dim=4, seq_lens=[8, 5], cache_len=8, sparse_block_size=2,
+                            kv_num_blks=[1, 3], kv_idx=[[2, 0, 0], [0, 2, 3]], sparse_shape=(1, 2),
+                            seed=22, scale=0.7))
     # a draft-token tree over the new tokens; the second row is shorter than q_len
     cases.append(W.make_gqa(name="tree_q5", batch=2, num_q_heads=4, num_kv_heads=2,
                             head_dim=4, seq_lens=[8, 3], cache_len=8, seed=19, scale=0.8,
@@ -378,6 +389,30 @@ def _with_mask(w, rows):
     """The workload with every row's draft mask set to ``rows`` (one int per token)."""
     m = torch.tensor(rows, dtype=torch.int64).view(1, -1, 1).expand(w.batch, -1, -1)
     return dict(w.tensors, spec_mask=m.to(torch.int32).contiguous())
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 2), (3, 1), (2, 2)])
+def test_broadcast_block_mask_equals_the_expanded_tables(shape):
+    # tables of extents (SZ, SH) read at (b % SZ, h % SH): the same result as
+    # tables written out for every (b, kv head)
+    SZ, SH = shape
+    B, HKV, L, blk = 6, 4, 256, 32
+    g = torch.Generator().manual_seed(50 + SZ * 10 + SH)
+    nb = torch.randint(0, 5, (SZ, SH), generator=g, dtype=torch.int32)
+    idx = torch.stack([torch.stack([torch.randperm(L // blk, generator=g)[:5] for _ in range(SH)])
+                       for _ in range(SZ)]).to(torch.int32)
+    lens = [256, 200, 31, 0, 129, 64]
+    w = W.make_gqa(name="bc", batch=B, num_q_heads=8, num_kv_heads=HKV, head_dim=16, seq_lens=lens,
+                   cache_len=L, sparse_block_size=blk, kv_num_blks=nb, kv_idx=idx,
+                   sparse_shape=shape, seed=51, poison=False)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=2)
+    rows = torch.arange(B) % SZ
+    heads = torch.arange(HKV) % SH
+    full = dict(w.tensors, kv_num_blks=nb[rows][:, heads].contiguous(),
+                kv_idx=idx[rows][:, heads].contiguous())
+    prob = dict(oracle.problem_from(w), sparse_batch=0, sparse_heads=0)
+    o2, l2 = oracle.decode(prob, full, w.scale, num_threads=2)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2)
 
 
 def test_tree_mask_lower_triangle_is_the_causal_mask():
