@@ -47,7 +47,8 @@ class Problem(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
         ("sparse_block_size", ctypes.c_int32), ("max_sparse_blocks", ctypes.c_int32),
-        ("q_len", ctypes.c_int32),
+        ("q_len", ctypes.c_int32), ("sparse_batch", ctypes.c_int32),
+        ("sparse_heads", ctypes.c_int32),
     ]
 
 
@@ -305,4 +306,5 @@ def problem_kwargs(work) -> dict:
                 kv_dtype=(DA_DTYPE_FP8_E4M3_TOKEN_SCALE if getattr(w, "kv_token_scale", False)
                           else DA_DTYPE_FP8_E4M3) if w.kv_fp8 else DA_DTYPE_BF16,
                 sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks,
-                q_len=getattr(w, "q_len", 1))
+                q_len=getattr(w, "q_len", 1), sparse_batch=getattr(w, "sparse_batch", 0),
+                sparse_heads=getattr(w, "sparse_heads", 0))

@@ -3,6 +3,7 @@
 // here; every device buffer is the caller's.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -244,6 +245,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.capacity = paged ? p.max_pages_per_seq * p.page_size : p.max_seq_len;
   gp.sparse_block_size = p.sparse_block_size;
   gp.max_sparse_blocks = p.max_sparse_blocks;
+  gp.sparse_batch = p.sparse_batch > 0 ? p.sparse_batch : std::max(p.batch, 1);
+  gp.sparse_heads = p.sparse_heads > 0 ? p.sparse_heads : p.num_kv_heads;
   if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,
                      token_scale ? ctx->kssmap : ctx->kmap, token_scale ? ctx->vssmap : ctx->vmap,
                      gp, pl.grid_x, stream) !=

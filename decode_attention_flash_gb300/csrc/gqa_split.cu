@@ -133,7 +133,8 @@ __device__ __forceinline__ uint64_t low_bits(int n) {
 
 struct UnitInfo {
   int b, h, n_valid, tiles;
-  int nbp;  // sparse: blocks of the first table (the full table's follow them)
+  int nbp;   // sparse: blocks of the first table (the full table's follow them)
+  int trow;  // sparse: the block tables' row, (b % SZ) * SH + h % SH
 };
 
 // Length (checked against the cache) and tile count of unit u.
@@ -147,13 +148,16 @@ __device__ __forceinline__ UnitInfo unit_info(const GqaParams &p, int u, uint32_
     n = n < 0 ? 0 : p.capacity;
   }
   x.n_valid = n;
+  x.trow = 0;
   if (p.sparse_block_size > 0) {
-    int nb = p.kv_num_blks[u];
+    // block masks broadcast over rows and heads (flex's SPARSE_Z / SPARSE_HQ)
+    x.trow = (x.b % p.sparse_batch) * p.sparse_heads + x.h % p.sparse_heads;
+    int nb = p.kv_num_blks[x.trow];
     if (nb < 0 || nb > p.max_sparse_blocks) {
       err |= DA_DEVERR_SPARSE_INDEX;
       nb = nb < 0 ? 0 : p.max_sparse_blocks;
     }
-    int nf = p.kv_full_num_blks ? p.kv_full_num_blks[u] : 0;  // the flex FULL_KV table
+    int nf = p.kv_full_num_blks ? p.kv_full_num_blks[x.trow] : 0;  // the flex FULL_KV table
     if (nf < 0 || nf > p.max_sparse_blocks) {
       err |= DA_DEVERR_SPARSE_INDEX;
       nf = nf < 0 ? 0 : p.max_sparse_blocks;
@@ -196,6 +200,7 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *scratch, int *to
 
 struct TileDesc {
   int unit, b, h, n_valid, j, tiles, nbp;  // unit, its row / head, length, tile index, tile count
+  int trow;                                // sparse: the block tables' row
   int64_t P;                          // global index of the unit's first tile
   int c_first, n_seg;                 // CTAs holding the unit's segments
   int wi;                             // position in this CTA's processing order
@@ -809,6 +814,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.n_valid = x.n_valid;
       d.tiles = x.tiles;
       d.nbp = x.nbp;
+      d.trow = x.trow;
       d.j = j;
       d.P = P0;
       d.c_first = cta_of(d.P, T, CTAS);
@@ -830,8 +836,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       if (p.sparse_block_size > 0) {
         const int e = d.j / (p.sparse_block_size / kTile);
         // list entry e: the first table's, then the full table's
-        const int blk = e < d.nbp ? p.kv_idx[(int64_t)d.unit * p.max_sparse_blocks + e]
-                                  : p.kv_full_idx[(int64_t)d.unit * p.max_sparse_blocks + e - d.nbp];
+        const int blk = e < d.nbp ? p.kv_idx[(int64_t)d.trow * p.max_sparse_blocks + e]
+                                  : p.kv_full_idx[(int64_t)d.trow * p.max_sparse_blocks + e - d.nbp];
         const bool bad = blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len;
         dev_err |= bad ? DA_DEVERR_SPARSE_INDEX : 0u;
         return bad ? -1 : blk;
@@ -862,6 +868,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.n_valid = x.n_valid;
       d.tiles = x.tiles;
       d.nbp = x.nbp;
+      d.trow = x.trow;
       d.j = 0;
       d.c_first = cta_of(d.P, T, CTAS);
       d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;

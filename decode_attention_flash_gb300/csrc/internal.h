@@ -47,6 +47,7 @@ struct GqaParams {
   int32_t paged, page_size, cache_len, max_pages, num_pages;
   int32_t capacity;            // max positions per row
   int32_t sparse_block_size, max_sparse_blocks;
+  int32_t sparse_batch, sparse_heads;  // block tables' extents (row (b % SZ, h % SH))
 };
 
 // Group counters per GQA unit for the two-level merge of a unit cut into many

@@ -62,6 +62,7 @@ da_status validate_problem(const da_problem *p) {
     if (P % 16 != 0 || !(kGqaTile % P == 0 || P % kGqaTile == 0)) return DA_ERR_UNSUPPORTED;
   }
   if (p->sparse_block_size < 0 || p->max_sparse_blocks < 0) return DA_ERR_INVALID_ARG;
+  if (p->sparse_batch < 0 || p->sparse_heads < 0) return DA_ERR_INVALID_ARG;
   // per-token scale words are fetched by TMA in rows of four: cache rows per
   // (b, kv head) a multiple of 4
   if (p->kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE && p->kv_layout == DA_KV_CONTIGUOUS &&
@@ -121,9 +122,12 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
     for (int h = 0; h < heads; ++h) {
       int64_t len;
       if (sparse) {
+        // the tables' row for (b, h): broadcast over rows / heads by modulo
+        const int64_t sz = p->sparse_batch > 0 ? p->sparse_batch : p->batch;
+        const int64_t sh = p->sparse_heads > 0 ? p->sparse_heads : heads;
         int64_t nblk = p->max_sparse_blocks;
         if (kv_num_blks_host)
-          nblk = std::min<int64_t>(std::max<int32_t>(kv_num_blks_host[(int64_t)b * heads + h], 0),
+          nblk = std::min<int64_t>(std::max<int32_t>(kv_num_blks_host[(b % sz) * sh + h % sh], 0),
                                    p->max_sparse_blocks);
         len = nblk * p->sparse_block_size;
       } else {

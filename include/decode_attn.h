@@ -97,7 +97,10 @@ enum {
  *        (MLA: 64); max_pages_per_seq table columns; num_pages pool size.
  *   Contiguous: max_seq_len is the cache length L of [B][HKV][L][D].
  *   Sparse (GQA, contiguous only): sparse_block_size a multiple of 64,
- *        max_sparse_blocks columns of kv_idx; 0 = dense.
+ *        max_sparse_blocks columns of kv_idx; 0 = dense. sparse_batch and
+ *        sparse_heads (SZ, SH; 0 = B and HKV) are the block tables' first two
+ *        extents: row b and kv head h read table row (b % SZ, h % SH), the
+ *        broadcast of the flex decode template (SPARSE_Z, SPARSE_HQ).
  *   q_len: query tokens per row, 0 or 1 = one. Q > 1 needs GQA, a dense
  *        cache and G * Q <= 16 (the G*Q rows of a kv head share one pass).
  */
@@ -115,6 +118,8 @@ typedef struct {
   int32_t sparse_block_size;
   int32_t max_sparse_blocks;
   int32_t q_len;              /* query tokens per row; 0 or 1 = one */
+  int32_t sparse_batch;       /* sparse: block tables' batch extent SZ (0 = batch) */
+  int32_t sparse_heads;       /* sparse: block tables' head extent SH (0 = num_kv_heads) */
 } da_problem;
 
 /*
@@ -135,7 +140,8 @@ typedef struct {
  *   block_table paged: int32 [B][max_pages_per_seq]; entries past a row's
  *              last page are never read
  *   seq_lens   int32 [B]
- *   kv_num_blks, kv_idx  sparse only: int32 [B][HKV] and [B][HKV][max_sparse_blocks]
+ *   kv_num_blks, kv_idx  sparse only: int32 [SZ][SH] and [SZ][SH][max_sparse_blocks]
+ *              (SZ, SH = sparse_batch, sparse_heads, default B and HKV)
  *   kv_full_num_blks, kv_full_idx  sparse only, optional (both NULL or both set): the
  *              second table pair of the flex block mask (FULL_KV_NUM_BLKS / FULL_KV_IDX,
  *              blocks that need no mask_mod), same shapes; their blocks are attended

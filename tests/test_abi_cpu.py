@@ -243,3 +243,15 @@ def test_several_query_tokens_per_row(lib):
     with pytest.raises(da.DecodeAttnError) as e:
         da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=2)), 152)
     assert e.value.status == da.DA_ERR_UNSUPPORTED
+
+
+def test_broadcast_block_mask_extents_are_validated(lib):
+    """sparse_batch / sparse_heads: 0 (the problem's own) or a positive extent."""
+    base = dict(batch=4, num_q_heads=8, num_kv_heads=2, head_dim_qk=128, head_dim_v=128,
+                max_seq_len=256, sparse_block_size=64, max_sparse_blocks=4)
+    for sb, sh in ((0, 0), (1, 1), (1, 2), (4, 1), (3, 5)):
+        da.decode_attn_plan_info(da.make_problem(**base, sparse_batch=sb, sparse_heads=sh), 152)
+    for sb, sh in ((-1, 0), (0, -2)):
+        with pytest.raises(da.DecodeAttnError) as e:
+            da.decode_attn_plan_info(da.make_problem(**base, sparse_batch=sb, sparse_heads=sh), 152)
+        assert e.value.status == da.DA_ERR_INVALID_ARG

@@ -540,3 +540,34 @@ def test_tree_mask_lower_triangle_is_bitwise_causal():
     out2, _, _, _ = run_gpu(w, engine=eng)
     assert not torch.equal(out0, out2)
     eng.close()
+
+
+# ------------------------------------------------------------------ block masks broadcast over rows / heads
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 4), (5, 1), (2, 2)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_broadcast_block_mask(shape, splits):
+    SZ, SH = shape
+    B, HKV, L, blk = 5, 4, 2048, 128
+    g = torch.Generator().manual_seed(500 + 10 * SZ + SH)
+    nb = torch.randint(0, 9, (SZ, SH), generator=g, dtype=torch.int32)
+    idx = torch.stack([torch.stack([torch.randperm(L // blk, generator=g)[:8] for _ in range(SH)])
+                       for _ in range(SZ)]).to(torch.int32)
+    w = W.make_gqa(name="bcast", batch=B, num_q_heads=16, num_kv_heads=HKV,
+                   seq_lens=[2048, 1000, 64, 0, 1500], cache_len=L, sparse_block_size=blk,
+                   kv_num_blks=nb, kv_idx=idx, sparse_shape=shape, seed=501)
+    eng = da.DecodeAttention(device=0, seq_lens_host=w.tensors["seq_lens"], kv_num_blks_host=nb,
+                             num_splits_override=splits, **da.problem_kwargs(w))
+    out, lse, flags, _ = run_gpu(w, engine=eng)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"broadcast {shape} S={splits}")
+    # the written-out tables give the same bits
+    rows, heads = torch.arange(B) % SZ, torch.arange(HKV) % SH
+    full = W.make_gqa(name="bcast_full", batch=B, num_q_heads=16, num_kv_heads=HKV,
+                      seq_lens=[2048, 1000, 64, 0, 1500], cache_len=L, sparse_block_size=blk,
+                      kv_num_blks=nb[rows][:, heads], kv_idx=idx[rows][:, heads], seed=501)
+    out2, lse2, flags2, _ = run_gpu(full, num_splits_override=splits)
+    if splits:
+        assert flags2 == 0 and torch.equal(out, out2) and torch.equal(lse, lse2)
+    eng.close()
