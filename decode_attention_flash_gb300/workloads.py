@@ -71,6 +71,7 @@ class Workload:
     sparse_batch: int = 0  # block mask extents (batch, kv heads), broadcast by
     sparse_heads: int = 0  # modulo; 0 = the problem's
     kv_token_scale: bool = False  # fp8 KV with a per-token fp16 scale and shift
+    kv_int4_groups: int = 0       # int4 group-wise KV: the number of groups per row
     tensors: dict = field(default_factory=dict)
 
     @property
@@ -148,6 +149,32 @@ def quantize_e4m3_per_token(x: torch.Tensor):
     return y.contiguous(), words.contiguous()
 
 
+def quantize_int4_groups(x: torch.Tensor, groups: int):
+    """Int4 group-wise asymmetric rows (last axis = D): per group fp16 shift =
+    min and fp16 scale = (max - min) / 15 (1 for a constant group), codes
+    round((x - shift) / scale) clamped to 0..15. Returns int32 rows of
+    ``groups`` coefficient words (scale bits low, shift bits high) followed by
+    D / 8 words of eight codes, element 8w + i in bits 4i.. of word w. Rows
+    holding NaN get NaN coefficients."""
+    D = x.shape[-1]
+    finite = torch.nan_to_num(x, nan=0.0)
+    xg = finite.reshape(*x.shape[:-1], groups, D // groups)
+    mx, mn = xg.amax(dim=-1), xg.amin(dim=-1)
+    shift = mn.to(torch.float16)
+    scale = ((mx - mn) / 15).to(torch.float16)
+    scale = torch.where(scale > 0, scale, torch.ones_like(scale))
+    codes = torch.round((xg - shift.float().unsqueeze(-1)) / scale.float().unsqueeze(-1))
+    codes = codes.clamp(0, 15).to(torch.int64).reshape(*x.shape[:-1], D // 8, 8)
+    data = (codes << (4 * torch.arange(8, dtype=torch.int64))).sum(dim=-1)
+    nanrow = torch.isnan(x).any(dim=-1, keepdim=True)
+    sbits = scale.view(torch.int16).to(torch.int64) & 0xFFFF
+    hbits = shift.view(torch.int16).to(torch.int64) & 0xFFFF
+    coef = torch.where(nanrow, torch.full_like(sbits, 0x7E007E00), sbits | (hbits << 16))
+    words = torch.cat([coef, data], dim=-1)
+    words = torch.where(words >= 2 ** 31, words - 2 ** 32, words)
+    return words.to(torch.int32).contiguous()
+
+
 def quantize_e4m3(x: torch.Tensor, head_axis: int):
     """Per-kv-head e4m3 quantisation: scale_h = amax_h / 448, RNE saturating cast."""
     dims = [d for d in range(x.dim()) if d != head_axis]
@@ -163,10 +190,13 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
              layout="contiguous", page_size=16, cache_len=None, kv_fp8=False,
              sparse_block_size=0, kv_num_blks=None, kv_idx=None, scale=None, seed=0,
              num_splits=0, poison=True, shape_only=False, q_len=1,
-             kv_token_scale=False, tree_mask=False, sparse_shape=None) -> Workload:
+             kv_token_scale=False, tree_mask=False, sparse_shape=None,
+             kv_int4_groups=0) -> Workload:
     """A GQA decode workload. ``seq_lens`` is a list/tensor of per-row lengths;
     ``q_len`` > 1 gives each row that many query tokens (its last positions);
     ``tree_mask`` adds a random draft-token tree over them (``spec_mask``).
+    ``kv_int4_groups`` > 0 stores K/V as int4 group-wise rows with that many
+    groups (``quantize_int4_groups``).
     ``sparse_shape`` = (SZ, SH): the block tables' batch and head extents when
     the mask is broadcast (row b, kv head h read table (b % SZ, h % SH)).
 
@@ -181,7 +211,8 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
     w = Workload(name=name, batch=B, num_q_heads=HQ, num_kv_heads=HKV, head_dim_qk=D,
                  head_dim_v=D, scale=float(torch.tensor(scale, dtype=torch.float32)),
                  kv_fp8=kv_fp8, num_splits=num_splits, q_len=max(1, q_len),
-                 kv_token_scale=bool(kv_fp8 and kv_token_scale))
+                 kv_token_scale=bool(kv_fp8 and kv_token_scale), kv_int4_groups=kv_int4_groups)
+    assert not (kv_fp8 and kv_int4_groups)
     t = {"q": q, "seq_lens": seq_lens}
     if tree_mask and q_len > 1:
         t["spec_mask"] = draft_tree_mask(B, q_len, _gen(seed + 7919))
@@ -240,7 +271,9 @@ def make_gqa(*, name="gqa", batch, num_q_heads, num_kv_heads, head_dim=128, seq_
                     mask &= torch.arange(w.cache_len) < int(seq_lens[b])
                     k[b, h, ~mask] = float("nan")
                     v[b, h, ~mask] = float("nan")
-    if kv_fp8 and kv_token_scale:
+    if kv_int4_groups:
+        t.update(k=quantize_int4_groups(k, kv_int4_groups), v=quantize_int4_groups(v, kv_int4_groups))
+    elif kv_fp8 and kv_token_scale:
         kq, kss = quantize_e4m3_per_token(k)
         vq, vss = quantize_e4m3_per_token(v)
         t.update(k=kq, v=vq, k_scale_shift=kss, v_scale_shift=vss)

@@ -45,7 +45,7 @@ class OracleProblem(ctypes.Structure):
         "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "is_mla",
         "ckv_dim", "kpe_dim", "paged", "page_size", "cache_len", "max_pages_per_seq",
         "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks", "q_len",
-        "sparse_batch", "sparse_heads")]
+        "sparse_batch", "sparse_heads", "kv_groups")]
 
 
 class OracleInputs(ctypes.Structure):
@@ -196,7 +196,9 @@ def problem_from(work) -> dict:
         head_dim_qk=w.head_dim_qk, head_dim_v=w.head_dim_v, is_mla=int(w.is_mla),
         ckv_dim=w.ckv_dim, kpe_dim=w.kpe_dim, paged=int(w.paged), page_size=w.page_size,
         cache_len=w.cache_len, max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
-        kv_fp8=(2 if getattr(w, "kv_token_scale", False) else 1) if w.kv_fp8 else 0,
+        kv_fp8=3 if getattr(w, "kv_int4_groups", 0) else
+        ((2 if getattr(w, "kv_token_scale", False) else 1) if w.kv_fp8 else 0),
+        kv_groups=getattr(w, "kv_int4_groups", 0),
         sparse_block_size=w.sparse_block_size,
         max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1),
         sparse_batch=getattr(w, "sparse_batch", 0), sparse_heads=getattr(w, "sparse_heads", 0))

@@ -48,7 +48,13 @@
  *     dequantised value is e4m3(byte) * scale[kv head], or, with a per-token
  *     scale and shift (the split-K page's fp8 scale_shift words),
  *     e4m3(byte) * scale[row] + shift[row];
- *   - fp16 (the scale and shift) is IEEE-754 binary16.
+ *   - int4 group-wise (the split-K page's PACKED_PER_VAL = 8 rows): a cache
+ *     row is int32 words, first N_GROUPS coefficient words (fp16 scale in the
+ *     low half, fp16 shift in the high half), then D / 8 words of eight
+ *     unsigned 4-bit codes, element 8w + i in bits 4i..4i+3 of data word w;
+ *     element d belongs to group d / (D / N_GROUPS) and is code * scale +
+ *     shift of its group;
+ *   - fp16 (the scales and shifts) is IEEE-754 binary16.
  *
  * Parity pins: see tests/test_oracle_pins.py (closed forms, invariants, brute
  * force with exact decimal arithmetic, all-code decoder checks).
@@ -173,12 +179,14 @@ typedef struct {
   int32_t max_pages_per_seq;
   int32_t num_pages;
   int32_t kv_fp8;         /* 0: bf16 bits, 1: e4m3 bytes with per-kv-head scale,
-                             2: e4m3 bytes with a per-token fp16 scale and shift */
+                             2: e4m3 bytes with a per-token fp16 scale and shift,
+                             3: int4 group-wise rows of int32 words (kv_groups groups) */
   int32_t sparse_block_size; /* 0: dense */
   int32_t max_sparse_blocks;
   int32_t q_len;          /* query tokens per row (0 or 1: one) */
   int32_t sparse_batch;   /* sparse: extents of the tables' batch and head axes, */
   int32_t sparse_heads;   /* 0 = B and HKV; row (b, h) reads table (b % SZ, h % SH) */
+  int32_t kv_groups;      /* kv_fp8 == 3: N_GROUPS, 1, 2, 4 or 8 */
 } oracle_problem;
 
 typedef struct {
@@ -306,6 +314,27 @@ static int fetch_kv(const oracle_problem *p, const oracle_inputs *in, int b, int
       kr[p->ckv_dim + d] = kv_elem(p, in->v, row * p->kpe_dim + d, 1.0);
     return ORACLE_OK;
   }
+  if (p->kv_fp8 == 3) {
+    /* int4 group-wise (the split-K decode page: `dequantize` with
+     * PACKED_PER_VAL = 8 splits each data word into eight 4-bit codes, element
+     * 8w + i from bits 4i.., and applies its group's fp16 scale and shift) */
+    const int ng = p->kv_groups;
+    const uint32_t *kw = (const uint32_t *)in->k + row * (ng + p->head_dim_qk / 8);
+    const uint32_t *vw = (const uint32_t *)in->v + row * (ng + p->head_dim_v / 8);
+    for (int d = 0; d < p->head_dim_qk; ++d) {
+      const uint32_t coef = kw[d / (p->head_dim_qk / ng)];
+      const uint32_t code = (kw[ng + d / 8] >> (4 * (d % 8))) & 0xFu;
+      kr[d] = (double)code * oracle_f16_to_double((uint16_t)(coef & 0xFFFF)) +
+              oracle_f16_to_double((uint16_t)(coef >> 16));
+    }
+    for (int d = 0; d < p->head_dim_v; ++d) {
+      const uint32_t coef = vw[d / (p->head_dim_v / ng)];
+      const uint32_t code = (vw[ng + d / 8] >> (4 * (d % 8))) & 0xFu;
+      vr[d] = (double)code * oracle_f16_to_double((uint16_t)(coef & 0xFFFF)) +
+              oracle_f16_to_double((uint16_t)(coef >> 16));
+    }
+    return ORACLE_OK;
+  }
   if (p->kv_fp8 == 2) {
     /* per-token asymmetric e4m3 (the split-K decode page's fp8 K/V with a
      * per-token scale_shift word: `cast_uint32_to_half2` splits it into an
@@ -362,7 +391,12 @@ static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
     return ORACLE_BAD_ARG;
   if (p->kv_fp8 == 1 && (!in->k_scale || !in->v_scale)) return ORACLE_BAD_ARG;
   if (p->kv_fp8 == 2 && (!in->k_scale_shift || !in->v_scale_shift || p->is_mla)) return ORACLE_BAD_ARG;
-  if (p->kv_fp8 < 0 || p->kv_fp8 > 2) return ORACLE_BAD_ARG;
+  if (p->kv_fp8 < 0 || p->kv_fp8 > 3) return ORACLE_BAD_ARG;
+  if (p->kv_fp8 == 3) {
+    const int ng = p->kv_groups;
+    if (p->is_mla || !(ng == 1 || ng == 2 || ng == 4 || ng == 8)) return ORACLE_BAD_ARG;
+    if (p->head_dim_qk % (8 * ng) || p->head_dim_v % (8 * ng)) return ORACLE_BAD_ARG;
+  }
   if (p->sparse_block_size > 0 && (!in->kv_num_blks || !in->kv_idx)) return ORACLE_BAD_ARG;
   if ((in->kv_full_num_blks != NULL) != (in->kv_full_idx != NULL)) return ORACLE_BAD_ARG;
   if (in->kv_full_num_blks && p->sparse_block_size <= 0) return ORACLE_BAD_ARG;

@@ -211,6 +211,23 @@ def _token_dequant(codes, words):
     return codes.double() * scale.unsqueeze(-1) + shift.unsqueeze(-1)
 
 
+def _int4_dequant(words, groups):
+    """int32 rows [groups coefficient words | D/8 data words] -> float64 [.., D],
+    decoded with numpy bit operations: code of element 8w + i = bits 4i.. of
+    data word w, times its group's fp16 scale, plus its fp16 shift."""
+    u = words.numpy().astype(np.int64) & 0xFFFFFFFF
+    data = u[..., groups:]
+    codes = (data[..., :, None] >> (4 * np.arange(8))) & 0xF
+    codes = codes.reshape(*data.shape[:-1], -1).astype(np.float64)
+    D = codes.shape[-1]
+    coef = u[..., :groups]
+    scale = (coef & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+    shift = (coef >> 16).astype(np.uint16).view(np.float16).astype(np.float64)
+    scale = np.repeat(scale, D // groups, axis=-1)
+    shift = np.repeat(shift, D // groups, axis=-1)
+    return torch.from_numpy(codes * scale + shift)
+
+
 def _dec_tanh(x: Decimal) -> Decimal:
     e = (2 * x).exp()
     return (e - 1) / (e + 1)
@@ -223,7 +240,10 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
     B, HQ, HKV = w.batch, w.num_q_heads, w.num_kv_heads
     G = HQ // HKV
     q = t["q"].double()
-    if w.kv_fp8 and w.kv_token_scale:
+    if w.kv_int4_groups:
+        k = _int4_dequant(t["k"], w.kv_int4_groups)
+        v = _int4_dequant(t["v"], w.kv_int4_groups)
+    elif w.kv_fp8 and w.kv_token_scale:
         k = _token_dequant(t["k"], t["k_scale_shift"])
         v = _token_dequant(t["v"], t["v_scale_shift"])
     elif w.kv_fp8:
@@ -340,6 +360,12 @@ def _tiny_cases():
                             head_dim=4, seq_lens=[8, 5], cache_len=8, sparse_block_size=2,
                             kv_num_blks=[1, 3], kv_idx=[[2, 0, 0], [0, 2, 3]], sparse_shape=(1, 2),
                             seed=22, scale=0.7))
+    # int4 group-wise rows (2 and 4 groups), contiguous and paged
+    cases.append(W.make_gqa(name="int4_g2", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                            seq_lens=[6, 2], cache_len=6, kv_int4_groups=2, seed=23, scale=0.6))
+    cases.append(W.make_gqa(name="int4_g4_paged", batch=2, num_q_heads=2, num_kv_heads=1,
+                            head_dim=32, seq_lens=[5, 3], layout="paged", page_size=2,
+                            kv_int4_groups=4, seed=24, scale=0.5))
     # a draft-token tree over the new tokens; the second row is shorter than q_len
     cases.append(W.make_gqa(name="tree_q5", batch=2, num_q_heads=4, num_kv_heads=2,
                             head_dim=4, seq_lens=[8, 3], cache_len=8, seed=19, scale=0.8,
@@ -389,6 +415,70 @@ def _with_mask(w, rows):
     """The workload with every row's draft mask set to ``rows`` (one int per token)."""
     m = torch.tensor(rows, dtype=torch.int64).view(1, -1, 1).expand(w.batch, -1, -1)
     return dict(w.tensors, spec_mask=m.to(torch.int32).contiguous())
+
+
+def _pack_int4(codes, scales, shifts):
+    """Hand-packed int4 rows: codes [.., D] (0..15), per-group fp16-exact scales
+    and shifts [.., G] -> int32 rows in the group-wise layout."""
+    G, D = scales.shape[-1], codes.shape[-1]
+    words = []
+    for gi in range(G):
+        sb = int(np.array([scales[gi]], dtype=np.float16).view(np.uint16)[0])
+        hb = int(np.array([shifts[gi]], dtype=np.float16).view(np.uint16)[0])
+        words.append(sb | (hb << 16))
+    for wi in range(D // 8):
+        words.append(sum(int(codes[8 * wi + i]) << (4 * i) for i in range(8)))
+    return [x - (1 << 32) if x >= (1 << 31) else x for x in words]
+
+
+def test_int4_every_code_through_a_single_key():
+    # one key: out is that key's value row exactly, code * scale + shift of
+    # its group, for all sixteen codes in every nibble position and group
+    D, G = 64, 4
+    codes = np.array([(7 * d + d // 8) % 16 for d in range(D)])
+    scales = np.array([0.5, 0.25, 2.0, 0.125])
+    shifts = np.array([-3.0, 1.5, -0.75, 4.0])
+    row = _pack_int4(codes, scales, shifts)
+    k = torch.tensor([[[_pack_int4(codes[::-1].copy(), scales, shifts)]]], dtype=torch.int32)
+    v = torch.tensor([[[row]]], dtype=torch.int32)
+    q = torch.ones((1, 1, D), dtype=torch.bfloat16)
+    prob = dict(batch=1, num_q_heads=1, num_kv_heads=1, head_dim_qk=D, head_dim_v=D,
+                cache_len=1, kv_fp8=3, kv_groups=G)
+    out, lse = oracle.decode(prob, dict(q=q, k=k, v=v, seq_lens=torch.tensor([1])), 0.1)
+    want = codes * np.repeat(scales, D // G) + np.repeat(shifts, D // G)
+    assert np.array_equal(out[0, 0], want)
+    kvals = codes[::-1] * np.repeat(scales, D // G) + np.repeat(shifts, D // G)
+    assert abs(lse[0, 0] - 0.1 * kvals.sum()) < 1e-12
+
+
+@pytest.mark.parametrize("groups", [1, 2, 4, 8])
+def test_int4_equals_bf16_on_the_same_values(groups):
+    # scales 2^-k and small shifts make every code * scale + shift exact in
+    # bf16: the int4 oracle on the packed rows and the bf16 oracle on the
+    # values give the same bits
+    D = 64
+    g = torch.Generator().manual_seed(60 + groups)
+    B, HKV, L = 2, 2, 9
+    codes = torch.randint(0, 16, (B, HKV, L, D), generator=g).numpy()
+    scales = 2.0 ** -torch.randint(0, 4, (B, HKV, L, groups), generator=g).numpy()
+    shifts = torch.randint(-8, 8, (B, HKV, L, groups), generator=g).numpy() / 4.0
+    packed = [[[_pack_int4(codes[b, h, n], scales[b, h, n], shifts[b, h, n]) for n in range(L)]
+               for h in range(HKV)] for b in range(B)]
+    vals = codes * np.repeat(scales, D // groups, -1) + np.repeat(shifts, D // groups, -1)
+    w = W.make_gqa(name="i4", batch=B, num_q_heads=4, num_kv_heads=HKV, head_dim=D,
+                   seq_lens=[9, 4], cache_len=L, seed=61)
+    vb = torch.from_numpy(vals).to(torch.bfloat16)
+    assert np.array_equal(vb.double().numpy(), vals)
+    dense = dict(w.tensors, k=vb, v=torch.flip(vb, dims=[-1]).contiguous())
+    o1, l1 = oracle.decode(oracle.problem_from(w), dense, w.scale, num_threads=2)
+    pk = torch.tensor(packed, dtype=torch.int32)
+    pv = torch.tensor([[[_pack_int4(codes[b, h, n][::-1].copy(),
+                                    scales[b, h, n][::-1].copy(), shifts[b, h, n][::-1].copy())
+                         for n in range(L)] for h in range(HKV)] for b in range(B)],
+                      dtype=torch.int32)
+    prob = dict(oracle.problem_from(w), kv_fp8=3, kv_groups=groups)
+    o2, l2 = oracle.decode(prob, dict(w.tensors, k=pk, v=pv), w.scale, num_threads=2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
 @pytest.mark.parametrize("shape", [(1, 1), (1, 2), (3, 1), (2, 2)])
