@@ -6,11 +6,14 @@ the workload, K/V cache resident in HBM. Default workload: paged GQA decode
 achieved KV-cache bandwidth (algorithmic KV bytes / time, GB/s), with us per
 call and the fraction of measured HBM peak alongside.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..7] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..8] [--impl reference]
+                  [--tree-mask] [--softcap C]
 
 Configs 1-5 are the five decode workloads; 6 is the speculative-decoding one
-(the paged GQA shapes with 4 query tokens per row, causal over the new tokens);
-7 is config 3 with e4m3 K/V scaled per token (fp16 scale and shift per row).
+(the paged GQA shapes with 4 query tokens per row, causal over the new tokens,
+or a random draft-token tree with --tree-mask); 7 is config 3 with e4m3 K/V
+scaled per token (fp16 scale and shift per row); 8 is config 2 with int4
+group-wise K/V (4 groups of 32 elements per row).
 
 Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
 units are independent, no collective on the data path); rank 0 prints one
@@ -89,7 +92,8 @@ def algorithmic_bytes(w) -> dict:
         for b in range(w.batch):
             n_b = int(t["seq_lens"][b])
             for h in range(w.num_kv_heads):
-                blocks = t["kv_idx"][b, h, :int(nb[b, h])].long()
+                zb, zh = b % (w.sparse_batch or w.batch), h % (w.sparse_heads or w.num_kv_heads)
+                blocks = t["kv_idx"][zb, zh, :int(nb[zb, zh])].long()
                 positions += int(torch.clamp(n_b - blocks * w.sparse_block_size, 0,
                                              w.sparse_block_size).sum())
         kv_tokens_heads = positions
@@ -103,6 +107,8 @@ def algorithmic_bytes(w) -> dict:
         flops = kv_tokens_heads * w.num_q_heads * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
     else:
         kv = kv_tokens_heads * (w.head_dim_qk + w.head_dim_v) * elt
+        if getattr(w, "kv_int4_groups", 0):  # int32 rows: groups coefficient words + D / 8 data words
+            kv = kv_tokens_heads * 2 * (w.kv_int4_groups + w.head_dim_qk // 8) * 4
         if getattr(w, "kv_token_scale", False):
             kv += kv_tokens_heads * 2 * 4  # the K and V scale words of every row
         q = w.batch * w.num_q_heads * Q * w.head_dim_qk * 2
@@ -373,7 +379,7 @@ def run_ours(args, w, cfg):
             "metric": "decode attention KV GB/s & % of GB300 HBM peak; \u00b5s per decode call",
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_call, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f8e4m3" if w.kv_fp8 else "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4" if w.kv_int4_groups else ("f8e4m3" if w.kv_fp8 else "bf16"),
             "data": "synthetic",
             "config": {"workload": workload_name(cfg, args), "us_per_call": mean_call * 1e3,
                        "pct_hbm_peak_kv_q_o": pct_hbm, "hbm_peak_gbs": hbm_peak,

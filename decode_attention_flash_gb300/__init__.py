@@ -28,7 +28,7 @@ __all__ = [
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_CUDA = 0, 1, 2, 3
 DA_ERR_WORKSPACE, DA_ERR_NOT_PLANNED, DA_ERR_DEVICE = 4, 5, 6
 DA_KV_CONTIGUOUS, DA_KV_PAGED = 0, 1
-DA_DTYPE_BF16, DA_DTYPE_FP8_E4M3, DA_DTYPE_FP8_E4M3_TOKEN_SCALE = 0, 1, 2
+DA_DTYPE_BF16, DA_DTYPE_FP8_E4M3, DA_DTYPE_FP8_E4M3_TOKEN_SCALE, DA_DTYPE_INT4_GROUPS = 0, 1, 2, 3
 DA_DEVERR_PAGE_INDEX, DA_DEVERR_SPARSE_INDEX, DA_DEVERR_SEQ_LEN, DA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 
@@ -48,7 +48,7 @@ class Problem(ctypes.Structure):
         ("num_pages", ctypes.c_int32), ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
         ("sparse_block_size", ctypes.c_int32), ("max_sparse_blocks", ctypes.c_int32),
         ("q_len", ctypes.c_int32), ("sparse_batch", ctypes.c_int32),
-        ("sparse_heads", ctypes.c_int32),
+        ("sparse_heads", ctypes.c_int32), ("kv_groups", ctypes.c_int32),
     ]
 
 
@@ -303,8 +303,10 @@ def problem_kwargs(work) -> dict:
                 page_size=w.page_size, max_seq_len=w.max_seq_len,
                 max_pages_per_seq=w.max_pages_per_seq, num_pages=w.num_pages,
                 q_dtype=DA_DTYPE_BF16,
-                kv_dtype=(DA_DTYPE_FP8_E4M3_TOKEN_SCALE if getattr(w, "kv_token_scale", False)
-                          else DA_DTYPE_FP8_E4M3) if w.kv_fp8 else DA_DTYPE_BF16,
+                kv_dtype=DA_DTYPE_INT4_GROUPS if getattr(w, "kv_int4_groups", 0) else
+                ((DA_DTYPE_FP8_E4M3_TOKEN_SCALE if getattr(w, "kv_token_scale", False)
+                  else DA_DTYPE_FP8_E4M3) if w.kv_fp8 else DA_DTYPE_BF16),
+                kv_groups=getattr(w, "kv_int4_groups", 0),
                 sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks,
                 q_len=getattr(w, "q_len", 1), sparse_batch=getattr(w, "sparse_batch", 0),
                 sparse_heads=getattr(w, "sparse_heads", 0))

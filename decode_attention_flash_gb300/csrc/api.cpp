@@ -119,6 +119,37 @@ da_status encode_bf16_halves(CUtensorMap *map, const void *base, uint64_t rows, 
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
+// int4 group-wise rows viewed as int32 [rows][W] (W = groups + 16 words): the
+// 16 data words of `box_rows` rows, 64B-swizzled (the kernel loads at x = groups).
+da_status encode_int4_data(CUtensorMap *map, const void *base, uint64_t rows, uint32_t W,
+                           uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {W, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)W * 4};
+  const cuuint32_t box[2] = {16u, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
+// ... and their coefficient words: `groups` words of `box_rows` rows (x = 0).
+da_status encode_int4_coef(CUtensorMap *map, const void *base, uint64_t rows, uint32_t W,
+                           uint32_t groups, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[2] = {W, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)W * 4};
+  const cuuint32_t box[2] = {groups, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
 // Per-token scale words: one int32 per cache row, viewed as [rows / 4][4] so a
 // box of `box_rows` rows is 4 words wide (16 bytes); rows past the end read 0.
 da_status encode_scale_words(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
@@ -158,6 +189,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   const da_problem &p = ctx->prob;
   const bool fp8 = p.kv_dtype != DA_DTYPE_BF16;
   const bool token_scale = p.kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE;
+  const bool int4 = p.kv_dtype == DA_DTYPE_INT4_GROUPS;  // takes the f16 (fp8) kernel path
   const bool paged = p.kv_layout == DA_KV_PAGED;
   const bool sparse = p.sparse_block_size > 0;
   if (!a->q || !a->k || !a->v || !a->seq_lens || !a->out) return DA_ERR_INVALID_ARG;
@@ -165,7 +197,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   if (sparse && (!a->kv_num_blks || !a->kv_idx)) return DA_ERR_INVALID_ARG;
   if ((a->kv_full_num_blks != nullptr) != (a->kv_full_idx != nullptr)) return DA_ERR_INVALID_ARG;
   if (a->kv_full_num_blks && !sparse) return DA_ERR_INVALID_ARG;
-  if (fp8 && !token_scale && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
+  if (fp8 && !token_scale && !int4 && (!a->k_scale || !a->v_scale)) return DA_ERR_INVALID_ARG;
   if (token_scale && (!a->k_scale_shift || !a->v_scale_shift || !aligned(a->k_scale_shift, 16) ||
                       !aligned(a->v_scale_shift, 16)))
     return DA_ERR_INVALID_ARG;
@@ -182,7 +214,17 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   if (ctx->map_k_base != a->k || ctx->map_v_base != a->v || ctx->map_q_base != a->q) {
     ctx->map_k_base = ctx->map_v_base = ctx->map_q_base = nullptr;
     da_status st;
-    if (fp8) {
+    if (int4) {
+      const uint32_t W = (uint32_t)p.kv_groups + 16u;
+      if ((st = encode_int4_data(&ctx->kmap, a->k, rows, W, box_tokens)) != DA_OK) return st;
+      if ((st = encode_int4_data(&ctx->vmap, a->v, rows, W, box_tokens)) != DA_OK) return st;
+      if ((st = encode_int4_coef(&ctx->kssmap, a->k, rows, W, (uint32_t)p.kv_groups, box_tokens)) !=
+          DA_OK)
+        return st;
+      if ((st = encode_int4_coef(&ctx->vssmap, a->v, rows, W, (uint32_t)p.kv_groups, box_tokens)) !=
+          DA_OK)
+        return st;
+    } else if (fp8) {
       // one 128-byte row per token
       if ((st = encode_rows(&ctx->kmap, a->k, false, rows, box_tokens)) != DA_OK) return st;
       if ((st = encode_rows(&ctx->vmap, a->v, false, rows, box_tokens)) != DA_OK) return st;
@@ -237,6 +279,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.group = R;
   gp.q_len = Q;
   gp.token_scale = token_scale ? 1 : 0;
+  gp.kv_groups = int4 ? p.kv_groups : 0;
   gp.paged = paged ? 1 : 0;
   gp.page_size = p.page_size;
   gp.cache_len = paged ? 0 : p.max_seq_len;
@@ -248,7 +291,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.sparse_batch = p.sparse_batch > 0 ? p.sparse_batch : std::max(p.batch, 1);
   gp.sparse_heads = p.sparse_heads > 0 ? p.sparse_heads : p.num_kv_heads;
   if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,
-                     token_scale ? ctx->kssmap : ctx->kmap, token_scale ? ctx->vssmap : ctx->vmap,
+                     token_scale || int4 ? ctx->kssmap : ctx->kmap,
+                     token_scale || int4 ? ctx->vssmap : ctx->vmap,
                      gp, pl.grid_x, stream) !=
       cudaSuccess)
     return DA_ERR_CUDA;

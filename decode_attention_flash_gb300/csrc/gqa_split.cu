@@ -55,11 +55,15 @@ constexpr int kD = 128;               // head dimension
 constexpr int kRedStride = kD + 4;    // padded row of the epilogue reduction buffer
 constexpr uint32_t kConsumerBar = 1;  // named barrier of the 128 consumer threads
 
-template <bool FP8, int NT, bool TOK = false>
+// int4 group-wise rows: the K/V data of a token is 16 words (64 bytes) after
+// its coefficient words; at most 8 coefficient words per row
+constexpr int kI4MaxGroups = 8;
+
+template <bool FP8, int NT, bool TOK = false, bool I4 = false>
 struct Cfg {
-  static constexpr int kBytesPerTok = FP8 ? kD : 2 * kD;
+  static constexpr int kBytesPerTok = I4 ? kD / 2 : (FP8 ? kD : 2 * kD);
   static constexpr int kTileBytes = kTile * kBytesPerTok;  // one of K or V
-  static constexpr int kStages = FP8 ? (NT == 1 ? 5 : 4) : 3;
+  static constexpr int kStages = I4 ? 6 : (FP8 ? (NT == 1 ? 5 : 4) : 3);
   static constexpr int kQSlot = NT * 8 * kD * 2;             // the query group (bf16 rows)
   // shared-memory layout (byte offsets from a 1024-aligned base)
   static constexpr int oRing = 0;                            // [stage][K|V][tile]
@@ -92,9 +96,17 @@ struct Cfg {
   static constexpr int oSS = (oMergeBar + 4 * 8 + 127) & ~127;
   static constexpr int kSSBytes = TOK ? kStages * 2 * kSSWords * 4 : 0;
   static constexpr int oStatZ = oSS + kSSBytes;
-  static constexpr int kTotal = oStatZ + (TOK ? kConsumerWarps * 16 * 4 : 0) + 1024;  // + slack
+  // int4: [stage][K|V][kTile rows][groups] coefficient words (TMA destinations;
+  // a page box of r rows starts r * groups words into its stage's region)
+  static constexpr int kCoefWords = kTile * kI4MaxGroups;
+  static constexpr int oCoef = (oStatZ + (TOK ? kConsumerWarps * 16 * 4 : 0) + 127) & ~127;
+  static constexpr int kCoefBytes = I4 ? kStages * 2 * kCoefWords * 4 : 0;
+  static constexpr int kTotal = oCoef + kCoefBytes + 1024;  // + slack
   static_assert(oSS % 128 == 0 && (2 * kSSWords * 4) % 128 == 0, "TMA destinations need 128 B");
   static_assert(oQ % 128 == 0 && kQSlot % 128 == 0 && kTileBytes % 128 == 0, "TMA destinations");
+  static_assert(!I4 || (FP8 && !TOK), "int4 rows take the f16 operand path and their own scales");
+  static_assert(oCoef % 128 == 0 && (kCoefWords * 4) % 128 == 0, "TMA destinations need 128 B");
+  static_assert(!I4 || kTileBytes % 1024 == 0, "64-byte swizzle atoms of int4 tiles");
 };
 
 // What the producer tells the consumers about the tile in a stage.
@@ -232,6 +244,29 @@ __device__ __forceinline__ uint32_t chunk_addr(uint32_t base, uint32_t tok_off, 
 
 __device__ __forceinline__ uint32_t lo16_mask(bool a, bool b) {
   return (a ? 0x0000FFFFu : 0u) | (b ? 0xFFFF0000u : 0u);
+}
+
+// int4 tiles: 64-byte rows (a token's 16 data words), 64B-swizzled by TMA:
+// 16-byte chunk c of row t sits at chunk c ^ ((t >> 1) & 3), so the eight rows
+// an ldmatrix reads fall in eight different bank groups.
+__device__ __forceinline__ uint32_t i4_addr(uint32_t base, int t, int c) {
+  return base + (uint32_t)t * 64u + (uint32_t)((c ^ (t >> 1)) & 3) * 16u;
+}
+
+// The two 4-bit codes in bits 4j.. of each 16-bit half of x, as an f16 pair
+// 1024 + code (an f16 whose unit in the last place is 1).
+__device__ __forceinline__ uint32_t i4_codes(uint32_t x, int j) {
+  return ((x >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+}
+
+// code * scale + shift on f16 pairs: the 1024 is subtracted exactly first.
+__device__ __forceinline__ uint32_t i4_dequant(uint32_t codes, uint32_t scale2, uint32_t shift2) {
+  const uint32_t bias = 0x64006400u;
+  const __half2 n = __hsub2(*reinterpret_cast<const __half2 *>(&codes),
+                            *reinterpret_cast<const __half2 *>(&bias));
+  const __half2 r = __hfma2(n, *reinterpret_cast<const __half2 *>(&scale2),
+                            *reinterpret_cast<const __half2 *>(&shift2));
+  return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
@@ -678,14 +713,14 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
 }
 
 // TOK: e4m3 K/V with per-token scale and shift words (FP8 only).
-template <bool FP8, int NT, bool TOK>
+template <bool FP8, int NT, bool TOK, bool I4>
 __global__ void __launch_bounds__(threads_for<NT>(), 2)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kssmap,
                      const __grid_constant__ CUtensorMap vssmap, const GqaParams p) {
-  using C = Cfg<FP8, NT, TOK>;
+  using C = Cfg<FP8, NT, TOK, I4>;
   static_assert(!TOK || FP8, "per-token scales are an e4m3 format");
   constexpr int kThreads = threads_for<NT>();
   constexpr bool kHelper = has_helper<NT>();
@@ -694,6 +729,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = smem + C::oRing;
   uint8_t *qslots = smem + C::oQ;
+  int32_t *coef = reinterpret_cast<int32_t *>(smem + C::oCoef);  // int4 coefficient words
   float *red = reinterpret_cast<float *>(smem + C::oRed);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oFull);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + C::oEmpty);
@@ -799,7 +835,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     const uint64_t q_policy = l2_policy_evict_last();
     const int P = p.page_size;
     const int pages_per_tile = p.paged ? (P >= kTile ? 1 : kTile / P) : 1;
-    const bool multi_box = !FP8 && pages_per_tile > 1;  // several page boxes per tile
+    const bool multi_box = (!FP8 || I4) && pages_per_tile > 1;  // several page boxes per tile
 
     // Walker over (unit, tile) in processing order. When the range ends in the
     // head of a unit that goes on into the next CTA, that segment is streamed
@@ -958,6 +994,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         const uint32_t box_tokens = (p.paged && P < kTile) ? (uint32_t)P : (uint32_t)kTile;
         uint32_t bytes = 2u * (uint32_t)nbox * box_tokens * C::kBytesPerTok;
         if (TOK) bytes += 2u * (uint32_t)nbox * box_tokens * 4;  // scale words
+        if (I4) bytes += 2u * (uint32_t)nbox * box_tokens * p.kv_groups * 4;  // coefficient words
         if (first) bytes += (uint32_t)G * kD * 2;
         mbar_arrive_expect_tx(&full[st], bytes);
         if (!multi_box) {
@@ -971,7 +1008,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           for (int k = 0; k < nb; ++k) {
             if (ys[k] < 0) continue;
             const int off = k * box_rows * C::kBytesPerTok;  // box k of a multi-page tile
-            if (FP8) {
+            if (I4) {
+              // the rows' 16 data words (x = groups: after the coefficient
+              // words) and their coefficient words
+              tma_load_2d(kdst + off, &kmap, &full[st], p.kv_groups, ys[k], policy);
+              tma_load_2d(vdst + off, &vmap, &full[st], p.kv_groups, ys[k], policy);
+              int32_t *cf = coef + st * 2 * C::kCoefWords + k * box_rows * p.kv_groups;
+              tma_load_2d(cf, &kssmap, &full[st], 0, ys[k], policy);
+              tma_load_2d(cf + C::kCoefWords, &vssmap, &full[st], 0, ys[k], policy);
+            } else if (FP8) {
               tma_load_2d(kdst + off, &kmap, &full[st], 0, ys[k], policy);
               tma_load_2d(vdst + off, &vmap, &full[st], 0, ys[k], policy);
               if (TOK) {
@@ -1006,7 +1051,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           const bool isv = lane >= 8;
           uint8_t *dst = ring + (size_t)st * 2 * C::kTileBytes + (isv ? C::kTileBytes : 0) +
                          k * P * C::kBytesPerTok;
-          tma_load_3d(dst, isv ? &vmap : &kmap, &full[st], 0, y, 0, policy);
+          if (I4) {
+            tma_load_2d(dst, isv ? &vmap : &kmap, &full[st], p.kv_groups, y, policy);
+            tma_load_2d(coef + st * 2 * C::kCoefWords + (isv ? C::kCoefWords : 0) + k * P * p.kv_groups,
+                        isv ? &vssmap : &kssmap, &full[st], 0, y, policy);
+          } else {
+            tma_load_3d(dst, isv ? &vmap : &kmap, &full[st], 0, y, 0, policy);
+          }
         }
         if (first && lane == 16)
           tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
@@ -1121,7 +1172,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           const uint32_t *qrow = qs + (g < G ? g : 0) * (kD / 2);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            if (!FP8) {
+            if (I4) {
+              // k-step 2c+s pairs the elements one int4 data word gives a lane:
+              // 32c + 8q4 + 2s + {0, 4} (b0) and 32c + 8q4 + 2s + 1 + {0, 4} (b1)
+              const __nv_bfloat16 *qh = reinterpret_cast<const __nv_bfloat16 *>(qrow);
+              const int d0 = 32 * (ks >> 1) + 8 * q4 + 2 * (ks & 1);
+              qf[nt][ks][0] = g < G ? pack_f16(__bfloat162float(qh[d0]), __bfloat162float(qh[d0 + 4])) : 0u;
+              qf[nt][ks][1] =
+                  g < G ? pack_f16(__bfloat162float(qh[d0 + 1]), __bfloat162float(qh[d0 + 5])) : 0u;
+            } else if (!FP8) {
               qf[nt][ks][0] = g < G ? qrow[(16 * ks + 2 * q4) / 2] : 0u;
               qf[nt][ks][1] = g < G ? qrow[(16 * ks + 8 + 2 * q4) / 2] : 0u;
             } else {
@@ -1153,7 +1212,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             qsum[nt][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * q4));
             qsum[nt][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * q4 + 1));
           }
-        } else if (FP8) {
+        } else if (FP8 && !I4) {
           sscale = p.score_scale * p.k_scale[h];
           vmul = p.v_scale[h];
         }
@@ -1175,7 +1234,38 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
         {
           const int t = tok_lane + (mi & 1) * 8;
-          if (!FP8) {
+          if (I4) {
+            // int4 K: each lane's ldmatrix word is 8 codes of one token row;
+            // its pairs (j, j + 4) are the A fragments of two k-steps, scaled
+            // by the row's group coefficients
+            const int32_t *cfk = coef + st * 2 * C::kCoefWords;
+            const int ng = p.kv_groups;
+            const int tA = 16 * warp + r8, tB = tA + 8;
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+              uint32_t r[4];
+              ldsm_x4(i4_addr(kbase, t, 2 * cp + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {  // chunk 2cp + h2: words r[2h2] (row tA), r[2h2+1] (tB)
+                const int cc = 2 * cp + h2;
+                const int gi = ng == 4 ? cc : 2 * cc + (q4 >> 1);
+                const uint32_t wA = (uint32_t)cfk[tA * ng + gi], wB = (uint32_t)cfk[tB * ng + gi];
+                const uint32_t sA = prmt(wA, 0, 0x1010), hA = prmt(wA, 0, 0x3232);
+                const uint32_t sB = prmt(wB, 0, 0x1010), hB = prmt(wB, 0, 0x3232);
+#pragma unroll
+                for (int sidx = 0; sidx < 2; ++sidx) {
+                  const uint32_t a0 = i4_dequant(i4_codes(r[2 * h2], 2 * sidx), sA, hA);
+                  const uint32_t a2 = i4_dequant(i4_codes(r[2 * h2], 2 * sidx + 1), sA, hA);
+                  const uint32_t a1 = i4_dequant(i4_codes(r[2 * h2 + 1], 2 * sidx), sB, hB);
+                  const uint32_t a3 = i4_dequant(i4_codes(r[2 * h2 + 1], 2 * sidx + 1), sB, hB);
+                  const int ks = 2 * cc + sidx;
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma_f16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+                }
+              }
+            }
+          } else if (!FP8) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               uint32_t a0, a1, a2, a3;
@@ -1284,7 +1374,45 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         const uint32_t m01 = lo16_mask((vbits >> (2 * q4)) & 1u, (vbits >> (2 * q4 + 1)) & 1u);
         const uint32_t m89 =
             lo16_mask((vbits >> (2 * q4 + 8)) & 1u, (vbits >> (2 * q4 + 9)) & 1u);
-        if (!FP8) {
+        if (I4) {
+          // int4 V through ldmatrix.trans: a lane's word holds four codes of each
+          // of two tokens (2q4, 2q4+1 or +8, +9) for elements 32c + 4r8 + 0..3;
+          // code j of chunks 2cp / 2cp + 1 gives rows r8 / r8 + 8 of the
+          // O^T tile 4cp + j (elements 64cp + 4r8 + j and + 32)
+          const int32_t *cfv = coef + st * 2 * C::kCoefWords + C::kCoefWords;
+          const int ng = p.kv_groups;
+          const int t0 = 16 * warp + 2 * q4;
+          const int t = tok_lane + (mi & 1) * 8;
+#pragma unroll
+          for (int cp = 0; cp < 2; ++cp) {
+            uint32_t r[4];
+            ldsm_x4_trans(i4_addr(vbase, t, 2 * cp + (mi >> 1)), r[0], r[1], r[2], r[3]);
+            // coefficient pairs (scale, shift) of the token pairs, per chunk
+            uint32_t sc[2][2], sh[2][2];  // [chunk 2cp + h2][lo pair | hi pair]
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int cc = 2 * cp + h2;
+              const int gi = ng == 4 ? cc : 2 * cc + (r8 >> 2);
+#pragma unroll
+              for (int hp = 0; hp < 2; ++hp) {
+                const int ta = t0 + 8 * hp;
+                const uint32_t w0 = (uint32_t)cfv[ta * ng + gi], w1 = (uint32_t)cfv[(ta + 1) * ng + gi];
+                sc[h2][hp] = prmt(w0, w1, 0x5410);
+                sh[h2][hp] = prmt(w0, w1, 0x7632);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t a0 = i4_dequant(i4_codes(r[0], j), sc[0][0], sh[0][0]) & m01;
+              const uint32_t a2 = i4_dequant(i4_codes(r[1], j), sc[0][1], sh[0][1]) & m89;
+              const uint32_t a1 = i4_dequant(i4_codes(r[2], j), sc[1][0], sh[1][0]) & m01;
+              const uint32_t a3 = i4_dequant(i4_codes(r[3], j), sc[1][1], sh[1][1]) & m89;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(oacc[nt][4 * cp + j], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+          }
+        } else if (!FP8) {
           const int t = tok_lane + (mi >> 1) * 8;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -1417,8 +1545,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             const int x = C::kScrSwizzled ? (g & 7) << 2 : 0;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-              const int d0 = FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8;
-              const int d1 = FP8 ? d0 + 1 : d0 + 8;
+              const int d0 = I4 ? 64 * (mt >> 2) + 4 * r8 + (mt & 3)
+                                : (FP8 ? 16 * mt + 2 * r8 : 16 * mt + r8);
+              const int d1 = I4 ? d0 + 32 : (FP8 ? d0 + 1 : d0 + 8);
               const float v0 = oacc[nt][mt][e] * wscale, v1 = oacc[nt][mt][2 + e] * wscale;
               if (!add) {
                 dst[d0 ^ x] = v0;
@@ -1576,24 +1705,26 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   if (dev_err) atomicOr(p.err, dev_err);
 }
 
-template <bool FP8, int NT, bool TOK>
+template <bool FP8, int NT, bool TOK, bool I4 = false>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK>,
+  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK, I4>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<FP8, NT, TOK>::kTotal);
+                              Cfg<FP8, NT, TOK, I4>::kTotal);
 }
 
-template <bool FP8, int NT, bool TOK>
+template <bool FP8, int NT, bool TOK, bool I4 = false>
 void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
             const CUtensorMap &kssmap, const CUtensorMap &vssmap, const GqaParams &p, int ctas,
             cudaStream_t stream) {
-  gqa_split_kernel<FP8, NT, TOK><<<ctas, threads_for<NT>(), Cfg<FP8, NT, TOK>::kTotal, stream>>>(
-      kmap, vmap, qmap, kssmap, vssmap, p);
+  gqa_split_kernel<FP8, NT, TOK, I4>
+      <<<ctas, threads_for<NT>(), Cfg<FP8, NT, TOK, I4>::kTotal, stream>>>(kmap, vmap, qmap, kssmap,
+                                                                           vssmap, p);
 }
 
 }  // namespace
 
-int gqa_smem_bytes(bool fp8, int group, bool token_scale) {
+int gqa_smem_bytes(bool fp8, int group, bool token_scale, bool int4) {
+  if (int4) return group <= 8 ? Cfg<true, 1, false, true>::kTotal : Cfg<true, 2, false, true>::kTotal;
   if (fp8 && token_scale) return group <= 8 ? Cfg<true, 1, true>::kTotal : Cfg<true, 2, true>::kTotal;
   if (fp8) return group <= 8 ? Cfg<true, 1>::kTotal : Cfg<true, 2>::kTotal;
   return group <= 8 ? Cfg<false, 1>::kTotal : Cfg<false, 2>::kTotal;
@@ -1613,6 +1744,8 @@ cudaError_t gqa_prepare(int /*device*/) {
   if ((e = set_attr<true, 2, false>()) != cudaSuccess) return e;
   if ((e = set_attr<true, 1, true>()) != cudaSuccess) return e;
   if ((e = set_attr<true, 2, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 1, false, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, 2, false, true>()) != cudaSuccess) return e;
   return cudaSuccess;
 }
 
@@ -1624,6 +1757,9 @@ cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUten
   if (!fp8) {
     if (!two) launch<false, 1, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
     else launch<false, 2, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+  } else if (p.kv_groups > 0) {
+    if (!two) launch<true, 1, false, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+    else launch<true, 2, false, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   } else if (!p.token_scale) {
     if (!two) launch<true, 1, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
     else launch<true, 2, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);

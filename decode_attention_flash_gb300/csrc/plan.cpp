@@ -32,8 +32,14 @@ da_status validate_problem(const da_problem *p) {
   if (p->q_dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout != DA_KV_CONTIGUOUS && p->kv_layout != DA_KV_PAGED) return DA_ERR_INVALID_ARG;
   if (p->kv_dtype != DA_DTYPE_BF16 && p->kv_dtype != DA_DTYPE_FP8_E4M3 &&
-      p->kv_dtype != DA_DTYPE_FP8_E4M3_TOKEN_SCALE)
+      p->kv_dtype != DA_DTYPE_FP8_E4M3_TOKEN_SCALE && p->kv_dtype != DA_DTYPE_INT4_GROUPS)
     return DA_ERR_INVALID_ARG;
+  if (p->kv_dtype == DA_DTYPE_INT4_GROUPS) {
+    if (!(p->kv_groups == 1 || p->kv_groups == 2 || p->kv_groups == 4 || p->kv_groups == 8))
+      return DA_ERR_INVALID_ARG;
+    // rows of groups + 16 words: TMA strides them only when a multiple of 16 bytes
+    if (p->kv_groups < 4) return DA_ERR_UNSUPPORTED;
+  }
   if (p->max_seq_len < 0 || p->q_len < 0) return DA_ERR_INVALID_ARG;
   const int Q = p->q_len > 1 ? p->q_len : 1;  // query tokens per row
   if (p->kv_layout == DA_KV_PAGED) {
@@ -88,7 +94,8 @@ static int ctas_per_sm(const da_problem *p, int32_t smem_per_sm) {
                            : gqa_smem_bytes(p->kv_dtype != DA_DTYPE_BF16,
                                             p->num_q_heads / p->num_kv_heads *
                                                 (p->q_len > 1 ? p->q_len : 1),
-                                            p->kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE)) +
+                                            p->kv_dtype == DA_DTYPE_FP8_E4M3_TOKEN_SCALE,
+                                            p->kv_dtype == DA_DTYPE_INT4_GROUPS)) +
                       1024;  // the runtime reserves 1 KB per CTA
   const int threads = mla ? mla_threads() : gqa_threads();
   return std::max(1, std::min(smem_per_sm / per_cta, 2048 / threads));

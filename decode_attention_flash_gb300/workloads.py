@@ -157,6 +157,10 @@ def quantize_int4_groups(x: torch.Tensor, groups: int):
     D / 8 words of eight codes, element 8w + i in bits 4i.. of word w. Rows
     holding NaN get NaN coefficients."""
     D = x.shape[-1]
+    if x.dim() > 1 and x.shape[0] > 1 and x.numel() > (1 << 24):  # in slices, to bound memory
+        n = max(1, (1 << 24) // (x.numel() // x.shape[0]))
+        return torch.cat([quantize_int4_groups(x[i:i + n], groups)
+                          for i in range(0, x.shape[0], n)]).contiguous()
     finite = torch.nan_to_num(x, nan=0.0)
     xg = finite.reshape(*x.shape[:-1], groups, D // groups)
     mx, mn = xg.amax(dim=-1), xg.amin(dim=-1)
@@ -370,6 +374,7 @@ CONFIG_NAMES = {
     5: "MLA latent decode (B64 HQ128, ckv512+kpe64, N_b~U[2048,8192], page 64)",
     6: "speculative paged GQA decode (B32 HQ32 HKV8 D128, 4 query tokens, N_b~U[1024,8192], page 16)",
     7: "long-context fp8 KV, per-token scale+shift (B1 HQ64 HKV8 D128, contiguous L131072, e4m3)",
+    8: "paged GQA decode, int4 group-wise KV (B32 HQ32 HKV8 D128, 4 groups of 32, N_b~U[1024,8192], page 16)",
 }
 
 
@@ -408,4 +413,10 @@ def config(i: int, shape_only: bool = False) -> Workload:
         return make_gqa(name="fp8_token_long", batch=1, num_q_heads=64, num_kv_heads=8,
                         seq_lens=[131072], cache_len=131072, kv_fp8=True, kv_token_scale=True,
                         seed=seed, **so)
+    if i == 8:
+        g = _gen(1002 + 500)  # the lengths of the bf16 paged workload (2)
+        lens = _lengths(32, 1024, 8192, g)
+        return make_gqa(name="int4_paged_gqa", batch=32, num_q_heads=32, num_kv_heads=8,
+                        seq_lens=lens, layout="paged", page_size=16, seed=seed, kv_int4_groups=4,
+                        **so)
     raise ValueError(f"no workload {i}")

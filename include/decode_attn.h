@@ -68,13 +68,19 @@ typedef enum {
 
 typedef enum { DA_KV_CONTIGUOUS = 0, DA_KV_PAGED = 1 } da_kv_layout;
 /* KV element types: bf16; e4m3 with one fp32 scale per kv head (k_scale /
- * v_scale); or e4m3 with a per-token fp16 scale and shift (k_scale_shift /
+ * v_scale); e4m3 with a per-token fp16 scale and shift (k_scale_shift /
  * v_scale_shift: value = e4m3 * scale + shift, the fp8 scale_shift words of
- * the split-K decode page, mslk splitk_kernels.py `dequantize`). */
+ * the split-K decode page, mslk splitk_kernels.py `dequantize`); or int4
+ * group-wise rows, the same page's PACKED_PER_VAL = 8 layout: each cache row
+ * of k / v is int32 words, first kv_groups coefficient words (fp16 scale in
+ * the low half, fp16 shift in the high half), then D / 8 words of eight
+ * unsigned 4-bit codes, element 8w + i in bits 4i..4i+3 of data word w;
+ * element d has value code * scale + shift of group d / (D / kv_groups). */
 typedef enum {
   DA_DTYPE_BF16 = 0,
   DA_DTYPE_FP8_E4M3 = 1,
-  DA_DTYPE_FP8_E4M3_TOKEN_SCALE = 2
+  DA_DTYPE_FP8_E4M3_TOKEN_SCALE = 2,
+  DA_DTYPE_INT4_GROUPS = 3
 } da_dtype;
 
 /* Bits of the device error word (sticky until decode_attn_get_error clears it). */
@@ -120,6 +126,8 @@ typedef struct {
   int32_t q_len;              /* query tokens per row; 0 or 1 = one */
   int32_t sparse_batch;       /* sparse: block tables' batch extent SZ (0 = batch) */
   int32_t sparse_heads;       /* sparse: block tables' head extent SH (0 = num_kv_heads) */
+  int32_t kv_groups;          /* DA_DTYPE_INT4_GROUPS: groups per row, 4 or 8 (rows of 1 or
+                                 2 groups are not a multiple of 16 bytes: unsupported) */
 } da_problem;
 
 /*
@@ -129,7 +137,8 @@ typedef struct {
  *   q_pe       MLA only: bf16 [B][HQ][64]; else NULL
  *   k, v       contiguous [B][HKV][L][D]; paged [num_pages][HKV][page_size][D];
  *              MLA: k = ckv [num_pages][page_size][512], v = kpe [num_pages][page_size][64].
- *              Element type bf16, or e4m3 bytes when kv_dtype is an e4m3 type.
+ *              Element type bf16, or e4m3 bytes when kv_dtype is an e4m3 type;
+ *              DA_DTYPE_INT4_GROUPS: int32 rows of kv_groups + D / 8 words.
  *              Base addresses 16-byte aligned.
  *   k_scale, v_scale  DA_DTYPE_FP8_E4M3 only: fp32 [HKV]; dequantised value = e4m3 * scale
  *   k_scale_shift, v_scale_shift  DA_DTYPE_FP8_E4M3_TOKEN_SCALE only: int32, one word per

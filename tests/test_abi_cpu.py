@@ -168,7 +168,7 @@ def _check_mla_plan(plan, row_tiles, num_sms=152):
     assert plan["workspace_bytes"] - plan["partial_lse_offset"] >= (U + C) * 2 * 128 * 4
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_planner_covers_every_position_once(lib, cfg):
     w = W.config(cfg, shape_only=True)
     nb = w.tensors.get("kv_num_blks")
@@ -255,3 +255,18 @@ def test_broadcast_block_mask_extents_are_validated(lib):
         with pytest.raises(da.DecodeAttnError) as e:
             da.decode_attn_plan_info(da.make_problem(**base, sparse_batch=sb, sparse_heads=sh), 152)
         assert e.value.status == da.DA_ERR_INVALID_ARG
+
+
+def test_int4_groups_are_validated(lib):
+    """int4 rows: 4 or 8 groups run; 1 and 2 are the format's but unsupported
+    (rows not a multiple of 16 bytes); anything else is invalid."""
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim_qk=128, head_dim_v=128,
+                max_seq_len=256, kv_dtype=da.DA_DTYPE_INT4_GROUPS)
+    for g in (4, 8):
+        da.decode_attn_plan_info(da.make_problem(**base, kv_groups=g), 152)
+    for g, status in ((1, da.DA_ERR_UNSUPPORTED), (2, da.DA_ERR_UNSUPPORTED),
+                      (3, da.DA_ERR_INVALID_ARG), (0, da.DA_ERR_INVALID_ARG),
+                      (16, da.DA_ERR_INVALID_ARG)):
+        with pytest.raises(da.DecodeAttnError) as e:
+            da.decode_attn_plan_info(da.make_problem(**base, kv_groups=g), 152)
+        assert e.value.status == status

@@ -14,7 +14,7 @@ from helpers import assert_parity, reference, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 6, 7])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 6, 7, 8])
 def test_full_size_gqa_configs(cfg):
     w = W.config(cfg)
     out, lse, flags, eng = run_gpu(w)

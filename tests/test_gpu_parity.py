@@ -571,3 +571,49 @@ def test_broadcast_block_mask(shape, splits):
     if splits:
         assert flags2 == 0 and torch.equal(out, out2) and torch.equal(lse, lse2)
     eng.close()
+
+
+# ------------------------------------------------------------------ int4 group-wise K/V
+
+@pytest.mark.parametrize("groups", [4, 8])
+@pytest.mark.parametrize("layout,page", [("contiguous", 0), ("paged", 16), ("paged", 32),
+                                         ("paged", 128)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_int4_groups(groups, layout, page, splits):
+    lens = [1000, 17, 1, 300, 0, 64]
+    w = W.make_gqa(name="i4", batch=6, num_q_heads=16, num_kv_heads=2, seq_lens=lens,
+                   layout=layout, page_size=page or 16, cache_len=1024 if layout == "contiguous" else None,
+                   kv_int4_groups=groups, seed=510 + groups + page + splits)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"int4 g={groups} {layout}/{page} S={splits}")
+
+
+@pytest.mark.parametrize("group", [1, 4, 8, 16])
+def test_int4_group_sizes_and_two_n_tiles(group):
+    w = W.make_gqa(name="i4g", batch=3, num_q_heads=2 * group, num_kv_heads=2, seq_lens=[700, 65, 5],
+                   cache_len=704, kv_int4_groups=4, seed=530 + group)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=2)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"int4 G={group}")
+
+
+def test_int4_with_query_tokens_tree_softcap_and_sparse():
+    w = W.make_gqa(name="i4q", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[500, 2, 65],
+                   layout="paged", page_size=16, q_len=3, tree_mask=True, kv_int4_groups=8, seed=540)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=3, softcap=4.0)
+    assert flags == 0
+    ref_out, ref_lse = reference(w, softcap=4.0)
+    assert_parity(out, lse, ref_out, ref_lse, what="int4 q_len=3 tree softcap")
+    s = W.make_gqa(name="i4s", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[4096, 4000],
+                   cache_len=4096, sparse_block_size=128, kv_num_blks=[[5, 3], [0, 8]],
+                   kv_idx=[[[0, 3, 7, 9, 31, 0, 0, 0], [1, 2, 30, 0, 0, 0, 0, 0]],
+                           [[0] * 8, [4, 5, 6, 10, 11, 12, 29, 31]]],
+                   kv_int4_groups=4, seed=541)
+    for S in (0, 2):
+        out, lse, flags, _ = run_gpu(s, num_splits_override=S)
+        assert flags == 0
+        ref_out, ref_lse = reference(s)
+        assert_parity(out, lse, ref_out, ref_lse, what=f"int4 sparse S={S}")
