@@ -119,34 +119,21 @@ da_status encode_bf16_halves(CUtensorMap *map, const void *base, uint64_t rows, 
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
-// int4 group-wise rows viewed as int32 [rows][W] (W = groups + 16 words): the
-// 16 data words of `box_rows` rows, 64B-swizzled (the kernel loads at x = groups).
-da_status encode_int4_data(CUtensorMap *map, const void *base, uint64_t rows, uint32_t W,
-                           uint32_t box_rows) {
+// int4 group-wise rows (W = groups + 16 words each) viewed as 128-byte lines:
+// a box of `box_rows` consecutive rows is box_rows * W / 32 whole lines,
+// aligned, and lands as the rows are in the cache (unswizzled). The caller
+// keeps every box's first row a multiple of 32 / gcd(W, 32) rows.
+da_status encode_int4_lines(CUtensorMap *map, const void *base, uint64_t rows, uint32_t W,
+                            uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return DA_ERR_CUDA;
-  const cuuint64_t dims[2] = {W, rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)W * 4};
-  const cuuint32_t box[2] = {16u, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
-}
-
-// ... and their coefficient words: `groups` words of `box_rows` rows (x = 0).
-da_status encode_int4_coef(CUtensorMap *map, const void *base, uint64_t rows, uint32_t W,
-                           uint32_t groups, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return DA_ERR_CUDA;
-  const cuuint64_t dims[2] = {W, rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)W * 4};
-  const cuuint32_t box[2] = {groups, box_rows};
+  const cuuint64_t dims[2] = {32, rows * W / 32};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {32u, box_rows * W / 32};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
@@ -216,14 +203,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
     da_status st;
     if (int4) {
       const uint32_t W = (uint32_t)p.kv_groups + 16u;
-      if ((st = encode_int4_data(&ctx->kmap, a->k, rows, W, box_tokens)) != DA_OK) return st;
-      if ((st = encode_int4_data(&ctx->vmap, a->v, rows, W, box_tokens)) != DA_OK) return st;
-      if ((st = encode_int4_coef(&ctx->kssmap, a->k, rows, W, (uint32_t)p.kv_groups, box_tokens)) !=
-          DA_OK)
-        return st;
-      if ((st = encode_int4_coef(&ctx->vssmap, a->v, rows, W, (uint32_t)p.kv_groups, box_tokens)) !=
-          DA_OK)
-        return st;
+      if ((st = encode_int4_lines(&ctx->kmap, a->k, rows, W, box_tokens)) != DA_OK) return st;
+      if ((st = encode_int4_lines(&ctx->vmap, a->v, rows, W, box_tokens)) != DA_OK) return st;
     } else if (fp8) {
       // one 128-byte row per token
       if ((st = encode_rows(&ctx->kmap, a->k, false, rows, box_tokens)) != DA_OK) return st;
@@ -291,8 +272,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.sparse_batch = p.sparse_batch > 0 ? p.sparse_batch : std::max(p.batch, 1);
   gp.sparse_heads = p.sparse_heads > 0 ? p.sparse_heads : p.num_kv_heads;
   if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,
-                     token_scale || int4 ? ctx->kssmap : ctx->kmap,
-                     token_scale || int4 ? ctx->vssmap : ctx->vmap,
+                     token_scale ? ctx->kssmap : ctx->kmap, token_scale ? ctx->vssmap : ctx->vmap,
                      gp, pl.grid_x, stream) !=
       cudaSuccess)
     return DA_ERR_CUDA;

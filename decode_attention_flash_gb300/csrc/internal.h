@@ -42,8 +42,8 @@ struct GqaParams {
   float softcap_k;             // 2 / c: exp(2 x / c2) = exp2(x * softcap_k)
   int32_t batch, num_q_heads, num_kv_heads, group;  // num_q_heads, group: rows (heads x q_len)
   int32_t token_scale;         // e4m3 K/V with per-token scale words (maps kss / vss)
-  int32_t kv_groups;           // int4 group-wise K/V: groups per row (maps kss / vss read the
-                               // coefficient words, k / v the data words); 0 otherwise
+  int32_t kv_groups;           // int4 group-wise K/V: groups per row (whole rows of
+                               // groups + 16 words by maps k / v); 0 otherwise
   int32_t q_len;               // query tokens per row: token t of a unit row g * q_len + t
                                // sees the positions n <= seq_len - q_len + t
   int32_t paged, page_size, cache_len, max_pages, num_pages;

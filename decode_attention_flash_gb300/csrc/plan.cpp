@@ -39,6 +39,10 @@ da_status validate_problem(const da_problem *p) {
       return DA_ERR_INVALID_ARG;
     // rows of groups + 16 words: TMA strides them only when a multiple of 16 bytes
     if (p->kv_groups < 4) return DA_ERR_UNSUPPORTED;
+    // they travel as 128-byte lines: every tile's first row starts a line
+    // (80-byte rows: cache lengths a multiple of 8; 96-byte rows: of 4)
+    if (p->kv_layout == DA_KV_CONTIGUOUS && p->max_seq_len % (p->kv_groups == 4 ? 8 : 4) != 0)
+      return DA_ERR_UNSUPPORTED;
   }
   if (p->max_seq_len < 0 || p->q_len < 0) return DA_ERR_INVALID_ARG;
   const int Q = p->q_len > 1 ? p->q_len : 1;  // query tokens per row
