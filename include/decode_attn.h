@@ -127,7 +127,9 @@ typedef struct {
   int32_t sparse_batch;       /* sparse: block tables' batch extent SZ (0 = batch) */
   int32_t sparse_heads;       /* sparse: block tables' head extent SH (0 = num_kv_heads) */
   int32_t kv_groups;          /* DA_DTYPE_INT4_GROUPS: groups per row, 4 or 8 (rows of 1 or
-                                 2 groups are not a multiple of 16 bytes: unsupported) */
+                                 2 groups are not a multiple of 16 bytes: unsupported);
+                                 contiguous caches need max_seq_len a multiple of 8 (4
+                                 groups) or 4 (8 groups) */
 } da_problem;
 
 /*

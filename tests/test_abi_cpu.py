@@ -270,3 +270,12 @@ def test_int4_groups_are_validated(lib):
         with pytest.raises(da.DecodeAttnError) as e:
             da.decode_attn_plan_info(da.make_problem(**base, kv_groups=g), 152)
         assert e.value.status == status
+    # contiguous rows travel as 128-byte lines: L a multiple of 8 (4 groups) or 4 (8 groups)
+    for g, L, ok in ((4, 260, False), (4, 264, True), (8, 260, True), (8, 262, False)):
+        prob = da.make_problem(**dict(base, max_seq_len=L), kv_groups=g)
+        if ok:
+            da.decode_attn_plan_info(prob, 152)
+        else:
+            with pytest.raises(da.DecodeAttnError) as e:
+                da.decode_attn_plan_info(prob, 152)
+            assert e.value.status == da.DA_ERR_UNSUPPORTED
