@@ -28,7 +28,7 @@ def test_tiny_config_four_splits():
 
 
 @pytest.mark.parametrize("splits", [0, 1, 2, 5])
-@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
 def test_paged_ragged(splits, page_size):
     lens = [1, 17, 64, 65, 700, 1000, 0, 333]
     w = W.make_gqa(name="paged", batch=8, num_q_heads=32, num_kv_heads=8, seq_lens=lens,
@@ -63,6 +63,32 @@ def test_contiguous_group_sizes(group):
     assert flags == 0
     ref_out, ref_lse = reference(w)
     assert_parity(out, lse, ref_out, ref_lse, what=f"G={group}")
+
+
+@pytest.mark.parametrize("kind", ["paged", "contiguous", "sparse", "query_tokens", "int4", "mla"])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_every_row_empty(kind, splits):
+    """No row has a position, so the tile sequence is empty and no CTA streams:
+    every output row must still be written (zeros, LSE -inf; the buffers start
+    poisoned) and no error bit set."""
+    if kind == "mla":
+        w = W.make_mla(name="mla_empty", batch=3, seq_lens=[0, 0, 0], seed=61)
+    elif kind == "sparse":
+        w = W.make_gqa(name="sp_empty", batch=2, num_q_heads=8, num_kv_heads=2, seq_lens=[512, 300],
+                       cache_len=512, sparse_block_size=128, kv_num_blks=[[0, 0], [0, 0]],
+                       kv_idx=[[[0] * 4] * 2] * 2, seed=62)
+    else:
+        w = W.make_gqa(name=f"{kind}_empty", batch=5, num_q_heads=16, num_kv_heads=4, seq_lens=[0] * 5,
+                       layout="contiguous" if kind == "contiguous" else "paged", page_size=16,
+                       cache_len=256 if kind == "contiguous" else None,
+                       q_len=3 if kind == "query_tokens" else 1,
+                       kv_int4_groups=4 if kind == "int4" else 0, seed=63)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    assert torch.all(out == 0), f"{kind}: empty rows must be zero"
+    assert torch.all(lse == -float("inf")), f"{kind}: empty rows must have LSE -inf"
+    ref_out, ref_lse = reference(w)
+    assert np.all(ref_out == 0) and np.all(ref_lse == -np.inf)
 
 
 def test_lse_pointer_may_be_null():
