@@ -22,7 +22,7 @@ __all__ = [
     "decode_attn_plan", "decode_attn_plan_ex", "decode_attn_get_plan", "decode_attn_plan_info",
     "decode_attn_run", "decode_attn_run_noalloc", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
     "decode_attn_status_string", "DecodeAttention", "DA_KV_CONTIGUOUS", "DA_KV_PAGED",
-    "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3", "DA_DTYPE_FP8_E4M3_TOKEN_SCALE",
+    "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3", "DA_DTYPE_FP8_E4M3_TOKEN_SCALE", "DA_DTYPE_INT4_GROUPS",
 ]
 
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_CUDA = 0, 1, 2, 3
