@@ -34,6 +34,8 @@ struct da_ctx {
   CUtensorMap vssmap;
 };
 
+int da::ctx_device(const da_ctx *ctx) { return ctx->device; }
+
 namespace {
 
 using da::kWorkspaceHeader;

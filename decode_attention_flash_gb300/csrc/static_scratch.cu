@@ -59,14 +59,18 @@ extern "C" da_status decode_attn_run_noalloc(da_ctx *ctx, const da_args *args,
   if (plan.workspace_bytes > (int64_t)kNoAllocScratchBytes) return DA_ERR_WORKSPACE;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return DA_ERR_CUDA;
+  // the context's device must be current: the array's address is per device
+  if (device != da::ctx_device(ctx)) return DA_ERR_INVALID_ARG;
   void *scratch = nullptr;
   if ((st = scratch_address(device, &scratch)) != DA_OK) return st;
   // A call starts from a zero error word and zero counters, whatever the
   // previous call on this device left behind (an aborted call may leave its
-  // counters non-zero). The clear is an ordinary memset node on `stream`.
+  // counters non-zero): everything before the partial outputs is cleared (the
+  // counter region holds more than one word per unit: MLA counts per row and
+  // value half, GQA adds the group counters of its two-level merge). The clear
+  // is an ordinary memset node on `stream`.
   auto s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, (size_t)plan.counters_offset + (size_t)plan.num_units * 4, s) !=
-      cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, (size_t)plan.partial_o_offset, s) != cudaSuccess)
     return DA_ERR_CUDA;
   return decode_attn_run(ctx, args, scratch, kNoAllocScratchBytes, stream);
 }

@@ -309,7 +309,9 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
  * the array: calls whose work overlaps on the GPU (other streams, other
  * threads) race on it. Device-side error bits are not reported to the caller
  * (bad indices are still skipped on the device). A plan whose workspace
- * exceeds the array is refused with DA_ERR_WORKSPACE.
+ * exceeds the array is refused with DA_ERR_WORKSPACE, and a call made while
+ * another device than the context's is current with DA_ERR_INVALID_ARG
+ * (before anything is enqueued).
  * Errors: INVALID_ARG, NOT_PLANNED, WORKSPACE, UNSUPPORTED, CUDA.
  */
 #define DA_NOALLOC_SCRATCH_BYTES (32u << 20)
