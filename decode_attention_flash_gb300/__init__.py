@@ -120,9 +120,16 @@ def _check(status: int, what: str):
 
 
 def _ptr(t):
+    """Device pointer of a tensor argument. The library reads every tensor as
+    row-major device memory through the bare pointer, so host tensors and
+    strided views are refused here instead of being read as something else."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
+        if not t.is_cuda:
+            raise ValueError("tensor arguments must be in device memory (got a host tensor)")
+        if not t.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous (row-major, last index fastest)")
         return ctypes.c_void_p(t.data_ptr())
     return ctypes.c_void_p(int(t))
 

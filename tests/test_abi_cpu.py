@@ -279,3 +279,12 @@ def test_int4_groups_are_validated(lib):
             with pytest.raises(da.DecodeAttnError) as e:
                 da.decode_attn_plan_info(prob, 152)
             assert e.value.status == da.DA_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors_as_device_arguments():
+    # the library reads every tensor through a bare device pointer: a host
+    # tensor must be refused by the binding, not passed on as an address
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="device memory"):
+        da.make_args({"q": q}, 0.1, None, None)
+    assert da.make_args({}, 0.1, None, None).q is None
