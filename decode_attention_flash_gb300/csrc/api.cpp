@@ -34,7 +34,10 @@ struct da_ctx {
   CUtensorMap vssmap;
 };
 
-int da::ctx_device(const da_ctx *ctx) { return ctx->device; }
+namespace da {
+// The device a context was created for (its calls must run with it current).
+int ctx_device(const da_ctx *ctx) { return ctx->device; }
+}  // namespace da
 
 namespace {
 

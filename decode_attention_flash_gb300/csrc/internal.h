@@ -111,7 +111,4 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
                        int32_t num_splits_override, da_plan_info *info);
 da_status validate_problem(const da_problem *p);
 
-// The device a context was created for (its calls must run with it current).
-int ctx_device(const da_ctx *ctx);
-
 }  // namespace da

@@ -21,6 +21,11 @@
 
 #include "internal.h"
 
+namespace da {
+// The device a context was created for (defined beside the context in api.cpp).
+int ctx_device(const da_ctx *ctx);
+}  // namespace da
+
 namespace {
 
 // The largest workspace a plan may need to use this entry point.
