@@ -386,11 +386,17 @@ def run_ours(args, w, cfg):
         import oracle
         threads = oracle.default_threads()
         rows = pick_oracle_rows(w, target_s=10.0, threads=threads)
-        dt, frac = timed_oracle(w, rows, threads)
+        # a sample the oracle finishes quickly is evaluated again until about a
+        # second of wall time has gone by (the mean is reported)
+        dts = []
+        while not dts or (sum(dts) < 1.0 and len(dts) < 100):
+            dt, frac = timed_oracle(w, rows, threads)
+            dts.append(dt)
+        dt = statistics.mean(dts)
         cpu = {"value": ab["kv"] * frac / dt / 1e9, "unit": "GB/s", "cores": threads,
                "kind": "oracle",
                "sample": f"batch rows 0..{len(rows) - 1} of {w.batch} ({frac:.3f} of the KV bytes), "
-                         f"{dt:.1f} s wall"}
+                         f"mean of {len(dts)} runs of {dt:.2f} s wall"}
 
     kname = "mla_split_kernel" if w.is_mla else "gqa_split_kernel"
     if w.is_mla:
