@@ -815,3 +815,31 @@ def test_threads_do_not_change_results():
     a = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=1)
     b = oracle.decode(oracle.problem_from(w), w.tensors, w.scale, num_threads=7)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_int4_row_from_hand_encoded_words():
+    # tests/golden/int4_row.txt: coefficient and data words written out by
+    # hand; with one key the oracle's output row is that value row exactly
+    words, probes = None, []
+    with open(os.path.join(GOLDEN, "int4_row.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            if line.startswith("words"):
+                words = [int(x, 16) for x in line.split()[1:]]
+            else:
+                i, v = line.split()
+                probes.append((int(i), float(v)))
+    assert words is not None and len(words) == 4 + 64 // 8 and len(probes) == 16
+    row = [x - (1 << 32) if x >= (1 << 31) else x for x in words]
+    zero_key = [0] * 4 + [0] * 8  # scale 0, shift 0, codes 0: a zero key
+    k = torch.tensor([[[zero_key]]], dtype=torch.int32)
+    v = torch.tensor([[[row]]], dtype=torch.int32)
+    q = torch.ones((1, 1, 64), dtype=torch.bfloat16)
+    prob = dict(batch=1, num_q_heads=1, num_kv_heads=1, head_dim_qk=64, head_dim_v=64,
+                cache_len=1, kv_fp8=3, kv_groups=4)
+    out, lse = oracle.decode(prob, dict(q=q, k=k, v=v, seq_lens=torch.tensor([1])), 0.1)
+    for i, want in probes:
+        assert out[0, 0, i] == want, (i, out[0, 0, i], want)
+    assert lse[0, 0] == 0.0  # one key with score 0
