@@ -397,6 +397,12 @@ def run_ours(args, w, cfg):
                "kind": "oracle",
                "sample": f"batch rows 0..{len(rows) - 1} of {w.batch} ({frac:.3f} of the KV bytes), "
                          f"mean of {len(dts)} runs of {dt:.2f} s wall"}
+        # the same oracle on one core, over its own bounded sample (~3 s)
+        rows1 = pick_oracle_rows(w, target_s=3.0, threads=1)
+        dt1, frac1 = timed_oracle(w, rows1, 1)
+        cpu["single_core"] = {"value": ab["kv"] * frac1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"batch rows 0..{len(rows1) - 1} of {w.batch} "
+                                        f"({frac1:.3f} of the KV bytes), {dt1:.2f} s wall"}
 
     kname = "mla_split_kernel" if w.is_mla else "gqa_split_kernel"
     if w.is_mla:
