@@ -45,7 +45,6 @@ namespace da {
 namespace {
 
 constexpr int kTile = 64;             // tokens per pipeline stage
-constexpr int kIdAhead = 8;           // tiles whose page / block ids are fetched ahead (ids <= 32)
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
 // A sixth warp takes the row-counter atomics of partial segments off the
 // consumers and merges small units while they stream.
@@ -97,8 +96,7 @@ struct Cfg {
   // 16-token page box takes 32 words), and the per-warp sums of p * shift of
   // the value rows ([warp][16])
   static constexpr int kSSWords = 2 * kTile;
-  static constexpr int oIds = oMergeBar + 4 * 8;             // page / block id queue (32 ints)
-  static constexpr int oSS = (oIds + 32 * 4 + 127) & ~127;
+  static constexpr int oSS = (oMergeBar + 4 * 8 + 127) & ~127;
   static constexpr int kSSBytes = TOK ? kStages * 2 * kSSWords * 4 : 0;
   static constexpr int oStatZ = oSS + kSSBytes;
   static constexpr int kTotal = oStatZ + (TOK ? kConsumerWarps * 16 * 4 : 0) + 1024;  // + slack
@@ -730,7 +728,6 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = smem + C::oRing;
   uint8_t *qslots = smem + C::oQ;
-  int *idq = reinterpret_cast<int *>(smem + C::oIds);
   float *red = reinterpret_cast<float *>(smem + C::oRed);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oFull);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + C::oEmpty);
@@ -865,32 +862,26 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     if (reorder) set_at(cur, last_u, 0, last_P);
     else set_at(cur, start_u, start_j, start_P);
     cur.wi = 0;
-    // Page (paged) or block (sparse) id number k of a tile: where it sits in
-    // the tables (null when the tile has no such page), and its check when it
-    // is used (-1 when absent or invalid; an invalid one also sets its error
-    // bit and is skipped).
-    auto id_src = [&](const TileDesc &d, int k) -> const int32_t * {
+    // Page (paged) or block (sparse) id number k of a tile; -1 when absent or
+    // invalid (an invalid one also sets its error bit and is skipped). The
+    // check is a select, not a branch, so the lookahead's loads stay in flight
+    // together instead of each waiting for the one before.
+    auto load_id = [&](const TileDesc &d, int k) -> int {
       if (p.sparse_block_size > 0) {
         const int e = d.j / (p.sparse_block_size / kTile);
         // list entry e: the first table's, then the full table's
-        return e < d.nbp ? p.kv_idx + (int64_t)d.trow * p.max_sparse_blocks + e
-                         : p.kv_full_idx + (int64_t)d.trow * p.max_sparse_blocks + e - d.nbp;
-      }
-      const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
-      if (tok0 >= d.n_valid) return nullptr;
-      return p.block_table + (int64_t)d.b * p.max_pages + tok0 / P;
-    };
-    auto check_id = [&](const TileDesc &d, int k, int raw) -> int {
-      if (p.sparse_block_size > 0) {
-        const bool bad = raw < 0 || (int64_t)raw * p.sparse_block_size >= p.cache_len;
+        const int blk = e < d.nbp ? p.kv_idx[(int64_t)d.trow * p.max_sparse_blocks + e]
+                                  : p.kv_full_idx[(int64_t)d.trow * p.max_sparse_blocks + e - d.nbp];
+        const bool bad = blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len;
         dev_err |= bad ? DA_DEVERR_SPARSE_INDEX : 0u;
-        return bad ? -1 : raw;
+        return bad ? -1 : blk;
       }
       const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
       if (tok0 >= d.n_valid) return -1;
-      const bool bad = raw < 0 || raw >= p.num_pages;
+      const int page = p.block_table[(int64_t)d.b * p.max_pages + tok0 / P];
+      const bool bad = page < 0 || page >= p.num_pages;
       dev_err |= bad ? DA_DEVERR_PAGE_INDEX : 0u;
-      return bad ? -1 : raw;
+      return bad ? -1 : page;
     };
     auto advance = [&](TileDesc &d) {
       if (++d.wi == i_jump) {
@@ -917,23 +908,24 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;
     };
 
-    // Ids are fetched kIdAhead tiles before they are used, by 4-byte cp.async
-    // into a queue in shared memory (slot t % kIdAhead holds the L ids of tile
-    // t): no register waits on a table load in flight, so one tile's lookup
-    // never holds up the next tile's issue. Lanes 0 .. L-1 copy, one commit
-    // group per tile.
+    // Ids are looked up kAhead tiles before they are used, in a queue that
+    // lives in the warp's lanes: lanes k*L .. k*L+L-1 hold the L ids of the
+    // k-th next tile (L ids per tile: pages of a tile, or one block / page).
     const bool needs_ids = p.paged || p.sparse_block_size > 0;
     const int L = pages_per_tile;
+    const int ahead_n = min(8, 32 / L);  // tiles in flight in the queue
+    int idq = -1;
     TileDesc ahead = cur;
     if (needs_ids) {
-      for (int k = 0; k < kIdAhead; ++k) {
-        if (k < ntiles && lane < L) {
-          const int32_t *src = id_src(ahead, lane);
-          if (src) cp_async_4(idq + k * L + lane, src);
-        }
-        cp_async_commit();
+      // walk the first ahead_n tiles, each lane group keeping its tile, then
+      // load every lane's id at once (one load in flight per lane)
+      TileDesc mine = ahead;
+      const int my_k = lane / L;
+      for (int k = 0; k < ahead_n && k < ntiles; ++k) {
+        if (k == my_k) mine = ahead;
         if (k + 1 < ntiles) advance(ahead);
       }
+      if (my_k < ahead_n && my_k < ntiles) idq = load_id(mine, lane - my_k * L);
     }
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
@@ -946,18 +938,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         if (lane == 0) flags[0] = 1;
         break;
       }
-      const int *ids = idq + (i % kIdAhead) * L;  // this tile's ids
-      if (needs_ids) {
-        cp_async_wait_group<kIdAhead - 1>();  // this lane's copies for tile i have landed
-        __syncwarp();                         // and so have the other lanes'
-      }
+      const int id_cur = idq;  // lanes 0 .. L-1: this tile's ids
       // ---- this tile's boxes (y = first cache row of the box)
       uint64_t valid = 0;
       int nbox = 0;
       int ys[kTile / 16];
       const int tok_base = cur.j * kTile;
       if (p.sparse_block_size > 0) {
-        const int blk = check_id(cur, 0, ids[0]);
+        const int blk = __shfl_sync(0xffffffffu, id_cur, 0);
         if (blk >= 0) {
           const int tb = blk * p.sparse_block_size + (cur.j % (p.sparse_block_size / kTile)) * kTile;
           const int lim = min(min(cur.n_valid - tb, kTile), p.cache_len - tb);
@@ -973,7 +961,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         ys[0] = (int)(((int64_t)cur.unit * p.cache_len + tok_base) );
         nbox = 1;
       } else if (P >= kTile) {
-        const int page = check_id(cur, 0, ids[0]);
+        const int page = __shfl_sync(0xffffffffu, id_cur, 0);
         if (page >= 0) {
           valid = low_bits(min(cur.n_valid - tok_base, kTile));
           ys[0] = (int)((((int64_t)page * p.num_kv_heads + cur.h) * P + tok_base % P) );
@@ -981,7 +969,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         }
       } else {
         for (int k = 0; k < kTile / P; ++k) {
-          const int page = check_id(cur, k, ids[k]);
+          const int page = __shfl_sync(0xffffffffu, id_cur, k);
           ys[k] = -1;
           if (page >= 0) {
             valid |= low_bits(min(cur.n_valid - (tok_base + k * P), P)) << (k * P);
@@ -1070,21 +1058,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
                       (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
       }
-      // fetch the ids of tile i + kIdAhead into the slot just read
+      // shift the id queue by one tile and look up tile i + ahead_n
       if (needs_ids) {
-        __syncwarp();  // every lane has read this tile's ids
-        if (i + kIdAhead < ntiles) {
-          if (lane < L) {
-            const int32_t *src = id_src(ahead, lane);
-            if (src) cp_async_4(idq + (i % kIdAhead) * L + lane, src);
-          }
-          if (i + kIdAhead + 1 < ntiles) advance(ahead);
+        idq = __shfl_down_sync(0xffffffffu, idq, L);
+        if (i + ahead_n < ntiles) {
+          if (lane >= (ahead_n - 1) * L && lane < ahead_n * L)
+            idq = load_id(ahead, lane - (ahead_n - 1) * L);
+          if (i + ahead_n + 1 < ntiles) advance(ahead);
         }
-        cp_async_commit();
       }
       if (i + 1 < ntiles) advance(cur);
     }
-    if (needs_ids) cp_async_wait_group<0>();  // no copy outlives the loop (a timeout leaves early)
   } else if (warp > kConsumerWarps) {
     // ======================================================= helper (kHelper only)
     // Counts this range's partial segments as the consumers finish them and,

@@ -643,3 +643,30 @@ def test_int4_with_query_tokens_tree_softcap_and_sparse():
         assert flags == 0
         ref_out, ref_lse = reference(s)
         assert_parity(out, lse, ref_out, ref_lse, what=f"int4 sparse S={S}")
+
+
+# ------------------------------------------------------------------ large batches of short rows
+
+def test_mla_batch_larger_than_the_block():
+    # 400 rows: the prologue walks the batch in chunks of the block's 384
+    # threads, carrying the tile offset from one chunk to the next
+    g = torch.Generator().manual_seed(71)
+    lens = torch.randint(0, 300, (400,), generator=g).tolist()
+    lens[5] = lens[399] = 0
+    w = W.make_mla(name="mla_big", batch=400, seq_lens=lens, seed=72)
+    out, lse, flags, _ = run_gpu(w)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="MLA B=400")
+
+
+def test_gqa_thousands_of_units():
+    # 1000 rows x 8 kv heads: each prologue thread scans ~42 units
+    g = torch.Generator().manual_seed(74)
+    lens = torch.randint(0, 200, (1000,), generator=g).tolist()
+    w = W.make_gqa(name="gqa_big", batch=1000, num_q_heads=32, num_kv_heads=8, seq_lens=lens,
+                   layout="paged", page_size=16, seed=73)
+    out, lse, flags, _ = run_gpu(w)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="GQA B=1000")
