@@ -105,6 +105,9 @@ def load(build_if_missing: bool = False):
         "decode_attn_get_error": (st, [vp, vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "decode_attn_destroy": (None, [vp]),
         "decode_attn_status_string": (ctypes.c_char_p, [st]),
+        # test hooks (include/decode_attn_testing.h)
+        "decode_attn_test_fill_smem": (st, [ctypes.c_uint32, i32, vp]),
+        "decode_attn_test_set_stall": (st, [vp, ctypes.c_uint32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)

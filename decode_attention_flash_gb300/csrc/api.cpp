@@ -32,11 +32,16 @@ struct da_ctx {
   const void *map_vss_base;
   CUtensorMap kssmap;
   CUtensorMap vssmap;
+  // tests of the timeout path (decode_attn_testing.h): the stall of the next run
+  uint32_t test_stall_ns;
 };
 
 namespace da {
 // The device a context was created for (its calls must run with it current).
 int ctx_device(const da_ctx *ctx) { return ctx->device; }
+// Arms the test stall of the context's next GQA run (decode_attn_testing.h).
+void ctx_set_test_stall(da_ctx *ctx, uint32_t ns) { ctx->test_stall_ns = ns; }
+bool ctx_is_mla(const da_ctx *ctx) { return ctx->prob.is_mla != 0; }
 }  // namespace da
 
 namespace {
@@ -276,6 +281,8 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.max_sparse_blocks = p.max_sparse_blocks;
   gp.sparse_batch = p.sparse_batch > 0 ? p.sparse_batch : std::max(p.batch, 1);
   gp.sparse_heads = p.sparse_heads > 0 ? p.sparse_heads : p.num_kv_heads;
+  gp.test_stall_ns = ctx->test_stall_ns;
+  ctx->test_stall_ns = 0;  // one call only
   if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,
                      token_scale ? ctx->kssmap : ctx->kmap, token_scale ? ctx->vssmap : ctx->vmap,
                      gp, pl.grid_x, stream) !=

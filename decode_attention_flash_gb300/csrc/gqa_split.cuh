@@ -86,20 +86,26 @@ struct Cfg {
   static constexpr int oFull = oRed + kRedBytes;
   static constexpr int oEmpty = oFull + 8 * kStages;
   static constexpr int oMeta = oEmpty + 8 * kStages;
-  static constexpr int oStats = oMeta + 32 * kStages;        // m, l per (warp, g)
-  static constexpr int oScan = oStats + 2 * kConsumerWarps * 16 * 4;
+  // m, l per (warp, g), two copies: segment k's epilogue uses copy k & 1, so a
+  // warp that has finished segment k and reaches segment k + 1's epilogue never
+  // overwrites what another warp still reads for segment k (a warp with no
+  // valid token in a short segment gets there quickly)
+  static constexpr int kStatFloats = 2 * kConsumerWarps * 16;
+  static constexpr int oStats = oMeta + 32 * kStages;
+  static constexpr int oScan = oStats + 2 * kStatFloats * 4;
   static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
-  static constexpr int oMergeBar = oFlags + 32 * 4;          // 2 mbarriers of the merge staging,
-                                                             // 2 partial-segment
+  static constexpr int oMergeBar = oFlags + 32 * 4;          // mbarriers: 2 of the merge staging,
+                                                             // 2 partial-segment, 1 epilogue,
+                                                             // 1 never arrived on (test stall)
   // e4m3 with per-token scales: [stage][K|V][kSSWords] scale words (TMA
   // destinations: 128-byte aligned, each box at a multiple of 128 bytes, so a
   // 16-token page box takes 32 words), and the per-warp sums of p * shift of
   // the value rows ([warp][16])
   static constexpr int kSSWords = 2 * kTile;
-  static constexpr int oSS = (oMergeBar + 4 * 8 + 127) & ~127;
+  static constexpr int oSS = (oMergeBar + 6 * 8 + 127) & ~127;
   static constexpr int kSSBytes = TOK ? kStages * 2 * kSSWords * 4 : 0;
-  static constexpr int oStatZ = oSS + kSSBytes;
-  static constexpr int kTotal = oStatZ + (TOK ? kConsumerWarps * 16 * 4 : 0) + 1024;  // + slack
+  static constexpr int oStatZ = oSS + kSSBytes;                // [2 copies][warp][16]
+  static constexpr int kTotal = oStatZ + (TOK ? 2 * kConsumerWarps * 16 * 4 : 0) + 1024;  // + slack
   static_assert(oSS % 128 == 0 && (2 * kSSWords * 4) % 128 == 0, "TMA destinations need 128 B");
   static_assert(oQ % 128 == 0 && kQSlot % 128 == 0 && kTileBytes % 128 == 0, "TMA destinations");
   static_assert(!I4 || (FP8 && !TOK), "int4 rows take the f16 operand path and their own scales");
@@ -135,6 +141,23 @@ __device__ __forceinline__ float cap_tanh(float x, float c2, float k) {
 
 __device__ __forceinline__ uint64_t low_bits(int n) {
   return n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+}
+
+// Warp-uniform outcome of a bounded wait (every lane then takes the same path).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, limit_ns));
+}
+
+// Barrier of the consumer warps on an mbarrier of kConsumerWarps * 32 arrivals:
+// each consumer thread arrives and waits, bounded, for the phase (release /
+// acquire at CTA scope, like bar.sync for shared memory). A warp whose wait
+// runs out returns false instead of waiting forever for a warp that left the
+// stream after a failed wait of its own.
+__device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &phase) {
+  mbar_arrive(bar);
+  const bool ok = warp_wait(bar, phase, kWaitLimitNs);
+  phase ^= 1u;
+  return ok;
 }
 
 // ------------------------------------------------------------------ units and the schedule
@@ -732,11 +755,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::oFull);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + C::oEmpty);
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + C::oMeta);
-  float *stat_m = reinterpret_cast<float *>(smem + C::oStats);
-  float *stat_l = stat_m + kConsumerWarps * 16;
+  float *stats = reinterpret_cast<float *>(smem + C::oStats);  // [2 copies][m | l][warp][16]
   int *scan = reinterpret_cast<int *>(smem + C::oScan);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + C::oFlags);
-  // flags: [0] abort, [2] start unit, [3] start tile, [4..5] start P (int64),
+  // flags: [0] abort, [1] tiles the producer issued, [2] start unit, [3] start
+  //        tile, [4..5] start P (int64),
   //        [12] merges owed after the stream, [13] scratch, [24..31] those merges
   //        (unit, c_first, n_seg, group),
   //        [14..19] the range's partial segments (unit, c_first, n_seg) handed to
@@ -744,6 +767,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   //        its segment here is partial, [22..23] its first tile (int64)
   uint64_t *merge_bar = reinterpret_cast<uint64_t *>(smem + C::oMergeBar);
   uint64_t *part_bar = merge_bar + 2;  // [2] a partial segment is in global memory
+  uint64_t *epi_bar = merge_bar + 4;   // the consumer warps' segment-epilogue barrier
+  uint64_t *stall_bar = merge_bar + 5; // nothing arrives on it (the test stall of GqaParams)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
@@ -757,6 +782,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   // (their lengths now in L1) finds the range's first and last unit.
   if (threadIdx.x == 0) {
     flags[0] = 0;
+    flags[1] = 0;
     flags[2] = -1;
     flags[12] = 0;
   }
@@ -816,6 +842,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     mbar_init(&merge_bar[1], 1);
     mbar_init(&part_bar[0], kConsumerWarps * 32);
     mbar_init(&part_bar[1], kConsumerWarps * 32);
+    mbar_init(epi_bar, kConsumerWarps * 32);
+    mbar_init(stall_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -927,6 +955,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       }
       if (my_k < ahead_n && my_k < ntiles) idq = load_id(mine, lane - my_k * L);
     }
+    int issued = 0;  // tiles whose copies are issued (the drain after a timeout waits for them)
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
       bool ok = true;
@@ -1067,8 +1096,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           if (i + ahead_n + 1 < ntiles) advance(ahead);
         }
       }
+      issued = i + 1;
       if (i + 1 < ntiles) advance(cur);
     }
+    if (lane == 0) flags[1] = issued;
   } else if (warp > kConsumerWarps) {
     // ======================================================= helper (kHelper only)
     // Counts this range's partial segments as the consumers finish them and,
@@ -1148,10 +1179,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       for (int ks = 0; ks < 8; ++ks) qf[nt][ks][0] = qf[nt][ks][1] = 0u;
     bool ok = true;
     int npart = 0;  // partial segments written so far
+    int nseg = 0;   // segments finished so far (their parity picks the stats copy)
+    uint32_t epi_phase = 0;
 
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
-      if (!mbar_wait_bounded(&full[st], (i / C::kStages) & 1, kWaitLimitNs)) {
+      // (the test stall of GqaParams replaces the first wait of warp 0 by one on
+      // a barrier that nothing arrives on, with the stall's limit: the timeout
+      // path then runs as it would after a real failure)
+      const bool stall = p.test_stall_ns != 0 && i == 0 && warp == 0;
+      if (!warp_wait(stall ? stall_bar : &full[st], stall ? 0u : (uint32_t)((i / C::kStages) & 1),
+                     stall ? (uint64_t)p.test_stall_ns : kWaitLimitNs)) {
         ok = false;
         break;
       }
@@ -1500,6 +1538,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       // ======================= segment epilogue (consumer threads only)
       // (the segment's last stage is released at its end: it may serve as scratch)
       const int b = unit / p.num_kv_heads, h = unit - b * p.num_kv_heads;
+      float *stat_m = stats + (nseg & 1) * C::kStatFloats;  // this segment's copy
+      float *stat_l = stat_m + kConsumerWarps * 16;
+      float *stat_z = reinterpret_cast<float *>(smem + C::oStatZ) + (nseg & 1) * kConsumerWarps * 16;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1520,10 +1561,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             const int g = nt * 8 + 2 * q4 + e;
             stat_m[warp * 16 + g] = m_run[nt][e];
             stat_l[warp * 16 + g] = l;
-            if (tok_scale) reinterpret_cast<float *>(smem + C::oStatZ)[warp * 16 + g] = z;
+            if (tok_scale) stat_z[warp * 16 + g] = z;
           }
         }
-      named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+      if (!consumer_sync(epi_bar, epi_phase)) {
+        ok = false;
+        break;
+      }
       // each warp's O^T rescaled to the group maximum: into its own region of the
       // consumed stage when it fits (one barrier), else added into one buffer
       // one warp at a time
@@ -1564,13 +1608,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       };
       if (C::kStageScratch) {
         put(scr + warp * kWarpScr, false);
-        named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+        ok = consumer_sync(epi_bar, epi_phase);
       } else {
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < kConsumerWarps && ok; ++w) {
           if (warp == w) put(red, w > 0);
-          named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
+          ok = consumer_sync(epi_bar, epi_phase);
         }
       }
+      if (!ok) break;
       // thread tid (< 128) owns head-dim element d = tid for every g of the group
       const int d = threadIdx.x;
       const bool whole = m.n_seg == 1;
@@ -1593,7 +1638,6 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           acc = red[(size_t)g * kRedStride + d];
         }
         if (tok_scale) {  // the value shifts: the same term for every element of the row
-          const float *stat_z = reinterpret_cast<const float *>(smem + C::oStatZ);
 #pragma unroll
           for (int w = 0; w < kConsumerWarps; ++w)
             acc += (M == neg_inf()) ? 0.f : stat_z[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
@@ -1615,20 +1659,16 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
       if (!whole) {
-        if (kHelper) {
-          // the helper counts the segment (its writes are released by the arrivals)
-          if (threadIdx.x == 0) {
-            flags[14 + 3 * npart] = unit;
-            flags[15 + 3 * npart] = m.c_first;
-            flags[16 + 3 * npart] = m.n_seg;
-          }
-          mbar_arrive(&part_bar[npart & 1]);
-        } else {
-          named_barrier_sync(kConsumerBar, kConsumerWarps * 32);
-          if (threadIdx.x == 0) count_piece(p, flags, unit, m.c_first, m.n_seg, false);
+        // the helper warp counts the segment (its writes are released by the arrivals)
+        if (threadIdx.x == 0) {
+          flags[14 + 3 * npart] = unit;
+          flags[15 + 3 * npart] = m.c_first;
+          flags[16 + 3 * npart] = m.n_seg;
         }
+        mbar_arrive(&part_bar[npart & 1]);
         ++npart;
       }
+      ++nseg;
       reset();
     }
     if (!ok) {
@@ -1641,10 +1681,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   // has recorded every merge this CTA owes
   __syncthreads();
   if (flags[0]) {
-    // a wait gave up: drain copies still in flight (bounded) before leaving
+    // a wait gave up: before leaving, wait (bounded) for the copies of every
+    // tile the producer issued -- the last one of each stage (a stage's earlier
+    // uses completed before it was refilled). Tiles never issued are not waited
+    // for: their phase was never armed.
     if (threadIdx.x == kConsumerWarps * 32) {
-      for (int st = 0; st < C::kStages && st < ntiles; ++st) {
-        const int i_last = (ntiles - 1) - ((ntiles - 1 - st) % C::kStages);
+      const int issued = flags[1];
+      for (int st = 0; st < C::kStages && st < issued; ++st) {
+        const int i_last = (issued - 1) - ((issued - 1 - st) % C::kStages);
         mbar_wait_bounded(&full[st], (i_last / C::kStages) & 1, kWaitLimitNs);
       }
     }

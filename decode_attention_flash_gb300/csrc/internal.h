@@ -50,6 +50,9 @@ struct GqaParams {
   int32_t capacity;            // max positions per row
   int32_t sparse_block_size, max_sparse_blocks;
   int32_t sparse_batch, sparse_heads;  // block tables' extents (row (b % SZ, h % SH))
+  uint32_t test_stall_ns;      // 0; else (tests of the timeout path only) the first
+                               // pipeline wait of consumer warp 0 is one on a barrier
+                               // that nothing arrives on, given up after this long
 };
 
 // Group counters per GQA unit for the two-level merge of a unit cut into many

@@ -28,8 +28,10 @@ int ctx_device(const da_ctx *ctx);
 
 namespace {
 
-// The largest workspace a plan may need to use this entry point.
-constexpr size_t kNoAllocScratchBytes = 32ull << 20;
+// The largest workspace a plan may need to use this entry point (the header's
+// DA_NOALLOC_SCRATCH_BYTES).
+constexpr size_t kNoAllocScratchBytes = DA_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes == (32ull << 20), "the header documents 32 MiB");
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

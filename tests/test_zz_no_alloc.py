@@ -26,7 +26,7 @@ def _case():
 
 def _run(lib, ctx, w, t, noalloc):
     dev = t["q"].device
-    out = torch.full((w.batch, w.num_q_heads, 128), 3.0, dtype=torch.bfloat16, device=dev)
+    out = torch.full((w.batch, w.num_q_heads, w.head_dim_v), 3.0, dtype=torch.bfloat16, device=dev)
     lse = torch.full((w.batch, w.num_q_heads), 3.0, dtype=torch.float32, device=dev)
     args = da.make_args(t, w.scale, out, lse)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -59,6 +59,30 @@ def test_noalloc_matches_workspace_entry_point_twice():
             assert float((lse - ref_lse).abs().max()) <= LSE_ATOL
     finally:
         da.decode_attn_destroy(ctx)
+
+
+def test_noalloc_back_to_back_shapes_are_bitwise_the_workspace_entry_point():
+    """An MLA problem (its counters are per row and value half) and a second GQA
+    shape with another unit count, run back to back on the shared static array:
+    the same kernel on the same plan as decode_attn_run, so the same bits."""
+    lib = da.load()
+    cases = [
+        W.make_mla(name="noalloc_mla", batch=5, seq_lens=[700, 0, 64, 3000, 129], seed=33),
+        W.make_gqa(name="noalloc_gqa2", batch=9, num_q_heads=16, num_kv_heads=4,
+                   seq_lens=[90, 2500, 1, 640, 0, 1800, 77, 4096, 333], layout="paged",
+                   page_size=32, seed=34),
+    ]
+    for w in cases + cases:  # each shape twice, alternating
+        t = w.to("cuda")
+        ctx = da.decode_attn_create(da.make_problem(**da.problem_kwargs(w)), 0)
+        try:
+            da.decode_attn_plan(ctx, w.tensors["seq_lens"], 0)
+            ref_out, ref_lse = _run(lib, ctx, w, t, noalloc=False)
+            out, lse = _run(lib, ctx, w, t, noalloc=True)
+            assert torch.equal(out, ref_out), w.name
+            assert torch.equal(lse.nan_to_num(neginf=-1e30), ref_lse.nan_to_num(neginf=-1e30)), w.name
+        finally:
+            da.decode_attn_destroy(ctx)
 
 
 def test_noalloc_refuses_a_plan_beyond_the_static_scratch():
