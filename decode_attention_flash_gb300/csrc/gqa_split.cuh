@@ -289,10 +289,34 @@ __device__ __forceinline__ uint32_t i4_dequant(uint32_t codes, uint32_t scale2, 
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+// A bf16 pair times the power of two `s` (exact), rounded to an f16 pair.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float s) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&x);
   float2 f = __bfloat1622float2(v);
-  return pack_f16(f.x, f.y);
+  return pack_f16(f.x * s, f.y * s);
+}
+
+// 2^e as a float, for -126 <= e <= 127.
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// max|q| over this lane's quarter of a query row (the four lanes of a quad
+// share the row; each reads 16 of its 64 words, rotated by the row so that the
+// eight rows' reads fall in different banks).
+__device__ __forceinline__ float q_row_amax(const uint32_t *qrow, int q4, int r8) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t w = qrow[q4 * 16 + ((j + r8) & 15)];
+    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u))));
+  }
+  return amax;
+}
+
+// Exponent e of the power of two that puts `amax` in [2^14, 2^15) (0 for zero),
+// at most 100 (an all-but-zero query stays far below f16's largest value).
+__device__ __forceinline__ int q_exponent(float amax) {
+  const int lg = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2), normal amax
+  return amax > 0.f ? min(14 - lg, 100) : 0;
 }
 
 // Merge of one unit's segments (slots unit + c_first .. unit + c_first + n_seg
@@ -1182,14 +1206,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     int nseg = 0;   // segments finished so far (their parity picks the stats copy)
     uint32_t epi_phase = 0;
 
-    for (int i = 0; i < ntiles; ++i) {
+    // (the test stall of GqaParams: warp 0 waits on a barrier that nothing
+    // arrives on, with the stall's limit, instead of its first pipeline wait;
+    // the timeout path then runs as it would after a real failure)
+    if (p.test_stall_ns != 0 && warp == 0) ok = warp_wait(stall_bar, 0u, p.test_stall_ns);
+    for (int i = 0; ok && i < ntiles; ++i) {
       const int st = i % C::kStages;
-      // (the test stall of GqaParams replaces the first wait of warp 0 by one on
-      // a barrier that nothing arrives on, with the stall's limit: the timeout
-      // path then runs as it would after a real failure)
-      const bool stall = p.test_stall_ns != 0 && i == 0 && warp == 0;
-      if (!warp_wait(stall ? stall_bar : &full[st], stall ? 0u : (uint32_t)((i / C::kStages) & 1),
-                     stall ? (uint64_t)p.test_stall_ns : kWaitLimitNs)) {
+      if (!warp_wait(&full[st], (i / C::kStages) & 1, kWaitLimitNs)) {
         ok = false;
         break;
       }
@@ -1199,6 +1222,24 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         // the segment's query group: Q^T fragments (B operand), read once per segment
         const int h = unit % p.num_kv_heads;
         const uint32_t *qs = reinterpret_cast<const uint32_t *>(qslots + st * C::kQSlot);
+        // e4m3 / int4 keys meet Q in f16. The segment's query rows are scaled by
+        // an exact power of two 2^e that puts their largest |q| in [2^14, 2^15),
+        // so every finite bf16 q lands in f16's range (an element more than 2^28
+        // below that largest one becomes an f16 subnormal: an error under 2^-28
+        // of the largest product), and 2^-e joins the score factor.
+        int qexp = 0;
+        if (FP8) {
+          float amax = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 8 + r8;
+            amax = fmaxf(amax, q_row_amax(qs + (g < G ? g : 0) * (kD / 2), q4, r8));
+          }
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          qexp = q_exponent(amax);
+        }
+        const float q2 = pow2f(qexp);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int g = nt * 8 + r8;
@@ -1210,9 +1251,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
               // 32c + 8q4 + 2s + {0, 4} (b0) and 32c + 8q4 + 2s + 1 + {0, 4} (b1)
               const __nv_bfloat16 *qh = reinterpret_cast<const __nv_bfloat16 *>(qrow);
               const int d0 = 32 * (ks >> 1) + 8 * q4 + 2 * (ks & 1);
-              qf[nt][ks][0] = g < G ? pack_f16(__bfloat162float(qh[d0]), __bfloat162float(qh[d0 + 4])) : 0u;
+              qf[nt][ks][0] =
+                  g < G ? pack_f16(__bfloat162float(qh[d0]) * q2, __bfloat162float(qh[d0 + 4]) * q2) : 0u;
               qf[nt][ks][1] =
-                  g < G ? pack_f16(__bfloat162float(qh[d0 + 1]), __bfloat162float(qh[d0 + 5])) : 0u;
+                  g < G ? pack_f16(__bfloat162float(qh[d0 + 1]) * q2, __bfloat162float(qh[d0 + 5]) * q2)
+                        : 0u;
             } else if (!FP8) {
               qf[nt][ks][0] = g < G ? qrow[(16 * ks + 2 * q4) / 2] : 0u;
               qf[nt][ks][1] = g < G ? qrow[(16 * ks + 8 + 2 * q4) / 2] : 0u;
@@ -1220,8 +1263,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
               // k-step 2pp+e covers bytes 32pp + 16e + 4q4 .. +3 of each fp8 key row
               const int pp = ks >> 1, e = ks & 1;
               const int d0 = 32 * pp + 16 * e + 4 * q4;
-              qf[nt][ks][0] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2]) : 0u;
-              qf[nt][ks][1] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2 + 1]) : 0u;
+              qf[nt][ks][0] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2], q2) : 0u;
+              qf[nt][ks][1] = g < G ? bf16x2_to_f16x2(qrow[d0 / 2 + 1], q2) : 0u;
             }
           }
         }
@@ -1248,7 +1291,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         } else if (FP8 && !I4) {
           sscale = p.score_scale * p.k_scale[h];
           vmul = p.v_scale[h];
+        } else {
+          sscale = p.score_scale;
         }
+        if (FP8) sscale *= pow2f(-qexp);
         if (MOD && p.spec_mask != nullptr) {
           const uint32_t *mrow = p.spec_mask + (size_t)(unit / p.num_kv_heads) * p.q_len;
 #pragma unroll

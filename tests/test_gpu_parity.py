@@ -670,3 +670,53 @@ def test_gqa_thousands_of_units():
     assert flags == 0
     ref_out, ref_lse = reference(w)
     assert_parity(out, lse, ref_out, ref_lse, what="GQA B=1000")
+
+
+# ------------------------------------------------------------------ query range of the f16 operand paths
+
+def _scaled_q(w, factor):
+    w.tensors["q"] = (w.tensors["q"].float() * factor).to(torch.bfloat16)
+    return w
+
+
+@pytest.mark.parametrize("factor", [1e5, 1e-6])
+@pytest.mark.parametrize("kind", ["e4m3", "e4m3_token", "int4", "e4m3_g16"])
+def test_f16_operand_paths_take_any_bf16_query(kind, factor):
+    """e4m3 and int4 keys meet Q in f16, whose range is far narrower than bf16's:
+    q ~ N(0,1) x 1e5 has elements beyond f16's largest finite value, and
+    q ~ N(0,1) x 1e-6 lies in f16's subnormals. The query rows of a kv head are
+    scaled by an exact power of two before the f16 rounding and the score
+    factor takes it back, so both must match the oracle. For the large queries the scores reach
+    ~1e5: the LSE is then checked against a relative bound on top of the
+    absolute 1e-3 -- for e4m3 keys (decoded exactly) that of the fp32 score
+    arithmetic, 1e-5 |lse| (about 2^-17, a few roundings of a 128-term dot
+    product); for int4 keys, whose dequantised value code * scale + shift is
+    rounded to f16 (a relative 2^-11 per element), the bound of that rounding
+    on any score of the row, 2^-11 * scale * sum_d |q_d| * max |k|, with max |k|
+    at most 15 |scale| + |shift| over the cache's coefficient words."""
+    kw = dict(kv_fp8=True)
+    if kind == "e4m3_token":
+        kw = dict(kv_fp8=True, kv_token_scale=True)
+    elif kind == "int4":
+        kw = dict(kv_int4_groups=4)
+    hkv, g = (2, 16) if kind == "e4m3_g16" else (2, 8)
+    layout = "paged" if kind == "int4" else "contiguous"
+    w = W.make_gqa(name=f"qrange_{kind}", batch=3, num_q_heads=g * hkv, num_kv_heads=hkv,
+                   seq_lens=[2000, 129, 1], layout=layout, page_size=16,
+                   cache_len=2048 if layout == "contiguous" else None, seed=560, **kw)
+    _scaled_q(w, factor)
+    for S in (0, 3):
+        out, lse, flags, _ = run_gpu(w, num_splits_override=S)
+        assert flags == 0
+        ref_out, ref_lse = reference(w)
+        assert_parity(out, None, ref_out, None, fp8=True, what=f"{kind} x{factor} S={S}")
+        lg = lse.double().numpy()
+        assert np.all(np.isfinite(lg))
+        bound = 1e-3 + 1e-5 * np.abs(ref_lse)
+        if kind == "int4":
+            # (the spare pages are NaN-poisoned: they hold no key of any row)
+            coef = w.tensors["k"][..., :4].reshape(-1).numpy().view(np.float16).astype(np.float64)
+            kmax = 15 * np.nanmax(np.abs(coef[0::2])) + np.nanmax(np.abs(coef[1::2]))
+            q1 = w.tensors["q"].double().abs().sum(-1).numpy()
+            bound = bound + 2.0 ** -11 * w.scale * q1 * kmax
+        assert np.all(np.abs(lg - ref_lse) <= bound), f"{kind} x{factor} LSE"
