@@ -45,6 +45,7 @@ namespace da {
 namespace {
 
 constexpr int kTile = 64;             // tokens per pipeline stage
+constexpr int kIdAhead = 8;           // tiles whose page / block ids are fetched ahead (ids <= 32)
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
 // A sixth warp takes the row-counter atomics of partial segments off the
 // consumers and merges small units while they stream.
@@ -93,8 +94,9 @@ struct Cfg {
   static constexpr int kStatFloats = 2 * kConsumerWarps * 16;
   static constexpr int oStats = oMeta + 32 * kStages;
   static constexpr int oScan = oStats + 2 * kStatFloats * 4;
-  static constexpr int oFlags = oScan + 16 * 4;              // 32 ints (see the kernel)
-  static constexpr int oMergeBar = oFlags + 32 * 4;          // mbarriers: 2 of the merge staging,
+  static constexpr int oFlags = oScan + 16 * 4;              // 40 ints (see the kernel)
+  static constexpr int oIds = oFlags + 40 * 4;               // page / block id queue (32 ints)
+  static constexpr int oMergeBar = oIds + 32 * 4;            // mbarriers: 2 of the merge staging,
                                                              // 2 partial-segment, 1 epilogue,
                                                              // 1 never arrived on (test stall)
   // e4m3 with per-token scales: [stage][K|V][kSSWords] scale words (TMA
@@ -202,9 +204,23 @@ __device__ __forceinline__ UnitInfo unit_info(const GqaParams &p, int u, uint32_
   return x;
 }
 
-// CTA whose tile range [floor(c*T/C), floor((c+1)*T/C)) contains global tile t.
+// CTA whose tile range [floor(c*T/C), floor((c+1)*T/C)) contains global tile t
+// (a 32-bit division whenever the operands fit, as they do below 2^32 / C tiles).
 __device__ __forceinline__ int cta_of(int64_t t, int64_t T, int C) {
-  return (int)(((t + 1) * C - 1) / T);
+  const uint64_t num = (uint64_t)(t + 1) * (uint64_t)C - 1u;
+  if ((num >> 32) == 0 && ((uint64_t)T >> 32) == 0) return (int)((uint32_t)num / (uint32_t)T);
+  return (int)(num / (uint64_t)T);
+}
+
+// This CTA's share (1 / gridDim.x) of a table of `bytes` bytes prefetched into L2:
+// the whole 16-byte chunks inside [base, base + bytes), cut into equal pieces.
+__device__ __forceinline__ void prefetch_share_l2(const void *base, int64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(base);
+  const uint64_t lo = (a + 15) & ~uint64_t(15), hi = (a + (uint64_t)bytes) & ~uint64_t(15);
+  if (base == nullptr || bytes <= 0 || hi <= lo) return;
+  const uint64_t n16 = (hi - lo) / 16, per = (n16 + gridDim.x - 1) / gridDim.x;
+  const uint64_t s = (uint64_t)blockIdx.x * per, e = s + per < n16 ? s + per : n16;
+  if (e > s) prefetch_l2(reinterpret_cast<const void *>(lo + s * 16), (uint32_t)((e - s) * 16));
 }
 
 // Inclusive scan over the block's threads; returns the block total in *total.
@@ -781,14 +797,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   StageMeta *meta = reinterpret_cast<StageMeta *>(smem + C::oMeta);
   float *stats = reinterpret_cast<float *>(smem + C::oStats);  // [2 copies][m | l][warp][16]
   int *scan = reinterpret_cast<int *>(smem + C::oScan);
+  int *idq = reinterpret_cast<int *>(smem + C::oIds);
   volatile int *flags = reinterpret_cast<volatile int *>(smem + C::oFlags);
   // flags: [0] abort, [1] tiles the producer issued, [2] start unit, [3] start
-  //        tile, [4..5] start P (int64),
+  //        tile, [4..5] start P (int64), [6..9] the start unit's n_valid, tiles,
+  //        nbp, trow (UnitInfo, so the producer starts without a table load),
   //        [12] merges owed after the stream, [13] scratch, [24..31] those merges
   //        (unit, c_first, n_seg, group),
   //        [14..19] the range's partial segments (unit, c_first, n_seg) handed to
   //        the helper warp, [20] unit holding the range's last tile, [21] whether
-  //        its segment here is partial, [22..23] its first tile (int64)
+  //        its segment here is partial, [22..23] its first tile (int64), [32..35]
+  //        its UnitInfo as [6..9]
   uint64_t *merge_bar = reinterpret_cast<uint64_t *>(smem + C::oMergeBar);
   uint64_t *part_bar = merge_bar + 2;  // [2] a partial segment is in global memory
   uint64_t *epi_bar = merge_bar + 4;   // the consumer warps' segment-epilogue barrier
@@ -799,6 +818,21 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   const int U = p.batch * p.num_kv_heads;
   const int cta = blockIdx.x;
   uint32_t dev_err = 0;
+
+  // The producer's first page / block id loads depend on the schedule below (a
+  // scan of every unit's length), so the id tables are fetched into L2 now, by
+  // all CTAs together, and the first ids then come from L2 instead of DRAM.
+  if (threadIdx.x == kConsumerWarps * 32) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
+    if (p.paged) prefetch_share_l2(p.block_table, (int64_t)p.batch * p.max_pages * 4);
+    if (p.sparse_block_size > 0) {
+      const int64_t tb = (int64_t)p.sparse_batch * p.sparse_heads * p.max_sparse_blocks * 4;
+      prefetch_share_l2(p.kv_idx, tb);
+      prefetch_share_l2(p.kv_full_idx, tb);
+    }
+  }
 
   // ---- the schedule: this CTA's range of the global tile sequence. Thread t
   // takes the consecutive units [t*per, t*per + per): one scan gives each
@@ -833,6 +867,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         flags[2] = u;
         flags[3] = (int)(lo - Pu);
         *reinterpret_cast<volatile int64_t *>(flags + 4) = Pu;
+        flags[6] = x.n_valid;
+        flags[7] = x.tiles;
+        flags[8] = x.nbp;
+        flags[9] = x.trow;
       }
       if (t_u > 0 && Pu < hi && hi <= Pu + t_u) {
         // the unit holding the last tile: its segment here is partial when
@@ -840,6 +878,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         flags[20] = u;
         flags[21] = (Pu + t_u > hi || Pu < lo) ? 1 : 0;
         *reinterpret_cast<volatile int64_t *>(flags + 22) = Pu;
+        flags[32] = x.n_valid;
+        flags[33] = x.tiles;
+        flags[34] = x.nbp;
+        flags[35] = x.trow;
       }
       // a unit without tiles is written here by the CTA whose range holds its start
       if (t_u == 0 && ((Pu >= lo && Pu < hi) || (Pu >= T && cta == owner_of_tail))) {
@@ -876,11 +918,6 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
 
   if (warp == kConsumerWarps) {
     // ======================================================= producer
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&qmap);
-    }
     const uint64_t policy = l2_policy_evict_first();
     const uint64_t q_policy = l2_policy_evict_last();
     const int P = p.page_size;
@@ -892,8 +929,15 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     // first and the walk then jumps back to lo: both pieces of such a unit are
     // then finished early in their CTAs, so its merge (by the helper warp)
     // overlaps streaming instead of trailing the range.
-    auto set_at = [&](TileDesc &d, int u, int j, int64_t P0) {
-      UnitInfo x = unit_info(p, u, dev_err);
+    // (u, j, P0) with the unit's UnitInfo as the schedule staged it in flags[f..f+3]
+    auto set_at = [&](TileDesc &d, int u, int j, int64_t P0, int f) {
+      UnitInfo x;
+      x.b = u / p.num_kv_heads;
+      x.h = u - x.b * p.num_kv_heads;
+      x.n_valid = flags[f];
+      x.tiles = flags[f + 1];
+      x.nbp = flags[f + 2];
+      x.trow = flags[f + 3];
       d.unit = u;
       d.b = x.b;
       d.h = x.h;
@@ -911,33 +955,41 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     const bool reorder = kHelper && last_u != start_u && flags[21];
     const int i_jump = reorder ? (int)(hi - last_P) : ntiles;  // position of the jump back to lo
     TileDesc cur;
-    if (reorder) set_at(cur, last_u, 0, last_P);
-    else set_at(cur, start_u, start_j, start_P);
+    if (reorder) set_at(cur, last_u, 0, last_P, 32);
+    else set_at(cur, start_u, start_j, start_P, 6);
     cur.wi = 0;
-    // Page (paged) or block (sparse) id number k of a tile; -1 when absent or
-    // invalid (an invalid one also sets its error bit and is skipped). The
-    // check is a select, not a branch, so the lookahead's loads stay in flight
-    // together instead of each waiting for the one before.
-    auto load_id = [&](const TileDesc &d, int k) -> int {
+    // Page (paged) or block (sparse) id number k of a tile: where it sits in
+    // the tables (null when the tile has no such page), and its check when it
+    // is used (-1 when absent or invalid; an invalid one also sets its error
+    // bit and is skipped; a slot whose copy was never issued is never used).
+    auto id_src = [&](const TileDesc &d, int k) -> const int32_t * {
       if (p.sparse_block_size > 0) {
         const int e = d.j / (p.sparse_block_size / kTile);
         // list entry e: the first table's, then the full table's
-        const int blk = e < d.nbp ? p.kv_idx[(int64_t)d.trow * p.max_sparse_blocks + e]
-                                  : p.kv_full_idx[(int64_t)d.trow * p.max_sparse_blocks + e - d.nbp];
-        const bool bad = blk < 0 || (int64_t)blk * p.sparse_block_size >= p.cache_len;
+        return e < d.nbp ? p.kv_idx + (int64_t)d.trow * p.max_sparse_blocks + e
+                         : p.kv_full_idx + (int64_t)d.trow * p.max_sparse_blocks + e - d.nbp;
+      }
+      const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
+      if (tok0 >= d.n_valid) return nullptr;
+      return p.block_table + (int64_t)d.b * p.max_pages + tok0 / P;
+    };
+    auto check_id = [&](const TileDesc &d, int k, const int *slot) -> int {
+      if (p.sparse_block_size > 0) {
+        const int raw = *slot;
+        const bool bad = raw < 0 || (int64_t)raw * p.sparse_block_size >= p.cache_len;
         dev_err |= bad ? DA_DEVERR_SPARSE_INDEX : 0u;
-        return bad ? -1 : blk;
+        return bad ? -1 : raw;
       }
       const int tok0 = d.j * kTile + k * (P >= kTile ? 0 : P);
       if (tok0 >= d.n_valid) return -1;
-      const int page = p.block_table[(int64_t)d.b * p.max_pages + tok0 / P];
-      const bool bad = page < 0 || page >= p.num_pages;
+      const int raw = *slot;
+      const bool bad = raw < 0 || raw >= p.num_pages;
       dev_err |= bad ? DA_DEVERR_PAGE_INDEX : 0u;
-      return bad ? -1 : page;
+      return bad ? -1 : raw;
     };
     auto advance = [&](TileDesc &d) {
       if (++d.wi == i_jump) {
-        set_at(d, start_u, start_j, start_P);
+        set_at(d, start_u, start_j, start_P, 6);
         return;
       }
       if (++d.j < d.tiles) return;
@@ -960,24 +1012,23 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       d.n_seg = cta_of(d.P + d.tiles - 1, T, CTAS) - d.c_first + 1;
     };
 
-    // Ids are looked up kAhead tiles before they are used, in a queue that
-    // lives in the warp's lanes: lanes k*L .. k*L+L-1 hold the L ids of the
-    // k-th next tile (L ids per tile: pages of a tile, or one block / page).
+    // Ids are fetched kIdAhead tiles before they are used, by 4-byte cp.async
+    // into a queue in shared memory (slot t % kIdAhead holds the L ids of tile
+    // t; L ids per tile: the pages of a tile, or one block / page): no register
+    // waits on a table load in flight, so one tile's lookup never holds up the
+    // next tile's issue. Lanes 0 .. L-1 copy, one commit group per tile.
     const bool needs_ids = p.paged || p.sparse_block_size > 0;
     const int L = pages_per_tile;
-    const int ahead_n = min(8, 32 / L);  // tiles in flight in the queue
-    int idq = -1;
     TileDesc ahead = cur;
     if (needs_ids) {
-      // walk the first ahead_n tiles, each lane group keeping its tile, then
-      // load every lane's id at once (one load in flight per lane)
-      TileDesc mine = ahead;
-      const int my_k = lane / L;
-      for (int k = 0; k < ahead_n && k < ntiles; ++k) {
-        if (k == my_k) mine = ahead;
+      for (int k = 0; k < kIdAhead; ++k) {
+        if (k < ntiles && lane < L) {
+          const int32_t *src = id_src(ahead, lane);
+          if (src) cp_async_4(idq + k * L + lane, src);
+        }
+        cp_async_commit();
         if (k + 1 < ntiles) advance(ahead);
       }
-      if (my_k < ahead_n && my_k < ntiles) idq = load_id(mine, lane - my_k * L);
     }
     int issued = 0;  // tiles whose copies are issued (the drain after a timeout waits for them)
     for (int i = 0; i < ntiles; ++i) {
@@ -991,14 +1042,18 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         if (lane == 0) flags[0] = 1;
         break;
       }
-      const int id_cur = idq;  // lanes 0 .. L-1: this tile's ids
+      const int *ids = idq + (i % kIdAhead) * L;  // this tile's ids
+      if (needs_ids) {
+        cp_async_wait_group<kIdAhead - 1>();  // this lane's copies for tile i have landed
+        __syncwarp();                         // and so have the other lanes'
+      }
       // ---- this tile's boxes (y = first cache row of the box)
       uint64_t valid = 0;
       int nbox = 0;
       int ys[kTile / 16];
       const int tok_base = cur.j * kTile;
       if (p.sparse_block_size > 0) {
-        const int blk = __shfl_sync(0xffffffffu, id_cur, 0);
+        const int blk = check_id(cur, 0, ids);
         if (blk >= 0) {
           const int tb = blk * p.sparse_block_size + (cur.j % (p.sparse_block_size / kTile)) * kTile;
           const int lim = min(min(cur.n_valid - tb, kTile), p.cache_len - tb);
@@ -1014,7 +1069,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         ys[0] = (int)(((int64_t)cur.unit * p.cache_len + tok_base) );
         nbox = 1;
       } else if (P >= kTile) {
-        const int page = __shfl_sync(0xffffffffu, id_cur, 0);
+        const int page = check_id(cur, 0, ids);
         if (page >= 0) {
           valid = low_bits(min(cur.n_valid - tok_base, kTile));
           ys[0] = (int)((((int64_t)page * p.num_kv_heads + cur.h) * P + tok_base % P) );
@@ -1022,7 +1077,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         }
       } else {
         for (int k = 0; k < kTile / P; ++k) {
-          const int page = __shfl_sync(0xffffffffu, id_cur, k);
+          const int page = check_id(cur, k, ids + k);
           ys[k] = -1;
           if (page >= 0) {
             valid |= low_bits(min(cur.n_valid - (tok_base + k * P), P)) << (k * P);
@@ -1111,18 +1166,22 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           tma_load_2d(qslots + st * C::kQSlot, &qmap, &full[st], 0,
                       (int)((int64_t)cur.b * p.num_q_heads + cur.h * G), q_policy);
       }
-      // shift the id queue by one tile and look up tile i + ahead_n
+      // fetch the ids of tile i + kIdAhead into the slot just read
       if (needs_ids) {
-        idq = __shfl_down_sync(0xffffffffu, idq, L);
-        if (i + ahead_n < ntiles) {
-          if (lane >= (ahead_n - 1) * L && lane < ahead_n * L)
-            idq = load_id(ahead, lane - (ahead_n - 1) * L);
-          if (i + ahead_n + 1 < ntiles) advance(ahead);
+        __syncwarp();  // every lane has read this tile's ids
+        if (i + kIdAhead < ntiles) {
+          if (lane < L) {
+            const int32_t *src = id_src(ahead, lane);
+            if (src) cp_async_4(idq + (i % kIdAhead) * L + lane, src);
+          }
+          if (i + kIdAhead + 1 < ntiles) advance(ahead);
         }
+        cp_async_commit();
       }
       issued = i + 1;
       if (i + 1 < ntiles) advance(cur);
     }
+    if (needs_ids) cp_async_wait_group<0>();  // no copy outlives the loop (a timeout leaves early)
     if (lane == 0) flags[1] = issued;
   } else if (warp > kConsumerWarps) {
     // ======================================================= helper (kHelper only)
