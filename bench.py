@@ -201,6 +201,8 @@ def workload_name(cfg, args):
         name += ", draft-tree mask"
     if args.softcap:
         name += f", tanh soft cap {args.softcap:g}"
+    if args.seed is not None:
+        name += f", seed {args.seed}"
     return name
 
 
@@ -455,8 +457,10 @@ def main():
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="tanh soft cap c of the scaled scores, s -> c tanh(s / c) (0 = off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="another draw of the workload's recipe (default: its own seed, 1000 + config)")
     args = ap.parse_args()
-    w = W.config(args.config)
+    w = W.config(args.config, seed=args.seed)
     if args.tree_mask:
         if w.q_len < 2:
             raise SystemExit("--tree-mask needs a configuration with several query tokens")

@@ -378,9 +378,12 @@ CONFIG_NAMES = {
 }
 
 
-def config(i: int, shape_only: bool = False) -> Workload:
-    """The decode workloads (CONFIG_NAMES); ``shape_only`` skips drawing the K/V caches."""
-    seed = 1000 + i
+def config(i: int, shape_only: bool = False, seed: int | None = None) -> Workload:
+    """The decode workloads (CONFIG_NAMES); ``shape_only`` skips drawing the K/V caches.
+    ``seed`` replaces the workload's own seed (1000 + i): another draw of the same
+    recipe (lengths, tables, values)."""
+    own_seed = seed is None
+    seed = 1000 + i if seed is None else seed
     so = dict(shape_only=shape_only)
     if i == 1:
         return make_gqa(name="tiny_gqa", batch=1, num_q_heads=8, num_kv_heads=1,
@@ -414,7 +417,7 @@ def config(i: int, shape_only: bool = False) -> Workload:
                         seq_lens=[131072], cache_len=131072, kv_fp8=True, kv_token_scale=True,
                         seed=seed, **so)
     if i == 8:
-        g = _gen(1002 + 500)  # the lengths of the bf16 paged workload (2)
+        g = _gen((1002 if own_seed else seed) + 500)  # the lengths of the bf16 paged workload (2)
         lens = _lengths(32, 1024, 8192, g)
         return make_gqa(name="int4_paged_gqa", batch=32, num_q_heads=32, num_kv_heads=8,
                         seq_lens=lens, layout="paged", page_size=16, seed=seed, kv_int4_groups=4,
