@@ -58,6 +58,8 @@ class OracleInputs(ctypes.Structure):
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
         ("softcap", ctypes.c_double),
         ("spec_mask", ctypes.c_void_p),
+        ("mask_sink", ctypes.c_void_p), ("mask_window", ctypes.c_void_p),
+        ("alibi_slopes", ctypes.c_void_p),
     ]
 
 
@@ -172,16 +174,16 @@ class _Prepared:
         self.problem = p
         self.keep = {k: _bits(v) for k, v in tensors.items()}
         for k in ("block_table", "seq_lens", "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift",
-                  "kv_full_num_blks", "kv_full_idx", "spec_mask"):
+                  "kv_full_num_blks", "kv_full_idx", "spec_mask", "mask_sink", "mask_window"):
             if self.keep.get(k) is not None:
                 self.keep[k] = self.keep[k].to(torch.int32).contiguous()
-        for k in ("k_scale", "v_scale"):
+        for k in ("k_scale", "v_scale", "alibi_slopes"):
             if self.keep.get(k) is not None:
                 self.keep[k] = self.keep[k].to(torch.float32).contiguous()
         i = OracleInputs()
         for k in ("q", "q_pe", "k", "v", "k_scale", "v_scale", "block_table", "seq_lens",
                   "kv_num_blks", "kv_idx", "k_scale_shift", "v_scale_shift", "kv_full_num_blks",
-                  "kv_full_idx", "spec_mask"):
+                  "kv_full_idx", "spec_mask", "mask_sink", "mask_window", "alibi_slopes"):
             setattr(i, k, _ptr(self.keep.get(k)))
         i.scale = float(scale)
         i.softcap = float(softcap)

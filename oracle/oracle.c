@@ -20,6 +20,14 @@
  *     lse     = m + ln(l)                                    (natural log)
  *   and out = 0, lse = -inf when P is empty.
  *
+ *   A mask_mod and a score_mod in the sense of flex attention (the
+ *   flex_decode.py.jinja template calls them per element, with the query
+ *   head, for the blocks of KV_IDX; the blocks of FULL_KV_IDX take the
+ *   score_mod only), with q_pos = N_b - Q + t the query token's position:
+ *     sink/window mask: position n is kept when n < sink[hq], or window[hq]
+ *       < 0, or n > q_pos - window[hq] (the last window[hq] positions);
+ *     ALiBi score: s_n += slope[hq] * (n - q_pos).
+ *
  *   Several query tokens per row (q_len = Q > 1, speculative decoding): the
  *   row's new tokens are its last Q positions, so query token t < Q keeps the
  *   positions of P(b,h) with n <= N_b - Q + t (the causal mask of the split-K
@@ -210,6 +218,9 @@ typedef struct {
   double softcap;                  /* > 0: scores become softcap * tanh(score / softcap) */
   const uint32_t *spec_mask;       /* Q > 1, optional (else causal): [B][Q][ceil(Q / 32)] words;
                                       bit j of row (b, t) keeps position N_b - Q + j for token t */
+  const int32_t *mask_sink;        /* optional, with mask_window: [HQ] sink lengths */
+  const int32_t *mask_window;      /* optional: [HQ] windows (< 0: no window) -- the mask_mod */
+  const float *alibi_slopes;       /* optional: [HQ] slopes -- the score_mod */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -232,16 +243,19 @@ static int64_t max_positions(const oracle_problem *p) {
  * The valid positions of (b, h), in order. Dense: 0..N_b-1. Sparse (the
  * block-sparse traversal of flex_decode.py.jinja): for each listed block j <
  * KV_NUM_BLKS[b][h], positions KV_IDX[b][h][j] * SBS + t, t < SBS, kept when
- * < N_b. Returns the count, or a negative error code.
+ * < N_b. Returns the count, or a negative error code; *n_masked is the number
+ * of leading positions a mask_mod applies to (all of them but those of the
+ * full-block table).
  */
 static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b, int h,
-                         int64_t *pos) {
+                         int64_t *pos, int64_t *n_masked) {
   int64_t nb = in->seq_lens[b];
   int64_t capacity = p->paged ? (int64_t)p->max_pages_per_seq * p->page_size : p->cache_len;
   if (nb < 0 || nb > capacity) return ORACLE_BAD_INDEX;
   int64_t count = 0;
   if (p->sparse_block_size == 0) {
     for (int64_t n = 0; n < nb; ++n) pos[count++] = n;
+    *n_masked = count;
     return count;
   }
   int64_t sbs = p->sparse_block_size;
@@ -263,8 +277,9 @@ static int64_t positions(const oracle_problem *p, const oracle_inputs *in, int b
     }
   }
   /* the second table of the flex block mask (FULL_KV_NUM_BLKS / FULL_KV_IDX):
-   * blocks that need no mask_mod; with no mask_mod in this definition they
-   * are attended exactly like the first table's blocks, after them */
+   * blocks that need no mask_mod; they are attended like the first table's
+   * blocks, after them, with the score_mod but without the mask_mod */
+  *n_masked = count;
   if (in->kv_full_num_blks) {
     int32_t nfull = in->kv_full_num_blks[trow];
     if (nfull < 0 || nfull > p->max_sparse_blocks) return ORACLE_BAD_INDEX;
@@ -400,6 +415,9 @@ static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   if (p->sparse_block_size > 0 && (!in->kv_num_blks || !in->kv_idx)) return ORACLE_BAD_ARG;
   if ((in->kv_full_num_blks != NULL) != (in->kv_full_idx != NULL)) return ORACLE_BAD_ARG;
   if (in->kv_full_num_blks && p->sparse_block_size <= 0) return ORACLE_BAD_ARG;
+  if (in->mask_sink && !in->mask_window) return ORACLE_BAD_ARG;
+  /* a soft cap and ALiBi together would need an order of the two score_mods */
+  if (in->alibi_slopes && in->softcap > 0.0) return ORACLE_BAD_ARG;
   return ORACLE_OK;
 }
 
@@ -432,8 +450,25 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
   int h = hq / G;
   int dq = p->head_dim_qk, dv = p->head_dim_v;
 
-  int64_t n = positions(p, in, b, h, pos);
+  int64_t n_masked = 0;
+  int64_t n = positions(p, in, b, h, pos, &n_masked);
   if (n < 0) return (int)n;
+  /* the query token's position: the row's new tokens are its last Q positions */
+  const int64_t q_pos = (int64_t)in->seq_lens[b] - Q + t;
+  if (in->mask_window) {
+    /* the sink/window mask_mod, per query head, on the positions it applies to */
+    const int64_t sink = in->mask_sink ? in->mask_sink[hq] : 0, win = in->mask_window[hq];
+    int64_t kept = 0, kept_masked = 0;
+    for (int64_t j = 0; j < n; ++j) {
+      const int keep = j >= n_masked || pos[j] < sink || win < 0 || pos[j] > q_pos - win;
+      if (keep) {
+        pos[kept++] = pos[j];
+        if (j < n_masked) ++kept_masked;
+      }
+    }
+    n = kept;
+    n_masked = kept_masked;
+  }
   if (Q > 1) {
     /* Several new query tokens (speculative decoding): they are the row's last
      * Q positions. Token t sees every older position and, among the new ones,
@@ -467,6 +502,8 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
     /* tanh soft-capping of the scaled score (the FlashAttention-3 page:
      * tanh(scores * softmax_scale / softcap_val) * softcap_val) */
     if (in->softcap > 0.0) s[j] = in->softcap * tanh(s[j] / in->softcap);
+    /* the ALiBi score_mod: a per-head slope times the distance to the query */
+    if (in->alibi_slopes) s[j] += (double)in->alibi_slopes[hq] * (double)(pos[j] - q_pos);
   }
   if (job->num_chunks == 0) {
     oracle_softmax_attend(n, s, vrows, dv, job->out + row * dv, job->lse + row);

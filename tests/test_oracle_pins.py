@@ -257,19 +257,30 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
     for b, hq, tq in itertools.product(range(B), range(HQ), range(Q)):
         n_b = int(t["seq_lens"][b])
         h = hq // G
+        full = set()  # positions of the full-block table: no mask_mod there (flex)
         if w.sparse_block_size:
             pos = []
-            lists = [(t["kv_num_blks"], t["kv_idx"])]
+            lists = [(t["kv_num_blks"], t["kv_idx"], False)]
             if "kv_full_num_blks" in t:
-                lists.append((t["kv_full_num_blks"], t["kv_full_idx"]))
+                lists.append((t["kv_full_num_blks"], t["kv_full_idx"], True))
             zb, zh = b % (w.sparse_batch or B), h % (w.sparse_heads or HKV)
-            for nums, idx in lists:
+            for nums, idx, is_full in lists:
                 for j in range(int(nums[zb, zh])):
                     blk = int(idx[zb, zh, j])
-                    pos += [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
-                            if blk * w.sparse_block_size + i < n_b]
+                    ns = [blk * w.sparse_block_size + i for i in range(w.sparse_block_size)
+                          if blk * w.sparse_block_size + i < n_b]
+                    pos += ns
+                    if is_full:
+                        full |= set(ns)
         else:
             pos = list(range(n_b))
+        q_pos = n_b - Q + tq  # the query token's own position
+        if "mask_window" in t:
+            # sink/window mask_mod of query head hq: keep n < sink, or n within the
+            # last `window` positions up to the query's (window < 0: no window)
+            win = int(t["mask_window"][hq])
+            sink = int(t["mask_sink"][hq]) if "mask_sink" in t else 0
+            pos = [n for n in pos if n in full or n < sink or win < 0 or n > q_pos - win]
         # query token tq of Q is the row's position n_b - Q + tq: it sees n <= that,
         # or, with a draft-tree mask, the older positions and the new ones its row marks
         if "spec_mask" in t:
@@ -304,6 +315,9 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
         if softcap > 0:
             cap = _dec(softcap)
             s = [cap * _dec_tanh(x / cap) for x in s]
+        if "alibi_slopes" in t:  # ALiBi score_mod: slope of the head times (n - q_pos)
+            slope = _dec(t["alibi_slopes"][hq])
+            s = [x + slope * (n - q_pos) for x, n in zip(s, pos)]
         m = max(s)
         e = [(x - m).exp() for x in s]
         den = sum(e)
@@ -373,6 +387,33 @@ def _tiny_cases():
     cases.append(W.make_gqa(name="tree_q4_paged", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=4, seq_lens=[6, 4], layout="paged", page_size=2, seed=20,
                             scale=0.7, q_len=4, tree_mask=True))
+    # flex-style mods: a per-query-head sink/window mask (heads of one group with
+    # different windows, one without a window) and ALiBi slopes
+    mw = W.make_gqa(name="sink_window", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                    seq_lens=[7, 3], cache_len=8, seed=25, scale=0.8)
+    mw.tensors["mask_window"] = torch.tensor([2, -1, 1, 3], dtype=torch.int32)
+    mw.tensors["mask_sink"] = torch.tensor([1, 0, 2, 0], dtype=torch.int32)
+    cases.append(mw)
+    al = W.make_gqa(name="alibi_paged", batch=2, num_q_heads=4, num_kv_heads=1, head_dim=4,
+                    seq_lens=[6, 4], layout="paged", page_size=2, seed=26, scale=0.7)
+    al.tensors["alibi_slopes"] = torch.tensor([0.5, 0.25, -0.125, 0.0], dtype=torch.float32)
+    cases.append(al)
+    # the full-block table takes the score_mod but not the mask_mod
+    sf = W.make_gqa(name="window_full_blocks", batch=1, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                    seq_lens=[8], cache_len=8, sparse_block_size=2,
+                    kv_num_blks=torch.tensor([[2, 1]]), kv_idx=torch.tensor([[[3, 0, 0], [2, 0, 0]]]),
+                    seed=27, scale=0.6, poison=False)
+    sf.tensors["kv_full_num_blks"] = torch.tensor([[1, 1]], dtype=torch.int32)
+    sf.tensors["kv_full_idx"] = torch.tensor([[[1, 0, 0], [0, 0, 0]]], dtype=torch.int32)
+    sf.tensors["mask_window"] = torch.tensor([1, 3, 2, 0], dtype=torch.int32)
+    sf.tensors["alibi_slopes"] = torch.tensor([0.3, -0.2, 0.1, 0.05], dtype=torch.float32)
+    cases.append(sf)
+    # several query tokens: the window moves with each token's position
+    mq = W.make_gqa(name="window_alibi_q3", batch=2, num_q_heads=2, num_kv_heads=1, head_dim=4,
+                    seq_lens=[7, 4], cache_len=8, seed=28, scale=0.7, q_len=3)
+    mq.tensors["mask_window"] = torch.tensor([2, 4], dtype=torch.int32)
+    mq.tensors["alibi_slopes"] = torch.tensor([0.2, 0.4], dtype=torch.float32)
+    cases.append(mq)
     return cases
 
 
@@ -843,3 +884,95 @@ def test_int4_row_from_hand_encoded_words():
     for i, want in probes:
         assert out[0, 0, i] == want, (i, out[0, 0, i], want)
     assert lse[0, 0] == 0.0  # one key with score 0
+
+
+# ------------------------------------------------------------------ flex-style mask_mod / score_mod
+
+def _mods_case(seed=41, **kw):
+    return W.make_gqa(name="mods", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[300, 41, 1],
+                      cache_len=300, seed=seed, **kw)
+
+
+def test_window_wider_than_the_row_and_zero_slopes_change_nothing():
+    w = _mods_case()
+    base = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    t = dict(w.tensors)
+    t["mask_window"] = torch.full((8,), 400, dtype=torch.int32)
+    t["alibi_slopes"] = torch.zeros(8, dtype=torch.float32)
+    out = oracle.decode(oracle.problem_from(w), t, w.scale)
+    assert np.array_equal(out[0], base[0]) and np.array_equal(out[1], base[1])
+
+
+def test_sink_alone_equals_a_decode_over_the_first_positions():
+    # window 0 keeps no recent position: only the sink's first positions remain,
+    # i.e. the same as a row of length `sink`
+    w = _mods_case(seed=42)
+    t = dict(w.tensors)
+    t["mask_window"] = torch.zeros(8, dtype=torch.int32)
+    t["mask_sink"] = torch.full((8,), 20, dtype=torch.int32)
+    out, lse = oracle.decode(oracle.problem_from(w), t, w.scale)
+    short = dict(w.tensors)
+    short["seq_lens"] = torch.minimum(w.tensors["seq_lens"], torch.tensor(20, dtype=torch.int32))
+    ref_out, ref_lse = oracle.decode(oracle.problem_from(w), short, w.scale)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+
+
+def test_window_equals_a_decode_over_the_last_positions():
+    # a window of W (no sink) keeps the last W positions: the same scores as a
+    # cache holding only them (the row's tail moved to the front)
+    w = _mods_case(seed=43)
+    Wn = 17
+    t = dict(w.tensors)
+    t["mask_window"] = torch.full((8,), Wn, dtype=torch.int32)
+    out, lse = oracle.decode(oracle.problem_from(w), t, w.scale)
+    tail = dict(w.tensors)
+    k, v = w.tensors["k"].clone(), w.tensors["v"].clone()
+    lens = w.tensors["seq_lens"].clone()
+    for b, n in enumerate(w.tensors["seq_lens"].tolist()):
+        lo = max(0, n - Wn)
+        k[b, :, :n - lo] = w.tensors["k"][b, :, lo:n]
+        v[b, :, :n - lo] = w.tensors["v"][b, :, lo:n]
+        lens[b] = n - lo
+    tail.update(k=k, v=v, seq_lens=lens)
+    ref_out, ref_lse = oracle.decode(oracle.problem_from(w), tail, w.scale)
+    assert np.max(np.abs(out - ref_out)) < 1e-12 and np.max(np.abs(lse - ref_lse)) < 1e-12
+
+
+def test_alibi_two_keys_closed_form():
+    # two keys at positions 0 and 1, query at position 1: scores s0 - slope and s1
+    w = W.make_gqa(name="alibi2", batch=1, num_q_heads=1, num_kv_heads=1, head_dim=4,
+                   seq_lens=[2], cache_len=2, seed=44, scale=0.5)
+    w.tensors["alibi_slopes"] = torch.tensor([0.75], dtype=torch.float32)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    q = w.tensors["q"][0, 0].double()
+    k = w.tensors["k"][0, 0].double()
+    v = w.tensors["v"][0, 0].double()
+    s0 = float(w.scale * (q @ k[0])) - 0.75
+    s1 = float(w.scale * (q @ k[1]))
+    sig = 1.0 / (1.0 + math.exp(s1 - s0))
+    expect = sig * v[0].numpy() + (1 - sig) * v[1].numpy()
+    assert np.max(np.abs(out[0, 0] - expect)) < 1e-14
+    assert abs(lse[0, 0] - math.log(math.exp(s0) + math.exp(s1))) < 1e-14
+
+
+def test_mask_mod_skips_the_full_block_table():
+    # with every position in the full table, a mask that would drop them all
+    # changes nothing (flex applies no mask_mod to full blocks)
+    w = W.make_gqa(name="fullonly", batch=1, num_q_heads=2, num_kv_heads=1, seq_lens=[256],
+                   cache_len=256, sparse_block_size=64, kv_num_blks=torch.tensor([[0]]),
+                   kv_idx=torch.zeros((1, 1, 4), dtype=torch.int32), seed=45, poison=False)
+    w.tensors["kv_full_num_blks"] = torch.tensor([[4]], dtype=torch.int32)
+    w.tensors["kv_full_idx"] = torch.tensor([[[0, 1, 2, 3]]], dtype=torch.int32)
+    base = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    t = dict(w.tensors)
+    t["mask_window"] = torch.zeros(2, dtype=torch.int32)
+    out = oracle.decode(oracle.problem_from(w), t, w.scale)
+    assert np.array_equal(out[0], base[0]) and np.array_equal(out[1], base[1])
+
+
+def test_softcap_with_alibi_is_refused():
+    w = _mods_case(seed=46)
+    t = dict(w.tensors)
+    t["alibi_slopes"] = torch.full((8,), 0.1, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        oracle.decode(oracle.problem_from(w), t, w.scale, softcap=5.0)
