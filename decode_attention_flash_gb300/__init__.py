@@ -62,6 +62,8 @@ class Args(ctypes.Structure):
         ("k_scale_shift", ctypes.c_void_p), ("v_scale_shift", ctypes.c_void_p),
         ("kv_full_num_blks", ctypes.c_void_p), ("kv_full_idx", ctypes.c_void_p),
         ("softcap", ctypes.c_float), ("spec_mask", ctypes.c_void_p),
+        ("mask_sink", ctypes.c_void_p), ("mask_window", ctypes.c_void_p),
+        ("alibi_slopes", ctypes.c_void_p),
     ]
 
 
@@ -216,6 +218,10 @@ def make_args(tensors: dict, scale: float, out, lse=None, softcap: float = 0.0) 
     a.kv_full_idx = _ptr(tensors.get("kv_full_idx"))
     a.softcap = float(softcap)
     a.spec_mask = _ptr(tensors.get("spec_mask"))
+    # flex-style mods, per query head: the sink/window mask_mod and ALiBi slopes
+    a.mask_sink = _ptr(tensors.get("mask_sink"))
+    a.mask_window = _ptr(tensors.get("mask_window"))
+    a.alibi_slopes = _ptr(tensors.get("alibi_slopes"))
     return a
 
 

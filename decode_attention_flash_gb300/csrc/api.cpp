@@ -252,6 +252,11 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.kv_full_num_blks = a->kv_full_num_blks;
   gp.kv_full_idx = a->kv_full_idx;
   gp.spec_mask = Q > 1 ? a->spec_mask : nullptr;
+  if (a->mask_sink && !a->mask_window) return DA_ERR_INVALID_ARG;
+  if (a->alibi_slopes && a->softcap != 0.f) return DA_ERR_UNSUPPORTED;  // two score_mods, no order
+  gp.mask_sink = a->mask_sink;
+  gp.mask_window = a->mask_window;
+  gp.alibi_slopes = a->alibi_slopes;
   gp.k_scale = a->k_scale;
   gp.v_scale = a->v_scale;
   gp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);
@@ -295,7 +300,8 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   const da_problem &p = ctx->prob;
   if (!a->q || !a->q_pe || !a->k || !a->v || !a->seq_lens || !a->out || !a->block_table)
     return DA_ERR_INVALID_ARG;
-  if (a->softcap != 0.f) return DA_ERR_UNSUPPORTED;  // no score modification in the MLA kernel
+  // no score or mask modification in the MLA kernel
+  if (a->softcap != 0.f || a->mask_window || a->mask_sink || a->alibi_slopes) return DA_ERR_UNSUPPORTED;
   if (!aligned(a->k, 128) || !aligned(a->v, 128) || !aligned(a->q, 128) || !aligned(a->q_pe, 128) ||
       !aligned(a->out, 16))
     return DA_ERR_INVALID_ARG;

@@ -6,7 +6,7 @@ namespace da {
 
 cudaError_t gqa_prepare_kind_e4m3() { return prepare_kind<true, false, false>(); }
 
-cudaError_t gqa_launch_kind_e4m3(bool two, bool mod, const CUtensorMap &kmap,
+cudaError_t gqa_launch_kind_e4m3(bool two, int mod, const CUtensorMap &kmap,
                                  const CUtensorMap &vmap, const CUtensorMap &qmap,
                                  const CUtensorMap &kssmap, const CUtensorMap &vssmap,
                                  const GqaParams &p, int ctas, cudaStream_t stream) {

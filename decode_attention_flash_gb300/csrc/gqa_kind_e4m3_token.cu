@@ -6,7 +6,7 @@ namespace da {
 
 cudaError_t gqa_prepare_kind_e4m3_token() { return prepare_kind<true, true, false>(); }
 
-cudaError_t gqa_launch_kind_e4m3_token(bool two, bool mod, const CUtensorMap &kmap,
+cudaError_t gqa_launch_kind_e4m3_token(bool two, int mod, const CUtensorMap &kmap,
                                        const CUtensorMap &vmap, const CUtensorMap &qmap,
                                        const CUtensorMap &kssmap, const CUtensorMap &vssmap,
                                        const GqaParams &p, int ctas, cudaStream_t stream) {

@@ -31,9 +31,12 @@ cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUten
                        const CUtensorMap &qmap, const CUtensorMap &kssmap,
                        const CUtensorMap &vssmap, const GqaParams &p, int ctas,
                        cudaStream_t stream) {
-  // score modifications (several query tokens, a draft-tree mask, a soft cap)
-  // take their own instantiation: the plain decode keeps the shorter softmax
-  const bool mod = p.q_len > 1 || p.spec_mask != nullptr || p.softcap_l2 > 0.f;
+  // score and mask modifications (several query tokens, a draft-tree mask, a
+  // soft cap, the sink/window mask_mod, ALiBi) take their own instantiation:
+  // the plain decode keeps the shorter softmax
+  const int mod = (p.mask_window != nullptr || p.alibi_slopes != nullptr)
+                      ? 2
+                      : (p.q_len > 1 || p.spec_mask != nullptr || p.softcap_l2 > 0.f) ? 1 : 0;
   const bool two = group > 8;
   if (!fp8) return gqa_launch_kind_bf16(two, mod, kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   if (p.kv_groups > 0)

@@ -120,7 +120,8 @@ struct __align__(8) StageMeta {
   int32_t flags;    // kFirst: first tile of a segment (query group in the stage); kLast
   int32_t c_first;  // first CTA holding a segment of this unit
   int32_t n_seg;    // segments of this unit
-  int32_t nval;     // the row's length minus the tile's first position (sparse: kTile)
+  int32_t nval;     // the row's length minus the tile's first position
+  int32_t pos0;     // the tile's first position in the row (a kept block's for sparse)
 };
 static_assert(sizeof(StageMeta) == 32, "the shared-memory layout keeps 32 bytes per stage");
 
@@ -129,7 +130,8 @@ static_assert(sizeof(StageMeta) == 32, "the shared-memory layout keeps 32 bytes 
 __device__ __forceinline__ int ss_word(int t, int box_rows) {
   return box_rows >= 32 ? t : t + (t / box_rows) * (32 - box_rows);
 }
-constexpr int32_t kFirst = 1, kLast = 2;
+// kFull: a tile of the full-block table (flex's FULL_KV_IDX: no mask_mod there)
+constexpr int32_t kFirst = 1, kLast = 2, kFull = 4;
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -773,9 +775,12 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
 }
 
 // TOK: e4m3 K/V with per-token scale and shift words (FP8 only).
-// MOD: score modifications are possible (several query tokens with their mask
-// words, a soft cap); without them the softmax keeps only the length mask.
-template <bool FP8, int NT, bool TOK, bool I4, bool MOD>
+// MOD: 0 -- the plain decode, whose softmax keeps only the length mask; 1 --
+// score modifications are possible (several query tokens with their mask
+// words, a soft cap); 2 -- the flex-style mods too (the sink/window mask_mod and
+// the ALiBi score_mod, per query head), in an instantiation of their own so
+// that the other two keep their registers.
+template <bool FP8, int NT, bool TOK, bool I4, int MOD>
 __global__ void __launch_bounds__(threads_for<NT>(), 2)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -1052,10 +1057,12 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
       int nbox = 0;
       int ys[kTile / 16];
       const int tok_base = cur.j * kTile;
+      int pos0 = tok_base;  // the tile's first position in the row
       if (p.sparse_block_size > 0) {
         const int blk = check_id(cur, 0, ids);
         if (blk >= 0) {
           const int tb = blk * p.sparse_block_size + (cur.j % (p.sparse_block_size / kTile)) * kTile;
+          pos0 = tb;
           const int lim = min(min(cur.n_valid - tb, kTile), p.cache_len - tb);
           valid = low_bits(lim);
           if (lim > 0) {
@@ -1092,10 +1099,13 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         StageMeta m;
         m.valid = valid;
         m.unit = cur.unit;
-        m.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+        const bool full_blk =
+            p.sparse_block_size > 0 && cur.j / (p.sparse_block_size / kTile) >= cur.nbp;
+        m.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (full_blk ? kFull : 0);
         m.c_first = cur.c_first;
         m.n_seg = cur.n_seg;
-        m.nval = p.sparse_block_size > 0 ? kTile : cur.n_valid - tok_base;
+        m.nval = cur.n_valid - pos0;
+        m.pos0 = pos0;
         meta[st] = m;
         const uint32_t box_tokens = (p.paged && P < kTile) ? (uint32_t)P : (uint32_t)kTile;
         const uint32_t row_bytes = I4 ? (uint32_t)(p.kv_groups + kD / 8) * 4u : (uint32_t)C::kBytesPerTok;
@@ -1219,7 +1229,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     float oacc[NT][8][4];
     float m_run[NT][2], l_part[NT][2];
     float sscale = p.score_scale, vmul = 1.f;
-    const bool softcap = MOD && p.softcap_l2 > 0.f;
+    const bool softcap = MOD >= 1 && p.softcap_l2 > 0.f;
     // e4m3 with per-token scale and shift (value = e4m3 * sc + sh): the score
     // of a key is sc * (q . e4m3) + sh * sum(q), so the MMA runs on the codes
     // and qsum holds sum(q) of the thread's two query rows; a value's scale
@@ -1242,6 +1252,10 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         trow[nt][e] = (nt * 8 + 2 * q4 + e) % p.q_len;
         mword[nt][e] = (2u << trow[nt][e]) - 1u;
       }
+    // The flex-style mods (the sink/window mask_mod, the ALiBi score_mod) are
+    // per query head: row g * Q + t of a unit of kv head h belongs to query
+    // head h * (rows / Q) + g; their arrays are read per tile (L1 hits).
+    const bool mods = MOD == 2 && (p.mask_window != nullptr || p.alibi_slopes != nullptr);
     auto reset = [&]() {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -1354,7 +1368,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           sscale = p.score_scale;
         }
         if (FP8) sscale *= pow2f(-qexp);
-        if (MOD && p.spec_mask != nullptr) {
+        if (MOD >= 1 && p.spec_mask != nullptr) {
           const uint32_t *mrow = p.spec_mask + (size_t)(unit / p.num_kv_heads) * p.q_len;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -1466,13 +1480,30 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           for (int e = 0; e < 2; ++e) {
             // the query token's mask over the new tokens (the tile's valid bits
             // already stop at the row's length; one query token keeps all)
-            const bool ok0 = ok_r && (!MOD || jnew < 0 || ((mword[nt][e] >> min(jnew, 31)) & 1u));
-            const bool ok1 =
-                ok_r8 && (!MOD || jnew + 8 < 0 || ((mword[nt][e] >> min(jnew + 8, 31)) & 1u));
+            bool ok0 = ok_r && (MOD == 0 || jnew < 0 || ((mword[nt][e] >> min(jnew, 31)) & 1u));
+            bool ok1 =
+                ok_r8 && (MOD == 0 || jnew + 8 < 0 || ((mword[nt][e] >> min(jnew + 8, 31)) & 1u));
             float x0 = sacc[nt][e] * sscale, x1 = sacc[nt][2 + e] * sscale;
             if (softcap) {  // c * tanh(s / c), in log2 units: c2 * tanh(x / c2)
               x0 = cap_tanh(x0, p.softcap_l2, p.softcap_k);
               x1 = cap_tanh(x1, p.softcap_l2, p.softcap_k);
+            }
+            if (mods) {
+              const int row = min(nt * 8 + 2 * q4 + e, G - 1);
+              const int hq = (unit % p.num_kv_heads) * (G / p.q_len) + row / p.q_len;
+              // positions of the thread's two tokens and of the row's query token
+              const int kv0 = m.pos0 + 16 * warp + r8, kv1 = kv0 + 8;
+              const int qpos = m.nval + m.pos0 - p.q_len + trow[nt][e];
+              if (p.mask_window && !(m.flags & kFull)) {  // the mask_mod skips full blocks
+                const int w = __ldg(p.mask_window + hq), sk = p.mask_sink ? __ldg(p.mask_sink + hq) : 0;
+                ok0 = ok0 && (kv0 < sk || w < 0 || kv0 > qpos - w);
+                ok1 = ok1 && (kv1 < sk || w < 0 || kv1 > qpos - w);
+              }
+              if (p.alibi_slopes) {  // in log2 units, like the scores
+                const float sl = __ldg(p.alibi_slopes + hq) * 1.4426950408889634f;
+                x0 += sl * (float)(kv0 - qpos);
+                x1 += sl * (float)(kv1 - qpos);
+              }
             }
             x0 = ok0 ? x0 : neg_inf();
             x1 = ok1 ? x1 : neg_inf();
@@ -1857,14 +1888,14 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   if (dev_err) atomicOr(p.err, dev_err);
 }
 
-template <bool FP8, int NT, bool TOK, bool I4, bool MOD>
+template <bool FP8, int NT, bool TOK, bool I4, int MOD>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK, I4, MOD>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<FP8, NT, TOK, I4>::kTotal);
 }
 
-template <bool FP8, int NT, bool TOK, bool I4, bool MOD>
+template <bool FP8, int NT, bool TOK, bool I4, int MOD>
 void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
             const CUtensorMap &kssmap, const CUtensorMap &vssmap, const GqaParams &p, int ctas,
             cudaStream_t stream) {
@@ -1873,27 +1904,30 @@ void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap 
                                                                            vssmap, p);
 }
 
-// The four instantiations of one element kind (one or two n-tiles, with or
-// without score modifications), set up and launched from that kind's own
+// The six instantiations of one element kind (one or two n-tiles; no, some or
+// all score modifications), set up and launched from that kind's own
 // translation unit.
 template <bool FP8, bool TOK, bool I4>
 cudaError_t prepare_kind() {
   cudaError_t e;
-  if ((e = set_attr<FP8, 1, TOK, I4, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 2, TOK, I4, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 1, TOK, I4, true>()) != cudaSuccess) return e;
-  return set_attr<FP8, 2, TOK, I4, true>();
+  if ((e = set_attr<FP8, 1, TOK, I4, 0>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 2, TOK, I4, 0>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 1, TOK, I4, 1>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 2, TOK, I4, 1>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 1, TOK, I4, 2>()) != cudaSuccess) return e;
+  return set_attr<FP8, 2, TOK, I4, 2>();
 }
 
 template <bool FP8, bool TOK, bool I4>
-cudaError_t launch_kind(bool two, bool mod, const CUtensorMap &kmap, const CUtensorMap &vmap,
+cudaError_t launch_kind(bool two, int mod, const CUtensorMap &kmap, const CUtensorMap &vmap,
                         const CUtensorMap &qmap, const CUtensorMap &kssmap,
                         const CUtensorMap &vssmap, const GqaParams &p, int ctas,
                         cudaStream_t stream) {
-  if (!two && !mod) launch<FP8, 1, TOK, I4, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
-  else if (two && !mod) launch<FP8, 2, TOK, I4, false>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
-  else if (!two) launch<FP8, 1, TOK, I4, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
-  else launch<FP8, 2, TOK, I4, true>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+#define DA_LAUNCH(NT, M) launch<FP8, NT, TOK, I4, M>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream)
+  if (mod == 0) two ? DA_LAUNCH(2, 0) : DA_LAUNCH(1, 0);
+  else if (mod == 1) two ? DA_LAUNCH(2, 1) : DA_LAUNCH(1, 1);
+  else two ? DA_LAUNCH(2, 2) : DA_LAUNCH(1, 2);
+#undef DA_LAUNCH
   return cudaGetLastError();
 }
 
@@ -1904,7 +1938,7 @@ cudaError_t launch_kind(bool two, bool mod, const CUtensorMap &kmap, const CUten
 // own translation unit, gqa_kind_<kind>.cu.
 #define DA_GQA_KIND_DECL(name)                                                                 \
   cudaError_t gqa_prepare_kind_##name();                                                       \
-  cudaError_t gqa_launch_kind_##name(bool two, bool mod, const CUtensorMap &kmap,              \
+  cudaError_t gqa_launch_kind_##name(bool two, int mod, const CUtensorMap &kmap,               \
                                      const CUtensorMap &vmap, const CUtensorMap &qmap,         \
                                      const CUtensorMap &kssmap, const CUtensorMap &vssmap,     \
                                      const GqaParams &p, int ctas, cudaStream_t stream);

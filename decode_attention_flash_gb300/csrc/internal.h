@@ -29,6 +29,9 @@ struct GqaParams {
   const int32_t *kv_full_num_blks;  // sparse, optional: the full-block table, [B][HKV]
   const int32_t *kv_full_idx;       // and [B][HKV][max_sparse_blocks] (attended after kv_idx)
   const uint32_t *spec_mask;   // q_len > 1, optional: [B][q_len] draft-tree mask words
+  const int32_t *mask_sink;    // optional [HQ] (with mask_window): positions below are kept
+  const int32_t *mask_window;  // optional [HQ]: the sink/window mask_mod (< 0: no window)
+  const float *alibi_slopes;   // optional [HQ]: the ALiBi score_mod, slope * (n - q_pos)
   const float *k_scale;        // fp8: [HKV]
   const float *v_scale;        // fp8: [HKV]
   float *o_part;               // [units + ctas][G][128] partial slots (slot = unit + cta)

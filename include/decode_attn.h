@@ -168,6 +168,18 @@ typedef struct {
  *              bit j of word [b][t] is set. NULL: causal (bits 0..t). Ignored for Q = 1
  *   out        bf16 [B][HQ][Dv]    (q_len Q > 1: [B][HQ][Q][Dv])
  *   lse        fp32 [B][HQ], natural log; may be NULL (q_len Q > 1: [B][HQ][Q])
+ *   mask_window, mask_sink  GQA, optional: int32 [HQ] each (mask_sink may be NULL, meaning
+ *              0): a mask_mod per query head in the sense of flex attention (which
+ *              the flex_decode.py.jinja template applies element-wise, with the query
+ *              head, to the blocks of KV_IDX and not to those of FULL_KV_IDX). With
+ *              q_pos = seq_lens[b] - Q + t the query token's position, position n is
+ *              kept when n < mask_sink[hq], or mask_window[hq] < 0, or
+ *              n > q_pos - mask_window[hq] (the last mask_window[hq] positions): a
+ *              sliding window with attention sinks, per head. The blocks of
+ *              kv_full_idx are not masked. MLA: NULL only (DA_ERR_UNSUPPORTED)
+ *   alibi_slopes GQA, optional: fp32 [HQ]: a score_mod adding slope[hq] * (n - q_pos)
+ *              to every scaled score (ALiBi), full blocks included. Not with a soft cap
+ *              (the two score_mods would need an order: DA_ERR_UNSUPPORTED); MLA: NULL
  */
 typedef struct {
   const void *q;
@@ -189,6 +201,9 @@ typedef struct {
   const int32_t *kv_full_idx;
   float softcap;
   const uint32_t *spec_mask;
+  const int32_t *mask_sink;
+  const int32_t *mask_window;
+  const float *alibi_slopes;
 } da_args;
 
 /* What the planner decided (host-side, informational). */

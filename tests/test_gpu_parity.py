@@ -720,3 +720,79 @@ def test_f16_operand_paths_take_any_bf16_query(kind, factor):
             q1 = w.tensors["q"].double().abs().sum(-1).numpy()
             bound = bound + 2.0 ** -11 * w.scale * q1 * kmax
         assert np.all(np.abs(lg - ref_lse) <= bound), f"{kind} x{factor} LSE"
+
+
+# ------------------------------------------------------------------ flex-style mask_mod / score_mod
+
+def _mods(w, window=True, sink=True, alibi=True, seed=0):
+    g = torch.Generator().manual_seed(900 + seed)
+    HQ = w.num_q_heads
+    if window:
+        # per query head: a window of 1..300 positions, or none (-1) for some heads
+        win = torch.randint(1, 300, (HQ,), generator=g, dtype=torch.int32)
+        win[torch.randint(0, HQ, (max(1, HQ // 4),), generator=g)] = -1
+        w.tensors["mask_window"] = win
+        if sink:
+            w.tensors["mask_sink"] = torch.randint(0, 8, (HQ,), generator=g, dtype=torch.int32)
+    if alibi:
+        w.tensors["alibi_slopes"] = (torch.rand(HQ, generator=g) * 0.2 - 0.05).to(torch.float32)
+    return w
+
+
+@pytest.mark.parametrize("kind", ["paged", "contiguous_g16", "sparse_full", "query_tokens",
+                                  "fp8", "fp8token", "int4", "window_only", "alibi_only"])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_flex_mods_per_query_head(kind, splits):
+    """A sink/window mask_mod and ALiBi slopes that differ between the query heads
+    of one kv head's group (some heads with no window at all), against the oracle."""
+    lens = [700, 1, 65, 333]
+    fp8 = kind in ("fp8", "fp8token")
+    if kind == "contiguous_g16":
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=32, num_kv_heads=2, seq_lens=lens,
+                       cache_len=700, seed=910)
+    elif kind == "sparse_full":
+        # each list's last two blocks (the row's tail) move to the full-block table,
+        # which the mask_mod does not touch
+        w = _sparse(seed=911)
+        num, idx = w.tensors["kv_num_blks"], w.tensors["kv_idx"]
+        assert int(num.min()) == int(num.max()) == 7
+        w.tensors["kv_num_blks"] = (num - 2).contiguous()
+        w.tensors["kv_full_num_blks"] = torch.full_like(num, 2)
+        w.tensors["kv_full_idx"] = torch.cat([idx[..., 5:], idx[..., :5]], -1).contiguous()
+    elif kind == "query_tokens":
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=8, num_kv_heads=2, seq_lens=lens,
+                       layout="paged", page_size=16, q_len=3, seed=912)
+    else:
+        kw = {"fp8": dict(kv_fp8=True), "fp8token": dict(kv_fp8=True, kv_token_scale=True),
+              "int4": dict(kv_int4_groups=4)}.get(kind, {})
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=32, num_kv_heads=8, seq_lens=lens,
+                       layout="paged", page_size=16, seed=913, **kw)
+    _mods(w, window=kind != "alibi_only", alibi=kind != "window_only", seed=splits)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, fp8=fp8 or kind == "int4", what=f"mods {kind} S={splits}")
+
+
+def test_flex_mods_that_change_nothing_are_bitwise_the_plain_path():
+    w = W.make_gqa(name="noop_mods", batch=3, num_q_heads=16, num_kv_heads=4, seq_lens=[900, 17, 300],
+                   layout="paged", page_size=16, seed=914)
+    base_out, base_lse, _, eng = run_gpu(w, num_splits_override=2)
+    w.tensors["mask_window"] = torch.full((16,), 5000, dtype=torch.int32)
+    w.tensors["alibi_slopes"] = torch.zeros(16, dtype=torch.float32)
+    out, lse, flags, _ = run_gpu(w, engine=eng)
+    assert flags == 0 and torch.equal(out, base_out) and torch.equal(lse, base_lse)
+
+
+def test_flex_mods_refused_for_mla_and_alibi_with_softcap():
+    m = W.make_mla(name="mla_mods", batch=1, seq_lens=[64], seed=915)
+    m.tensors["mask_window"] = torch.full((128,), 8, dtype=torch.int32)
+    with pytest.raises(da.DecodeAttnError) as e:
+        run_gpu(m)
+    assert e.value.status == da.DA_ERR_UNSUPPORTED
+    w = W.make_gqa(name="alibi_cap", batch=1, num_q_heads=8, num_kv_heads=2, seq_lens=[100],
+                   cache_len=100, seed=916)
+    w.tensors["alibi_slopes"] = torch.full((8,), 0.1, dtype=torch.float32)
+    with pytest.raises(da.DecodeAttnError) as e:
+        run_gpu(w, softcap=5.0)
+    assert e.value.status == da.DA_ERR_UNSUPPORTED
