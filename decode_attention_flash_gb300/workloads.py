@@ -71,6 +71,7 @@ class Workload:
     sparse_batch: int = 0  # block mask extents (batch, kv heads), broadcast by
     sparse_heads: int = 0  # modulo; 0 = the problem's
     kv_token_scale: bool = False  # fp8 KV with a per-token fp16 scale and shift
+    fp8_mma: bool = False         # e4m3 tensor-core QK / PV (Q and the PV weights rounded to e4m3)
     kv_int4_groups: int = 0       # int4 group-wise KV: the number of groups per row
     tensors: dict = field(default_factory=dict)
 

@@ -45,7 +45,7 @@ class OracleProblem(ctypes.Structure):
         "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "is_mla",
         "ckv_dim", "kpe_dim", "paged", "page_size", "cache_len", "max_pages_per_seq",
         "num_pages", "kv_fp8", "sparse_block_size", "max_sparse_blocks", "q_len",
-        "sparse_batch", "sparse_heads", "kv_groups")]
+        "sparse_batch", "sparse_heads", "kv_groups", "fp8_mma")]
 
 
 class OracleInputs(ctypes.Structure):
@@ -60,6 +60,7 @@ class OracleInputs(ctypes.Structure):
         ("spec_mask", ctypes.c_void_p),
         ("mask_sink", ctypes.c_void_p), ("mask_window", ctypes.c_void_p),
         ("alibi_slopes", ctypes.c_void_p),
+        ("p8_bound", ctypes.c_void_p),
     ]
 
 
@@ -74,6 +75,10 @@ def lib():
         L.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         L.oracle_e4m3_to_double.restype = ctypes.c_double
         L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_f16_round.restype = ctypes.c_double
+        L.oracle_f16_round.argtypes = [ctypes.c_double]
         L.oracle_softmax_attend.restype = None
         L.oracle_softmax_attend.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
@@ -135,6 +140,16 @@ def f16_to_double(bits: int) -> float:
 
 def e4m3_to_double(byte: int) -> float:
     return lib().oracle_e4m3_to_double(byte)
+
+
+def e4m3_encode(x: float) -> int:
+    """float32 -> e4m3fn code byte, round to nearest even, saturating to +-448."""
+    return lib().oracle_e4m3_encode(float(x))
+
+
+def f16_round(x: float) -> float:
+    """The nearest binary16 value (ties to even), as a float."""
+    return lib().oracle_f16_round(float(x))
 
 
 def softmax_attend(s, v):
@@ -203,7 +218,8 @@ def problem_from(work) -> dict:
         kv_groups=getattr(w, "kv_int4_groups", 0),
         sparse_block_size=w.sparse_block_size,
         max_sparse_blocks=w.max_sparse_blocks, q_len=getattr(w, "q_len", 1),
-        sparse_batch=getattr(w, "sparse_batch", 0), sparse_heads=getattr(w, "sparse_heads", 0))
+        sparse_batch=getattr(w, "sparse_batch", 0), sparse_heads=getattr(w, "sparse_heads", 0),
+        fp8_mma=int(getattr(w, "fp8_mma", False)))
 
 
 def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = None,
@@ -220,6 +236,24 @@ def decode(prob: dict, tensors: dict, scale: float, num_threads: int | None = No
     if st != 0:
         raise ValueError(f"oracle_decode failed with status {st}")
     return out, lse
+
+
+def decode_p8_bound(prob: dict, tensors: dict, scale: float, num_threads: int | None = None,
+                    softcap: float = 0.0):
+    """decode() of an fp8_mma problem, with the rounding bound of its weights:
+    (out, lse, bound), bound shaped like out."""
+    prep = _Prepared(prob, tensors, scale, softcap)
+    p = prep.problem
+    lead = (p.batch, p.num_q_heads) + ((p.q_len,) if p.q_len > 1 else ())
+    out = np.zeros(lead + (p.head_dim_v,), dtype=np.float64)
+    lse = np.zeros(lead, dtype=np.float64)
+    bound = np.zeros(lead + (p.head_dim_v,), dtype=np.float64)
+    prep.inputs.p8_bound = bound.ctypes.data
+    st = lib().oracle_decode(ctypes.byref(p), ctypes.byref(prep.inputs), out.ctypes.data,
+                             lse.ctypes.data, num_threads or default_threads())
+    if st != 0:
+        raise ValueError(f"oracle_decode failed with status {st}")
+    return out, lse, bound
 
 
 def split(prob: dict, tensors: dict, scale: float, chunk_bounds, num_threads: int | None = None):

@@ -28,6 +28,19 @@
  *       < 0, or n > q_pos - window[hq] (the last window[hq] positions);
  *     ALiBi score: s_n += slope[hq] * (n - q_pos).
  *
+ *   fp8 tensor-core arithmetic (fp8_mma, with e4m3 K/V and per-kv-head
+ *   scales): the query row is quantised to e4m3 as the kernel does it, in
+ *   fp32 -- amax = max_d |q_d|, inv = 448 / amax, code_d = e4m3(q_d * inv)
+ *   rounded to nearest even and saturated to +-448, and q~_d = code_d * s with
+ *   s = amax / 448 (codes 0 and s = 0 when amax < 2^-100) -- and the scores
+ *   use q~. The weights that meet V are rounded too: w_n = r8(r16(2^8 p_n)) /
+ *   2^8 with p_n = exp(s_n - m), r16 / r8 the round-to-nearest-even into f16
+ *   and into e4m3 (saturating); out = sum_n w_n v_n / l with l = sum_n p_n
+ *   unrounded. The kernel rounds its weights relative to the running maximum
+ *   it holds at each tile, not the row's maximum, so the two differ by up to
+ *   twice the rounding bound of every weight, b(p) = (2^-4 + 2^-10) p + 2^-17,
+ *   which the oracle reports per output element as sum_n b(p_n) |v_n| / l.
+ *
  *   Several query tokens per row (q_len = Q > 1, speculative decoding): the
  *   row's new tokens are its last Q positions, so query token t < Q keeps the
  *   positions of P(b,h) with n <= N_b - Q + t (the causal mask of the split-K
@@ -168,6 +181,91 @@ void oracle_merge(int num_splits, int dv, const double *o, const double *lse_s,
   *lse = M + log(wsum);
 }
 
+/*
+ * Round-to-nearest-even of a float into OCP E4M3FN, saturating to +-448 (a
+ * value beyond 448 gives 448, NaN gives the NaN code 0x7F): the code byte.
+ * From the format: 3 mantissa bits, exponent bias 7, normal exponents -6..8,
+ * subnormals k * 2^-9.
+ */
+uint8_t oracle_e4m3_encode(float x) {
+  if (x != x) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  if (a == 0.0) return sign;
+  int E;
+  frexp(a, &E); /* a = f * 2^E, f in [0.5, 1): floor(log2 a) = E - 1 */
+  int e = E - 1;
+  if (e < -6) { /* subnormal: multiples of 2^-9 */
+    double k = rint(ldexp(a, 9));
+    if (k >= 8.0) return sign | 0x08; /* rounds up to 2^-6, the smallest normal */
+    return sign | (uint8_t)k;
+  }
+  double k = rint(ldexp(a, 3 - e)); /* 8 <= k <= 16 */
+  if (k >= 16.0) {
+    k = 8.0;
+    ++e;
+  }
+  return sign | (uint8_t)((e + 7) << 3) | (uint8_t)(k - 8.0);
+}
+
+/* Round-to-nearest-even of a double into IEEE binary16 (the value, as a double;
+ * overflow gives inf): 10 mantissa bits, normal exponents -14..15,
+ * subnormals k * 2^-24. */
+double oracle_f16_round(double x) {
+  if (x != x || isinf(x)) return x;
+  double a = fabs(x);
+  if (a == 0.0) return x;
+  int E;
+  frexp(a, &E);
+  int e = E - 1;
+  double r;
+  if (e < -14)
+    r = ldexp(rint(ldexp(a, 24)), -24);
+  else
+    r = ldexp(rint(ldexp(a, 10 - e)), e - 10);
+  if (r > 65504.0) r = INFINITY;
+  return x < 0 ? -r : r;
+}
+
+/*
+ * Softmax attention with the weights that meet V rounded as the fp8
+ * tensor-core path rounds them: w = r8(r16(2^8 p)) / 2^8, p = exp(s - m), out
+ * = sum w v / l, l = sum p; bound[d] = sum b(p) |v[d]| / l with b(p) =
+ * (2^-4 + 2^-10) p + 2^-17 (the rounding bound of one weight). n == 0 gives
+ * out = 0, lse = -inf, bound = 0.
+ */
+void oracle_softmax_attend_p8(int64_t n, const double *s, const double *v, int dv, double *out,
+                              double *lse, double *bound) {
+  for (int d = 0; d < dv; ++d) {
+    out[d] = 0.0;
+    if (bound) bound[d] = 0.0;
+  }
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j)
+    if (s[j] > m) m = s[j];
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
+  for (int64_t j = 0; j < n; ++j) {
+    const double p = exp(s[j] - m);
+    const double w = oracle_e4m3_to_double(oracle_e4m3_encode((float)oracle_f16_round(256.0 * p))) / 256.0;
+    const double b = (0.0625 + 0.0009765625) * p + 7.62939453125e-06;
+    for (int d = 0; d < dv; ++d) {
+      out[d] += w * v[j * (int64_t)dv + d];
+      if (bound) bound[d] += b * fabs(v[j * (int64_t)dv + d]);
+    }
+  }
+  for (int d = 0; d < dv; ++d) {
+    out[d] /= l;
+    if (bound) bound[d] /= l;
+  }
+  *lse = m + log(l);
+}
+
 /* ------------------------------------------------------------------ */
 /* problem description (the oracle's own; not shared with the kernels) */
 /* ------------------------------------------------------------------ */
@@ -195,6 +293,8 @@ typedef struct {
   int32_t sparse_batch;   /* sparse: extents of the tables' batch and head axes, */
   int32_t sparse_heads;   /* 0 = B and HKV; row (b, h) reads table (b % SZ, h % SH) */
   int32_t kv_groups;      /* kv_fp8 == 3: N_GROUPS, 1, 2, 4 or 8 */
+  int32_t fp8_mma;        /* 1: e4m3 tensor-core arithmetic (Q and the weights of V
+                             rounded as described at the top; kv_fp8 == 1 only) */
 } oracle_problem;
 
 typedef struct {
@@ -221,6 +321,8 @@ typedef struct {
   const int32_t *mask_sink;        /* optional, with mask_window: [HQ] sink lengths */
   const int32_t *mask_window;      /* optional: [HQ] windows (< 0: no window) -- the mask_mod */
   const float *alibi_slopes;       /* optional: [HQ] slopes -- the score_mod */
+  double *p8_bound;                /* fp8_mma, optional output [rows][Dv]: the weights'
+                                      rounding bound (unsplit decode only) */
 } oracle_inputs;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_INDEX = -2, ORACLE_NO_MEM = -3 };
@@ -389,6 +491,21 @@ static void fetch_q(const oracle_problem *p, const oracle_inputs *in, int b, int
   }
   const uint16_t *qq = in->q + r * p->head_dim_qk;
   for (int d = 0; d < p->head_dim_qk; ++d) qr[d] = oracle_bf16_to_double(qq[d]);
+  if (p->fp8_mma) {
+    /* the e4m3 query row, in the kernel's fp32 steps (see the top) */
+    float amax = 0.0f;
+    for (int d = 0; d < p->head_dim_qk; ++d) {
+      const float a = fabsf((float)qr[d]);
+      if (a > amax) amax = a;
+    }
+    const int tiny = !(amax >= 0x1p-100f);
+    const float inv = tiny ? 0.0f : 448.0f / amax;
+    const float sq = tiny ? 0.0f : amax / 448.0f;
+    for (int d = 0; d < p->head_dim_qk; ++d) {
+      const float x = (float)qr[d] * inv;
+      qr[d] = oracle_e4m3_to_double(oracle_e4m3_encode(x)) * (double)sq;
+    }
+  }
 }
 
 static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
@@ -418,6 +535,7 @@ static int check_problem(const oracle_problem *p, const oracle_inputs *in) {
   if (in->mask_sink && !in->mask_window) return ORACLE_BAD_ARG;
   /* a soft cap and ALiBi together would need an order of the two score_mods */
   if (in->alibi_slopes && in->softcap > 0.0) return ORACLE_BAD_ARG;
+  if (p->fp8_mma && (p->kv_fp8 != 1 || p->is_mla)) return ORACLE_BAD_ARG;
   return ORACLE_OK;
 }
 
@@ -506,9 +624,14 @@ static int run_row(job_t *job, int64_t row, int64_t *pos, double *s, double *vro
     if (in->alibi_slopes) s[j] += (double)in->alibi_slopes[hq] * (double)(pos[j] - q_pos);
   }
   if (job->num_chunks == 0) {
-    oracle_softmax_attend(n, s, vrows, dv, job->out + row * dv, job->lse + row);
+    if (p->fp8_mma)
+      oracle_softmax_attend_p8(n, s, vrows, dv, job->out + row * dv, job->lse + row,
+                               in->p8_bound ? in->p8_bound + row * dv : NULL);
+    else
+      oracle_softmax_attend(n, s, vrows, dv, job->out + row * dv, job->lse + row);
     return ORACLE_OK;
   }
+  if (p->fp8_mma) return ORACLE_BAD_ARG; /* split decode is defined on exact weights */
   for (int c = 0; c < job->num_chunks; ++c) {
     int64_t lo = job->chunk_bounds[c], hi = job->chunk_bounds[c + 1];
     if (lo > n) lo = n;

@@ -976,3 +976,116 @@ def test_softcap_with_alibi_is_refused():
     t["alibi_slopes"] = torch.full((8,), 0.1, dtype=torch.float32)
     with pytest.raises(ValueError):
         oracle.decode(oracle.problem_from(w), t, w.scale, softcap=5.0)
+
+
+# ------------------------------------------------------------------ e4m3 tensor-core arithmetic (fp8_mma)
+
+def test_e4m3_encoder_matches_torch_rounding():
+    # every e4m3 value, every midpoint between neighbours (ties to even), and
+    # random floats in range, against torch's float32 -> float8_e4m3fn cast
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float()
+    fin = vals[torch.isfinite(vals)].unique()
+    mids = (fin[1:] + fin[:-1]) / 2
+    g = torch.Generator().manual_seed(61)
+    rnd = (torch.rand(20000, generator=g) * 2 - 1) * 448 * torch.rand(20000, generator=g) ** 6
+    xs = torch.cat([fin, mids, rnd, -rnd]).float()
+    want = xs.to(torch.float8_e4m3fn).view(torch.uint8).tolist()
+    got = [oracle.e4m3_encode(x) for x in xs.tolist()]
+    assert got == want
+    # saturation and NaN, from the format (448 is the largest finite value)
+    assert oracle.e4m3_encode(449.0) == 0x7E and oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(-1e30) == 0xFE and oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_f16_rounding_matches_numpy():
+    g = np.random.default_rng(62)
+    xs = np.concatenate([g.standard_normal(20000) * 10.0 ** g.integers(-9, 5, 20000),
+                         np.float16(np.arange(1, 2000, dtype=np.float16)).astype(np.float64) * 1.000244140625])
+    for x in xs[:5000].tolist() + xs[20000:].tolist():
+        assert oracle.f16_round(x) == float(np.float16(x))
+
+
+def _mma_case(seed, lens=(257, 1, 40), exact_q=False, G=4, paged=False):
+    w = W.make_gqa(name="fp8mma", batch=len(lens), num_q_heads=2 * G, num_kv_heads=2,
+                   seq_lens=list(lens), cache_len=None if paged else max(lens), kv_fp8=True,
+                   layout="paged" if paged else "contiguous", page_size=16, seed=seed)
+    w.fp8_mma = True
+    if exact_q:
+        # query rows of e4m3 values times a power of two, each holding 448 * 2^j:
+        # the quantisation is then exact (scale 2^j, codes the values themselves)
+        g = torch.Generator().manual_seed(seed + 1)
+        codes = torch.randint(0, 256, w.tensors["q"].shape, generator=g, dtype=torch.int32)
+        v = codes.to(torch.uint8).view(torch.float8_e4m3fn).float()
+        v = torch.where(torch.isfinite(v), v, torch.zeros_like(v))
+        v[..., 0] = 448.0
+        j = torch.randint(-8, 3, w.tensors["q"].shape[:-1] + (1,), generator=g).float()
+        w.tensors["q"] = (v * torch.exp2(j)).to(torch.bfloat16)
+    return w
+
+
+def test_fp8_mma_single_key_returns_the_value_row_and_exact_queries_keep_their_scores():
+    w = _mma_case(63, lens=(1, 1, 1), exact_q=True)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    plain = oracle.problem_from(w)
+    plain["fp8_mma"] = 0
+    ref_out, ref_lse = oracle.decode(plain, w.tensors, w.scale)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+
+
+def test_fp8_mma_equal_scores_give_the_mean():
+    # q = 0: every weight is 1 (exact in e4m3 after the 2^8 scaling): the mean of the values
+    w = _mma_case(64, lens=(300, 17, 2))
+    w.tensors["q"] = torch.zeros_like(w.tensors["q"])
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    plain = oracle.problem_from(w)
+    plain["fp8_mma"] = 0
+    ref_out, ref_lse = oracle.decode(plain, w.tensors, w.scale)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+
+
+def test_fp8_mma_weight_rounding_stays_within_the_reported_bound():
+    # with exactly representable queries, the only difference from exact weights is
+    # the rounding of the weights, which the bound covers (one side rounds)
+    w = _mma_case(65, lens=(1000, 64, 3), exact_q=True)
+    out, lse, bound = oracle.decode_p8_bound(oracle.problem_from(w), w.tensors, w.scale)
+    plain = oracle.problem_from(w)
+    plain["fp8_mma"] = 0
+    ref_out, ref_lse = oracle.decode(plain, w.tensors, w.scale)
+    assert np.array_equal(lse, ref_lse)
+    assert np.all(np.abs(out - ref_out) <= bound * (1 + 1e-12))
+    assert np.max(np.abs(out - ref_out)) > 0  # the rounding did act
+
+
+def test_fp8_mma_brute_force():
+    """50-digit evaluation with the roundings done by torch's own casts:
+    the query in fp32 steps (amax, 448 / amax, q * inv, e4m3 cast, amax / 448),
+    the weights through float16 then float8_e4m3fn."""
+    getcontext().prec = 50
+    w = _mma_case(66, lens=(9, 2, 5), G=2)
+    w.tensors["q"] = (w.tensors["q"].float() * 37.0).to(torch.bfloat16)
+    out, lse = oracle.decode(oracle.problem_from(w), w.tensors, w.scale)
+    t = w.tensors
+    k = t["k"].double() * t["k_scale"].double().view(1, -1, 1, 1)
+    v = t["v"].double() * t["v_scale"].double().view(1, -1, 1, 1)
+    for b in range(w.batch):
+        for hq in range(w.num_q_heads):
+            h = hq // (w.num_q_heads // w.num_kv_heads)
+            q = t["q"][b, hq].float()
+            amax = q.abs().max()
+            inv = torch.tensor(448.0, dtype=torch.float32) / amax
+            codes = (q * inv).clamp(-448, 448).to(torch.float8_e4m3fn).float().double()
+            sq = float(amax / torch.tensor(448.0, dtype=torch.float32))
+            qt = [_dec(c) * _dec(sq) for c in codes.tolist()]
+            n = int(t["seq_lens"][b])
+            s = [_dec(w.scale) * sum(a * _dec(c) for a, c in zip(qt, k[b, h, j].tolist())) for j in range(n)]
+            m = max(s)
+            p = [(x - m).exp() for x in s]
+            l = sum(p)
+            wts = []
+            for pj in p:
+                y = torch.tensor(float(256 * pj), dtype=torch.float64).to(torch.float16).float()
+                wts.append(_dec(float(y.to(torch.float8_e4m3fn).float())) / 256)
+            for d in range(w.head_dim_v):
+                ref = float(sum(wj * _dec(v[b, h, j, d]) for j, wj in enumerate(wts)) / l)
+                assert abs(out[b, hq, d] - ref) < 1e-12
+            assert abs(lse[b, hq] - float(m + l.ln())) < 1e-12
