@@ -203,6 +203,8 @@ def workload_name(cfg, args):
         name += f", tanh soft cap {args.softcap:g}"
     if args.seed is not None:
         name += f", seed {args.seed}"
+    if args.fp8_mma:
+        name += ", e4m3 tensor-core QK/PV (fp8_mma)"
     return name
 
 
@@ -459,8 +461,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=None,
                     help="another draw of the workload's recipe (default: its own seed, 1000 + config)")
+    ap.add_argument("--fp8-mma", action="store_true",
+                    help="e4m3 K/V configurations: QK and PV on e4m3 tensor cores (queries and "
+                         "weights rounded to e4m3)")
     args = ap.parse_args()
     w = W.config(args.config, seed=args.seed)
+    if args.fp8_mma:
+        if not w.kv_fp8 or w.kv_token_scale:
+            raise SystemExit("--fp8-mma needs a configuration with e4m3 K/V and per-head scales")
+        w.fp8_mma = True
     if args.tree_mask:
         if w.q_len < 2:
             raise SystemExit("--tree-mask needs a configuration with several query tokens")

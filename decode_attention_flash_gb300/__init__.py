@@ -49,6 +49,7 @@ class Problem(ctypes.Structure):
         ("sparse_block_size", ctypes.c_int32), ("max_sparse_blocks", ctypes.c_int32),
         ("q_len", ctypes.c_int32), ("sparse_batch", ctypes.c_int32),
         ("sparse_heads", ctypes.c_int32), ("kv_groups", ctypes.c_int32),
+        ("fp8_mma", ctypes.c_int32),
     ]
 
 
@@ -325,4 +326,4 @@ def problem_kwargs(work) -> dict:
                 kv_groups=getattr(w, "kv_int4_groups", 0),
                 sparse_block_size=w.sparse_block_size, max_sparse_blocks=w.max_sparse_blocks,
                 q_len=getattr(w, "q_len", 1), sparse_batch=getattr(w, "sparse_batch", 0),
-                sparse_heads=getattr(w, "sparse_heads", 0))
+                sparse_heads=getattr(w, "sparse_heads", 0), fp8_mma=int(getattr(w, "fp8_mma", False)))

@@ -286,6 +286,7 @@ da_status run_gqa(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   gp.max_sparse_blocks = p.max_sparse_blocks;
   gp.sparse_batch = p.sparse_batch > 0 ? p.sparse_batch : std::max(p.batch, 1);
   gp.sparse_heads = p.sparse_heads > 0 ? p.sparse_heads : p.num_kv_heads;
+  gp.fp8_mma = p.fp8_mma;
   gp.test_stall_ns = ctx->test_stall_ns;
   ctx->test_stall_ns = 0;  // one call only
   if (da::launch_gqa(fp8, gp.group, ctx->kmap, ctx->vmap, ctx->qmap,

@@ -24,6 +24,7 @@ cudaError_t gqa_prepare(int /*device*/) {
   if ((e = gqa_prepare_kind_bf16()) != cudaSuccess) return e;
   if ((e = gqa_prepare_kind_e4m3()) != cudaSuccess) return e;
   if ((e = gqa_prepare_kind_e4m3_token()) != cudaSuccess) return e;
+  if ((e = gqa_prepare_kind_e4m3_mma()) != cudaSuccess) return e;
   return gqa_prepare_kind_int4();
 }
 
@@ -43,6 +44,8 @@ cudaError_t launch_gqa(bool fp8, int group, const CUtensorMap &kmap, const CUten
     return gqa_launch_kind_int4(two, mod, kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   if (p.token_scale)
     return gqa_launch_kind_e4m3_token(two, mod, kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
+  if (p.fp8_mma)
+    return gqa_launch_kind_e4m3_mma(two, mod, kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
   return gqa_launch_kind_e4m3(two, mod, kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream);
 }
 

@@ -780,7 +780,7 @@ __device__ __forceinline__ bool count_piece(const GqaParams &p, volatile int *fl
 // words, a soft cap); 2 -- the flex-style mods too (the sink/window mask_mod and
 // the ALiBi score_mod, per query head), in an instantiation of their own so
 // that the other two keep their registers.
-template <bool FP8, int NT, bool TOK, bool I4, int MOD>
+template <bool FP8, int NT, bool TOK, bool I4, int MOD, bool Q8>
 __global__ void __launch_bounds__(threads_for<NT>(), 2)
     gqa_split_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -789,6 +789,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
                      const __grid_constant__ CUtensorMap vssmap, const GqaParams p) {
   using C = Cfg<FP8, NT, TOK, I4>;
   static_assert(!TOK || FP8, "per-token scales are an e4m3 format");
+  static_assert(!Q8 || (FP8 && !TOK && !I4), "e4m3 tensor-core arithmetic: per-head e4m3 K/V");
   constexpr int kThreads = threads_for<NT>();
   constexpr bool kHelper = has_helper<NT>();
   extern __shared__ uint8_t smem_raw[];
@@ -1226,6 +1227,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
     const uint32_t toff_a = token_offset<FP8>(tok_lane + (mi & 1) * 8, br_shift);
     const uint32_t toff_b = token_offset<FP8>(tok_lane + (mi >> 1) * 8, br_shift);
     uint32_t qf[NT][8][2];
+    // fp8_mma (Q8): e4m3 query fragments (B operand of the k32 MMAs: dims
+    // 32pp + 16j + 4q4 .. +3 of row r8) and the score factor of the thread's
+    // rows nt * 8 + 2 * q4 + e, which holds each row's e4m3 scale
+    uint32_t qf8[NT][4][2];
+    float rq[NT][2];
     float oacc[NT][8][4];
     float m_run[NT][2], l_part[NT][2];
     float sscale = p.score_scale, vmul = 1.f;
@@ -1301,7 +1307,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         // below that largest one becomes an f16 subnormal: an error under 2^-28
         // of the largest product), and 2^-e joins the score factor.
         int qexp = 0;
-        if (FP8) {
+        if (FP8 && !Q8) {
           float amax = 0.f;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -1313,12 +1319,42 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           qexp = q_exponent(amax);
         }
         const float q2 = pow2f(qexp);
+        float qsq[NT];  // Q8: the e4m3 scale of the lane's row r8
+        if (Q8) {
+          // e4m3 queries in fp32 steps: amax = max |q| of the row, inv = 448 /
+          // amax, code = e4m3(q * inv) to nearest even, saturating; the row's
+          // scale amax / 448 goes into its score factor (rows with amax below
+          // 2^-100 are zero)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int g = nt * 8 + r8;
+            const uint32_t *qrow = qs + (g < G ? g : 0) * (kD / 2);
+            float amax = q_row_amax(qrow, q4, r8);
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const bool tiny = !(amax >= 0x1p-100f);
+            const float inv = tiny ? 0.f : __fdiv_rn(448.f, amax);
+            qsq[nt] = tiny ? 0.f : __fdiv_rn(amax, 448.f);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int d0 = 32 * pp + 16 * j + 4 * q4;  // four consecutive dims
+                const uint32_t w0 = qrow[d0 / 2], w1 = qrow[d0 / 2 + 1];
+                const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(w0 << 16), inv),
+                                                    __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), inv));
+                const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(__uint_as_float(w1 << 16), inv),
+                                                    __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), inv));
+                qf8[nt][pp][j] = g < G ? (lo | (hi << 16)) : 0u;
+              }
+          }
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int g = nt * 8 + r8;
           const uint32_t *qrow = qs + (g < G ? g : 0) * (kD / 2);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+          for (int ks = 0; ks < 8 && !Q8; ++ks) {
             if (I4) {
               // k-step 2c+s pairs the elements one int4 data word gives a lane:
               // 32c + 8q4 + 2s + {0, 4} (b0) and 32c + 8q4 + 2s + 1 + {0, 4} (b1)
@@ -1364,10 +1400,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         } else if (FP8 && !I4) {
           sscale = p.score_scale * p.k_scale[h];
           vmul = p.v_scale[h];
+          if (Q8) vmul *= 0.00390625f;  // the weights met V scaled by 2^8
         } else {
           sscale = p.score_scale;
         }
         if (FP8) sscale *= pow2f(-qexp);
+        if (Q8) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) rq[nt][e] = sscale * __shfl_sync(0xffffffffu, qsq[nt], 4 * (2 * q4 + e));
+        }
         if (MOD >= 1 && p.spec_mask != nullptr) {
           const uint32_t *mrow = p.spec_mask + (size_t)(unit / p.num_kv_heads) * p.q_len;
 #pragma unroll
@@ -1426,6 +1469,17 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
               for (int nt = 0; nt < NT; ++nt)
                 mma_bf16_16816(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
             }
+          } else if (Q8) {
+            // e4m3 K straight from ldmatrix: the four 8x16-byte matrices (rows 0-7
+            // and 8-15, bytes 32pp..+15 and +16..+31) are the k32 A fragment
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+              uint32_t r0, r1, r2, r3;
+              ldsm_x4(chunk_addr<true>(kbase, toff_a, t, 2 * pp + (mi >> 1), br_shift), r0, r1, r2, r3);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_e4m3_16832(sacc[nt], r0, r1, r2, r3, qf8[nt][pp][0], qf8[nt][pp][1]);
+            }
           } else {
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
@@ -1483,7 +1537,8 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             bool ok0 = ok_r && (MOD == 0 || jnew < 0 || ((mword[nt][e] >> min(jnew, 31)) & 1u));
             bool ok1 =
                 ok_r8 && (MOD == 0 || jnew + 8 < 0 || ((mword[nt][e] >> min(jnew + 8, 31)) & 1u));
-            float x0 = sacc[nt][e] * sscale, x1 = sacc[nt][2 + e] * sscale;
+            const float f = Q8 ? rq[nt][e] : sscale;
+            float x0 = sacc[nt][e] * f, x1 = sacc[nt][2 + e] * f;
             if (softcap) {  // c * tanh(s / c), in log2 units: c2 * tanh(x / c2)
               x0 = cap_tanh(x0, p.softcap_l2, p.softcap_k);
               x1 = cap_tanh(x1, p.softcap_l2, p.softcap_k);
@@ -1532,12 +1587,25 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             oacc[nt][mt][2] *= alpha[0];
             oacc[nt][mt][3] *= alpha[1];
           }
-          const uint32_t x0 = FP8 ? pack_f16(sacc[nt][0], sacc[nt][1])
-                                  : pack_bf16(sacc[nt][0], sacc[nt][1]);
-          const uint32_t x1 = FP8 ? pack_f16(sacc[nt][2], sacc[nt][3])
-                                  : pack_bf16(sacc[nt][2], sacc[nt][3]);
-          pb[nt][0] = movmatrix_trans(x0);
-          pb[nt][1] = movmatrix_trans(x1);
+          if (Q8) {
+            // the weights times 2^8 as f16, transposed (lane (g, t): tokens 2t,
+            // 2t+1 and 8+2t, 9+2t of head g), then rounded to e4m3: bytes in the
+            // token order (2t, 2t+1, 8+2t, 9+2t) of k 4t..4t+3 (tokens 16-31 of
+            // the k32 step are absent: 0)
+            const uint32_t y0 = movmatrix_trans(pack_f16(256.f * sacc[nt][0], 256.f * sacc[nt][1]));
+            const uint32_t y1 = movmatrix_trans(pack_f16(256.f * sacc[nt][2], 256.f * sacc[nt][3]));
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&y0));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&y1));
+            pb[nt][0] = f32x2_to_e4m3x2(f0.x, f0.y) | (f32x2_to_e4m3x2(f1.x, f1.y) << 16);
+            pb[nt][1] = 0u;
+          } else {
+            const uint32_t x0 = FP8 ? pack_f16(sacc[nt][0], sacc[nt][1])
+                                    : pack_bf16(sacc[nt][0], sacc[nt][1]);
+            const uint32_t x1 = FP8 ? pack_f16(sacc[nt][2], sacc[nt][3])
+                                    : pack_bf16(sacc[nt][2], sacc[nt][3]);
+            pb[nt][0] = movmatrix_trans(x0);
+            pb[nt][1] = movmatrix_trans(x1);
+          }
         }
         // ---------------- O^T += V^T P^T (masked tokens' V zeroed in registers)
         const bool full16 = vbits == 0xFFFFu;
@@ -1604,6 +1672,31 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_bf16_16816(oacc[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+          }
+        } else if (Q8) {
+          // e4m3 V^T (k32 A fragment, tokens in the order (2t, 2t+1, 8+2t, 9+2t) of
+          // the weights): ldmatrix.trans on byte pairs gives lane (g, t) tokens
+          // 2t, 2t+1 (r0: 0-7, r1: 8-15) x dims 2g, 2g+1 of a 16-dim chunk; a byte
+          // permutation splits the two dims into rows g (dim 2g) and g + 8 (dim
+          // 2g + 1) of the m-tile (the dim order the epilogue undoes)
+          const int t = tok_lane + (mi & 1) * 8;
+          const uint32_t tmask = full16 ? 0xFFFFFFFFu
+                                        : (((vbits >> (2 * q4)) & 1u) ? 0x000000FFu : 0u) |
+                                              (((vbits >> (2 * q4 + 1)) & 1u) ? 0x0000FF00u : 0u) |
+                                              (((vbits >> (2 * q4 + 8)) & 1u) ? 0x00FF0000u : 0u) |
+                                              (((vbits >> (2 * q4 + 9)) & 1u) ? 0xFF000000u : 0u);
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(chunk_addr<true>(vbase, toff_a, t, 2 * pp + (mi >> 1), br_shift), r0, r1, r2, r3);
+            // tokens past the row's end may hold anything (NaN): zero their bytes
+            const uint32_t a0 = prmt(r0, r1, 0x6420) & tmask, a1 = prmt(r0, r1, 0x7531) & tmask;
+            const uint32_t c0 = prmt(r2, r3, 0x6420) & tmask, c1 = prmt(r2, r3, 0x7531) & tmask;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_e4m3_16832(oacc[nt][2 * pp], a0, a1, 0u, 0u, pb[nt][0], 0u);
+              mma_e4m3_16832(oacc[nt][2 * pp + 1], c0, c1, 0u, 0u, pb[nt][0], 0u);
+            }
           }
         } else {
           const int t = tok_lane + (mi & 1) * 8;
@@ -1888,18 +1981,18 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
   if (dev_err) atomicOr(p.err, dev_err);
 }
 
-template <bool FP8, int NT, bool TOK, bool I4, int MOD>
+template <bool FP8, int NT, bool TOK, bool I4, int MOD, bool Q8>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK, I4, MOD>,
+  return cudaFuncSetAttribute(gqa_split_kernel<FP8, NT, TOK, I4, MOD, Q8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<FP8, NT, TOK, I4>::kTotal);
 }
 
-template <bool FP8, int NT, bool TOK, bool I4, int MOD>
+template <bool FP8, int NT, bool TOK, bool I4, int MOD, bool Q8>
 void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &qmap,
             const CUtensorMap &kssmap, const CUtensorMap &vssmap, const GqaParams &p, int ctas,
             cudaStream_t stream) {
-  gqa_split_kernel<FP8, NT, TOK, I4, MOD>
+  gqa_split_kernel<FP8, NT, TOK, I4, MOD, Q8>
       <<<ctas, threads_for<NT>(), Cfg<FP8, NT, TOK, I4>::kTotal, stream>>>(kmap, vmap, qmap, kssmap,
                                                                            vssmap, p);
 }
@@ -1907,23 +2000,24 @@ void launch(const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap 
 // The six instantiations of one element kind (one or two n-tiles; no, some or
 // all score modifications), set up and launched from that kind's own
 // translation unit.
-template <bool FP8, bool TOK, bool I4>
+template <bool FP8, bool TOK, bool I4, bool Q8 = false>
 cudaError_t prepare_kind() {
   cudaError_t e;
-  if ((e = set_attr<FP8, 1, TOK, I4, 0>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 2, TOK, I4, 0>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 1, TOK, I4, 1>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 2, TOK, I4, 1>()) != cudaSuccess) return e;
-  if ((e = set_attr<FP8, 1, TOK, I4, 2>()) != cudaSuccess) return e;
-  return set_attr<FP8, 2, TOK, I4, 2>();
+  if ((e = set_attr<FP8, 1, TOK, I4, 0, Q8>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 2, TOK, I4, 0, Q8>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 1, TOK, I4, 1, Q8>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 2, TOK, I4, 1, Q8>()) != cudaSuccess) return e;
+  if ((e = set_attr<FP8, 1, TOK, I4, 2, Q8>()) != cudaSuccess) return e;
+  return set_attr<FP8, 2, TOK, I4, 2, Q8>();
 }
 
-template <bool FP8, bool TOK, bool I4>
+template <bool FP8, bool TOK, bool I4, bool Q8 = false>
 cudaError_t launch_kind(bool two, int mod, const CUtensorMap &kmap, const CUtensorMap &vmap,
                         const CUtensorMap &qmap, const CUtensorMap &kssmap,
                         const CUtensorMap &vssmap, const GqaParams &p, int ctas,
                         cudaStream_t stream) {
-#define DA_LAUNCH(NT, M) launch<FP8, NT, TOK, I4, M>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream)
+#define DA_LAUNCH(NT, M) \
+  launch<FP8, NT, TOK, I4, M, Q8>(kmap, vmap, qmap, kssmap, vssmap, p, ctas, stream)
   if (mod == 0) two ? DA_LAUNCH(2, 0) : DA_LAUNCH(1, 0);
   else if (mod == 1) two ? DA_LAUNCH(2, 1) : DA_LAUNCH(1, 1);
   else two ? DA_LAUNCH(2, 2) : DA_LAUNCH(1, 2);
@@ -1945,6 +2039,7 @@ cudaError_t launch_kind(bool two, int mod, const CUtensorMap &kmap, const CUtens
 DA_GQA_KIND_DECL(bf16)
 DA_GQA_KIND_DECL(e4m3)
 DA_GQA_KIND_DECL(e4m3_token)
+DA_GQA_KIND_DECL(e4m3_mma)
 DA_GQA_KIND_DECL(int4)
 #undef DA_GQA_KIND_DECL
 

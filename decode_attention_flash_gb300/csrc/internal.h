@@ -53,6 +53,7 @@ struct GqaParams {
   int32_t capacity;            // max positions per row
   int32_t sparse_block_size, max_sparse_blocks;
   int32_t sparse_batch, sparse_heads;  // block tables' extents (row (b % SZ, h % SH))
+  int32_t fp8_mma;             // e4m3 tensor-core QK / PV (the e4m3_mma instantiations)
   uint32_t test_stall_ns;      // 0; else (tests of the timeout path only) the first
                                // pipeline wait of consumer warp 0 is one on a barrier
                                // that nothing arrives on, given up after this long

@@ -30,6 +30,9 @@ da_status validate_problem(const da_problem *p) {
   if (!p) return DA_ERR_INVALID_ARG;
   if (p->batch <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return DA_ERR_INVALID_ARG;
   if (p->q_dtype != DA_DTYPE_BF16) return DA_ERR_UNSUPPORTED;
+  if (p->fp8_mma != 0 && p->fp8_mma != 1) return DA_ERR_INVALID_ARG;
+  // e4m3 tensor-core arithmetic: e4m3 K/V with per-kv-head scales, GQA
+  if (p->fp8_mma && (p->is_mla || p->kv_dtype != DA_DTYPE_FP8_E4M3)) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout != DA_KV_CONTIGUOUS && p->kv_layout != DA_KV_PAGED) return DA_ERR_INVALID_ARG;
   if (p->kv_dtype != DA_DTYPE_BF16 && p->kv_dtype != DA_DTYPE_FP8_E4M3 &&
       p->kv_dtype != DA_DTYPE_FP8_E4M3_TOKEN_SCALE && p->kv_dtype != DA_DTYPE_INT4_GROUPS)

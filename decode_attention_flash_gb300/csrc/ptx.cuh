@@ -168,6 +168,27 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D (16x8 fp32) += A (16x32 e4m3, row) * B (32x8 e4m3, col): the 8-bit k32 shape;
+// A and B registers hold four consecutive k elements each, lowest byte first.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> two e4m3 bytes, round to nearest even, saturating to +-448:
+// `lo` in bits 0..7, `hi` in bits 8..15 (the instruction puts its first
+// source in the upper byte).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return (uint32_t)d;
+}
+
 // Two e4m3 bytes (low byte first) -> f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   uint32_t d;

@@ -130,6 +130,15 @@ typedef struct {
                                  2 groups are not a multiple of 16 bytes: unsupported);
                                  contiguous caches need max_seq_len a multiple of 8 (4
                                  groups) or 4 (8 groups) */
+  int32_t fp8_mma;            /* GQA with DA_DTYPE_FP8_E4M3 K/V only, optional: 1 runs QK and PV
+                                 on e4m3 tensor cores. Each query row is quantised to e4m3
+                                 in fp32 steps (amax = max |q|, code = e4m3(q * (448 / amax)),
+                                 round to nearest even, saturating; the row's scale amax /
+                                 448 joins the score factor), and the softmax weights that
+                                 meet V are scaled by 2^8, rounded to f16 and then to e4m3
+                                 (the row sum uses the unrounded weights). The e4m3 QK
+                                 products are exact; the weights' rounding (3 mantissa bits)
+                                 is the mode's approximation. 0 = f16 arithmetic */
 } da_problem;
 
 /*

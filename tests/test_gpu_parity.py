@@ -796,3 +796,81 @@ def test_flex_mods_refused_for_mla_and_alibi_with_softcap():
     with pytest.raises(da.DecodeAttnError) as e:
         run_gpu(w, softcap=5.0)
     assert e.value.status == da.DA_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ e4m3 tensor-core arithmetic (fp8_mma)
+
+def _assert_p8(out, lse, w, what):
+    """Parity of the fp8_mma path: the oracle quantises the queries exactly as the
+    kernel does, so the LSE keeps its 1e-3; the weights that meet V are rounded to
+    e4m3 by both, the kernel against its running maximum and the oracle against the
+    row's, so the outputs may differ by twice the weights' rounding bound, plus the
+    bf16 rounding of the output (2^-8 relative) and fp32 slack."""
+    import oracle
+    ref_out, ref_lse, bound = oracle.decode_p8_bound(oracle.problem_from(w), w.tensors, w.scale)
+    got = out.double().numpy()
+    assert np.all(np.isfinite(got)), what
+    excess = np.abs(got - ref_out) - (2 * bound + 2.0 ** -8 * np.abs(ref_out) + 1e-4)
+    assert np.all(excess <= 0), f"{what}: worst excess {excess.max():.3e}"
+    fin = np.isfinite(ref_lse)
+    lg = lse.double().numpy()
+    assert np.array_equal(np.isfinite(lg), fin), what
+    if fin.any():
+        assert np.max(np.abs(lg[fin] - ref_lse[fin])) <= 1e-3, what
+    return float(np.max(np.abs(got - ref_out)))
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "paged", "g16", "query_tokens", "softcap", "mods",
+                                  "sparse"])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_fp8_mma(kind, splits):
+    lens = [3000, 1, 77, 700]
+    if kind == "g16":
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=32, num_kv_heads=2, seq_lens=lens,
+                       cache_len=3000, kv_fp8=True, seed=950)
+    elif kind == "query_tokens":
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=16, num_kv_heads=4, seq_lens=lens,
+                       layout="paged", page_size=16, q_len=3, kv_fp8=True, seed=951)
+    elif kind == "sparse":
+        g = torch.Generator().manual_seed(952)
+        num, idx = W.sparse_lists(2, 4, 4096, 128, keep_random=5, keep_last=2, g=g, max_blocks=12)
+        w = W.make_gqa(name=kind, batch=2, num_q_heads=16, num_kv_heads=4, seq_lens=[4096, 4000],
+                       cache_len=4096, sparse_block_size=128, kv_num_blks=num, kv_idx=idx,
+                       kv_fp8=True, seed=953)
+    else:
+        w = W.make_gqa(name=kind, batch=4, num_q_heads=32, num_kv_heads=4, seq_lens=lens,
+                       layout="paged" if kind != "contiguous" else "contiguous", page_size=16,
+                       cache_len=3000 if kind == "contiguous" else None, kv_fp8=True, seed=954)
+    if kind == "mods":
+        w.tensors["mask_window"] = torch.tensor([100, -1, 5, 2000] * 8, dtype=torch.int32)
+        w.tensors["alibi_slopes"] = torch.linspace(-0.02, 0.05, 32, dtype=torch.float32)
+    w.fp8_mma = True
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits, softcap=30.0 if kind == "softcap" else 0.0)
+    assert flags == 0
+    if kind == "softcap":
+        import oracle
+        ref_out, ref_lse, bound = oracle.decode_p8_bound(oracle.problem_from(w), w.tensors, w.scale,
+                                                         softcap=30.0)
+        got = out.double().numpy()
+        assert np.all(np.abs(got - ref_out) <= 2 * bound + 2.0 ** -8 * np.abs(ref_out) + 1e-4)
+        assert np.max(np.abs(lse.double().numpy() - ref_lse)) <= 1e-3
+    else:
+        _assert_p8(out, lse, w, f"fp8_mma {kind} S={splits}")
+
+
+def test_fp8_mma_full_size_long_context():
+    w = W.config(3)
+    w.fp8_mma = True
+    out, lse, flags, _ = run_gpu(w)
+    assert flags == 0
+    err = _assert_p8(out, lse, w, "fp8_mma config 3 shapes")
+    assert err <= 3e-2  # the fp8 tolerance holds at this length (the weights' errors average out)
+
+
+def test_fp8_mma_refused_for_other_caches():
+    w = W.make_gqa(name="bf16_mma", batch=1, num_q_heads=8, num_kv_heads=2, seq_lens=[100],
+                   cache_len=100, seed=955)
+    w.fp8_mma = True
+    with pytest.raises(da.DecodeAttnError) as e:
+        run_gpu(w)
+    assert e.value.status == da.DA_ERR_UNSUPPORTED
