@@ -68,7 +68,6 @@ da_status validate_problem(const da_problem *p) {
   if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (G * Q > 16) return DA_ERR_UNSUPPORTED;  // the G x Q rows of a kv head: two n-tiles at most
-  if (Q > 1 && p->sparse_block_size > 0) return DA_ERR_UNSUPPORTED;
   if (p->head_dim_qk != 128 || p->head_dim_v != 128) return DA_ERR_UNSUPPORTED;
   if (p->kv_layout == DA_KV_PAGED) {
     const int P = p->page_size;

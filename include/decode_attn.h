@@ -12,8 +12,8 @@
  * (each block of sparse_block_size positions, clipped to seq_lens[b]). An empty
  * P gives out = 0 and lse = -inf.
  *
- * Several query tokens per row (q_len = Q > 1, speculative decoding; GQA with a
- * dense cache): the row's new tokens are its last Q positions, already in the
+ * Several query tokens per row (q_len = Q > 1, speculative decoding; GQA): the
+ * row's new tokens are its last Q positions, already in the
  * cache, and query token t < Q attends to the positions n <= seq_lens[b] - Q + t
  * of P(b,h) -- the causal mask of the split-K decode kernel (mslk
  * splitk_kernels.py, `_fwd_kernel_splitK` with IS_CAUSAL). q, out and lse then
@@ -107,8 +107,9 @@ enum {
  *        sparse_heads (SZ, SH; 0 = B and HKV) are the block tables' first two
  *        extents: row b and kv head h read table row (b % SZ, h % SH), the
  *        broadcast of the flex decode template (SPARSE_Z, SPARSE_HQ).
- *   q_len: query tokens per row, 0 or 1 = one. Q > 1 needs GQA, a dense
- *        cache and G * Q <= 16 (the G*Q rows of a kv head share one pass).
+ *   q_len: query tokens per row, 0 or 1 = one. Q > 1 needs GQA and G * Q <= 16
+ *        (the G*Q rows of a kv head share one pass); block-sparse tables apply
+ *        to every query token, the causal or tree mask on top of them.
  */
 typedef struct {
   int32_t batch, num_q_heads, num_kv_heads;

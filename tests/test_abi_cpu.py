@@ -235,10 +235,9 @@ def test_several_query_tokens_per_row(lib):
             with pytest.raises(da.DecodeAttnError) as e:
                 da.decode_attn_plan_info(prob, 152)
             assert e.value.status == status
+    # several query tokens over block-sparse tables are planned like the dense case
     sparse = dict(base, sparse_block_size=64, max_sparse_blocks=1, q_len=2)
-    with pytest.raises(da.DecodeAttnError) as e:
-        da.decode_attn_plan_info(da.make_problem(**sparse), 152)
-    assert e.value.status == da.DA_ERR_UNSUPPORTED
+    assert da.decode_attn_plan_info(da.make_problem(**sparse), 152)["rows_per_unit"] == 8
     m = W.config(5, shape_only=True)
     with pytest.raises(da.DecodeAttnError) as e:
         da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=2)), 152)

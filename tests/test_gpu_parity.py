@@ -874,3 +874,17 @@ def test_fp8_mma_refused_for_other_caches():
     with pytest.raises(da.DecodeAttnError) as e:
         run_gpu(w)
     assert e.value.status == da.DA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("q_len,tree", [(2, False), (4, False), (3, True)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_several_query_tokens_on_block_sparse_rows(q_len, tree, splits):
+    g = torch.Generator().manual_seed(960 + q_len)
+    num, idx = W.sparse_lists(3, 2, 4096, 128, keep_random=6, keep_last=2, g=g, max_blocks=12)
+    w = W.make_gqa(name="sparse_q", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[4096, 4000, 3970],
+                   cache_len=4096, sparse_block_size=128, kv_num_blks=num, kv_idx=idx, q_len=q_len,
+                   tree_mask=tree, seed=961 + q_len)
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"sparse q_len={q_len} tree={tree} S={splits}")

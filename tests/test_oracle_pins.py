@@ -387,6 +387,11 @@ def _tiny_cases():
     cases.append(W.make_gqa(name="tree_q4_paged", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=4, seq_lens=[6, 4], layout="paged", page_size=2, seed=20,
                             scale=0.7, q_len=4, tree_mask=True))
+    # several query tokens over a block-sparse row: the causal mask on the listed blocks
+    cases.append(W.make_gqa(name="sparse_q3", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
+                            seq_lens=[8, 5], cache_len=8, sparse_block_size=2,
+                            kv_num_blks=[[3, 1], [2, 2]], kv_idx=[[[3, 0, 1], [2, 0, 0]], [[2, 1, 0], [0, 2, 0]]],
+                            seed=29, scale=0.7, q_len=3))
     # flex-style mods: a per-query-head sink/window mask (heads of one group with
     # different windows, one without a window) and ALiBi slopes
     mw = W.make_gqa(name="sink_window", batch=2, num_q_heads=4, num_kv_heads=2, head_dim=4,
