@@ -74,7 +74,7 @@ constexpr int kKvBlock = kTok * 128;      // 8 KB: 64 tokens x 64 bf16
 constexpr int kKpeBlock = kTok * 64;     // 4 KB: 64 tokens x 32 bf16, 64B-swizzled
 constexpr int kKvStage = 4 * kKvBlock + kKpeBlock;  // 4 ckv blocks + the kpe half
 constexpr int kQpeBlock = kHeads * 64;   // 8 KB: 128 rows x 32 bf16, 64B-swizzled
-constexpr int kXBytes = kHeads * kTok * 4;  // one exchange buffer: 128 x 64 fp32
+constexpr int kXBytes = kHeads * kTok * 3;  // one exchange buffer: 128 x 64 scores, 24 bits each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // O half: columns 0..255
 constexpr uint32_t kTmemQ = 256;   // q_nope half, two bf16 per column: 256..383
@@ -101,7 +101,7 @@ struct Ctrl {
 struct Lay {
   static constexpr int QPE = 0;                              // 8 KB
   static constexpr int KV = QPE + kQpeBlock;                 // kStages x 36 KB
-  static constexpr int X = KV + kStages * kKvStage;          // 2 x [16][128] float4
+  static constexpr int X = KV + kStages * kKvStage;          // 2 x [12][128] uint4
   static constexpr int MR = X + 2 * kXBytes;                 // [2][128] running maximum
   static constexpr int LR = MR + 2 * kHeads * 4;             // [2][128] running sum
   static constexpr int META = LR + 2 * kHeads * 4;           // [kStages] TileMeta
@@ -154,6 +154,30 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
           addr),
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
+}
+
+__device__ __forceinline__ void st_async_u4(uint32_t addr, uint4 v, uint32_t remote_bar) {
+  st_async_v4(addr, __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+              __uint_as_float(v.w), remote_bar);
+}
+
+// Partial scores cross the cluster as the upper three bytes of their fp32
+// encoding (sign, exponent, 15 mantissa bits: a relative error below 2^-15,
+// far inside the bf16 rounding of the weights they become), four scores in
+// three words. DSMEM bandwidth, not arithmetic, limits the exchange.
+__device__ __forceinline__ void pack24(const float *s, uint32_t *w) {
+  const uint32_t a = __float_as_uint(s[0]), b = __float_as_uint(s[1]);
+  const uint32_t c = __float_as_uint(s[2]), d = __float_as_uint(s[3]);
+  w[0] = prmt(a, b, 0x5321);  // a1 a2 a3 b1
+  w[1] = prmt(b, c, 0x6532);  // b2 b3 c1 c2
+  w[2] = prmt(c, d, 0x7653);  // c3 d1 d2 d3
+}
+
+__device__ __forceinline__ void unpack24_add(const uint32_t *w, float *s) {
+  s[0] += __uint_as_float(w[0] << 8);
+  s[1] += __uint_as_float(prmt(w[0], w[1], 0x5430) & 0xffffff00u);
+  s[2] += __uint_as_float(prmt(w[1], w[2], 0x4320) & 0xffffff00u);
+  s[3] += __uint_as_float(w[2] & 0xffffff00u);
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
@@ -624,27 +648,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                              // TMEM lane quadrant of this warp
     const int h = quad * 32 + lane;                         // head row
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // exchange buffer g: the float4 holding scores 4q..4q+3 of head h sits at
-    // [q][h], so one warp-wide store moves 512 contiguous bytes
+    // exchange buffer g: words 4j..4j+3 of head h's 48 packed words sit in the
+    // uint4 at [j][h], so one warp-wide store moves 512 contiguous bytes
     const uint32_t peer_x = mapa_peer(smem_u32(sX + g * (kXBytes / 4) + 4 * h), peer);
     const uint32_t peer_xf = mapa_peer(smem_u32(&bar[B_XF + g]), peer);
-    const float4 *my_x = reinterpret_cast<const float4 *>(sX + g * (kXBytes / 4)) + h;
+    const uint4 *my_x = reinterpret_cast<const uint4 *>(sX + g * (kXBytes / 4)) + h;
     const float sscale = p.score_scale;
     bool ok = true;
     int x_next = g;         // first tile of this group whose peer scores have not been waited for
     bool x_posted = false;  // whether its expect_tx has been posted
     int epi = 0;            // partials written by this group (phase of B_EPI + g)
     // q_nope of a row (this CTA's half) into TMEM, the A operand of its score MMAs
+    // (two rounds of sixteen 16-byte loads per thread: at the start of a range
+    // the row comes from DRAM, and each round is one round trip)
     auto store_q = [&](int b) {
       const uint4 *src =
           reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 + 256 * r);
 #pragma unroll
-      for (int c0 = 0; c0 < 8; c0 += 2) {
-        uint4 qv[8];
+      for (int c0 = 0; c0 < 8; c0 += 4) {
+        uint4 qv[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = __ldg(src + 4 * c0 + e);
+        for (int e = 0; e < 16; ++e) qv[e] = __ldg(src + 4 * c0 + e);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
           float v[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -690,23 +716,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar[B_SE]);
       // ---- exchange the partial scores with the peer CTA
       if (ii >= 1 && !(ok = warp_wait_cluster(&bar[B_XE + g], (ii - 1) & 1))) break;
+      {
+        uint32_t w[48];
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_async_v4(peer_x + q * kHeads * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3],
-                    peer_xf);
+        for (int q = 0; q < 16; ++q) pack24(s + 4 * q, w + 3 * q);
+#pragma unroll
+        for (int j = 0; j < 12; ++j)
+          st_async_u4(peer_x + j * kHeads * 16, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]),
+                      peer_xf);
+      }
       // this tile's phase of x_full completes once the peer's 32 KB have landed
       if (tid == kGroupThreads * g) mbar_arrive_expect_tx(&bar[B_XF + g], kXBytes);
       x_posted = true;
       if (!(ok = warp_wait_cluster(&bar[B_XF + g], ii & 1))) break;
       x_next = i + 2;
       x_posted = false;
+      {
+        uint32_t w[48];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 o = my_x[q * kHeads];
-        s[4 * q] += o.x;
-        s[4 * q + 1] += o.y;
-        s[4 * q + 2] += o.z;
-        s[4 * q + 3] += o.w;
+        for (int j = 0; j < 12; ++j) {
+          const uint4 o = my_x[j * kHeads];
+          w[4 * j] = o.x;
+          w[4 * j + 1] = o.y;
+          w[4 * j + 2] = o.z;
+          w[4 * j + 3] = o.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) unpack24_add(w + 3 * q, s + 4 * q);
       }
       mbar_arrive(&bar[B_XR + g]);
       // ---- mask and tile maximum
