@@ -408,7 +408,7 @@ __device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_firs
 #pragma unroll 1
     for (int i = tid; i < n_seg * G; i += nthr) {
       const float l = w[i], Mg = stat[i % G];
-      w[i] = (l == neg_inf() || Mg == neg_inf()) ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
+      w[i] = l == neg_inf() ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
     }
     named_barrier_sync(kConsumerBar, nthr);
     if (tid < 32) {
@@ -433,7 +433,7 @@ __device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_firs
 #pragma unroll 1
       for (int i = tid; i < ns * G; i += nthr) {
         const float l = __ldcg(lse_base + (int64_t)s0 * G + i), Mg = stat[i % G];
-        w[i] = (l == neg_inf() || Mg == neg_inf()) ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
+        w[i] = l == neg_inf() ? 0.f : ex2((l - Mg) * 1.4426950408889634f);
       }
       named_barrier_sync(kConsumerBar, nthr);
       if (tid < G) {
@@ -478,12 +478,12 @@ __device__ __noinline__ bool merge_unit(const GqaParams &p, int unit, int c_firs
 #pragma unroll 1
   for (int e = tid; e < G * kD; e += nthr) {
     const float sum = stat[16 + e / kD];
-    out[e] = __float2bfloat16(sum > 0.f ? acc[e] / sum : 0.f);
+    out[e] = __float2bfloat16(sum == 0.f ? 0.f : acc[e] / sum);
   }
   if (tid < G && p.lse) {
     const float sum = stat[16 + tid];
     p.lse[(int64_t)b * p.num_q_heads + h * G + tid] =
-        sum > 0.f ? stat[tid] + __log2f(sum) * 0.69314718055994531f : neg_inf();
+        sum == 0.f ? neg_inf() : stat[tid] + __log2f(sum) * 0.69314718055994531f;
   }
   if (tid == 0) p.counters[unit] = 0u;  // ready for the next call
   named_barrier_sync(kConsumerBar, nthr);
@@ -534,7 +534,7 @@ __device__ __noinline__ void merge_slots_cta(const GqaParams &p, int unit, int G
     float ssum = 0.f;
     for (int s = lane; s < n_seg; s += 32) {
       const float l = w[s * G + g];
-      const float e = (l == neg_inf() || M == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
+      const float e = l == neg_inf() ? 0.f : ex2((l - M) * 1.4426950408889634f);
       w[s * G + g] = e;
       ssum += e;
     }
@@ -581,7 +581,7 @@ __device__ __noinline__ void merge_slots_cta(const GqaParams &p, int unit, int G
     __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
     for (int o = tid; o < nout; o += nthr) {
       const int g = o / (kD / 4);
-      const float inv = sum[g] > 0.f ? 1.f / sum[g] : 0.f;
+      const float inv = sum[g] == 0.f ? 0.f : 1.f / sum[g];
       const float4 a = acc[o];
       *reinterpret_cast<uint2 *>(out + 4 * o) =
           make_uint2(pack_bf16(a.x * inv, a.y * inv), pack_bf16(a.z * inv, a.w * inv));
@@ -590,13 +590,13 @@ __device__ __noinline__ void merge_slots_cta(const GqaParams &p, int unit, int G
     float4 *out = reinterpret_cast<float4 *>(p.o_part + dst * G * kD);
     for (int o = tid; o < nout; o += nthr) {
       const int g = o / (kD / 4);
-      const float inv = sum[g] > 0.f ? 1.f / sum[g] : 0.f;
+      const float inv = sum[g] == 0.f ? 0.f : 1.f / sum[g];
       const float4 a = acc[o];
       out[o] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     }
   }
   if (tid < G) {
-    const float lse = sum[tid] > 0.f ? mx[tid] + __log2f(sum[tid]) * 0.69314718055994531f : neg_inf();
+    const float lse = sum[tid] == 0.f ? neg_inf() : mx[tid] + __log2f(sum[tid]) * 0.69314718055994531f;
     if (!final_out) p.lse_part[dst * G + tid] = lse;
     else if (p.lse) p.lse[(int64_t)b * p.num_q_heads + h * G + tid] = lse;
   }
@@ -639,7 +639,7 @@ __device__ __noinline__ void merge_slots_small(const GqaParams &p, int unit, int
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kSmallMerge; ++k) {
-      const float e = (l[u][k] == neg_inf() || M == neg_inf()) ? 0.f : ex2((l[u][k] - M) * 1.4426950408889634f);
+      const float e = l[u][k] == neg_inf() ? 0.f : ex2((l[u][k] - M) * 1.4426950408889634f);
       if (e != 0.f) {  // a piece of weight 0 may hold anything
         sum += e;
         a.x += e * v[u][k].x;
@@ -648,9 +648,9 @@ __device__ __noinline__ void merge_slots_small(const GqaParams &p, int unit, int
         a.w += e * v[u][k].w;
       }
     }
-    lse_out[u] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+    lse_out[u] = sum == 0.f ? neg_inf() : M + __log2f(sum) * 0.69314718055994531f;
     if (o < nout) {
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      const float inv = sum == 0.f ? 0.f : 1.f / sum;
       if (final_out) {
         __nv_bfloat16 *out = p.out + ((int64_t)b * p.num_q_heads + h * G) * kD;
         *reinterpret_cast<uint2 *>(out + 4 * o) =
@@ -713,7 +713,7 @@ __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int s = 0; s < kWarpMergeSegs; ++s) {
-        const float w = (s < n_seg && l[s] != neg_inf() && M != neg_inf())
+        const float w = (s < n_seg && l[s] != neg_inf())
                             ? ex2((l[s] - M) * 1.4426950408889634f)
                             : 0.f;
         if (w != 0.f) {  // a piece of weight 0 may hold anything
@@ -724,12 +724,12 @@ __device__ __noinline__ void merge_unit_warp(const GqaParams &p, int unit, int c
           acc.w += w * v[r][s].w;
         }
       }
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      const float inv = sum == 0.f ? 0.f : 1.f / sum;
       *reinterpret_cast<uint2 *>(out + (int64_t)g * kD + 4 * lane) =
           make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
       if (lane == 0 && p.lse)
         p.lse[(int64_t)b * p.num_q_heads + h * G + g] =
-            sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+            sum == 0.f ? neg_inf() : M + __log2f(sum) * 0.69314718055994531f;
     }
   }
   if (lane == 0) p.counters[unit] = 0u;  // ready for the next call
@@ -1567,12 +1567,11 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
             const float m_new = fmaxf(m_run[nt][e], tmax);
-            float p0 = 0.f, p1 = 0.f, a = 1.f;
-            if (m_new != neg_inf()) {
-              a = ex2(m_run[nt][e] - m_new);
-              p0 = ex2(x0 - m_new);
-              p1 = ex2(x1 - m_new);
-            }
+            // while no score of the row is valid the reference is 0: masked
+            // scores weigh 0, NaN scores (a NaN query or key) weigh NaN
+            const float m_use = m_new == neg_inf() ? 0.f : m_new;
+            const float a = ex2(m_run[nt][e] - m_use);
+            const float p0 = ex2(x0 - m_use), p1 = ex2(x1 - m_use);
             l_part[nt][e] = l_part[nt][e] * a + (p0 + p1);
             if (tok_scale) zacc[nt][e] = zacc[nt][e] * a + (p0 * vsh0 + p1 * vsh1);
             m_run[nt][e] = m_new;
@@ -1856,7 +1855,7 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
         float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w)
-          L += (M == neg_inf()) ? 0.f : stat_l[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
+          L += (stat_l[w * 16 + g] == 0.f) ? 0.f : stat_l[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
         float acc;
         if (C::kStageScratch) {
           acc = 0.f;
@@ -1871,8 +1870,9 @@ __global__ void __launch_bounds__(threads_for<NT>(), 2)
           for (int w = 0; w < kConsumerWarps; ++w)
             acc += (M == neg_inf()) ? 0.f : stat_z[w * 16 + g] * ex2(stat_m[w * 16 + g] - M);
         }
-        const float o = (L > 0.f) ? acc * vmul / L : 0.f;
-        const float lse = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : neg_inf();
+        // no valid token: 0 and -inf; a NaN among the weights reaches both
+        const float o = (L == 0.f) ? 0.f : acc * vmul / L;
+        const float lse = (L == 0.f) ? neg_inf() : (M + __log2f(L)) * 0.69314718055994531f;
         if (whole) {
           const int64_t row = (int64_t)b * p.num_q_heads + h * G + g;
           p.out[row * kD + d] = __float2bfloat16(o);

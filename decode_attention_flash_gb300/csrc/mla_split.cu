@@ -163,8 +163,10 @@ __device__ __forceinline__ void st_async_u4(uint32_t addr, uint4 v, uint32_t rem
 
 // Partial scores cross the cluster as the upper three bytes of their fp32
 // encoding (sign, exponent, 15 mantissa bits: a relative error below 2^-15,
-// far inside the bf16 rounding of the weights they become), four scores in
-// three words. DSMEM bandwidth, not arithmetic, limits the exchange.
+// far inside the bf16 rounding of the weights they become; NaN and the
+// infinities keep their meaning), four scores in three words. DSMEM
+// bandwidth limits the exchange; a 16-bit code on per-group steps moved 25 %
+// fewer bytes but its encode and decode arithmetic cost more than that saved.
 __device__ __forceinline__ void pack24(const float *s, uint32_t *w) {
   const uint32_t a = __float_as_uint(s[0]), b = __float_as_uint(s[1]);
   const uint32_t c = __float_as_uint(s[2]), d = __float_as_uint(s[3]);
@@ -279,12 +281,12 @@ __device__ void mla_merge_row(const MlaParams &p, int b, int r, int c_first, int
     float sum = 0.f;
     for (int s = 0; s < n_seg; ++s) {
       const float l = w[s * kHeads + h];
-      const float e = (M == neg_inf() || l == neg_inf()) ? 0.f : ex2((l - M) * 1.4426950408889634f);
+      const float e = l == neg_inf() ? 0.f : ex2((l - M) * 1.4426950408889634f);
       w[s * kHeads + h] = e;
       sum += e;
     }
-    inv[h] = sum > 0.f ? 1.f / sum : 0.f;
-    lse_out[h] = sum > 0.f ? M + __log2f(sum) * 0.69314718055994531f : neg_inf();
+    inv[h] = sum == 0.f ? 0.f : 1.f / sum;
+    lse_out[h] = sum == 0.f ? neg_inf() : M + __log2f(sum) * 0.69314718055994531f;
   }
   __syncthreads();
   // out[b][h][256 r + 4c .. +3] for c < 64: each thread sums 8 float4 outputs
@@ -851,8 +853,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(&bar[B_PE + (i & 1)], (i >> 1) & 1))) break;
         tc_fence_after();
         const bool full = (m.flags & kFullRow) != 0;
-        const float inv = l_new > 0.f ? 1.f / l_new : 0.f;
-        const float lse = l_new > 0.f ? (m_new + __log2f(l_new)) * 0.69314718055994531f : neg_inf();
+        // no valid token: 0 and -inf; a NaN among the weights reaches both
+        const float inv = l_new == 0.f ? 0.f : 1.f / l_new;
+        const float lse = l_new == 0.f ? neg_inf() : (m_new + __log2f(l_new)) * 0.69314718055994531f;
         const int64_t slot = (int64_t)m.b + cl;
         for (int c0 = 0; c0 < 256; c0 += 64) {
           float v[64];  // four loads per wait

@@ -350,6 +350,64 @@ def test_mla_bad_page_sets_flag():
     assert torch.all(torch.isfinite(out.float()))
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_mla_non_finite_valid_keys_reach_the_sum_as_they_are(splits):
+    # The two CTAs of a pair each hold half of every score and exchange their
+    # halves in a narrowed float encoding that keeps NaN and the infinities.
+    # NaN in a latent key element of row 0 (the first value half's dimensions)
+    # turns all 128 heads of row 0 into NaN; +inf in a rope element of row 1
+    # (the second half's rope columns) turns the heads whose q_pe component is
+    # positive into NaN (inf - inf) and gives that token weight 0 in the others;
+    # row 2 is untouched.
+    w = W.make_mla(name="mla_nf", batch=3, seq_lens=[300, 200, 130], seed=49)
+    t = w.tensors
+    k, v, bt = t["k"].clone(), t["v"].clone(), t["block_table"]
+    k[int(bt[0, 1]), 5, 7] = float("nan")
+    v[int(bt[1, 2]), 10, 40] = float("inf")
+    t["k"], t["v"] = k, v
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    got, gl = out.double().numpy(), lse.double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref_out))
+    assert np.array_equal(np.isnan(gl), np.isnan(ref_lse))
+    assert np.isnan(ref_out[0]).all() and 0 < np.isnan(ref_out[1]).all(-1).sum() < 128
+    fin = ~np.isnan(ref_out)
+    assert np.max(np.abs(got[fin] - ref_out[fin])) <= 2e-2
+    lfin = ~np.isnan(ref_lse)
+    assert np.max(np.abs(gl[lfin] - ref_lse[lfin])) <= 1e-3
+
+
+@pytest.mark.parametrize("where", ["key", "query"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_gqa_nan_input_reaches_exactly_the_rows_that_read_it(where, splits):
+    # A NaN in a valid key of kv head 0 of row 0 poisons the G query heads of
+    # that group (every one of them weighs the token); a NaN in one query
+    # element poisons that head alone. The others stay within tolerance.
+    w = W.make_gqa(name="gqa_nan", batch=3, num_q_heads=8, num_kv_heads=2, seq_lens=[300, 200, 130],
+                   layout="paged", page_size=16, seed=50)
+    t = w.tensors
+    if where == "key":
+        k = t["k"].clone()
+        k[int(t["block_table"][0, 1]), 0, 5, 7] = float("nan")
+        t["k"] = k
+    else:
+        q = t["q"].clone()
+        q[1, 6, 3] = float("nan")
+        t["q"] = q
+    out, lse, flags, _ = run_gpu(w, num_splits_override=splits)
+    assert flags == 0
+    ref_out, ref_lse = reference(w)
+    got, gl = out.double().numpy(), lse.double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref_out))
+    assert np.array_equal(np.isnan(gl), np.isnan(ref_lse))
+    assert np.isnan(ref_lse).sum() == (4 if where == "key" else 1)
+    fin = ~np.isnan(ref_out)
+    assert np.max(np.abs(got[fin] - ref_out[fin])) <= 2e-2
+    lfin = ~np.isnan(ref_lse)
+    assert np.max(np.abs(gl[lfin] - ref_lse[lfin])) <= 1e-3
+
+
 # ------------------------------------------------------------------ several query tokens per row (causal)
 
 @pytest.mark.parametrize("q_len,group,layout", [(2, 4, "paged"), (3, 2, "contiguous"),
