@@ -335,21 +335,30 @@ def sparse_lists(batch, num_kv_heads, cache_len, block_size, keep_random, keep_l
 
 def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq_lens,
              page_size=64, scale=None, seed=0, num_splits=0, poison=True,
-             shape_only=False) -> Workload:
+             shape_only=False, q_len=1, tree_mask=False) -> Workload:
+    """An MLA decode workload over a paged latent cache; ``q_len`` > 1 gives
+    each row that many query tokens (its last positions, q_nope
+    [B][HQ][q_len][ckv], q_pe [B][HQ][q_len][kpe]); ``tree_mask`` adds a random
+    draft-token tree over them (``spec_mask``)."""
     g = _gen(seed)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32)
     B, HQ = batch, num_q_heads
     scale = 1.0 / math.sqrt(192.0) if scale is None else scale
-    q_nope = _randn_bf16((B, HQ, ckv_dim), g)
-    q_pe = _randn_bf16((B, HQ, kpe_dim), g)
+    lead = (B, HQ) if q_len <= 1 else (B, HQ, q_len)
+    q_nope = _randn_bf16(lead + (ckv_dim,), g)
+    q_pe = _randn_bf16(lead + (kpe_dim,), g)
     table, num_pages, max_pages, used = _page_pool(seq_lens, page_size, g)
     w = Workload(name=name, batch=B, num_q_heads=HQ, num_kv_heads=1,
                  head_dim_qk=ckv_dim + kpe_dim, head_dim_v=ckv_dim,
                  scale=float(torch.tensor(scale, dtype=torch.float32)), is_mla=True,
                  ckv_dim=ckv_dim, kpe_dim=kpe_dim, paged=True, page_size=page_size,
-                 max_pages_per_seq=max_pages, num_pages=num_pages, num_splits=num_splits)
+                 max_pages_per_seq=max_pages, num_pages=num_pages, num_splits=num_splits,
+                 q_len=max(1, q_len))
+    extra = {}
+    if tree_mask and q_len > 1:
+        extra["spec_mask"] = draft_tree_mask(B, q_len, _gen(seed + 7919))
     if shape_only:
-        w.tensors = {"q": q_nope, "q_pe": q_pe, "block_table": table, "seq_lens": seq_lens}
+        w.tensors = {"q": q_nope, "q_pe": q_pe, "block_table": table, "seq_lens": seq_lens, **extra}
         return w
     ckv = torch.randn((num_pages, page_size, ckv_dim), generator=g, dtype=torch.float32)
     kpe = torch.randn((num_pages, page_size, kpe_dim), generator=g, dtype=torch.float32)
@@ -358,7 +367,7 @@ def make_mla(*, name="mla", batch, num_q_heads=128, ckv_dim=512, kpe_dim=64, seq
         _poison_paged(kpe, table, seq_lens, page_size, used, False)
     w.tensors = {"q": q_nope, "q_pe": q_pe, "k": ckv.to(torch.bfloat16).contiguous(),
                  "v": kpe.to(torch.bfloat16).contiguous(), "block_table": table,
-                 "seq_lens": seq_lens}
+                 "seq_lens": seq_lens, **extra}
     return w
 
 

@@ -304,9 +304,8 @@ def brute_force(w: W.Workload, softcap: float = 0.0):
             else:
                 keys.append(k[b, h, n])
                 vals.append(v[b, h, n])
-        qv = torch.cat([q[b, hq], t["q_pe"][b, hq].double()]) if w.is_mla else q[b, hq]
-        if Q > 1:
-            qv = q[b, hq, tq]
+        qi = (b, hq, tq) if Q > 1 else (b, hq)
+        qv = torch.cat([q[qi], t["q_pe"][qi].double()]) if w.is_mla else q[qi]
         if not pos:
             lse[b, hq, tq] = -math.inf
             continue
@@ -354,6 +353,13 @@ def _tiny_cases():
     cases.append(full)
     cases.append(W.make_mla(name="mla", batch=2, num_q_heads=3, ckv_dim=4, kpe_dim=2,
                             seq_lens=[4, 2], page_size=2, seed=15, scale=0.9))
+    # several query tokens on the latent cache: causal, with a row shorter than
+    # q_len, and a draft-token tree
+    cases.append(W.make_mla(name="mla_causal_q3", batch=2, num_q_heads=3, ckv_dim=4, kpe_dim=2,
+                            seq_lens=[5, 2], page_size=2, seed=30, scale=0.8, q_len=3))
+    cases.append(W.make_mla(name="mla_tree_q4", batch=2, num_q_heads=2, ckv_dim=4, kpe_dim=2,
+                            seq_lens=[7, 4], page_size=2, seed=31, scale=0.7, q_len=4,
+                            tree_mask=True))
     cases.append(W.make_gqa(name="empty_row", batch=2, num_q_heads=2, num_kv_heads=1,
                             head_dim=3, seq_lens=[0, 2], cache_len=2, seed=16, scale=1.0))
     # several query tokens per row, causal over the new tokens; the second row is
