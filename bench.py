@@ -104,8 +104,8 @@ def algorithmic_bytes(w) -> dict:
     Q = getattr(w, "q_len", 1)  # query tokens per row (their causal triangle is not subtracted)
     if w.is_mla:
         kv = kv_tokens_heads * (w.ckv_dim + w.kpe_dim) * 2
-        q = w.batch * w.num_q_heads * (w.ckv_dim + w.kpe_dim) * 2
-        flops = kv_tokens_heads * w.num_q_heads * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
+        q = w.batch * w.num_q_heads * Q * (w.ckv_dim + w.kpe_dim) * 2
+        flops = kv_tokens_heads * w.num_q_heads * Q * (2 * (w.ckv_dim + w.kpe_dim) + 2 * w.ckv_dim)
     else:
         kv = kv_tokens_heads * (w.head_dim_qk + w.head_dim_v) * elt
         if getattr(w, "kv_int4_groups", 0):  # int32 rows: groups coefficient words + D / 8 data words
@@ -205,6 +205,8 @@ def workload_name(cfg, args):
         name += f", seed {args.seed}"
     if args.fp8_mma:
         name += ", e4m3 tensor-core QK/PV (fp8_mma)"
+    if args.q_len > 1:
+        name += f", {args.q_len} query tokens per row"
     return name
 
 
@@ -461,11 +463,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=None,
                     help="another draw of the workload's recipe (default: its own seed, 1000 + config)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="the MLA configuration: query tokens per row (speculative decoding, causal "
+                         "over the row's last q_len positions)")
     ap.add_argument("--fp8-mma", action="store_true",
                     help="e4m3 K/V configurations: QK and PV on e4m3 tensor cores (queries and "
                          "weights rounded to e4m3)")
     args = ap.parse_args()
-    w = W.config(args.config, seed=args.seed)
+    if args.q_len > 1 and args.config != 5:
+        raise SystemExit("--q-len applies to the MLA configuration (5); config 6 is the GQA one")
+    w = W.config(args.config, seed=args.seed, q_len=args.q_len)
     if args.fp8_mma:
         if not w.kv_fp8 or w.kv_token_scale:
             raise SystemExit("--fp8-mma needs a configuration with e4m3 K/V and per-head scales")

@@ -113,6 +113,23 @@ da_status encode_bf16_rows_sw64(CUtensorMap *map, const void *base, uint64_t row
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
 }
 
+// The MLA rope queries [B*HQ][Q][64] as a 3-D tensor (64 elements, token, head
+// row): one box copies 32 columns of query token t for `box_rows` head rows,
+// 64B-swizzled, and lands as [row][32].
+da_status encode_qpe_tokens(CUtensorMap *map, const void *base, uint64_t head_rows, uint32_t Q,
+                            uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DA_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, Q, head_rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)Q * 128};
+  const cuuint32_t box[3] = {32u, 1u, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_CUDA;
+}
+
 // A bf16 cache of rows of 128 elements as a 3-D tensor (64 elements, row, half)
 // with the half stride (128 B) below the row stride (256 B): one box copies
 // `box_rows` rows and lands as [half][row][64], 128B-swizzled.
@@ -314,7 +331,9 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
     da_status st;
     if ((st = encode_bf16_rows(&ctx->kmap, a->k, 512, tokens, 64)) != DA_OK) return st;
     if ((st = encode_bf16_rows_sw64(&ctx->vmap, a->v, 64, tokens, 64)) != DA_OK) return st;
-    if ((st = encode_bf16_rows_sw64(&ctx->qpemap, a->q_pe, 64, qrows, 128)) != DA_OK) return st;
+    st = p.q_len > 1 ? encode_qpe_tokens(&ctx->qpemap, a->q_pe, qrows, (uint32_t)p.q_len, 128)
+                     : encode_bf16_rows_sw64(&ctx->qpemap, a->q_pe, 64, qrows, 128);
+    if (st != DA_OK) return st;
     ctx->map_k_base = a->k;
     ctx->map_v_base = a->v;
     ctx->map_q_base = a->q;
@@ -327,13 +346,18 @@ da_status run_mla(da_ctx *ctx, const da_args *a, uint8_t *ws, cudaStream_t strea
   mp.q_pe = reinterpret_cast<const __nv_bfloat16 *>(a->q_pe);
   mp.block_table = a->block_table;
   mp.seq_lens = a->seq_lens;
+  mp.q_len = p.q_len > 1 ? p.q_len : 1;
+  mp.spec_mask = mp.q_len > 1 ? a->spec_mask : nullptr;
   mp.o_part = reinterpret_cast<float *>(ws + pl.partial_o_offset);
   mp.lse_part = reinterpret_cast<float *>(ws + pl.partial_lse_offset);
   mp.out = reinterpret_cast<__nv_bfloat16 *>(a->out);
   mp.lse = a->lse;
   mp.err = reinterpret_cast<uint32_t *>(ws);
   mp.counters = reinterpret_cast<uint32_t *>(ws + pl.counters_offset);
-  mp.score_scale = a->scale * 1.4426950408889634f;
+  // a zero scale (uniform weights) becomes 2^-100: every finite score then
+  // weighs exactly 1 against the maximum, while a padded (masked) score times
+  // the factor stays -inf, so the kernel needs no per-token select
+  mp.score_scale = a->scale == 0.f ? 0x1p-100f : a->scale * 1.4426950408889634f;
   mp.batch = p.batch;
   mp.max_pages = p.max_pages_per_seq;
   mp.num_pages = p.num_pages;

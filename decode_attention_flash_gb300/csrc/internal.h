@@ -77,20 +77,25 @@ struct MergeParams {
   int32_t rows, num_splits, rows_per_unit, dv;
 };
 
+// MLA rows are (b, t) pairs, v = b * Q + t for the Q query tokens of batch
+// row b: token t attends to the positions n <= seq_lens[b] - Q + t (or those
+// its draft-tree mask word selects among the last Q).
 struct MlaParams {
-  const __nv_bfloat16 *q_nope;  // [B][128][512]
-  const __nv_bfloat16 *q_pe;    // [B][128][64]
+  const __nv_bfloat16 *q_nope;  // [B][128][Q][512]
+  const __nv_bfloat16 *q_pe;    // [B][128][Q][64]
   const int32_t *block_table;
   const int32_t *seq_lens;
-  float *o_part;                // [B + clusters][128][512]: slot b + cluster of a row segment
+  const uint32_t *spec_mask;    // Q > 1, optional: [B][Q] draft-tree mask words
+  float *o_part;                // [B*Q + clusters][128][512]: slot v + cluster of a row segment
                                 // (rank r writes columns 256r..256r+255)
-  float *lse_part;              // [B + clusters][2][128] (one copy per rank)
-  __nv_bfloat16 *out;           // [B][128][512]
-  float *lse;
+  float *lse_part;              // [B*Q + clusters][2][128] (one copy per rank)
+  __nv_bfloat16 *out;           // [B][128][Q][512]
+  float *lse;                   // [B][128][Q]
   uint32_t *err;
-  uint32_t *counters;           // [B][2]: finished segments per (row, rank)
+  uint32_t *counters;           // [B*Q][2]: finished segments per (row, rank)
   float score_scale;
   int32_t batch, max_pages, num_pages, capacity;
+  int32_t q_len;                // Q >= 1
 };
 
 // Kernel launchers (return the launch error).

@@ -85,7 +85,9 @@ constexpr float kRescaleThreshold = 8.f;
 // What the producer tells the other roles about the tile in a KV stage.
 struct TileMeta {
   int32_t b, k, nval, flags;  // row, tile of the row, valid tokens, kFirst | kLast | kFullRow
-  int32_t c_first, n_seg, pad0, pad1;  // clusters holding the row's pieces
+  int32_t c_first, n_seg;     // clusters holding the row's pieces
+  int32_t draft0;             // position of the batch row's first new token (seq_len - Q)
+  uint32_t tree;              // the query token's draft-tree mask word (all ones: none)
 };
 enum { kFirst = 1, kLast = 2, kFullRow = 4 };
 
@@ -231,14 +233,26 @@ __device__ __forceinline__ int cluster_of(int64_t t, int64_t T, int C) {
 }
 
 // Tiles of row b; an out-of-range length is clamped and flagged.
-__device__ __forceinline__ int row_tiles(const MlaParams &p, int b, int &len, uint32_t &err) {
+// Batch row of row v = b * Q + t (query token t of batch row b).
+__device__ __forceinline__ int batch_of(const MlaParams &p, int v) { return p.q_len == 1 ? v : v / p.q_len; }
+
+// Index of (row v, head h) in the [B][128][Q] layouts of q, out and lse.
+__device__ __forceinline__ int64_t head_row(const MlaParams &p, int v, int h) {
+  const int b = batch_of(p, v), t = v - b * p.q_len;
+  return ((int64_t)b * kHeads + h) * p.q_len + t;
+}
+
+// Positions of row v: token t of Q sees n <= seq_lens[b] - Q + t.
+__device__ __forceinline__ int row_tiles(const MlaParams &p, int v, int &len, uint32_t &err) {
+  const int b = batch_of(p, v);
   int n = p.seq_lens[b];
   if (n < 0 || n > p.capacity) {
     err |= DA_DEVERR_SEQ_LEN;
     n = n < 0 ? 0 : p.capacity;
   }
-  len = n;
-  return (n + kTok - 1) / kTok;
+  n -= p.q_len - 1 - (v - b * p.q_len);
+  len = n > 0 ? n : 0;
+  return (len + kTok - 1) / kTok;
 }
 
 __device__ int block_scan(int v, int *scratch, int *total) {
@@ -331,14 +345,14 @@ __device__ void mla_merge_row(const MlaParams &p, int b, int r, int c_first, int
       if (i < kHeads * 64) {
         const int h = i / 64, c = i % 64;
         const float iv = inv[h];
-        __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(p.out + ((int64_t)b * kHeads + h) * 512 +
+        __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(p.out + head_row(p, b, h) * 512 +
                                                                  r * 256 + 4 * c);
         dst[0] = __floats2bfloat162_rn(acc[u].x * iv, acc[u].y * iv);
         dst[1] = __floats2bfloat162_rn(acc[u].z * iv, acc[u].w * iv);
       }
     }
   }
-  if (r == 0 && threadIdx.x < kHeads && p.lse) p.lse[(int64_t)b * kHeads + threadIdx.x] = lse_out[threadIdx.x];
+  if (r == 0 && threadIdx.x < kHeads && p.lse) p.lse[head_row(p, b, threadIdx.x)] = lse_out[threadIdx.x];
   if (threadIdx.x == 0) p.counters[b * 2 + r] = 0u;  // ready for the next call
   __syncthreads();
 }
@@ -364,7 +378,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- the cluster's tile range
   uint32_t dev_err = 0;
   int local = 0;
-  for (int b = threadIdx.x; b < p.batch; b += kThreads) {
+  const int nrows = p.batch * p.q_len;
+  for (int b = threadIdx.x; b < nrows; b += kThreads) {
     int len;
     local += row_tiles(p, b, len, dev_err);
   }
@@ -386,15 +401,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   {
     int64_t base = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += kThreads) {
+    for (int b0 = 0; b0 < nrows; b0 += kThreads) {
       const int b = b0 + threadIdx.x;
       int len = 0;
       uint32_t ignored = 0;
-      const int t_b = b < p.batch ? row_tiles(p, b, len, ignored) : 0;
+      const int t_b = b < nrows ? row_tiles(p, b, len, ignored) : 0;
       int total = 0;
       const int incl = block_scan(t_b, scan, &total);
       const int64_t Pb = base + incl - t_b;
-      if (b < p.batch) {
+      if (b < nrows) {
         if (t_b > 0 && Pb <= lo && lo < Pb + t_b) {
           ctrl->start_b = b;
           ctrl->start_k = (int)(lo - Pb);
@@ -409,9 +424,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int e = threadIdx.x; e < ne * kHeads * 32; e += kThreads) {
         // this CTA's value half of the row: zeros; lse = -inf
         const int rb = empty_rows[e / (kHeads * 32)], h = (e / 32) % kHeads, c = e % 32;
-        *reinterpret_cast<uint4 *>(p.out + ((int64_t)rb * kHeads + h) * 512 + r * 256 + 8 * c) =
+        *reinterpret_cast<uint4 *>(p.out + head_row(p, rb, h) * 512 + r * 256 + 8 * c) =
             make_uint4(0, 0, 0, 0);
-        if (r == 0 && c == 0 && p.lse) p.lse[(int64_t)rb * kHeads + h] = neg_inf();
+        if (r == 0 && c == 0 && p.lse) p.lse[head_row(p, rb, h)] = neg_inf();
       }
       __syncthreads();
       if (threadIdx.x == 0) ctrl->nempty = 0;
@@ -484,7 +499,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int c_first, n_seg;
       bool full;
       row_pieces(c_first, n_seg, full);
-      int page_next = p.block_table[(int64_t)b * p.max_pages + k];
+      // the row's new positions and its query token's tree-mask word (read
+      // only when there is a tree mask: the causal cut is the row's length)
+      int draft0 = 0;
+      uint32_t tree = ~0u;
+      auto row_draft = [&] {
+        if (!p.spec_mask) return;
+        const int bb = batch_of(p, b);
+        const int n = min(max(p.seq_lens[bb], 0), p.capacity);
+        draft0 = n - p.q_len;
+        tree = p.spec_mask[(int64_t)bb * p.q_len + (b - bb * p.q_len)];
+      };
+      row_draft();
+      int page_next = p.block_table[(int64_t)batch_of(p, b) * p.max_pages + k];
       for (int i = 0, st = 0, ph = 0; i < n; ++i) {
         if (i >= kStages && !mbar_wait_bounded(&bar[B_KVE + st], ph ^ 1, kWaitLimitNs)) {
           dev_err |= DA_DEVERR_TIMEOUT;
@@ -502,11 +529,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   (full ? kFullRow : 0);
         m.c_first = c_first;
         m.n_seg = n_seg;
+        m.draft0 = draft0;
+        m.tree = tree;
         if (m.flags & kFirst) {
           // the row's queries into L2 ahead of their use at the row's first
           // tile (this CTA's half of q_nope's rows, and its q_pe columns' rows)
-          prefetch_l2(p.q_nope + ((int64_t)b * kHeads + 64 * (int)r) * 512, 64 * 512 * 2);
-          prefetch_l2(p.q_pe + ((int64_t)b * kHeads + 64 * (int)r) * 64, 64 * 64 * 2);
+          // (all Q tokens' rows of these heads: [64][Q][512] and [64][Q][64])
+          const int64_t q0 = ((int64_t)batch_of(p, b) * kHeads + 64 * (int)r) * p.q_len;
+          prefetch_l2(p.q_nope + q0 * 512, 64u * p.q_len * 512 * 2);
+          prefetch_l2(p.q_pe + q0 * 64, 64u * p.q_len * 64 * 2);
         }
         uint8_t *dst = sKV + st * kKvStage;
         if (bad) {
@@ -532,12 +563,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             Pb += t_b;
             do {
               ++b;
-              t_b = b < p.batch ? row_tiles(p, b, len, ignored) : 1;
+              t_b = b < nrows ? row_tiles(p, b, len, ignored) : 1;
             } while (t_b == 0);
             k = 0;
             row_pieces(c_first, n_seg, full);
+            if (b < nrows) row_draft();
           }
-          page_next = b < p.batch ? p.block_table[(int64_t)b * p.max_pages + k] : -1;
+          page_next = b < nrows ? p.block_table[(int64_t)batch_of(p, b) * p.max_pages + k] : -1;
         }
       }
     }
@@ -564,7 +596,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (k >= 1 && !(ok = mbar_wait_bounded(&bar[B_SF + ((k - 1) & 1)], ((k - 1) >> 1) & 1, kWaitLimitNs)))
             break;
           mbar_arrive_expect_tx(&bar[B_QPE], kQpeBlock);
-          tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b * kHeads, q_policy);
+          if (p.q_len == 1) {
+            tma_load_2d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b * kHeads, q_policy);
+          } else {
+            const int bb = batch_of(p, m.b);
+            tma_load_3d(sQpe, &qp_map, &bar[B_QPE], 32 * (int)r, m.b - bb * p.q_len, bb * kHeads, q_policy);
+          }
           qpe_seg = seg;
           if (!(ok = mbar_wait_bounded(&bar[B_QT], seg & 1, kWaitLimitNs))) break;
           if (!(ok = mbar_wait_bounded(&bar[B_QPE], seg & 1, kWaitLimitNs))) break;
@@ -665,7 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the row comes from DRAM, and each round is one round trip)
     auto store_q = [&](int b) {
       const uint4 *src =
-          reinterpret_cast<const uint4 *>(p.q_nope + ((int64_t)b * kHeads + h) * 512 + 256 * r);
+          reinterpret_cast<const uint4 *>(p.q_nope + head_row(p, b, h) * 512 + 256 * r);
 #pragma unroll
       for (int c0 = 0; c0 < 8; c0 += 4) {
         uint4 qv[16];
@@ -749,13 +786,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar[B_XR + g]);
       // ---- mask and tile maximum
       const int nval = m.nval;
-      // raw scores past the valid tokens become a value that never wins the
-      // extreme below (uniform branch: ragged tiles only)
+      // the tile's live tokens: the valid ones, less those the query token's
+      // draft-tree mask removes among the batch row's last Q positions (a
+      // uniform branch: ragged tiles and tiles that reach the new positions)
+      const int first_new = kTok * m.k - m.draft0;  // the tile's first token among the new ones
+      const bool tree_tile = p.spec_mask != nullptr && first_new > -kTok;
+      const bool masked = nval < kTok || tree_tile;
+      uint64_t live = ~0ull;
       const float pad = sscale >= 0.f ? neg_inf() : -neg_inf();
-      if (nval < kTok) {
+      if (masked) {
+        live = nval >= kTok ? ~0ull : (1ull << nval) - 1ull;
+        if (tree_tile) {
+          const uint64_t w = m.tree;
+          live &= first_new >= 0 ? (w >> first_new) : ((w << -first_new) | ((1ull << -first_new) - 1ull));
+        }
+        // raw scores of the other tokens become a value that never wins the
+        // extreme below
 #pragma unroll
         for (int k = 0; k < 64; ++k)
-          if (k >= nval) s[k] = pad;
+          if (!((live >> k) & 1ull)) s[k] = pad;
       }
       // the scaled maximum is the raw maximum (minimum for a negative scale)
       // times the scale; four independent chains
@@ -769,7 +818,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const float ext = sscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
                                       : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
-      const float mt = nval > 0 ? ext * sscale : neg_inf();
+      const float mt = live != 0ull && nval > 0 ? ext * sscale : neg_inf();
       // ---- running maximum of the row through tile i - 1 (the other group);
       // the hand-off is waited for on a row's first tile too, which keeps the
       // other group's read of this group's previous value ahead of the overwrite
@@ -786,21 +835,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float neg_m = m_new == neg_inf() ? 0.f : -m_new;
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
-      auto exp_pack = [&](auto ragged) {
+      // (a masked token's padded score times the scale is -inf: the scale is
+      // never 0, see the score factor)
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          float t0 = fmaf(s[k], sscale, neg_m), t1 = fmaf(s[k + 1], sscale, neg_m);
-          if (decltype(ragged)::value) {
-            t0 = k < nval ? t0 : neg_inf();
-            t1 = k + 1 < nval ? t1 : neg_inf();
-          }
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          ps4[(k >> 1) & 3] += p0 + p1;
-          pk[k / 2] = pack_bf16(p0, p1);
-        }
-      };
-      if (nval < kTok) exp_pack(std::true_type{});
-      else exp_pack(std::false_type{});
+      for (int k = 0; k < 64; k += 2) {
+        const float p0 = ex2(fmaf(s[k], sscale, neg_m)), p1 = ex2(fmaf(s[k + 1], sscale, neg_m));
+        ps4[(k >> 1) & 3] += p0 + p1;
+        pk[k / 2] = pack_bf16(p0, p1);
+      }
       // ---- running sum of the row through tile i, relative to m_new
       float l_prev = 0.f;
       if (i >= 1) {
@@ -868,7 +910,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tmem_wait_ld();
           if (full) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)m.b * kHeads + h) * 512 + r * 256 + c0);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + head_row(p, m.b, h) * 512 + r * 256 + c0);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               dst[e] = make_uint4(pack_bf16(v[8 * e] * inv, v[8 * e + 1] * inv),
@@ -885,7 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bar[B_OFREE]);
         if (full) {
-          if (r == 0 && p.lse) p.lse[(int64_t)m.b * kHeads + h] = lse;
+          if (r == 0 && p.lse) p.lse[head_row(p, m.b, h)] = lse;
         } else {
           p.lse_part[(slot * 2 + r) * kHeads + h] = lse;
           // the whole piece is in global memory before the row's counter counts it

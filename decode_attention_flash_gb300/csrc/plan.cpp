@@ -56,7 +56,7 @@ da_status validate_problem(const da_problem *p) {
       return DA_ERR_INVALID_ARG;
   }
   if (p->is_mla) {
-    if (Q > 1) return DA_ERR_UNSUPPORTED;
+    if (Q > 16) return DA_ERR_UNSUPPORTED;  // the draft-tree mask is one word per query token
     if (p->num_kv_heads != 1 || p->ckv_dim != 512 || p->kpe_dim != 64 || p->head_dim_qk != 576 ||
         p->head_dim_v != 512 || p->num_q_heads != 128)
       return DA_ERR_UNSUPPORTED;
@@ -120,13 +120,14 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
   const bool paged = p->kv_layout == DA_KV_PAGED;
   const int tile = mla ? kMlaTile : kGqaTile;
   const int align = sparse ? p->sparse_block_size : tile;
-  const int heads = mla ? 1 : p->num_kv_heads;
+  // units: GQA (row, kv head); MLA (row, query token), whose heads share the latent cache
+  const int Q = p->q_len > 1 ? p->q_len : 1;
+  const int heads = mla ? Q : p->num_kv_heads;
   const int64_t units = (int64_t)p->batch * heads;
   const int64_t capacity =
       paged ? (int64_t)p->max_pages_per_seq * p->page_size : (int64_t)p->max_seq_len;
   // rows per unit: the G query heads (times the query tokens) of a kv head; MLA: all heads
-  const int rows = mla ? p->num_q_heads
-                       : p->num_q_heads / p->num_kv_heads * (p->q_len > 1 ? p->q_len : 1);
+  const int rows = mla ? p->num_q_heads : p->num_q_heads / p->num_kv_heads * Q;
   const int dv = p->head_dim_v;
 
   // positions per unit the split kernel walks (sparse: the compacted list)
@@ -146,6 +147,8 @@ da_status plan_compute(const da_problem *p, int32_t num_sms, int32_t smem_per_sm
       } else {
         len = seq_lens_host ? std::min<int64_t>(std::max<int32_t>(seq_lens_host[b], 0), capacity)
                             : std::min<int64_t>(p->max_seq_len, capacity);
+        // MLA query token h of Q sees the positions n <= seq_len - Q + h
+        if (mla) len = std::max<int64_t>(0, len - (Q - 1 - h));
       }
       unit_len[(size_t)((int64_t)b * heads + h)] = len;
     }

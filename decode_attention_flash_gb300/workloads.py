@@ -388,10 +388,11 @@ CONFIG_NAMES = {
 }
 
 
-def config(i: int, shape_only: bool = False, seed: int | None = None) -> Workload:
+def config(i: int, shape_only: bool = False, seed: int | None = None, q_len: int = 1) -> Workload:
     """The decode workloads (CONFIG_NAMES); ``shape_only`` skips drawing the K/V caches.
     ``seed`` replaces the workload's own seed (1000 + i): another draw of the same
-    recipe (lengths, tables, values)."""
+    recipe (lengths, tables, values). ``q_len`` gives the MLA workload (5) several
+    query tokens per row."""
     own_seed = seed is None
     seed = 1000 + i if seed is None else seed
     so = dict(shape_only=shape_only)
@@ -416,7 +417,7 @@ def config(i: int, shape_only: bool = False, seed: int | None = None) -> Workloa
     if i == 5:
         g = _gen(seed + 500)
         lens = _lengths(64, 2048, 8192, g)
-        return make_mla(name="mla", batch=64, seq_lens=lens, seed=seed, **so)
+        return make_mla(name="mla", batch=64, seq_lens=lens, seed=seed, q_len=q_len, **so)
     if i == 6:
         g = _gen(seed + 500)
         lens = _lengths(32, 1024, 8192, g)

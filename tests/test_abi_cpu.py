@@ -218,7 +218,7 @@ def test_planner_without_host_lengths_assumes_full_rows(lib):
 
 def test_several_query_tokens_per_row(lib):
     """q_len > 1: the G x q_len rows of a kv head are one unit (rows_per_unit), at
-    most 16 of them; MLA and block-sparse problems take one query token."""
+    most 16 of them; MLA takes up to 16 query tokens, one unit each."""
     w = W.config(6, shape_only=True)
     assert w.q_len == 4 and w.tensors["q"].shape == (32, 32, 4, 128)
     plan = da.decode_attn_plan_info(_problem(w), 152, w.tensors["seq_lens"], 0)
@@ -238,9 +238,17 @@ def test_several_query_tokens_per_row(lib):
     # several query tokens over block-sparse tables are planned like the dense case
     sparse = dict(base, sparse_block_size=64, max_sparse_blocks=1, q_len=2)
     assert da.decode_attn_plan_info(da.make_problem(**sparse), 152)["rows_per_unit"] == 8
+    # MLA: a unit per (row, query token); token t of Q sees seq_len - Q + 1 + t positions
     m = W.config(5, shape_only=True)
+    lens = m.tensors["seq_lens"]
+    for q_len in (2, 4, 16):
+        info = da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=q_len)), 152,
+                                        lens, 0)
+        assert info["num_units"] == m.batch * q_len and info["rows_per_unit"] == 128
+        tiles = sum(-(-max(int(n) - (q_len - 1 - t), 0) // 64) for n in lens.tolist() for t in range(q_len))
+        assert info["grid_x"] == 2 * min(76, tiles)
     with pytest.raises(da.DecodeAttnError) as e:
-        da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=2)), 152)
+        da.decode_attn_plan_info(da.make_problem(**dict(da.problem_kwargs(m), q_len=17)), 152)
     assert e.value.status == da.DA_ERR_UNSUPPORTED
 
 

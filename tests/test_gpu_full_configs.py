@@ -28,3 +28,13 @@ def test_full_size_mla_config():
     assert flags == 0
     ref_out, ref_lse = reference(w)
     assert_parity(out, lse, ref_out, ref_lse, what="config 5")
+
+
+def test_full_size_mla_config_with_four_query_tokens():
+    # the MLA workload with 4 query tokens per row (causal over each row's last
+    # 4 positions), every output row against the oracle
+    w = W.config(5, q_len=4)
+    out, lse, flags, eng = run_gpu(w)
+    assert flags == 0 and out.shape == (64, 128, 4, 512)
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what="config 5, q_len 4")

@@ -350,6 +350,22 @@ def test_mla_bad_page_sets_flag():
     assert torch.all(torch.isfinite(out.float()))
 
 
+@pytest.mark.parametrize("q_len,tree", [(2, False), (3, False), (4, True), (16, False), (5, True)])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_mla_several_query_tokens(q_len, tree, splits):
+    # Query token t of q_len sees the positions n <= N_b - q_len + t (or those its
+    # draft-tree word selects among the last q_len): rows shorter than q_len
+    # leave their first tokens without a position (out 0, LSE -inf); the cut
+    # falls inside a page, on a page boundary and in the first page.
+    lens = [1, 2, 64, 65, 700, 0, 130, 17]
+    w = W.make_mla(name="mla_q", batch=8, seq_lens=lens, seed=500 + q_len, q_len=q_len, tree_mask=tree)
+    out, lse, flags, eng = run_gpu(w, num_splits_override=splits)
+    assert flags == 0 and out.shape == (8, 128, q_len, 512) and lse.shape == (8, 128, q_len)
+    assert eng.plan["num_units"] == 8 * q_len
+    ref_out, ref_lse = reference(w)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"MLA q_len={q_len} tree={tree} S={splits}")
+
+
 @pytest.mark.parametrize("splits", [1, 3])
 def test_mla_non_finite_valid_keys_reach_the_sum_as_they_are(splits):
     # The two CTAs of a pair each hold half of every score and exchange their
