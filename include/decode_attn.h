@@ -12,8 +12,8 @@
  * (each block of sparse_block_size positions, clipped to seq_lens[b]). An empty
  * P gives out = 0 and lse = -inf.
  *
- * Several query tokens per row (q_len = Q > 1, speculative decoding; GQA): the
- * row's new tokens are its last Q positions, already in the
+ * Several query tokens per row (q_len = Q > 1, speculative decoding; GQA and
+ * MLA): the row's new tokens are its last Q positions, already in the
  * cache, and query token t < Q attends to the positions n <= seq_lens[b] - Q + t
  * of P(b,h) -- the causal mask of the split-K decode kernel (mslk
  * splitk_kernels.py, `_fwd_kernel_splitK` with IS_CAUSAL). q, out and lse then
@@ -107,9 +107,11 @@ enum {
  *        sparse_heads (SZ, SH; 0 = B and HKV) are the block tables' first two
  *        extents: row b and kv head h read table row (b % SZ, h % SH), the
  *        broadcast of the flex decode template (SPARSE_Z, SPARSE_HQ).
- *   q_len: query tokens per row, 0 or 1 = one. Q > 1 needs GQA and G * Q <= 16
- *        (the G*Q rows of a kv head share one pass); block-sparse tables apply
- *        to every query token, the causal or tree mask on top of them.
+ *   q_len: query tokens per row, 0 or 1 = one. GQA: G * Q <= 16 (the G*Q rows
+ *        of a kv head share one pass); block-sparse tables apply to every query
+ *        token, the causal or tree mask on top of them. MLA: Q <= 16, each query
+ *        token a row of its own over the shared latent cache (its pages come
+ *        from L2 for the row's other tokens).
  */
 typedef struct {
   int32_t batch, num_q_heads, num_kv_heads;
@@ -145,8 +147,9 @@ typedef struct {
 /*
  * Per-call arguments: device pointers, caller-owned.
  *
- *   q          bf16 [B][HQ][Dqk]   (MLA: q_nope [B][HQ][512]; q_len Q > 1: [B][HQ][Q][Dqk])
- *   q_pe       MLA only: bf16 [B][HQ][64]; else NULL
+ *   q          bf16 [B][HQ][Dqk]   (MLA: q_nope [B][HQ][512]; q_len Q > 1: [B][HQ][Q][Dqk],
+ *              MLA [B][HQ][Q][512])
+ *   q_pe       MLA only: bf16 [B][HQ][64] (q_len Q > 1: [B][HQ][Q][64]); else NULL
  *   k, v       contiguous [B][HKV][L][D]; paged [num_pages][HKV][page_size][D];
  *              MLA: k = ckv [num_pages][page_size][512], v = kpe [num_pages][page_size][64].
  *              Element type bf16, or e4m3 bytes when kv_dtype is an e4m3 type;
