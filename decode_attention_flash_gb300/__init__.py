@@ -20,7 +20,8 @@ from . import _build
 __all__ = [
     "DecodeAttnError", "Problem", "Args", "PlanInfo", "load", "decode_attn_create",
     "decode_attn_plan", "decode_attn_plan_ex", "decode_attn_get_plan", "decode_attn_plan_info",
-    "decode_attn_run", "decode_attn_run_noalloc", "decode_attn_merge", "decode_attn_get_error", "decode_attn_destroy",
+    "decode_attn_run", "decode_attn_run_noalloc", "decode_attn_merge", "decode_attn_get_error",
+    "decode_attn_get_error_noalloc", "decode_attn_destroy",
     "decode_attn_status_string", "DecodeAttention", "DA_KV_CONTIGUOUS", "DA_KV_PAGED",
     "DA_DTYPE_BF16", "DA_DTYPE_FP8_E4M3", "DA_DTYPE_FP8_E4M3_TOKEN_SCALE", "DA_DTYPE_INT4_GROUPS",
 ]
@@ -106,6 +107,7 @@ def load(build_if_missing: bool = False):
         "decode_attn_merge": (st, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
         "decode_attn_run_noalloc": (st, [vp, ctypes.POINTER(Args), vp]),
         "decode_attn_get_error": (st, [vp, vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "decode_attn_get_error_noalloc": (st, [vp, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "decode_attn_destroy": (None, [vp]),
         "decode_attn_status_string": (ctypes.c_char_p, [st]),
         # test hooks (include/decode_attn_testing.h)
@@ -251,6 +253,14 @@ def decode_attn_get_error(ctx, workspace: torch.Tensor, stream=None) -> int:
     st = load().decode_attn_get_error(ctx, _ptr(workspace), _stream(stream), ctypes.byref(flags))
     if st not in (DA_OK, DA_ERR_DEVICE):
         raise DecodeAttnError(st, "decode_attn_get_error")
+    return flags.value
+
+
+def decode_attn_get_error_noalloc(ctx, stream=None) -> int:
+    flags = ctypes.c_uint32()
+    st = load().decode_attn_get_error_noalloc(ctx, _stream(stream), ctypes.byref(flags))
+    if st not in (DA_OK, DA_ERR_DEVICE):
+        raise DecodeAttnError(st, "decode_attn_get_error_noalloc")
     return flags.value
 
 

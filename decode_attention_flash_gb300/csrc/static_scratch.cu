@@ -81,3 +81,14 @@ extern "C" da_status decode_attn_run_noalloc(da_ctx *ctx, const da_args *args,
     return DA_ERR_CUDA;
   return decode_attn_run(ctx, args, scratch, kNoAllocScratchBytes, stream);
 }
+
+extern "C" da_status decode_attn_get_error_noalloc(da_ctx *ctx, da_stream_t stream, uint32_t *flags) {
+  if (!ctx || !flags) return DA_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return DA_ERR_CUDA;
+  if (device != da::ctx_device(ctx)) return DA_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  da_status st = scratch_address(device, &scratch);
+  if (st != DA_OK) return st;
+  return decode_attn_get_error(ctx, scratch, stream, flags);
+}

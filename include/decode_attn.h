@@ -335,8 +335,9 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
  * then clears the error word and counters with a memset on `stream` and
  * enqueues the same kernel as decode_attn_run. All calls on a device share
  * the array: calls whose work overlaps on the GPU (other streams, other
- * threads) race on it. Device-side error bits are not reported to the caller
- * (bad indices are still skipped on the device). A plan whose workspace
+ * threads) race on it. Device-side error bits (bad indices are skipped on
+ * the device) stay in the array's error word until the next call clears it:
+ * decode_attn_get_error_noalloc reads them. A plan whose workspace
  * exceeds the array is refused with DA_ERR_WORKSPACE, and a call made while
  * another device than the context's is current with DA_ERR_INVALID_ARG
  * (before anything is enqueued).
@@ -344,6 +345,17 @@ da_status decode_attn_get_error(da_ctx *ctx, void *workspace, da_stream_t stream
  */
 #define DA_NOALLOC_SCRATCH_BYTES (32u << 20)
 da_status decode_attn_run_noalloc(da_ctx *ctx, const da_args *args, da_stream_t stream);
+
+/*
+ * decode_attn_get_error for the calls of decode_attn_run_noalloc: the error
+ * word of the device's static array (the context's device must be current),
+ * read and cleared on `stream` like decode_attn_get_error does (it
+ * synchronises the stream; after a DA_DEVERR_TIMEOUT it re-zeroes the
+ * counters). *flags = 0 before the first no-alloc call on the device. Returns
+ * DA_ERR_DEVICE when the word was non-zero. Errors: INVALID_ARG, UNSUPPORTED,
+ * CUDA.
+ */
+da_status decode_attn_get_error_noalloc(da_ctx *ctx, da_stream_t stream, uint32_t *flags);
 
 /* Releases the context (NULL is allowed). */
 void decode_attn_destroy(da_ctx *ctx);

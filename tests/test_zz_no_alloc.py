@@ -100,3 +100,27 @@ def test_noalloc_refuses_a_plan_beyond_the_static_scratch():
         assert st == da.DA_ERR_WORKSPACE
     finally:
         da.decode_attn_destroy(ctx)
+
+
+def test_noalloc_error_word_reports_a_bad_page():
+    # a block-table entry outside the pool: the page is skipped on the device and
+    # its bit waits in the static array's error word until read (and cleared)
+    lib = da.load()
+    w = _case()
+    bt = w.tensors["block_table"].clone()
+    bt[0, 3] = w.num_pages + 5
+    w.tensors["block_table"] = bt
+    dev = torch.device("cuda", 0)
+    t = w.to(dev)
+    ctx = da.decode_attn_create(da.make_problem(**da.problem_kwargs(w)), 0)
+    try:
+        da.decode_attn_plan(ctx, w.tensors["seq_lens"], 0)
+        assert da.decode_attn_get_error_noalloc(ctx) == 0  # what earlier calls left is read out here
+        _run(lib, ctx, w, t, noalloc=True)
+        assert da.decode_attn_get_error_noalloc(ctx) & da.DA_DEVERR_PAGE_INDEX
+        assert da.decode_attn_get_error_noalloc(ctx) == 0  # cleared by the read
+        w.tensors["block_table"][0, 3] = bt[0, 2]  # a valid page again
+        _run(lib, ctx, w, w.to(dev), noalloc=True)
+        assert da.decode_attn_get_error_noalloc(ctx) == 0
+    finally:
+        da.decode_attn_destroy(ctx)
