@@ -56,7 +56,8 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "gqa_split_kernel": ["gqa_split.cuh", "gqa_split.cu", "gqa_kind_bf16.cu", "gqa_kind_e4m3.cu",
-                         "gqa_kind_e4m3_token.cu", "gqa_kind_int4.cu", "ptx.cuh", "internal.h"],
+                         "gqa_kind_e4m3_token.cu", "gqa_kind_int4.cu", "gqa_kind_e4m3_mma.cu", "ptx.cuh",
+                         "internal.h"],
     "mla_split_kernel": ["mla_split.cu", "ptx.cuh", "internal.h"],
 }
 
