@@ -72,9 +72,14 @@ def kernel_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, cfg: int):
+def recorded_traffic(kernel: str, cfg: int, args=None):
     """DRAM read+write bytes per launch from the committed ncu summary, or None
-    when the kernel's sources changed since that capture."""
+    when the kernel's sources changed since that capture or the run is another
+    workload than the captured one (another seed, query-token count, mask,
+    soft cap or arithmetic)."""
+    if args is not None and (args.seed is not None or args.q_len > 1 or args.tree_mask or args.softcap
+                             or args.fp8_mma or args.splits):
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -432,7 +437,7 @@ def run_ours(args, w, cfg):
                        "us_min": min(call_ms) * 1e3, "us_max": max(call_ms) * 1e3},
             "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": split_gbs / hbm_peak,
-                         "traffic": recorded_traffic(kname, cfg),
+                         "traffic": recorded_traffic(kname, cfg, args),
                          "kernel": kname, "kernel_us": mean_split * 1e3,
                          "peak_source": f"of {peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'fallback'})"},
             "cpu_baseline": cpu,

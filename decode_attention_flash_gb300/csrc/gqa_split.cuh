@@ -45,7 +45,7 @@ namespace da {
 namespace {
 
 constexpr int kTile = 64;             // tokens per pipeline stage
-constexpr int kIdAhead = 8;           // tiles whose page / block ids are fetched ahead (ids <= 32)
+constexpr int kIdAhead = 4;           // tiles whose page / block ids are fetched ahead (ids <= 32)
 constexpr int kConsumerWarps = 4;     // 16 tokens of each tile per warp
 // A sixth warp takes the row-counter atomics of partial segments off the
 // consumers and merges small units while they stream.
