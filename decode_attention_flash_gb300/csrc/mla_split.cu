@@ -81,6 +81,11 @@ constexpr uint32_t kTmemQ = 256;   // q_nope half, two bf16 per column: 256..383
 constexpr uint32_t kTmemS = 384;   // score tile: 384..447
 constexpr uint32_t kTmemP = 448;   // P tiles of the two groups: 448..479, 480..511
 constexpr float kRescaleThreshold = 8.f;
+// The schedule weighs a row's start like this many tiles: a row change costs
+// a CTA pair ~5 tiles' time (the row's epilogue in one softmax group, which
+// holds up the running maximum's hand-off, and the next row's queries into
+// TMEM), so equal ranges of tiles alone leave the pairs with more rows behind.
+constexpr int kRowCost = 4;
 
 // What the producer tells the other roles about the tile in a KV stage.
 struct TileMeta {
@@ -96,7 +101,7 @@ struct Ctrl {
   int abort;
   int start_b, start_k;
   long long start_P;
-  int npend, nempty;
+  int npend, nempty, ntiles;
   int pend[4][3];  // rows this CTA merges: b, c_first, n_seg
 };
 
@@ -377,26 +382,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- the cluster's tile range
   uint32_t dev_err = 0;
+  // Ranges are cut in cost units: a row with tiles costs kRowCost + its tiles,
+  // its tile k sitting at cost position Q_b + kRowCost + k (Q_b the row's
+  // start, the prefix of the costs before it); the first kRowCost positions
+  // of a row hold no tile. A cluster takes the tiles whose positions fall in
+  // its range (possibly none) and the pieces of a row come from the
+  // consecutive clusters c_first..c_last.
   int local = 0;
   const int nrows = p.batch * p.q_len;
   for (int b = threadIdx.x; b < nrows; b += kThreads) {
     int len;
-    local += row_tiles(p, b, len, dev_err);
+    const int t_b = row_tiles(p, b, len, dev_err);
+    local += t_b > 0 ? t_b + kRowCost : 0;
   }
   int T32 = 0;
   block_scan(local, scan, &T32);
   const int64_t T = T32;
-  // never more ranges than tiles: every working cluster holds at least one tile
-  // and the pieces of a row come from consecutive clusters c_first..c_last
   const int C = (int)(T < (int64_t)NC ? T : (int64_t)NC);
   const int64_t lo = cl < C ? (int64_t)cl * T / C : 0;
   const int64_t hi = cl < C ? (int64_t)(cl + 1) * T / C : 0;
-  const int tail_owner = C > 0 ? C - 1 : 0;  // writes rows without tokens past the last tile
+  const int tail_owner = C > 0 ? C - 1 : 0;  // writes rows without tokens past the last position
   if (threadIdx.x == 0) {
     ctrl->abort = 0;
     ctrl->start_b = -1;
     ctrl->npend = 0;
     ctrl->nempty = 0;
+    ctrl->ntiles = 0;
   }
   __syncthreads();
   {
@@ -406,14 +417,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int len = 0;
       uint32_t ignored = 0;
       const int t_b = b < nrows ? row_tiles(p, b, len, ignored) : 0;
+      const int c_b = t_b > 0 ? t_b + kRowCost : 0;
       int total = 0;
-      const int incl = block_scan(t_b, scan, &total);
-      const int64_t Pb = base + incl - t_b;
+      const int incl = block_scan(c_b, scan, &total);
+      const int64_t Pb = base + incl - c_b;  // the row's start in cost units
       if (b < nrows) {
-        if (t_b > 0 && Pb <= lo && lo < Pb + t_b) {
-          ctrl->start_b = b;
-          ctrl->start_k = (int)(lo - Pb);
-          ctrl->start_P = Pb;
+        if (t_b > 0) {
+          if (Pb <= lo && lo < Pb + c_b) {  // the row holding the range's first position
+            ctrl->start_b = b;
+            ctrl->start_k = lo - Pb > kRowCost ? (int)(lo - Pb - kRowCost) : 0;
+            ctrl->start_P = Pb;
+          }
+          // the row's tiles in this range
+          const int64_t t0 = lo > Pb + kRowCost ? lo : Pb + kRowCost, t1 = hi < Pb + c_b ? hi : Pb + c_b;
+          if (t1 > t0) atomicAdd(&ctrl->ntiles, (int)(t1 - t0));
         }
         // a row without tokens is written by the cluster whose range holds its start
         if (t_b == 0 && ((Pb >= lo && Pb < hi) || (Pb >= T && cl == tail_owner)))
@@ -434,11 +451,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (cl >= C) {  // no tiles for this cluster (both CTAs take this exit)
+  const int n = ctrl->ntiles;
+  if (cl >= C || n == 0) {  // no tiles for this cluster (both CTAs take this exit)
     if (dev_err) atomicOr(p.err, dev_err);
     return;
   }
-  const int n = (int)(hi - lo);  // >= 1
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -492,9 +509,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int64_t Pb = ctrl->start_P;
       int t_b = row_tiles(p, b, len, ignored);
       auto row_pieces = [&](int &c_first, int &n_seg, bool &full) {
-        c_first = cluster_of(Pb, T, C);
-        n_seg = cluster_of(Pb + t_b - 1, T, C) - c_first + 1;
-        full = Pb >= lo && Pb + t_b <= hi;
+        c_first = cluster_of(Pb + kRowCost, T, C);
+        n_seg = cluster_of(Pb + kRowCost + t_b - 1, T, C) - c_first + 1;
+        full = n_seg == 1;
       };
       int c_first, n_seg;
       bool full;
@@ -560,7 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // fetched now, while this warp waits for a free stage
         if (i + 1 < n) {
           if (++k == t_b) {
-            Pb += t_b;
+            Pb += t_b + kRowCost;
             do {
               ++b;
               t_b = b < nrows ? row_tiles(p, b, len, ignored) : 1;
