@@ -916,10 +916,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float inv = l_new == 0.f ? 0.f : 1.f / l_new;
         const float lse = l_new == 0.f ? neg_inf() : (m_new + __log2f(l_new)) * 0.69314718055994531f;
         const int64_t slot = (int64_t)m.b + cl;
-        for (int c0 = 0; c0 < 256; c0 += 64) {
-          float v[64];  // four loads per wait
+        for (int c0 = 0; c0 < 256; c0 += 128) {
+          float v[128];  // eight loads per wait
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 8; ++q) {
             float t[16];
             tmem_ld16(tmem + lane_off + kTmemO + c0 + 16 * q, t);
 #pragma unroll
@@ -929,7 +929,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (full) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + head_row(p, m.b, h) * 512 + r * 256 + c0);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < 16; ++e)
               dst[e] = make_uint4(pack_bf16(v[8 * e] * inv, v[8 * e + 1] * inv),
                                   pack_bf16(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
                                   pack_bf16(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
@@ -937,7 +937,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
             float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * kHeads + h) * 512 + r * 256 + c0);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < 32; ++e)
               dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
           }
         }
