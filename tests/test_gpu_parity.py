@@ -644,9 +644,12 @@ def test_tree_mask_lower_triangle_is_bitwise_causal():
 
 # ------------------------------------------------------------------ block masks broadcast over rows / heads
 
-@pytest.mark.parametrize("shape", [(1, 1), (1, 4), (5, 1), (2, 2)])
+@pytest.mark.parametrize("shape", [(1, 1), (1, 4), (5, 1), (2, 2), (2, 16)])
 @pytest.mark.parametrize("splits", [0, 3])
 def test_broadcast_block_mask(shape, splits):
+    # (2, 16): tables with a row per query head (SPARSE_HQ = HQ); the flex
+    # decode template reads them at the kv head (off_hkv % SPARSE_HQ), so kv
+    # head h reads row h and the rows of the other query heads are not read
     SZ, SH = shape
     B, HKV, L, blk = 5, 4, 2048, 128
     g = torch.Generator().manual_seed(500 + 10 * SZ + SH)

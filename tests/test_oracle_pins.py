@@ -533,10 +533,11 @@ def test_int4_equals_bf16_on_the_same_values(groups):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-@pytest.mark.parametrize("shape", [(1, 1), (1, 2), (3, 1), (2, 2)])
+@pytest.mark.parametrize("shape", [(1, 1), (1, 2), (3, 1), (2, 2), (2, 8)])
 def test_broadcast_block_mask_equals_the_expanded_tables(shape):
     # tables of extents (SZ, SH) read at (b % SZ, h % SH): the same result as
-    # tables written out for every (b, kv head)
+    # tables written out for every (b, kv head); SH = 8 = HQ is the flex
+    # template's per-query-head extent, still read at the kv head h
     SZ, SH = shape
     B, HKV, L, blk = 6, 4, 256, 32
     g = torch.Generator().manual_seed(50 + SZ * 10 + SH)
